@@ -1,0 +1,211 @@
+"""Float64 CPU oracle for the DLR / S5 hot path.
+
+TEST INFRASTRUCTURE ONLY: imported by the test-suite, by ``__graft_entry__.smoke()`` and by
+the benchmark's CPU-baseline leg, never by the library. It shares no code with the CUDA path.
+
+The arithmetic lives in ``oracle.c`` (plain float64 loops) plus numpy library primitives
+(complex matmul, exp) where a step is a plain matrix product. Each function cites the passage
+it follows; the design doc lists the readings taken where the pages are silent.
+
+Parity status: every function here is pinned by ``tests/test_oracle_pins.py`` against closed
+forms, library routines (numpy FFT, scipy lfilter / toeplitz / expm) or brute force.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lib = None
+
+DEFAULT_THREADS = max(1, min(os.cpu_count() or 1, 16))
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with gcc into oracle/_build/liboracle.so (portable flags only)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-ffp-contract=off", "-pthread",
+           _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = build()
+        lib = ctypes.CDLL(path)
+        P = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        lib.orc_lambda.argtypes = [i64, i64, P, P, P]
+        lib.orc_dlr_kernel.argtypes = [i64, i64, i64, P, P, P, ctypes.c_int, P]
+        lib.orc_dlr_recurrence.argtypes = [i64, i64, i64, i64, P, P, P, P, P, P, P,
+                                           ctypes.c_int]
+        lib.orc_toeplitz_causal.argtypes = [i64, i64, i64, P, P, P, ctypes.c_int]
+        lib.orc_diag_scan.argtypes = [i64, i64, P, P, P]
+        _lib = lib
+    return _lib
+
+
+def _f32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _f64(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _p(a: Optional[np.ndarray]):
+    return None if a is None else a.ctypes.data
+
+
+# ------------------------------------------------------------------------------------------
+# DLR ("Simplifying and Understanding State Space Models with Diagonal Linear RNNs")
+
+def dlr_lambda(log_re, log_im) -> np.ndarray:
+    """lambda = exp(-(log Lambda)_re^2 + i (log Lambda)_im), complex128 [H, N] (section 2.2)."""
+    log_re, log_im = _f32(log_re), _f32(log_im)
+    out = np.empty(log_re.shape + (2,), np.float64)
+    _load().orc_lambda(log_re.shape[0], log_re.shape[1], _p(log_re), _p(log_im), _p(out))
+    return out[..., 0] + 1j * out[..., 1]
+
+
+def dlr_kernel(log_re, log_im, W, L: int, cast: str = "re") -> np.ndarray:
+    """K_j = sum_n W_n lambda_n^j for j < L (section 2, Eq. 3/4), cast 're', 're_im' or
+    'complex' (section 2 Re cast; section 2.1 DLR-prod cast Re(K)*Im(K))."""
+    log_re, log_im, W = _f32(log_re), _f32(log_im), _f32(W)
+    H, N = log_re.shape
+    code = {"re": 0, "re_im": 1, "complex": 2}[cast]
+    shape = (H, L, 2) if code == 2 else (H, L)
+    K = np.empty(shape, np.float64)
+    _load().orc_dlr_kernel(H, N, L, _p(log_re), _p(log_im), _p(W), code, _p(K))
+    if code == 2:
+        return K[..., 0] + 1j * K[..., 1]
+    return K
+
+
+def dlr_recurrence(u, log_re, log_im, W, x0=None, return_state: bool = False,
+                   nthreads: int = DEFAULT_THREADS):
+    """Sequential DLR recurrence with the Re cast (section 2, Eq. 1):
+    x_{n,k} = lambda_n x_{n,k-1} + u_k, y_k = sum_n Re(w_n x_{n,k}); u [B, H, L]."""
+    u = _f32(u)
+    log_re, log_im, W = _f32(log_re), _f32(log_im), _f32(W)
+    B, H, L = u.shape
+    N = log_re.shape[1]
+    y = np.empty((B, H, L), np.float64)
+    x0a = None
+    if x0 is not None:
+        x0 = np.asarray(x0)
+        x0a = _f64(np.stack([x0.real, x0.imag], -1))
+    xT = np.empty((B, H, N, 2), np.float64) if return_state else None
+    _load().orc_dlr_recurrence(B, H, N, L, _p(u), _p(log_re), _p(log_im), _p(W), _p(x0a),
+                               _p(y), _p(xT), int(nthreads))
+    if return_state:
+        return y, xT[..., 0] + 1j * xT[..., 1]
+    return y
+
+
+def toeplitz_causal(u, kappa, nthreads: int = DEFAULT_THREADS) -> np.ndarray:
+    """Direct causal Toeplitz sum y_k = sum_{j<=k} kappa_{h,j} u_{k-j} (section 2)."""
+    u = _f32(u)
+    kappa = _f64(kappa)
+    B, H, L = u.shape
+    assert kappa.shape == (H, L)
+    y = np.empty((B, H, L), np.float64)
+    _load().orc_toeplitz_causal(B, H, L, _p(u), _p(kappa), _p(y), int(nthreads))
+    return y
+
+
+def dlr_bidirectional(u, fwd, bwd, nthreads: int = DEFAULT_THREADS) -> np.ndarray:
+    """Bidirectional DLR (section 2.1): the sum of two independent DLRs, the second one run
+    on the time-reversed sequence and its output reversed back. Lag 0 is counted by both."""
+    u = _f32(u)
+    y1 = dlr_recurrence(u, *fwd, nthreads=nthreads)
+    y2 = dlr_recurrence(u[..., ::-1], *bwd, nthreads=nthreads)[..., ::-1]
+    return y1 + y2
+
+
+def dlr_prod_layer(u, fwd, bwd=None, nthreads: int = DEFAULT_THREADS) -> np.ndarray:
+    """DLR-prod (section 2.1): kernel kappa_j = Re(K_j) * Im(K_j), applied by the direct
+    Toeplitz sum; with ``bwd`` the anti-causal direction is added as in the bidirectional DLR."""
+    u = _f32(u)
+    L = u.shape[-1]
+    k1 = dlr_kernel(*fwd, L, cast="re_im")
+    y = toeplitz_causal(u, k1, nthreads)
+    if bwd is not None:
+        k2 = dlr_kernel(*bwd, L, cast="re_im")
+        y = y + toeplitz_causal(np.ascontiguousarray(u[..., ::-1]), k2, nthreads)[..., ::-1]
+    return y
+
+
+def dlr_layer(u, fwd, bwd=None, cast: str = "re", nthreads: int = DEFAULT_THREADS):
+    """The DLR layer as the pages define it for the given cast and direction(s).
+    ``fwd``/``bwd`` are (log_re, log_im, W) tuples."""
+    if cast == "re":
+        if bwd is None:
+            return dlr_recurrence(u, *fwd, nthreads=nthreads)
+        return dlr_bidirectional(u, fwd, bwd, nthreads)
+    return dlr_prod_layer(u, fwd, bwd, nthreads)
+
+
+# ------------------------------------------------------------------------------------------
+# S5 ("Simplified State Space Layers for Sequence Modeling")
+
+def s5_zoh(lam, log_delta, Bt):
+    """Zero-order hold of the diagonal system (section 3.2 'Discretization'), the standard
+    diagonal ZOH: Lambda_bar = exp(Lambda Delta), B_bar = Lambda^{-1} (Lambda_bar - 1) B~,
+    Delta = exp(log_delta) per state. Returns complex128 Lambda_bar [P], B_bar [P, H]."""
+    lam = _f64(lam)
+    lamc = lam[:, 0] + 1j * lam[:, 1]
+    delta = np.exp(_f64(log_delta))
+    abar = np.exp(lamc * delta)
+    Bt = _f64(Bt)
+    Btc = Bt[..., 0] + 1j * Bt[..., 1]
+    bbar = ((abar - 1.0) / lamc)[:, None] * Btc
+    return abar, bbar
+
+
+def s5_layer(u, lam, log_delta, Bt, Ct, D) -> np.ndarray:
+    """S5 SSM outputs (sections 2.2 and 3): per batch row,
+    x_k = Lambda_bar x_{k-1} + B_bar u_k (x_{-1} = 0), y_k = Re(C~ x_k) + D (.) u_k.
+    u: [B, L, H] float32. B_bar u_k is a library complex matmul over all k at once."""
+    u = _f32(u)
+    Bsz, L, H = u.shape
+    abar, bbar = s5_zoh(lam, log_delta, Bt)
+    P = abar.shape[0]
+    Ct = _f64(Ct)
+    Ctc = Ct[..., 0] + 1j * Ct[..., 1]  # [H, P]
+    D = _f64(D)
+    ab = _f64(np.stack([abar.real, abar.imag], -1))
+    y = np.empty((Bsz, L, H), np.float64)
+    lib = _load()
+    for b in range(Bsz):
+        ub = u[b].astype(np.float64)
+        v = ub @ bbar.T                                   # [L, P] complex
+        va = _f64(np.stack([v.real, v.imag], -1))
+        x = np.empty_like(va)
+        lib.orc_diag_scan(L, P, _p(ab), _p(va), _p(x))
+        xc = x[..., 0] + 1j * x[..., 1]
+        y[b] = (xc @ Ctc.T).real + ub * D[None, :]
+    return y
+
+
+def rel_l2(y, y_ref) -> float:
+    """||y - y_ref||_2 / ||y_ref||_2 over the whole tensor."""
+    y = np.asarray(y, np.float64)
+    y_ref = np.asarray(y_ref, np.float64)
+    den = np.linalg.norm(y_ref.ravel())
+    num = np.linalg.norm((y - y_ref).ravel())
+    return float(num / den) if den > 0 else float(num)

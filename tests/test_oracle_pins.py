@@ -1,0 +1,400 @@
+"""Pins for the float64 oracle: each test checks the oracle against something other than
+itself -- a closed form, a library routine (numpy FFT / convolve, scipy lfilter / toeplitz /
+expm, a general eigensolver), brute force on tiny inputs, or an invariant the pages state.
+
+Sources: "Simplifying and Understanding State Space Models with Diagonal Linear RNNs"
+(section 2: recurrence, kernel, Re cast; 2.1: DLR-prod, bidirectional, Toeplitz/FFT; 2.2:
+parameterisation, DFT identity at (log Lambda)_re = 0, L = N), "The Annotated S4" (part 1:
+unrolling the recurrence into a convolution; part 1b: HiPPO matrix; part 2: HiPPO-N) and
+"Simplified State Space Layers for Sequence Modeling" (sections 2.2, 3: scan, diagonalised
+MIMO system, ZOH, per-state Delta).
+"""
+import os
+
+import numpy as np
+import pytest
+import scipy.linalg
+import scipy.signal
+
+import oracle
+from state_space_sequence_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _params(H, N, seed, unit=0):
+    rng = np.random.default_rng(seed)
+    p = inputs.dlr_params(rng, H, N, unit)
+    return p.log_re, p.log_im, p.W
+
+
+def _lam_np(log_re, log_im):
+    a = log_re.astype(np.float64)
+    t = log_im.astype(np.float64)
+    return np.exp(-a * a) * np.exp(1j * t)
+
+
+def _w_np(W):
+    return W[..., 0].astype(np.float64) + 1j * W[..., 1].astype(np.float64)
+
+
+# ---------------------------------------------------------------------------------------
+# Kernel K_j = sum_n w_n lambda_n^j
+
+@pytest.mark.parametrize("N", [4, 8, 16, 64])
+def test_kernel_dft_identity(N):
+    """(log Lambda)_re = 0, (log Lambda)_im = 2 pi n / N, L = N  =>  K = N * IDFT(w)
+    (DLR paper section 2.2; with lambda_n = e^{+2 pi i n/N} the sum is numpy's ifft times N).
+    theta is stored as float32, so K may differ from the exact DFT by at most
+    sum_n |w_n| * j * |theta_n - 2 pi n/N| at lag j -- the test uses that bound."""
+    rng = np.random.default_rng(100 + N)
+    log_re = np.zeros((1, N), np.float32)
+    log_im = (2 * np.pi * np.arange(N) / N).astype(np.float32)[None, :]
+    W = rng.standard_normal((1, N, 2)).astype(np.float32)
+    K = oracle.dlr_kernel(log_re, log_im, W, N, cast="complex")[0]
+    w = _w_np(W)[0]
+    ref = N * np.fft.ifft(w)
+    dtheta = np.max(np.abs(log_im.astype(np.float64) - 2 * np.pi * np.arange(N) / N))
+    bound = np.sum(np.abs(w)) * np.arange(N) * dtheta * 1.01 + 1e-12 * np.sum(np.abs(w))
+    assert np.all(np.abs(K - ref) <= bound)
+    # a sign or index slip gives an O(|w|) error, far above the bound
+    assert np.max(bound) < 1e-4 * np.sum(np.abs(w))
+
+
+def test_kernel_periodic_on_unit_circle():
+    """At (log Lambda)_re = 0 and theta_n = 2 pi n/N the kernel has period N (DLR paper 2.2)."""
+    N = 8
+    log_re = np.zeros((1, N), np.float32)
+    log_im = (2 * np.pi * np.arange(N) / N).astype(np.float32)[None, :]
+    W = np.random.default_rng(3).standard_normal((1, N, 2)).astype(np.float32)
+    K = oracle.dlr_kernel(log_re, log_im, W, 4 * N, cast="complex")[0]
+    w = np.abs(_w_np(W)[0])
+    dtheta = np.abs(log_im[0].astype(np.float64) - 2 * np.pi * np.arange(N) / N)
+    for r in range(1, 4):
+        # |K_{j+rN} - K_j| <= sum_n |w_n| |lambda_n^{rN} - 1| <= sum_n |w_n| r N dtheta_n
+        bound = np.sum(w * r * N * dtheta) * 1.01 + 1e-12
+        assert np.max(np.abs(K[r * N:(r + 1) * N] - K[:N])) <= bound
+        assert bound < 1e-4 * np.sum(w)
+
+
+def test_kernel_brute_force_powers():
+    """Tiny case: K_j against sum_n w_n * (lambda_n ** j) with Python's complex power."""
+    lr, li, W = _params(2, 5, seed=7)
+    L = 40
+    K = oracle.dlr_kernel(lr, li, W, L, cast="complex")
+    lam = _lam_np(lr, li)
+    w = _w_np(W)
+    for h in range(2):
+        for j in range(L):
+            ref = sum(complex(w[h, n]) * complex(lam[h, n]) ** j for n in range(5))
+            assert abs(K[h, j] - ref) <= 1e-12 * (1 + abs(ref))
+
+
+def test_kernel_casts():
+    """Re cast and DLR-prod cast are the real part and Re*Im of the complex kernel."""
+    lr, li, W = _params(3, 6, seed=8)
+    Kc = oracle.dlr_kernel(lr, li, W, 50, cast="complex")
+    np.testing.assert_array_equal(oracle.dlr_kernel(lr, li, W, 50, cast="re"), Kc.real)
+    np.testing.assert_allclose(oracle.dlr_kernel(lr, li, W, 50, cast="re_im"),
+                               Kc.real * Kc.imag, rtol=1e-15, atol=0)
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4])
+def test_dlr_prod_is_a_dlr_with_n_squared_states(N):
+    """DLR paper 2.1 / A.2: the DLR-prod kernel Re(K)Im(K) = Im(K^2)/2 is the Re-cast kernel
+    of a DLR whose states are the products lambda_n lambda_m with weights -i w_n w_m / 2."""
+    lr, li, W = _params(2, N, seed=20 + N)
+    L = 64
+    kp = oracle.dlr_kernel(lr, li, W, L, cast="re_im")
+    lam = _lam_np(lr, li)
+    w = _w_np(W)
+    j = np.arange(L)
+    for h in range(2):
+        mu = (lam[h][:, None] * lam[h][None, :]).ravel()
+        nu = (-0.5j * w[h][:, None] * w[h][None, :]).ravel()
+        ref = np.real((nu[None, :] * mu[None, :] ** j[:, None]).sum(1))
+        np.testing.assert_allclose(kp[h], ref, rtol=1e-10, atol=1e-14)
+
+
+# ---------------------------------------------------------------------------------------
+# Recurrence (scan) and its convolution view
+
+def test_recurrence_matches_scipy_lfilter():
+    """Each state is the first-order IIR filter 1/(1 - lambda z^-1) driven by u (DLR paper
+    section 2, Eq. 1); y = sum_n Re(w_n x_n). scipy.signal.lfilter runs the same recurrence
+    independently (complex coefficients)."""
+    lr, li, W = _params(3, 7, seed=9)
+    u = np.random.default_rng(10).standard_normal((2, 3, 300)).astype(np.float32)
+    y = oracle.dlr_recurrence(u, lr, li, W, nthreads=2)
+    lam = _lam_np(lr, li)
+    w = _w_np(W)
+    for b in range(2):
+        for h in range(3):
+            ref = np.zeros(300)
+            for n in range(7):
+                x = scipy.signal.lfilter([1.0], [1.0, -lam[h, n]], u[b, h].astype(np.float64))
+                ref += np.real(w[h, n] * x)
+            np.testing.assert_allclose(y[b, h], ref, rtol=1e-11, atol=1e-12)
+
+
+def test_impulse_response_is_kernel():
+    """u = delta_0  =>  y_k = Re K_k (Annotated S4 part 1: the unrolled recurrence is a
+    convolution with K = (CB, CAB, CA^2B, ...))."""
+    lr, li, W = _params(4, 9, seed=11)
+    L = 200
+    u = np.zeros((1, 4, L), np.float32)
+    u[..., 0] = 1.0
+    y = oracle.dlr_recurrence(u, lr, li, W)[0]
+    K = oracle.dlr_kernel(lr, li, W, L, cast="re")
+    np.testing.assert_allclose(y, K, rtol=1e-12, atol=1e-14)
+
+
+def test_recurrence_equals_library_convolution():
+    """Recurrence == numpy.convolve(u, Re K)[:L] (the Re cast of section 2)."""
+    lr, li, W = _params(2, 6, seed=12)
+    L = 257
+    u = np.random.default_rng(13).standard_normal((3, 2, L)).astype(np.float32)
+    y = oracle.dlr_recurrence(u, lr, li, W)
+    K = oracle.dlr_kernel(lr, li, W, L, cast="re")
+    for b in range(3):
+        for h in range(2):
+            ref = np.convolve(u[b, h].astype(np.float64), K[h])[:L]
+            np.testing.assert_allclose(y[b, h], ref, rtol=1e-10, atol=1e-12)
+
+
+def test_toeplitz_equals_library_convolution():
+    rng = np.random.default_rng(14)
+    u = rng.standard_normal((2, 3, 129)).astype(np.float32)
+    kap = rng.standard_normal((3, 129))
+    y = oracle.toeplitz_causal(u, kap)
+    for b in range(2):
+        for h in range(3):
+            np.testing.assert_allclose(y[b, h], np.convolve(u[b, h], kap[h])[:129],
+                                       rtol=1e-12, atol=1e-12)
+
+
+def test_constant_input_geometric_series():
+    """u = 1  =>  y_k = Re sum_n w_n (1 - lambda_n^{k+1}) / (1 - lambda_n)."""
+    lr, li, W = _params(2, 5, seed=15)
+    L = 500
+    y = oracle.dlr_recurrence(np.ones((1, 2, L), np.float32), lr, li, W)[0]
+    lam = _lam_np(lr, li)
+    w = _w_np(W)
+    k = np.arange(L)
+    for h in range(2):
+        ref = np.real((w[h][None, :] * (1 - lam[h][None, :] ** (k[:, None] + 1))
+                       / (1 - lam[h][None, :])).sum(1))
+        np.testing.assert_allclose(y[h], ref, rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("splits", [[1], [64], [100, 101], [7, 63, 64, 200, 511]])
+def test_scan_chunking_associativity(splits):
+    """S5 paper section 2.2: the recurrence is a scan with an associative operator, so running
+    it chunk by chunk with the carried state gives the sequential result exactly."""
+    lr, li, W = _params(2, 8, seed=16)
+    L = 512
+    u = np.random.default_rng(17).standard_normal((2, 2, L)).astype(np.float32)
+    y_full = oracle.dlr_recurrence(u, lr, li, W)
+    bounds = [0] + list(splits) + [L]
+    x = None
+    parts = []
+    for s, e in zip(bounds[:-1], bounds[1:]):
+        yp, x = oracle.dlr_recurrence(np.ascontiguousarray(u[..., s:e]), lr, li, W, x0=x,
+                                      return_state=True)
+        parts.append(yp)
+    np.testing.assert_allclose(np.concatenate(parts, -1), y_full, rtol=1e-12, atol=1e-13)
+
+
+def test_thread_count_does_not_change_results():
+    lr, li, W = _params(5, 4, seed=18)
+    u = np.random.default_rng(19).standard_normal((3, 5, 100)).astype(np.float32)
+    np.testing.assert_array_equal(oracle.dlr_recurrence(u, lr, li, W, nthreads=1),
+                                  oracle.dlr_recurrence(u, lr, li, W, nthreads=7))
+
+
+# ---------------------------------------------------------------------------------------
+# Bidirectional DLR
+
+def test_bidirectional_is_toeplitz_matvec():
+    """DLR paper 2.1: the bidirectional output is a Toeplitz matrix-vector product whose
+    lower part holds Re K^1, upper part Re K^2, diagonal Re K^1_0 + Re K^2_0. Built with
+    scipy.linalg.toeplitz and multiplied densely."""
+    f = _params(2, 5, seed=21)
+    g = _params(2, 5, seed=22)
+    L = 90
+    u = np.random.default_rng(23).standard_normal((2, 2, L)).astype(np.float32)
+    y = oracle.dlr_bidirectional(u, f, g)
+    K1 = oracle.dlr_kernel(*f, L, cast="re")
+    K2 = oracle.dlr_kernel(*g, L, cast="re")
+    for h in range(2):
+        col = K1[h].copy()
+        row = K2[h].copy()
+        col[0] = row[0] = K1[h, 0] + K2[h, 0]
+        T = scipy.linalg.toeplitz(col, row)
+        for b in range(2):
+            np.testing.assert_allclose(y[b, h], T @ u[b, h].astype(np.float64),
+                                       rtol=1e-10, atol=1e-12)
+
+
+def test_bidirectional_symmetry():
+    """Same parameters both ways and a palindromic input give a palindromic output."""
+    f = _params(1, 6, seed=24)
+    half = np.random.default_rng(25).standard_normal(50).astype(np.float32)
+    u = np.concatenate([half, half[::-1]])[None, None, :]
+    y = oracle.dlr_bidirectional(u, f, f)[0, 0]
+    np.testing.assert_allclose(y, y[::-1], rtol=1e-12, atol=1e-12)
+
+
+def test_prod_layer_bidirectional_matches_toeplitz_matrix():
+    f = _params(1, 4, seed=26)
+    g = _params(1, 4, seed=27)
+    L = 70
+    u = np.random.default_rng(28).standard_normal((1, 1, L)).astype(np.float32)
+    y = oracle.dlr_prod_layer(u, f, g)[0, 0]
+    k1 = oracle.dlr_kernel(*f, L, cast="re_im")[0]
+    k2 = oracle.dlr_kernel(*g, L, cast="re_im")[0]
+    col, row = k1.copy(), k2.copy()
+    col[0] = row[0] = k1[0] + k2[0]
+    np.testing.assert_allclose(y, scipy.linalg.toeplitz(col, row) @ u[0, 0].astype(np.float64),
+                               rtol=1e-10, atol=1e-13)
+
+
+# ---------------------------------------------------------------------------------------
+# S5
+
+def _s5_small(H, P, seed, equal_delta=False):
+    rng = np.random.default_rng(seed)
+    lam = np.stack([-np.abs(rng.uniform(0.1, 2.0, P)), rng.uniform(-5, 5, P)], -1)
+    if equal_delta:
+        log_delta = np.full(P, np.log(0.05))
+    else:
+        log_delta = rng.uniform(np.log(1e-3), np.log(1e-1), P)
+    Bt = rng.standard_normal((P, H, 2)) / np.sqrt(H)
+    Ct = rng.standard_normal((H, P, 2)) / np.sqrt(H)
+    D = rng.standard_normal(H)
+    f = lambda a: np.asarray(a, np.float32)
+    return f(lam), f(log_delta), f(Bt), f(Ct), f(D)
+
+
+def test_zoh_matches_augmented_matrix_exponential():
+    """ZOH of state p with step Delta_p: expm([[lambda_p Delta_p, Delta_p B~_p],[0, 0]]) has
+    exp(lambda Delta) and B_bar_p as its first row (Van Loan's block exponential)."""
+    lam, ld, Bt, _, _ = _s5_small(3, 5, seed=30)
+    abar, bbar = oracle.s5_zoh(lam, ld, Bt)
+    lamc = lam[:, 0].astype(np.float64) + 1j * lam[:, 1]
+    delta = np.exp(ld.astype(np.float64))
+    Btc = Bt[..., 0].astype(np.float64) + 1j * Bt[..., 1]
+    H = Bt.shape[1]
+    for p in range(5):
+        M = np.zeros((1 + H, 1 + H), complex)
+        M[0, 0] = lamc[p] * delta[p]
+        M[0, 1:] = delta[p] * Btc[p]
+        E = scipy.linalg.expm(M)
+        np.testing.assert_allclose(abar[p], E[0, 0], rtol=1e-12)
+        np.testing.assert_allclose(bbar[p], E[0, 1:], rtol=1e-10, atol=1e-14)
+
+
+def test_s5_equals_dense_system_in_original_coordinates():
+    """S5 paper section 3: A = V Lambda V^-1, B~ = V^-1 B, C~ = C V. With one shared Delta the
+    diagonal layer must equal the dense system discretised by expm and run as a dense
+    recurrence in the original coordinates."""
+    H, P, L = 3, 4, 40
+    lam, ld, Bt, Ct, D = _s5_small(H, P, seed=31, equal_delta=True)
+    rng = np.random.default_rng(32)
+    V = rng.standard_normal((P, P)) + 1j * rng.standard_normal((P, P))
+    lamc = lam[:, 0].astype(np.float64) + 1j * lam[:, 1]
+    A = V @ np.diag(lamc) @ np.linalg.inv(V)
+    Btc = Bt[..., 0].astype(np.float64) + 1j * Bt[..., 1]
+    Ctc = Ct[..., 0].astype(np.float64) + 1j * Ct[..., 1]
+    Bd = V @ Btc
+    Cd = Ctc @ np.linalg.inv(V)
+    delta = float(np.exp(np.float64(ld[0])))
+    M = np.zeros((P + H, P + H), complex)
+    M[:P, :P] = A * delta
+    M[:P, P:] = Bd * delta
+    E = scipy.linalg.expm(M)
+    Abar, Bbar = E[:P, :P], E[:P, P:]
+    u = rng.standard_normal((2, L, H)).astype(np.float32)
+    y = oracle.s5_layer(u, lam, ld, Bt, Ct, D)
+    for b in range(2):
+        x = np.zeros(P, complex)
+        for k in range(L):
+            x = Abar @ x + Bbar @ u[b, k].astype(np.float64)
+            ref = np.real(Cd @ x) + D.astype(np.float64) * u[b, k]
+            np.testing.assert_allclose(y[b, k], ref, rtol=1e-9, atol=1e-11)
+
+
+def test_s5_zoh_exact_for_constant_input():
+    """One state, constant input c: the discrete states equal the continuous solution
+    x((k+1) Delta) = (e^{lambda (k+1) Delta} - 1)/lambda * B~ c."""
+    lam = np.array([[-0.7, 3.0]], np.float32)
+    ld = np.array([np.log(0.03)], np.float32)
+    Bt = np.array([[[0.8, -0.4]]], np.float32)
+    D = np.zeros(1, np.float32)
+    L = 300
+    c = 1.5
+    u = np.full((1, L, 1), c, np.float32)
+    lamc = complex(lam[0, 0], lam[0, 1])
+    delta = float(np.exp(np.float64(ld[0])))
+    t = (np.arange(L) + 1) * delta
+    xs = (np.exp(lamc * t) - 1) / lamc * complex(Bt[0, 0, 0], Bt[0, 0, 1]) * c
+    y_re = oracle.s5_layer(u, lam, ld, Bt, np.array([[[1.0, 0.0]]], np.float32), D)[0, :, 0]
+    y_im = oracle.s5_layer(u, lam, ld, Bt, np.array([[[0.0, -1.0]]], np.float32), D)[0, :, 0]
+    np.testing.assert_allclose(y_re, xs.real, rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(y_im, xs.imag, rtol=1e-10, atol=1e-13)
+
+
+def test_s5_feedthrough_and_linearity():
+    H, P, L = 4, 3, 30
+    lam, ld, Bt, Ct, D = _s5_small(H, P, seed=33)
+    rng = np.random.default_rng(34)
+    u1 = rng.standard_normal((1, L, H)).astype(np.float32)
+    u2 = rng.standard_normal((1, L, H)).astype(np.float32)
+    zero_c = np.zeros_like(Ct)
+    np.testing.assert_allclose(oracle.s5_layer(u1, lam, ld, Bt, zero_c, D)[0],
+                               u1[0] * D.astype(np.float64), rtol=1e-15)
+    np.testing.assert_allclose(oracle.s5_layer(u1, lam, ld, np.zeros_like(Bt), Ct, D)[0],
+                               u1[0] * D.astype(np.float64), rtol=1e-15)
+    a, b = 0.75, -2.0
+    ysum = oracle.s5_layer(u1 * np.float32(a) + u2 * np.float32(b), lam, ld, Bt, Ct, D)
+    y1 = oracle.s5_layer(u1, lam, ld, Bt, Ct, D)
+    y2 = oracle.s5_layer(u2, lam, ld, Bt, Ct, D)
+    np.testing.assert_allclose(ysum, a * y1 + b * y2, rtol=1e-5, atol=1e-6)
+
+
+# ---------------------------------------------------------------------------------------
+# Input generator structure (HiPPO-N spectrum)
+
+def test_hippo_legs_golden():
+    rows = []
+    with open(os.path.join(GOLDEN, "hippo_legs_p4.txt")) as fh:
+        for line in fh:
+            if line.startswith("#") or not line.strip():
+                continue
+            rows.append([eval(tok, {"sqrt": np.sqrt}) for tok in line.split()])
+    np.testing.assert_allclose(inputs.hippo_legs(4), np.array(rows), rtol=1e-15)
+
+
+@pytest.mark.parametrize("P", [8, 64, 256])
+def test_hippo_n_spectrum(P):
+    """Annotated S4 part 2: S = A + p p^T is -1/2 I plus a skew-symmetric matrix, so every
+    eigenvalue has real part -1/2 and they come in conjugate pairs; a general (non-Hermitian)
+    eigensolver on the dense S agrees with the generator's Hermitian route."""
+    lam = inputs.hippo_n_eigenvalues(P)
+    np.testing.assert_allclose(lam[:, 0], -0.5, rtol=0, atol=1e-12)
+    n = np.arange(P, dtype=np.float64)
+    S = inputs.hippo_legs(P) + np.outer(np.sqrt(n + 0.5), np.sqrt(n + 0.5))
+    np.testing.assert_allclose(np.diagonal(S), -0.5, atol=1e-12)
+    ev = np.linalg.eigvals(S)
+    np.testing.assert_allclose(np.sort(ev.imag), np.sort(lam[:, 1]), rtol=1e-8,
+                               atol=1e-8 * np.max(np.abs(lam[:, 1])))
+    np.testing.assert_allclose(np.sort(lam[:, 1]), -np.sort(lam[:, 1])[::-1], atol=1e-6)
+
+
+def test_dlr_init_ranges():
+    """DLR paper 2.2: |lambda| = exp(-(log Lambda)_re^2) lies in [e^-0.25, e^-0.00025]."""
+    p = inputs.dlr_params(np.random.default_rng(0), 64, 64)
+    mag = np.exp(-p.log_re.astype(np.float64) ** 2)
+    assert mag.min() >= np.exp(-0.25) * (1 - 1e-6)
+    assert mag.max() <= np.exp(-0.00025) * (1 + 1e-6)
+    np.testing.assert_allclose(p.log_im[0], 2 * np.pi * np.arange(64) / 64, rtol=1e-6)
