@@ -1,0 +1,416 @@
+#!/usr/bin/env python
+"""Benchmark of the DLR layer (kernel generation + FFT convolution) on GB300.
+
+One step = one pass of the whole DLR hot path over one batch: dlr_kernel (lambda powers ->
+K), dlr_conv_spectrum (K -> per-channel spectra) and dlr_conv_apply (u -> y) on the
+B=8, H=256, N=64, L=4096 bank (float32, synthetic seeded inputs resident in HBM). L2 is
+flushed (a 2 x L2 write) before every step; the flush is outside the timed events.
+
+Prints ONE JSON line (rank 0). Multi-GPU (torchrun): every rank runs its own batch (weak
+scaling, no data-path collective); a barrier and a max-over-ranks reduction bracket the timing.
+
+--impl reference times the float64 CPU oracle (the reference arm) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+WORKLOAD = "dlr_b8_h256_n64_l4096"
+METRIC = "DLR layer elements/s (B*H*L/s) and achieved HBM GB/s vs peak, 1xGB300"
+UNIT = "elements/s"
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+CONV_SOURCES = ["state_space_sequence_gb300/csrc/dlr_conv.cu",
+                "state_space_sequence_gb300/csrc/fft_smem.cuh",
+                "state_space_sequence_gb300/csrc/dlr_common.cuh"]
+
+
+def source_hash(paths) -> str:
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def rank_seed(base: int, rank: int) -> int:
+    """Each rank draws its own batch (weak scaling): seed offset by the rank."""
+    return base + 1000 * rank
+
+
+def aggregate(per_rank_seconds, units_per_rank: int):
+    """Whole-job throughput: all ranks' units over the slowest rank's time."""
+    t = max(per_rank_seconds)
+    return units_per_rank * len(per_rank_seconds) / t, t
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed loop runs."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.window = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-i", str(self.index), "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = self.samples
+        if self.window is not None:
+            inside = [r for r in rows if self.window[0] <= r[0] <= self.window[1]]
+            rows = inside or rows
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1][0]) for r in rows if r[1][0].replace(".", "").isdigit()]
+        mx = [float(r[1][1]) for r in rows if r[1][1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[1][2 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    from state_space_sequence_gb300 import dlr, inputs
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    cfg = dict(inputs.WORKLOADS[WORKLOAD])
+    B, H, N, L = cfg["B"], cfg["H"], cfg["N"], cfg["L"]
+    w = inputs.make_dlr(B, H, N, L, seed=rank_seed(cfg["seed"], rank))
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    u = dev(w.u)
+    fwd = (dev(w.fwd.log_re), dev(w.fwd.log_im), dev(w.fwd.W))
+    K = torch.empty((H, L), dtype=torch.float32, device="cuda")
+    ws = torch.empty(dlr.dlr_conv_workspace_size(H, L), dtype=torch.uint8, device="cuda")
+    y = torch.empty_like(u)
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 128 << 20) or (128 << 20))
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step(evs=None):
+        dlr.dlr_kernel(*fwd, L, "re", out=K)
+        dlr.dlr_conv_spectrum(K, workspace=ws)
+        if evs is not None:
+            evs[0].record(stream)
+        dlr.dlr_conv_apply(u, ws, out=y)
+        if evs is not None:
+            evs[1].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if dlr.device_status() != 0:
+        raise RuntimeError("device status non-zero after warm-up")
+
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    starts, ends, a0s, a1s = [], [], [], []
+    for _ in range(args.steps):
+        flush.zero_()
+        s, e, a0, a1 = ev(), ev(), ev(), ev()
+        s.record(stream)
+        step((a0, a1))
+        e.record(stream)
+        starts.append(s), ends.append(e), a0s.append(a0), a1s.append(a1)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    sampler.window = (t_wall0, t_wall1)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    apply_ms = [a.elapsed_time(b) for a, b in zip(a0s, a1s)]
+    total_s = sum(step_ms) / 1e3
+    if dist is not None:
+        t = torch.tensor([total_s], dtype=torch.float64, device="cuda")
+        gathered = [torch.zeros_like(t) for _ in range(world)]
+        dist.all_gather(gathered, t)
+        per_rank = [float(g.item()) for g in gathered]
+    else:
+        per_rank = [total_s]
+    units = B * H * L * args.steps
+    value, t_max = aggregate(per_rank, units)
+
+    # end to end through the public API with host buffers (pinned), copies inside the timing
+    u_h = torch.from_numpy(w.u).pin_memory()
+    p_h = [torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+           for a in (w.fwd.log_re, w.fwd.log_im, w.fwd.W)]
+    y_h = torch.empty(u_h.shape, dtype=torch.float32).pin_memory()
+    u_d, p_d = torch.empty_like(u), [torch.empty_like(t) for t in fwd]
+    e2e_steps = min(args.steps, 200)
+    e2e_ms = []
+    for i in range(e2e_steps + 3):
+        flush.zero_()
+        s, e = ev(), ev()
+        s.record(stream)
+        u_d.copy_(u_h, non_blocking=True)
+        for dst, src in zip(p_d, p_h):
+            dst.copy_(src, non_blocking=True)
+        dlr.dlr_layer(u_d, tuple(p_d), path="fft", workspace=ws, out=y)
+        y_h.copy_(y, non_blocking=True)
+        e.record(stream)
+        if i >= 3:
+            e2e_ms.append((s, e))
+    torch.cuda.synchronize()
+    e2e_total = sum(s.elapsed_time(e) for s, e in e2e_ms) / 1e3
+    e2e_value = B * H * L * e2e_steps / e2e_total
+    h2d = u_h.numel() * 4 + sum(t.numel() * 4 for t in p_h)
+    d2h = y_h.numel() * 4
+    if dlr.device_status() != 0:
+        raise RuntimeError("device status non-zero after timing")
+
+    sampler.stop()
+    clocks = sampler.summary() if rank == 0 else None
+
+    # roofline of the dominant kernel (dlr_conv_apply: one launch of the FFT row kernel)
+    n = 1 << max(0, int(np.ceil(np.log2(L))))
+    apply_bytes = 4 * B * H * L * 2 + 8 * H * (n + 1)  # u in + y out + spectra read once
+    apply_avg = sum(apply_ms) / len(apply_ms) / 1e3
+    peak, peak_kind = load_peaks()
+    achieved = apply_bytes / apply_avg / 1e9
+    traffic = None
+    if os.path.exists(PROFILE_TRAFFIC):
+        with open(PROFILE_TRAFFIC) as fh:
+            prof = json.load(fh)
+        entry = prof.get("conv_rows")
+        if entry and entry.get("source_hash") == source_hash(CONV_SOURCES):
+            traffic = entry.get("dram_bytes_per_launch")
+    layer_bytes = 4 * B * H * L * 2 + 4 * H * N * 4  # u + y + (log_re, log_im, W)
+    step_avg = total_s / args.steps
+
+    extras = {}
+    if rank == 0 and world == 1 and not args.no_extras:
+        extras = run_extras(torch, dlr, inputs, flush)
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    cpu = None if world > 1 or args.no_cpu_baseline else cpu_baseline(w)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; DLR init of the pages, u ~ N(0,1))",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "L": L, "path": "fft",
+                   "cast": "re", "causal": True, "parallelism": f"replicas x{world}",
+                   "l2": "flushed before every step (2 x L2 write), flush outside the events",
+                   "step": "dlr_kernel + dlr_conv_spectrum + dlr_conv_apply"},
+        "layer_hbm": {"algorithmic_bytes": layer_bytes,
+                      "achieved_gbs": layer_bytes / step_avg / 1e9,
+                      "frac_of_measured_peak": layer_bytes / step_avg / 1e9 / peak},
+        "roofline": {"kernel": "conv_rows (dlr_conv_apply)", "bound": "hbm",
+                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes": apply_bytes, "avg_launch_us": apply_avg * 1e6},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "paths": extras,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def _time_steps(torch, fn, steps, warmup, flush):
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(steps):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        ms.append((s, e))
+    torch.cuda.synchronize()
+    return statistics.median(s.elapsed_time(e) for s, e in ms)
+
+
+def run_extras(torch, dlr, inputs, flush):
+    """Secondary lines: the scan path on the same bank, and the other workloads."""
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    out = {}
+    w = inputs.make_workload(WORKLOAD)
+    u, fwd = dev(w.u), (dev(w.fwd.log_re), dev(w.fwd.log_im), dev(w.fwd.W))
+    y = torch.empty_like(u)
+    ms = _time_steps(torch, lambda: dlr.dlr_scan(u, fwd, out=y), 20, 3, flush)
+    out["scan_" + WORKLOAD] = {"ms": ms, "elements_per_s": w.B * w.H * w.L / ms * 1e3}
+    del u, y
+
+    w = inputs.make_workload("dlrprod_bidir_b4_h128_n1024_l16384")
+    u = dev(w.u)
+    f = (dev(w.fwd.log_re), dev(w.fwd.log_im), dev(w.fwd.W))
+    b = (dev(w.bwd.log_re), dev(w.bwd.log_im), dev(w.bwd.W))
+    y = torch.empty_like(u)
+    ws = torch.empty(dlr.dlr_conv_workspace_size(w.H, w.L, True), dtype=torch.uint8,
+                     device="cuda")
+    ms = _time_steps(torch, lambda: dlr.dlr_layer(u, f, b, cast="re_im", workspace=ws, out=y),
+                     10, 2, flush)
+    out["fft_" + w.name] = {"ms": ms, "elements_per_s": w.B * w.H * w.L / ms * 1e3}
+    del u, y, ws
+
+    w = inputs.make_workload("dlr_b1_h256_n64_l65536_unit8")
+    u, fwd = dev(w.u), (dev(w.fwd.log_re), dev(w.fwd.log_im), dev(w.fwd.W))
+    y = torch.empty_like(u)
+    ms = _time_steps(torch, lambda: dlr.dlr_scan(u, fwd, out=y), 10, 2, flush)
+    out["scan_" + w.name] = {"ms": ms, "elements_per_s": w.B * w.H * w.L / ms * 1e3}
+    del u, y
+
+    w = inputs.make_workload("s5_b8_l16384_h512_p256")
+    p = w.params
+    u = dev(w.u)
+    args5 = (dev(p.lam), dev(p.log_delta), dev(p.Bt), dev(p.Ct), dev(p.D))
+    ws = torch.empty(dlr.s5_workspace_size(w.B, w.L, w.H, w.P), dtype=torch.uint8,
+                     device="cuda")
+    y = torch.empty_like(u)
+    ms = _time_steps(torch, lambda: dlr.s5_layer(u, *args5, workspace=ws, out=y), 5, 2, flush)
+    out["s5_fp32_" + w.name] = {"ms": ms, "elements_per_s": w.B * w.L * w.H / ms * 1e3}
+    return out
+
+
+def cpu_baseline(w):
+    """The float64 oracle (as it stands) on the full bank, threaded over (b, h) rows."""
+    import oracle
+    threads = max(1, min(os.cpu_count() or 1, 64))
+    t0 = time.perf_counter()
+    oracle.dlr_layer(w.u, (w.fwd.log_re, w.fwd.log_im, w.fwd.W), nthreads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": w.B * w.H * w.L / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"full {WORKLOAD} bank (sequential float64 recurrence), {dt:.2f} s"}
+
+
+# --------------------------------------------------------------------------------------------
+def run_reference(args):
+    """Reference arm: the float64 CPU oracle, each step a bounded sample (8 (b,h) rows)."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from state_space_sequence_gb300 import inputs
+    cfg = dict(inputs.WORKLOADS[WORKLOAD])
+    w = inputs.make_dlr(cfg["B"], cfg["H"], cfg["N"], cfg["L"], seed=cfg["seed"])
+    rows = 8
+    threads = max(1, min(os.cpu_count() or 1, rows))
+    u = np.ascontiguousarray(w.u[:1, :rows])
+    par = (w.fwd.log_re[:rows], w.fwd.log_im[:rows], w.fwd.W[:rows])
+    for _ in range(args.warmup):
+        oracle.dlr_layer(u, par, nthreads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.dlr_layer(u, par, nthreads=threads)
+    dt = time.perf_counter() - t0
+    value = rows * cfg["L"] * args.steps / dt
+    sample = f"{rows} (b,h) rows of {WORKLOAD} per step (sequential float64 recurrence)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "B": cfg["B"], "H": cfg["H"],
+                                        "N": cfg["N"], "L": cfg["L"]},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,155 @@
+/*
+ * dlr.h -- C ABI of libdlr.so: diagonal linear recurrences (DLR, diagonal SSM, S5) on one
+ * NVIDIA GB300 GPU (sm_103a).
+ *
+ * Conventions shared by every entry point
+ *  - All tensor pointers are DEVICE pointers owned by the caller. The library never
+ *    allocates, frees or keeps them; scratch memory is passed in as `workspace`, sized by the
+ *    matching *_workspace_size() query (a size of 0 means no workspace is needed and the
+ *    pointer may be NULL).
+ *  - Sizes are int64_t element counts. Real tensors are float32, row-major, innermost index
+ *    last. A complex value is two consecutive float32 (re, im).
+ *  - Every compute call is asynchronous on `stream` (NULL = legacy default stream). Argument
+ *    validation happens before anything is launched: an invalid call returns
+ *    DLR_ERR_INVALID_ARG / DLR_ERR_UNSUPPORTED / DLR_ERR_WORKSPACE synchronously and launches
+ *    nothing. A launch failure returns DLR_ERR_CUDA. Faults detected on the device (a bounded
+ *    wait that ran out) are latched in a device status word read by dlr_get_device_status().
+ *  - Tensor pointers must be 16-byte aligned (128-bit vector loads / bulk copies).
+ *  - The arithmetic is float32 throughout except where an entry point says otherwise.
+ *
+ * Notation follows "Simplifying and Understanding State Space Models with Diagonal Linear
+ * RNNs" (DLR) and "Simplified State Space Layers for Sequence Modeling" (S5).
+ */
+#ifndef DLR_H_
+#define DLR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so the header needs no CUDA headers. */
+typedef struct CUstream_st* dlr_stream_t;
+
+typedef enum {
+  DLR_OK = 0,
+  DLR_ERR_INVALID_ARG = 1, /* NULL/misaligned pointer, non-positive or inconsistent size */
+  DLR_ERR_UNSUPPORTED = 2, /* valid request outside what the kernels implement           */
+  DLR_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed                 */
+  DLR_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (see dlr_get_device_status) */
+  DLR_ERR_WORKSPACE = 5    /* workspace missing or smaller than *_workspace_size()        */
+} dlr_status;
+
+/* Kernel cast. DLR paper section 2: y_k = sum_{j<=k} Re(K_j) u_{k-j} (the Re cast);
+ * section 2.1: DLR-prod uses Re(K_j) * Im(K_j) instead. */
+typedef enum { DLR_CAST_RE = 0, DLR_CAST_RE_IM = 1 } dlr_cast;
+
+/* Direction. DLR paper section 2.1: the bidirectional DLR sums two independent DLRs, the
+ * second one applied to the time-reversed sequence (lag 0 is counted by both). */
+typedef enum { DLR_CAUSAL = 0, DLR_BIDIR = 1 } dlr_dir;
+
+/* Precision tier of s5_layer's projections. */
+typedef enum { DLR_FP32 = 0, DLR_BF16_TC = 1 } dlr_prec;
+
+/*
+ * dlr_kernel -- the DLR convolution kernel (DLR paper section 2, Eq. 3/4 and section 2.2):
+ *   lambda_{h,n} = exp(-log_re[h,n]^2 + i*log_im[h,n])
+ *   K_{h,j}      = sum_n W_{h,n} lambda_{h,n}^j ,  j = 0..L-1
+ *   out K[h,j]   = Re K_{h,j}                 (cast = DLR_CAST_RE)
+ *                = Re K_{h,j} * Im K_{h,j}    (cast = DLR_CAST_RE_IM, "DLR-prod")
+ * log_re, log_im: [H, N] float32. W: [H, N, 2] complex. K: [H, L] float32 (written).
+ * lambda^j is formed from the parameters with an exactly reduced phase j*theta, not by
+ * repeated multiplication of a rounded lambda. Limits: 1 <= N, 1 <= L < 2^24.
+ */
+dlr_status dlr_kernel(const float* log_re, const float* log_im, const float* W, int64_t H,
+                      int64_t N, int64_t L, dlr_cast cast, float* K, dlr_stream_t stream);
+
+/*
+ * dlr_conv -- apply the (already cast) real kernels by FFT convolution (DLR paper section 2.1
+ * and appendix A.1: the Toeplitz product as a circulant product of size >= 2L):
+ *   causal : y[b,h,k] = sum_{j=0}^{k} K_fwd[h,j] u[b,h,k-j]
+ *   bidir  : y[b,h,k] = sum_{j=0}^{k} K_fwd[h,j] u[b,h,k-j] + sum_{j=0}^{L-1-k} K_bwd[h,j] u[b,h,k+j]
+ * u, y: [B, H, L] float32. K_fwd, K_bwd: [H, L] float32 (K_bwd NULL when dir = DLR_CAUSAL).
+ * workspace: >= dlr_conv_workspace_size(H, L, dir) bytes of device memory holding the twiddle
+ * table and the per-channel kernel spectra (no initialisation needed; overwritten).
+ * u and y must not overlap. Limits: 1 <= L <= 16384.
+ * dlr_conv is exactly dlr_conv_spectrum followed by dlr_conv_apply on the same stream.
+ */
+size_t dlr_conv_workspace_size(int64_t H, int64_t L, dlr_dir dir);
+dlr_status dlr_conv(const float* u, const float* K_fwd, const float* K_bwd, dlr_dir dir,
+                    int64_t B, int64_t H, int64_t L, float* y, void* workspace,
+                    size_t workspace_bytes, dlr_stream_t stream);
+
+/*
+ * dlr_conv_spectrum -- first half of dlr_conv: writes the twiddle table and the spectrum of
+ * each channel's length-2n circulant column (n = next power of two >= L) into `workspace`.
+ * The spectra depend only on the kernels, so one call can serve many dlr_conv_apply calls
+ * (e.g. every batch) as long as the workspace is left untouched in between.
+ */
+dlr_status dlr_conv_spectrum(const float* K_fwd, const float* K_bwd, dlr_dir dir, int64_t H,
+                             int64_t L, void* workspace, size_t workspace_bytes,
+                             dlr_stream_t stream);
+
+/*
+ * dlr_conv_apply -- second half of dlr_conv: y = FFT convolution of u with the spectra that
+ * a preceding dlr_conv_spectrum (same H and L, earlier in stream order) left in `workspace`.
+ * Reads the workspace only; one kernel launch, one CTA per (b, h) row.
+ */
+dlr_status dlr_conv_apply(const float* u, int64_t B, int64_t H, int64_t L, float* y,
+                          const void* workspace, size_t workspace_bytes, dlr_stream_t stream);
+
+/*
+ * dlr_scan -- the DLR as a chunked scan of the recurrence (DLR paper section 2, Eq. 1; S5
+ * paper section 2.2, parallel scan over a diagonal state matrix):
+ *   x_{n,k} = lambda_n x_{n,k-1} + u_k  (x_{-1} = 0),   y_k = sum_n Re(W_n x_{n,k})
+ * computed per (b,h) row without materialising the kernel. With dir = DLR_BIDIR the second
+ * parameter set (log_re2, log_im2, W2) runs on the reversed sequence and its output is added.
+ * Only the Re cast exists here (DLR-prod has no N-state recurrence; use dlr_conv).
+ * u, y: [B, H, L]; parameter layouts as in dlr_kernel. No workspace. u and y must not
+ * overlap. Limits: 1 <= N <= 128, 1 <= L < 2^24.
+ */
+dlr_status dlr_scan(const float* u, const float* log_re, const float* log_im, const float* W,
+                    const float* log_re2, const float* log_im2, const float* W2, dlr_dir dir,
+                    int64_t B, int64_t H, int64_t N, int64_t L, float* y,
+                    dlr_stream_t stream);
+
+/*
+ * s5_layer -- S5 SSM outputs (S5 paper section 3: diagonalised MIMO system; zero-order hold
+ * with one timescale per state; diagonal feedthrough):
+ *   Delta_p   = exp(log_delta[p])
+ *   Lbar_p    = exp(Lambda_p Delta_p),   Bbar[p,:] = (Lbar_p - 1) / Lambda_p * Bt[p,:]
+ *   x_k       = Lbar (.) x_{k-1} + Bbar u_k   (x_{-1} = 0)
+ *   y_k       = Re(Ct x_k) + D (.) u_k
+ * u, y: [B, L, H] float32. lambda: [P, 2]. log_delta: [P]. Bt: [P, H, 2]. Ct: [H, P, 2].
+ * D: [H]. prec = DLR_FP32: all products in float32 FMA. prec = DLR_BF16_TC: the two
+ * projections on tensor cores with bfloat16 operands and float32 accumulation.
+ * workspace: >= s5_workspace_size(B, L, H, P, prec) bytes. u and y must not overlap.
+ * Limits: H % 32 == 0, P % 32 == 0, 32 <= H, P <= 1024.
+ */
+size_t s5_workspace_size(int64_t B, int64_t L, int64_t H, int64_t P, dlr_prec prec);
+dlr_status s5_layer(const float* u, const float* lambda, const float* log_delta,
+                    const float* Bt, const float* Ct, const float* D, int64_t B, int64_t L,
+                    int64_t H, int64_t P, dlr_prec prec, float* y, void* workspace,
+                    size_t workspace_bytes, dlr_stream_t stream);
+
+/*
+ * dlr_get_device_status -- synchronise `stream`, then read and clear the device status word
+ * shared by all kernels of this library on the current device. Returns DLR_OK when no kernel
+ * reported a fault since the last call, DLR_ERR_TIMEOUT when a bounded wait gave up, or
+ * DLR_ERR_CUDA when the synchronisation itself failed.
+ */
+dlr_status dlr_get_device_status(dlr_stream_t stream);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* dlr_status_string(dlr_status status);
+
+/* Library ABI version (incremented on any signature change). */
+int dlr_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DLR_H_ */

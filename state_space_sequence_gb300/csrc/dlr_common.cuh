@@ -1,0 +1,128 @@
+// dlr_common.cuh -- device helpers shared by the libdlr kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dlr.h"
+
+namespace dlr {
+
+struct cf {
+  float re, im;
+};
+
+__device__ __forceinline__ cf cmul(cf a, cf b) {
+  return {fmaf(a.re, b.re, -a.im * b.im), fmaf(a.re, b.im, a.im * b.re)};
+}
+__device__ __forceinline__ cf cadd(cf a, cf b) { return {a.re + b.re, a.im + b.im}; }
+__device__ __forceinline__ cf cconj(cf a) { return {a.re, -a.im}; }
+// a*b + c
+__device__ __forceinline__ cf cfma(cf a, cf b, cf c) {
+  return {fmaf(a.re, b.re, fmaf(-a.im, b.im, c.re)), fmaf(a.re, b.im, fmaf(a.im, b.re, c.im))};
+}
+
+// 2*pi as the unevaluated sum A + B + C of three floats (Cody & Waite's additive argument
+// reduction, "Software Manual for the Elementary Functions", 1980). A = float(2 pi),
+// B = float(2 pi - A), C = float(2 pi - A - B), computed from a 60-digit value of pi.
+constexpr float kTwoPiA = 0x1.921fb6p+2f;
+constexpr float kTwoPiB = -0x1.777a5cp-23f;
+constexpr float kTwoPiC = -0x1.ee59dap-48f;
+constexpr float kInvTwoPi = 0x1.45f306p-3f;
+
+// Reduced angle of j*(th_hi + th_lo) modulo 2 pi, in about [-pi, pi].
+//  - j*th_hi is carried exactly as hi + lo (fmaf gives the rounding error of the product;
+//    j < 2^24 is exact in float).
+//  - k = nearest integer to hi / 2pi (|k| < 2^23 because |th_hi| <= pi + ulp).
+//  - hi - k*A is exact: both are multiples of 2^-21 when |hi| >= 4 (and k is 0 or +-1 below),
+//    and the difference is below 8 in magnitude, so it fits a 24-bit significand. The B and C
+//    terms each add at most half an ulp of a value below 4.
+// The absolute error is about 2^-23 rad, independent of j.
+__device__ __forceinline__ float reduce_phase(float jf, float th_hi, float th_lo) {
+  float hi = jf * th_hi;
+  float lo = fmaf(jf, th_hi, -hi);
+  float k = rintf(hi * kInvTwoPi);
+  float r = fmaf(-k, kTwoPiA, hi);
+  r = fmaf(-k, kTwoPiB, r);
+  r = fmaf(-k, kTwoPiC, r);
+  return r + fmaf(jf, th_lo, lo);
+}
+
+// Per-state parameters prepared once: a2 = (log Lambda)_re^2 and the phase theta reduced to
+// (-pi, pi] and split into float hi + lo (reduction done in double: one per state).
+struct lam_param {
+  float a2;
+  float th_hi, th_lo;
+};
+
+__device__ __forceinline__ lam_param make_lam_param(float log_re, float log_im) {
+  lam_param p;
+  p.a2 = log_re * log_re;
+  double t = (double)log_im;
+  const double two_pi = 6.283185307179586476925286766559;
+  t = t - two_pi * rint(t / two_pi);
+  p.th_hi = (float)t;
+  p.th_lo = (float)(t - (double)p.th_hi);
+  return p;
+}
+
+// lambda^j = exp(-j a^2) * (cos(j theta) + i sin(j theta)), j >= 0, evaluated directly from
+// the parameters. Magnitude: the argument j*a2 carries a relative error of one rounding, which
+// changes exp(-x) by x*2^-24 relative -- at most e^-1 * 2^-24 of the largest term. Phase: the
+// reduction above. Uses CUDA's expf / sincosf (compiled without fast-math).
+__device__ __forceinline__ cf lam_pow(const lam_param& p, int j) {
+  float jf = (float)j;
+  float mag = expf(-jf * p.a2);
+  float s, c;
+  sincosf(reduce_phase(jf, p.th_hi, p.th_lo), &s, &c);
+  return {mag * c, mag * s};
+}
+
+// ---------------------------------------------------------------------------------------
+// Two-float ("double-float") arithmetic, after Dekker (1971) and Knuth's TwoSum: a value is
+// hi + lo with |lo| <= ulp(hi)/2.
+struct ff {
+  float hi, lo;
+};
+
+__device__ __forceinline__ ff two_sum(float a, float b) {
+  float s = a + b;
+  float bb = s - a;
+  float e = (a - (s - bb)) + (b - bb);
+  return {s, e};
+}
+__device__ __forceinline__ ff fast_two_sum(float a, float b) {
+  float s = a + b;
+  return {s, b - (s - a)};
+}
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+  ff s = two_sum(a.hi, b.hi);
+  float lo = s.lo + (a.lo + b.lo);
+  return fast_two_sum(s.hi, lo);
+}
+__device__ __forceinline__ ff ff_mul(ff a, ff b) {
+  float p = a.hi * b.hi;
+  float e = fmaf(a.hi, b.hi, -p);
+  e = fmaf(a.hi, b.lo, fmaf(a.lo, b.hi, e));
+  return fast_two_sum(p, e);
+}
+__device__ __forceinline__ ff ff_neg(ff a) { return {-a.hi, -a.lo}; }
+
+struct cff {
+  ff re, im;
+};
+// a*b + c in two-float complex arithmetic
+__device__ __forceinline__ cff cff_fma(cff a, cff b, cff c) {
+  ff re = ff_add(ff_add(ff_mul(a.re, b.re), ff_neg(ff_mul(a.im, b.im))), c.re);
+  ff im = ff_add(ff_add(ff_mul(a.re, b.im), ff_mul(a.im, b.re)), c.im);
+  return {re, im};
+}
+
+// Kernels whose bounded waits run out record the reason in the library's device status
+// word (its address is passed to them as a kernel argument); dlr_get_device_status() reads
+// and clears it.
+__device__ __forceinline__ void report_status(int* status, int code) {
+  if (status) atomicMax(status, code);
+}
+
+}  // namespace dlr

@@ -1,0 +1,263 @@
+// s5_layer.cu -- S5 SSM outputs ("Simplified State Space Layers for Sequence Modeling",
+// section 2.2 (linear recurrence as a scan), section 3 (diagonalised MIMO system with B~, C~,
+// diagonal D, one timescale per state, zero-order hold)):
+//   Lbar = exp(Lambda Delta), Bbar = (Lbar - 1)/Lambda * B~,
+//   x_k = Lbar x_{k-1} + Bbar u_k,   y_k = Re(C~ x_k) + D u_k.
+//
+// Float32 tier, as a sequence of kernels over a workspace:
+//   prep   (one CTA per state p, double precision): Lbar_p, the powers Lbar_p^t (t <= T) and
+//          Lbar_p^T as two floats, Bbar as the real [H, 2P] operand, C~ as the real [2P, H]
+//          operand [Re C~^T ; -Im C~^T].
+//   gemm   V[B*L, 2P] = u[B*L, H] * Bbar^T (float32 FFMA, register tiled)
+//   chunk  S_c = sum_t Lbar^{T-1-t} V_t (end state of chunk c from a zero start)
+//   carry  X_c = Lbar^T X_{c-1} + S_c, sequential over chunks in two-float arithmetic;
+//          stores the state entering each chunk
+//   apply  x_t = Lbar^{t+1} X_in + sum_{s<=t} Lbar^{t-s} V_s, written over V in place
+//   gemm   y = x * [Re C~^T ; -Im C~^T] + D (.) u
+#include "dlr_common.cuh"
+
+namespace dlr {
+namespace {
+
+constexpr int kT = 64;   // steps per chunk
+constexpr int kPB = 32;  // complex states per chunk-kernel CTA
+
+struct S5Work {
+  float* bbar;     // [H][2P]
+  float* cmat;     // [2P][H]
+  float2* lbar_pw; // [P][T+1]  Lbar^t
+  float4* lbar_T;  // [P] (re.hi, re.lo, im.hi, im.lo) of Lbar^T
+  float2* S;       // [B][NC][P]
+  float2* Xin;     // [B][NC][P]
+  float* xv;       // [B*L][2P]: V, then x
+};
+
+__global__ void s5_prep(const float* __restrict__ lambda, const float* __restrict__ log_delta,
+                        const float2* __restrict__ Bt, const float2* __restrict__ Ct, int H, int P,
+                        S5Work w) {
+  const int p = blockIdx.x;
+  const double lr = lambda[2 * p], li = lambda[2 * p + 1];
+  const double delta = exp((double)log_delta[p]);
+  const double zr = lr * delta, zi = li * delta;
+  const double er = exp(zr);
+  const double ar = er * cos(zi), ai = er * sin(zi);  // Lbar
+  // (Lbar - 1) / Lambda
+  const double nr = ar - 1.0, ni = ai;
+  const double den = lr * lr + li * li;
+  const double qr = (nr * lr + ni * li) / den, qi = (ni * lr - nr * li) / den;
+  for (int h = threadIdx.x; h < H; h += blockDim.x) {
+    float2 b = Bt[(size_t)p * H + h];
+    double br = qr * b.x - qi * b.y, bi = qr * b.y + qi * b.x;
+    w.bbar[(size_t)h * 2 * P + 2 * p] = (float)br;
+    w.bbar[(size_t)h * 2 * P + 2 * p + 1] = (float)bi;
+    float2 c = Ct[(size_t)h * P + p];
+    w.cmat[(size_t)(2 * p) * H + h] = c.x;
+    w.cmat[(size_t)(2 * p + 1) * H + h] = -c.y;
+  }
+  for (int t = threadIdx.x; t <= kT; t += blockDim.x) {
+    const double m = exp(zr * t), ph = zi * t;
+    w.lbar_pw[(size_t)p * (kT + 1) + t] = make_float2((float)(m * cos(ph)), (float)(m * sin(ph)));
+    if (t == kT) {
+      double re = m * cos(ph), im = m * sin(ph);
+      float rh = (float)re, ih = (float)im;
+      w.lbar_T[p] = make_float4(rh, (float)(re - rh), ih, (float)(im - ih));
+    }
+  }
+}
+
+// C[M, N] = A[M, K] * Bm[K, N] (+ D[n] * E[m, n] when E != nullptr); row-major, K % 16 == 0.
+constexpr int kGM = 64, kGN = 64, kGK = 16;
+__global__ void __launch_bounds__(256)
+gemm_f32(const float* __restrict__ A, const float* __restrict__ Bm, float* __restrict__ C, int M,
+         int N, int K, const float* __restrict__ D, const float* __restrict__ E) {
+  __shared__ float sA[kGK][kGM + 4];
+  __shared__ __align__(16) float sB[kGK][kGN];
+  const int tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+  const int m0 = blockIdx.y * kGM, n0 = blockIdx.x * kGN;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += kGK) {
+    for (int e = tid; e < kGM * kGK; e += 256) {
+      int r = e / kGK, k = e % kGK;
+      int m = m0 + r;
+      sA[k][r] = (m < M) ? A[(size_t)m * K + k0 + k] : 0.f;
+    }
+    for (int e = tid; e < kGK * kGN; e += 256) {
+      int k = e / kGN, c = e % kGN;
+      int n = n0 + c;
+      sB[k][c] = (n < N) ? Bm[(size_t)(k0 + k) * N + n] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kGK; ++k) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = sA[k][ty + 16 * i];
+      float4 bv = *reinterpret_cast<const float4*>(&sB[k][4 * tx]);
+      b[0] = bv.x; b[1] = bv.y; b[2] = bv.z; b[3] = bv.w;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    int m = m0 + ty + 16 * i;
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int n = n0 + 4 * tx + j;
+      if (n >= N) continue;
+      float v = acc[i][j];
+      if (E) v = fmaf(D[n], E[(size_t)m * N + n], v);
+      C[(size_t)m * N + n] = v;
+    }
+  }
+}
+
+// grid (P / kPB, NC, B): chunk end states from a zero start.
+__global__ void __launch_bounds__(256)
+s5_chunk_state(S5Work w, int L, int P, int NC) {
+  __shared__ float2 sV[kT][kPB + 1];
+  __shared__ float2 sPart[8][kPB];
+  const int pb = blockIdx.x * kPB, c = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x;
+  const int t0 = c * kT;
+  const int valid = min(kT, L - t0);
+  for (int e = tid; e < kT * kPB; e += 256) {
+    int t = e / kPB, pl = e % kPB;
+    float2 v = make_float2(0.f, 0.f);
+    if (t < valid)
+      v = *reinterpret_cast<const float2*>(w.xv + ((size_t)b * L + t0 + t) * 2 * P + 2 * (pb + pl));
+    sV[t][pl] = v;
+  }
+  __syncthreads();
+  const int pl = tid & 31, g = tid >> 5;  // 8 groups of 8 steps
+  const float2* pw = w.lbar_pw + (size_t)(pb + pl) * (kT + 1);
+  cf acc = {0.f, 0.f};
+  for (int t = 8 * g; t < 8 * g + 8; ++t) {
+    float2 a = pw[kT - 1 - t], v = sV[t][pl];
+    acc = cfma({a.x, a.y}, {v.x, v.y}, acc);
+  }
+  sPart[g][pl] = make_float2(acc.re, acc.im);
+  __syncthreads();
+  if (tid < kPB) {
+    float sr = 0.f, si = 0.f;
+    for (int q = 0; q < 8; ++q) {
+      sr += sPart[q][tid].x;
+      si += sPart[q][tid].y;
+    }
+    w.S[((size_t)b * NC + c) * P + pb + tid] = make_float2(sr, si);
+  }
+}
+
+// one thread per (b, p): the state entering each chunk, chained in two-float arithmetic
+__global__ void s5_carry(S5Work w, int B, int P, int NC) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= B * P) return;
+  const int b = i / P, p = i % P;
+  const float4 lt = w.lbar_T[p];
+  const cff m = {{lt.x, lt.y}, {lt.z, lt.w}};
+  cff x = {{0.f, 0.f}, {0.f, 0.f}};
+  for (int c = 0; c < NC; ++c) {
+    const size_t o = ((size_t)b * NC + c) * P + p;
+    w.Xin[o] = make_float2(x.re.hi + x.re.lo, x.im.hi + x.im.lo);
+    float2 s = w.S[o];
+    x = cff_fma(m, x, {{s.x, 0.f}, {s.y, 0.f}});
+  }
+}
+
+// grid (P / kPB, NC, B): x_t = Lbar^{t+1} X_in + sum_{s<=t} Lbar^{t-s} V_s, in place over V.
+__global__ void __launch_bounds__(256)
+s5_chunk_apply(S5Work w, int L, int P, int NC) {
+  __shared__ float2 sV[kT][kPB + 1];
+  __shared__ float2 sPw[kPB][kT + 2];
+  const int pb = blockIdx.x * kPB, c = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x;
+  const int t0 = c * kT;
+  const int valid = min(kT, L - t0);
+  for (int e = tid; e < kT * kPB; e += 256) {
+    int t = e / kPB, pl = e % kPB;
+    float2 v = make_float2(0.f, 0.f);
+    if (t < valid)
+      v = *reinterpret_cast<const float2*>(w.xv + ((size_t)b * L + t0 + t) * 2 * P + 2 * (pb + pl));
+    sV[t][pl] = v;
+  }
+  for (int e = tid; e < kPB * (kT + 1); e += 256) {
+    int pl = e / (kT + 1), t = e % (kT + 1);
+    sPw[pl][t] = w.lbar_pw[(size_t)(pb + pl) * (kT + 1) + t];
+  }
+  __syncthreads();
+  const int pl = tid & 31, g = tid >> 5;
+  const float2 xi = w.Xin[((size_t)b * NC + c) * P + pb + pl];
+  const cf xin = {xi.x, xi.y};
+  for (int t = g; t < valid; t += 8) {
+    float2 a = sPw[pl][t + 1];
+    cf acc = cmul({a.x, a.y}, xin);
+    for (int s = 0; s <= t; ++s) {
+      float2 q = sPw[pl][t - s], v = sV[s][pl];
+      acc = cfma({q.x, q.y}, {v.x, v.y}, acc);
+    }
+    *reinterpret_cast<float2*>(w.xv + ((size_t)b * L + t0 + t) * 2 * P + 2 * (pb + pl)) =
+        make_float2(acc.re, acc.im);
+  }
+}
+
+S5Work carve(void* ws, int64_t B, int64_t L, int64_t H, int64_t P, size_t* total) {
+  const int64_t NC = (L + kT - 1) / kT;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off += (bytes + 255) & ~size_t(255);
+    return o;
+  };
+  size_t o_bbar = take(sizeof(float) * H * 2 * P);
+  size_t o_cmat = take(sizeof(float) * 2 * P * H);
+  size_t o_pw = take(sizeof(float2) * P * (kT + 1));
+  size_t o_lt = take(sizeof(float4) * P);
+  size_t o_S = take(sizeof(float2) * B * NC * P);
+  size_t o_X = take(sizeof(float2) * B * NC * P);
+  size_t o_xv = take(sizeof(float) * B * L * 2 * P);
+  if (total) *total = off;
+  char* base = reinterpret_cast<char*>(ws);
+  S5Work w;
+  w.bbar = reinterpret_cast<float*>(base + o_bbar);
+  w.cmat = reinterpret_cast<float*>(base + o_cmat);
+  w.lbar_pw = reinterpret_cast<float2*>(base + o_pw);
+  w.lbar_T = reinterpret_cast<float4*>(base + o_lt);
+  w.S = reinterpret_cast<float2*>(base + o_S);
+  w.Xin = reinterpret_cast<float2*>(base + o_X);
+  w.xv = reinterpret_cast<float*>(base + o_xv);
+  return w;
+}
+
+}  // namespace
+
+size_t s5_workspace_bytes(int64_t B, int64_t L, int64_t H, int64_t P) {
+  size_t total = 0;
+  carve(nullptr, B, L, H, P, &total);
+  return total;
+}
+
+cudaError_t launch_s5_fp32(const float* u, const float* lambda, const float* log_delta,
+                           const float* Bt, const float* Ct, const float* D, int B, int L, int H,
+                           int P, float* y, void* ws, cudaStream_t s) {
+  const int NC = (L + kT - 1) / kT;
+  S5Work w = carve(ws, B, L, H, P, nullptr);
+  s5_prep<<<P, 128, 0, s>>>(lambda, log_delta, reinterpret_cast<const float2*>(Bt),
+                            reinterpret_cast<const float2*>(Ct), H, P, w);
+  const int M = B * L;
+  dim3 g1((2 * P + kGN - 1) / kGN, (M + kGM - 1) / kGM);
+  gemm_f32<<<g1, 256, 0, s>>>(u, w.bbar, w.xv, M, 2 * P, H, nullptr, nullptr);
+  dim3 gc(P / kPB, NC, B);
+  s5_chunk_state<<<gc, 256, 0, s>>>(w, L, P, NC);
+  s5_carry<<<(B * P + 127) / 128, 128, 0, s>>>(w, B, P, NC);
+  s5_chunk_apply<<<gc, 256, 0, s>>>(w, L, P, NC);
+  dim3 g2((H + kGN - 1) / kGN, (M + kGM - 1) / kGM);
+  gemm_f32<<<g2, 256, 0, s>>>(w.xv, w.cmat, y, M, H, 2 * P, D, u);
+  return cudaGetLastError();
+}
+
+}  // namespace dlr

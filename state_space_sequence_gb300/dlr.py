@@ -1,0 +1,211 @@
+"""Thin Python binding over libdlr.so (include/dlr.h): argument marshalling only.
+
+Every compute step runs in the library's CUDA kernels; this module passes device pointers,
+sizes and the current torch CUDA stream, and turns non-zero status codes into exceptions.
+There is no CPU fallback: if the library cannot be loaded, or a tensor is not a float32 CUDA
+tensor, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+from . import build as _build
+
+DLR_OK, DLR_ERR_INVALID_ARG, DLR_ERR_UNSUPPORTED, DLR_ERR_CUDA, DLR_ERR_TIMEOUT, \
+    DLR_ERR_WORKSPACE = range(6)
+CAST = {"re": 0, "re_im": 1}
+PREC = {"fp32": 0, "bf16": 1}
+
+_lib = None
+
+
+class DLRError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        name = _load().dlr_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{fn} failed: {name}")
+        self.status = status
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        P, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+        lib.dlr_kernel.argtypes = [P, P, P, i64, i64, i64, i32, P, P]
+        lib.dlr_kernel.restype = i32
+        lib.dlr_conv_workspace_size.argtypes = [i64, i64, i32]
+        lib.dlr_conv_workspace_size.restype = sz
+        lib.dlr_conv.argtypes = [P, P, P, i32, i64, i64, i64, P, P, sz, P]
+        lib.dlr_conv.restype = i32
+        lib.dlr_conv_spectrum.argtypes = [P, P, i32, i64, i64, P, sz, P]
+        lib.dlr_conv_spectrum.restype = i32
+        lib.dlr_conv_apply.argtypes = [P, i64, i64, i64, P, P, sz, P]
+        lib.dlr_conv_apply.restype = i32
+        lib.dlr_scan.argtypes = [P, P, P, P, P, P, P, i32, i64, i64, i64, i64, P, P]
+        lib.dlr_scan.restype = i32
+        lib.s5_workspace_size.argtypes = [i64, i64, i64, i64, i32]
+        lib.s5_workspace_size.restype = sz
+        lib.s5_layer.argtypes = [P, P, P, P, P, P, i64, i64, i64, i64, i32, P, P, sz, P]
+        lib.s5_layer.restype = i32
+        lib.dlr_get_device_status.argtypes = [P]
+        lib.dlr_get_device_status.restype = i32
+        lib.dlr_status_string.argtypes = [i32]
+        lib.dlr_status_string.restype = ctypes.c_char_p
+        lib.dlr_abi_version.restype = i32
+        _lib = lib
+    return _lib
+
+
+def library_path() -> str:
+    """Absolute path of the loaded libdlr.so (loads it if needed)."""
+    _load()
+    return os.path.abspath(_build.LIB)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream: Optional[torch.cuda.Stream] = None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_f32(*ts):
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+            raise TypeError("expected contiguous float32 CUDA tensors")
+
+
+def _ok(fn: str, status: int):
+    if status != DLR_OK:
+        raise DLRError(fn, status)
+
+
+def _params(p: Sequence[torch.Tensor]):
+    log_re, log_im, W = p
+    _check_f32(log_re, log_im, W)
+    return log_re, log_im, W
+
+
+def dlr_kernel(log_re, log_im, W, L: int, cast: str = "re", out=None, stream=None):
+    """K[h, j] = Re (or Re*Im) of sum_n W[h,n] lambda[h,n]^j, j < L.  Returns [H, L]."""
+    _check_f32(log_re, log_im, W)
+    H, N = log_re.shape
+    if out is None:
+        out = torch.empty((H, L), dtype=torch.float32, device=log_re.device)
+    _check_f32(out)
+    _ok("dlr_kernel", _load().dlr_kernel(_ptr(log_re), _ptr(log_im), _ptr(W), H, N, L,
+                                         CAST[cast], _ptr(out), _stream(stream)))
+    return out
+
+
+def dlr_conv_workspace_size(H: int, L: int, bidir: bool = False) -> int:
+    return int(_load().dlr_conv_workspace_size(H, L, 1 if bidir else 0))
+
+
+def dlr_conv(u, K_fwd, K_bwd=None, out=None, workspace=None, stream=None):
+    """y = causal (or, with K_bwd, bidirectional) Toeplitz product of u [B, H, L] with K."""
+    _check_f32(u, K_fwd, K_bwd)
+    B, H, L = u.shape
+    if out is None:
+        out = torch.empty_like(u)
+    _check_f32(out)
+    need = dlr_conv_workspace_size(H, L, K_bwd is not None)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=u.device)
+    _ok("dlr_conv", _load().dlr_conv(_ptr(u), _ptr(K_fwd), _ptr(K_bwd),
+                                     1 if K_bwd is not None else 0, B, H, L, _ptr(out),
+                                     _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def dlr_conv_spectrum(K_fwd, K_bwd=None, workspace=None, stream=None):
+    """Prepare the twiddle table and kernel spectra for dlr_conv_apply; returns the workspace."""
+    _check_f32(K_fwd, K_bwd)
+    H, L = K_fwd.shape
+    need = dlr_conv_workspace_size(H, L, K_bwd is not None)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=K_fwd.device)
+    _ok("dlr_conv_spectrum", _load().dlr_conv_spectrum(
+        _ptr(K_fwd), _ptr(K_bwd), 1 if K_bwd is not None else 0, H, L, _ptr(workspace),
+        workspace.numel(), _stream(stream)))
+    return workspace
+
+
+def dlr_conv_apply(u, workspace, out=None, stream=None):
+    """y = FFT convolution of u [B, H, L] with the spectra prepared in ``workspace``."""
+    _check_f32(u)
+    B, H, L = u.shape
+    if out is None:
+        out = torch.empty_like(u)
+    _check_f32(out)
+    _ok("dlr_conv_apply", _load().dlr_conv_apply(_ptr(u), B, H, L, _ptr(out), _ptr(workspace),
+                                                 workspace.numel(), _stream(stream)))
+    return out
+
+
+def dlr_scan(u, fwd, bwd=None, out=None, stream=None):
+    """DLR recurrence (Re cast) as a chunked scan; ``fwd``/``bwd`` = (log_re, log_im, W)."""
+    _check_f32(u)
+    B, H, L = u.shape
+    lr, li, W = _params(fwd)
+    lr2 = li2 = W2 = None
+    if bwd is not None:
+        lr2, li2, W2 = _params(bwd)
+    N = lr.shape[1]
+    if out is None:
+        out = torch.empty_like(u)
+    _check_f32(out)
+    _ok("dlr_scan", _load().dlr_scan(_ptr(u), _ptr(lr), _ptr(li), _ptr(W), _ptr(lr2), _ptr(li2),
+                                     _ptr(W2), 1 if bwd is not None else 0, B, H, N, L,
+                                     _ptr(out), _stream(stream)))
+    return out
+
+
+def s5_workspace_size(B: int, L: int, H: int, P: int, prec: str = "fp32") -> int:
+    return int(_load().s5_workspace_size(B, L, H, P, PREC[prec]))
+
+
+def s5_layer(u, lam, log_delta, Bt, Ct, D, prec: str = "fp32", out=None, workspace=None,
+             stream=None):
+    """S5 SSM outputs for u [B, L, H]; parameters as in include/dlr.h."""
+    _check_f32(u, lam, log_delta, Bt, Ct, D)
+    B, L, H = u.shape
+    P = lam.shape[0]
+    if out is None:
+        out = torch.empty_like(u)
+    _check_f32(out)
+    need = s5_workspace_size(B, L, H, P, prec)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=u.device)
+    _ok("s5_layer", _load().s5_layer(_ptr(u), _ptr(lam), _ptr(log_delta), _ptr(Bt), _ptr(Ct),
+                                     _ptr(D), B, L, H, P, PREC[prec], _ptr(out),
+                                     _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def device_status(stream=None) -> int:
+    """Synchronise and return (then clear) the library's device status word."""
+    return int(_load().dlr_get_device_status(_stream(stream)))
+
+
+def dlr_layer(u, fwd, bwd=None, cast: str = "re", path: str = "fft", workspace=None,
+              stream=None, out=None):
+    """The whole DLR layer u -> y: kernel generation + FFT convolution (path='fft') or the
+    chunked scan (path='scan', Re cast only)."""
+    L = u.shape[-1]
+    if path == "scan":
+        if cast != "re":
+            raise ValueError("the scan path exists only for the Re cast")
+        return dlr_scan(u, fwd, bwd, out=out, stream=stream)
+    K1 = dlr_kernel(*fwd, L, cast, stream=stream)
+    K2 = dlr_kernel(*bwd, L, cast, stream=stream) if bwd is not None else None
+    return dlr_conv(u, K1, K2, out=out, workspace=workspace, stream=stream)

@@ -1,0 +1,93 @@
+"""C-ABI checks that need no GPU: libdlr.so builds, loads, exports every function declared in
+include/dlr.h, and rejects invalid arguments on the host before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from state_space_sequence_gb300 import build as dlr_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dlr.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_\s\*]*?\b([a-z0-9_]+)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while")))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = dlr_build.build()
+    lib = ctypes.CDLL(path)
+    return lib
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ["dlr_kernel", "dlr_conv", "dlr_conv_workspace_size", "dlr_scan", "s5_layer",
+                 "s5_workspace_size", "dlr_get_device_status", "dlr_status_string",
+                 "dlr_abi_version"]:
+        assert must in names, must
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libdlr.so does not export {name}"
+
+
+def test_status_strings_and_version(lib):
+    lib.dlr_status_string.restype = ctypes.c_char_p
+    assert lib.dlr_status_string(0) == b"DLR_OK"
+    assert lib.dlr_status_string(4) == b"DLR_ERR_TIMEOUT"
+    assert lib.dlr_abi_version() == 1
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    P, i64 = ctypes.c_void_p, ctypes.c_int64
+    lib.dlr_kernel.argtypes = [P, P, P, i64, i64, i64, ctypes.c_int, P, P]
+    fake = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    # non-positive sizes
+    assert lib.dlr_kernel(fake, fake, fake, 0, 4, 8, 0, fake, None) == 1
+    assert lib.dlr_kernel(fake, fake, fake, 2, 4, -1, 0, fake, None) == 1
+    # NULL and misaligned pointers
+    assert lib.dlr_kernel(None, fake, fake, 2, 4, 8, 0, fake, None) == 1
+    assert lib.dlr_kernel(ctypes.c_void_p(0x1004), fake, fake, 2, 4, 8, 0, fake, None) == 1
+    # bad cast enum
+    assert lib.dlr_kernel(fake, fake, fake, 2, 4, 8, 7, fake, None) == 1
+    lib.dlr_scan.argtypes = [P] * 7 + [ctypes.c_int, i64, i64, i64, i64, P, P]
+    # N above the scan's limit -> unsupported
+    assert lib.dlr_scan(fake, fake, fake, fake, None, None, None, 0, 1, 1, 129, 8,
+                        ctypes.c_void_p(0x9000), None) == 2
+    # bidirectional without second parameter set
+    assert lib.dlr_scan(fake, fake, fake, fake, None, None, None, 1, 1, 1, 4, 8,
+                        ctypes.c_void_p(0x9000), None) == 1
+    # overlapping u and y
+    assert lib.dlr_scan(fake, fake, fake, fake, None, None, None, 0, 1, 1, 4, 64,
+                        ctypes.c_void_p(0x1010), None) == 1
+    lib.dlr_conv.argtypes = [P, P, P, ctypes.c_int, i64, i64, i64, P, P, ctypes.c_size_t, P]
+    # missing workspace
+    assert lib.dlr_conv(fake, fake, None, 0, 1, 1, 16, ctypes.c_void_p(0x9000), None, 0,
+                        None) == 5
+    # causal call given a backward kernel
+    assert lib.dlr_conv(fake, fake, fake, 0, 1, 1, 16, ctypes.c_void_p(0x9000), fake, 1 << 20,
+                        None) == 1
+    lib.s5_layer.argtypes = [P] * 6 + [i64] * 4 + [ctypes.c_int, P, P, ctypes.c_size_t, P]
+    # H not a multiple of 32
+    assert lib.s5_layer(fake, fake, fake, fake, fake, fake, 1, 16, 48, 32, 0,
+                        ctypes.c_void_p(0x90000), fake, 1 << 30, None) == 2
+
+
+def test_workspace_queries(lib):
+    lib.dlr_conv_workspace_size.restype = ctypes.c_size_t
+    lib.dlr_conv_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int]
+    # L = 4096 -> n = 4096 packed points: twiddles n*8 B + spectra H*(n+1)*8 B
+    assert lib.dlr_conv_workspace_size(256, 4096, 0) == 4096 * 8 + 256 * 4097 * 8
+    assert lib.dlr_conv_workspace_size(0, 4096, 0) == 0
+    lib.s5_workspace_size.restype = ctypes.c_size_t
+    lib.s5_workspace_size.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int]
+    assert lib.s5_workspace_size(8, 16384, 512, 256, 0) >= 8 * 16384 * 512 * 4

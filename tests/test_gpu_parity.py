@@ -1,0 +1,199 @@
+"""Parity of the CUDA path (through the C ABI) with the float64 oracle.
+
+Tolerance: relative L2 error over the whole output tensor <= 1e-5 for the float32 tier
+(the bar the workloads state), computed against the oracle's float64 result on the same
+float32 inputs. Full-size workloads whose oracle is too slow are compared on sampled rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from state_space_sequence_gb300 import dlr, inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-5
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def host(t):
+    torch.cuda.synchronize()
+    return t.detach().cpu().numpy().astype(np.float64)
+
+
+def params_dev(p):
+    return dev(p.log_re), dev(p.log_im), dev(p.W)
+
+
+def params_np(p):
+    return p.log_re, p.log_im, p.W
+
+
+def check_status():
+    assert dlr.device_status() == 0
+
+
+# ------------------------------------------------------------------------------------------
+# dlr_kernel
+
+@pytest.mark.parametrize("H,N,L", [(1, 1, 1), (3, 5, 1000), (2, 16, 256), (4, 64, 4096),
+                                   (2, 33, 4097), (2, 64, 70000)])
+@pytest.mark.parametrize("cast", ["re", "re_im"])
+def test_kernel_matches_oracle(H, N, L, cast):
+    w = inputs.make_dlr(1, H, N, 1, seed=H * 1000 + N, unit_channels=min(1, H))
+    K = host(dlr.dlr_kernel(*params_dev(w.fwd), L, cast))
+    ref = oracle.dlr_kernel(*params_np(w.fwd), L, cast=cast)
+    assert oracle.rel_l2(K, ref) <= TOL
+    check_status()
+
+
+def test_kernel_dft_identity_on_gpu():
+    """(log Lambda)_re = 0, theta_n = 2 pi n / N, L = N: K = N * IDFT(w) (real part)."""
+    N = 64
+    rng = np.random.default_rng(5)
+    log_re = np.zeros((1, N), np.float32)
+    log_im = (2 * np.pi * np.arange(N) / N).astype(np.float32)[None]
+    W = rng.standard_normal((1, N, 2)).astype(np.float32)
+    K = host(dlr.dlr_kernel(dev(log_re), dev(log_im), dev(W), N, "re"))[0]
+    ref = oracle.dlr_kernel(log_re, log_im, W, N, cast="re")[0]
+    assert oracle.rel_l2(K, ref) <= TOL
+    w = W[0, :, 0].astype(np.float64) + 1j * W[0, :, 1]
+    assert oracle.rel_l2(K, (N * np.fft.ifft(w)).real) <= 1e-4  # float32 theta, see pins
+
+
+# ------------------------------------------------------------------------------------------
+# dlr_conv (given kernels) and dlr_scan on small and ragged shapes
+
+@pytest.mark.parametrize("B,H,L", [(1, 1, 1), (1, 1, 2), (2, 3, 3), (1, 2, 5), (2, 2, 64),
+                                   (3, 2, 100), (1, 3, 1000), (2, 2, 4095), (1, 2, 4096),
+                                   (1, 1, 8192), (1, 1, 16383), (1, 2, 16384)])
+@pytest.mark.parametrize("bidir", [False, True])
+def test_conv_matches_oracle_toeplitz(B, H, L, bidir):
+    rng = np.random.default_rng(B * 7 + H * 11 + L)
+    u = rng.standard_normal((B, H, L)).astype(np.float32)
+    K1 = (rng.standard_normal((H, L)) * np.exp(-np.arange(L) / 300.0)).astype(np.float32)
+    K2 = (rng.standard_normal((H, L)) * np.exp(-np.arange(L) / 500.0)).astype(np.float32)
+    y = host(dlr.dlr_conv(dev(u), dev(K1), dev(K2) if bidir else None))
+    ref = oracle.toeplitz_causal(u, K1.astype(np.float64))
+    if bidir:
+        ref = ref + oracle.toeplitz_causal(np.ascontiguousarray(u[..., ::-1]),
+                                           K2.astype(np.float64))[..., ::-1]
+    assert oracle.rel_l2(y, ref) <= TOL
+    check_status()
+
+
+@pytest.mark.parametrize("B,H,N,L", [(1, 1, 1, 1), (1, 1, 1, 7), (2, 3, 5, 63), (1, 2, 16, 64),
+                                     (2, 2, 16, 65), (1, 2, 64, 4095), (1, 2, 64, 4097),
+                                     (2, 1, 65, 1000), (1, 2, 128, 5000), (1, 1, 64, 12289)])
+@pytest.mark.parametrize("bidir", [False, True])
+def test_scan_matches_oracle(B, H, N, L, bidir):
+    w = inputs.make_dlr(B, H, N, L, seed=B + 10 * H + 100 * N + L, bidir=bidir,
+                        unit_channels=1)
+    bwd_d = params_dev(w.bwd) if bidir else None
+    y = host(dlr.dlr_scan(dev(w.u), params_dev(w.fwd), bwd_d))
+    ref = oracle.dlr_layer(w.u, params_np(w.fwd), params_np(w.bwd) if bidir else None)
+    assert oracle.rel_l2(y, ref) <= TOL
+    check_status()
+
+
+@pytest.mark.parametrize("bidir", [False, True])
+def test_fft_and_scan_layers_agree_small(bidir):
+    w = inputs.make_dlr(2, 4, 32, 3000, seed=77, bidir=bidir, unit_channels=1)
+    bwd_d = params_dev(w.bwd) if bidir else None
+    y_fft = host(dlr.dlr_layer(dev(w.u), params_dev(w.fwd), bwd_d, path="fft"))
+    y_scan = host(dlr.dlr_layer(dev(w.u), params_dev(w.fwd), bwd_d, path="scan"))
+    ref = oracle.dlr_layer(w.u, params_np(w.fwd), params_np(w.bwd) if bidir else None)
+    assert oracle.rel_l2(y_fft, ref) <= TOL
+    assert oracle.rel_l2(y_scan, ref) <= TOL
+    assert oracle.rel_l2(y_fft, y_scan) <= TOL
+
+
+# ------------------------------------------------------------------------------------------
+# the named workloads at full size
+
+@pytest.fixture(scope="module")
+def wl_small():
+    return inputs.make_workload("dlr_b1_h1_n16_l256")
+
+
+@pytest.fixture(scope="module")
+def wl_bank():
+    return inputs.make_workload("dlr_b8_h256_n64_l4096")
+
+
+def test_workload_single_channel(wl_small):
+    w = wl_small
+    ref = oracle.dlr_layer(w.u, params_np(w.fwd))
+    for path in ("fft", "scan"):
+        y = host(dlr.dlr_layer(dev(w.u), params_dev(w.fwd), path=path))
+        assert oracle.rel_l2(y, ref) <= TOL, path
+
+
+def test_workload_bank_b8_h256_n64_l4096(wl_bank):
+    w = wl_bank
+    ref = oracle.dlr_layer(w.u, params_np(w.fwd))
+    y_fft = host(dlr.dlr_layer(dev(w.u), params_dev(w.fwd), path="fft"))
+    y_scan = host(dlr.dlr_layer(dev(w.u), params_dev(w.fwd), path="scan"))
+    assert oracle.rel_l2(y_fft, ref) <= TOL
+    assert oracle.rel_l2(y_scan, ref) <= TOL
+    assert oracle.rel_l2(y_fft, y_scan) <= TOL
+    check_status()
+
+
+def test_workload_prod_bidir_sampled_rows():
+    """DLR-prod, bidirectional, B=4 H=128 N=1024 L=16384: the GPU runs the full layer; the
+    oracle (direct O(L^2) Toeplitz sums) checks 3 channels x all 4 batch rows."""
+    w = inputs.make_workload("dlrprod_bidir_b4_h128_n1024_l16384")
+    y = host(dlr.dlr_layer(dev(w.u), params_dev(w.fwd), params_dev(w.bwd), cast="re_im"))
+    hs = [0, 57, 127]
+    sub = lambda p: (p.log_re[hs], p.log_im[hs], p.W[hs])
+    ref = oracle.dlr_prod_layer(np.ascontiguousarray(w.u[:, hs]), sub(w.fwd), sub(w.bwd))
+    assert oracle.rel_l2(y[:, hs], ref) <= TOL
+    assert np.all(np.isfinite(y))
+    check_status()
+
+
+def test_workload_long_unit_circle_scan():
+    """B=1 H=256 N=64 L=65536, 8 channels at |lambda| = 1: chunked scan vs the oracle."""
+    w = inputs.make_workload("dlr_b1_h256_n64_l65536_unit8")
+    y = host(dlr.dlr_layer(dev(w.u), params_dev(w.fwd), path="scan"))
+    ref = oracle.dlr_layer(w.u, params_np(w.fwd))
+    assert oracle.rel_l2(y, ref) <= TOL
+    # the unit-circle channels alone (they dominate the norm, and are the hard case)
+    assert oracle.rel_l2(y[:, :8], ref[:, :8]) <= TOL
+    check_status()
+
+
+# ------------------------------------------------------------------------------------------
+# S5
+
+def s5_dev(p):
+    return dev(p.lam), dev(p.log_delta), dev(p.Bt), dev(p.Ct), dev(p.D)
+
+
+def s5_np(p):
+    return p.lam, p.log_delta, p.Bt, p.Ct, p.D
+
+
+@pytest.mark.parametrize("B,L,H,P", [(1, 1, 32, 32), (2, 63, 32, 32), (1, 200, 64, 32),
+                                     (2, 1000, 96, 64)])
+def test_s5_fp32_matches_oracle(B, L, H, P):
+    w = inputs.make_s5(B, L, H, P, seed=B + L + H + P)
+    y = host(dlr.s5_layer(dev(w.u), *s5_dev(w.params)))
+    ref = oracle.s5_layer(w.u, *s5_np(w.params))
+    assert oracle.rel_l2(y, ref) <= TOL
+    check_status()
+
+
+def test_s5_workload_fp32_sampled_batch_row():
+    """B=8 L=16384 H=512 P=256: the GPU runs the full layer; the oracle checks batch row 5."""
+    w = inputs.make_workload("s5_b8_l16384_h512_p256")
+    y = host(dlr.s5_layer(dev(w.u), *s5_dev(w.params)))
+    ref = oracle.s5_layer(w.u[5:6], *s5_np(w.params))
+    assert oracle.rel_l2(y[5:6], ref) <= TOL
+    assert np.all(np.isfinite(y))
+    check_status()
