@@ -101,6 +101,28 @@ dlr_status dlr_conv_apply(const float* u, int64_t B, int64_t H, int64_t L, float
                           const void* workspace, size_t workspace_bytes, dlr_stream_t stream);
 
 /*
+ * dlr_conv_noalloc -- the same computation as dlr_conv (same kernels, same results), for
+ * callers that cannot allocate device memory: programs whose host application owns every byte
+ * of device memory through a plan fixed at start-up, or code on a latency-critical path where
+ * the device-wide synchronisation a cudaMalloc may cause is not acceptable. The papers have no
+ * counterpart of this entry point; it exists for such deployments only.
+ *  - It allocates nothing (no cudaMalloc, no cudaFree, no allocating library call). Its scratch
+ *    is a fixed 16 MiB array inside the library's device memory, held by every GPU that loads
+ *    the library until the process exits.
+ *  - Limit: the call needs 8*n (rounded up to 256) + 8*H*(n+1) bytes of scratch, n = the next
+ *    power of two >= L; larger requests return DLR_ERR_WORKSPACE and launch nothing (e.g.
+ *    up to H = 510 at L = 4096, up to H = 126 at L = 16384). L <= 16384 as for dlr_conv.
+ *  - The first call on a device looks up the scratch's device address (with that device
+ *    current) and caches it; make that first call before any stream capture.
+ *  - All calls in the process share the one scratch array, which keeps the last call's
+ *    contents; nothing in it needs to start at zero. Calls whose executions overlap on the GPU
+ *    (different streams, or several host threads) race on it: serialise them.
+ * Arguments, layouts and other errors as for dlr_conv.
+ */
+dlr_status dlr_conv_noalloc(const float* u, const float* K_fwd, const float* K_bwd, dlr_dir dir,
+                            int64_t B, int64_t H, int64_t L, float* y, dlr_stream_t stream);
+
+/*
  * dlr_scan -- the DLR as a chunked scan of the recurrence (DLR paper section 2, Eq. 1; S5
  * paper section 2.2, parallel scan over a diagonal state matrix):
  *   x_{n,k} = lambda_n x_{n,k-1} + u_k  (x_{-1} = 0),   y_k = sum_n Re(W_n x_{n,k})
