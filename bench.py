@@ -35,6 +35,7 @@ UNIT = "elements/s"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
 CONV_SOURCES = ["state_space_sequence_gb300/csrc/dlr_conv.cu",
                 "state_space_sequence_gb300/csrc/fft_smem.cuh",
+                "state_space_sequence_gb300/csrc/fft_rows.cuh",
                 "state_space_sequence_gb300/csrc/dlr_common.cuh"]
 
 
@@ -62,6 +63,14 @@ def aggregate(per_rank_seconds, units_per_rank: int):
     """Whole-job throughput: all ranks' units over the slowest rank's time."""
     t = max(per_rank_seconds)
     return units_per_rank * len(per_rank_seconds) / t, t
+
+
+def load_sm_max_mhz() -> float:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            return float(json.load(fh).get("sm_max_mhz", 2070.0))
+    return 2070.0
 
 
 def load_peaks():
@@ -236,12 +245,21 @@ def run_ours(args):
     sampler.stop()
     clocks = sampler.summary() if rank == 0 else None
 
-    # roofline of the dominant kernel (dlr_conv_apply: one launch of the FFT row kernel)
+    # roofline of the dominant kernel (dlr_conv_apply: one launch of the FFT row kernel). It is
+    # bound by FP32 arithmetic, not by HBM: the algorithmic count of a real FFT of size M is
+    # 2.5 M log2 M flops, forward + inverse 5 M log2 M, plus 6 flops per spectral bin.
     n = 1 << max(0, int(np.ceil(np.log2(L))))
+    M = 2 * n
+    apply_flops = B * H * (5 * M * np.log2(M) + 6 * (M // 2 + 1))
     apply_bytes = 4 * B * H * L * 2 + 8 * H * (n + 1)  # u in + y out + spectra read once
     apply_avg = sum(apply_ms) / len(apply_ms) / 1e3
-    peak, peak_kind = load_peaks()
+    peak_gbs, peak_kind = load_peaks()
+    sm_count = props.multi_processor_count
+    sm_mhz = load_sm_max_mhz()
+    peak_tflops = sm_count * 128 * 2 * sm_mhz * 1e6 / 1e12  # FP32 lanes x FMA x clock
+    achieved_tflops = apply_flops / apply_avg / 1e12
     achieved = apply_bytes / apply_avg / 1e9
+    peak = peak_gbs
     traffic = None
     if os.path.exists(PROFILE_TRAFFIC):
         with open(PROFILE_TRAFFIC) as fh:
@@ -273,10 +291,14 @@ def run_ours(args):
         "layer_hbm": {"algorithmic_bytes": layer_bytes,
                       "achieved_gbs": layer_bytes / step_avg / 1e9,
                       "frac_of_measured_peak": layer_bytes / step_avg / 1e9 / peak},
-        "roofline": {"kernel": "conv_rows (dlr_conv_apply)", "bound": "hbm",
-                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
-                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
-                     "algorithmic_bytes": apply_bytes, "avg_launch_us": apply_avg * 1e6},
+        "roofline": {"kernel": "conv_rows (dlr_conv_apply)", "bound": "alu",
+                     "achieved": achieved_tflops, "peak": peak_tflops,
+                     "peak_kind": f"derived: {sm_count} SMs x 128 FP32 lanes x 2 x {sm_mhz:.0f} MHz",
+                     "unit": "TFLOP/s", "frac": achieved_tflops / peak_tflops,
+                     "traffic": traffic, "algorithmic_flops": apply_flops,
+                     "algorithmic_bytes": apply_bytes, "avg_launch_us": apply_avg * 1e6,
+                     "hbm": {"achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+                             "unit": "GB/s", "frac": achieved / peak}},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},

@@ -22,59 +22,47 @@ __device__ __forceinline__ cf cfma(cf a, cf b, cf c) {
   return {fmaf(a.re, b.re, fmaf(-a.im, b.im, c.re)), fmaf(a.re, b.im, fmaf(a.im, b.re, c.im))};
 }
 
-// 2*pi as the unevaluated sum A + B + C of three floats (Cody & Waite's additive argument
-// reduction, "Software Manual for the Elementary Functions", 1980). A = float(2 pi),
-// B = float(2 pi - A), C = float(2 pi - A - B), computed from a 60-digit value of pi.
-constexpr float kTwoPiA = 0x1.921fb6p+2f;
-constexpr float kTwoPiB = -0x1.777a5cp-23f;
-constexpr float kTwoPiC = -0x1.ee59dap-48f;
-constexpr float kInvTwoPi = 0x1.45f306p-3f;
-
-// Reduced angle of j*(th_hi + th_lo) modulo 2 pi, in about [-pi, pi].
-//  - j*th_hi is carried exactly as hi + lo (fmaf gives the rounding error of the product;
-//    j < 2^24 is exact in float).
-//  - k = nearest integer to hi / 2pi (|k| < 2^23 because |th_hi| <= pi + ulp).
-//  - hi - k*A is exact: both are multiples of 2^-21 when |hi| >= 4 (and k is 0 or +-1 below),
-//    and the difference is below 8 in magnitude, so it fits a 24-bit significand. The B and C
-//    terms each add at most half an ulp of a value below 4.
-// The absolute error is about 2^-23 rad, independent of j.
-__device__ __forceinline__ float reduce_phase(float jf, float th_hi, float th_lo) {
-  float hi = jf * th_hi;
-  float lo = fmaf(jf, th_hi, -hi);
-  float k = rintf(hi * kInvTwoPi);
-  float r = fmaf(-k, kTwoPiA, hi);
-  r = fmaf(-k, kTwoPiB, r);
-  r = fmaf(-k, kTwoPiC, r);
-  return r + fmaf(jf, th_lo, lo);
-}
-
-// Per-state parameters prepared once: a2 = (log Lambda)_re^2 and the phase theta reduced to
-// (-pi, pi] and split into float hi + lo (reduction done in double: one per state).
+// Per-state parameters prepared once: a2 = (log Lambda)_re^2 and the phase theta / pi reduced
+// to (-1, 1] and split into float hi + lo (the reduction is done in double: one per state).
 struct lam_param {
   float a2;
-  float th_hi, th_lo;
+  float th_hi, th_lo;  // theta / pi = th_hi + th_lo (mod 2)
 };
 
 __device__ __forceinline__ lam_param make_lam_param(float log_re, float log_im) {
   lam_param p;
   p.a2 = log_re * log_re;
-  double t = (double)log_im;
-  const double two_pi = 6.283185307179586476925286766559;
-  t = t - two_pi * rint(t / two_pi);
+  const double inv_pi = 0.318309886183790671537767526745;
+  double t = (double)log_im * inv_pi;
+  t = t - 2.0 * rint(0.5 * t);
   p.th_hi = (float)t;
   p.th_lo = (float)(t - (double)p.th_hi);
   return p;
 }
 
+// Reduced phase of j * theta in half-turns, in about [-1, 1]:
+//  - j * th_hi is carried exactly as hi + lo (fmaf returns the rounding error of the product;
+//    j < 2^24 is exact in float),
+//  - hi - 2 round(hi / 2) is exact (both are multiples of ulp(hi) and the difference is at
+//    most 1 in magnitude),
+//  - lo and j * th_lo are added last.
+// The absolute error is about 2^-24 half-turns, independent of j.
+__device__ __forceinline__ float reduce_halfturns(float jf, float th_hi, float th_lo) {
+  const float hi = jf * th_hi;
+  const float lo = fmaf(jf, th_hi, -hi);
+  const float r = hi - 2.0f * rintf(0.5f * hi);
+  return r + fmaf(jf, th_lo, lo);
+}
+
 // lambda^j = exp(-j a^2) * (cos(j theta) + i sin(j theta)), j >= 0, evaluated directly from
 // the parameters. Magnitude: the argument j*a2 carries a relative error of one rounding, which
 // changes exp(-x) by x*2^-24 relative -- at most e^-1 * 2^-24 of the largest term. Phase: the
-// reduction above. Uses CUDA's expf / sincosf (compiled without fast-math).
+// reduction above, then CUDA's sincospif (compiled without fast-math).
 __device__ __forceinline__ cf lam_pow(const lam_param& p, int j) {
-  float jf = (float)j;
-  float mag = expf(-jf * p.a2);
+  const float jf = (float)j;
+  const float mag = expf(-jf * p.a2);
   float s, c;
-  sincosf(reduce_phase(jf, p.th_hi, p.th_lo), &s, &c);
+  sincospif(reduce_halfturns(jf, p.th_hi, p.th_lo), &s, &c);
   return {mag * c, mag * s};
 }
 

@@ -14,7 +14,7 @@
 //                    a single pass that unpacks the real spectrum, multiplies by S and re-packs
 //                    for the inverse, one inverse complex FFT, and the first L reals are y.
 // The row never leaves shared memory between its HBM read and its HBM write.
-#include "fft_smem.cuh"
+#include "fft_rows.cuh"
 
 namespace dlr {
 namespace {
@@ -32,13 +32,6 @@ __global__ void twiddle_table(float2* __restrict__ tw, int logn) {
   }
 }
 
-template <int kLog>
-struct Cfg {
-  static constexpr int n = 1 << kLog;
-  static constexpr int threads = (n / 16) < 32 ? 32 : ((n / 16) > 512 ? 512 : n / 16);
-  static constexpr size_t smem = sizeof(float2) * padded_size(n);
-};
-
 // e^{-i pi k / n} (the M-point twiddle used to split the packed spectrum)
 __device__ __forceinline__ cf half_twiddle(int k, int logn) {
   float s, c;
@@ -46,147 +39,263 @@ __device__ __forceinline__ cf half_twiddle(int k, int logn) {
   return {c, -s};
 }
 
+// One CTA per channel h: the real circulant column c (length M = 2n) is read as n packed
+// complex points z_m = c_{2m} + i c_{2m+1} straight into the first pass, transformed, and the
+// Hermitian half S_k, k = 0..n, of its real spectrum is written (scaled, see below).
 template <int kLog>
-__global__ void __launch_bounds__(Cfg<kLog>::threads)
+__global__ void __launch_bounds__(fftr::Plan<kLog>::T)
 conv_spectrum(const float* __restrict__ K1, const float* __restrict__ K2, int L,
               const float2* __restrict__ tw, float2* __restrict__ spec) {
-  constexpr int n = Cfg<kLog>::n;
-  constexpr int T = Cfg<kLog>::threads;
-  extern __shared__ float2 buf[];
-  float* fb = reinterpret_cast<float*>(buf);
+  using P = fftr::Plan<kLog>;
+  constexpr int n = P::n, T = P::T, R0 = P::R0, NB0 = P::NB0;
+  extern __shared__ float2 smem[];
+  float2* cur = smem;
+  float2* nxt = P::kDouble ? smem + P::buf_elems : smem;
   const int h = blockIdx.x;
   const int tid = threadIdx.x;
   const float* k1 = K1 + (size_t)h * L;
   const float* k2 = K2 ? K2 + (size_t)h * L : nullptr;
-  for (int m = tid; m < n; m += T) buf[padded(m)] = make_float2(0.f, 0.f);
-  __syncthreads();
-  // real circulant column c of length M = 2n; c[j] lives at float slot 2*padded(j/2) + j%2
-  for (int j = tid; j < L; j += T) {
-    float v = k1[j];
-    if (j == 0 && k2) v += k2[0];
-    fb[2 * padded(j >> 1) + (j & 1)] = v;
-  }
-  if (k2) {
-    for (int j = 1 + tid; j < L; j += T) {
-      int m = 2 * n - j;
-      fb[2 * padded(m >> 1) + (m & 1)] = k2[j];
+  // circulant column: c_0 = K1_0 (+ K2_0), c_i = K1_i (0 < i < L), c_{2n-i} = K2_i (0 < i < L)
+  auto col = [&](int i) -> float {
+    float v = (i < L) ? k1[i] : 0.f;
+    if (k2) {
+      if (i == 0) v += k2[0];
+      else if (i > 2 * n - L) v += k2[2 * n - i];
+    }
+    return v;
+  };
+  cf a[P::PER0][R0];
+#pragma unroll
+  for (int q = 0; q < P::PER0; ++q) {
+    const int j = tid + q * T;
+    if (NB0 % T == 0 || j < NB0) {
+#pragma unroll
+      for (int r = 0; r < R0; ++r) {
+        const int m = j + r * NB0;
+        a[q][r] = {col(2 * m), col(2 * m + 1)};
+      }
+      fft::dft<R0, false>(a[q]);
     }
   }
+  fftr::pass0_store<kLog>(cur, a);
   __syncthreads();
-  fft::fft<kLog, false, T>(buf, tw);
-  const float scale = 1.0f / (float)(2 * n);
+  int ns = R0;
+#pragma unroll 1
+  for (int p = 0; p < P::n16; ++p) {
+    cf v[P::PER16][16];
+    fftr::pass16_load_compute<kLog, false>(cur, ns, tw, v);
+    if (!P::kDouble) __syncthreads();
+    fftr::pass16_store<kLog>(nxt, ns, v);
+    __syncthreads();
+    float2* t = cur;
+    cur = nxt;
+    nxt = t;
+    ns *= 16;
+  }
+  // 1/M for the inverse transform and 1/2 for the row kernel's unscaled unpack (M = 2n)
+  const float scale = 1.0f / (float)(4 * n);
   float2* out = spec + (size_t)h * (n + 1);
   for (int k = tid; k <= n / 2; k += T) {
-    float2 a = buf[padded(k)], b = buf[padded((n - k) & (n - 1))];
-    cf zk = {a.x, a.y}, zp = {b.x, b.y};
-    cf E = {0.5f * (zk.re + zp.re), 0.5f * (zk.im - zp.im)};
-    cf O = {0.5f * (zk.im + zp.im), -0.5f * (zk.re - zp.re)};  // -i/2 (zk - conj zp)
-    cf wO = cmul(half_twiddle(k, kLog), O);
-    cf Xk = cadd(E, wO);
-    cf Xn = {E.re - wO.re, -(E.im - wO.im)};
+    const float2 fa = cur[padded(k)], fb = cur[padded((n - k) & (n - 1))];
+    const cf E = {0.5f * (fa.x + fb.x), 0.5f * (fa.y - fb.y)};
+    const cf O = {0.5f * (fa.y + fb.y), -0.5f * (fa.x - fb.x)};  // -i/2 (zk - conj zp)
+    const cf wO = cmul(half_twiddle(k, kLog), O);
+    const cf Xk = cadd(E, wO);
+    const cf Xn = {E.re - wO.re, -(E.im - wO.im)};
     out[k] = make_float2(Xk.re * scale, Xk.im * scale);
     out[n - k] = make_float2(Xn.re * scale, Xn.im * scale);
   }
 }
 
 template <int kLog>
-__global__ void __launch_bounds__(Cfg<kLog>::threads)
+__global__ void __launch_bounds__(fftr::Plan<kLog>::T)
 conv_rows(const float* __restrict__ u, const float2* __restrict__ spec,
           const float2* __restrict__ tw, float* __restrict__ y, int H, int L) {
-  constexpr int n = Cfg<kLog>::n;
-  constexpr int T = Cfg<kLog>::threads;
-  extern __shared__ float2 buf[];
-  float* fb = reinterpret_cast<float*>(buf);
+  using P = fftr::Plan<kLog>;
+  constexpr int n = P::n, T = P::T, R0 = P::R0, NB0 = P::NB0;
+  extern __shared__ float2 smem[];
+  float2* cur = smem;
+  float2* nxt = P::kDouble ? smem + P::buf_elems : smem;
   const int row = blockIdx.x;
   const int h = row % H;
   const int tid = threadIdx.x;
   const float* ur = u + (size_t)row * L;
   float* yr = y + (size_t)row * L;
+  const int half = (L + 1) >> 1;  // packed points that hold data
+  const bool even = (L & 1) == 0;
 
-  // 1) load the row as packed complex points, zero padded to n
-  const int half = (L + 1) >> 1;  // packed points holding data
-  if ((L & 3) == 0) {
-    const float4* u4 = reinterpret_cast<const float4*>(ur);
-    for (int i = tid; i < (L >> 2); i += T) {
-      float4 f = __ldg(&u4[i]);
-      buf[padded(2 * i)] = make_float2(f.x, f.y);
-      buf[padded(2 * i + 1)] = make_float2(f.z, f.w);
-    }
-  } else {
-    for (int m = tid; m < half; m += T) {
-      float a = ur[2 * m];
-      float b = (2 * m + 1 < L) ? ur[2 * m + 1] : 0.f;
-      buf[padded(m)] = make_float2(a, b);
+  // ---- forward pass 0 (radix R0, no twiddles): inputs straight from global memory ----
+  cf a[P::PER0][R0];
+#pragma unroll
+  for (int q = 0; q < P::PER0; ++q) {
+    const int j = tid + q * T;
+    if (NB0 % T == 0 || j < NB0) {
+#pragma unroll
+      for (int r = 0; r < R0; ++r) {
+        const int m = j + r * NB0;
+        cf z = {0.f, 0.f};
+        if (m < half) {
+          if (even) {
+            float2 f = __ldg(reinterpret_cast<const float2*>(ur) + m);
+            z = {f.x, f.y};
+          } else {
+            z.re = ur[2 * m];
+            z.im = (2 * m + 1 < L) ? ur[2 * m + 1] : 0.f;
+          }
+        }
+        a[q][r] = z;
+      }
+      // inputs m >= n/2 (r >= R0/2) are the zero padding: L <= n
+      if constexpr (R0 == 16) fft::dft16_lowhalf<false>(a[q]);
+      else fft::dft<R0, false>(a[q]);
     }
   }
-  for (int m = half + tid; m < n; m += T) buf[padded(m)] = make_float2(0.f, 0.f);
+  fftr::pass0_store<kLog>(cur, a);
   __syncthreads();
 
-  // 2) forward FFT of the packed row
-  fft::fft<kLog, false, T>(buf, tw);
+  // ---- forward radix-16 passes ----
+  int ns = R0;
+#pragma unroll 1
+  for (int p = 0; p < P::n16; ++p) {
+    cf v[P::PER16][16];
+    fftr::pass16_load_compute<kLog, false>(cur, ns, tw, v);
+    if (!P::kDouble) __syncthreads();
+    fftr::pass16_store<kLog>(nxt, ns, v);
+    __syncthreads();
+    float2* t = cur;
+    cur = nxt;
+    nxt = t;
+    ns *= 16;
+  }
 
-  // 3) unpack to the real spectrum X, multiply by S, re-pack for the inverse
+  // ---- spectral step: unpack the real spectrum, multiply, re-pack; the results are the
+  // inputs k = j + r n/R0 of the first inverse pass ----
   const float2* S = spec + (size_t)h * (n + 1);
-  for (int k = tid; k <= n / 2; k += T) {
-    const int kp = (n - k) & (n - 1);
-    float2 a = buf[padded(k)], b = buf[padded(kp)];
-    cf zk = {a.x, a.y}, zp = {b.x, b.y};
-    cf E = {0.5f * (zk.re + zp.re), 0.5f * (zk.im - zp.im)};
-    cf O = {0.5f * (zk.im + zp.im), -0.5f * (zk.re - zp.re)};
-    cf w = half_twiddle(k, kLog);
-    cf wO = cmul(w, O);
-    cf Xk = cadd(E, wO);
-    cf Xn = {E.re - wO.re, -(E.im - wO.im)};
-    float2 sk = __ldg(&S[k]), sn = __ldg(&S[n - k]);
-    cf Yk = cmul(Xk, {sk.x, sk.y});
-    cf Yn = cmul(Xn, {sn.x, sn.y});
-    cf Ep = {Yk.re + Yn.re, Yk.im - Yn.im};                       // Yk + conj(Yn)
-    cf Op = cmul({Yk.re - Yn.re, Yk.im + Yn.im}, cconj(w));       // (Yk - conj(Yn)) conj(w)
-    buf[padded(k)] = make_float2(Ep.re - Op.im, Ep.im + Op.re);   // Ep + i Op
-    if (k != 0 && k != kp)
-      buf[padded(kp)] = make_float2(Ep.re + Op.im, -Ep.im + Op.re);  // conj(Ep) + i conj(Op)
+#pragma unroll
+  for (int q = 0; q < P::PER0; ++q) {
+    const int j = tid + q * T;
+    if (NB0 % T == 0 || j < NB0) {
+      cf base = {1.f, 0.f};
+      if constexpr (NB0 % 2 == 0) {
+        float sb, cb;
+        sincospif(ldexpf((float)j, -kLog), &sb, &cb);
+        base = {cb, -sb};  // e^{-i pi j / n}
+      }
+#pragma unroll
+      for (int r = 0; r < R0; ++r) {
+        const int k = j + r * NB0;
+        const int kp = (n - k) & (n - 1);
+        cf w;
+        if constexpr (R0 == 16 && NB0 % 2 == 0) {
+          w = cmul(base, fftr::half16(r));     // e^{-i pi r / 16}
+        } else if constexpr (NB0 % 2 == 0) {
+          float2 c = __ldg(&tw[r * (NB0 / 2)]);  // e^{-i pi r / R0}
+          w = cmul(base, {c.x, c.y});
+        } else {
+          float sw, cw;
+          sincospif(ldexpf((float)k, -kLog), &sw, &cw);
+          w = {cw, -sw};
+        }
+        float2 fa = cur[padded(k)], fb = cur[padded(kp)];
+        // 2E = Zk + conj(Zp), 2O = -i (Zk - conj(Zp)); the 1/2 lives in the spectrum
+        cf E = {fa.x + fb.x, fa.y - fb.y};
+        cf O = {fa.y + fb.y, fb.x - fa.x};
+        cf wO = cmul(w, O);
+        cf X = cadd(E, wO);
+        cf Xn = {E.re - wO.re, wO.im - E.im};
+        float2 sk = __ldg(&S[k]), sn = __ldg(&S[n - k]);
+        cf Yk = cmul(X, {sk.x, sk.y});
+        cf Yn = cmul(Xn, {sn.x, sn.y});
+        cf Ep = {Yk.re + Yn.re, Yk.im - Yn.im};
+        cf Op = cmul({Yk.re - Yn.re, Yk.im + Yn.im}, cconj(w));
+        a[q][r] = {Ep.re - Op.im, Ep.im + Op.re};
+      }
+      fft::dft<R0, true>(a[q]);
+    }
   }
+  if (!P::kDouble) __syncthreads();
+  fftr::pass0_store<kLog>(nxt, a);
   __syncthreads();
+  {
+    float2* t = cur;
+    cur = nxt;
+    nxt = t;
+  }
+  ns = R0;
 
-  // 4) inverse FFT; z'_m = y_{2m} + i y_{2m+1}
-  fft::fft<kLog, true, T>(buf, tw);
-
-  // 5) store the first L reals
-  if ((L & 3) == 0) {
-    float4* y4 = reinterpret_cast<float4*>(yr);
-    for (int i = tid; i < (L >> 2); i += T) {
-      float2 a = buf[padded(2 * i)], b = buf[padded(2 * i + 1)];
-      y4[i] = make_float4(a.x, a.y, b.x, b.y);
+  // ---- inverse radix-16 passes; the last one writes y ----
+  if constexpr (P::n16 == 0) {
+    for (int m = tid; m < half; m += T) {
+      float2 z = cur[padded(m)];
+      if (even) {
+        reinterpret_cast<float2*>(yr)[m] = z;
+      } else {
+        yr[2 * m] = z.x;
+        if (2 * m + 1 < L) yr[2 * m + 1] = z.y;
+      }
     }
   } else {
-    for (int j = tid; j < L; j += T) yr[j] = fb[2 * padded(j >> 1) + (j & 1)];
+#pragma unroll 1
+    for (int p = 0; p < P::n16; ++p) {
+      cf v[P::PER16][16];
+      fftr::pass16_load_compute<kLog, true>(cur, ns, tw, v);
+      if (p < P::n16 - 1) {
+        if (!P::kDouble) __syncthreads();
+        fftr::pass16_store<kLog>(nxt, ns, v);
+        __syncthreads();
+        float2* t = cur;
+        cur = nxt;
+        nxt = t;
+        ns *= 16;
+      } else {
+        // last pass: thread j holds outputs j + r n/16 (ns = n/16, so k = j)
+#pragma unroll
+        for (int q = 0; q < P::PER16; ++q) {
+          const int j = tid + q * T;
+          if (P::NB16 % T == 0 || j < P::NB16) {
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+              const int m = j + r * P::NB16;
+              if (m < half) {
+                if (even) {
+                  reinterpret_cast<float2*>(yr)[m] = make_float2(v[q][r].re, v[q][r].im);
+                } else {
+                  yr[2 * m] = v[q][r].re;
+                  if (2 * m + 1 < L) yr[2 * m + 1] = v[q][r].im;
+                }
+              }
+            }
+          }
+        }
+      }
+    }
   }
 }
 
 template <int kLog>
 cudaError_t launch_spectrum(const float* K1, const float* K2, int H, int L, float2* tw,
                             float2* spec, cudaStream_t s) {
-  using C = Cfg<kLog>;
-  if (C::smem > 48 * 1024) {
+  using P = fftr::Plan<kLog>;
+  if (P::smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(conv_spectrum<kLog>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P::smem);
     if (e != cudaSuccess) return e;
   }
-  twiddle_table<<<(C::n + 255) / 256, 256, 0, s>>>(tw, kLog);
-  conv_spectrum<kLog><<<H, C::threads, C::smem, s>>>(K1, K2, L, tw, spec);
+  twiddle_table<<<(P::n + 255) / 256, 256, 0, s>>>(tw, kLog);
+  conv_spectrum<kLog><<<H, P::T, P::smem, s>>>(K1, K2, L, tw, spec);
   return cudaGetLastError();
 }
 
 template <int kLog>
 cudaError_t launch_apply(const float* u, int B, int H, int L, float* y, const float2* tw,
                          const float2* spec, cudaStream_t s) {
-  using C = Cfg<kLog>;
-  if (C::smem > 48 * 1024) {
+  using P = fftr::Plan<kLog>;
+  if (P::smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(conv_rows<kLog>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::smem);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P::smem);
     if (e != cudaSuccess) return e;
   }
-  conv_rows<kLog><<<(unsigned)((size_t)B * H), C::threads, C::smem, s>>>(u, spec, tw, y, H, L);
+  conv_rows<kLog><<<(unsigned)((size_t)B * H), P::T, P::smem, s>>>(u, spec, tw, y, H, L);
   return cudaGetLastError();
 }
 

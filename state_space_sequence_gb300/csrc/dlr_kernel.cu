@@ -2,37 +2,53 @@
 // Re K or Re K * Im K ("Simplifying and Understanding State Space Models with Diagonal Linear
 // RNNs", section 2, Eq. 3/4; section 2.1 for the DLR-prod cast; section 2.2 for lambda).
 //
-// Chunked powers: write j = j0 + c*T + t (T = 64, c < 64 chunks per CTA, t < T). Then
-//   K_{j} = sum_n (W_n lambda_n^{j0 + cT}) * lambda_n^{t}  =  sum_n A[c][n] * Bm[n][t],
-// a complex [64 x N] x [N x 64] product per CTA tile, done as an FFMA register-tiled GEMM out
-// of shared memory. Both factors come from a few directly evaluated powers per state:
-//   lambda^t      = lambda^{t mod 8} * lambda^{8 floor(t/8)}            (8 + 8 evaluations)
-//   lambda^{j0+cT} = lambda^{T (c mod 8)} * lambda^{j0 + 8T floor(c/8)}  (8 + 8 evaluations)
-// so every term of the sum is a product of at most four correctly rounded-ish factors: its
-// relative error stays a few ulp regardless of j (no j-long multiplication chain).
+// Chunked powers: write j = j0 + c*T + t (T = 64 lags, c < 32 chunks per CTA). Then
+//   K_j = sum_n (W_n lambda_n^{j0 + cT}) * lambda_n^t = sum_n A[c][n] * Bm[n][t],
+// a complex [32 x N] x [N x 64] product per CTA, done as an FFMA register-tiled GEMM out of
+// shared memory (4 chunks x 4 lags per thread).
+// The factors come from five directly evaluated powers per state -- lambda, lambda^8,
+// lambda^64, lambda^512 and W lambda^{j0} -- combined by short product trees:
+//   lambda^t       = lambda^{t mod 8} * (lambda^8)^{floor(t/8)}
+//   lambda^{j0+cT} = (lambda^64)^{c mod 8} * W lambda^{j0} (lambda^512)^{floor(c/8)}
+// with every small power built from at most three multiplications, so each term of the sum
+// is within ~12 roundings of exact, whatever j is (never a j-long multiplication chain).
 #include "dlr_common.cuh"
 
 namespace dlr {
 namespace {
 
-constexpr int kT = 64;        // lags per chunk (t)
-constexpr int kC = 64;        // chunks per CTA (c)
-constexpr int kNB = 32;       // states per shared-memory block
-constexpr int kThreads = 256;  // 16 (t groups of 4) x 16 (c groups of 4)
+constexpr int kT = 64;         // lags per chunk (t)
+constexpr int kC = 32;         // chunks per CTA (c)
+constexpr int kNB = 32;        // states per shared-memory block
+constexpr int kThreads = 128;  // 16 (t groups of 4) x 8 (c groups of 4)
+
+// p[e] = x^e for e < 8 from p[1] = x, at most three multiplications deep
+__device__ __forceinline__ void small_powers(cf (&p)[8], cf x) {
+  p[0] = {1.f, 0.f};
+  p[1] = x;
+  p[2] = cmul(x, x);
+  p[3] = cmul(p[2], x);
+  p[4] = cmul(p[2], p[2]);
+  p[5] = cmul(p[4], x);
+  p[6] = cmul(p[4], p[2]);
+  p[7] = cmul(p[4], p[3]);
+}
 
 template <bool kReIm>
 __global__ void __launch_bounds__(kThreads)
 dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_im,
                const float2* __restrict__ W, int N, int L, float* __restrict__ K) {
-  __shared__ float2 sA[kC][kNB + 1];  // A[c][n]
+  __shared__ float2 sA[kC][kNB + 1];            // A[c][n]
   __shared__ __align__(16) float2 sB[kNB][kT];  // Bm[n][t]
-  __shared__ float2 sP0[kNB][8], sP1[kNB][8], sQ0[kNB][8], sQ1[kNB][8];
+  __shared__ float2 sE[kNB][5];                 // lambda, lambda^8, lambda^64, lambda^512, W lambda^j0
+  __shared__ float2 sPw[4][kNB][9];             // small powers: lambda^t0, lambda^{8 t1}, lambda^{64 c0},
+                                                // W lambda^{j0 + 512 c1}; odd row stride
 
   const int h = blockIdx.y;
   const int j0 = blockIdx.x * (kT * kC);
   const int tid = threadIdx.x;
-  const int tx = tid & 15;   // t = 4*tx + {0..3}
-  const int ty = tid >> 4;   // c = 4*ty + {0..3}
+  const int tx = tid & 15;  // t in {2 tx, 2 tx + 1, 32 + 2 tx, 33 + 2 tx}
+  const int ty = tid >> 4;  // c = ty + 8 i, i < 4
 
   float acc_re[4][4], acc_im[4][4];
 #pragma unroll
@@ -41,52 +57,68 @@ dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_i
     for (int k = 0; k < 4; ++k) acc_re[i][k] = acc_im[i][k] = 0.f;
 
   for (int nb = 0; nb < N; nb += kNB) {
-    // 1) anchor powers: 32 states x 32 values = 1024 evaluations, 4 per thread
-    for (int e = tid; e < kNB * 32; e += kThreads) {
-      int nl = e >> 5, which = (e >> 3) & 3, idx = e & 7;
-      int n = nb + nl;
+    // 1) five direct evaluations per state
+    for (int e = tid; e < kNB * 5; e += kThreads) {
+      const int nl = e / 5, which = e % 5, n = nb + nl;
       cf v = {0.f, 0.f};
       if (n < N) {
-        lam_param p = make_lam_param(log_re[(size_t)h * N + n], log_im[(size_t)h * N + n]);
-        if (which == 0) v = lam_pow(p, idx);                      // lambda^{t0}
-        else if (which == 1) v = lam_pow(p, 8 * idx);             // lambda^{8 t1}
-        else if (which == 2) v = lam_pow(p, kT * idx);            // lambda^{T c0}
-        else {                                                    // W lambda^{j0 + 8T c1}
-          float2 w = W[(size_t)h * N + n];
-          v = cmul({w.x, w.y}, lam_pow(p, j0 + 8 * kT * idx));
+        const lam_param p = make_lam_param(log_re[(size_t)h * N + n], log_im[(size_t)h * N + n]);
+        if (which < 4) {
+          v = lam_pow(p, which == 0 ? 1 : (which == 1 ? 8 : (which == 2 ? 64 : 512)));
+        } else {
+          const float2 w = W[(size_t)h * N + n];
+          v = cmul({w.x, w.y}, lam_pow(p, j0));
         }
       }
-      float2 f = make_float2(v.re, v.im);
-      if (which == 0) sP0[nl][idx] = f;
-      else if (which == 1) sP1[nl][idx] = f;
-      else if (which == 2) sQ0[nl][idx] = f;
-      else sQ1[nl][idx] = f;
+      sE[nl][which] = make_float2(v.re, v.im);
     }
     __syncthreads();
-    // 2) expand: Bm[n][t] (2048 entries) and A[c][n] (2048 entries)
+    // 2) small powers, one table per thread: (state nl, table part)
+    {
+      const int nl = tid >> 2, part = tid & 3;
+      cf p[8];
+      if (part < 3) {
+        const float2 e = sE[nl][part];  // lambda, lambda^8, lambda^64
+        small_powers(p, {e.x, e.y});
+      } else {
+        const float2 ew = sE[nl][4], e5 = sE[nl][3];
+        const cf s512 = {e5.x, e5.y};
+        p[0] = {ew.x, ew.y};
+        p[1] = cmul(p[0], s512);
+        const cf s2 = cmul(s512, s512);
+        p[2] = cmul(p[0], s2);
+        p[3] = cmul(p[1], s2);
+#pragma unroll
+        for (int i = 4; i < 8; ++i) p[i] = {0.f, 0.f};
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sPw[part][nl][i] = make_float2(p[i].re, p[i].im);
+    }
+    __syncthreads();
+    // 3) expand (consecutive threads write consecutive entries)
     for (int e = tid; e < kNB * kT; e += kThreads) {
-      int nl = e / kT, t = e % kT;
-      float2 a = sP0[nl][t & 7], b = sP1[nl][t >> 3];
-      cf v = cmul({a.x, a.y}, {b.x, b.y});
+      const int nl = e >> 6, t = e & 63;
+      const float2 a = sPw[0][nl][t & 7], b = sPw[1][nl][t >> 3];
+      const cf v = cmul({a.x, a.y}, {b.x, b.y});
       sB[nl][t] = make_float2(v.re, v.im);
     }
     for (int e = tid; e < kNB * kC; e += kThreads) {
-      int c = e / kNB, nl = e % kNB;
-      float2 a = sQ0[nl][c & 7], b = sQ1[nl][c >> 3];
-      cf v = cmul({a.x, a.y}, {b.x, b.y});
+      const int c = e >> 5, nl = e & 31;
+      const float2 a = sPw[2][nl][c & 7], b = sPw[3][nl][c >> 3];
+      const cf v = cmul({a.x, a.y}, {b.x, b.y});
       sA[c][nl] = make_float2(v.re, v.im);
     }
     __syncthreads();
-    // 3) register-tiled complex GEMM over this block of states
-    const int nmax = min(kNB, N - nb);
-    for (int nl = 0; nl < nmax; ++nl) {
+    // 4) register-tiled complex GEMM over this block of states (missing states are zero)
+#pragma unroll 4
+    for (int nl = 0; nl < kNB; ++nl) {
       float2 a[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = sA[4 * ty + i][nl];
-      const float4* brow = reinterpret_cast<const float4*>(&sB[nl][4 * tx]);
-      float4 b01 = brow[0], b23 = brow[1];
-      float2 b[4] = {make_float2(b01.x, b01.y), make_float2(b01.z, b01.w),
-                     make_float2(b23.x, b23.y), make_float2(b23.z, b23.w)};
+      for (int i = 0; i < 4; ++i) a[i] = sA[ty + 8 * i][nl];
+      const float4 b01 = *reinterpret_cast<const float4*>(&sB[nl][2 * tx]);
+      const float4 b23 = *reinterpret_cast<const float4*>(&sB[nl][32 + 2 * tx]);
+      const float2 b[4] = {make_float2(b01.x, b01.y), make_float2(b01.z, b01.w),
+                           make_float2(b23.x, b23.y), make_float2(b23.z, b23.w)};
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -98,21 +130,24 @@ dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_i
     __syncthreads();
   }
 
-  // 4) store: row h, j = j0 + c*T + t
+  // 5) store: row h, j = j0 + c T + t for t in {2 tx, 2 tx + 1} and {32 + 2 tx, 33 + 2 tx}
   float* krow = K + (size_t)h * L;
-  const bool vec = ((L & 3) == 0);
+  const bool vec = ((L & 1) == 0);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    int j = j0 + (4 * ty + i) * kT + 4 * tx;
+    const int jc = j0 + (ty + 8 * i) * kT;
     float v[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) v[k] = kReIm ? acc_re[i][k] * acc_im[i][k] : acc_re[i][k];
-    if (vec && j + 3 < L) {
-      *reinterpret_cast<float4*>(krow + j) = make_float4(v[0], v[1], v[2], v[3]);
-    } else {
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (j + k < L) krow[j + k] = v[k];
+    for (int half = 0; half < 2; ++half) {
+      const int j = jc + 32 * half + 2 * tx;
+      if (vec && j + 1 < L) {
+        *reinterpret_cast<float2*>(krow + j) = make_float2(v[2 * half], v[2 * half + 1]);
+      } else {
+        if (j < L) krow[j] = v[2 * half];
+        if (j + 1 < L) krow[j + 1] = v[2 * half + 1];
+      }
     }
   }
 }

@@ -65,10 +65,18 @@ dlr_scan_rows(const float* __restrict__ u, const float* __restrict__ log_re,
   float* yr = y + (size_t)row * L;
 
   // ---- per-channel tables (states n >= N are zero) ----
+  // per-state parameters first (one double-precision phase reduction per state), parked in
+  // the u-segment buffer, which is not in use yet
+  lam_param* sPar = reinterpret_cast<lam_param*>(sU);
+  static_assert(sizeof(lam_param) * NMAX <= sizeof(float) * kCS * (kT + 1), "parameter scratch");
+  for (int n = tid; n < NMAX; n += kThreads)
+    sPar[n] = (n < N) ? make_lam_param(log_re[(size_t)h * N + n], log_im[(size_t)h * N + n])
+                      : lam_param{0.f, 0.f, 0.f};
+  __syncthreads();
   for (int e = tid; e < NMAX * PS; e += kThreads) {
     int n = e / PS, t = e % PS;
     cf v = {0.f, 0.f};
-    if (n < N) v = lam_pow(make_lam_param(log_re[(size_t)h * N + n], log_im[(size_t)h * N + n]), t);
+    if (n < N) v = lam_pow(sPar[n], t);
     sP[e] = make_float2(v.re, v.im);
   }
   for (int e = tid; e < NMAX * 8; e += kThreads) {
@@ -76,7 +84,7 @@ dlr_scan_rows(const float* __restrict__ u, const float* __restrict__ log_re,
     cf v = {0.f, 0.f};
     if (n < N) {
       if (k < 7) {
-        v = lam_pow(make_lam_param(log_re[(size_t)h * N + n], log_im[(size_t)h * N + n]), kT << k);
+        v = lam_pow(sPar[n], kT << k);
       } else {
         float2 w = W[(size_t)h * N + n];
         v = {w.x, w.y};

@@ -133,6 +133,41 @@ __device__ __forceinline__ void dft<16, false>(cf (&v)[16]) { dft16_impl<false>(
 template <>
 __device__ __forceinline__ void dft<16, true>(cf (&v)[16]) { dft16_impl<true>(v); }
 
+// DFT of size 16 whose inputs 8..15 are zero (the zero-padded half of a row): the first
+// stage's DFT4s see (x_r, x_{r+4}, 0, 0).
+template <bool kInv>
+__device__ __forceinline__ void dft16_lowhalf(cf (&v)[16]) {
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const cf a = v[r], b = v[r + 4], rb = rot90<kInv>(v[r + 4]);
+    v[r] = cadd(a, b);
+    v[r + 8] = {a.re - b.re, a.im - b.im};
+    v[r + 4] = cadd(a, rb);
+    v[r + 12] = {a.re - rb.re, a.im - rb.im};
+  }
+  v[5] = w16<kInv, 1>(v[5]);
+  v[6] = w16<kInv, 2>(v[6]);
+  v[7] = w16<kInv, 3>(v[7]);
+  v[9] = w16<kInv, 2>(v[9]);
+  v[10] = rot90<kInv>(v[10]);
+  v[11] = rot90<kInv>(w16<kInv, 2>(v[11]));
+  v[13] = w16<kInv, 3>(v[13]);
+  v[14] = rot90<kInv>(w16<kInv, 2>(v[14]));
+  {
+    cf t = w16<kInv, 1>(v[15]);
+    v[15] = {-t.re, -t.im};
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) dft4<kInv>(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  cf o[16];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int s = 0; s < 4; ++s) o[q + 4 * s] = v[4 * q + s];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = o[i];
+}
+
 // One Stockham pass of radix R over n = 2^kLog points with kThreads threads.
 // tw[m] = exp(-2 pi i m / n), m < n.
 template <int kLog, int R, bool kInv, int kThreads>
