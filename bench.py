@@ -368,6 +368,15 @@ def run_extras(torch, dlr, inputs, flush):
     y = torch.empty_like(u)
     ms = _time_steps(torch, lambda: dlr.s5_layer(u, *args5, workspace=ws, out=y), 5, 2, flush)
     out["s5_fp32_" + w.name] = {"ms": ms, "elements_per_s": w.B * w.L * w.H / ms * 1e3}
+    del ws
+    ws = torch.empty(dlr.s5_workspace_size(w.B, w.L, w.H, w.P, "bf16"), dtype=torch.uint8,
+                     device="cuda")
+    ms = _time_steps(torch, lambda: dlr.s5_layer(u, *args5, prec="bf16", workspace=ws, out=y),
+                     10, 3, flush)
+    # two projections of 2 * (B L) * H * 2P flops each
+    gemm_flops = 2 * 2 * w.B * w.L * w.H * 2 * w.P
+    out["s5_bf16_tc_" + w.name] = {"ms": ms, "elements_per_s": w.B * w.L * w.H / ms * 1e3,
+                                   "projection_tflops": gemm_flops / ms / 1e9}
     return out
 
 

@@ -16,10 +16,10 @@ cudaError_t launch_dlr_conv_apply(const float* u, int B, int H, int L, float* y,
 cudaError_t launch_dlr_scan(const float* u, const float* lr, const float* li, const float* W,
                             const float* lr2, const float* li2, const float* W2, bool bidir,
                             int B, int H, int N, int L, float* y, cudaStream_t s);
-size_t s5_workspace_bytes(int64_t B, int64_t L, int64_t H, int64_t P);
-cudaError_t launch_s5_fp32(const float* u, const float* lambda, const float* log_delta,
-                           const float* Bt, const float* Ct, const float* D, int B, int L, int H,
-                           int P, float* y, void* ws, cudaStream_t s);
+size_t s5_workspace_bytes(int64_t B, int64_t L, int64_t H, int64_t P, bool bf16);
+cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delta,
+                      const float* Bt, const float* Ct, const float* D, int B, int L, int H, int P,
+                      bool bf16, float* y, void* ws, int* status, cudaStream_t s);
 }  // namespace dlr
 
 // The library's device status word (one per device that loads the library).
@@ -29,6 +29,13 @@ namespace {
 
 constexpr int64_t kMaxL = (int64_t(1) << 24) - 1;
 constexpr int64_t kMaxGrid = 2147483647;
+
+// Device address of the status word on the current device (kernels with bounded waits write it).
+int* status_word() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_dlr_device_status) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -157,8 +164,7 @@ dlr_status dlr_scan(const float* u, const float* log_re, const float* log_im, co
 
 size_t s5_workspace_size(int64_t B, int64_t L, int64_t H, int64_t P, dlr_prec prec) {
   if (B < 1 || L < 1 || H < 1 || P < 1) return 0;
-  (void)prec;
-  return dlr::s5_workspace_bytes(B, L, H, P);
+  return dlr::s5_workspace_bytes(B, L, H, P, prec == DLR_BF16_TC);
 }
 
 dlr_status s5_layer(const float* u, const float* lambda, const float* log_delta,
@@ -174,11 +180,13 @@ dlr_status s5_layer(const float* u, const float* lambda, const float* log_delta,
   if (ranges_overlap(u, bytes, y, bytes)) return DLR_ERR_INVALID_ARG;
   if (H % 32 || P % 32 || H > 1024 || P > 1024) return DLR_ERR_UNSUPPORTED;
   if (B > 65535 || (L + 63) / 64 > 65535 || B * L > kMaxGrid / 4) return DLR_ERR_UNSUPPORTED;
-  if (prec == DLR_BF16_TC) return DLR_ERR_UNSUPPORTED;
-  const size_t need = dlr::s5_workspace_bytes(B, L, H, P);
+  const bool bf16 = prec == DLR_BF16_TC;
+  const size_t need = dlr::s5_workspace_bytes(B, L, H, P, bf16);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DLR_ERR_WORKSPACE;
-  return from_cuda(dlr::launch_s5_fp32(u, lambda, log_delta, Bt, Ct, D, (int)B, (int)L, (int)H,
-                                       (int)P, y, workspace, (cudaStream_t)stream));
+  int* status = bf16 ? status_word() : nullptr;
+  if (bf16 && !status) return DLR_ERR_CUDA;
+  return from_cuda(dlr::launch_s5(u, lambda, log_delta, Bt, Ct, D, (int)B, (int)L, (int)H,
+                                  (int)P, bf16, y, workspace, status, (cudaStream_t)stream));
 }
 
 dlr_status dlr_get_device_status(dlr_stream_t stream) {

@@ -23,6 +23,10 @@ constexpr int kT = 64;   // steps per chunk
 constexpr int kPB = 32;  // complex states per chunk-kernel CTA
 
 struct S5Work {
+  void* bbar_t16;  // bf16 [2P][H]   (bf16 tier only)
+  void* cmat_t16;  // bf16 [H][2P]
+  void* u16;       // bf16 [B*L][H]
+  void* x16;       // bf16 [B*L][2P]
   float* bbar;     // [H][2P]
   float* cmat;     // [2P][H]
   float2* lbar_pw; // [P][T+1]  Lbar^t
@@ -205,7 +209,7 @@ s5_chunk_apply(S5Work w, int L, int P, int NC) {
   }
 }
 
-S5Work carve(void* ws, int64_t B, int64_t L, int64_t H, int64_t P, size_t* total) {
+S5Work carve(void* ws, int64_t B, int64_t L, int64_t H, int64_t P, bool bf16, size_t* total) {
   const int64_t NC = (L + kT - 1) / kT;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -220,6 +224,13 @@ S5Work carve(void* ws, int64_t B, int64_t L, int64_t H, int64_t P, size_t* total
   size_t o_S = take(sizeof(float2) * B * NC * P);
   size_t o_X = take(sizeof(float2) * B * NC * P);
   size_t o_xv = take(sizeof(float) * B * L * 2 * P);
+  size_t o_b16 = 0, o_c16 = 0, o_u16 = 0, o_x16 = 0;
+  if (bf16) {
+    o_b16 = take(2 * 2 * P * H);
+    o_c16 = take(2 * H * 2 * P);
+    o_u16 = take(2 * B * L * H);
+    o_x16 = take(2 * B * L * 2 * P);
+  }
   if (total) *total = off;
   char* base = reinterpret_cast<char*>(ws);
   S5Work w;
@@ -230,34 +241,63 @@ S5Work carve(void* ws, int64_t B, int64_t L, int64_t H, int64_t P, size_t* total
   w.S = reinterpret_cast<float2*>(base + o_S);
   w.Xin = reinterpret_cast<float2*>(base + o_X);
   w.xv = reinterpret_cast<float*>(base + o_xv);
+  w.bbar_t16 = bf16 ? base + o_b16 : nullptr;
+  w.cmat_t16 = bf16 ? base + o_c16 : nullptr;
+  w.u16 = bf16 ? base + o_u16 : nullptr;
+  w.x16 = bf16 ? base + o_x16 : nullptr;
   return w;
 }
 
 }  // namespace
 
-size_t s5_workspace_bytes(int64_t B, int64_t L, int64_t H, int64_t P) {
+size_t s5_workspace_bytes(int64_t B, int64_t L, int64_t H, int64_t P, bool bf16) {
   size_t total = 0;
-  carve(nullptr, B, L, H, P, &total);
+  carve(nullptr, B, L, H, P, bf16, &total);
   return total;
 }
 
-cudaError_t launch_s5_fp32(const float* u, const float* lambda, const float* log_delta,
-                           const float* Bt, const float* Ct, const float* D, int B, int L, int H,
-                           int P, float* y, void* ws, cudaStream_t s) {
+cudaError_t launch_to_bf16(const float* x, void* y, size_t n, cudaStream_t s);
+cudaError_t launch_to_bf16_t(const float* x, void* y, int R, int C, cudaStream_t s);
+cudaError_t launch_tc_gemm(const void* A, const void* B, float* C, int M, int N, int K,
+                           const float* D, const float* E, int* status, cudaStream_t s);
+
+// The chunked diagonal scan shared by both tiers: V (in w.xv) -> x (in w.xv), in place.
+static cudaError_t s5_scan_xv(const S5Work& w, int B, int L, int P, cudaStream_t s) {
   const int NC = (L + kT - 1) / kT;
-  S5Work w = carve(ws, B, L, H, P, nullptr);
-  s5_prep<<<P, 128, 0, s>>>(lambda, log_delta, reinterpret_cast<const float2*>(Bt),
-                            reinterpret_cast<const float2*>(Ct), H, P, w);
-  const int M = B * L;
-  dim3 g1((2 * P + kGN - 1) / kGN, (M + kGM - 1) / kGM);
-  gemm_f32<<<g1, 256, 0, s>>>(u, w.bbar, w.xv, M, 2 * P, H, nullptr, nullptr);
   dim3 gc(P / kPB, NC, B);
   s5_chunk_state<<<gc, 256, 0, s>>>(w, L, P, NC);
   s5_carry<<<(B * P + 127) / 128, 128, 0, s>>>(w, B, P, NC);
   s5_chunk_apply<<<gc, 256, 0, s>>>(w, L, P, NC);
-  dim3 g2((H + kGN - 1) / kGN, (M + kGM - 1) / kGM);
-  gemm_f32<<<g2, 256, 0, s>>>(w.xv, w.cmat, y, M, H, 2 * P, D, u);
   return cudaGetLastError();
+}
+
+cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delta,
+                      const float* Bt, const float* Ct, const float* D, int B, int L, int H, int P,
+                      bool bf16, float* y, void* ws, int* status, cudaStream_t s) {
+  S5Work w = carve(ws, B, L, H, P, bf16, nullptr);
+  s5_prep<<<P, 128, 0, s>>>(lambda, log_delta, reinterpret_cast<const float2*>(Bt),
+                            reinterpret_cast<const float2*>(Ct), H, P, w);
+  const int M = B * L;
+  cudaError_t e;
+  if (!bf16) {
+    dim3 g1((2 * P + kGN - 1) / kGN, (M + kGM - 1) / kGM);
+    gemm_f32<<<g1, 256, 0, s>>>(u, w.bbar, w.xv, M, 2 * P, H, nullptr, nullptr);
+    e = s5_scan_xv(w, B, L, P, s);
+    if (e != cudaSuccess) return e;
+    dim3 g2((H + kGN - 1) / kGN, (M + kGM - 1) / kGM);
+    gemm_f32<<<g2, 256, 0, s>>>(w.xv, w.cmat, y, M, H, 2 * P, D, u);
+    return cudaGetLastError();
+  }
+  // bf16 operands on the tensor cores, f32 accumulation; the scan stays f32
+  if ((e = launch_to_bf16_t(w.bbar, w.bbar_t16, H, 2 * P, s)) != cudaSuccess) return e;
+  if ((e = launch_to_bf16_t(w.cmat, w.cmat_t16, 2 * P, H, s)) != cudaSuccess) return e;
+  if ((e = launch_to_bf16(u, w.u16, (size_t)M * H, s)) != cudaSuccess) return e;
+  if ((e = launch_tc_gemm(w.u16, w.bbar_t16, w.xv, M, 2 * P, H, nullptr, nullptr, status, s)) !=
+      cudaSuccess)
+    return e;
+  if ((e = s5_scan_xv(w, B, L, P, s)) != cudaSuccess) return e;
+  if ((e = launch_to_bf16(w.xv, w.x16, (size_t)M * 2 * P, s)) != cudaSuccess) return e;
+  return launch_tc_gemm(w.x16, w.cmat_t16, y, M, H, 2 * P, D, u, status, s);
 }
 
 }  // namespace dlr

@@ -197,3 +197,25 @@ def test_s5_workload_fp32_sampled_batch_row():
     assert oracle.rel_l2(y[5:6], ref) <= TOL
     assert np.all(np.isfinite(y))
     check_status()
+
+
+TOL_BF16 = 1e-2  # the bf16 tensor-core tier's bar
+
+
+@pytest.mark.parametrize("B,L,H,P", [(1, 1, 32, 32), (1, 200, 64, 32), (2, 1000, 96, 64),
+                                     (1, 300, 512, 256)])
+def test_s5_bf16_tensor_cores_match_oracle(B, L, H, P):
+    w = inputs.make_s5(B, L, H, P, seed=7 * B + L + H + P)
+    y = host(dlr.s5_layer(dev(w.u), *s5_dev(w.params), prec="bf16"))
+    ref = oracle.s5_layer(w.u, *s5_np(w.params))
+    assert oracle.rel_l2(y, ref) <= TOL_BF16
+    check_status()
+
+
+def test_s5_workload_bf16_sampled_batch_row():
+    w = inputs.make_workload("s5_b8_l16384_h512_p256")
+    y = host(dlr.s5_layer(dev(w.u), *s5_dev(w.params), prec="bf16"))
+    ref = oracle.s5_layer(w.u[2:3], *s5_np(w.params))
+    assert oracle.rel_l2(y[2:3], ref) <= TOL_BF16
+    assert np.all(np.isfinite(y))
+    check_status()
