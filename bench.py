@@ -357,7 +357,11 @@ def run_extras(torch, dlr, inputs, flush):
     y = torch.empty_like(u)
     ms = _time_steps(torch, lambda: dlr.dlr_scan(u, fwd, out=y), 10, 2, flush)
     out["scan_" + w.name] = {"ms": ms, "elements_per_s": w.B * w.H * w.L / ms * 1e3}
-    del u, y
+    ws = torch.empty(dlr.dlr_conv_workspace_size(w.H, w.L), dtype=torch.uint8, device="cuda")
+    ms = _time_steps(torch, lambda: dlr.dlr_layer(u, fwd, path="fft", workspace=ws, out=y), 10,
+                     2, flush)
+    out["fft_cluster_" + w.name] = {"ms": ms, "elements_per_s": w.B * w.H * w.L / ms * 1e3}
+    del u, y, ws
 
     w = inputs.make_workload("s5_b8_l16384_h512_p256")
     p = w.params

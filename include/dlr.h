@@ -74,7 +74,8 @@ dlr_status dlr_kernel(const float* log_re, const float* log_im, const float* W, 
  * u, y: [B, H, L] float32. K_fwd, K_bwd: [H, L] float32 (K_bwd NULL when dir = DLR_CAUSAL).
  * workspace: >= dlr_conv_workspace_size(H, L, dir) bytes of device memory holding the twiddle
  * table and the per-channel kernel spectra (no initialisation needed; overwritten).
- * u and y must not overlap. Limits: 1 <= L <= 16384.
+ * u and y must not overlap. Limits: 1 <= L <= 65536 (rows longer than 16384 are transformed
+ * by a cluster of 8 CTAs sharing the row through distributed shared memory).
  * dlr_conv is exactly dlr_conv_spectrum followed by dlr_conv_apply on the same stream.
  */
 size_t dlr_conv_workspace_size(int64_t H, int64_t L, dlr_dir dir);

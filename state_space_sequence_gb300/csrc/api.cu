@@ -84,7 +84,7 @@ dlr_status dlr_kernel(const float* log_re, const float* log_im, const float* W, 
 
 size_t dlr_conv_workspace_size(int64_t H, int64_t L, dlr_dir dir) {
   (void)dir;
-  if (H < 1 || L < 1 || L > 16384) return 0;
+  if (H < 1 || L < 1 || L > 65536) return 0;
   return dlr::conv_workspace_bytes(H, L);
 }
 
@@ -101,7 +101,7 @@ dlr_status dlr_conv_spectrum(const float* K_fwd, const float* K_bwd, dlr_dir dir
   if (!K_fwd || !aligned16(K_fwd)) return DLR_ERR_INVALID_ARG;
   if (dir == DLR_BIDIR && (!K_bwd || !aligned16(K_bwd))) return DLR_ERR_INVALID_ARG;
   if (dir == DLR_CAUSAL && K_bwd) return DLR_ERR_INVALID_ARG;
-  if (L > 16384 || H > kMaxGrid) return DLR_ERR_UNSUPPORTED;
+  if (L > 65536 || H > kMaxGrid / 8) return DLR_ERR_UNSUPPORTED;
   dlr_status st = check_conv_ws(H, L, workspace, workspace_bytes);
   if (st != DLR_OK) return st;
   return from_cuda(dlr::launch_dlr_conv_spectrum(K_fwd, dir == DLR_BIDIR ? K_bwd : nullptr,
@@ -115,7 +115,7 @@ dlr_status dlr_conv_apply(const float* u, int64_t B, int64_t H, int64_t L, float
   if (!u || !y || !aligned16(u) || !aligned16(y)) return DLR_ERR_INVALID_ARG;
   const size_t bytes = sizeof(float) * (size_t)B * (size_t)H * (size_t)L;
   if (ranges_overlap(u, bytes, y, bytes)) return DLR_ERR_INVALID_ARG;
-  if (L > 16384 || B * H > kMaxGrid) return DLR_ERR_UNSUPPORTED;
+  if (L > 65536 || B * H > kMaxGrid / 8) return DLR_ERR_UNSUPPORTED;
   dlr_status st = check_conv_ws(H, L, workspace, workspace_bytes);
   if (st != DLR_OK) return st;
   return from_cuda(dlr::launch_dlr_conv_apply(u, (int)B, (int)H, (int)L, y, workspace,
@@ -133,7 +133,7 @@ dlr_status dlr_conv(const float* u, const float* K_fwd, const float* K_bwd, dlr_
   if (!K_fwd || !aligned16(K_fwd)) return DLR_ERR_INVALID_ARG;
   if (dir == DLR_BIDIR && (!K_bwd || !aligned16(K_bwd))) return DLR_ERR_INVALID_ARG;
   if (dir == DLR_CAUSAL && K_bwd) return DLR_ERR_INVALID_ARG;
-  if (L > 16384 || B * H > kMaxGrid) return DLR_ERR_UNSUPPORTED;
+  if (L > 65536 || B * H > kMaxGrid / 8) return DLR_ERR_UNSUPPORTED;
   dlr_status st = check_conv_ws(H, L, workspace, workspace_bytes);
   if (st != DLR_OK) return st;
   st = dlr_conv_spectrum(K_fwd, K_bwd, dir, H, L, workspace, workspace_bytes, stream);

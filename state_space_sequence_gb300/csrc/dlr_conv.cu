@@ -336,10 +336,21 @@ size_t conv_workspace_bytes(int64_t H, int64_t L) {
     default: return cudaErrorInvalidValue;                                                 \
   }
 
+cudaError_t launch_cluster_spectrum(const float* K1, const float* K2, int H, int L, int lg,
+                                    const float2* tw_loc, float2* spec, cudaStream_t s);
+cudaError_t launch_cluster_apply(const float* u, int B, int H, int L, int lg,
+                                 const float2* tw_loc, const float2* spec, float* y,
+                                 cudaStream_t s);
+
 cudaError_t launch_dlr_conv_spectrum(const float* K1, const float* K2, int H, int L, void* ws,
                                      cudaStream_t s) {
   const int lg = conv_log2_size(L);
   ConvWs w = carve_conv(ws, lg);
+  if (lg > 14) {  // a cluster of 8 CTAs per channel; local transforms of n / 8 points
+    const int lloc = lg - 3;
+    twiddle_table<<<((1 << lloc) + 255) / 256, 256, 0, s>>>(w.tw, lloc);
+    return launch_cluster_spectrum(K1, K2, H, L, lg, w.tw, w.spec, s);
+  }
 #define SPEC_CALL(G) launch_spectrum<G>(K1, K2, H, L, w.tw, w.spec, s)
   DLR_CONV_SWITCH(SPEC_CALL)
 #undef SPEC_CALL
@@ -349,6 +360,7 @@ cudaError_t launch_dlr_conv_apply(const float* u, int B, int H, int L, float* y,
                                   cudaStream_t s) {
   const int lg = conv_log2_size(L);
   ConvWs w = carve_conv(ws, lg);
+  if (lg > 14) return launch_cluster_apply(u, B, H, L, lg, w.tw, w.spec, y, s);
 #define APPLY_CALL(G) launch_apply<G>(u, B, H, L, y, w.tw, w.spec, s)
   DLR_CONV_SWITCH(APPLY_CALL)
 #undef APPLY_CALL

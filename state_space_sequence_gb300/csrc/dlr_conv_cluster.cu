@@ -1,0 +1,323 @@
+// dlr_conv_cluster.cu -- FFT convolution for rows too long for one CTA's shared memory
+// (16384 < L <= 65536): the packed transform of n = 8 * n_loc complex points is spread over a
+// cluster of 8 CTAs and exchanged through distributed shared memory.
+//
+// Four-step factorisation with m = c n_loc + i (c = CTA rank) and k = k1 + 8 k2:
+//   Z[k1 + 8 k2] = sum_i W_{n_loc}^{i k2} ( W_n^{i k1} sum_c z[c n_loc + i] W_8^{c k1} )
+// so a row is transformed by
+//   F1  radix-8 DFT across the cluster (each CTA takes n_loc/8 columns i, reads the 8 values
+//       z[c n_loc + i] from the 8 CTAs, twiddles by W_n^{i k1} and writes output k1 into CTA k1),
+//   F2  a local n_loc-point Stockham FFT in each CTA: CTA k1 then holds Z[k1 + 8 k2] at k2,
+// the spectral step pairs k with n - k (the mirror sits in CTA (8 - k1) mod 8), and the inverse
+// runs the same two steps backwards: local inverse FFT, then the radix-8 inverse DFT across the
+// cluster, whose outputs go straight to global memory. Same arithmetic as the one-CTA row
+// kernel otherwise ("Simplifying and Understanding State Space Models with Diagonal Linear
+// RNNs", section 2.1 and appendix A.1: Toeplitz product as a circulant product of size >= 2L).
+// Spectra are stored in cluster order S'[k1 n_loc + k2] = S[k1 + 8 k2], with S[n] last.
+#include "fft_rows.cuh"
+
+namespace dlr {
+namespace {
+
+using fft::padded;
+using fft::padded_size;
+constexpr int kC = 8;  // CTAs per cluster
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// shared::cluster address of the same shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_rank(uint32_t local_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float2 ld_cluster(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_cluster(uint32_t addr, float2 v) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(v.x), "f"(v.y)
+               : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n"
+      "barrier.cluster.wait.acquire.aligned;" ::
+          : "memory");
+}
+
+// x^e for e < 8, at most three multiplications deep
+__device__ __forceinline__ void powers8(cf (&p)[8], cf x) {
+  p[0] = {1.f, 0.f};
+  p[1] = x;
+  p[2] = cmul(x, x);
+  p[3] = cmul(p[2], x);
+  p[4] = cmul(p[2], p[2]);
+  p[5] = cmul(p[4], x);
+  p[6] = cmul(p[4], p[2]);
+  p[7] = cmul(p[4], p[3]);
+}
+
+// Local Stockham FFT of n_loc = 2^kLog points held in `cur` (natural order); the result ends
+// in natural order in `cur` (the pointers are swapped as the passes alternate buffers).
+template <int kLog, bool kInv>
+__device__ __forceinline__ void local_fft(float2*& cur, float2*& nxt,
+                                          const float2* __restrict__ tw) {
+  using P = fftr::Plan<kLog>;
+  cf a[P::PER0][P::R0];
+#pragma unroll
+  for (int q = 0; q < P::PER0; ++q) {
+    const int j = threadIdx.x + q * P::T;
+    if (P::NB0 % P::T == 0 || j < P::NB0) {
+#pragma unroll
+      for (int r = 0; r < P::R0; ++r) {
+        const float2 f = cur[padded(j + r * P::NB0)];
+        a[q][r] = {f.x, f.y};
+      }
+      fft::dft<P::R0, kInv>(a[q]);
+    }
+  }
+  fftr::pass0_store<kLog>(nxt, a);
+  __syncthreads();
+  {
+    float2* t = cur;
+    cur = nxt;
+    nxt = t;
+  }
+  int ns = P::R0;
+#pragma unroll 1
+  for (int p = 0; p < P::n16; ++p) {
+    cf v[P::PER16][16];
+    fftr::pass16_load_compute<kLog, kInv>(cur, ns, tw, v);
+    fftr::pass16_store<kLog>(nxt, ns, v);
+    __syncthreads();
+    float2* t = cur;
+    cur = nxt;
+    nxt = t;
+    ns *= 16;
+  }
+}
+
+// kSpectrum: transform the circulant column of channel `row` and write its spectrum.
+// Otherwise: convolve row `row` of u with the spectra and write y.
+template <int kLog, bool kSpectrum>
+__global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(fftr::Plan<kLog>::T)
+conv_cluster(const float* __restrict__ src, const float* __restrict__ src2, int H, int L,
+             const float2* __restrict__ tw, float2* __restrict__ spec, float* __restrict__ y) {
+  using P = fftr::Plan<kLog>;
+  constexpr int nl = P::n;          // points per CTA
+  constexpr int n = kC * nl;        // packed points per row
+  constexpr int T = P::T;
+  constexpr int colsPer = nl / kC;  // F1 / I1 columns per CTA
+  extern __shared__ float2 smem[];
+  float2* buf0 = smem;
+  float2* buf1 = smem + P::buf_elems;
+  const uint32_t rank = cluster_rank();
+  const int row = blockIdx.x / kC;
+  const int tid = threadIdx.x;
+  const int half = (L + 1) >> 1;
+
+  // ---- 0) this CTA's slice of the packed row: z[rank * nl + i] ----
+  if constexpr (kSpectrum) {
+    const float* k1 = src + (size_t)row * L;
+    const float* k2 = src2 ? src2 + (size_t)row * L : nullptr;
+    auto col = [&](int i) -> float {  // circulant column of length 2n
+      float v = (i < L) ? k1[i] : 0.f;
+      if (k2) {
+        if (i == 0) v += k2[0];
+        else if (i > 2 * n - L) v += k2[2 * n - i];
+      }
+      return v;
+    };
+    for (int i = tid; i < nl; i += T) {
+      const int m = (int)rank * nl + i;
+      buf0[padded(i)] = make_float2(col(2 * m), col(2 * m + 1));
+    }
+  } else {
+    const float* ur = src + (size_t)row * L;
+    const bool even = (L & 1) == 0;
+    for (int i = tid; i < nl; i += T) {
+      const int m = (int)rank * nl + i;
+      float2 z = make_float2(0.f, 0.f);
+      if (m < half) {
+        if (even) z = __ldg(reinterpret_cast<const float2*>(ur) + m);
+        else z = make_float2(ur[2 * m], (2 * m + 1 < L) ? ur[2 * m + 1] : 0.f);
+      }
+      buf0[padded(i)] = z;
+    }
+  }
+  cluster_sync();
+
+  // ---- F1: radix-8 DFT across the cluster, twiddle W_n^{i k1}, output k1 -> CTA k1 ----
+  {
+    const uint32_t b0 = smem_addr(buf0), b1 = smem_addr(buf1);
+    for (int ii = tid; ii < colsPer; ii += T) {
+      const int i = (int)rank * colsPer + ii;
+      cf v[8];
+#pragma unroll
+      for (int c = 0; c < kC; ++c) {
+        // the conv input is zero for m >= n/2, i.e. c >= 4
+        if (!kSpectrum && c >= kC / 2) {
+          v[c] = {0.f, 0.f};
+        } else {
+          const float2 f = ld_cluster(map_rank(b0, c) + 8u * padded(i));
+          v[c] = {f.x, f.y};
+        }
+      }
+      fft::dft<8, false>(v);
+      float s, co;
+      sincospif(-ldexpf((float)i, 1 - (kLog + 3)), &s, &co);  // W_n^i = e^{-2 pi i i / n}
+      cf w[8];
+      powers8(w, {co, s});
+#pragma unroll
+      for (int k1 = 0; k1 < kC; ++k1) {
+        const cf t = k1 ? cmul(v[k1], w[k1]) : v[k1];
+        st_cluster(map_rank(b1, k1) + 8u * padded(i), make_float2(t.re, t.im));
+      }
+    }
+  }
+  cluster_sync();
+
+  // ---- F2: local FFT over i; CTA k1 = rank then holds Z[k1 + 8 k2] at k2 ----
+  float2* cur = buf1;
+  float2* nxt = buf0;
+  local_fft<kLog, false>(cur, nxt, tw);
+  cluster_sync();  // every CTA's Z is complete before mirrors are read
+
+  const int k1 = (int)rank;
+  const uint32_t curAddr = smem_addr(cur);
+  const uint32_t mirrorRank = (kC - k1) & (kC - 1);
+  const uint32_t mirrorBase = map_rank(curAddr, mirrorRank);
+  auto mirror_local = [&](int k2) { return k1 == 0 ? (nl - k2) & (nl - 1) : nl - 1 - k2; };
+
+  if constexpr (kSpectrum) {
+    // ---- real spectrum X_k, k = k1 + 8 k2, scaled by 1/(4n), stored in cluster order ----
+    const float scale = 1.0f / (float)(4 * n);
+    float2* out = spec + (size_t)row * (n + 1);
+    for (int k2 = tid; k2 < nl; k2 += T) {
+      const int k = k1 + kC * k2;
+      const float2 fa = cur[padded(k2)];
+      const float2 fb = ld_cluster(mirrorBase + 8u * padded(mirror_local(k2)));
+      const cf E = {0.5f * (fa.x + fb.x), 0.5f * (fa.y - fb.y)};
+      const cf O = {0.5f * (fa.y + fb.y), -0.5f * (fa.x - fb.x)};
+      float s, co;
+      sincospif(ldexpf((float)k, -(kLog + 3)), &s, &co);
+      const cf wO = cmul({co, -s}, O);
+      const cf Xk = cadd(E, wO);
+      out[k1 * nl + k2] = make_float2(Xk.re * scale, Xk.im * scale);
+      if (k == 0) {  // X_n = E - O at k = 0
+        const cf Xn = {E.re - wO.re, -(E.im - wO.im)};
+        out[n] = make_float2(Xn.re * scale, Xn.im * scale);
+      }
+    }
+    cluster_sync();  // mirrors read before any CTA exits
+    return;
+  } else {
+    // ---- spectral step: Z'_k from Z_k, Z_{n-k} and the spectra, into nxt ----
+    const float2* S = spec + (size_t)(row % H) * (n + 1);
+    for (int k2 = tid; k2 < nl; k2 += T) {
+      const int k = k1 + kC * k2;
+      const int mk2 = mirror_local(k2);
+      const float2 fa = cur[padded(k2)];
+      const float2 fb = ld_cluster(mirrorBase + 8u * padded(mk2));
+      float s, co;
+      sincospif(ldexpf((float)k, -(kLog + 3)), &s, &co);
+      const cf w = {co, -s};  // e^{-i pi k / n}
+      const cf E = {fa.x + fb.x, fa.y - fb.y};
+      const cf O = {fa.y + fb.y, fb.x - fa.x};
+      const cf wO = cmul(w, O);
+      const cf X = cadd(E, wO);
+      const cf Xn = {E.re - wO.re, wO.im - E.im};
+      const float2 sk = __ldg(&S[k1 * nl + k2]);
+      const float2 sn = __ldg(&S[k == 0 ? n : (int)mirrorRank * nl + mk2]);
+      const cf Yk = cmul(X, {sk.x, sk.y});
+      const cf Yn = cmul(Xn, {sn.x, sn.y});
+      const cf Ep = {Yk.re + Yn.re, Yk.im - Yn.im};
+      const cf Op = cmul({Yk.re - Yn.re, Yk.im + Yn.im}, cconj(w));
+      nxt[padded(k2)] = make_float2(Ep.re - Op.im, Ep.im + Op.re);
+    }
+    cluster_sync();  // mirror reads of `cur` done everywhere before it is reused
+    {
+      float2* t = cur;
+      cur = nxt;
+      nxt = t;
+    }
+    // ---- I2: local inverse FFT over k2 -> index i ----
+    local_fft<kLog, true>(cur, nxt, tw);
+    cluster_sync();
+
+    // ---- I1: twiddle conj(W_n^{i k1}) and radix-8 inverse DFT across the cluster ----
+    const uint32_t cAddr = smem_addr(cur);
+    float* yr = y + (size_t)row * L;
+    const bool even = (L & 1) == 0;
+    for (int ii = tid; ii < colsPer; ii += T) {
+      const int i = (int)rank * colsPer + ii;
+      float s, co;
+      sincospif(ldexpf((float)i, 1 - (kLog + 3)), &s, &co);  // W_n^{-i}
+      cf w[8];
+      powers8(w, {co, s});
+      cf v[8];
+#pragma unroll
+      for (int c = 0; c < kC; ++c) {
+        const float2 f = ld_cluster(map_rank(cAddr, c) + 8u * padded(i));
+        v[c] = c ? cmul({f.x, f.y}, w[c]) : cf{f.x, f.y};
+      }
+      fft::dft<8, true>(v);
+#pragma unroll
+      for (int c = 0; c < kC / 2; ++c) {  // outputs m = c nl + i < n/2 hold y
+        const int m = c * nl + i;
+        if (m < half) {
+          if (even) {
+            reinterpret_cast<float2*>(yr)[m] = make_float2(v[c].re, v[c].im);
+          } else {
+            yr[2 * m] = v[c].re;
+            if (2 * m + 1 < L) yr[2 * m + 1] = v[c].im;
+          }
+        }
+      }
+    }
+    cluster_sync();  // no CTA exits while others still read its shared memory
+  }
+}
+
+template <int kLog, bool kSpectrum>
+cudaError_t launch_cluster(const float* src, const float* src2, int rows, int H, int L,
+                           const float2* tw, float2* spec, float* y, cudaStream_t s) {
+  using P = fftr::Plan<kLog>;
+  const size_t smem = 2 * P::buf_elems * sizeof(float2);
+  cudaError_t e = cudaFuncSetAttribute(conv_cluster<kLog, kSpectrum>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  conv_cluster<kLog, kSpectrum><<<(unsigned)(rows * kC), P::T, smem, s>>>(src, src2, H, L, tw,
+                                                                        spec, y);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// n = next power of two >= L lies in (16384, 65536]; n_loc = n / 8 points per CTA.
+cudaError_t launch_cluster_spectrum(const float* K1, const float* K2, int H, int L, int lg,
+                                    const float2* tw_loc, float2* spec, cudaStream_t s) {
+  if (lg == 15) return launch_cluster<12, true>(K1, K2, H, H, L, tw_loc, spec, nullptr, s);
+  if (lg == 16) return launch_cluster<13, true>(K1, K2, H, H, L, tw_loc, spec, nullptr, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_cluster_apply(const float* u, int B, int H, int L, int lg,
+                                 const float2* tw_loc, const float2* spec, float* y,
+                                 cudaStream_t s) {
+  float2* sp = const_cast<float2*>(spec);
+  if (lg == 15) return launch_cluster<12, false>(u, nullptr, B * H, H, L, tw_loc, sp, y, s);
+  if (lg == 16) return launch_cluster<13, false>(u, nullptr, B * H, H, L, tw_loc, sp, y, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dlr

@@ -86,6 +86,24 @@ def test_conv_matches_oracle_toeplitz(B, H, L, bidir):
     check_status()
 
 
+@pytest.mark.parametrize("B,H,L", [(1, 1, 16385), (2, 1, 20000), (1, 2, 32768), (1, 1, 40001),
+                                   (1, 1, 65536)])
+@pytest.mark.parametrize("bidir", [False, True])
+def test_conv_long_rows_cluster_path(B, H, L, bidir):
+    """Rows longer than 16384: the transform is spread over a cluster of 8 CTAs."""
+    rng = np.random.default_rng(B * 5 + H * 13 + L)
+    u = rng.standard_normal((B, H, L)).astype(np.float32)
+    K1 = (rng.standard_normal((H, L)) * np.exp(-np.arange(L) / 3000.0)).astype(np.float32)
+    K2 = (rng.standard_normal((H, L)) * np.exp(-np.arange(L) / 9000.0)).astype(np.float32)
+    y = host(dlr.dlr_conv(dev(u), dev(K1), dev(K2) if bidir else None))
+    ref = oracle.toeplitz_causal(u, K1.astype(np.float64))
+    if bidir:
+        ref = ref + oracle.toeplitz_causal(np.ascontiguousarray(u[..., ::-1]),
+                                           K2.astype(np.float64))[..., ::-1]
+    assert oracle.rel_l2(y, ref) <= TOL
+    check_status()
+
+
 @pytest.mark.parametrize("B,H,N,L", [(1, 1, 1, 1), (1, 1, 1, 7), (2, 3, 5, 63), (1, 2, 16, 64),
                                      (2, 2, 16, 65), (1, 2, 64, 4095), (1, 2, 64, 4097),
                                      (2, 1, 65, 1000), (1, 2, 128, 5000), (1, 1, 64, 12289)])
@@ -165,6 +183,19 @@ def test_workload_long_unit_circle_scan():
     assert oracle.rel_l2(y, ref) <= TOL
     # the unit-circle channels alone (they dominate the norm, and are the hard case)
     assert oracle.rel_l2(y[:, :8], ref[:, :8]) <= TOL
+    check_status()
+
+
+def test_workload_long_unit_circle_fft_and_scan():
+    """B=1 H=256 N=64 L=65536: the FFT path (2L = 131072, cluster transform) against the oracle,
+    and FFT and scan paths against each other."""
+    w = inputs.make_workload("dlr_b1_h256_n64_l65536_unit8")
+    y_fft = host(dlr.dlr_layer(dev(w.u), params_dev(w.fwd), path="fft"))
+    y_scan = host(dlr.dlr_layer(dev(w.u), params_dev(w.fwd), path="scan"))
+    ref = oracle.dlr_layer(w.u, params_np(w.fwd))
+    assert oracle.rel_l2(y_fft, ref) <= TOL
+    assert oracle.rel_l2(y_fft[:, :8], ref[:, :8]) <= TOL
+    assert oracle.rel_l2(y_fft, y_scan) <= TOL
     check_status()
 
 
