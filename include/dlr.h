@@ -110,9 +110,9 @@ dlr_status dlr_conv_apply(const float* u, int64_t B, int64_t H, int64_t L, float
  *  - It allocates nothing (no cudaMalloc, no cudaFree, no allocating library call). Its scratch
  *    is a fixed 16 MiB array inside the library's device memory, held by every GPU that loads
  *    the library until the process exits.
- *  - Limit: the call needs 8*n (rounded up to 256) + 8*H*(n+1) bytes of scratch, n = the next
+ *  - Limit: the call needs 24*n (two twiddle tables) + 8*H*(n+1) bytes of scratch, n = the next
  *    power of two >= L; larger requests return DLR_ERR_WORKSPACE and launch nothing (e.g.
- *    up to H = 510 at L = 4096, up to H = 126 at L = 16384). L <= 16384 as for dlr_conv.
+ *    up to H = 508 at L = 4096, up to H = 124 at L = 16384). L <= 16384 as for dlr_conv.
  *  - The first call on a device looks up the scratch's device address (with that device
  *    current) and caches it; make that first call before any stream capture.
  *  - All calls in the process share the one scratch array, which keeps the last call's
@@ -164,6 +164,16 @@ dlr_status s5_layer(const float* u, const float* lambda, const float* log_delta,
  * DLR_ERR_CUDA when the synchronisation itself failed.
  */
 dlr_status dlr_get_device_status(dlr_stream_t stream);
+
+/*
+ * dlr_selftest_timeout -- exercises the device-side failure reporting without faulting the
+ * GPU: one thread waits on a shared-memory barrier that nothing will ever complete, with a
+ * wait limit of `limit_ms` milliseconds (1..2000), the same kind of bounded wait the
+ * tensor-core pipelines use. When the limit runs out the kernel records DLR_ERR_TIMEOUT in the
+ * device status word and returns normally, so the context stays usable; the next
+ * dlr_get_device_status() reports DLR_ERR_TIMEOUT and clears it. Returns DLR_OK once launched.
+ */
+dlr_status dlr_selftest_timeout(int limit_ms, dlr_stream_t stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* dlr_status_string(dlr_status status);

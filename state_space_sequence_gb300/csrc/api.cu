@@ -20,6 +20,7 @@ size_t s5_workspace_bytes(int64_t B, int64_t L, int64_t H, int64_t P, bool bf16)
 cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delta,
                       const float* Bt, const float* Ct, const float* D, int B, int L, int H, int P,
                       bool bf16, float* y, void* ws, int* status, cudaStream_t s);
+cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
 }  // namespace dlr
 
 // The library's device status word (one per device that loads the library).
@@ -187,6 +188,14 @@ dlr_status s5_layer(const float* u, const float* lambda, const float* log_delta,
   if (bf16 && !status) return DLR_ERR_CUDA;
   return from_cuda(dlr::launch_s5(u, lambda, log_delta, Bt, Ct, D, (int)B, (int)L, (int)H,
                                   (int)P, bf16, y, workspace, status, (cudaStream_t)stream));
+}
+
+dlr_status dlr_selftest_timeout(int limit_ms, dlr_stream_t stream) {
+  if (limit_ms < 1 || limit_ms > 2000) return DLR_ERR_INVALID_ARG;
+  int* status = status_word();
+  if (!status) return DLR_ERR_CUDA;
+  return from_cuda(dlr::launch_selftest_timeout((uint64_t)limit_ms * 1000000ull, status,
+                                                (cudaStream_t)stream));
 }
 
 dlr_status dlr_get_device_status(dlr_stream_t stream) {

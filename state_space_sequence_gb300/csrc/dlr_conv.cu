@@ -272,6 +272,219 @@ conv_rows(const float* __restrict__ u, const float2* __restrict__ spec,
   }
 }
 
+// Two rows of the same channel per CTA, as the real and imaginary parts of one complex
+// sequence z = u_b0 + i u_b1 of M = 2n points (zero beyond L): one forward and one inverse
+// complex FFT of size M per pair, and between them a plain complex product with the full
+// kernel spectrum (the spectrum of a real kernel is Hermitian, so Re / Im of the result are the
+// two rows' convolutions). Because z is zero on its upper half, the first radix-2 pass of the
+// forward transform only duplicates points: the first real pass reads z[i >> 1] straight from
+// global memory. The last inverse pass (radix 2) computes only the outputs m < L.
+template <int kG>
+struct PairPlan {
+  using P = fftr::Plan<kG>;                     // radix-16 passes over M points
+  static constexpr int M = 1 << kG;
+  static constexpr int G1 = kG - 1;             // bits after the duplicating radix-2 pass
+  static constexpr int R1 = (G1 % 4 == 0) ? 16 : (1 << (G1 % 4));
+  static constexpr int n16 = (G1 % 4 == 0) ? G1 / 4 - 1 : G1 / 4;
+  static constexpr int T = P::T;
+  static constexpr int NB1 = M / R1;
+  static constexpr int PER1 = (NB1 + T - 1) / T;
+  static constexpr size_t buf_elems = padded_size(M);
+  static constexpr bool kDouble = 2 * buf_elems * sizeof(float2) <= 72 * 1024;
+  static constexpr size_t smem = (kDouble ? 2 : 1) * buf_elems * sizeof(float2);
+};
+
+template <int kG>
+__global__ void __launch_bounds__(PairPlan<kG>::T)
+conv_pairs(const float* __restrict__ u, const float2* __restrict__ spec,
+           const float2* __restrict__ twM, float* __restrict__ y, int B, int H, int L) {
+  using PP = PairPlan<kG>;
+  using P = typename PP::P;
+  constexpr int M = PP::M, T = PP::T, R1 = PP::R1, NB1 = PP::NB1;
+  constexpr int n = M / 2;
+  extern __shared__ float2 smem[];
+  float2* cur = smem;
+  float2* nxt = PP::kDouble ? smem + PP::buf_elems : smem;
+  const int pair = blockIdx.x / H, h = blockIdx.x % H;
+  const int b0 = 2 * pair, b1 = 2 * pair + 1;
+  const bool has1 = b1 < B;
+  const float* u0 = u + ((size_t)b0 * H + h) * L;
+  const float* u1 = u + ((size_t)(has1 ? b1 : b0) * H + h) * L;
+  const int tid = threadIdx.x;
+
+  // ---- forward pass 1 (radix R1, ns = 2): inputs z[i >> 1] from global memory ----
+  {
+    cf a[PP::PER1][R1];
+    int dst[PP::PER1];
+#pragma unroll
+    for (int q = 0; q < PP::PER1; ++q) {
+      const int j = tid + q * T;
+      dst[q] = -1;
+      if (NB1 % T == 0 || j < NB1) {
+#pragma unroll
+        for (int r = 0; r < R1; ++r) {
+          const int m = (j >> 1) + r * (NB1 / 2);
+          cf z = {0.f, 0.f};
+          if (m < L) z = {__ldg(&u0[m]), has1 ? __ldg(&u1[m]) : 0.f};
+          a[q][r] = z;
+        }
+        const int k = j & 1;
+        if (k) {
+#pragma unroll
+          for (int r = 1; r < R1; ++r) a[q][r] = cmul(a[q][r], fftr::half16(r * (16 / R1)));
+        }
+        fft::dft<R1, false>(a[q]);
+        dst[q] = (j - k) * R1 + k;
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < PP::PER1; ++q)
+      if (dst[q] >= 0) {
+#pragma unroll
+        for (int r = 0; r < R1; ++r)
+          cur[padded(dst[q] + 2 * r)] = make_float2(a[q][r].re, a[q][r].im);
+      }
+  }
+  __syncthreads();
+
+  // ---- forward radix-16 passes; the last leaves Z[j + r M/16] in registers ----
+  int ns = 2 * R1;
+  cf v[P::PER16][16];
+#pragma unroll 1
+  for (int p = 0; p < PP::n16; ++p) {
+    fftr::pass16_load_compute<kG, false>(cur, ns, twM, v);
+    if (p < PP::n16 - 1) {
+      if (!PP::kDouble) __syncthreads();
+      fftr::pass16_store<kG>(nxt, ns, v);
+      __syncthreads();
+      float2* t = cur;
+      cur = nxt;
+      nxt = t;
+      ns *= 16;
+    }
+  }
+
+  // ---- spectral product: Y_k = Z_k * C_k, C_k = 2 S_k (k <= n), conj(2 S_{M-k}) (k > n) ----
+  const float2* S = spec + (size_t)h * (n + 1);
+#pragma unroll
+  for (int q = 0; q < P::PER16; ++q) {
+    const int j = tid + q * T;
+    if (P::NB16 % T == 0 || j < P::NB16) {
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const int k = j + r * P::NB16;
+        float2 c;
+        if (k <= n) {
+          c = __ldg(&S[k]);
+        } else {
+          c = __ldg(&S[M - k]);
+          c.y = -c.y;
+        }
+        v[q][r] = cmul(v[q][r], {2.f * c.x, 2.f * c.y});
+      }
+    }
+  }
+
+  // ---- inverse pass 1 (radix R1, ns = 1) ----
+  if constexpr (R1 == 16) {
+    // the registers already hold the inputs x[j + r M/16] of a radix-16 first pass
+#pragma unroll
+    for (int q = 0; q < P::PER16; ++q) {
+      const int j = tid + q * T;
+      if (P::NB16 % T == 0 || j < P::NB16) fft::dft<16, true>(v[q]);
+    }
+    if (!PP::kDouble) __syncthreads();
+#pragma unroll
+    for (int q = 0; q < P::PER16; ++q) {
+      const int j = tid + q * T;
+      if (P::NB16 % T == 0 || j < P::NB16) {
+        float2* d0 = nxt + padded(16 * j);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) d0[r] = make_float2(v[q][r].re, v[q][r].im);
+      }
+    }
+  } else {
+    // park Y in natural order, then run the radix-R1 pass from shared memory
+    if (!PP::kDouble) __syncthreads();
+    fftr::pass16_store<kG>(nxt, P::NB16, v);  // ns = M/16: positions j + r M/16
+    __syncthreads();
+    {
+      float2* t = cur;
+      cur = nxt;
+      nxt = t;
+    }
+    cf a[PP::PER1][R1];
+#pragma unroll
+    for (int q = 0; q < PP::PER1; ++q) {
+      const int j = tid + q * T;
+      if (NB1 % T == 0 || j < NB1) {
+#pragma unroll
+        for (int r = 0; r < R1; ++r) {
+          const float2 f = cur[padded(j + r * NB1)];
+          a[q][r] = {f.x, f.y};
+        }
+        fft::dft<R1, true>(a[q]);
+      }
+    }
+    if (!PP::kDouble) __syncthreads();
+#pragma unroll
+    for (int q = 0; q < PP::PER1; ++q) {
+      const int j = tid + q * T;
+      if (NB1 % T == 0 || j < NB1) {
+        float2* d0 = nxt + padded(j * R1);
+#pragma unroll
+        for (int r = 0; r < R1; ++r) d0[r] = make_float2(a[q][r].re, a[q][r].im);
+      }
+    }
+  }
+  __syncthreads();
+  {
+    float2* t = cur;
+    cur = nxt;
+    nxt = t;
+  }
+
+  // ---- inverse radix-16 passes (ns = R1 ... M/32) ----
+  ns = R1;
+#pragma unroll 1
+  for (int p = 0; p < PP::n16; ++p) {
+    fftr::pass16_load_compute<kG, true>(cur, ns, twM, v);
+    if (!PP::kDouble) __syncthreads();
+    fftr::pass16_store<kG>(nxt, ns, v);
+    __syncthreads();
+    float2* t = cur;
+    cur = nxt;
+    nxt = t;
+    ns *= 16;
+  }
+
+  // ---- last inverse pass (radix 2, ns = M/2), only outputs m < L: x_m + w^m x_{m + M/2} ----
+  float* y0 = y + ((size_t)b0 * H + h) * L;
+  float* y1 = y + ((size_t)(has1 ? b1 : b0) * H + h) * L;
+  for (int m = tid; m < L; m += T) {
+    const float2 a = cur[padded(m)], b = cur[padded(m + n)];
+    const float2 w = __ldg(&twM[m]);
+    const cf t = cmul({b.x, b.y}, {w.x, -w.y});
+    y0[m] = a.x + t.re;
+    if (has1) y1[m] = a.y + t.im;
+  }
+}
+
+template <int kG>
+cudaError_t launch_pairs(const float* u, int B, int H, int L, float* y, const float2* twM,
+                         const float2* spec, cudaStream_t s) {
+  using PP = PairPlan<kG>;
+  if (PP::smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(conv_pairs<kG>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)PP::smem);
+    if (e != cudaSuccess) return e;
+  }
+  const unsigned grid = (unsigned)(((size_t)B + 1) / 2 * H);
+  conv_pairs<kG><<<grid, PP::T, PP::smem, s>>>(u, spec, twM, y, B, H, L);
+  return cudaGetLastError();
+}
+
 template <int kLog>
 cudaError_t launch_spectrum(const float* K1, const float* K2, int H, int L, float2* tw,
                             float2* spec, cudaStream_t s) {
@@ -300,15 +513,18 @@ cudaError_t launch_apply(const float* u, int B, int H, int L, float* y, const fl
 }
 
 struct ConvWs {
-  float2* tw;
-  float2* spec;
+  float2* tw;    // n-point table  e^{-2 pi i m / n}
+  float2* tw2;   // 2n-point table e^{-2 pi i m / 2n}
+  float2* spec;  // [H][n + 1]
 };
 
 ConvWs carve_conv(const void* ws, int lg) {
   const size_t n = size_t(1) << lg;
   const size_t twb = (sizeof(float2) * n + 255) & ~size_t(255);
+  const size_t tw2b = (sizeof(float2) * 2 * n + 255) & ~size_t(255);
   char* base = const_cast<char*>(reinterpret_cast<const char*>(ws));
-  return {reinterpret_cast<float2*>(base), reinterpret_cast<float2*>(base + twb)};
+  return {reinterpret_cast<float2*>(base), reinterpret_cast<float2*>(base + twb),
+          reinterpret_cast<float2*>(base + twb + tw2b)};
 }
 
 }  // namespace
@@ -321,9 +537,9 @@ int conv_log2_size(int64_t L) {
 
 size_t conv_workspace_bytes(int64_t H, int64_t L) {
   const int64_t n = int64_t(1) << conv_log2_size(L);
-  size_t tw = sizeof(float2) * (size_t)n;
-  tw = (tw + 255) & ~size_t(255);
-  return tw + sizeof(float2) * (size_t)H * (size_t)(n + 1);
+  const size_t tw = (sizeof(float2) * (size_t)n + 255) & ~size_t(255);
+  const size_t tw2 = (sizeof(float2) * 2 * (size_t)n + 255) & ~size_t(255);
+  return tw + tw2 + sizeof(float2) * (size_t)H * (size_t)(n + 1);
 }
 
 #define DLR_CONV_SWITCH(CALL)                                                              \
@@ -351,6 +567,8 @@ cudaError_t launch_dlr_conv_spectrum(const float* K1, const float* K2, int H, in
     twiddle_table<<<((1 << lloc) + 255) / 256, 256, 0, s>>>(w.tw, lloc);
     return launch_cluster_spectrum(K1, K2, H, L, lg, w.tw, w.spec, s);
   }
+  if (lg >= 11 && lg <= 13)  // the two-rows-per-transform kernel also needs the 2n-point table
+    twiddle_table<<<((2 << lg) + 255) / 256, 256, 0, s>>>(w.tw2, lg + 1);
 #define SPEC_CALL(G) launch_spectrum<G>(K1, K2, H, L, w.tw, w.spec, s)
   DLR_CONV_SWITCH(SPEC_CALL)
 #undef SPEC_CALL
@@ -361,6 +579,11 @@ cudaError_t launch_dlr_conv_apply(const float* u, int B, int H, int L, float* y,
   const int lg = conv_log2_size(L);
   ConvWs w = carve_conv(ws, lg);
   if (lg > 14) return launch_cluster_apply(u, B, H, L, lg, w.tw, w.spec, y, s);
+  if (B >= 2 && lg >= 11 && lg <= 13) {  // two rows per complex transform of size 2n
+    if (lg == 11) return launch_pairs<12>(u, B, H, L, y, w.tw2, w.spec, s);
+    if (lg == 12) return launch_pairs<13>(u, B, H, L, y, w.tw2, w.spec, s);
+    return launch_pairs<14>(u, B, H, L, y, w.tw2, w.spec, s);
+  }
 #define APPLY_CALL(G) launch_apply<G>(u, B, H, L, y, w.tw, w.spec, s)
   DLR_CONV_SWITCH(APPLY_CALL)
 #undef APPLY_CALL

@@ -30,8 +30,8 @@ cudaError_t launch_dlr_conv_apply(const float* u, int B, int H, int L, float* y,
 
 namespace {
 
-// 16 MiB: room for the twiddle table and the spectra of H channels at length L as long as
-// 8 * n + 8 * H * (n + 1) bytes fit (n = next power of two >= L, the twiddle part rounded up
+// 16 MiB: room for the twiddle tables and the spectra of H channels at length L as long as
+// 24 * n + 8 * H * (n + 1) bytes fit (n = next power of two >= L, the twiddle parts rounded up
 // to 256 bytes): up to H = 510 channels at L = 4096, up to H = 126 at L = 16384.
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 

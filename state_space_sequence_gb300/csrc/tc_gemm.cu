@@ -138,6 +138,16 @@ tc_gemm_bf16(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
   if (warp == 2) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+// Failure-reporting self-test: one thread waits on a barrier that nothing completes.
+__global__ void selftest_wait_timeout(uint64_t limit_ns, int* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    tc::mbar_fence_init();
+    if (!tc::mbar_wait(&bar, 0, limit_ns)) report_status(status, DLR_ERR_TIMEOUT);
+  }
+}
+
 // fp32 -> bf16, same layout (n a multiple of 4, 16-byte aligned pointers)
 __global__ void to_bf16(const float4* __restrict__ x, __nv_bfloat162* __restrict__ y, size_t n4) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
@@ -206,6 +216,11 @@ cudaError_t launch_to_bf16(const float* x, void* y, size_t n, cudaStream_t s) {
 cudaError_t launch_to_bf16_t(const float* x, void* y, int R, int C, cudaStream_t s) {
   dim3 grid((C + 31) / 32, (R + 31) / 32);
   to_bf16_t<<<grid, dim3(32, 8), 0, s>>>(x, reinterpret_cast<__nv_bfloat16*>(y), R, C);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s) {
+  selftest_wait_timeout<<<1, 32, 0, s>>>(limit_ns, status);
   return cudaGetLastError();
 }
 

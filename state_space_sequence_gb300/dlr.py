@@ -52,6 +52,8 @@ def _load():
         lib.s5_workspace_size.restype = sz
         lib.s5_layer.argtypes = [P, P, P, P, P, P, i64, i64, i64, i64, i32, P, P, sz, P]
         lib.s5_layer.restype = i32
+        lib.dlr_selftest_timeout.argtypes = [i32, P]
+        lib.dlr_selftest_timeout.restype = i32
         lib.dlr_get_device_status.argtypes = [P]
         lib.dlr_get_device_status.restype = i32
         lib.dlr_status_string.argtypes = [i32]
@@ -190,6 +192,12 @@ def s5_layer(u, lam, log_delta, Bt, Ct, D, prec: str = "fp32", out=None, workspa
                                      _ptr(D), B, L, H, P, PREC[prec], _ptr(out),
                                      _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
+
+
+def selftest_timeout(limit_ms: int = 50, stream=None) -> None:
+    """Launch the bounded-wait self-test (see include/dlr.h); read the result with
+    device_status()."""
+    _ok("dlr_selftest_timeout", _load().dlr_selftest_timeout(limit_ms, _stream(stream)))
 
 
 def device_status(stream=None) -> int:

@@ -85,8 +85,8 @@ def test_host_validation_rejects_bad_arguments(lib):
 def test_workspace_queries(lib):
     lib.dlr_conv_workspace_size.restype = ctypes.c_size_t
     lib.dlr_conv_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int]
-    # L = 4096 -> n = 4096 packed points: twiddles n*8 B + spectra H*(n+1)*8 B
-    assert lib.dlr_conv_workspace_size(256, 4096, 0) == 4096 * 8 + 256 * 4097 * 8
+    # L = 4096 -> n = 4096: twiddle tables of n and 2n points + spectra H*(n+1) complex
+    assert lib.dlr_conv_workspace_size(256, 4096, 0) == 4096 * 8 + 8192 * 8 + 256 * 4097 * 8
     assert lib.dlr_conv_workspace_size(0, 4096, 0) == 0
     lib.s5_workspace_size.restype = ctypes.c_size_t
     lib.s5_workspace_size.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int]

@@ -70,7 +70,10 @@ def test_kernel_dft_identity_on_gpu():
 
 @pytest.mark.parametrize("B,H,L", [(1, 1, 1), (1, 1, 2), (2, 3, 3), (1, 2, 5), (2, 2, 64),
                                    (3, 2, 100), (1, 3, 1000), (2, 2, 4095), (1, 2, 4096),
-                                   (1, 1, 8192), (1, 1, 16383), (1, 2, 16384)])
+                                   (1, 1, 8192), (1, 1, 16383), (1, 2, 16384),
+                                   # two rows per transform (B >= 2, 1024 < L <= 8192), odd B
+                                   (3, 2, 1025), (2, 1, 2048), (3, 1, 5000), (2, 2, 8192),
+                                   (5, 1, 4096)])
 @pytest.mark.parametrize("bidir", [False, True])
 def test_conv_matches_oracle_toeplitz(B, H, L, bidir):
     rng = np.random.default_rng(B * 7 + H * 11 + L)
