@@ -12,7 +12,7 @@
 //   chunk  S_c = sum_t Lbar^{T-1-t} V_t (end state of chunk c from a zero start)
 //   carry  X_c = Lbar^T X_{c-1} + S_c, sequential over chunks in two-float arithmetic;
 //          stores the state entering each chunk
-//   apply  x_t = Lbar^{t+1} X_in + sum_{s<=t} Lbar^{t-s} V_s, written over V in place
+//   apply  x_t = Lbar^{t+1} X_in + l_t, l_t = Lbar l_{t-1} + V_t, written over V in place
 //   gemm   y = x * [Re C~^T ; -Im C~^T] + D (.) u
 #include "dlr_common.cuh"
 
@@ -157,7 +157,8 @@ s5_chunk_state(S5Work w, int L, int P, int NC) {
   }
 }
 
-// one thread per (b, p): the state entering each chunk, chained in two-float arithmetic
+// one thread per (b, p): the state entering each chunk, chained in two-float arithmetic.
+// The chunk end states do not depend on the chain, so they are fetched eight at a time.
 __global__ void s5_carry(S5Work w, int B, int P, int NC) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= B * P) return;
@@ -165,47 +166,45 @@ __global__ void s5_carry(S5Work w, int B, int P, int NC) {
   const float4 lt = w.lbar_T[p];
   const cff m = {{lt.x, lt.y}, {lt.z, lt.w}};
   cff x = {{0.f, 0.f}, {0.f, 0.f}};
-  for (int c = 0; c < NC; ++c) {
-    const size_t o = ((size_t)b * NC + c) * P + p;
-    w.Xin[o] = make_float2(x.re.hi + x.re.lo, x.im.hi + x.im.lo);
-    float2 s = w.S[o];
-    x = cff_fma(m, x, {{s.x, 0.f}, {s.y, 0.f}});
+  const size_t base = (size_t)b * NC * P + p;
+  for (int c0 = 0; c0 < NC; c0 += 8) {
+    float2 sv[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      sv[q] = (c0 + q < NC) ? w.S[base + (size_t)(c0 + q) * P] : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (c0 + q >= NC) break;
+      w.Xin[base + (size_t)(c0 + q) * P] = make_float2(x.re.hi + x.re.lo, x.im.hi + x.im.lo);
+      x = cff_fma(m, x, {{sv[q].x, 0.f}, {sv[q].y, 0.f}});
+    }
   }
 }
 
-// grid (P / kPB, NC, B): x_t = Lbar^{t+1} X_in + sum_{s<=t} Lbar^{t-s} V_s, in place over V.
+// grid (NC, B), one thread per state p: x_t = Lbar^{t+1} X_in + l_t with the in-chunk part
+// l_t = Lbar l_{t-1} + V_t (l_{-1} = 0) run as a 64-step recurrence, written over V in place.
+// The carried state enters through the directly computed power Lbar^{t+1}; only in-chunk lags
+// go through the float32 product chain (at most 64 roundings).
 __global__ void __launch_bounds__(256)
 s5_chunk_apply(S5Work w, int L, int P, int NC) {
-  __shared__ float2 sV[kT][kPB + 1];
-  __shared__ float2 sPw[kPB][kT + 2];
-  const int pb = blockIdx.x * kPB, c = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x;
+  const int c = blockIdx.x, b = blockIdx.y;
   const int t0 = c * kT;
   const int valid = min(kT, L - t0);
-  for (int e = tid; e < kT * kPB; e += 256) {
-    int t = e / kPB, pl = e % kPB;
-    float2 v = make_float2(0.f, 0.f);
-    if (t < valid)
-      v = *reinterpret_cast<const float2*>(w.xv + ((size_t)b * L + t0 + t) * 2 * P + 2 * (pb + pl));
-    sV[t][pl] = v;
-  }
-  for (int e = tid; e < kPB * (kT + 1); e += 256) {
-    int pl = e / (kT + 1), t = e % (kT + 1);
-    sPw[pl][t] = w.lbar_pw[(size_t)(pb + pl) * (kT + 1) + t];
-  }
-  __syncthreads();
-  const int pl = tid & 31, g = tid >> 5;
-  const float2 xi = w.Xin[((size_t)b * NC + c) * P + pb + pl];
-  const cf xin = {xi.x, xi.y};
-  for (int t = g; t < valid; t += 8) {
-    float2 a = sPw[pl][t + 1];
-    cf acc = cmul({a.x, a.y}, xin);
-    for (int s = 0; s <= t; ++s) {
-      float2 q = sPw[pl][t - s], v = sV[s][pl];
-      acc = cfma({q.x, q.y}, {v.x, v.y}, acc);
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const float2 xi = w.Xin[((size_t)b * NC + c) * P + p];
+    const cf xin = {xi.x, xi.y};
+    const float2* pw = w.lbar_pw + (size_t)p * (kT + 1);
+    const float2 lb = pw[1];
+    const cf lam = {lb.x, lb.y};
+    cf l = {0.f, 0.f};
+    float2* row = reinterpret_cast<float2*>(w.xv + ((size_t)b * L + t0) * 2 * P) + p;
+    for (int t = 0; t < valid; ++t) {
+      const float2 v = row[(size_t)t * P];
+      l = cfma(lam, l, {v.x, v.y});
+      const float2 a = pw[t + 1];
+      const cf x = cfma({a.x, a.y}, xin, l);
+      row[(size_t)t * P] = make_float2(x.re, x.im);
     }
-    *reinterpret_cast<float2*>(w.xv + ((size_t)b * L + t0 + t) * 2 * P + 2 * (pb + pl)) =
-        make_float2(acc.re, acc.im);
   }
 }
 
@@ -267,7 +266,7 @@ static cudaError_t s5_scan_xv(const S5Work& w, int B, int L, int P, cudaStream_t
   dim3 gc(P / kPB, NC, B);
   s5_chunk_state<<<gc, 256, 0, s>>>(w, L, P, NC);
   s5_carry<<<(B * P + 127) / 128, 128, 0, s>>>(w, B, P, NC);
-  s5_chunk_apply<<<gc, 256, 0, s>>>(w, L, P, NC);
+  s5_chunk_apply<<<dim3(NC, B), 256, 0, s>>>(w, L, P, NC);
   return cudaGetLastError();
 }
 

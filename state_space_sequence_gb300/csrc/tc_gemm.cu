@@ -102,35 +102,54 @@ tc_gemm_bf16(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
   }
   __syncwarp();
 
-  // ---- epilogue: all four warps ----
+  // ---- epilogue: all four warps. Each 32-column slice of the accumulator goes TMEM ->
+  // registers (thread = row) -> shared memory (the drained stages) -> row-coalesced float4
+  // stores, with D (.) E added on the way out. ----
   const bool acc_ok = tc::mbar_wait(acc_full, 0);
   tc::fence_after_sync();
-  const int row = m0 + warp * 32 + lane;
+  float* tile = reinterpret_cast<float*>(base);  // [128][33]
   const bool vec = (g.N & 3) == 0;
 #pragma unroll 1
   for (int c = 0; c < kBN / 32; ++c) {
     const int nc = n0 + c * 32;
-    if (nc >= g.N) break;  // warp-uniform
+    if (nc >= g.N) break;  // block-uniform
     float v[32];
     tc::tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c * 32), v);
-    if (row < g.M && acc_ok) {
-      float* crow = g.C + (size_t)row * g.N;
-      if (g.E) {
-        const float* erow = g.E + (size_t)row * g.N;
+    const int r_own = warp * 32 + lane;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (nc + j < g.N) v[j] = fmaf(__ldg(&g.D[nc + j]), __ldg(&erow[nc + j]), v[j]);
-      }
-      if (vec && nc + 32 <= g.N) {
+    for (int j = 0; j < 32; ++j) tile[r_own * 33 + j] = v[j];
+    __syncthreads();
 #pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          *reinterpret_cast<float4*>(crow + nc + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-      } else {
+    for (int it = 0; it < 8; ++it) {
+      const int idx = it * 128 + threadIdx.x;  // 128 rows x 8 float4 per slice
+      const int r = idx >> 3, c4 = (idx & 7) * 4;
+      const int row = m0 + r, col = nc + c4;
+      if (row < g.M && acc_ok) {
+        float o[4] = {tile[r * 33 + c4], tile[r * 33 + c4 + 1], tile[r * 33 + c4 + 2],
+                      tile[r * 33 + c4 + 3]};
+        if (vec && col + 3 < g.N) {
+          if (g.E) {
+            const float4 e = __ldg(reinterpret_cast<const float4*>(g.E + (size_t)row * g.N + col));
+            const float4 d = __ldg(reinterpret_cast<const float4*>(g.D + col));
+            o[0] = fmaf(d.x, e.x, o[0]);
+            o[1] = fmaf(d.y, e.y, o[1]);
+            o[2] = fmaf(d.z, e.z, o[2]);
+            o[3] = fmaf(d.w, e.w, o[3]);
+          }
+          *reinterpret_cast<float4*>(g.C + (size_t)row * g.N + col) =
+              make_float4(o[0], o[1], o[2], o[3]);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (nc + j < g.N) crow[nc + j] = v[j];
+          for (int q = 0; q < 4; ++q)
+            if (col + q < g.N) {
+              float val = o[q];
+              if (g.E) val = fmaf(g.D[col + q], g.E[(size_t)row * g.N + col + q], val);
+              g.C[(size_t)row * g.N + col + q] = val;
+            }
+        }
       }
     }
+    __syncthreads();
   }
   if (!ok || !acc_ok) report_status(g.status, DLR_ERR_TIMEOUT);
   tc::fence_before_sync();
