@@ -164,18 +164,24 @@ def run_ours(args):
 
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
-    def step(evs=None):
+    def step():
         dlr.dlr_kernel(*fwd, L, "re", out=K)
         dlr.dlr_conv_spectrum(K, workspace=ws)
-        if evs is not None:
-            evs[0].record(stream)
         dlr.dlr_conv_apply(u, ws, out=y)
-        if evs is not None:
-            evs[1].record(stream)
 
+    for _ in range(3):  # eager: loads the module, sets kernel attributes
+        step()
+    torch.cuda.synchronize()
+    # The step's four launches are recorded once in a CUDA graph and replayed, so the timing
+    # holds no host-side launch gaps; the dominant kernel is recorded alone for its roofline.
+    g_step, g_apply = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        step()
+    with torch.cuda.graph(g_apply):
+        dlr.dlr_conv_apply(u, ws, out=y)
     for _ in range(args.warmup):
         flush.zero_()
-        step()
+        g_step.replay()
     torch.cuda.synchronize()
     if dlr.device_status() != 0:
         raise RuntimeError("device status non-zero after warm-up")
@@ -188,14 +194,22 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     t_wall0 = time.time()
-    starts, ends, a0s, a1s = [], [], [], []
+    starts, ends = [], []
     for _ in range(args.steps):
         flush.zero_()
-        s, e, a0, a1 = ev(), ev(), ev(), ev()
+        s, e = ev(), ev()
         s.record(stream)
-        step((a0, a1))
+        g_step.replay()
         e.record(stream)
-        starts.append(s), ends.append(e), a0s.append(a0), a1s.append(a1)
+        starts.append(s), ends.append(e)
+    a0s, a1s = [], []
+    for _ in range(min(args.steps, 1000)):
+        flush.zero_()
+        a0, a1 = ev(), ev()
+        a0.record(stream)
+        g_apply.replay()
+        a1.record(stream)
+        a0s.append(a0), a1s.append(a1)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     if dist is not None:
@@ -287,7 +301,8 @@ def run_ours(args):
         "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "L": L, "path": "fft",
                    "cast": "re", "causal": True, "parallelism": f"replicas x{world}",
                    "l2": "flushed before every step (2 x L2 write), flush outside the events",
-                   "step": "dlr_kernel + dlr_conv_spectrum + dlr_conv_apply"},
+                   "step": "dlr_kernel + dlr_conv_spectrum + dlr_conv_apply, replayed as one "
+                           "CUDA graph"},
         "layer_hbm": {"algorithmic_bytes": layer_bytes,
                       "achieved_gbs": layer_bytes / step_avg / 1e9,
                       "frac_of_measured_peak": layer_bytes / step_avg / 1e9 / peak},

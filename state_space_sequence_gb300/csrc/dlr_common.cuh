@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "dlr.h"
 
 namespace dlr {
@@ -111,6 +113,21 @@ __device__ __forceinline__ cff cff_fma(cff a, cff b, cff c) {
 // and clears it.
 __device__ __forceinline__ void report_status(int* status, int code) {
   if (status) atomicMax(status, code);
+}
+
+// Raise a kernel's dynamic shared-memory limit once per device (later launches -- including
+// ones recorded into a CUDA graph -- skip the call).
+template <auto Kernel>
+inline cudaError_t max_smem_once(size_t bytes) {
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
 }
 
 }  // namespace dlr

@@ -22,13 +22,18 @@ namespace {
 using fft::padded;
 using fft::padded_size;
 
-__global__ void twiddle_table(float2* __restrict__ tw, int logn) {
+// tw[m] = exp(-2 pi i m / n) for m < n = 2^logn; when tw2 is given, also the 2n-point table.
+__global__ void twiddle_table(float2* __restrict__ tw, int logn, float2* __restrict__ tw2) {
   const int n = 1 << logn;
-  for (int m = blockIdx.x * blockDim.x + threadIdx.x; m < n; m += gridDim.x * blockDim.x) {
+  const int total = tw2 ? 3 * n : n;
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
+    const bool second = e >= n;
+    const int m = second ? e - n : e;
+    const int lg = second ? logn + 1 : logn;
     float s, c;
-    // 2m/n is exact in float for a power-of-two n: exp(-2 pi i m/n) = cos(pi x) - i sin(pi x)
-    sincospif(ldexpf((float)m, 1 - logn), &s, &c);
-    tw[m] = make_float2(c, -s);
+    // 2m/N is exact in float for a power-of-two N: exp(-2 pi i m/N) = cos(pi x) - i sin(pi x)
+    sincospif(ldexpf((float)m, 1 - lg), &s, &c);
+    (second ? tw2 : tw)[m] = make_float2(c, -s);
   }
 }
 
@@ -475,9 +480,7 @@ cudaError_t launch_pairs(const float* u, int B, int H, int L, float* y, const fl
                          const float2* spec, cudaStream_t s) {
   using PP = PairPlan<kG>;
   if (PP::smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(conv_pairs<kG>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)PP::smem);
+    cudaError_t e = max_smem_once<conv_pairs<kG>>(PP::smem);
     if (e != cudaSuccess) return e;
   }
   const unsigned grid = (unsigned)(((size_t)B + 1) / 2 * H);
@@ -490,11 +493,9 @@ cudaError_t launch_spectrum(const float* K1, const float* K2, int H, int L, floa
                             float2* spec, cudaStream_t s) {
   using P = fftr::Plan<kLog>;
   if (P::smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(conv_spectrum<kLog>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P::smem);
+    cudaError_t e = max_smem_once<conv_spectrum<kLog>>(P::smem);
     if (e != cudaSuccess) return e;
   }
-  twiddle_table<<<(P::n + 255) / 256, 256, 0, s>>>(tw, kLog);
   conv_spectrum<kLog><<<H, P::T, P::smem, s>>>(K1, K2, L, tw, spec);
   return cudaGetLastError();
 }
@@ -504,8 +505,7 @@ cudaError_t launch_apply(const float* u, int B, int H, int L, float* y, const fl
                          const float2* spec, cudaStream_t s) {
   using P = fftr::Plan<kLog>;
   if (P::smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(conv_rows<kLog>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P::smem);
+    cudaError_t e = max_smem_once<conv_rows<kLog>>(P::smem);
     if (e != cudaSuccess) return e;
   }
   conv_rows<kLog><<<(unsigned)((size_t)B * H), P::T, P::smem, s>>>(u, spec, tw, y, H, L);
@@ -564,11 +564,14 @@ cudaError_t launch_dlr_conv_spectrum(const float* K1, const float* K2, int H, in
   ConvWs w = carve_conv(ws, lg);
   if (lg > 14) {  // a cluster of 8 CTAs per channel; local transforms of n / 8 points
     const int lloc = lg - 3;
-    twiddle_table<<<((1 << lloc) + 255) / 256, 256, 0, s>>>(w.tw, lloc);
+    twiddle_table<<<((1 << lloc) + 255) / 256, 256, 0, s>>>(w.tw, lloc, nullptr);
     return launch_cluster_spectrum(K1, K2, H, L, lg, w.tw, w.spec, s);
   }
-  if (lg >= 11 && lg <= 13)  // the two-rows-per-transform kernel also needs the 2n-point table
-    twiddle_table<<<((2 << lg) + 255) / 256, 256, 0, s>>>(w.tw2, lg + 1);
+  // one launch for the n-point table and, where the two-rows-per-transform kernel may run,
+  // the 2n-point table
+  const bool pairs = lg >= 11 && lg <= 13;
+  twiddle_table<<<((pairs ? 3 : 1) * (1 << lg) + 255) / 256, 256, 0, s>>>(w.tw, lg,
+                                                                            pairs ? w.tw2 : nullptr);
 #define SPEC_CALL(G) launch_spectrum<G>(K1, K2, H, L, w.tw, w.spec, s)
   DLR_CONV_SWITCH(SPEC_CALL)
 #undef SPEC_CALL

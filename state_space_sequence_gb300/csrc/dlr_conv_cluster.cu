@@ -293,8 +293,7 @@ cudaError_t launch_cluster(const float* src, const float* src2, int rows, int H,
                            const float2* tw, float2* spec, float* y, cudaStream_t s) {
   using P = fftr::Plan<kLog>;
   const size_t smem = 2 * P::buf_elems * sizeof(float2);
-  cudaError_t e = cudaFuncSetAttribute(conv_cluster<kLog, kSpectrum>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = max_smem_once<conv_cluster<kLog, kSpectrum>>(smem);
   if (e != cudaSuccess) return e;
   conv_cluster<kLog, kSpectrum><<<(unsigned)(rows * kC), P::T, smem, s>>>(src, src2, H, L, tw,
                                                                         spec, y);

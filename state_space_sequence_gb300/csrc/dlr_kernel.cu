@@ -20,7 +20,8 @@ namespace {
 constexpr int kT = 64;         // lags per chunk (t)
 constexpr int kC = 32;         // chunks per CTA (c)
 constexpr int kNB = 32;        // states per shared-memory block
-constexpr int kThreads = 128;  // 16 (t groups of 4) x 8 (c groups of 4)
+constexpr int kGroup = 128;    // threads per state group: 16 (t pairs) x 8 (c groups of 4)
+constexpr int kThreads = 2 * kGroup;  // two groups split the states, then reduce
 
 // p[e] = x^e for e < 8 from p[1] = x, at most three multiplications deep
 __device__ __forceinline__ void small_powers(cf (&p)[8], cf x) {
@@ -34,21 +35,35 @@ __device__ __forceinline__ void small_powers(cf (&p)[8], cf x) {
   p[7] = cmul(p[4], p[3]);
 }
 
+// per state group: A[c][n], Bm[n][t], five evaluations per state, small-power tables
+struct GroupSmem {
+  float2 sA[kC][kNB + 1];
+  float2 sB[kNB][kT];
+  float2 sE[kNB][5];
+  float2 sPw[4][kNB][9];  // lambda^t0, lambda^{8 t1}, lambda^{64 c0}, W lambda^{j0 + 512 c1}
+};
+constexpr size_t kGenSmem = 2 * sizeof(GroupSmem);
+
+// barrier over one state group only (named barriers 1 and 2; 0 is __syncthreads)
+__device__ __forceinline__ void group_sync(int g) {
+  if (g == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
+  else asm volatile("bar.sync 2, 128;" ::: "memory");
+}
+
 template <bool kReIm>
 __global__ void __launch_bounds__(kThreads)
 dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_im,
                const float2* __restrict__ W, int N, int L, float* __restrict__ K) {
-  __shared__ float2 sA[kC][kNB + 1];            // A[c][n]
-  __shared__ __align__(16) float2 sB[kNB][kT];  // Bm[n][t]
-  __shared__ float2 sE[kNB][5];                 // lambda, lambda^8, lambda^64, lambda^512, W lambda^j0
-  __shared__ float2 sPw[4][kNB][9];             // small powers: lambda^t0, lambda^{8 t1}, lambda^{64 c0},
-                                                // W lambda^{j0 + 512 c1}; odd row stride
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  GroupSmem* gs = reinterpret_cast<GroupSmem*>(smem_raw);
 
   const int h = blockIdx.y;
   const int j0 = blockIdx.x * (kT * kC);
-  const int tid = threadIdx.x;
+  const int g = threadIdx.x / kGroup;   // state group: blocks nb = 32 g, 32 g + 64, ...
+  const int tid = threadIdx.x % kGroup;
   const int tx = tid & 15;  // t in {2 tx, 2 tx + 1, 32 + 2 tx, 33 + 2 tx}
   const int ty = tid >> 4;  // c = ty + 8 i, i < 4
+  GroupSmem& S = gs[g];
 
   float acc_re[4][4], acc_im[4][4];
 #pragma unroll
@@ -56,9 +71,9 @@ dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_i
 #pragma unroll
     for (int k = 0; k < 4; ++k) acc_re[i][k] = acc_im[i][k] = 0.f;
 
-  for (int nb = 0; nb < N; nb += kNB) {
+  for (int nb = g * kNB; nb < N; nb += 2 * kNB) {
     // 1) five direct evaluations per state
-    for (int e = tid; e < kNB * 5; e += kThreads) {
+    for (int e = tid; e < kNB * 5; e += kGroup) {
       const int nl = e / 5, which = e % 5, n = nb + nl;
       cf v = {0.f, 0.f};
       if (n < N) {
@@ -70,18 +85,18 @@ dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_i
           v = cmul({w.x, w.y}, lam_pow(p, j0));
         }
       }
-      sE[nl][which] = make_float2(v.re, v.im);
+      S.sE[nl][which] = make_float2(v.re, v.im);
     }
-    __syncthreads();
+    group_sync(g);
     // 2) small powers, one table per thread: (state nl, table part)
     {
       const int nl = tid >> 2, part = tid & 3;
       cf p[8];
       if (part < 3) {
-        const float2 e = sE[nl][part];  // lambda, lambda^8, lambda^64
+        const float2 e = S.sE[nl][part];  // lambda, lambda^8, lambda^64
         small_powers(p, {e.x, e.y});
       } else {
-        const float2 ew = sE[nl][4], e5 = sE[nl][3];
+        const float2 ew = S.sE[nl][4], e5 = S.sE[nl][3];
         const cf s512 = {e5.x, e5.y};
         p[0] = {ew.x, ew.y};
         p[1] = cmul(p[0], s512);
@@ -92,31 +107,31 @@ dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_i
         for (int i = 4; i < 8; ++i) p[i] = {0.f, 0.f};
       }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sPw[part][nl][i] = make_float2(p[i].re, p[i].im);
+      for (int i = 0; i < 8; ++i) S.sPw[part][nl][i] = make_float2(p[i].re, p[i].im);
     }
-    __syncthreads();
+    group_sync(g);
     // 3) expand (consecutive threads write consecutive entries)
-    for (int e = tid; e < kNB * kT; e += kThreads) {
+    for (int e = tid; e < kNB * kT; e += kGroup) {
       const int nl = e >> 6, t = e & 63;
-      const float2 a = sPw[0][nl][t & 7], b = sPw[1][nl][t >> 3];
+      const float2 a = S.sPw[0][nl][t & 7], b = S.sPw[1][nl][t >> 3];
       const cf v = cmul({a.x, a.y}, {b.x, b.y});
-      sB[nl][t] = make_float2(v.re, v.im);
+      S.sB[nl][t] = make_float2(v.re, v.im);
     }
-    for (int e = tid; e < kNB * kC; e += kThreads) {
+    for (int e = tid; e < kNB * kC; e += kGroup) {
       const int c = e >> 5, nl = e & 31;
-      const float2 a = sPw[2][nl][c & 7], b = sPw[3][nl][c >> 3];
+      const float2 a = S.sPw[2][nl][c & 7], b = S.sPw[3][nl][c >> 3];
       const cf v = cmul({a.x, a.y}, {b.x, b.y});
-      sA[c][nl] = make_float2(v.re, v.im);
+      S.sA[c][nl] = make_float2(v.re, v.im);
     }
-    __syncthreads();
+    group_sync(g);
     // 4) register-tiled complex GEMM over this block of states (missing states are zero)
 #pragma unroll 4
     for (int nl = 0; nl < kNB; ++nl) {
       float2 a[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = sA[ty + 8 * i][nl];
-      const float4 b01 = *reinterpret_cast<const float4*>(&sB[nl][2 * tx]);
-      const float4 b23 = *reinterpret_cast<const float4*>(&sB[nl][32 + 2 * tx]);
+      for (int i = 0; i < 4; ++i) a[i] = S.sA[ty + 8 * i][nl];
+      const float4 b01 = *reinterpret_cast<const float4*>(&S.sB[nl][2 * tx]);
+      const float4 b23 = *reinterpret_cast<const float4*>(&S.sB[nl][32 + 2 * tx]);
       const float2 b[4] = {make_float2(b01.x, b01.y), make_float2(b01.z, b01.w),
                            make_float2(b23.x, b23.y), make_float2(b23.z, b23.w)};
 #pragma unroll
@@ -127,10 +142,32 @@ dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_i
           if (kReIm) acc_im[i][k] = fmaf(a[i].x, b[k].y, fmaf(a[i].y, b[k].x, acc_im[i][k]));
         }
     }
-    __syncthreads();
+    group_sync(g);
   }
 
-  // 5) store: row h, j = j0 + c T + t for t in {2 tx, 2 tx + 1} and {32 + 2 tx, 33 + 2 tx}
+  // 5) the second group hands its partial sums to the first through shared memory
+  __syncthreads();
+  float* red = reinterpret_cast<float*>(&gs[1].sB[0][0]);  // 128 threads x 32 floats
+  if (g == 1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        red[(i * 4 + k) * kGroup + tid] = acc_re[i][k];
+        if (kReIm) red[(16 + i * 4 + k) * kGroup + tid] = acc_im[i][k];
+      }
+  }
+  __syncthreads();
+  if (g == 1) return;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      acc_re[i][k] += red[(i * 4 + k) * kGroup + tid];
+      if (kReIm) acc_im[i][k] += red[(16 + i * 4 + k) * kGroup + tid];
+    }
+
+  // 6) store: row h, j = j0 + c T + t for t in {2 tx, 2 tx + 1} and {32 + 2 tx, 33 + 2 tx}
   float* krow = K + (size_t)h * L;
   const bool vec = ((L & 1) == 0);
 #pragma unroll
@@ -157,12 +194,19 @@ dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_i
 cudaError_t launch_dlr_kernel(const float* log_re, const float* log_im, const float* W, int H,
                               int N, int L, bool re_im, float* K, cudaStream_t s) {
   dim3 grid((L + kT * kC - 1) / (kT * kC), H);
-  if (re_im)
-    dlr_kernel_gen<true><<<grid, kThreads, 0, s>>>(log_re, log_im,
-                                                   reinterpret_cast<const float2*>(W), N, L, K);
-  else
-    dlr_kernel_gen<false><<<grid, kThreads, 0, s>>>(log_re, log_im,
-                                                    reinterpret_cast<const float2*>(W), N, L, K);
+  const int smem = (int)kGenSmem;
+  cudaError_t e;
+  if (re_im) {
+    e = max_smem_once<dlr_kernel_gen<true>>(kGenSmem);
+    if (e != cudaSuccess) return e;
+    dlr_kernel_gen<true><<<grid, kThreads, smem, s>>>(log_re, log_im,
+                                                      reinterpret_cast<const float2*>(W), N, L, K);
+  } else {
+    e = max_smem_once<dlr_kernel_gen<false>>(kGenSmem);
+    if (e != cudaSuccess) return e;
+    dlr_kernel_gen<false><<<grid, kThreads, smem, s>>>(log_re, log_im,
+                                                       reinterpret_cast<const float2*>(W), N, L, K);
+  }
   return cudaGetLastError();
 }
 

@@ -229,8 +229,7 @@ template <int kNT, bool kRev>
 cudaError_t launch_scan(const float* u, const float* lr, const float* li, const float* W, int B,
                         int H, int N, int L, float* y, cudaStream_t s) {
   const size_t smem = ScanSmem<kNT>::bytes;
-  cudaError_t e = cudaFuncSetAttribute(dlr_scan_rows<kNT, kRev>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = max_smem_once<dlr_scan_rows<kNT, kRev>>(smem);
   if (e != cudaSuccess) return e;
   dlr_scan_rows<kNT, kRev><<<(unsigned)((size_t)B * H), kThreads, smem, s>>>(
       u, lr, li, reinterpret_cast<const float2*>(W), H, N, L, y);

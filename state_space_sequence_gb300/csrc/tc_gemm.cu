@@ -249,8 +249,7 @@ cudaError_t launch_tc_gemm(const void* A, const void* B, float* C, int M, int N,
   CUtensorMap ma, mb;
   if (!make_map(&ma, A, (uint64_t)M, (uint64_t)K, kBM)) return cudaErrorInvalidValue;
   if (!make_map(&mb, B, (uint64_t)N, (uint64_t)K, kBN)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
+  cudaError_t e = max_smem_once<tc_gemm_bf16>(kSmemBytes);
   if (e != cudaSuccess) return e;
   GemmArgs g{M, N, K, C, D, E, status};
   dim3 grid((M + kBM - 1) / kBM, (N + kBN - 1) / kBN);
