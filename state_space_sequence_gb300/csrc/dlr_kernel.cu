@@ -19,7 +19,6 @@ namespace {
 
 constexpr int kT = 64;         // lags per chunk (t)
 constexpr int kC = 32;         // chunks per CTA (c)
-constexpr int kNB = 32;        // states per shared-memory block
 constexpr int kGroup = 128;    // threads per state group: 16 (t pairs) x 8 (c groups of 4)
 constexpr int kThreads = 2 * kGroup;  // two groups split the states, then reduce
 
@@ -35,14 +34,18 @@ __device__ __forceinline__ void small_powers(cf (&p)[8], cf x) {
   p[7] = cmul(p[4], p[3]);
 }
 
-// per state group: A[c][n], Bm[n][t], five evaluations per state, small-power tables
+// per state group: A[c][n], Bm[n][t], five evaluations per state, small-power tables, for
+// blocks of kNB states (16 keeps up to six CTAs per SM for small N, so the whole grid of the
+// usual shapes runs in one wave; 32 amortises the per-block work better when N is large)
+template <int kNB>
 struct GroupSmem {
   float2 sA[kC][kNB + 1];
   float2 sB[kNB][kT];
   float2 sE[kNB][5];
   float2 sPw[4][kNB][9];  // lambda^t0, lambda^{8 t1}, lambda^{64 c0}, W lambda^{j0 + 512 c1}
 };
-constexpr size_t kGenSmem = 2 * sizeof(GroupSmem);
+template <int kNB>
+constexpr size_t gen_smem() { return 2 * sizeof(GroupSmem<kNB>); }
 
 // barrier over one state group only (named barriers 1 and 2; 0 is __syncthreads)
 __device__ __forceinline__ void group_sync(int g) {
@@ -50,12 +53,13 @@ __device__ __forceinline__ void group_sync(int g) {
   else asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 
-template <bool kReIm>
+template <bool kReIm, int kNB>
 __global__ void __launch_bounds__(kThreads)
 dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_im,
                const float2* __restrict__ W, int N, int L, float* __restrict__ K) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  GroupSmem* gs = reinterpret_cast<GroupSmem*>(smem_raw);
+  using GS = GroupSmem<kNB>;
+  GS* gs = reinterpret_cast<GS*>(smem_raw);
 
   const int h = blockIdx.y;
   const int j0 = blockIdx.x * (kT * kC);
@@ -63,7 +67,7 @@ dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_i
   const int tid = threadIdx.x % kGroup;
   const int tx = tid & 15;  // t in {2 tx, 2 tx + 1, 32 + 2 tx, 33 + 2 tx}
   const int ty = tid >> 4;  // c = ty + 8 i, i < 4
-  GroupSmem& S = gs[g];
+  GS& S = gs[g];
 
   float acc_re[4][4], acc_im[4][4];
 #pragma unroll
@@ -89,7 +93,7 @@ dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_i
     }
     group_sync(g);
     // 2) small powers, one table per thread: (state nl, table part)
-    {
+    if (tid < 4 * kNB) {
       const int nl = tid >> 2, part = tid & 3;
       cf p[8];
       if (part < 3) {
@@ -112,13 +116,13 @@ dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_i
     group_sync(g);
     // 3) expand (consecutive threads write consecutive entries)
     for (int e = tid; e < kNB * kT; e += kGroup) {
-      const int nl = e >> 6, t = e & 63;
+      const int nl = e / kT, t = e % kT;
       const float2 a = S.sPw[0][nl][t & 7], b = S.sPw[1][nl][t >> 3];
       const cf v = cmul({a.x, a.y}, {b.x, b.y});
       S.sB[nl][t] = make_float2(v.re, v.im);
     }
     for (int e = tid; e < kNB * kC; e += kGroup) {
-      const int c = e >> 5, nl = e & 31;
+      const int c = e / kNB, nl = e % kNB;
       const float2 a = S.sPw[2][nl][c & 7], b = S.sPw[3][nl][c >> 3];
       const cf v = cmul({a.x, a.y}, {b.x, b.y});
       S.sA[c][nl] = make_float2(v.re, v.im);
@@ -147,7 +151,8 @@ dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_i
 
   // 5) the second group hands its partial sums to the first through shared memory
   __syncthreads();
-  float* red = reinterpret_cast<float*>(&gs[1].sB[0][0]);  // 128 threads x 32 floats
+  float* red = reinterpret_cast<float*>(&gs[1]);  // 128 threads x 32 floats
+  static_assert(sizeof(GS) >= sizeof(float) * 32 * kGroup, "reduction scratch");
   if (g == 1) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -189,25 +194,27 @@ dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_i
   }
 }
 
+template <bool kReIm, int kNB>
+cudaError_t launch_gen(const float* log_re, const float* log_im, const float* W, int H, int N,
+                       int L, float* K, cudaStream_t s) {
+  dim3 grid((L + kT * kC - 1) / (kT * kC), H);
+  cudaError_t e = max_smem_once<dlr_kernel_gen<kReIm, kNB>>(gen_smem<kNB>());
+  if (e != cudaSuccess) return e;
+  dlr_kernel_gen<kReIm, kNB><<<grid, kThreads, gen_smem<kNB>(), s>>>(
+      log_re, log_im, reinterpret_cast<const float2*>(W), N, L, K);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_dlr_kernel(const float* log_re, const float* log_im, const float* W, int H,
                               int N, int L, bool re_im, float* K, cudaStream_t s) {
-  dim3 grid((L + kT * kC - 1) / (kT * kC), H);
-  const int smem = (int)kGenSmem;
-  cudaError_t e;
-  if (re_im) {
-    e = max_smem_once<dlr_kernel_gen<true>>(kGenSmem);
-    if (e != cudaSuccess) return e;
-    dlr_kernel_gen<true><<<grid, kThreads, smem, s>>>(log_re, log_im,
-                                                      reinterpret_cast<const float2*>(W), N, L, K);
-  } else {
-    e = max_smem_once<dlr_kernel_gen<false>>(kGenSmem);
-    if (e != cudaSuccess) return e;
-    dlr_kernel_gen<false><<<grid, kThreads, smem, s>>>(log_re, log_im,
-                                                       reinterpret_cast<const float2*>(W), N, L, K);
-  }
-  return cudaGetLastError();
+  const bool big = N >= 256;
+  if (re_im)
+    return big ? launch_gen<true, 32>(log_re, log_im, W, H, N, L, K, s)
+               : launch_gen<true, 16>(log_re, log_im, W, H, N, L, K, s);
+  return big ? launch_gen<false, 32>(log_re, log_im, W, H, N, L, K, s)
+             : launch_gen<false, 16>(log_re, log_im, W, H, N, L, K, s);
 }
 
 }  // namespace dlr
