@@ -278,7 +278,7 @@ def run_ours(args):
     if os.path.exists(PROFILE_TRAFFIC):
         with open(PROFILE_TRAFFIC) as fh:
             prof = json.load(fh)
-        entry = prof.get("conv_rows")
+        entry = prof.get("conv_pairs")
         if entry and entry.get("source_hash") == source_hash(CONV_SOURCES):
             traffic = entry.get("dram_bytes_per_launch")
     layer_bytes = 4 * B * H * L * 2 + 4 * H * N * 4  # u + y + (log_re, log_im, W)
@@ -306,7 +306,7 @@ def run_ours(args):
         "layer_hbm": {"algorithmic_bytes": layer_bytes,
                       "achieved_gbs": layer_bytes / step_avg / 1e9,
                       "frac_of_measured_peak": layer_bytes / step_avg / 1e9 / peak},
-        "roofline": {"kernel": "conv_rows (dlr_conv_apply)", "bound": "alu",
+        "roofline": {"kernel": "conv_pairs (dlr_conv_apply)", "bound": "alu",
                      "achieved": achieved_tflops, "peak": peak_tflops,
                      "peak_kind": f"derived: {sm_count} SMs x 128 FP32 lanes x 2 x {sm_mhz:.0f} MHz",
                      "unit": "TFLOP/s", "frac": achieved_tflops / peak_tflops,

@@ -32,7 +32,7 @@ namespace {
 
 // 16 MiB: room for the twiddle tables and the spectra of H channels at length L as long as
 // 24 * n + 8 * H * (n + 1) bytes fit (n = next power of two >= L, the twiddle parts rounded up
-// to 256 bytes): up to H = 510 channels at L = 4096, up to H = 126 at L = 16384.
+// to 256 bytes): up to H = 508 channels at L = 4096, up to H = 124 at L = 16384.
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 
 static __device__ __align__(256) unsigned char g_conv_scratch[kNoAllocScratchBytes];
