@@ -53,6 +53,13 @@ typedef enum { DLR_CAUSAL = 0, DLR_BIDIR = 1 } dlr_dir;
 /* Precision tier of s5_layer's projections. */
 typedef enum { DLR_FP32 = 0, DLR_BF16_TC = 1 } dlr_prec;
 
+/* Kernels behind dlr_scan_ex. DLR_SCAN_FP32: every product in float32 FMA (N <= 128).
+ * DLR_SCAN_TENSOR: the chunked scan's three dense contractions on tensor cores, each operand
+ * split into two float16 halves with power-of-two scaling (three MMAs per product, float32
+ * accumulation), the carries between chunks in float32 (N <= 64). DLR_SCAN_AUTO: TENSOR
+ * when N <= 64, else FP32. */
+typedef enum { DLR_SCAN_AUTO = 0, DLR_SCAN_FP32 = 1, DLR_SCAN_TENSOR = 2 } dlr_scan_algo;
+
 /*
  * dlr_kernel -- the DLR convolution kernel (DLR paper section 2, Eq. 3/4 and section 2.2):
  *   lambda_{h,n} = exp(-log_re[h,n]^2 + i*log_im[h,n])
@@ -130,6 +137,7 @@ dlr_status dlr_conv_noalloc(const float* u, const float* K_fwd, const float* K_b
  * computed per (b,h) row without materialising the kernel. With dir = DLR_BIDIR the second
  * parameter set (log_re2, log_im2, W2) runs on the reversed sequence and its output is added.
  * Only the Re cast exists here (DLR-prod has no N-state recurrence; use dlr_conv).
+ * Runs the tensor-core kernel of dlr_scan_ex when N <= 64, the float32 one otherwise.
  * u, y: [B, H, L]; parameter layouts as in dlr_kernel. No workspace. u and y must not
  * overlap. Limits: 1 <= N <= 128, 1 <= L < 2^24.
  */
@@ -137,6 +145,20 @@ dlr_status dlr_scan(const float* u, const float* log_re, const float* log_im, co
                     const float* log_re2, const float* log_im2, const float* W2, dlr_dir dir,
                     int64_t B, int64_t H, int64_t N, int64_t L, float* y,
                     dlr_stream_t stream);
+
+/*
+ * dlr_scan_ex -- dlr_scan with the kernel chosen by `algo` (dlr_scan is DLR_SCAN_AUTO).
+ * DLR_SCAN_TENSOR computes, per channel and chunk of 64 steps, the chunk-end states, the
+ * in-chunk Toeplitz product with the first 64 kernel taps and the carried-state output as
+ * tensor-core contractions, and runs the carry recurrence across chunks in float32 (S5 paper
+ * section 2.2; the chunked form of the DLR recurrence). Same arguments, layouts and limits as
+ * dlr_scan, except N <= 64 for DLR_SCAN_TENSOR (DLR_ERR_UNSUPPORTED above). Faults of its
+ * bounded waits are reported through dlr_get_device_status().
+ */
+dlr_status dlr_scan_ex(const float* u, const float* log_re, const float* log_im, const float* W,
+                       const float* log_re2, const float* log_im2, const float* W2, dlr_dir dir,
+                       int64_t B, int64_t H, int64_t N, int64_t L, float* y,
+                       dlr_scan_algo algo, dlr_stream_t stream);
 
 /*
  * s5_layer -- S5 SSM outputs (S5 paper section 3: diagonalised MIMO system; zero-order hold

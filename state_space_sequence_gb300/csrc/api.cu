@@ -16,6 +16,10 @@ cudaError_t launch_dlr_conv_apply(const float* u, int B, int H, int L, float* y,
 cudaError_t launch_dlr_scan(const float* u, const float* lr, const float* li, const float* W,
                             const float* lr2, const float* li2, const float* W2, bool bidir,
                             int B, int H, int N, int L, float* y, cudaStream_t s);
+cudaError_t launch_dlr_scan_tc(const float* u, const float* lr, const float* li, const float* W,
+                               const float* lr2, const float* li2, const float* W2, bool bidir,
+                               int B, int H, int N, int L, float* y, int* status,
+                               cudaStream_t s);
 size_t s5_workspace_bytes(int64_t B, int64_t L, int64_t H, int64_t P, bool bf16);
 cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delta,
                       const float* Bt, const float* Ct, const float* D, int B, int L, int H, int P,
@@ -146,7 +150,17 @@ dlr_status dlr_scan(const float* u, const float* log_re, const float* log_im, co
                     const float* log_re2, const float* log_im2, const float* W2, dlr_dir dir,
                     int64_t B, int64_t H, int64_t N, int64_t L, float* y,
                     dlr_stream_t stream) {
+  return dlr_scan_ex(u, log_re, log_im, W, log_re2, log_im2, W2, dir, B, H, N, L, y,
+                     DLR_SCAN_AUTO, stream);
+}
+
+dlr_status dlr_scan_ex(const float* u, const float* log_re, const float* log_im, const float* W,
+                       const float* log_re2, const float* log_im2, const float* W2, dlr_dir dir,
+                       int64_t B, int64_t H, int64_t N, int64_t L, float* y,
+                       dlr_scan_algo algo, dlr_stream_t stream) {
   if (B < 1 || H < 1 || N < 1 || L < 1) return DLR_ERR_INVALID_ARG;
+  if (algo != DLR_SCAN_AUTO && algo != DLR_SCAN_FP32 && algo != DLR_SCAN_TENSOR)
+    return DLR_ERR_INVALID_ARG;
   if (dir != DLR_CAUSAL && dir != DLR_BIDIR) return DLR_ERR_INVALID_ARG;
   if (!u || !y || !aligned16(u) || !aligned16(y)) return DLR_ERR_INVALID_ARG;
   dlr_status st = check_params(log_re, log_im, W);
@@ -158,6 +172,11 @@ dlr_status dlr_scan(const float* u, const float* log_re, const float* log_im, co
   const size_t bytes = sizeof(float) * (size_t)B * (size_t)H * (size_t)L;
   if (ranges_overlap(u, bytes, y, bytes)) return DLR_ERR_INVALID_ARG;
   if (N > 128 || L > kMaxL || B * H > kMaxGrid) return DLR_ERR_UNSUPPORTED;
+  if (algo == DLR_SCAN_TENSOR && N > 64) return DLR_ERR_UNSUPPORTED;
+  if (algo == DLR_SCAN_TENSOR || (algo == DLR_SCAN_AUTO && N <= 64))
+    return from_cuda(dlr::launch_dlr_scan_tc(u, log_re, log_im, W, log_re2, log_im2, W2,
+                                             dir == DLR_BIDIR, (int)B, (int)H, (int)N, (int)L,
+                                             y, status_word(), (cudaStream_t)stream));
   return from_cuda(dlr::launch_dlr_scan(u, log_re, log_im, W, log_re2, log_im2, W2,
                                         dir == DLR_BIDIR, (int)B, (int)H, (int)N, (int)L, y,
                                         (cudaStream_t)stream));

@@ -95,7 +95,7 @@ tc_gemm_bf16(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
       const uint64_t bd = tc::smem_desc_k_sw128(a + kABytes);
 #pragma unroll
       for (int kk = 0; kk < kBK / 16; ++kk)  // advance 16 bf16 = 32 bytes = 2 descriptor units
-        tc::mma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+        tc::mma_kind_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
       tc::mma_commit(&empty[s]);
     }
     tc::mma_commit(acc_full);

@@ -48,6 +48,8 @@ def _load():
         lib.dlr_conv_apply.restype = i32
         lib.dlr_scan.argtypes = [P, P, P, P, P, P, P, i32, i64, i64, i64, i64, P, P]
         lib.dlr_scan.restype = i32
+        lib.dlr_scan_ex.argtypes = [P, P, P, P, P, P, P, i32, i64, i64, i64, i64, P, i32, P]
+        lib.dlr_scan_ex.restype = i32
         lib.s5_workspace_size.argtypes = [i64, i64, i64, i64, i32]
         lib.s5_workspace_size.restype = sz
         lib.s5_layer.argtypes = [P, P, P, P, P, P, i64, i64, i64, i64, i32, P, P, sz, P]
@@ -154,8 +156,13 @@ def dlr_conv_apply(u, workspace, out=None, stream=None):
     return out
 
 
-def dlr_scan(u, fwd, bwd=None, out=None, stream=None):
-    """DLR recurrence (Re cast) as a chunked scan; ``fwd``/``bwd`` = (log_re, log_im, W)."""
+SCAN_ALGO = {"auto": 0, "fp32": 1, "tensor": 2}
+
+
+def dlr_scan(u, fwd, bwd=None, out=None, stream=None, algo: str = "auto"):
+    """DLR recurrence (Re cast) as a chunked scan; ``fwd``/``bwd`` = (log_re, log_im, W).
+    ``algo``: "fp32" (float32 FMA kernel), "tensor" (tensor-core contractions, N <= 64) or
+    "auto" (tensor when N <= 64)."""
     _check_f32(u)
     B, H, L = u.shape
     lr, li, W = _params(fwd)
@@ -166,9 +173,9 @@ def dlr_scan(u, fwd, bwd=None, out=None, stream=None):
     if out is None:
         out = torch.empty_like(u)
     _check_f32(out)
-    _ok("dlr_scan", _load().dlr_scan(_ptr(u), _ptr(lr), _ptr(li), _ptr(W), _ptr(lr2), _ptr(li2),
-                                     _ptr(W2), 1 if bwd is not None else 0, B, H, N, L,
-                                     _ptr(out), _stream(stream)))
+    _ok("dlr_scan", _load().dlr_scan_ex(_ptr(u), _ptr(lr), _ptr(li), _ptr(W), _ptr(lr2),
+                                        _ptr(li2), _ptr(W2), 1 if bwd is not None else 0, B, H,
+                                        N, L, _ptr(out), SCAN_ALGO[algo], _stream(stream)))
     return out
 
 

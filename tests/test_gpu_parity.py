@@ -111,13 +111,47 @@ def test_conv_long_rows_cluster_path(B, H, L, bidir):
                                      (2, 2, 16, 65), (1, 2, 64, 4095), (1, 2, 64, 4097),
                                      (2, 1, 65, 1000), (1, 2, 128, 5000), (1, 1, 64, 12289)])
 @pytest.mark.parametrize("bidir", [False, True])
-def test_scan_matches_oracle(B, H, N, L, bidir):
+@pytest.mark.parametrize("algo", ["fp32", "tensor"])
+def test_scan_matches_oracle(B, H, N, L, bidir, algo):
+    if algo == "tensor" and N > 64:
+        pytest.skip("the tensor-core scan holds at most 64 states")
     w = inputs.make_dlr(B, H, N, L, seed=B + 10 * H + 100 * N + L, bidir=bidir,
                         unit_channels=1)
     bwd_d = params_dev(w.bwd) if bidir else None
-    y = host(dlr.dlr_scan(dev(w.u), params_dev(w.fwd), bwd_d))
+    y = host(dlr.dlr_scan(dev(w.u), params_dev(w.fwd), bwd_d, algo=algo))
     ref = oracle.dlr_layer(w.u, params_np(w.fwd), params_np(w.bwd) if bidir else None)
     assert oracle.rel_l2(y, ref) <= TOL
+    check_status()
+
+
+@pytest.mark.parametrize("B,H,N,L", [(5, 3, 64, 256), (3, 2, 40, 3000), (9, 2, 64, 8192),
+                                     (2, 2, 64, 8193), (1, 3, 64, 30000), (2, 1, 8, 100)])
+@pytest.mark.parametrize("bidir", [False, True])
+def test_tensor_scan_tile_layouts(B, H, N, L, bidir):
+    """Tensor-core scan: several rows packed in one tile (L <= 8192: floor(128 / chunks) rows
+    per tile, ragged last tile), rows that walk several tiles with their state carried
+    (L > 8192), ragged last chunks, N < 64 (zero state rows)."""
+    w = inputs.make_dlr(B, H, N, L, seed=7 * B + 11 * H + N + L, bidir=bidir, unit_channels=1)
+    bwd_d = params_dev(w.bwd) if bidir else None
+    y = host(dlr.dlr_scan(dev(w.u), params_dev(w.fwd), bwd_d, algo="tensor"))
+    ref = oracle.dlr_layer(w.u, params_np(w.fwd), params_np(w.bwd) if bidir else None)
+    assert oracle.rel_l2(y, ref) <= TOL
+    check_status()
+
+
+def test_tensor_scan_input_scaling_extremes():
+    """Per-chunk power-of-two scaling of u before the f16 split: rows of very different
+    magnitude (1e-30 .. 1e30) and exactly zero chunks stay within the tolerance row by row."""
+    B, H, N, L = 4, 2, 64, 4096
+    w = inputs.make_dlr(B, H, N, L, seed=99, unit_channels=1)
+    u = w.u.copy()
+    u[0] *= 1e-30
+    u[1] *= 1e30
+    u[2, :, 1024:2048] = 0.0
+    y = host(dlr.dlr_scan(dev(u), params_dev(w.fwd), algo="tensor"))
+    ref = oracle.dlr_layer(u, params_np(w.fwd))
+    for b in range(B):
+        assert oracle.rel_l2(y[b], ref[b]) <= TOL, b
     check_status()
 
 
