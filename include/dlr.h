@@ -137,28 +137,34 @@ dlr_status dlr_conv_noalloc(const float* u, const float* K_fwd, const float* K_b
  * computed per (b,h) row without materialising the kernel. With dir = DLR_BIDIR the second
  * parameter set (log_re2, log_im2, W2) runs on the reversed sequence and its output is added.
  * Only the Re cast exists here (DLR-prod has no N-state recurrence; use dlr_conv).
- * Runs the tensor-core kernel of dlr_scan_ex when N <= 64, the float32 one otherwise.
- * u, y: [B, H, L]; parameter layouts as in dlr_kernel. No workspace. u and y must not
- * overlap. Limits: 1 <= N <= 128, 1 <= L < 2^24.
+ * u, y: [B, H, L]; parameter layouts as in dlr_kernel. u and y must not overlap.
+ * Runs the tensor-core kernel of dlr_scan_ex when N <= 64 (it needs `workspace` of at least
+ * dlr_scan_workspace_size(B, H, N, L) bytes, else DLR_ERR_WORKSPACE), the float32 one
+ * otherwise (workspace unused, may be NULL). Limits: 1 <= N <= 128, 1 <= L < 2^24.
  */
+size_t dlr_scan_workspace_size(int64_t B, int64_t H, int64_t N, int64_t L);
 dlr_status dlr_scan(const float* u, const float* log_re, const float* log_im, const float* W,
                     const float* log_re2, const float* log_im2, const float* W2, dlr_dir dir,
-                    int64_t B, int64_t H, int64_t N, int64_t L, float* y,
-                    dlr_stream_t stream);
+                    int64_t B, int64_t H, int64_t N, int64_t L, float* y, void* workspace,
+                    size_t workspace_bytes, dlr_stream_t stream);
 
 /*
  * dlr_scan_ex -- dlr_scan with the kernel chosen by `algo` (dlr_scan is DLR_SCAN_AUTO).
  * DLR_SCAN_TENSOR computes, per channel and chunk of 64 steps, the chunk-end states, the
  * in-chunk Toeplitz product with the first 64 kernel taps and the carried-state output as
  * tensor-core contractions, and runs the carry recurrence across chunks in float32 (S5 paper
- * section 2.2; the chunked form of the DLR recurrence). Same arguments, layouts and limits as
- * dlr_scan, except N <= 64 for DLR_SCAN_TENSOR (DLR_ERR_UNSUPPORTED above). Faults of its
- * bounded waits are reported through dlr_get_device_status().
+ * section 2.2; the chunked form of the DLR recurrence). A first kernel writes each channel's
+ * tables (powers of lambda, the taps, the operand images) into `workspace`
+ * (dlr_scan_workspace_size bytes: about 83 KB per channel). Same arguments, layouts and limits
+ * as dlr_scan, except N <= 64 for DLR_SCAN_TENSOR (DLR_ERR_UNSUPPORTED above). Faults of its
+ * bounded waits are reported through dlr_get_device_status(). DLR_SCAN_FP32 needs no
+ * workspace.
  */
 dlr_status dlr_scan_ex(const float* u, const float* log_re, const float* log_im, const float* W,
                        const float* log_re2, const float* log_im2, const float* W2, dlr_dir dir,
                        int64_t B, int64_t H, int64_t N, int64_t L, float* y,
-                       dlr_scan_algo algo, dlr_stream_t stream);
+                       dlr_scan_algo algo, void* workspace, size_t workspace_bytes,
+                       dlr_stream_t stream);
 
 /*
  * s5_layer -- S5 SSM outputs (S5 paper section 3: diagonalised MIMO system; zero-order hold

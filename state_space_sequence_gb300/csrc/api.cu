@@ -16,9 +16,10 @@ cudaError_t launch_dlr_conv_apply(const float* u, int B, int H, int L, float* y,
 cudaError_t launch_dlr_scan(const float* u, const float* lr, const float* li, const float* W,
                             const float* lr2, const float* li2, const float* W2, bool bidir,
                             int B, int H, int N, int L, float* y, cudaStream_t s);
+size_t scan_tc_workspace_bytes(int64_t H);
 cudaError_t launch_dlr_scan_tc(const float* u, const float* lr, const float* li, const float* W,
                                const float* lr2, const float* li2, const float* W2, bool bidir,
-                               int B, int H, int N, int L, float* y, int* status,
+                               int B, int H, int N, int L, float* y, void* ws, int* status,
                                cudaStream_t s);
 size_t s5_workspace_bytes(int64_t B, int64_t L, int64_t H, int64_t P, bool bf16);
 cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delta,
@@ -61,7 +62,7 @@ dlr_status check_params(const float* log_re, const float* log_im, const float* W
 
 extern "C" {
 
-int dlr_abi_version(void) { return 1; }
+int dlr_abi_version(void) { return 2; }
 
 const char* dlr_status_string(dlr_status s) {
   switch (s) {
@@ -146,18 +147,24 @@ dlr_status dlr_conv(const float* u, const float* K_fwd, const float* K_bwd, dlr_
   return dlr_conv_apply(u, B, H, L, y, workspace, workspace_bytes, stream);
 }
 
+size_t dlr_scan_workspace_size(int64_t B, int64_t H, int64_t N, int64_t L) {
+  if (B < 1 || H < 1 || N < 1 || L < 1 || N > 64) return 0;
+  return dlr::scan_tc_workspace_bytes(H);
+}
+
 dlr_status dlr_scan(const float* u, const float* log_re, const float* log_im, const float* W,
                     const float* log_re2, const float* log_im2, const float* W2, dlr_dir dir,
-                    int64_t B, int64_t H, int64_t N, int64_t L, float* y,
-                    dlr_stream_t stream) {
+                    int64_t B, int64_t H, int64_t N, int64_t L, float* y, void* workspace,
+                    size_t workspace_bytes, dlr_stream_t stream) {
   return dlr_scan_ex(u, log_re, log_im, W, log_re2, log_im2, W2, dir, B, H, N, L, y,
-                     DLR_SCAN_AUTO, stream);
+                     DLR_SCAN_AUTO, workspace, workspace_bytes, stream);
 }
 
 dlr_status dlr_scan_ex(const float* u, const float* log_re, const float* log_im, const float* W,
                        const float* log_re2, const float* log_im2, const float* W2, dlr_dir dir,
                        int64_t B, int64_t H, int64_t N, int64_t L, float* y,
-                       dlr_scan_algo algo, dlr_stream_t stream) {
+                       dlr_scan_algo algo, void* workspace, size_t workspace_bytes,
+                       dlr_stream_t stream) {
   if (B < 1 || H < 1 || N < 1 || L < 1) return DLR_ERR_INVALID_ARG;
   if (algo != DLR_SCAN_AUTO && algo != DLR_SCAN_FP32 && algo != DLR_SCAN_TENSOR)
     return DLR_ERR_INVALID_ARG;
@@ -173,10 +180,16 @@ dlr_status dlr_scan_ex(const float* u, const float* log_re, const float* log_im,
   if (ranges_overlap(u, bytes, y, bytes)) return DLR_ERR_INVALID_ARG;
   if (N > 128 || L > kMaxL || B * H > kMaxGrid) return DLR_ERR_UNSUPPORTED;
   if (algo == DLR_SCAN_TENSOR && N > 64) return DLR_ERR_UNSUPPORTED;
-  if (algo == DLR_SCAN_TENSOR || (algo == DLR_SCAN_AUTO && N <= 64))
+  const bool tensor = algo == DLR_SCAN_TENSOR || (algo == DLR_SCAN_AUTO && N <= 64);
+  if (tensor) {
+    const size_t need = dlr::scan_tc_workspace_bytes(H);
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DLR_ERR_WORKSPACE;
+    if (ranges_overlap(workspace, need, u, bytes) || ranges_overlap(workspace, need, y, bytes))
+      return DLR_ERR_INVALID_ARG;
     return from_cuda(dlr::launch_dlr_scan_tc(u, log_re, log_im, W, log_re2, log_im2, W2,
                                              dir == DLR_BIDIR, (int)B, (int)H, (int)N, (int)L,
-                                             y, status_word(), (cudaStream_t)stream));
+                                             y, workspace, status_word(), (cudaStream_t)stream));
+  }
   return from_cuda(dlr::launch_dlr_scan(u, log_re, log_im, W, log_re2, log_im2, W2,
                                         dir == DLR_BIDIR, (int)B, (int)H, (int)N, (int)L, y,
                                         (cudaStream_t)stream));

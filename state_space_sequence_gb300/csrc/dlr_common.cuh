@@ -25,20 +25,28 @@ __device__ __forceinline__ cf cfma(cf a, cf b, cf c) {
 }
 
 // Per-state parameters prepared once: a2 = (log Lambda)_re^2 and the phase theta / pi reduced
-// to (-1, 1] and split into float hi + lo (the reduction is done in double: one per state).
+// to about [-1, 1] and split into float hi + lo.
 struct lam_param {
   float a2;
   float th_hi, th_lo;  // theta / pi = th_hi + th_lo (mod 2)
 };
 
+// theta / pi in two-float arithmetic (no double precision, which is slow on this GPU):
+// 1/pi = kInvPiHi + kInvPiLo (float hi part, then the float rounding of the remainder), so
+// theta * kInvPiHi = p + e exactly (e from fmaf) and theta * kInvPiLo adds the next ~24 bits;
+// p - 2 round(p / 2) is exact (both are multiples of ulp(p), difference at most 1 in
+// magnitude). The result is theta / pi mod 2 to about 2^-45 relative to |theta / pi|.
 __device__ __forceinline__ lam_param make_lam_param(float log_re, float log_im) {
+  constexpr float kInvPiHi = 0.318309873f;        // float nearest to 1/pi
+  constexpr float kInvPiLo = 1.28412765e-08f;     // float nearest to 1/pi - kInvPiHi
   lam_param p;
   p.a2 = log_re * log_re;
-  const double inv_pi = 0.318309886183790671537767526745;
-  double t = (double)log_im * inv_pi;
-  t = t - 2.0 * rint(0.5 * t);
-  p.th_hi = (float)t;
-  p.th_lo = (float)(t - (double)p.th_hi);
+  const float hi = log_im * kInvPiHi;
+  const float e = fmaf(log_im, kInvPiHi, -hi) + log_im * kInvPiLo;
+  const float r = hi - 2.0f * rintf(0.5f * hi);
+  const float s = r + e;
+  p.th_hi = s;
+  p.th_lo = e - (s - r);
   return p;
 }
 

@@ -32,11 +32,27 @@
 // Powers lambda^j are evaluated from an exactly reduced phase (lam_pow) for j = 8a and j < 8
 // and combined by one complex product, so no power carries a long multiplication chain.
 //
-// One CTA per SM (persistent), 4 warps; thread i owns TMEM lane i: a state row r in step 2,
-// a chunk g in the u conversion and the output epilogue. Thread 0 issues the MMAs.
+// Two kernels. dlr_scan_tc_tables (one CTA per channel) evaluates the per-channel tables --
+// Q, the Toeplitz block of K_0..K_63 and G as scaled f16 pairs in the exact byte layout the
+// MMAs read, lambda^64, the re-anchoring correction and the two scales -- into a workspace
+// blob per channel. dlr_scan_tc_kernel then runs one persistent CTA per SM with three warp
+// roles joined by mbarriers and two tiles in flight:
+//   warps 0-3  "scan":  thread r owns TMEM lane r = state row r; runs step 2 on S, writes Xin
+//                       (scaled f16 pair, MN-major) to shared memory; loads Q into TMEM when
+//                       the channel changes,
+//   warps 4-7  "io":    thread g owns TMEM lane g = chunk g; loads u and writes its scaled f16
+//                       pair (tile k+1), then reads Y1, Y2 and stores y (tile k),
+//   warp 8, lane 0:     issues the MMAs, GEMM1 or GEMM2, whichever has its inputs first.
+// Buffers: u operand x2, S accumulator x2 (TMEM), Xin x1, Y1/Y2 x1; Q lives in TMEM as the A
+// operand of GEMM1, the Toeplitz block and G in shared memory (one bulk copy per channel).
 // Units of work: a tile holds floor(128 / C) whole rows when a row has C <= 128 chunks
 // (several batch rows of one channel), otherwise one row walks its tiles in order and carries
-// its state from tile to tile. Per-channel tables are rebuilt when the channel changes.
+// its state from tile to tile. A CTA takes a contiguous range of units; at a change of channel
+// the pipeline drains and the next channel's tables are copied in.
+//
+// Every wait is bounded (global timer, 1 s); a wait that runs out sets a CTA-wide abort flag,
+// all roles leave their loops at the next wait or role barrier, and the kernel records
+// DLR_ERR_TIMEOUT in the library's status word.
 #include <cuda_fp16.h>
 
 #include <algorithm>
@@ -50,37 +66,59 @@ namespace {
 
 constexpr int kT = 64;        // steps per chunk
 constexpr int kCols = 128;    // chunks per tile
-constexpr int kThreads = 128;
 constexpr int kNMax = 64;     // complex states (2N real rows of the state GEMM)
 constexpr int kPw = kT + 1;   // powers lambda^0 .. lambda^64
-constexpr uint32_t kTmemCols = 256;  // S: 0..127, Y1: 128..191, Y2: 192..255
+constexpr int kThreads = 288; // warps 0-3 scan, 4-7 io, 8 mma
+constexpr int kScanBar = 1, kIoBar = 2;  // named barriers of the scan and io warps
 
-// shared memory (bytes from a 1024-byte aligned base); f16 tiles in the K-major 128-byte
-// swizzled layout (rows of 64 elements, 8-row atoms of 1024 bytes, 16-byte chunk index XOR
-// (row & 7)); K = 128 operands are two such tiles ("K-blocks") one after the other
-constexpr uint32_t kQHi = 0, kQLo = 16384;         // Q        [128 rows x 64]
-constexpr uint32_t kUHi = 32768, kULo = 49152;     // u chunks [128 chunks x 64]
-constexpr uint32_t kXHi = 65536, kXLo = 98304;     // Xin      [128 chunks x 128]
-constexpr uint32_t kTkHi = 131072, kTkLo = 139264; // Toeplitz [64 t x 64 s]
-constexpr uint32_t kGHi = 147456, kGLo = 163840;   // G        [64 t x 128]
-constexpr uint32_t kInvU = 180224;                 // float[128]: 2^-14 / (u scale of chunk g)
-constexpr uint32_t kRed = kInvU + 512;             // float[8] reductions
-constexpr uint32_t kKtap = kRed + 64;              // float[64] K_0..K_63
-constexpr uint32_t kPar = kKtap + 256;             // lam_param[64]
-constexpr uint32_t kWs = kPar + 64 * sizeof(lam_param);  // float2[64]
-constexpr uint32_t kDelta = kWs + 512;             // float2[64] lambda^2048 - mu^32
-constexpr uint32_t kRowMax = kDelta + 512;         // float[128][4] per-row, per-warp max |Xin|
-constexpr uint32_t kColSx = kRowMax + 2048;        // float[128] Xin scale of chunk g
-constexpr uint32_t kBar = (kColSx + 512 + 7) & ~7u; // mbarrier
-constexpr uint32_t kSlot = kBar + 8;               // TMEM base address
-constexpr uint32_t kEnd = kSlot + 8;
-constexpr size_t kSmemBytes = kEnd + 1024;         // + alignment slack
-// scratch while building the per-channel tables (inside the Xin region, which is idle then)
-constexpr uint32_t kPow = kXHi;                          // float2 [64][65] lambda_n^j
-constexpr uint32_t kPow8 = kPow + kNMax * kPw * 8;       // float2 [64][9]  lambda_n^{8a}
-constexpr uint32_t kPow1 = kPow8 + kNMax * 9 * 8;        // float2 [64][8]  lambda_n^b
-static_assert(kPow1 + kNMax * 8 * 8 <= kTkHi, "table scratch must fit the Xin region");
+// TMEM columns (512 allocated): Q hi/lo (A operand of GEMM1, 2 f16 per column), S x2, Y1, Y2
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTQHi = 0, kTQLo = 32, kTS = 64, kTY1 = 320, kTY2 = 384;
+
+// shared memory (bytes from a 1024-byte aligned base). K-major f16 tiles use the 128-byte
+// swizzled layout: rows of 64 elements (128 bytes), 8-row atoms of 1024 bytes, 16-byte chunk
+// index XOR (row & 7); K = 128 operands are two such tiles ("K-blocks") one after the other.
+// Xin is MN-major: atoms of 8 K-rows (state rows) x 64 chunks (128 bytes per K-row, chunk
+// index XOR (K-row & 7)); atom (K-group kg, M-half ma) at kg * 2048 + ma * 1024.
+constexpr uint32_t kU = 0;              // u operand [128 chunks x 64], 2 buffers of hi + lo
+constexpr uint32_t kUBuf = 32768, kULo = 16384;
+constexpr uint32_t kXHi = 65536, kXLo = 98304;      // Xin [128 chunks x 128 rows], MN-major
+constexpr uint32_t kTkHi = 131072, kTkLo = 139264;  // Toeplitz [64 t x 64 s], K-major
+constexpr uint32_t kGHi = 147456, kGLo = 163840;    // G [64 t x 128 rows], K-major
+constexpr uint32_t kInvU = 180224;   // float[2][128] 2^-14 / (u scale of chunk g), by parity
+constexpr uint32_t kInvSu = kInvU + 1024;   // float[2][128] 1 / (u scale of chunk g)
+constexpr uint32_t kColSx = kInvSu + 1024;  // float[2][128] Xin scale of chunk g
+constexpr uint32_t kBy = kColSx + 1024;     // float[2][128] 1 / (Xin scale * G scale)
+constexpr uint32_t kRowMax = kBy + 1024;    // float[128][4] per-row, per-warp max |Xin|
+constexpr uint32_t kSig = kRowMax + 2048;   // float[4] K scale, G scale of the channel
+constexpr uint32_t kBars = kSig + 16;       // mbarriers
+// A waiter may trail the phase it waits for by at most one completed phase (the parity test
+// cannot tell phase j from phase j + 2), so every wait below is on a barrier that cannot
+// complete twice more before the waiter has passed: the u buffers get their own "free"
+// barriers instead of sharing the GEMM2 one.
+constexpr int kBarUFull = 0, kBarSFull = 2, kBarSFree = 4, kBarXFull = 6, kBarG2 = 7,
+              kBarYFree = 8, kBarTab = 9, kBarScale = 10, kBarUFree = 12, kBarTabLoad = 14,
+              kNumBars = 15;
+constexpr uint32_t kSlot = kBars + 8 * kNumBars;  // TMEM base address
+constexpr uint32_t kAbort = kSlot + 4;            // abort flag
+constexpr uint32_t kEnd = kAbort + 4;
+constexpr size_t kSmemBytes = kEnd + 1024;        // + alignment slack
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+
+// Per-channel table blob in the workspace (bytes). Its first 48 KB are the shared-memory image
+// of the Toeplitz and G operands (kTkHi .. kGLo + 16 KB), copied in one piece.
+constexpr uint32_t kBlobSmem = kGLo + 16384 - kTkHi;  // 49152
+constexpr uint32_t kBlobQ = kBlobSmem;       // uint32 [128 rows][64]: 32 hi then 32 lo words
+constexpr uint32_t kBlobMu = kBlobQ + 32768;  // float4 [64]: lambda^64 (re, im), correction
+constexpr uint32_t kBlobSig = kBlobMu + 1024; // float [4]: K scale, G scale
+constexpr uint32_t kBlobBytes = kBlobSig + 1024;  // 83968, a multiple of 1024
+static_assert(kBlobSmem == 49152 && kBlobBytes % 1024 == 0, "blob layout");
+
+// Shared memory of the tables kernel.
+constexpr uint32_t kTbKp = 0;                  // float [64 states][65] Re(W_n lambda_n^j)
+constexpr uint32_t kTbK = kTbKp + 64 * 65 * 4; // float [64] K_0..K_63
+constexpr uint32_t kTbRed = kTbK + 256;        // float [32]
+constexpr uint32_t kTbBytes = kTbRed + 128;
 
 struct TcScanArgs {
   const float* u;
@@ -93,6 +131,7 @@ struct TcScanArgs {
   int R;            // rows per tile (C <= 128), 0: one row per unit, walked tile by tile
   int tiles_per_h;  // ceil(B / R) when R > 0
   int units;
+  const uint8_t* tables;  // H table blobs of kBlobBytes
   int* status;
 };
 
@@ -128,14 +167,49 @@ __device__ __forceinline__ void store_row64(uint8_t* hi_tile, uint8_t* lo_tile, 
   }
 }
 
-__device__ __forceinline__ float block_max(float v, float* red, int slot) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if ((threadIdx.x & 31) == 0) red[slot * 4 + (threadIdx.x >> 5)] = v;
-  __syncthreads();
-  const float m = fmaxf(fmaxf(red[slot * 4], red[slot * 4 + 1]),
-                        fmaxf(red[slot * 4 + 2], red[slot * 4 + 3]));
-  return m;
+__device__ __forceinline__ void named_bar(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// Barrier over `n` threads of named barrier `id` that also ANDs a predicate across them.
+__device__ __forceinline__ bool named_bar_and(int id, int n, bool v) {
+  int r;
+  asm volatile(
+      "{\n"
+      "  .reg .pred p, q;\n"
+      "  setp.ne.s32 p, %1, 0;\n"
+      "  bar.red.and.pred q, %2, %3, p;\n"
+      "  selp.s32 %0, 1, 0, q;\n"
+      "}\n"
+      : "=r"(r)
+      : "r"((int)v), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
+}
+
+// Bounded wait on an mbarrier phase (one thread) that also gives up when another role has
+// aborted. Each try may suspend the thread for a few microseconds.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (tc::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = tc::global_timer_ns();
+  while (true) {
+    if (tc::mbar_try_wait_hint(bar, parity, 20000u)) return true;
+    if (*abort) return false;
+    if (tc::global_timer_ns() - t0 > tc::kWaitLimitNs) {
+      *abort = 1;
+      return false;
+    }
+  }
+}
+// The same for a whole warp: lane 0 waits, the other lanes are held at the shuffle.
+__device__ __forceinline__ bool warp_wait_phase(uint64_t* bar, uint32_t parity,
+                                                volatile int* abort) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = wait_phase(bar, parity, abort);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
 // u_{g,t} for t < 64 of the chunk starting at step k0 of a row (the reversed row when kRev);
@@ -198,120 +272,606 @@ __device__ __forceinline__ void store_part(float* __restrict__ row, int L, int k
   }
 }
 
-// Per-channel tables: Q, the Toeplitz block of K_0..K_63, G (all as scaled f16 pairs), the
-// chunk multiplier lambda^64 of this thread's state and the scales of K and G.
-__device__ void build_tables(const TcScanArgs& a, int h, uint8_t* sm, float& mu_re,
-                             float& mu_im_signed, float& dl_re, float& dl_im_signed,
-                             float& sig_k, float& sig_g) {
-  const int tid = threadIdx.x;
-  float2* sPow = reinterpret_cast<float2*>(sm + kPow);
-  float2* sPow8 = reinterpret_cast<float2*>(sm + kPow8);
-  float2* sPow1 = reinterpret_cast<float2*>(sm + kPow1);
-  lam_param* sPar = reinterpret_cast<lam_param*>(sm + kPar);
-  float2* sW = reinterpret_cast<float2*>(sm + kWs);
-  float* sK = reinterpret_cast<float*>(sm + kKtap);
-  float* sRed = reinterpret_cast<float*>(sm + kRed);
-  const int N = a.N;
+// Where tile k of this CTA lies: channel, first batch row and row count, segment of the row.
+struct TileInfo {
+  int h, b0, nrows, seg;
+};
+__device__ __forceinline__ TileInfo tile_info(const TcScanArgs& a, int u0, int segs, int k) {
+  const int unit = u0 + k / segs;
+  TileInfo t;
+  t.seg = k - (k / segs) * segs;
+  if (a.R > 0) {
+    t.h = unit / a.tiles_per_h;
+    t.b0 = (unit - t.h * a.tiles_per_h) * a.R;
+    t.nrows = min(a.R, a.B - t.b0);
+  } else {
+    t.h = unit / a.B;
+    t.b0 = unit - t.h * a.B;
+    t.nrows = 1;
+  }
+  return t;
+}
 
-  __syncthreads();  // the previous tile is done with every region reused below
-  if (tid < kNMax) {
-    const bool on = tid < N;
-    sPar[tid] = on ? make_lam_param(a.log_re[(size_t)h * N + tid], a.log_im[(size_t)h * N + tid])
-                   : lam_param{0.f, 0.f, 0.f};
-    sW[tid] = on ? a.W[(size_t)h * N + tid] : make_float2(0.f, 0.f);
+// Column g of a tile: its batch row offset (elements) and first step, and whether it is used.
+struct ColInfo {
+  size_t rowoff;
+  int k0;
+  bool valid;
+};
+__device__ __forceinline__ ColInfo col_info(const TcScanArgs& a, const TileInfo& t, int g) {
+  int rl, c;
+  if (a.R > 0) {
+    rl = g / a.C;
+    c = g - rl * a.C;
+  } else {
+    rl = 0;
+    c = t.seg * kCols + g;
   }
+  ColInfo ci;
+  ci.valid = (a.R > 0) ? (rl < t.nrows) : (c < a.C);
+  ci.rowoff = ((size_t)(t.b0 + (ci.valid ? rl : 0)) * a.H + t.h) * (size_t)a.L;
+  ci.k0 = c * kT;
+  return ci;
+}
+
+// Max over the 256 threads of the tables kernel; `slot` picks 8 floats of `red`.
+__device__ __forceinline__ float block_max256(float v, float* red, int slot) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) red[slot * 8 + (threadIdx.x >> 5)] = v;
   __syncthreads();
-  // directly evaluated powers lambda^{8a} (a <= 8) and lambda^b (b < 8)
-  for (int e = tid; e < kNMax * 17; e += kThreads) {
-    const int n = e / 17, k = e % 17;
-    const int j = (k < 9) ? 8 * k : (k - 9);
-    cf v = {0.f, 0.f};
-    if (n < N) v = lam_pow(sPar[n], j);
-    if (k < 9) sPow8[n * 9 + k] = make_float2(v.re, v.im);
-    else sPow1[n * 8 + (k - 9)] = make_float2(v.re, v.im);
-  }
-  __syncthreads();
-  for (int e = tid; e < kNMax * kPw; e += kThreads) {
-    const int n = e / kPw, j = e % kPw;
-    const float2 p8 = sPow8[n * 9 + (j >> 3)], p1 = sPow1[n * 8 + (j & 7)];
-    const cf v = cmul({p8.x, p8.y}, {p1.x, p1.y});
-    sPow[e] = make_float2(v.re, v.im);
-  }
-  __syncthreads();
-  // K_j = Re sum_n W_n lambda_n^j (threads 0..63) and the scales
-  float kj = 0.f, wabs = 0.f;
-  if (tid < kT) {
-    for (int n = 0; n < N; ++n) {
-      const float2 w = sW[n], p = sPow[n * kPw + tid];
-      kj = fmaf(w.x, p.x, fmaf(-w.y, p.y, kj));
-    }
-    sK[tid] = kj;
-    const float2 w = sW[tid];
-    wabs = fmaxf(fabsf(w.x), fabsf(w.y));
-  }
-  const float kmax = block_max(fabsf(kj), sRed, 0);
-  const float wmax = block_max(wabs, sRed, 1);
-  const int ek = scale_exp(kmax), eg = scale_exp(wmax);
-  sig_k = exp2i(ek);
-  sig_g = exp2i(eg);
-  float v[64];
-  // Q row r = tid: Re|Im lambda_n^{63-t}, times 2^14
+  float m = red[slot * 8];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) m = fmaxf(m, red[slot * 8 + i]);
+  return m;
+}
+
+// Eight values of one K-major row of an f16 operand tile pair (16-byte chunk `chunk`), at a
+// shared or global address.
+__device__ __forceinline__ void store_chunk8(uint8_t* hi_tile, uint8_t* lo_tile, int row,
+                                             int chunk, const float* v) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) split2(v[2 * q], v[2 * q + 1], h[q], l[q]);
+  const uint32_t off = uint32_t(row) * 128u + ((uint32_t(chunk) ^ uint32_t(row & 7)) << 4);
+  *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Per-channel tables (one CTA of 256 threads per channel h) into the channel's blob: the
+// Toeplitz block of K_0..K_63 and G (scaled f16 pairs, swizzled exactly as in the main
+// kernel's shared memory), Q (scaled f16 pairs as TMEM words), lambda^64 and the re-anchoring
+// correction lambda^2048 - (lambda^64)^32 of every state, the scales of K and G.
+// Thread (n, q) = (tid >> 2, tid & 3) owns state n and exponents j = 16q .. 16q + 16, held in
+// registers: lambda^{16q + 4c} (c <= 4) and lambda^d (d < 4) evaluated directly, the others
+// as one product of two of them.
+__global__ void __launch_bounds__(256) dlr_scan_tc_tables(const TcScanArgs a, uint8_t* ws) {
+  extern __shared__ __align__(16) uint8_t tsm[];
+  const int tid = threadIdx.x;
+  const int h = blockIdx.x;
+  uint8_t* blob = ws + (size_t)h * kBlobBytes;
+  float* sKp = reinterpret_cast<float*>(tsm + kTbKp);  // [64 states][65] Re(W_n lambda_n^j)
+  float* sK = reinterpret_cast<float*>(tsm + kTbK);
+  float* sRed = reinterpret_cast<float*>(tsm + kTbRed);
+  const int N = a.N;
+  const int n = tid >> 2, q = tid & 3;
+  const bool on = n < N;
+  const lam_param p = on ? make_lam_param(a.log_re[(size_t)h * N + n], a.log_im[(size_t)h * N + n])
+                         : lam_param{0.f, 0.f, 0.f};
+  const float2 w = on ? __ldg(&a.W[(size_t)h * N + n]) : make_float2(0.f, 0.f);
+  const float sig_g = exp2i(scale_exp(block_max256(fmaxf(fabsf(w.x), fabsf(w.y)), sRed, 0)));
+
+  // pw[i] = lambda^{16q + i}, i = 0..16
+  cf pw[17];
   {
-    const int n = tid >> 1, c = tid & 1;
+    cf base[5], small[4];
 #pragma unroll
-    for (int t = 0; t < kT; ++t) {
-      const float2 p = sPow[n * kPw + (kT - 1 - t)];
-      v[t] = (c ? p.y : p.x) * 16384.f;
+    for (int c = 0; c < 5; ++c) base[c] = on ? lam_pow(p, 16 * q + 4 * c) : cf{0.f, 0.f};
+#pragma unroll
+    for (int d = 0; d < 4; ++d) small[d] = on ? lam_pow(p, d) : cf{0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 17; ++i) pw[i] = (i & 3) ? cmul(base[i >> 2], small[i & 3]) : base[i >> 2];
+  }
+  // Q rows 2n (Re) and 2n+1 (Im) at steps t = 63 - j, j in [16q, 16q + 16): TMEM words
+  // (lower step in the low half) 24 - 8q .. 31 - 8q of each row
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    uint32_t hi[8], lo[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const cf p0 = pw[15 - 2 * m], p1 = pw[14 - 2 * m];  // steps t0 = 48 - 16q + 2m, t0 + 1
+      split2((c ? p0.im : p0.re) * 16384.f, (c ? p1.im : p1.re) * 16384.f, hi[m], lo[m]);
     }
-    store_row64(sm + kQHi, sm + kQLo, tid, v);
+    uint4* row = reinterpret_cast<uint4*>(blob + kBlobQ + (2 * n + c) * 256);
+    row[6 - 2 * q] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    row[7 - 2 * q] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+    row[14 - 2 * q] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    row[15 - 2 * q] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
   }
-  // Toeplitz row t = tid (< 64): K_{t-s} for s <= t
-  if (tid < kT) {
-#pragma unroll
-    for (int s = 0; s < kT; ++s) v[s] = (s <= tid) ? sK[tid - s] * sig_k : 0.f;
-    store_row64(sm + kTkHi, sm + kTkLo, tid, v);
-  }
-  // G row t = tid >> 1, K-block tid & 1: Re(W_n lambda_n^{t+1}), -Im(...)
+  // G rows t = 16q .. 16q + 15, columns 2n, 2n+1: Re, -Im of W_n lambda_n^{t+1}; and the
+  // products' real parts for the tap sums
   {
-    const int t = tid >> 1, kb = tid & 1;
+    const int kb = n >> 5;
+    const uint32_t colb = uint32_t(((2 * n) & 7) * 2);  // byte offset of the pair in its chunk
+    const uint32_t chunk = uint32_t((n & 31) >> 2);
+    uint8_t* gh = blob + (kGHi - kTkHi) + kb * 8192;
+    uint8_t* gl = blob + (kGLo - kTkHi) + kb * 8192;
 #pragma unroll
-    for (int k = 0; k < 64; ++k) {
-      const int r = kb * 64 + k, n = r >> 1;
-      const float2 w = sW[n], p = sPow[n * kPw + t + 1];
-      const cf g = cmul({w.x, w.y}, {p.x, p.y});
-      v[k] = ((r & 1) ? -g.im : g.re) * sig_g;
+    for (int i = 0; i < 16; ++i) {
+      const int t = 16 * q + i;
+      const cf g = cmul({w.x, w.y}, pw[i + 1]);
+      uint32_t hb, lb;
+      split2(g.re * sig_g, -g.im * sig_g, hb, lb);
+      const uint32_t off = uint32_t(t) * 128u + ((chunk ^ uint32_t(t & 7)) << 4) + colb;
+      *reinterpret_cast<uint32_t*>(gh + off) = hb;
+      *reinterpret_cast<uint32_t*>(gl + off) = lb;
+      sKp[n * 65 + 16 * q + i] = cmul({w.x, w.y}, pw[i]).re;  // Re(W lambda^j), j = 16q + i
     }
-    store_row64(sm + kGHi + kb * 8192, sm + kGLo + kb * 8192, t, v);
   }
-  // re-anchoring correction lambda^2048 - mu^32 (mu = the float lambda^64 the chain uses)
-  float2* sDelta = reinterpret_cast<float2*>(sm + kDelta);
-  if (tid < kNMax) {
+  // lambda^64 and the re-anchoring correction (state n, thread q = 3 holds lambda^64)
+  if (q == 3) {
     float2 d = make_float2(0.f, 0.f);
-    if (tid < N) {
-      const float2 m = sPow[tid * kPw + kT];
-      cff p = {{m.x, 0.f}, {m.y, 0.f}};
+    const cf m = pw[16];
+    if (on) {
+      cff pp = {{m.re, 0.f}, {m.im, 0.f}};
 #pragma unroll 1
-      for (int i = 0; i < 5; ++i) p = cff_fma(p, p, cff{{0.f, 0.f}, {0.f, 0.f}});
-      const cf a32 = lam_pow(sPar[tid], 32 * kT);
-      const ff dr = ff_add(ff{a32.re, 0.f}, ff_neg(p.re));
-      const ff di = ff_add(ff{a32.im, 0.f}, ff_neg(p.im));
+      for (int i = 0; i < 5; ++i) pp = cff_fma(pp, pp, cff{{0.f, 0.f}, {0.f, 0.f}});
+      const cf a32 = lam_pow(p, 32 * kT);
+      const ff dr = ff_add(ff{a32.re, 0.f}, ff_neg(pp.re));
+      const ff di = ff_add(ff{a32.im, 0.f}, ff_neg(pp.im));
       d = make_float2(dr.hi + dr.lo, di.hi + di.lo);
     }
-    sDelta[tid] = d;
+    reinterpret_cast<float4*>(blob + kBlobMu)[n] = make_float4(m.re, m.im, d.x, d.y);
   }
   __syncthreads();
+  // K_j = sum_n Re(W_n lambda_n^j): thread (j, part) = (tid >> 2, tid & 3) sums 16 states
+  const int j = tid >> 2, part = tid & 3;
+  float ks = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) ks += sKp[(16 * part + i) * 65 + j];
+  ks += __shfl_xor_sync(0xffffffffu, ks, 1);
+  ks += __shfl_xor_sync(0xffffffffu, ks, 2);
+  if (part == 0) sK[j] = ks;
+  const float sig_k = exp2i(scale_exp(block_max256(part == 0 ? fabsf(ks) : 0.f, sRed, 1)));
+  if (tid == 0) {
+    reinterpret_cast<float*>(blob + kBlobSig)[0] = sig_k;
+    reinterpret_cast<float*>(blob + kBlobSig)[1] = sig_g;
+  }
+  // Toeplitz row t = j, s in [16 part, 16 part + 16): K_{t-s} for s <= t (sK complete after the
+  // barrier inside block_max256)
+  float tv[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int ss = 16 * part + i;
+    tv[i] = (ss <= j) ? sK[j - ss] * sig_k : 0.f;
+  }
+  store_chunk8(blob, blob + (kTkLo - kTkHi), j, 2 * part, tv);
+  store_chunk8(blob, blob + (kTkLo - kTkHi), j, 2 * part + 1, tv + 8);
+}
+
+// Scan warps at the start of a channel: Q from the blob into TMEM (thread r = lane r), this
+// thread's lambda^64 and correction, the scales; thread 0 starts the bulk copy of the
+// Toeplitz and G operands into shared memory (completing on kBarTabLoad).
+__device__ __forceinline__ void load_tables(const uint8_t* blob, uint8_t* sm, uint32_t tmem,
+                                            float& mu_re, float& mu_im_signed, float& dl_re,
+                                            float& dl_im_signed, float& sig_g) {
+  const int tid = threadIdx.x, warp = tid >> 5;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  if (tid == 0) {
+    tc::mbar_arrive_expect_tx(&bars[kBarTabLoad], kBlobSmem);
+    tc::bulk_load(sm + kTkHi, blob, kBlobSmem, &bars[kBarTabLoad]);
+  }
+  const uint4* q = reinterpret_cast<const uint4*>(blob + kBlobQ + tid * 256);
+  float hi[32], lo[32];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint4 a = __ldg(q + i), b = __ldg(q + 8 + i);
+    hi[4 * i] = __uint_as_float(a.x); hi[4 * i + 1] = __uint_as_float(a.y);
+    hi[4 * i + 2] = __uint_as_float(a.z); hi[4 * i + 3] = __uint_as_float(a.w);
+    lo[4 * i] = __uint_as_float(b.x); lo[4 * i + 1] = __uint_as_float(b.y);
+    lo[4 * i + 2] = __uint_as_float(b.z); lo[4 * i + 3] = __uint_as_float(b.w);
+  }
+  const uint32_t tl = tmem + (uint32_t(warp * 32) << 16);
+  tc::tmem_st32(tl + kTQHi, hi);
+  tc::tmem_st32(tl + kTQLo, lo);
+  const float4 m = __ldg(reinterpret_cast<const float4*>(blob + kBlobMu) + (tid >> 1));
+  mu_re = m.x;
+  dl_re = m.z;
+  // the state recurrence keeps (own, other) components; the Im row runs it with the sign of
+  // the imaginary parts flipped
+  mu_im_signed = (tid & 1) ? -m.y : m.y;
+  dl_im_signed = (tid & 1) ? -m.w : m.w;
+  const float sk = __ldg(reinterpret_cast<const float*>(blob + kBlobSig));
+  sig_g = __ldg(reinterpret_cast<const float*>(blob + kBlobSig) + 1);
+  if (tid == 0) reinterpret_cast<float*>(sm + kSig)[0] = sk;
+  tc::tmem_wait_st();
+  tc::fence_before_sync();
+}
+
+// ---- the three roles ------------------------------------------------------------------
+
+// Scan warps, one tile: carries along the chunks, then Xin as a scaled f16 pair.
+__device__ __forceinline__ bool scan_tile(const TcScanArgs& a, uint8_t* sm, uint32_t tmem,
+                                          int k, bool new_row, float mu_re, float mu_im,
+                                          float dl_re, float dl_im, float sig_g, float& xo,
+                                          float& xt, float& ao, float& at,
+                                          volatile int* abort) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int par = k & 1;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  const float* sInvU = reinterpret_cast<const float*>(sm + kInvU) + par * 128;
+  float* sColSx = reinterpret_cast<float*>(sm + kColSx) + par * 128;
+  float* sBy = reinterpret_cast<float*>(sm + kBy) + par * 128;
+  float* sRowMax = reinterpret_cast<float*>(sm + kRowMax);
+  const uint32_t tS = tmem + (uint32_t(warp * 32) << 16) + kTS + uint32_t(par) * 128;
+
+  // S of this tile, and (for the per-chunk u scales) the io threads' release of tile k
+  bool ok = warp_wait_phase(&bars[kBarSFull + par], (k >> 1) & 1, abort) &&
+            warp_wait_phase(&bars[kBarUFull + par], (k >> 1) & 1, abort);
+  if (!named_bar_and(kScanBar, 128, ok)) return false;
+  tc::fence_after_sync();
+
+  if (new_row) xo = xt = ao = at = 0.f;
+  const int C = a.C;
+  if (a.R > 0 && (C == 32 || C == 64)) {
+    // two independent chains: columns [0, 64) and [64, 128) (whole rows of 32 or 64 chunks);
+    // row starts and anchors fall on 32-column block starts
+    float xoB = 0.f, xtB = 0.f, aoB = 0.f, atB = 0.f, lA = 0.f, lB = 0.f;
+#pragma unroll 1
+    for (int bb = 0; bb < 2; ++bb) {
+      const int cA = bb * 32, cB = 64 + bb * 32;
+      if (cA % C == 0) {
+        xo = xt = ao = at = 0.f;
+        xoB = xtB = aoB = atB = 0.f;
+      } else {
+        xo = fmaf(dl_re, ao, fmaf(-dl_im, at, xo));
+        xt = fmaf(dl_re, at, fmaf(dl_im, ao, xt));
+        ao = xo;
+        at = xt;
+        xoB = fmaf(dl_re, aoB, fmaf(-dl_im, atB, xoB));
+        xtB = fmaf(dl_re, atB, fmaf(dl_im, aoB, xtB));
+        aoB = xoB;
+        atB = xtB;
+      }
+      float sA[32], sB[32];
+      tc::tmem_ld32(tS + cA, sA);
+      tc::tmem_ld32(tS + cB, sB);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float ivA = sInvU[cA + j], ivB = sInvU[cB + j];
+        const float pA = __shfl_xor_sync(0xffffffffu, sA[j], 1);
+        const float pB = __shfl_xor_sync(0xffffffffu, sB[j], 1);
+        const float oA = xo, oB = xoB;
+        lA = fmaxf(lA, fabsf(oA));
+        lB = fmaxf(lB, fabsf(oB));
+        const float noA = fmaf(mu_re, xo, fmaf(-mu_im, xt, sA[j] * ivA));
+        const float ntA = fmaf(mu_re, xt, fmaf(mu_im, xo, pA * ivA));
+        const float noB = fmaf(mu_re, xoB, fmaf(-mu_im, xtB, sB[j] * ivB));
+        const float ntB = fmaf(mu_re, xtB, fmaf(mu_im, xoB, pB * ivB));
+        sA[j] = oA;
+        sB[j] = oB;
+        xo = noA;
+        xt = ntA;
+        xoB = noB;
+        xtB = ntB;
+      }
+      tc::tmem_st32(tS + cA, sA);
+      tc::tmem_st32(tS + cB, sB);
+      if ((cA + 32) % C == 0) {  // rows end with this block
+        const unsigned mA = __reduce_max_sync(0xffffffffu, __float_as_uint(lA));
+        const unsigned mB = __reduce_max_sync(0xffffffffu, __float_as_uint(lB));
+        if (lane == 0) {
+          sRowMax[(cA / C) * 4 + warp] = __uint_as_float(mA);
+          sRowMax[(cB / C) * 4 + warp] = __uint_as_float(mB);
+        }
+        lA = lB = 0.f;
+      }
+    }
+    tc::tmem_wait_st();
+  } else if (a.R == 0 || C % 32 == 0) {
+    // one chain (one row per tile): a row start at column 0 when new_row, anchors at every
+    // other 32-column block start
+    float l = 0.f;
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+      const int c0 = blk * 32;
+      if (a.R > 0 && c0 % C == 0) {
+        xo = xt = ao = at = 0.f;
+      } else {
+        xo = fmaf(dl_re, ao, fmaf(-dl_im, at, xo));
+        xt = fmaf(dl_re, at, fmaf(dl_im, ao, xt));
+        ao = xo;
+        at = xt;
+      }
+      float sv[32];
+      tc::tmem_ld32(tS + c0, sv);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float iv = sInvU[c0 + j];
+        const float p = __shfl_xor_sync(0xffffffffu, sv[j], 1);
+        const float o = xo;
+        l = fmaxf(l, fabsf(o));
+        const float no = fmaf(mu_re, xo, fmaf(-mu_im, xt, sv[j] * iv));
+        const float nt = fmaf(mu_re, xt, fmaf(mu_im, xo, p * iv));
+        sv[j] = o;
+        xo = no;
+        xt = nt;
+      }
+      tc::tmem_st32(tS + c0, sv);
+    }
+    tc::tmem_wait_st();
+    const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(l));
+    if (lane == 0) sRowMax[warp] = __uint_as_float(m);
+  } else {
+    // any other row length: row starts and anchors checked column by column
+    int next_reset = 0;
+    int next_anchor = 0;
+    float lmax = 0.f;
+    int row_i = 0;
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+      float sv[32], o[32];
+      tc::tmem_ld32(tS + blk * 32, sv);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int g = blk * 32 + j;
+        const float iv = sInvU[g];
+        const float sother = __shfl_xor_sync(0xffffffffu, sv[j], 1);
+        if (g == next_anchor) {
+          xo = fmaf(dl_re, ao, fmaf(-dl_im, at, xo));
+          xt = fmaf(dl_re, at, fmaf(dl_im, ao, xt));
+          ao = xo;
+          at = xt;
+          next_anchor += 32;
+        }
+        if (g == next_reset) {
+          if (g > 0) {
+            const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(lmax));
+            if (lane == 0) sRowMax[row_i * 4 + warp] = __uint_as_float(m);
+            ++row_i;
+            lmax = 0.f;
+          }
+          xo = xt = ao = at = 0.f;
+          next_reset += C;
+          next_anchor = g + 32;
+        }
+        o[j] = xo;
+        lmax = fmaxf(lmax, fabsf(xo));
+        const float no = fmaf(mu_re, xo, fmaf(-mu_im, xt, sv[j] * iv));
+        const float nt = fmaf(mu_re, xt, fmaf(mu_im, xo, sother * iv));
+        xo = no;
+        xt = nt;
+      }
+      tc::tmem_st32(tS + blk * 32, o);
+    }
+    tc::tmem_wait_st();
+    const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(lmax));
+    if (lane == 0) sRowMax[row_i * 4 + warp] = __uint_as_float(m);
+  }
+  named_bar(kScanBar, 128);
+  // Xin scale of chunk column tid (the scale of its batch row)
   {
-    const int n = tid >> 1;
-    const float2 m = sPow[n * kPw + kT];
-    const float2 d = sDelta[n];
-    mu_re = m.x;
-    dl_re = d.x;
-    // the state recurrence below keeps (own, other) components; the Im row runs it with the
-    // sign of the imaginary parts flipped
-    mu_im_signed = (tid & 1) ? -m.y : m.y;
-    dl_im_signed = (tid & 1) ? -d.y : d.y;
+    const int row = (a.R > 0) ? tid / a.C : 0;
+    const float xmax = fmaxf(fmaxf(sRowMax[row * 4], sRowMax[row * 4 + 1]),
+                             fmaxf(sRowMax[row * 4 + 2], sRowMax[row * 4 + 3]));
+    const int ex = scale_exp(xmax);
+    sColSx[tid] = exp2i(ex);
+    sBy[tid] = exp2i(-ex) / sig_g;
   }
-  __syncthreads();
+  mbar_arrive(&bars[kBarScale + par]);  // releases sBy (and the channel scales) to the io warps
+  // the Xin buffer is free once GEMM2 of the previous tile has completed
+  ok = (k == 0) || warp_wait_phase(&bars[kBarG2], (k - 1) & 1, abort);
+  if (!named_bar_and(kScanBar, 128, ok)) return false;
+  // Xin -> scaled f16 pair, MN-major: this thread writes state row r = tid, 8 chunks per
+  // 16-byte store
+  {
+    const int r = tid;
+    const uint32_t kbase = uint32_t(r >> 3) * 2048u + uint32_t(r & 7) * 128u;
+    const uint32_t kr = uint32_t(r & 7);
+#pragma unroll 1
+    for (int blk = 0; blk < 4; ++blk) {
+      float v[32];
+      tc::tmem_ld32(tS + blk * 32, v);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int g0 = blk * 32 + q * 8;
+        const float4 c0 = *reinterpret_cast<const float4*>(sColSx + g0);
+        const float4 c1 = *reinterpret_cast<const float4*>(sColSx + g0 + 4);
+        const float sc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+          split2(v[q * 8 + 2 * p] * sc[2 * p], v[q * 8 + 2 * p + 1] * sc[2 * p + 1], h[p], l[p]);
+        const uint32_t cg = uint32_t(g0 >> 3);  // 16-byte chunk index along the chunks
+        const uint32_t off = kbase + (cg >> 3) * 1024u + (((cg & 7u) ^ kr) << 4);
+        *reinterpret_cast<uint4*>(sm + kXHi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(sm + kXLo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+      }
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  mbar_arrive(&bars[kBarXFull]);
+  mbar_arrive(&bars[kBarSFree + par]);
+  return true;
+}
+
+// IO warps: u chunks of tile k -> scaled f16 pair (thread = chunk column g).
+template <bool kRev>
+__device__ __forceinline__ bool load_tile(const TcScanArgs& a, uint8_t* sm, int u0, int segs,
+                                          int k, volatile int* abort) {
+  const int g = threadIdx.x - 128;
+  const int par = k & 1;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  // the u buffer is free once GEMM2 of tile k-2 has completed
+  const bool ok =
+      (k < 2) || warp_wait_phase(&bars[kBarUFree + par], ((k - 2) >> 1) & 1, abort);
+  if (!named_bar_and(kIoBar, 128, ok)) return false;
+  const TileInfo ti = tile_info(a, u0, segs, k);
+  const ColInfo ci = col_info(a, ti, g);
+  float v[64];
+  load_chunk<kRev>(a.u + ci.rowoff, a.L, ci.k0, ci.valid, v);
+  float m = 0.f;
+#pragma unroll
+  for (int t = 0; t < kT; ++t) m = fmaxf(m, fabsf(v[t]));
+  const int es = scale_exp(m);
+  const float su = exp2i(es);
+#pragma unroll
+  for (int t = 0; t < kT; ++t) v[t] *= su;
+  uint8_t* ubuf = sm + kU + par * kUBuf;
+  store_row64(ubuf, ubuf + kULo, g, v);
+  const float inv_su = exp2i(-es);
+  reinterpret_cast<float*>(sm + kInvU)[par * 128 + g] = inv_su * (1.f / 16384.f);
+  reinterpret_cast<float*>(sm + kInvSu)[par * 128 + g] = inv_su;
+  tc::fence_proxy_async_smem();
+  mbar_arrive(&bars[kBarUFull + par]);
+  return true;
+}
+
+// IO warps: outputs of tile k (thread = chunk column g = TMEM lane).
+template <bool kRev>
+__device__ __forceinline__ bool store_tile(const TcScanArgs& a, uint8_t* sm, uint32_t tmem,
+                                           int u0, int segs, int k, volatile int* abort) {
+  const int g = threadIdx.x - 128, warp = threadIdx.x >> 5;
+  const int par = k & 1;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  const bool ok = warp_wait_phase(&bars[kBarG2], k & 1, abort) &&
+                  warp_wait_phase(&bars[kBarScale + par], (k >> 1) & 1, abort);
+  if (!named_bar_and(kIoBar, 128, ok)) return false;
+  tc::fence_after_sync();
+  const float sig_k = reinterpret_cast<const float*>(sm + kSig)[0];
+  const float ay = reinterpret_cast<const float*>(sm + kInvSu)[par * 128 + g] / sig_k;
+  const float by = reinterpret_cast<const float*>(sm + kBy)[par * 128 + g];
+  const uint32_t lane_base = tmem + (uint32_t((warp & 3) * 32) << 16);
+  float y[64];
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    float y1[32], y2[32];
+    tc::tmem_ld32(lane_base + kTY1 + half * 32, y1);
+    tc::tmem_ld32(lane_base + kTY2 + half * 32, y2);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) y[half * 32 + j] = fmaf(y1[j], ay, y2[j] * by);
+  }
+  tc::fence_before_sync();
+  mbar_arrive(&bars[kBarYFree]);
+  const TileInfo ti = tile_info(a, u0, segs, k);
+  const ColInfo ci = col_info(a, ti, g);
+  if (ci.valid) {
+    float* yrow = a.y + ci.rowoff;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float o[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) o[j] = y[half * 32 + j];
+      store_part<kRev>(yrow, a.L, ci.k0 + half * 32, o);
+    }
+  }
+  return true;
+}
+
+// MMA thread: are the inputs of GEMM1 of tile k in place? (u operand written, S buffer k & 1
+// released by the scan of tile k-2, the channel's tables loaded for the first tile of a channel)
+__device__ __forceinline__ bool gemm1_ready(uint64_t* bars, int k, bool first_of_group,
+                                            uint32_t group) {
+  const int par = k & 1;
+  if (first_of_group && !(tc::mbar_try_wait(&bars[kBarTab], group & 1) &&
+                          tc::mbar_try_wait(&bars[kBarTabLoad], group & 1)))
+    return false;
+  if (!tc::mbar_try_wait(&bars[kBarUFull + par], (k >> 1) & 1)) return false;
+  return k < 2 || tc::mbar_try_wait(&bars[kBarSFree + par], ((k - 2) >> 1) & 1);
+}
+
+// GEMM1 of tile k: S = Q u^T into S buffer k & 1 (A = Q from TMEM, B = u operand).
+__device__ __forceinline__ void gemm1(uint8_t* sm, uint32_t tmem, int k) {
+  const int par = k & 1;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  tc::fence_after_sync();
+  constexpr uint32_t id1 = tc::idesc_f16_f32(128, 128);
+  const uint8_t* ubuf = sm + kU + par * kUBuf;
+  const uint64_t uh = tc::smem_desc_k_sw128(ubuf), ul = tc::smem_desc_k_sw128(ubuf + kULo);
+  const uint32_t dS = tmem + kTS + uint32_t(par) * 128;
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    const uint32_t qh = tmem + kTQHi + kk * 8, ql = tmem + kTQLo + kk * 8;
+    asm volatile(
+        "{\n"
+        "  .reg .pred p;\n"
+        "  setp.ne.b32 p, %4, 0;\n"
+        "  tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+        "  tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %3, 1;\n"
+        "  tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %2, %3, 1;\n"
+        "}\n" ::"r"(dS),
+        "r"(qh), "l"(uh + 2 * kk), "r"(id1), "r"(kk), "l"(ul + 2 * kk), "r"(ql)
+        : "memory");
+  }
+  tc::mma_commit(&bars[kBarSFull + par]);
+}
+
+// MMA thread: are the inputs of GEMM2 of tile k in place? (Xin written, Y read out for k-1)
+__device__ __forceinline__ bool gemm2_ready(uint64_t* bars, int k) {
+  if (!tc::mbar_try_wait(&bars[kBarXFull], k & 1)) return false;
+  return k < 1 || tc::mbar_try_wait(&bars[kBarYFree], (k - 1) & 1);
+}
+
+// GEMM2 of tile k: Y1 = u Tk^T, Y2 = Xin G^T; its completion also frees u buffer k & 1.
+__device__ __forceinline__ void gemm2(uint8_t* sm, uint32_t tmem, int k) {
+  const int par = k & 1;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  tc::fence_after_sync();
+  constexpr uint32_t idk = tc::idesc_f16_f32(128, 64);
+  constexpr uint32_t idm = idk | (1u << 15);  // A (Xin) MN-major
+  const uint8_t* ubuf = sm + kU + par * kUBuf;
+  const uint64_t uh = tc::smem_desc_k_sw128(ubuf), ul = tc::smem_desc_k_sw128(ubuf + kULo);
+  const uint64_t th = tc::smem_desc_k_sw128(sm + kTkHi), tl = tc::smem_desc_k_sw128(sm + kTkLo);
+  const uint64_t gh = tc::smem_desc_k_sw128(sm + kGHi), gl = tc::smem_desc_k_sw128(sm + kGLo);
+  const uint64_t xh = tc::smem_desc_mn_sw128(sm + kXHi, 1024, 2048);
+  const uint64_t xl = tc::smem_desc_mn_sw128(sm + kXLo, 1024, 2048);
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    tc::mma_kind_f16(tmem + kTY1, uh + 2 * kk, th + 2 * kk, idk, kk != 0);
+    tc::mma_kind_f16(tmem + kTY1, uh + 2 * kk, tl + 2 * kk, idk, 1);
+    tc::mma_kind_f16(tmem + kTY1, ul + 2 * kk, th + 2 * kk, idk, 1);
+  }
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const uint64_t ao = uint64_t(s) * (4096 >> 4);                     // 16 rows = 2 K-groups
+    const uint64_t bo = uint64_t(s >> 2) * (8192 >> 4) + 2 * (s & 3);  // K-block, 32 bytes
+    tc::mma_kind_f16(tmem + kTY2, xh + ao, gh + bo, idm, s != 0);
+    tc::mma_kind_f16(tmem + kTY2, xh + ao, gl + bo, idm, 1);
+    tc::mma_kind_f16(tmem + kTY2, xl + ao, gh + bo, idm, 1);
+  }
+  tc::mma_commit(&bars[kBarG2]);
+  tc::mma_commit(&bars[kBarUFree + par]);
+}
+
+// MMA thread, tiles [k0, k1) of one channel: issues GEMM2 of the oldest tile whose Xin is
+// ready, else GEMM1 of the next tile whose u is ready. Gives up (abort flag) after the wait
+// limit without progress.
+__device__ __forceinline__ void mma_role(uint8_t* sm, uint32_t tmem, int k0, int k1,
+                                         uint32_t group, volatile int* abort) {
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  int n1 = k0, n2 = k0;
+  uint64_t t_last = tc::global_timer_ns();
+  while (n2 < k1) {
+    bool did = false;
+    if (n2 < n1 && gemm2_ready(bars, n2)) {
+      gemm2(sm, tmem, n2++);
+      did = true;
+    } else if (n1 < k1 && gemm1_ready(bars, n1, n1 == k0, group)) {
+      gemm1(sm, tmem, n1++);
+      did = true;
+    }
+    if (did) {
+      t_last = tc::global_timer_ns();
+    } else {
+      if (*abort) return;
+      if (tc::global_timer_ns() - t_last > tc::kWaitLimitNs) {
+        *abort = 1;
+        return;
+      }
+      __nanosleep(32);
+    }
+  }
 }
 
 template <bool kRev>
@@ -319,15 +879,28 @@ __global__ void __launch_bounds__(kThreads, 1) dlr_scan_tc_kernel(const TcScanAr
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* sInvU = reinterpret_cast<float*>(sm + kInvU);
-  float* sRowMax = reinterpret_cast<float*>(sm + kRowMax);
-  float* sColSx = reinterpret_cast<float*>(sm + kColSx);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kBar);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
   uint32_t* slot = reinterpret_cast<uint32_t*>(sm + kSlot);
+  volatile int* abort = reinterpret_cast<volatile int*>(sm + kAbort);
 
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   if (tid == 0) {
-    tc::mbar_init(bar, 1);
+    tc::mbar_init(&bars[kBarUFull], 128);
+    tc::mbar_init(&bars[kBarUFull + 1], 128);
+    tc::mbar_init(&bars[kBarSFull], 1);
+    tc::mbar_init(&bars[kBarSFull + 1], 1);
+    tc::mbar_init(&bars[kBarSFree], 128);
+    tc::mbar_init(&bars[kBarSFree + 1], 128);
+    tc::mbar_init(&bars[kBarXFull], 128);
+    tc::mbar_init(&bars[kBarG2], 1);
+    tc::mbar_init(&bars[kBarYFree], 128);
+    tc::mbar_init(&bars[kBarTab], 128);
+    tc::mbar_init(&bars[kBarScale], 128);
+    tc::mbar_init(&bars[kBarScale + 1], 128);
+    tc::mbar_init(&bars[kBarUFree], 1);
+    tc::mbar_init(&bars[kBarUFree + 1], 1);
+    tc::mbar_init(&bars[kBarTabLoad], 1);
+    *abort = 0;
     tc::mbar_fence_init();
   }
   if (warp == 0) {
@@ -338,219 +911,50 @@ __global__ void __launch_bounds__(kThreads, 1) dlr_scan_tc_kernel(const TcScanAr
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *slot;
-  const uint32_t tS = tmem + (uint32_t(warp * 32) << 16);  // this warp's lanes
-  const uint32_t tY1 = tS + 128, tY2 = tS + 192;
 
   const int u0 = (int)((long long)blockIdx.x * a.units / gridDim.x);
   const int u1 = (int)((long long)(blockIdx.x + 1) * a.units / gridDim.x);
   const int segs = (a.R > 0) ? 1 : (a.C + kCols - 1) / kCols;
-  const int reset_every = a.C;
+  const int ntiles = (u1 - u0) * segs;
 
-  int cur_h = -1;
-  float mu_re = 0.f, mu_im = 0.f, dl_re = 0.f, dl_im = 0.f, sig_k = 1.f, sig_g = 1.f;
-  uint32_t parity = 0;
-  bool ok = true;
+  // scan-thread state
+  float mu_re = 0.f, mu_im = 0.f, dl_re = 0.f, dl_im = 0.f, sig_g = 1.f;
+  float xo = 0.f, xt = 0.f, ao = 0.f, at = 0.f;
+  uint32_t group = 0;
 
-  for (int unit = u0; unit < u1 && ok; ++unit) {
-    int h, b0, nrows;
-    if (a.R > 0) {
-      h = unit / a.tiles_per_h;
-      b0 = (unit - h * a.tiles_per_h) * a.R;
-      nrows = min(a.R, a.B - b0);
-    } else {
-      h = unit / a.B;
-      b0 = unit - h * a.B;
-      nrows = 1;
+  for (int k0 = 0; k0 < ntiles; ++group) {
+    // the tiles [k0, k1) share one channel
+    const int h = tile_info(a, u0, segs, k0).h;
+    const int u_end = min(u1, (a.R > 0) ? (h + 1) * a.tiles_per_h : (h + 1) * a.B);
+    const int k1 = (u_end - u0) * segs;
+
+    if (warp < 4) {
+      load_tables(a.tables + (size_t)h * kBlobBytes, sm, tmem, mu_re, mu_im, dl_re, dl_im,
+                  sig_g);
+      mbar_arrive(&bars[kBarTab]);
+      for (int k = k0; k < k1; ++k) {
+        const TileInfo ti = tile_info(a, u0, segs, k);
+        if (!scan_tile(a, sm, tmem, k, ti.seg == 0, mu_re, mu_im, dl_re, dl_im, sig_g, xo, xt,
+                       ao, at, abort))
+          break;
+      }
+    } else if (warp < 8) {
+      bool ok = true;
+      for (int k = k0; k < k1 && ok; ++k) {
+        ok = load_tile<kRev>(a, sm, u0, segs, k, abort);
+        if (ok && k > k0) ok = store_tile<kRev>(a, sm, tmem, u0, segs, k - 1, abort);
+      }
+      if (ok) store_tile<kRev>(a, sm, tmem, u0, segs, k1 - 1, abort);
+    } else if ((tid & 31) == 0) {
+      mma_role(sm, tmem, k0, k1, group, abort);
     }
-    if (h != cur_h) {
-      build_tables(a, h, sm, mu_re, mu_im, dl_re, dl_im, sig_k, sig_g);
-      cur_h = h;
-    }
-    // this thread's state and the last anchor, as (own component, other component)
-    float xo = 0.f, xt = 0.f, ao = 0.f, at = 0.f;
-
-    for (int seg = 0; seg < segs && ok; ++seg) {
-      // ---- u chunks -> scaled f16 pairs (thread = chunk column) ----
-      int rl, c;
-      if (a.R > 0) {
-        rl = tid / a.C;
-        c = tid - rl * a.C;
-      } else {
-        rl = 0;
-        c = seg * kCols + tid;
-      }
-      const bool valid = (a.R > 0) ? (rl < nrows) : (c < a.C);
-      const size_t rowoff = ((size_t)(b0 + (valid ? rl : 0)) * a.H + h) * (size_t)a.L;
-      const int k0 = c * kT;
-      float inv_su;
-      {
-        float v[64];
-        load_chunk<kRev>(a.u + rowoff, a.L, k0, valid, v);
-        float m = 0.f;
-#pragma unroll
-        for (int t = 0; t < kT; ++t) m = fmaxf(m, fabsf(v[t]));
-        const int es = scale_exp(m);
-        const float su = exp2i(es);
-#pragma unroll
-        for (int t = 0; t < kT; ++t) v[t] *= su;
-        store_row64(sm + kUHi, sm + kULo, tid, v);
-        inv_su = exp2i(-es);
-        sInvU[tid] = inv_su * (1.f / 16384.f);  // also undoes the 2^14 of Q
-      }
-      tc::fence_proxy_async_smem();
-      tc::fence_before_sync();
-      __syncthreads();
-      if (tid == 0) {
-        tc::fence_after_sync();
-        constexpr uint32_t id1 = tc::idesc_f16_f32(128, 128);
-        const uint64_t qh = tc::smem_desc_k_sw128(sm + kQHi), ql = tc::smem_desc_k_sw128(sm + kQLo);
-        const uint64_t uh = tc::smem_desc_k_sw128(sm + kUHi), ul = tc::smem_desc_k_sw128(sm + kULo);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          tc::mma_kind_f16(tmem, qh + 2 * kk, uh + 2 * kk, id1, kk != 0);
-          tc::mma_kind_f16(tmem, qh + 2 * kk, ul + 2 * kk, id1, 1);
-          tc::mma_kind_f16(tmem, ql + 2 * kk, uh + 2 * kk, id1, 1);
-        }
-        tc::mma_commit(bar);
-      }
-      ok = __syncthreads_and(tc::mbar_wait(bar, parity));
-      parity ^= 1;
-      if (!ok) break;
-      tc::fence_after_sync();
-
-      // ---- carries along the chunks (thread = state row) ----
-      // The largest |Xin| of each batch row in the tile goes to sRowMax[row][warp].
-      float lmax = 0.f;
-      int row_i = 0;
-      {
-        // row mode: a row starts every C columns and is anchored 32, 64, .. chunks into it;
-        // one-row mode: anchors at every 32nd column (tiles hold 128 = 4 x 32 chunks)
-        int next_reset = (a.R > 0) ? 0 : (1 << 30);
-        int next_anchor = 0;
-#pragma unroll 1
-        for (int blk = 0; blk < 4; ++blk) {
-          float s[32], o[32];
-          tc::tmem_ld32(tS + blk * 32, s);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int g = blk * 32 + j;
-            const float sother = __shfl_xor_sync(0xffffffffu, s[j], 1);
-            const float iv = sInvU[g];
-            if (g == next_anchor) {
-              xo = fmaf(dl_re, ao, fmaf(-dl_im, at, xo));
-              xt = fmaf(dl_re, at, fmaf(dl_im, ao, xt));
-              ao = xo;
-              at = xt;
-              next_anchor += 32;
-            }
-            if (g == next_reset) {
-              if (g > 0) {
-                const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(lmax));
-                if (lane == 0) sRowMax[row_i * 4 + warp] = __uint_as_float(m);
-                ++row_i;
-                lmax = 0.f;
-              }
-              xo = xt = ao = at = 0.f;
-              next_reset += reset_every;
-              next_anchor = g + 32;
-            }
-            o[j] = xo;
-            lmax = fmaxf(lmax, fabsf(xo));
-            const float no = fmaf(mu_re, xo, fmaf(-mu_im, xt, s[j] * iv));
-            const float nt = fmaf(mu_re, xt, fmaf(mu_im, xo, sother * iv));
-            xo = no;
-            xt = nt;
-          }
-          tc::tmem_st32(tS + blk * 32, o);
-        }
-        tc::tmem_wait_st();
-        const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(lmax));
-        if (lane == 0) sRowMax[row_i * 4 + warp] = __uint_as_float(m);
-      }
-      __syncthreads();
-      // Xin scale of this thread's chunk column (the scale of its batch row)
-      float inv_sx;
-      {
-        const int row = (a.R > 0) ? tid / a.C : 0;
-        const float xmax = fmaxf(fmaxf(sRowMax[row * 4], sRowMax[row * 4 + 1]),
-                                 fmaxf(sRowMax[row * 4 + 2], sRowMax[row * 4 + 3]));
-        const int ex = scale_exp(xmax);
-        sColSx[tid] = exp2i(ex);
-        inv_sx = exp2i(-ex);
-      }
-      __syncthreads();
-      // ---- Xin -> scaled f16 pairs, A operand [chunk g][state row r] ----
-      {
-        const int r = tid;
-        const uint32_t kbase = uint32_t(r >> 6) * 16384u + uint32_t(r & 7) * 2u;
-        const uint32_t kc = uint32_t((r & 63) >> 3);
-#pragma unroll 1
-        for (int blk = 0; blk < 4; ++blk) {
-          float v[32];
-          tc::tmem_ld32(tS + blk * 32, v);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int g = blk * 32 + j;
-            const float x = v[j] * sColSx[g];
-            const __half hh = __float2half_rn(x);
-            const __half hl = __float2half_rn(x - __half2float(hh));
-            const uint32_t off = kbase + uint32_t(g) * 128u + ((kc ^ uint32_t(g & 7)) << 4);
-            *reinterpret_cast<__half*>(sm + kXHi + off) = hh;
-            *reinterpret_cast<__half*>(sm + kXLo + off) = hl;
-          }
-        }
-      }
-      tc::fence_proxy_async_smem();
-      tc::fence_before_sync();
-      __syncthreads();
-      if (tid == 0) {
-        tc::fence_after_sync();
-        constexpr uint32_t id2 = tc::idesc_f16_f32(128, 64);
-        const uint64_t uh = tc::smem_desc_k_sw128(sm + kUHi), ul = tc::smem_desc_k_sw128(sm + kULo);
-        const uint64_t th = tc::smem_desc_k_sw128(sm + kTkHi), tl = tc::smem_desc_k_sw128(sm + kTkLo);
-        const uint64_t xh = tc::smem_desc_k_sw128(sm + kXHi), xl = tc::smem_desc_k_sw128(sm + kXLo);
-        const uint64_t gh = tc::smem_desc_k_sw128(sm + kGHi), gl = tc::smem_desc_k_sw128(sm + kGLo);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          tc::mma_kind_f16(tmem + 128, uh + 2 * kk, th + 2 * kk, id2, kk != 0);
-          tc::mma_kind_f16(tmem + 128, uh + 2 * kk, tl + 2 * kk, id2, 1);
-          tc::mma_kind_f16(tmem + 128, ul + 2 * kk, th + 2 * kk, id2, 1);
-        }
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t ao = kb * (16384 >> 4) + 2 * kk, bo = kb * (8192 >> 4) + 2 * kk;
-            tc::mma_kind_f16(tmem + 192, xh + ao, gh + bo, id2, (kb | kk) != 0);
-            tc::mma_kind_f16(tmem + 192, xh + ao, gl + bo, id2, 1);
-            tc::mma_kind_f16(tmem + 192, xl + ao, gh + bo, id2, 1);
-          }
-        tc::mma_commit(bar);
-      }
-      ok = __syncthreads_and(tc::mbar_wait(bar, parity));
-      parity ^= 1;
-      if (!ok) break;
-      tc::fence_after_sync();
-
-      // ---- outputs (thread = chunk column) ----
-      {
-        const float ay = inv_su / sig_k;
-        const float by = inv_sx / sig_g;
-        float* yrow = a.y + rowoff;
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          float y1[32], y2[32];
-          tc::tmem_ld32(tY1 + half * 32, y1);
-          tc::tmem_ld32(tY2 + half * 32, y2);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) y1[j] = fmaf(y1[j], ay, y2[j] * by);
-          if (valid) store_part<kRev>(yrow, a.L, k0 + half * 32, y1);
-        }
-      }
-      tc::fence_before_sync();
-    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (*abort) break;
+    k0 = k1;
   }
-  if (!ok) report_status(a.status, DLR_ERR_TIMEOUT);
+  if (*abort) report_status(a.status, DLR_ERR_TIMEOUT);
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
@@ -571,11 +975,14 @@ int sm_count() {
 }
 
 template <bool kRev>
-cudaError_t launch_one(const TcScanArgs& a, cudaStream_t s) {
+cudaError_t launch_one(const TcScanArgs& a, uint8_t* ws, cudaStream_t s) {
   cudaError_t e = max_smem_once<dlr_scan_tc_kernel<kRev>>(kSmemBytes);
   if (e != cudaSuccess) return e;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorUnknown;
+  dlr_scan_tc_tables<<<a.H, 256, kTbBytes, s>>>(a, ws);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   const int grid = std::min(a.units, sms);
   dlr_scan_tc_kernel<kRev><<<grid, kThreads, kSmemBytes, s>>>(a);
   return cudaGetLastError();
@@ -583,10 +990,13 @@ cudaError_t launch_one(const TcScanArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-// N <= 64 complex states; u, y [B, H, L]; bidirectional adds the reversed pass.
+size_t scan_tc_workspace_bytes(int64_t H) { return (size_t)H * kBlobBytes; }
+
+// N <= 64 complex states; u, y [B, H, L]; bidirectional adds the reversed pass (run after the
+// forward one, reusing the workspace for its tables).
 cudaError_t launch_dlr_scan_tc(const float* u, const float* lr, const float* li, const float* W,
                                const float* lr2, const float* li2, const float* W2, bool bidir,
-                               int B, int H, int N, int L, float* y, int* status,
+                               int B, int H, int N, int L, float* y, void* ws, int* status,
                                cudaStream_t s) {
   TcScanArgs a{};
   a.u = u;
@@ -606,15 +1016,16 @@ cudaError_t launch_dlr_scan_tc(const float* u, const float* lr, const float* li,
     a.units = B * H;
   }
   a.status = status;
+  a.tables = static_cast<const uint8_t*>(ws);
   a.log_re = lr;
   a.log_im = li;
   a.W = reinterpret_cast<const float2*>(W);
-  cudaError_t e = launch_one<false>(a, s);
+  cudaError_t e = launch_one<false>(a, static_cast<uint8_t*>(ws), s);
   if (e != cudaSuccess || !bidir) return e;
   a.log_re = lr2;
   a.log_im = li2;
   a.W = reinterpret_cast<const float2*>(W2);
-  return launch_one<true>(a, s);
+  return launch_one<true>(a, static_cast<uint8_t*>(ws), s);
 }
 
 }  // namespace dlr

@@ -50,6 +50,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
+// try_wait that may suspend the thread for up to about `hint_ns` nanoseconds while the phase
+// is incomplete (instead of returning at once), so a waiting thread does not spin on issue.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "  selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 // Waits for the phase with the given parity to complete; false if `limit_ns` ran out.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           uint64_t limit_ns = kWaitLimitNs) {
@@ -70,6 +87,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Contiguous copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from global to
+// shared memory, completing that many bytes of transaction count on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -136,6 +164,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
       : "memory");
 }
+// Stores 16 consecutive 32-bit columns of the warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -158,6 +196,20 @@ __device__ __forceinline__ uint64_t smem_desc_k_sw128(const void* tile) {
   uint64_t d = (addr & 0x3FFFFull) >> 4;
   d |= uint64_t(1) << 16;
   d |= uint64_t(1024 >> 4) << 32;
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(2) << 61;
+  return d;
+}
+
+// The same for an MN-major tile with 128-byte swizzling: atoms of 8 K-rows x 64 MN-elements
+// (one 128-byte line per K-row); `lbo` = byte stride between atoms along MN, `sbo` = byte
+// stride between 8-row groups along K.
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(const void* tile, uint32_t lbo,
+                                                       uint32_t sbo) {
+  const uint64_t addr = smem_u32(tile);
+  uint64_t d = (addr & 0x3FFFFull) >> 4;
+  d |= uint64_t(lbo >> 4) << 16;
+  d |= uint64_t(sbo >> 4) << 32;
   d |= uint64_t(1) << 46;
   d |= uint64_t(2) << 61;
   return d;

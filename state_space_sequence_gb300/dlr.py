@@ -46,9 +46,12 @@ def _load():
         lib.dlr_conv_spectrum.restype = i32
         lib.dlr_conv_apply.argtypes = [P, i64, i64, i64, P, P, sz, P]
         lib.dlr_conv_apply.restype = i32
-        lib.dlr_scan.argtypes = [P, P, P, P, P, P, P, i32, i64, i64, i64, i64, P, P]
+        lib.dlr_scan_workspace_size.argtypes = [i64, i64, i64, i64]
+        lib.dlr_scan_workspace_size.restype = sz
+        lib.dlr_scan.argtypes = [P, P, P, P, P, P, P, i32, i64, i64, i64, i64, P, P, sz, P]
         lib.dlr_scan.restype = i32
-        lib.dlr_scan_ex.argtypes = [P, P, P, P, P, P, P, i32, i64, i64, i64, i64, P, i32, P]
+        lib.dlr_scan_ex.argtypes = [P, P, P, P, P, P, P, i32, i64, i64, i64, i64, P, i32, P, sz,
+                                    P]
         lib.dlr_scan_ex.restype = i32
         lib.s5_workspace_size.argtypes = [i64, i64, i64, i64, i32]
         lib.s5_workspace_size.restype = sz
@@ -159,10 +162,16 @@ def dlr_conv_apply(u, workspace, out=None, stream=None):
 SCAN_ALGO = {"auto": 0, "fp32": 1, "tensor": 2}
 
 
-def dlr_scan(u, fwd, bwd=None, out=None, stream=None, algo: str = "auto"):
+def dlr_scan_workspace_size(B: int, H: int, N: int, L: int) -> int:
+    """Bytes of workspace the tensor-core scan needs (0 when N > 64)."""
+    return int(_load().dlr_scan_workspace_size(B, H, N, L))
+
+
+def dlr_scan(u, fwd, bwd=None, out=None, stream=None, algo: str = "auto", workspace=None):
     """DLR recurrence (Re cast) as a chunked scan; ``fwd``/``bwd`` = (log_re, log_im, W).
     ``algo``: "fp32" (float32 FMA kernel), "tensor" (tensor-core contractions, N <= 64) or
-    "auto" (tensor when N <= 64)."""
+    "auto" (tensor when N <= 64). The tensor path takes a uint8 device ``workspace`` of
+    dlr_scan_workspace_size bytes (allocated here when not given)."""
     _check_f32(u)
     B, H, L = u.shape
     lr, li, W = _params(fwd)
@@ -173,9 +182,14 @@ def dlr_scan(u, fwd, bwd=None, out=None, stream=None, algo: str = "auto"):
     if out is None:
         out = torch.empty_like(u)
     _check_f32(out)
+    need = dlr_scan_workspace_size(B, H, N, L) if algo != "fp32" else 0
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=u.device)
+    ws_bytes = workspace.numel() if workspace is not None else 0
     _ok("dlr_scan", _load().dlr_scan_ex(_ptr(u), _ptr(lr), _ptr(li), _ptr(W), _ptr(lr2),
                                         _ptr(li2), _ptr(W2), 1 if bwd is not None else 0, B, H,
-                                        N, L, _ptr(out), SCAN_ALGO[algo], _stream(stream)))
+                                        N, L, _ptr(out), SCAN_ALGO[algo], _ptr(workspace),
+                                        ws_bytes, _stream(stream)))
     return out
 
 

@@ -44,7 +44,7 @@ def test_status_strings_and_version(lib):
     lib.dlr_status_string.restype = ctypes.c_char_p
     assert lib.dlr_status_string(0) == b"DLR_OK"
     assert lib.dlr_status_string(4) == b"DLR_ERR_TIMEOUT"
-    assert lib.dlr_abi_version() == 1
+    assert lib.dlr_abi_version() == 2
 
 
 def test_host_validation_rejects_bad_arguments(lib):
@@ -59,16 +59,31 @@ def test_host_validation_rejects_bad_arguments(lib):
     assert lib.dlr_kernel(ctypes.c_void_p(0x1004), fake, fake, 2, 4, 8, 0, fake, None) == 1
     # bad cast enum
     assert lib.dlr_kernel(fake, fake, fake, 2, 4, 8, 7, fake, None) == 1
-    lib.dlr_scan.argtypes = [P] * 7 + [ctypes.c_int, i64, i64, i64, i64, P, P]
+    sz = ctypes.c_size_t
+    lib.dlr_scan.argtypes = [P] * 7 + [ctypes.c_int, i64, i64, i64, i64, P, P, sz, P]
     # N above the scan's limit -> unsupported
     assert lib.dlr_scan(fake, fake, fake, fake, None, None, None, 0, 1, 1, 129, 8,
-                        ctypes.c_void_p(0x9000), None) == 2
+                        ctypes.c_void_p(0x9000), None, 0, None) == 2
     # bidirectional without second parameter set
     assert lib.dlr_scan(fake, fake, fake, fake, None, None, None, 1, 1, 1, 4, 8,
-                        ctypes.c_void_p(0x9000), None) == 1
+                        ctypes.c_void_p(0x9000), None, 0, None) == 1
     # overlapping u and y
     assert lib.dlr_scan(fake, fake, fake, fake, None, None, None, 0, 1, 1, 4, 64,
-                        ctypes.c_void_p(0x1010), None) == 1
+                        ctypes.c_void_p(0x1010), None, 0, None) == 1
+    # tensor-core path (N <= 64) without its workspace
+    assert lib.dlr_scan(fake, fake, fake, fake, None, None, None, 0, 1, 1, 4, 64,
+                        ctypes.c_void_p(0x9000), None, 0, None) == 5
+    lib.dlr_scan_ex.argtypes = [P] * 7 + [ctypes.c_int, i64, i64, i64, i64, P, ctypes.c_int, P,
+                                          sz, P]
+    # tensor-core path forced above 64 states -> unsupported; unknown algorithm -> invalid
+    assert lib.dlr_scan_ex(fake, fake, fake, fake, None, None, None, 0, 1, 1, 65, 64,
+                           ctypes.c_void_p(0x9000), 2, fake, 1 << 30, None) == 2
+    assert lib.dlr_scan_ex(fake, fake, fake, fake, None, None, None, 0, 1, 1, 4, 64,
+                           ctypes.c_void_p(0x9000), 7, None, 0, None) == 1
+    # the float32 kernel needs no workspace (validation passes up to the launch, which is not
+    # reached here: N above 128 keeps the call on the host)
+    assert lib.dlr_scan_ex(fake, fake, fake, fake, None, None, None, 0, 1, 1, 129, 64,
+                           ctypes.c_void_p(0x9000), 1, None, 0, None) == 2
     lib.dlr_conv.argtypes = [P, P, P, ctypes.c_int, i64, i64, i64, P, P, ctypes.c_size_t, P]
     # missing workspace
     assert lib.dlr_conv(fake, fake, None, 0, 1, 1, 16, ctypes.c_void_p(0x9000), None, 0,
@@ -88,6 +103,11 @@ def test_workspace_queries(lib):
     # L = 4096 -> n = 4096: twiddle tables of n and 2n points + spectra H*(n+1) complex
     assert lib.dlr_conv_workspace_size(256, 4096, 0) == 4096 * 8 + 8192 * 8 + 256 * 4097 * 8
     assert lib.dlr_conv_workspace_size(0, 4096, 0) == 0
+    lib.dlr_scan_workspace_size.restype = ctypes.c_size_t
+    lib.dlr_scan_workspace_size.argtypes = [ctypes.c_int64] * 4
+    # one table blob of 83968 bytes per channel for the tensor-core scan; none above 64 states
+    assert lib.dlr_scan_workspace_size(8, 256, 64, 4096) == 256 * 83968
+    assert lib.dlr_scan_workspace_size(8, 256, 65, 4096) == 0
     lib.s5_workspace_size.restype = ctypes.c_size_t
     lib.s5_workspace_size.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int]
     assert lib.s5_workspace_size(8, 16384, 512, 256, 0) >= 8 * 16384 * 512 * 4
