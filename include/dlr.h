@@ -206,6 +206,10 @@ dlr_status dlr_selftest_timeout(int limit_ms, dlr_stream_t stream);
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* dlr_status_string(dlr_status status);
 
+/* The CUDA runtime's message for the last error that a call made on this host thread
+ * reported as DLR_ERR_CUDA ("no error" if none). The string is static; do not free it. */
+const char* dlr_last_cuda_error(void);
+
 /* Library ABI version (incremented on any signature change). */
 int dlr_abi_version(void);
 

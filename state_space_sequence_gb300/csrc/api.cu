@@ -45,7 +45,14 @@ int* status_word() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-dlr_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DLR_OK : DLR_ERR_CUDA; }
+// The last CUDA error a call of this thread turned into DLR_ERR_CUDA (for diagnostics).
+thread_local const char* t_last_cuda_error = "no error";
+
+dlr_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return DLR_OK;
+  t_last_cuda_error = cudaGetErrorString(e);
+  return DLR_ERR_CUDA;
+}
 
 bool ranges_overlap(const void* a, size_t an, const void* b, size_t bn) {
   uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
@@ -63,6 +70,8 @@ dlr_status check_params(const float* log_re, const float* log_im, const float* W
 extern "C" {
 
 int dlr_abi_version(void) { return 2; }
+
+const char* dlr_last_cuda_error(void) { return t_last_cuda_error; }
 
 const char* dlr_status_string(dlr_status s) {
   switch (s) {

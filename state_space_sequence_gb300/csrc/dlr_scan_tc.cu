@@ -26,29 +26,36 @@
 // rounding of a - a_hi), and each product is hi*hi + hi*lo + lo*hi (three MMAs, f32
 // accumulation in tensor memory; the dropped lo*lo term is below 2^-22 relative). Before the
 // split every operand is scaled by a power of two so that its largest entry lies in
-// [2^13, 2^14): per chunk for u, per batch row and tile for Xin, per channel for K and G,
+// [2^13, 2^14): per batch row and tile for u and for Xin, per channel for K and G,
 // 2^14 for Q (|Q| <= 1), so that one row's scale never depends on another row's magnitude.
-// The scalings are exact and undone in fp32 when S is read and when y is written.
-// Powers lambda^j are evaluated from an exactly reduced phase (lam_pow) for j = 8a and j < 8
-// and combined by one complex product, so no power carries a long multiplication chain.
+// The scalings are exact and undone in fp32 when Xin and y are written (the carries run on
+// S in its scaled units; a row continued into the next tile is rescaled to that tile's units).
+// Powers lambda^j are evaluated from an exactly reduced phase (lam_pow) for j = 16q + 4c and
+// j < 4 and combined by one complex product, so no power carries a long multiplication chain.
 //
 // Two kernels. dlr_scan_tc_tables (one CTA per channel) evaluates the per-channel tables --
 // Q, the Toeplitz block of K_0..K_63 and G as scaled f16 pairs in the exact byte layout the
 // MMAs read, lambda^64, the re-anchoring correction and the two scales -- into a workspace
-// blob per channel. dlr_scan_tc_kernel then runs one persistent CTA per SM with three warp
-// roles joined by mbarriers and two tiles in flight:
-//   warps 0-3  "scan":  thread r owns TMEM lane r = state row r; runs step 2 on S, writes Xin
-//                       (scaled f16 pair, MN-major) to shared memory; loads Q into TMEM when
-//                       the channel changes,
-//   warps 4-7  "io":    thread g owns TMEM lane g = chunk g; loads u and writes its scaled f16
-//                       pair (tile k+1), then reads Y1, Y2 and stores y (tile k),
-//   warp 8, lane 0:     issues the MMAs, GEMM1 or GEMM2, whichever has its inputs first.
-// Buffers: u operand x2, S accumulator x2 (TMEM), Xin x1, Y1/Y2 x1; Q lives in TMEM as the A
-// operand of GEMM1, the Toeplitz block and G in shared memory (one bulk copy per channel).
+// blob per channel. dlr_scan_tc_kernel then runs one persistent CTA per SM with four roles
+// joined by mbarriers, two tiles in flight:
+//   warps 0-3   "scan": thread r owns TMEM lane r = state row r; runs step 2 on S in place
+//                       (S becomes Xin), and the per-row Xin scales,
+//   warps 4-7   "conv": loads u (3D TMA tiles into a staging buffer, or plain loads when the
+//                       rows are not whole chunks) and writes its scaled f16 pair, MN-major
+//                       (tile k); then reads Xin from TMEM (thread = state row) and writes its
+//                       scaled f16 pair, MN-major (tile k-1); loads Q into TMEM for a new
+//                       channel,
+//   warps 8-11  "epi":  thread g owns TMEM lane g = chunk g; reads Y1, Y2, scales them and
+//                       writes y through a shared-memory staging image with row-coalesced
+//                       stores (the staging is the u operand buffer GEMM2 has finished with),
+//   warp 12, lane 0:    issues the MMAs, GEMM2 of the oldest tile whose Xin is ready, else
+//                       GEMM1 of the next tile whose u is ready, and copies the Toeplitz and G
+//                       operands of a new channel in between GEMM2s.
+// Buffers: u operand x2, S accumulator x2 (TMEM), Xin x1, Y1/Y2 x1, Q x2 (TMEM), Toeplitz and
+// G x1 (shared memory), u staging x1.
 // Units of work: a tile holds floor(128 / C) whole rows when a row has C <= 128 chunks
 // (several batch rows of one channel), otherwise one row walks its tiles in order and carries
-// its state from tile to tile. A CTA takes a contiguous range of units; at a change of channel
-// the pipeline drains and the next channel's tables are copied in.
+// its state from tile to tile. A CTA takes a contiguous range of units.
 //
 // Every wait is bounded (global timer, 1 s); a wait that runs out sets a CTA-wide abort flag,
 // all roles leave their loops at the next wait or role barrier, and the kernel records
@@ -57,6 +64,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstring>
 
 #include "dlr_common.cuh"
 #include "tc_ptx.cuh"
@@ -64,41 +72,50 @@
 namespace dlr {
 namespace {
 
-constexpr int kT = 64;        // steps per chunk
-constexpr int kCols = 128;    // chunks per tile
-constexpr int kNMax = 64;     // complex states (2N real rows of the state GEMM)
-constexpr int kPw = kT + 1;   // powers lambda^0 .. lambda^64
-constexpr int kThreads = 288; // warps 0-3 scan, 4-7 io, 8 mma
-constexpr int kScanBar = 1, kIoBar = 2;  // named barriers of the scan and io warps
+constexpr int kT = 64;          // steps per chunk
+constexpr int kCols = 128;      // chunks per tile
+constexpr int kThreads = 416;   // warps 0-3 scan, 4-7 conv, 8-11 epi, 12 mma
+constexpr int kScanBar = 1, kConvBar = 2, kEpiBar = 3;  // named barriers (128 threads each)
 
-// TMEM columns (512 allocated): Q hi/lo (A operand of GEMM1, 2 f16 per column), S x2, Y1, Y2
+// TMEM columns (512 allocated): Q (hi 32 + lo 32 columns: A operand of GEMM1, two f16 per
+// column), S x2, Y1 x2, Y2
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTQHi = 0, kTQLo = 32, kTS = 64, kTY1 = 320, kTY2 = 384;
+constexpr uint32_t kTQ = 0, kTS = 64, kTY1 = 320, kTY2 = 448;
 
-// shared memory (bytes from a 1024-byte aligned base). K-major f16 tiles use the 128-byte
-// swizzled layout: rows of 64 elements (128 bytes), 8-row atoms of 1024 bytes, 16-byte chunk
-// index XOR (row & 7); K = 128 operands are two such tiles ("K-blocks") one after the other.
-// Xin is MN-major: atoms of 8 K-rows (state rows) x 64 chunks (128 bytes per K-row, chunk
-// index XOR (K-row & 7)); atom (K-group kg, M-half ma) at kg * 2048 + ma * 1024.
-constexpr uint32_t kU = 0;              // u operand [128 chunks x 64], 2 buffers of hi + lo
+// Shared memory (bytes from a 1024-byte aligned base). f16 operand tiles use 128-byte
+// swizzling. K-major (Toeplitz, G): rows of 64 elements (128 bytes), 8-row atoms of 1024
+// bytes, 16-byte chunk index XOR (row & 7); K = 128 operands are two such tiles one after the
+// other. MN-major (u operand, Xin): atoms of 8 K-rows x 64 MN-elements (128 bytes per K-row,
+// chunk index XOR (K-row & 7)); atom (K-group kg, MN-half ma) at kg * 2048 + ma * 1024.
+constexpr uint32_t kU = 0;                          // u operand [128 chunks x 64], x2 (hi, lo)
 constexpr uint32_t kUBuf = 32768, kULo = 16384;
-constexpr uint32_t kXHi = 65536, kXLo = 98304;      // Xin [128 chunks x 128 rows], MN-major
+constexpr uint32_t kXHi = 65536, kXLo = 98304;      // Xin [128 chunks x 128 rows]
 constexpr uint32_t kTkHi = 131072, kTkLo = 139264;  // Toeplitz [64 t x 64 s], K-major
 constexpr uint32_t kGHi = 147456, kGLo = 163840;    // G [64 t x 128 rows], K-major
-constexpr uint32_t kInvU = 180224;   // float[2][128] 2^-14 / (u scale of chunk g), by parity
-constexpr uint32_t kInvSu = kInvU + 1024;   // float[2][128] 1 / (u scale of chunk g)
-constexpr uint32_t kColSx = kInvSu + 1024;  // float[2][128] Xin scale of chunk g
+constexpr uint32_t kStage = 180224;  // u staging: [2 halves][128 lines][32 floats], swizzled
+constexpr uint32_t kRowEs = kStage + 32768;  // int[2][128] u scale exponent of each row
+constexpr uint32_t kRowMaxU = kRowEs + 1024;  // uint[128] max |u| of each row (scratch)
+constexpr uint32_t kAy = kRowMaxU + 512;      // float[2][128] 1 / (u scale * K scale)
+constexpr uint32_t kColSx = kAy + 1024;     // float[2][128] Xin scale of chunk g
 constexpr uint32_t kBy = kColSx + 1024;     // float[2][128] 1 / (Xin scale * G scale)
 constexpr uint32_t kRowMax = kBy + 1024;    // float[128][4] per-row, per-warp max |Xin|
-constexpr uint32_t kSig = kRowMax + 2048;   // float[4] K scale, G scale of the channel
-constexpr uint32_t kBars = kSig + 16;       // mbarriers
+constexpr uint32_t kChoice = kRowMax + 2048;     // int: the conv warps' next step
+constexpr uint32_t kBars = kChoice + 16;         // mbarriers
 // A waiter may trail the phase it waits for by at most one completed phase (the parity test
-// cannot tell phase j from phase j + 2), so every wait below is on a barrier that cannot
-// complete twice more before the waiter has passed: the u buffers get their own "free"
-// barriers instead of sharing the GEMM2 one.
-constexpr int kBarUFull = 0, kBarSFull = 2, kBarSFree = 4, kBarXFull = 6, kBarG2 = 7,
-              kBarYFree = 8, kBarTab = 9, kBarScale = 10, kBarUFree = 12, kBarTabLoad = 14,
-              kNumBars = 15;
+// cannot tell phase j from phase j + 2): every wait below is on a barrier that cannot
+// complete twice more before the waiter has passed it.
+constexpr int kBarStage = 0,   // u tile landed in the staging buffer (TMA bytes)
+    kBarUFull = 1,             // [2] u operand and its scales written (conv, 128)
+    kBarG1 = 3,                // [2] GEMM1 + Toeplitz done: S, Y1 ready, u buffer free (commit)
+    kBarSFree = 5,             // [2] Xin read out of S (conv, 128)
+    kBarXpReady = 7,           // [2] carries done, Xin in S, Xin scales written (scan, 128)
+    kBarXFull = 9,             // Xin operand written (conv, 128)
+    kBarG2 = 10,               // GEMM2 (state part) done: Y2 ready, Xin buffer free (commit)
+    kBarY1Free = 11,           // [2] Y1 read out of TMEM (epi, 128)
+    kBarY2Free = 13,           // Y2 read out of TMEM (epi, 128)
+    kBarTabTk = 14,            // Toeplitz operand copied (bytes)
+    kBarTabG = 15,             // G operand copied (bytes)
+    kNumBars = 16;
 constexpr uint32_t kSlot = kBars + 8 * kNumBars;  // TMEM base address
 constexpr uint32_t kAbort = kSlot + 4;            // abort flag
 constexpr uint32_t kEnd = kAbort + 4;
@@ -108,7 +125,7 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 // Per-channel table blob in the workspace (bytes). Its first 48 KB are the shared-memory image
 // of the Toeplitz and G operands (kTkHi .. kGLo + 16 KB), copied in one piece.
 constexpr uint32_t kBlobSmem = kGLo + 16384 - kTkHi;  // 49152
-constexpr uint32_t kBlobQ = kBlobSmem;       // uint32 [128 rows][64]: 32 hi then 32 lo words
+constexpr uint32_t kBlobQ = kBlobSmem;        // uint32 [128 rows][64]: 32 hi then 32 lo words
 constexpr uint32_t kBlobMu = kBlobQ + 32768;  // float4 [64]: lambda^64 (re, im), correction
 constexpr uint32_t kBlobSig = kBlobMu + 1024; // float [4]: K scale, G scale
 constexpr uint32_t kBlobBytes = kBlobSig + 1024;  // 83968, a multiple of 1024
@@ -131,6 +148,8 @@ struct TcScanArgs {
   int R;            // rows per tile (C <= 128), 0: one row per unit, walked tile by tile
   int tiles_per_h;  // ceil(B / R) when R > 0
   int units;
+  int tma;          // u tiles by TMA (L % 64 == 0 and C in {32, 64, 128} or C > 128, C % 64 == 0)
+  int bc;           // chunks per TMA box (32 or 64)
   const uint8_t* tables;  // H table blobs of kBlobBytes
   int* status;
 };
@@ -151,20 +170,6 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
   const __half2 l = __floats2half2_rn(a - f.x, b - f.y);
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = *reinterpret_cast<const uint32_t*>(&l);
-}
-
-// One 64-element K-major row of an f16 operand tile pair (swizzled as described above).
-__device__ __forceinline__ void store_row64(uint8_t* hi_tile, uint8_t* lo_tile, int row,
-                                            const float (&v)[64]) {
-#pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) split2(v[8 * p + 2 * q], v[8 * p + 2 * q + 1], h[q], l[q]);
-    const uint32_t off = uint32_t(row) * 128u + ((uint32_t(p) ^ uint32_t(row & 7)) << 4);
-    *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
-  }
 }
 
 __device__ __forceinline__ void named_bar(int id, int n) {
@@ -210,6 +215,86 @@ __device__ __forceinline__ bool warp_wait_phase(uint64_t* bar, uint32_t parity,
   bool ok = true;
   if ((threadIdx.x & 31) == 0) ok = wait_phase(bar, parity, abort);
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// Max over the 256 threads of the tables kernel; `slot` picks 8 floats of `red`.
+__device__ __forceinline__ float block_max256(float v, float* red, int slot) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) red[slot * 8 + (threadIdx.x >> 5)] = v;
+  __syncthreads();
+  float m = red[slot * 8];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) m = fmaxf(m, red[slot * 8 + i]);
+  return m;
+}
+
+// Eight values of one K-major row of an f16 operand tile pair (16-byte chunk `chunk`), at a
+// shared or global address.
+__device__ __forceinline__ void store_chunk8(uint8_t* hi_tile, uint8_t* lo_tile, int row,
+                                             int chunk, const float* v) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) split2(v[2 * q], v[2 * q + 1], h[q], l[q]);
+  const uint32_t off = uint32_t(row) * 128u + ((uint32_t(chunk) ^ uint32_t(row & 7)) << 4);
+  *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Where tile k of this CTA lies: channel, first batch row and row count, segment of the row.
+struct TileInfo {
+  int h, b0, nrows, seg;
+};
+__device__ __forceinline__ TileInfo tile_info(const TcScanArgs& a, int u0, int segs, int k) {
+  const int unit = u0 + k / segs;
+  TileInfo t;
+  t.seg = k - (k / segs) * segs;
+  if (a.R > 0) {
+    t.h = unit / a.tiles_per_h;
+    t.b0 = (unit - t.h * a.tiles_per_h) * a.R;
+    t.nrows = min(a.R, a.B - t.b0);
+  } else {
+    t.h = unit / a.B;
+    t.b0 = unit - t.h * a.B;
+    t.nrows = 1;
+  }
+  return t;
+}
+
+// Column g of a tile: its row within the tile, chunk index within its row, batch row offset
+// (elements) and first step, and whether it is used.
+struct ColInfo {
+  size_t rowoff;
+  int rl, c, k0;
+  bool valid;
+};
+__device__ __forceinline__ ColInfo col_info(const TcScanArgs& a, const TileInfo& t, int g) {
+  ColInfo ci;
+  if (a.R > 0) {
+    ci.rl = g / a.C;
+    ci.c = g - ci.rl * a.C;
+  } else {
+    ci.rl = 0;
+    ci.c = t.seg * kCols + g;
+  }
+  ci.valid = (a.R > 0) ? (ci.rl < t.nrows) : (ci.c < a.C);
+  ci.rowoff = ((size_t)(t.b0 + (ci.valid ? ci.rl : 0)) * a.H + t.h) * (size_t)a.L;
+  ci.k0 = ci.c * kT;
+  return ci;
+}
+
+// One 64-element K-major row of an f16 operand tile pair (swizzled as described above).
+__device__ __forceinline__ void store_row64(uint8_t* hi_tile, uint8_t* lo_tile, int row,
+                                            const float (&v)[64]) {
+#pragma unroll
+  for (int p = 0; p < 8; ++p) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) split2(v[8 * p + 2 * q], v[8 * p + 2 * q + 1], h[q], l[q]);
+    const uint32_t off = uint32_t(row) * 128u + ((uint32_t(p) ^ uint32_t(row & 7)) << 4);
+    *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
 }
 
 // u_{g,t} for t < 64 of the chunk starting at step k0 of a row (the reversed row when kRev);
@@ -270,72 +355,6 @@ __device__ __forceinline__ void store_part(float* __restrict__ row, int L, int k
         else row[L - 1 - kb - j] += o[j];
       }
   }
-}
-
-// Where tile k of this CTA lies: channel, first batch row and row count, segment of the row.
-struct TileInfo {
-  int h, b0, nrows, seg;
-};
-__device__ __forceinline__ TileInfo tile_info(const TcScanArgs& a, int u0, int segs, int k) {
-  const int unit = u0 + k / segs;
-  TileInfo t;
-  t.seg = k - (k / segs) * segs;
-  if (a.R > 0) {
-    t.h = unit / a.tiles_per_h;
-    t.b0 = (unit - t.h * a.tiles_per_h) * a.R;
-    t.nrows = min(a.R, a.B - t.b0);
-  } else {
-    t.h = unit / a.B;
-    t.b0 = unit - t.h * a.B;
-    t.nrows = 1;
-  }
-  return t;
-}
-
-// Column g of a tile: its batch row offset (elements) and first step, and whether it is used.
-struct ColInfo {
-  size_t rowoff;
-  int k0;
-  bool valid;
-};
-__device__ __forceinline__ ColInfo col_info(const TcScanArgs& a, const TileInfo& t, int g) {
-  int rl, c;
-  if (a.R > 0) {
-    rl = g / a.C;
-    c = g - rl * a.C;
-  } else {
-    rl = 0;
-    c = t.seg * kCols + g;
-  }
-  ColInfo ci;
-  ci.valid = (a.R > 0) ? (rl < t.nrows) : (c < a.C);
-  ci.rowoff = ((size_t)(t.b0 + (ci.valid ? rl : 0)) * a.H + t.h) * (size_t)a.L;
-  ci.k0 = c * kT;
-  return ci;
-}
-
-// Max over the 256 threads of the tables kernel; `slot` picks 8 floats of `red`.
-__device__ __forceinline__ float block_max256(float v, float* red, int slot) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if ((threadIdx.x & 31) == 0) red[slot * 8 + (threadIdx.x >> 5)] = v;
-  __syncthreads();
-  float m = red[slot * 8];
-#pragma unroll
-  for (int i = 1; i < 8; ++i) m = fmaxf(m, red[slot * 8 + i]);
-  return m;
-}
-
-// Eight values of one K-major row of an f16 operand tile pair (16-byte chunk `chunk`), at a
-// shared or global address.
-__device__ __forceinline__ void store_chunk8(uint8_t* hi_tile, uint8_t* lo_tile, int row,
-                                             int chunk, const float* v) {
-  uint32_t h[4], l[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) split2(v[2 * q], v[2 * q + 1], h[q], l[q]);
-  const uint32_t off = uint32_t(row) * 128u + ((uint32_t(chunk) ^ uint32_t(row & 7)) << 4);
-  *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
-  *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 // Per-channel tables (one CTA of 256 threads per channel h) into the channel's blob: the
@@ -449,69 +468,411 @@ __global__ void __launch_bounds__(256) dlr_scan_tc_tables(const TcScanArgs a, ui
   store_chunk8(blob, blob + (kTkLo - kTkHi), j, 2 * part + 1, tv + 8);
 }
 
-// Scan warps at the start of a channel: Q from the blob into TMEM (thread r = lane r), this
-// thread's lambda^64 and correction, the scales; thread 0 starts the bulk copy of the
-// Toeplitz and G operands into shared memory (completing on kBarTabLoad).
-__device__ __forceinline__ void load_tables(const uint8_t* blob, uint8_t* sm, uint32_t tmem,
-                                            float& mu_re, float& mu_im_signed, float& dl_re,
-                                            float& dl_im_signed, float& sig_g) {
-  const int tid = threadIdx.x, warp = tid >> 5;
+// ---- the roles ----------------------------------------------------------------------------
+
+// conv thread 0: the TMA tiles of u for tile k into the staging buffer (forward chunk order,
+// one 128-byte line per chunk and half), completing on kBarStage. Row mode: boxes of bc chunks
+// of each valid row; one-row mode: two boxes of 64 chunks. Chunks past the row (or before it,
+// reversed) read as zero.
+template <bool kRev>
+__device__ __forceinline__ void issue_u_tma(const TcScanArgs& a, const CUtensorMap* map,
+                                            uint8_t* sm, int u0, int segs, int k) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-  if (tid == 0) {
-    tc::mbar_arrive_expect_tx(&bars[kBarTabLoad], kBlobSmem);
-    tc::bulk_load(sm + kTkHi, blob, kBlobSmem, &bars[kBarTabLoad]);
-  }
-  const uint4* q = reinterpret_cast<const uint4*>(blob + kBlobQ + tid * 256);
-  float hi[32], lo[32];
+  const TileInfo ti = tile_info(a, u0, segs, k);
+  const int bc = a.bc;
+  const int nrows = (a.R > 0) ? ti.nrows : 1;
+  const int nblk = (a.R > 0) ? a.C / bc : kCols / bc;
+  tc::mbar_arrive_expect_tx(&bars[kBarStage], uint32_t(nrows * nblk * 2 * bc * 128));
+  for (int rl = 0; rl < nrows; ++rl)
+    for (int cb = 0; cb < nblk; ++cb) {
+      const int line0 = ((a.R > 0) ? rl * a.C : 0) + cb * bc;
+      const int c0 = ((a.R > 0) ? 0 : ti.seg * kCols) + cb * bc;  // first (reversed) chunk
+      const int y = kRev ? (a.C - c0 - bc) : c0;
+      const int z = (ti.b0 + rl) * a.H + ti.h;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint4 a = __ldg(q + i), b = __ldg(q + 8 + i);
-    hi[4 * i] = __uint_as_float(a.x); hi[4 * i + 1] = __uint_as_float(a.y);
-    hi[4 * i + 2] = __uint_as_float(a.z); hi[4 * i + 3] = __uint_as_float(a.w);
-    lo[4 * i] = __uint_as_float(b.x); lo[4 * i + 1] = __uint_as_float(b.y);
-    lo[4 * i + 2] = __uint_as_float(b.z); lo[4 * i + 3] = __uint_as_float(b.w);
-  }
-  const uint32_t tl = tmem + (uint32_t(warp * 32) << 16);
-  tc::tmem_st32(tl + kTQHi, hi);
-  tc::tmem_st32(tl + kTQLo, lo);
-  const float4 m = __ldg(reinterpret_cast<const float4*>(blob + kBlobMu) + (tid >> 1));
-  mu_re = m.x;
-  dl_re = m.z;
-  // the state recurrence keeps (own, other) components; the Im row runs it with the sign of
-  // the imaginary parts flipped
-  mu_im_signed = (tid & 1) ? -m.y : m.y;
-  dl_im_signed = (tid & 1) ? -m.w : m.w;
-  const float sk = __ldg(reinterpret_cast<const float*>(blob + kBlobSig));
-  sig_g = __ldg(reinterpret_cast<const float*>(blob + kBlobSig) + 1);
-  if (tid == 0) reinterpret_cast<float*>(sm + kSig)[0] = sk;
-  tc::tmem_wait_st();
-  tc::fence_before_sync();
+      for (int half = 0; half < 2; ++half)
+        tc::tma_load_3d(sm + kStage + half * 16384 + line0 * 128, map, half * 32, y, z,
+                        &bars[kBarStage]);
+    }
 }
 
-// ---- the three roles ------------------------------------------------------------------
+// Staging line holding column g's chunk when the staging is in forward chunk order and the
+// columns count reversed chunks (TMA path, reversed pass).
+__device__ __forceinline__ int mirrored_line(const TcScanArgs& a, int g) {
+  const int bc = a.bc;
+  const int base = (a.R > 0) ? (g / a.C) * a.C : 0;
+  const int c = g - base, cb = c / bc, j = c - cb * bc;
+  return base + cb * bc + (bc - 1 - j);
+}
 
-// Scan warps, one tile: carries along the chunks, then Xin as a scaled f16 pair.
+// conv warps: u chunks of tile k -> scaled f16 pair, K-major (thread = chunk column g), from
+// the staging buffer (TMA path) or straight from memory. Returns false on abort.
+// Called once u_ready(k) holds (see conv_role).
+template <bool kRev>
+__device__ __forceinline__ void convert_u(const TcScanArgs& a, uint8_t* sm, int u0, int segs,
+                                          int k, float sig_k) {
+  const int g = threadIdx.x - 128;
+  const int par = k & 1;
+  const TileInfo ti = tile_info(a, u0, segs, k);
+  const ColInfo ci = col_info(a, ti, g);
+  float v[64];
+  if (a.tma) {
+    const int line = kRev ? mirrored_line(a, g) : g;
+    const uint32_t sw = uint32_t(line & 7);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const float4 x = *reinterpret_cast<const float4*>(
+          sm + kStage + (q >> 3) * 16384 + line * 128 + ((uint32_t(q & 7) ^ sw) << 4));
+      if (!kRev) {
+        v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+      } else {
+        v[63 - 4 * q] = x.x; v[62 - 4 * q] = x.y; v[61 - 4 * q] = x.z; v[60 - 4 * q] = x.w;
+      }
+    }
+    if (!ci.valid) {
+#pragma unroll
+      for (int t = 0; t < kT; ++t) v[t] = 0.f;
+    }
+  } else {
+    load_chunk<kRev>(a.u + ci.rowoff, a.L, ci.k0, ci.valid, v);
+  }
+  // the row's largest |u| in this tile: a warp reduction when the warp's 32 chunks share a
+  // row, else one shared-memory atomic per chunk (non-negative floats order as their bits)
+  float m = 0.f;
+#pragma unroll
+  for (int t = 0; t < kT; ++t) m = fmaxf(m, fabsf(v[t]));
+  unsigned* rmax = reinterpret_cast<unsigned*>(sm + kRowMaxU);
+  const int rl = ci.rl;
+  const bool warp_row = __shfl_sync(0xffffffffu, rl, 0) == __shfl_sync(0xffffffffu, rl, 31);
+  if (warp_row) {
+    const unsigned mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+    if ((g & 31) == 0) atomicMax(&rmax[rl], mw);
+  } else {
+    atomicMax(&rmax[rl], __float_as_uint(m));
+  }
+  named_bar(kConvBar, 128);
+  const int es = scale_exp(__uint_as_float(rmax[rl]));
+  const float su = exp2i(es);
+#pragma unroll
+  for (int t = 0; t < kT; ++t) v[t] *= su;
+  uint8_t* ubuf = sm + kU + par * kUBuf;
+  store_row64(ubuf, ubuf + kULo, g, v);
+  if (ci.c == 0 || g == 0) reinterpret_cast<int*>(sm + kRowEs)[par * 128 + rl] = es;
+  reinterpret_cast<float*>(sm + kAy)[par * 128 + g] = exp2i(-es) / sig_k;
+  tc::fence_proxy_async_smem();
+}
+
+// conv warps, at the first tile of a channel: Q of the channel from its blob into TMEM
+// (thread r = lane r).
+__device__ __forceinline__ void load_q(const uint8_t* blob, uint32_t tmem) {
+  const int r = threadIdx.x - 128, warp = threadIdx.x >> 5;
+  const uint4* q = reinterpret_cast<const uint4*>(blob + kBlobQ + r * 256);
+  const uint32_t tl = tmem + (uint32_t((warp & 3) * 32) << 16) + kTQ;
+#pragma unroll
+  for (int part = 0; part < 4; ++part) {  // words 16 part .. 16 part + 15 (hi: 0, 1; lo: 2, 3)
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 x = __ldg(q + 4 * part + i);
+      w[4 * i] = x.x; w[4 * i + 1] = x.y; w[4 * i + 2] = x.z; w[4 * i + 3] = x.w;
+    }
+    tc::tmem_st16(tl + 16 * part, w);
+  }
+}
+
+// conv warps: Xin of tile k (in S, thread = state row r) -> scaled f16 pair, MN-major.
+// Called once xin_ready(k) holds (see conv_role).
+__device__ __forceinline__ void convert_xin(uint8_t* sm, uint32_t tmem, int k) {
+  const int r = threadIdx.x - 128, warp = threadIdx.x >> 5;
+  const int par = k & 1;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  tc::fence_after_sync();
+  const float* sColSx = reinterpret_cast<const float*>(sm + kColSx) + par * 128;
+  const uint32_t tS = tmem + (uint32_t((warp & 3) * 32) << 16) + kTS + uint32_t(par) * 128;
+  const uint32_t kbase = uint32_t(r >> 3) * 2048u + uint32_t(r & 7) * 128u;
+  const uint32_t kr = uint32_t(r & 7);
+#pragma unroll 1
+  for (int blk = 0; blk < 4; ++blk) {
+    float v[32];
+    tc::tmem_ld32(tS + blk * 32, v);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int g0 = blk * 32 + q * 8;
+      const float4 c0 = *reinterpret_cast<const float4*>(sColSx + g0);
+      const float4 c1 = *reinterpret_cast<const float4*>(sColSx + g0 + 4);
+      const float sc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      uint32_t h[4], l[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+        split2(v[q * 8 + 2 * p] * sc[2 * p], v[q * 8 + 2 * p + 1] * sc[2 * p + 1], h[p], l[p]);
+      const uint32_t cg = uint32_t(g0 >> 3);
+      const uint32_t off = kbase + (cg >> 3) * 1024u + (((cg & 7u) ^ kr) << 4);
+      *reinterpret_cast<uint4*>(sm + kXHi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<uint4*>(sm + kXLo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+    }
+  }
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  mbar_arrive(&bars[kBarXFull]);
+  mbar_arrive(&bars[kBarSFree + par]);
+}
+
+// conv warps over all tiles of the CTA, in the order u of tile k+1, Xin of tile k (u of tile
+// k+1 only needs GEMM1 of tile k-1 to have released its buffers, which happens long before
+// the carries of tile k are done). u of tile k+1 is requested by TMA as soon as the u of tile
+// k has been read out of the staging buffer.
+template <bool kRev>
+__device__ __forceinline__ bool conv_u_step(const TcScanArgs& a, const CUtensorMap* map,
+                                            uint8_t* sm, uint32_t tmem, int u0, int segs,
+                                            int ntiles, int k, int& cur_h, float& sig_k,
+                                            volatile int* abort) {
+  const int tid = threadIdx.x;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  const TileInfo ti = tile_info(a, u0, segs, k);
+  const bool new_channel = ti.h != cur_h;
+  const int par = k & 1;
+  // the u buffer and scale slots of tile k-2 released (its GEMM1 done, its scales read by the
+  // epilogue); at a new channel also GEMM1 of tile k-1 done (Q is reloaded); the u tile landed
+  bool ok = true;
+  if (k >= 2)
+    ok = warp_wait_phase(&bars[kBarG1 + par], ((k - 2) >> 1) & 1, abort) &&
+         warp_wait_phase(&bars[kBarY1Free + par], ((k - 2) >> 1) & 1, abort);
+  if (ok && new_channel && k >= 1)
+    ok = warp_wait_phase(&bars[kBarG1 + (par ^ 1)], ((k - 1) >> 1) & 1, abort);
+  if (ok && a.tma) ok = warp_wait_phase(&bars[kBarStage], k & 1, abort);
+  if (!named_bar_and(kConvBar, 128, ok)) return false;
+  const uint8_t* blob = a.tables + (size_t)ti.h * kBlobBytes;
+  if (new_channel) {
+    cur_h = ti.h;
+    sig_k = __ldg(reinterpret_cast<const float*>(blob + kBlobSig));
+  }
+  convert_u<kRev>(a, sm, u0, segs, k, sig_k);
+  if (new_channel) {
+    load_q(blob, tmem);
+    tc::tmem_wait_st();
+  }
+  tc::fence_before_sync();
+  named_bar(kConvBar, 128);  // the staging buffer is read: the next tile may land in it
+  reinterpret_cast<unsigned*>(sm + kRowMaxU)[tid - 128] = 0u;  // row maxima for the next tile
+  if (a.tma && tid == 128 && k + 1 < ntiles) issue_u_tma<kRev>(a, map, sm, u0, segs, k + 1);
+  mbar_arrive(&bars[kBarUFull + par]);
+  return true;
+}
+
+template <bool kRev>
+__device__ __forceinline__ void conv_role(const TcScanArgs& a, const CUtensorMap* map,
+                                          uint8_t* sm, uint32_t tmem, int u0, int segs,
+                                          int ntiles, volatile int* abort) {
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  if (ntiles == 0) return;
+  if (a.tma && threadIdx.x == 128) issue_u_tma<kRev>(a, map, sm, u0, segs, 0);
+  int cur_h = -1;
+  float sig_k = 1.f;
+  if (!conv_u_step<kRev>(a, map, sm, tmem, u0, segs, ntiles, 0, cur_h, sig_k, abort)) return;
+  for (int k = 0; k < ntiles; ++k) {
+    if (k + 1 < ntiles &&
+        !conv_u_step<kRev>(a, map, sm, tmem, u0, segs, ntiles, k + 1, cur_h, sig_k, abort))
+      return;
+    // Xin of tile k: its carries done and the Xin buffer free (GEMM2 of tile k-1 complete)
+    bool ok = warp_wait_phase(&bars[kBarXpReady + (k & 1)], (k >> 1) & 1, abort);
+    if (ok && k >= 1) ok = warp_wait_phase(&bars[kBarG2], (k - 1) & 1, abort);
+    if (!named_bar_and(kConvBar, 128, ok)) return;
+    convert_xin(sm, tmem, k);
+  }
+}
+
+// epi warps: y of tile k (thread = chunk column g = TMEM lane). Y1 (Toeplitz part, ready with
+// GEMM1) is read first into registers, releasing its TMEM buffer early; then Y2 (state part),
+// and y = Y1 / (u scale * K scale) + Y2 / (Xin scale * G scale) is stored (added at the
+// mirrored steps when kRev).
+template <bool kRev>
+__device__ __forceinline__ bool store_tile(const TcScanArgs& a, uint8_t* sm, uint32_t tmem,
+                                           int u0, int segs, int k, volatile int* abort) {
+  const int g = threadIdx.x - 256, warp = threadIdx.x >> 5;
+  const int par = k & 1;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  const uint32_t lane_base = tmem + (uint32_t((warp & 3) * 32) << 16);
+  // Y1 of tile k with the u scales (conv) and Xin scales (scan) of tile k: once read, the Y1
+  // buffer and both scale slots may take tile k + 2
+  bool ok = warp_wait_phase(&bars[kBarG1 + par], (k >> 1) & 1, abort) &&
+            warp_wait_phase(&bars[kBarXpReady + par], (k >> 1) & 1, abort) &&
+            warp_wait_phase(&bars[kBarUFull + par], (k >> 1) & 1, abort);
+  if (!named_bar_and(kEpiBar, 128, ok)) return false;
+  tc::fence_after_sync();
+  const float ay = reinterpret_cast<const float*>(sm + kAy)[par * 128 + g];
+  const float by = reinterpret_cast<const float*>(sm + kBy)[par * 128 + g];
+  float y[64];
+  tc::tmem_ld32(lane_base + kTY1 + par * 64, *reinterpret_cast<float(*)[32]>(y));
+  tc::tmem_ld32(lane_base + kTY1 + par * 64 + 32, *reinterpret_cast<float(*)[32]>(y + 32));
+  tc::fence_before_sync();
+  mbar_arrive(&bars[kBarY1Free + par]);
+  // Y2 of tile k
+  ok = warp_wait_phase(&bars[kBarG2], k & 1, abort);
+  if (!named_bar_and(kEpiBar, 128, ok)) return false;
+  tc::fence_after_sync();
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    float y2[16];
+    tc::tmem_ld16(lane_base + kTY2 + q4 * 16, y2);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) y[q4 * 16 + j] = fmaf(y[q4 * 16 + j], ay, y2[j] * by);
+  }
+  tc::fence_before_sync();
+  mbar_arrive(&bars[kBarY2Free]);
+  const TileInfo ti = tile_info(a, u0, segs, k);
+  const ColInfo ci = col_info(a, ti, g);
+  if (ci.valid) {
+    float* yrow = a.y + ci.rowoff;
+    store_part<kRev>(yrow, a.L, ci.k0, *reinterpret_cast<float(*)[32]>(y));
+    store_part<kRev>(yrow, a.L, ci.k0 + 32, *reinterpret_cast<float(*)[32]>(y + 32));
+  }
+  return true;
+}
+
+// GEMM1 of tile k with the Toeplitz part of GEMM2 (both need only the u operand):
+// S = Q u^T into S buffer k & 1 (A = Q from TMEM), Y1 = u Tk^T into Y1 buffer k & 1.
+__device__ __forceinline__ void gemm1(uint8_t* sm, uint32_t tmem, int k) {
+  const int par = k & 1;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  tc::fence_after_sync();
+  constexpr uint32_t id1 = tc::idesc_f16_f32(128, 128);
+  constexpr uint32_t idk = tc::idesc_f16_f32(128, 64);
+  const uint8_t* ubuf = sm + kU + par * kUBuf;
+  const uint64_t uh = tc::smem_desc_k_sw128(ubuf), ul = tc::smem_desc_k_sw128(ubuf + kULo);
+  const uint64_t th = tc::smem_desc_k_sw128(sm + kTkHi), tl = tc::smem_desc_k_sw128(sm + kTkLo);
+  const uint32_t dS = tmem + kTS + uint32_t(par) * 128;
+  const uint32_t dY1 = tmem + kTY1 + uint32_t(par) * 64;
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    const uint32_t qh = tmem + kTQ + kk * 8, ql = tmem + kTQ + 32 + kk * 8;
+    asm volatile(
+        "{\n"
+        "  .reg .pred p;\n"
+        "  setp.ne.b32 p, %4, 0;\n"
+        "  tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+        "  tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %3, 1;\n"
+        "  tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %2, %3, 1;\n"
+        "}\n" ::"r"(dS),
+        "r"(qh), "l"(uh + 2 * kk), "r"(id1), "r"(kk), "l"(ul + 2 * kk), "r"(ql)
+        : "memory");
+  }
+#pragma unroll
+  for (int kk = 0; kk < 4; ++kk) {
+    tc::mma_kind_f16(dY1, uh + 2 * kk, th + 2 * kk, idk, kk != 0);
+    tc::mma_kind_f16(dY1, uh + 2 * kk, tl + 2 * kk, idk, 1);
+    tc::mma_kind_f16(dY1, ul + 2 * kk, th + 2 * kk, idk, 1);
+  }
+  tc::mma_commit(&bars[kBarG1 + par]);
+}
+
+// GEMM2 (state part) of tile k: Y2 = Xin G^T.
+__device__ __forceinline__ void gemm2(uint8_t* sm, uint32_t tmem, int k) {
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  tc::fence_after_sync();
+  constexpr uint32_t idm = tc::idesc_f16_f32(128, 64) | (1u << 15);  // A (Xin) MN-major
+  const uint64_t gh = tc::smem_desc_k_sw128(sm + kGHi), gl = tc::smem_desc_k_sw128(sm + kGLo);
+  const uint64_t xh = tc::smem_desc_mn_sw128(sm + kXHi, 1024, 2048);
+  const uint64_t xl = tc::smem_desc_mn_sw128(sm + kXLo, 1024, 2048);
+#pragma unroll
+  for (int s = 0; s < 8; ++s) {
+    const uint64_t ao = uint64_t(s) * (4096 >> 4);                     // 16 rows = 2 K-groups
+    const uint64_t bo = uint64_t(s >> 2) * (8192 >> 4) + 2 * (s & 3);  // K-block, 32 bytes
+    tc::mma_kind_f16(tmem + kTY2, xh + ao, gh + bo, idm, s != 0);
+    tc::mma_kind_f16(tmem + kTY2, xh + ao, gl + bo, idm, 1);
+    tc::mma_kind_f16(tmem + kTY2, xl + ao, gh + bo, idm, 1);
+  }
+  tc::mma_commit(&bars[kBarG2]);
+}
+
+// MMA thread over all tiles of the CTA, in the order GEMM1 of tile k+1, GEMM2 of tile k. At a
+// change of channel the Toeplitz operand is copied in once GEMM1 of the previous tile has
+// completed, and the G operand once GEMM2 of the previous tile has completed, so only the work
+// that needs them waits. Returns false on abort.
+__device__ __forceinline__ bool mma_g1(const TcScanArgs& a, uint8_t* sm, uint32_t tmem, int u0,
+                                       int segs, int k, int& tk_h, uint32_t& tk_n,
+                                       volatile int* abort) {
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  const int par = k & 1;
+  const int h = tile_info(a, u0, segs, k).h;
+  if (h != tk_h) {
+    if (k >= 1 && !wait_phase(&bars[kBarG1 + (par ^ 1)], ((k - 1) >> 1) & 1, abort)) return false;
+    tc::mbar_arrive_expect_tx(&bars[kBarTabTk], kGHi - kTkHi);
+    tc::bulk_load(sm + kTkHi, a.tables + (size_t)h * kBlobBytes, kGHi - kTkHi, &bars[kBarTabTk]);
+    if (!wait_phase(&bars[kBarTabTk], tk_n & 1, abort)) return false;
+    ++tk_n;
+    tk_h = h;
+  }
+  if (!wait_phase(&bars[kBarUFull + par], (k >> 1) & 1, abort)) return false;
+  if (k >= 2 && !(wait_phase(&bars[kBarSFree + par], ((k - 2) >> 1) & 1, abort) &&
+                  wait_phase(&bars[kBarY1Free + par], ((k - 2) >> 1) & 1, abort)))
+    return false;
+  gemm1(sm, tmem, k);
+  return true;
+}
+
+__device__ __forceinline__ bool mma_g2(const TcScanArgs& a, uint8_t* sm, uint32_t tmem, int u0,
+                                       int segs, int k, int& g_h, uint32_t& g_n,
+                                       volatile int* abort) {
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  const int h = tile_info(a, u0, segs, k).h;
+  if (h != g_h) {
+    if (k >= 1 && !wait_phase(&bars[kBarG2], (k - 1) & 1, abort)) return false;
+    tc::mbar_arrive_expect_tx(&bars[kBarTabG], kGLo + 16384 - kGHi);
+    tc::bulk_load(sm + kGHi, a.tables + (size_t)h * kBlobBytes + (kGHi - kTkHi),
+                  kGLo + 16384 - kGHi, &bars[kBarTabG]);
+    if (!wait_phase(&bars[kBarTabG], g_n & 1, abort)) return false;
+    ++g_n;
+    g_h = h;
+  }
+  if (!wait_phase(&bars[kBarXFull], k & 1, abort)) return false;
+  if (k >= 1 && !wait_phase(&bars[kBarY2Free], (k - 1) & 1, abort)) return false;
+  gemm2(sm, tmem, k);
+  return true;
+}
+
+__device__ __forceinline__ void mma_role(const TcScanArgs& a, uint8_t* sm, uint32_t tmem,
+                                         int u0, int segs, int ntiles, volatile int* abort) {
+  int tk_h = -1, g_h = -1;
+  uint32_t tk_n = 0, g_n = 0;
+  if (ntiles == 0 || !mma_g1(a, sm, tmem, u0, segs, 0, tk_h, tk_n, abort)) return;
+  for (int k = 0; k < ntiles; ++k) {
+    if (k + 1 < ntiles && !mma_g1(a, sm, tmem, u0, segs, k + 1, tk_h, tk_n, abort)) return;
+    if (!mma_g2(a, sm, tmem, u0, segs, k, g_h, g_n, abort)) return;
+  }
+}
+
+// scan warps, one tile: carries along the chunks of S (in place: S becomes Xin), then the
+// Xin scale of every chunk column (the scale of its batch row).
 __device__ __forceinline__ bool scan_tile(const TcScanArgs& a, uint8_t* sm, uint32_t tmem,
                                           int k, bool new_row, float mu_re, float mu_im,
                                           float dl_re, float dl_im, float sig_g, float& xo,
-                                          float& xt, float& ao, float& at,
+                                          float& xt, float& ao, float& at, int& es_prev,
                                           volatile int* abort) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int par = k & 1;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-  const float* sInvU = reinterpret_cast<const float*>(sm + kInvU) + par * 128;
+  const int* sRowEs = reinterpret_cast<const int*>(sm + kRowEs) + par * 128;
   float* sColSx = reinterpret_cast<float*>(sm + kColSx) + par * 128;
   float* sBy = reinterpret_cast<float*>(sm + kBy) + par * 128;
   float* sRowMax = reinterpret_cast<float*>(sm + kRowMax);
   const uint32_t tS = tmem + (uint32_t(warp * 32) << 16) + kTS + uint32_t(par) * 128;
 
-  // S of this tile, and (for the per-chunk u scales) the io threads' release of tile k
-  bool ok = warp_wait_phase(&bars[kBarSFull + par], (k >> 1) & 1, abort) &&
+  // S of this tile, and (for the row scales) the conv threads' release of tile k
+  bool ok = warp_wait_phase(&bars[kBarG1 + par], (k >> 1) & 1, abort) &&
             warp_wait_phase(&bars[kBarUFull + par], (k >> 1) & 1, abort);
   if (!named_bar_and(kScanBar, 128, ok)) return false;
   tc::fence_after_sync();
 
-  if (new_row) xo = xt = ao = at = 0.f;
+  if (new_row) {
+    xo = xt = ao = at = 0.f;
+  } else {
+    // the carried state and anchor, from the previous tile's units of S to this tile's
+    // (S scales with the row's u scale 2^es): times 2^(es - es_prev), in two exact steps
+    const int d = max(-252, min(252, sRowEs[0] - es_prev));
+    const float f = exp2i(d / 2) * exp2i(d - d / 2);
+    xo *= f; xt *= f; ao *= f; at *= f;
+  }
+  es_prev = sRowEs[0];
   const int C = a.C;
   if (a.R > 0 && (C == 32 || C == 64)) {
     // two independent chains: columns [0, 64) and [64, 128) (whole rows of 32 or 64 chunks);
@@ -533,21 +894,22 @@ __device__ __forceinline__ bool scan_tile(const TcScanArgs& a, uint8_t* sm, uint
         aoB = xoB;
         atB = xtB;
       }
-      float sA[32], sB[32];
-      tc::tmem_ld32(tS + cA, sA);
-      tc::tmem_ld32(tS + cB, sB);
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+      float sA[16], sB[16];
+      tc::tmem_ld16(tS + cA + 16 * hf, sA);
+      tc::tmem_ld16(tS + cB + 16 * hf, sB);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float ivA = sInvU[cA + j], ivB = sInvU[cB + j];
+      for (int j = 0; j < 16; ++j) {
         const float pA = __shfl_xor_sync(0xffffffffu, sA[j], 1);
         const float pB = __shfl_xor_sync(0xffffffffu, sB[j], 1);
         const float oA = xo, oB = xoB;
         lA = fmaxf(lA, fabsf(oA));
         lB = fmaxf(lB, fabsf(oB));
-        const float noA = fmaf(mu_re, xo, fmaf(-mu_im, xt, sA[j] * ivA));
-        const float ntA = fmaf(mu_re, xt, fmaf(mu_im, xo, pA * ivA));
-        const float noB = fmaf(mu_re, xoB, fmaf(-mu_im, xtB, sB[j] * ivB));
-        const float ntB = fmaf(mu_re, xtB, fmaf(mu_im, xoB, pB * ivB));
+        const float noA = fmaf(mu_re, xo, fmaf(-mu_im, xt, sA[j]));
+        const float ntA = fmaf(mu_re, xt, fmaf(mu_im, xo, pA));
+        const float noB = fmaf(mu_re, xoB, fmaf(-mu_im, xtB, sB[j]));
+        const float ntB = fmaf(mu_re, xtB, fmaf(mu_im, xoB, pB));
         sA[j] = oA;
         sB[j] = oB;
         xo = noA;
@@ -555,8 +917,9 @@ __device__ __forceinline__ bool scan_tile(const TcScanArgs& a, uint8_t* sm, uint
         xoB = noB;
         xtB = ntB;
       }
-      tc::tmem_st32(tS + cA, sA);
-      tc::tmem_st32(tS + cB, sB);
+      tc::tmem_st16(tS + cA + 16 * hf, sA);
+      tc::tmem_st16(tS + cB + 16 * hf, sB);
+      }
       if ((cA + 32) % C == 0) {  // rows end with this block
         const unsigned mA = __reduce_max_sync(0xffffffffu, __float_as_uint(lA));
         const unsigned mB = __reduce_max_sync(0xffffffffu, __float_as_uint(lB));
@@ -583,21 +946,23 @@ __device__ __forceinline__ bool scan_tile(const TcScanArgs& a, uint8_t* sm, uint
         ao = xo;
         at = xt;
       }
-      float sv[32];
-      tc::tmem_ld32(tS + c0, sv);
+#pragma unroll 1
+      for (int hf = 0; hf < 2; ++hf) {
+      float sv[16];
+      tc::tmem_ld16(tS + c0 + 16 * hf, sv);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float iv = sInvU[c0 + j];
+      for (int j = 0; j < 16; ++j) {
         const float p = __shfl_xor_sync(0xffffffffu, sv[j], 1);
         const float o = xo;
         l = fmaxf(l, fabsf(o));
-        const float no = fmaf(mu_re, xo, fmaf(-mu_im, xt, sv[j] * iv));
-        const float nt = fmaf(mu_re, xt, fmaf(mu_im, xo, p * iv));
+        const float no = fmaf(mu_re, xo, fmaf(-mu_im, xt, sv[j]));
+        const float nt = fmaf(mu_re, xt, fmaf(mu_im, xo, p));
         sv[j] = o;
         xo = no;
         xt = nt;
       }
-      tc::tmem_st32(tS + c0, sv);
+      tc::tmem_st16(tS + c0 + 16 * hf, sv);
+      }
     }
     tc::tmem_wait_st();
     const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(l));
@@ -615,7 +980,6 @@ __device__ __forceinline__ bool scan_tile(const TcScanArgs& a, uint8_t* sm, uint
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int g = blk * 32 + j;
-        const float iv = sInvU[g];
         const float sother = __shfl_xor_sync(0xffffffffu, sv[j], 1);
         if (g == next_anchor) {
           xo = fmaf(dl_re, ao, fmaf(-dl_im, at, xo));
@@ -637,8 +1001,8 @@ __device__ __forceinline__ bool scan_tile(const TcScanArgs& a, uint8_t* sm, uint
         }
         o[j] = xo;
         lmax = fmaxf(lmax, fabsf(xo));
-        const float no = fmaf(mu_re, xo, fmaf(-mu_im, xt, sv[j] * iv));
-        const float nt = fmaf(mu_re, xt, fmaf(mu_im, xo, sother * iv));
+        const float no = fmaf(mu_re, xo, fmaf(-mu_im, xt, sv[j]));
+        const float nt = fmaf(mu_re, xt, fmaf(mu_im, xo, sother));
         xo = no;
         xt = nt;
       }
@@ -649,233 +1013,24 @@ __device__ __forceinline__ bool scan_tile(const TcScanArgs& a, uint8_t* sm, uint
     if (lane == 0) sRowMax[row_i * 4 + warp] = __uint_as_float(m);
   }
   named_bar(kScanBar, 128);
-  // Xin scale of chunk column tid (the scale of its batch row)
   {
     const int row = (a.R > 0) ? tid / a.C : 0;
     const float xmax = fmaxf(fmaxf(sRowMax[row * 4], sRowMax[row * 4 + 1]),
                              fmaxf(sRowMax[row * 4 + 2], sRowMax[row * 4 + 3]));
     const int ex = scale_exp(xmax);
     sColSx[tid] = exp2i(ex);
-    sBy[tid] = exp2i(-ex) / sig_g;
-  }
-  mbar_arrive(&bars[kBarScale + par]);  // releases sBy (and the channel scales) to the io warps
-  // the Xin buffer is free once GEMM2 of the previous tile has completed
-  ok = (k == 0) || warp_wait_phase(&bars[kBarG2], (k - 1) & 1, abort);
-  if (!named_bar_and(kScanBar, 128, ok)) return false;
-  // Xin -> scaled f16 pair, MN-major: this thread writes state row r = tid, 8 chunks per
-  // 16-byte store
-  {
-    const int r = tid;
-    const uint32_t kbase = uint32_t(r >> 3) * 2048u + uint32_t(r & 7) * 128u;
-    const uint32_t kr = uint32_t(r & 7);
-#pragma unroll 1
-    for (int blk = 0; blk < 4; ++blk) {
-      float v[32];
-      tc::tmem_ld32(tS + blk * 32, v);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int g0 = blk * 32 + q * 8;
-        const float4 c0 = *reinterpret_cast<const float4*>(sColSx + g0);
-        const float4 c1 = *reinterpret_cast<const float4*>(sColSx + g0 + 4);
-        const float sc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        uint32_t h[4], l[4];
-#pragma unroll
-        for (int p = 0; p < 4; ++p)
-          split2(v[q * 8 + 2 * p] * sc[2 * p], v[q * 8 + 2 * p + 1] * sc[2 * p + 1], h[p], l[p]);
-        const uint32_t cg = uint32_t(g0 >> 3);  // 16-byte chunk index along the chunks
-        const uint32_t off = kbase + (cg >> 3) * 1024u + (((cg & 7u) ^ kr) << 4);
-        *reinterpret_cast<uint4*>(sm + kXHi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(sm + kXLo + off) = make_uint4(l[0], l[1], l[2], l[3]);
-      }
-    }
-  }
-  tc::fence_proxy_async_smem();
-  tc::fence_before_sync();
-  mbar_arrive(&bars[kBarXFull]);
-  mbar_arrive(&bars[kBarSFree + par]);
-  return true;
-}
-
-// IO warps: u chunks of tile k -> scaled f16 pair (thread = chunk column g).
-template <bool kRev>
-__device__ __forceinline__ bool load_tile(const TcScanArgs& a, uint8_t* sm, int u0, int segs,
-                                          int k, volatile int* abort) {
-  const int g = threadIdx.x - 128;
-  const int par = k & 1;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-  // the u buffer is free once GEMM2 of tile k-2 has completed
-  const bool ok =
-      (k < 2) || warp_wait_phase(&bars[kBarUFree + par], ((k - 2) >> 1) & 1, abort);
-  if (!named_bar_and(kIoBar, 128, ok)) return false;
-  const TileInfo ti = tile_info(a, u0, segs, k);
-  const ColInfo ci = col_info(a, ti, g);
-  float v[64];
-  load_chunk<kRev>(a.u + ci.rowoff, a.L, ci.k0, ci.valid, v);
-  float m = 0.f;
-#pragma unroll
-  for (int t = 0; t < kT; ++t) m = fmaxf(m, fabsf(v[t]));
-  const int es = scale_exp(m);
-  const float su = exp2i(es);
-#pragma unroll
-  for (int t = 0; t < kT; ++t) v[t] *= su;
-  uint8_t* ubuf = sm + kU + par * kUBuf;
-  store_row64(ubuf, ubuf + kULo, g, v);
-  const float inv_su = exp2i(-es);
-  reinterpret_cast<float*>(sm + kInvU)[par * 128 + g] = inv_su * (1.f / 16384.f);
-  reinterpret_cast<float*>(sm + kInvSu)[par * 128 + g] = inv_su;
-  tc::fence_proxy_async_smem();
-  mbar_arrive(&bars[kBarUFull + par]);
-  return true;
-}
-
-// IO warps: outputs of tile k (thread = chunk column g = TMEM lane).
-template <bool kRev>
-__device__ __forceinline__ bool store_tile(const TcScanArgs& a, uint8_t* sm, uint32_t tmem,
-                                           int u0, int segs, int k, volatile int* abort) {
-  const int g = threadIdx.x - 128, warp = threadIdx.x >> 5;
-  const int par = k & 1;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-  const bool ok = warp_wait_phase(&bars[kBarG2], k & 1, abort) &&
-                  warp_wait_phase(&bars[kBarScale + par], (k >> 1) & 1, abort);
-  if (!named_bar_and(kIoBar, 128, ok)) return false;
-  tc::fence_after_sync();
-  const float sig_k = reinterpret_cast<const float*>(sm + kSig)[0];
-  const float ay = reinterpret_cast<const float*>(sm + kInvSu)[par * 128 + g] / sig_k;
-  const float by = reinterpret_cast<const float*>(sm + kBy)[par * 128 + g];
-  const uint32_t lane_base = tmem + (uint32_t((warp & 3) * 32) << 16);
-  float y[64];
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    float y1[32], y2[32];
-    tc::tmem_ld32(lane_base + kTY1 + half * 32, y1);
-    tc::tmem_ld32(lane_base + kTY2 + half * 32, y2);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) y[half * 32 + j] = fmaf(y1[j], ay, y2[j] * by);
+    // true Xin = (S units) * 2^(-14 - es_row): Y2 / (2^ex sig_g) * 2^(-14 - es_row)
+    const int er = max(-126, -14 - sRowEs[row]);
+    sBy[tid] = exp2i(-ex) * exp2i(er) / sig_g;
   }
   tc::fence_before_sync();
-  mbar_arrive(&bars[kBarYFree]);
-  const TileInfo ti = tile_info(a, u0, segs, k);
-  const ColInfo ci = col_info(a, ti, g);
-  if (ci.valid) {
-    float* yrow = a.y + ci.rowoff;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float o[32];
-#pragma unroll
-      for (int j = 0; j < 32; ++j) o[j] = y[half * 32 + j];
-      store_part<kRev>(yrow, a.L, ci.k0 + half * 32, o);
-    }
-  }
+  mbar_arrive(&bars[kBarXpReady + par]);
   return true;
 }
 
-// MMA thread: are the inputs of GEMM1 of tile k in place? (u operand written, S buffer k & 1
-// released by the scan of tile k-2, the channel's tables loaded for the first tile of a channel)
-__device__ __forceinline__ bool gemm1_ready(uint64_t* bars, int k, bool first_of_group,
-                                            uint32_t group) {
-  const int par = k & 1;
-  if (first_of_group && !(tc::mbar_try_wait(&bars[kBarTab], group & 1) &&
-                          tc::mbar_try_wait(&bars[kBarTabLoad], group & 1)))
-    return false;
-  if (!tc::mbar_try_wait(&bars[kBarUFull + par], (k >> 1) & 1)) return false;
-  return k < 2 || tc::mbar_try_wait(&bars[kBarSFree + par], ((k - 2) >> 1) & 1);
-}
-
-// GEMM1 of tile k: S = Q u^T into S buffer k & 1 (A = Q from TMEM, B = u operand).
-__device__ __forceinline__ void gemm1(uint8_t* sm, uint32_t tmem, int k) {
-  const int par = k & 1;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-  tc::fence_after_sync();
-  constexpr uint32_t id1 = tc::idesc_f16_f32(128, 128);
-  const uint8_t* ubuf = sm + kU + par * kUBuf;
-  const uint64_t uh = tc::smem_desc_k_sw128(ubuf), ul = tc::smem_desc_k_sw128(ubuf + kULo);
-  const uint32_t dS = tmem + kTS + uint32_t(par) * 128;
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    const uint32_t qh = tmem + kTQHi + kk * 8, ql = tmem + kTQLo + kk * 8;
-    asm volatile(
-        "{\n"
-        "  .reg .pred p;\n"
-        "  setp.ne.b32 p, %4, 0;\n"
-        "  tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
-        "  tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %3, 1;\n"
-        "  tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %2, %3, 1;\n"
-        "}\n" ::"r"(dS),
-        "r"(qh), "l"(uh + 2 * kk), "r"(id1), "r"(kk), "l"(ul + 2 * kk), "r"(ql)
-        : "memory");
-  }
-  tc::mma_commit(&bars[kBarSFull + par]);
-}
-
-// MMA thread: are the inputs of GEMM2 of tile k in place? (Xin written, Y read out for k-1)
-__device__ __forceinline__ bool gemm2_ready(uint64_t* bars, int k) {
-  if (!tc::mbar_try_wait(&bars[kBarXFull], k & 1)) return false;
-  return k < 1 || tc::mbar_try_wait(&bars[kBarYFree], (k - 1) & 1);
-}
-
-// GEMM2 of tile k: Y1 = u Tk^T, Y2 = Xin G^T; its completion also frees u buffer k & 1.
-__device__ __forceinline__ void gemm2(uint8_t* sm, uint32_t tmem, int k) {
-  const int par = k & 1;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-  tc::fence_after_sync();
-  constexpr uint32_t idk = tc::idesc_f16_f32(128, 64);
-  constexpr uint32_t idm = idk | (1u << 15);  // A (Xin) MN-major
-  const uint8_t* ubuf = sm + kU + par * kUBuf;
-  const uint64_t uh = tc::smem_desc_k_sw128(ubuf), ul = tc::smem_desc_k_sw128(ubuf + kULo);
-  const uint64_t th = tc::smem_desc_k_sw128(sm + kTkHi), tl = tc::smem_desc_k_sw128(sm + kTkLo);
-  const uint64_t gh = tc::smem_desc_k_sw128(sm + kGHi), gl = tc::smem_desc_k_sw128(sm + kGLo);
-  const uint64_t xh = tc::smem_desc_mn_sw128(sm + kXHi, 1024, 2048);
-  const uint64_t xl = tc::smem_desc_mn_sw128(sm + kXLo, 1024, 2048);
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) {
-    tc::mma_kind_f16(tmem + kTY1, uh + 2 * kk, th + 2 * kk, idk, kk != 0);
-    tc::mma_kind_f16(tmem + kTY1, uh + 2 * kk, tl + 2 * kk, idk, 1);
-    tc::mma_kind_f16(tmem + kTY1, ul + 2 * kk, th + 2 * kk, idk, 1);
-  }
-#pragma unroll
-  for (int s = 0; s < 8; ++s) {
-    const uint64_t ao = uint64_t(s) * (4096 >> 4);                     // 16 rows = 2 K-groups
-    const uint64_t bo = uint64_t(s >> 2) * (8192 >> 4) + 2 * (s & 3);  // K-block, 32 bytes
-    tc::mma_kind_f16(tmem + kTY2, xh + ao, gh + bo, idm, s != 0);
-    tc::mma_kind_f16(tmem + kTY2, xh + ao, gl + bo, idm, 1);
-    tc::mma_kind_f16(tmem + kTY2, xl + ao, gh + bo, idm, 1);
-  }
-  tc::mma_commit(&bars[kBarG2]);
-  tc::mma_commit(&bars[kBarUFree + par]);
-}
-
-// MMA thread, tiles [k0, k1) of one channel: issues GEMM2 of the oldest tile whose Xin is
-// ready, else GEMM1 of the next tile whose u is ready. Gives up (abort flag) after the wait
-// limit without progress.
-__device__ __forceinline__ void mma_role(uint8_t* sm, uint32_t tmem, int k0, int k1,
-                                         uint32_t group, volatile int* abort) {
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-  int n1 = k0, n2 = k0;
-  uint64_t t_last = tc::global_timer_ns();
-  while (n2 < k1) {
-    bool did = false;
-    if (n2 < n1 && gemm2_ready(bars, n2)) {
-      gemm2(sm, tmem, n2++);
-      did = true;
-    } else if (n1 < k1 && gemm1_ready(bars, n1, n1 == k0, group)) {
-      gemm1(sm, tmem, n1++);
-      did = true;
-    }
-    if (did) {
-      t_last = tc::global_timer_ns();
-    } else {
-      if (*abort) return;
-      if (tc::global_timer_ns() - t_last > tc::kWaitLimitNs) {
-        *abort = 1;
-        return;
-      }
-      __nanosleep(32);
-    }
-  }
-}
-
 template <bool kRev>
-__global__ void __launch_bounds__(kThreads, 1) dlr_scan_tc_kernel(const TcScanArgs a) {
+__global__ void __maxnreg__(128)
+    dlr_scan_tc_kernel(const TcScanArgs a, const __grid_constant__ CUtensorMap umap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -885,21 +1040,19 @@ __global__ void __launch_bounds__(kThreads, 1) dlr_scan_tc_kernel(const TcScanAr
 
   const int tid = threadIdx.x, warp = tid >> 5;
   if (tid == 0) {
-    tc::mbar_init(&bars[kBarUFull], 128);
-    tc::mbar_init(&bars[kBarUFull + 1], 128);
-    tc::mbar_init(&bars[kBarSFull], 1);
-    tc::mbar_init(&bars[kBarSFull + 1], 1);
-    tc::mbar_init(&bars[kBarSFree], 128);
-    tc::mbar_init(&bars[kBarSFree + 1], 128);
-    tc::mbar_init(&bars[kBarXFull], 128);
+    tc::mbar_init(&bars[kBarStage], 1);
+    tc::mbar_init(&bars[kBarTabTk], 1);
+    tc::mbar_init(&bars[kBarTabG], 1);
     tc::mbar_init(&bars[kBarG2], 1);
-    tc::mbar_init(&bars[kBarYFree], 128);
-    tc::mbar_init(&bars[kBarTab], 128);
-    tc::mbar_init(&bars[kBarScale], 128);
-    tc::mbar_init(&bars[kBarScale + 1], 128);
-    tc::mbar_init(&bars[kBarUFree], 1);
-    tc::mbar_init(&bars[kBarUFree + 1], 1);
-    tc::mbar_init(&bars[kBarTabLoad], 1);
+    tc::mbar_init(&bars[kBarXFull], 128);
+    tc::mbar_init(&bars[kBarY2Free], 128);
+    for (int p = 0; p < 2; ++p) {
+      tc::mbar_init(&bars[kBarUFull + p], 128);
+      tc::mbar_init(&bars[kBarG1 + p], 1);
+      tc::mbar_init(&bars[kBarSFree + p], 128);
+      tc::mbar_init(&bars[kBarXpReady + p], 128);
+      tc::mbar_init(&bars[kBarY1Free + p], 128);
+    }
     *abort = 0;
     tc::mbar_fence_init();
   }
@@ -907,6 +1060,7 @@ __global__ void __launch_bounds__(kThreads, 1) dlr_scan_tc_kernel(const TcScanAr
     tc::tmem_alloc(slot, kTmemCols);
     tc::tmem_relinquish();
   }
+  if (tid < 128) reinterpret_cast<unsigned*>(sm + kRowMaxU)[tid] = 0u;
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -917,46 +1071,41 @@ __global__ void __launch_bounds__(kThreads, 1) dlr_scan_tc_kernel(const TcScanAr
   const int segs = (a.R > 0) ? 1 : (a.C + kCols - 1) / kCols;
   const int ntiles = (u1 - u0) * segs;
 
-  // scan-thread state
-  float mu_re = 0.f, mu_im = 0.f, dl_re = 0.f, dl_im = 0.f, sig_g = 1.f;
-  float xo = 0.f, xt = 0.f, ao = 0.f, at = 0.f;
-  uint32_t group = 0;
-
-  for (int k0 = 0; k0 < ntiles; ++group) {
-    // the tiles [k0, k1) share one channel
-    const int h = tile_info(a, u0, segs, k0).h;
-    const int u_end = min(u1, (a.R > 0) ? (h + 1) * a.tiles_per_h : (h + 1) * a.B);
-    const int k1 = (u_end - u0) * segs;
-
-    if (warp < 4) {
-      load_tables(a.tables + (size_t)h * kBlobBytes, sm, tmem, mu_re, mu_im, dl_re, dl_im,
-                  sig_g);
-      mbar_arrive(&bars[kBarTab]);
-      for (int k = k0; k < k1; ++k) {
-        const TileInfo ti = tile_info(a, u0, segs, k);
-        if (!scan_tile(a, sm, tmem, k, ti.seg == 0, mu_re, mu_im, dl_re, dl_im, sig_g, xo, xt,
-                       ao, at, abort))
-          break;
+  if (warp < 4) {
+    float mu_re = 0.f, mu_im = 0.f, dl_re = 0.f, dl_im = 0.f, sig_g = 1.f;
+    float xo = 0.f, xt = 0.f, ao = 0.f, at = 0.f;
+    int es_prev = 0;
+    int cur_h = -1;
+    for (int k = 0; k < ntiles; ++k) {
+      const TileInfo ti = tile_info(a, u0, segs, k);
+      if (ti.h != cur_h) {
+        // this thread's lambda^64 and re-anchoring correction; the G scale of the channel.
+        // The state recurrence keeps (own, other) components; the Im row runs it with the
+        // sign of the imaginary parts flipped.
+        cur_h = ti.h;
+        const uint8_t* blob = a.tables + (size_t)ti.h * kBlobBytes;
+        const float4 m = __ldg(reinterpret_cast<const float4*>(blob + kBlobMu) + (tid >> 1));
+        mu_re = m.x;
+        dl_re = m.z;
+        mu_im = (tid & 1) ? -m.y : m.y;
+        dl_im = (tid & 1) ? -m.w : m.w;
+        sig_g = __ldg(reinterpret_cast<const float*>(blob + kBlobSig) + 1);
       }
-    } else if (warp < 8) {
-      bool ok = true;
-      for (int k = k0; k < k1 && ok; ++k) {
-        ok = load_tile<kRev>(a, sm, u0, segs, k, abort);
-        if (ok && k > k0) ok = store_tile<kRev>(a, sm, tmem, u0, segs, k - 1, abort);
-      }
-      if (ok) store_tile<kRev>(a, sm, tmem, u0, segs, k1 - 1, abort);
-    } else if ((tid & 31) == 0) {
-      mma_role(sm, tmem, k0, k1, group, abort);
+      if (!scan_tile(a, sm, tmem, k, ti.seg == 0, mu_re, mu_im, dl_re, dl_im, sig_g, xo, xt, ao,
+                     at, es_prev, abort))
+        break;
     }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    if (*abort) break;
-    k0 = k1;
+  } else if (warp < 8) {
+    conv_role<kRev>(a, &umap, sm, tmem, u0, segs, ntiles, abort);
+  } else if (warp < 12) {
+    for (int k = 0; k < ntiles; ++k)
+      if (!store_tile<kRev>(a, sm, tmem, u0, segs, k, abort)) break;
+  } else if ((tid & 31) == 0) {
+    mma_role(a, sm, tmem, u0, segs, ntiles, abort);
   }
-  if (*abort) report_status(a.status, DLR_ERR_TIMEOUT);
   tc::fence_before_sync();
   __syncthreads();
+  if (*abort) report_status(a.status, DLR_ERR_TIMEOUT);
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -974,8 +1123,25 @@ int sm_count() {
   return n;
 }
 
+// 3D view of u for the TMA loads: [64 steps][C chunks][B*H rows], boxes of 32 steps x bc chunks
+// x 1 row, 128-byte swizzle (one 128-byte line per chunk and half).
+bool make_u_map(CUtensorMap* m, const float* u, int B, int H, int L, int bc) {
+  auto fn = tc::tensor_map_encoder();
+  if (!fn) return false;
+  const int C = L / kT;
+  cuuint64_t dims[3] = {(cuuint64_t)kT, (cuuint64_t)C, (cuuint64_t)B * (cuuint64_t)H};
+  cuuint64_t strides[2] = {(cuuint64_t)kT * 4, (cuuint64_t)L * 4};
+  cuuint32_t box[3] = {32, (cuuint32_t)bc, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(u), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 template <bool kRev>
-cudaError_t launch_one(const TcScanArgs& a, uint8_t* ws, cudaStream_t s) {
+cudaError_t launch_one(const TcScanArgs& a, uint8_t* ws, const CUtensorMap& umap,
+                       cudaStream_t s) {
   cudaError_t e = max_smem_once<dlr_scan_tc_kernel<kRev>>(kSmemBytes);
   if (e != cudaSuccess) return e;
   const int sms = sm_count();
@@ -984,7 +1150,7 @@ cudaError_t launch_one(const TcScanArgs& a, uint8_t* ws, cudaStream_t s) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int grid = std::min(a.units, sms);
-  dlr_scan_tc_kernel<kRev><<<grid, kThreads, kSmemBytes, s>>>(a);
+  dlr_scan_tc_kernel<kRev><<<grid, kThreads, kSmemBytes, s>>>(a, umap);
   return cudaGetLastError();
 }
 
@@ -1017,15 +1183,22 @@ cudaError_t launch_dlr_scan_tc(const float* u, const float* lr, const float* li,
   }
   a.status = status;
   a.tables = static_cast<const uint8_t*>(ws);
+  // u tiles by TMA when every row is whole chunks and a tile's rows are whole boxes
+  const bool tma_shape = (L % kT == 0) && ((a.R > 0) ? (a.C == 32 || a.C == 64 || a.C == 128)
+                                                      : (a.C % 64 == 0));
+  a.bc = (a.C == 32) ? 32 : 64;
+  CUtensorMap umap;
+  std::memset(&umap, 0, sizeof(umap));
+  a.tma = tma_shape && make_u_map(&umap, u, B, H, L, a.bc) ? 1 : 0;
   a.log_re = lr;
   a.log_im = li;
   a.W = reinterpret_cast<const float2*>(W);
-  cudaError_t e = launch_one<false>(a, static_cast<uint8_t*>(ws), s);
+  cudaError_t e = launch_one<false>(a, static_cast<uint8_t*>(ws), umap, s);
   if (e != cudaSuccess || !bidir) return e;
   a.log_re = lr2;
   a.log_im = li2;
   a.W = reinterpret_cast<const float2*>(W2);
-  return launch_one<true>(a, static_cast<uint8_t*>(ws), s);
+  return launch_one<true>(a, static_cast<uint8_t*>(ws), umap, s);
 }
 
 }  // namespace dlr

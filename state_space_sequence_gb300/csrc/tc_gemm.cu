@@ -193,23 +193,9 @@ __global__ void to_bf16_t(const float* __restrict__ x, __nv_bfloat16* __restrict
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 // Row-major bf16 [rows, cols] with boxes of box_rows x 64 columns, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-  auto fn = encode_fn();
+  auto fn = tc::tensor_map_encoder();
   if (!fn) return false;
   if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (cols * 2) % 16) return false;
   cuuint64_t dims[2] = {cols, rows};

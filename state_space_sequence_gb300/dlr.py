@@ -26,6 +26,8 @@ _lib = None
 class DLRError(RuntimeError):
     def __init__(self, fn: str, status: int):
         name = _load().dlr_status_string(status).decode() if _lib is not None else str(status)
+        if status == DLR_ERR_CUDA and _lib is not None:
+            name += " (" + _lib.dlr_last_cuda_error().decode() + ")"
         super().__init__(f"{fn} failed: {name}")
         self.status = status
 
@@ -64,6 +66,7 @@ def _load():
         lib.dlr_status_string.argtypes = [i32]
         lib.dlr_status_string.restype = ctypes.c_char_p
         lib.dlr_abi_version.restype = i32
+        lib.dlr_last_cuda_error.restype = ctypes.c_char_p
         _lib = lib
     return _lib
 
