@@ -1,10 +1,12 @@
 #!/usr/bin/env python
-"""Benchmark of the DLR layer (kernel generation + FFT convolution) on GB300.
+"""Benchmark of the DLR layer on GB300.
 
-One step = one pass of the whole DLR hot path over one batch: dlr_kernel (lambda powers ->
-K), dlr_conv_spectrum (K -> per-channel spectra) and dlr_conv_apply (u -> y) on the
-B=8, H=256, N=64, L=4096 bank (float32, synthetic seeded inputs resident in HBM). L2 is
-flushed (a 2 x L2 write) before every step; the flush is outside the timed events.
+One step = one pass of the whole DLR hot path over one batch: the layer u -> y on the
+B=8, H=256, N=64, L=4096 bank (float32 inputs, synthetic seeded data resident in HBM) through
+dlr_scan -- the per-channel table kernel and the tensor-core chunked scan kernel, replayed as
+one CUDA graph. L2 is flushed (a 2 x L2 write) before every step; the flush is outside the
+timed events. The FFT path of the same layer (dlr_kernel + dlr_conv_spectrum + dlr_conv_apply)
+and the other workloads are reported as secondary lines.
 
 Prints ONE JSON line (rank 0). Multi-GPU (torchrun): every rank runs its own batch (weak
 scaling, no data-path collective); a barrier and a max-over-ranks reduction bracket the timing.
@@ -33,6 +35,9 @@ WORKLOAD = "dlr_b8_h256_n64_l4096"
 METRIC = "DLR layer elements/s (B*H*L/s) and achieved HBM GB/s vs peak, 1xGB300"
 UNIT = "elements/s"
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+SCAN_TC_SOURCES = ["state_space_sequence_gb300/csrc/dlr_scan_tc.cu",
+                   "state_space_sequence_gb300/csrc/tc_ptx.cuh",
+                   "state_space_sequence_gb300/csrc/dlr_common.cuh"]
 CONV_SOURCES = ["state_space_sequence_gb300/csrc/dlr_conv.cu",
                 "state_space_sequence_gb300/csrc/fft_smem.cuh",
                 "state_space_sequence_gb300/csrc/fft_rows.cuh",
@@ -80,6 +85,18 @@ def load_peaks():
             d = json.load(fh)
         return float(d["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def load_tensor_peak():
+    """Dense f16/bf16 tensor throughput (TFLOP/s), burst figure: the step is timed alone.
+    f16 and bf16 share one nominal rate, so the measured bf16 GEMM stands for both."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured (bf16 burst; f16 has the same rate)"
+    return 1900.0, "fallback"
 
 
 class ClockSampler:
@@ -154,8 +171,7 @@ def run_ours(args):
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     u = dev(w.u)
     fwd = (dev(w.fwd.log_re), dev(w.fwd.log_im), dev(w.fwd.W))
-    K = torch.empty((H, L), dtype=torch.float32, device="cuda")
-    ws = torch.empty(dlr.dlr_conv_workspace_size(H, L), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(dlr.dlr_scan_workspace_size(B, H, N, L), dtype=torch.uint8, device="cuda")
     y = torch.empty_like(u)
     props = torch.cuda.get_device_properties(local)
     l2 = int(getattr(props, "L2_cache_size", 128 << 20) or (128 << 20))
@@ -165,20 +181,16 @@ def run_ours(args):
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
     def step():
-        dlr.dlr_kernel(*fwd, L, "re", out=K)
-        dlr.dlr_conv_spectrum(K, workspace=ws)
-        dlr.dlr_conv_apply(u, ws, out=y)
+        dlr.dlr_scan(u, fwd, out=y, algo="tensor", workspace=ws)
 
     for _ in range(3):  # eager: loads the module, sets kernel attributes
         step()
     torch.cuda.synchronize()
-    # The step's four launches are recorded once in a CUDA graph and replayed, so the timing
-    # holds no host-side launch gaps; the dominant kernel is recorded alone for its roofline.
-    g_step, g_apply = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    # The step's launches are recorded once in a CUDA graph and replayed, so the timing holds no
+    # host-side launch gaps.
+    g_step = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step):
         step()
-    with torch.cuda.graph(g_apply):
-        dlr.dlr_conv_apply(u, ws, out=y)
     for _ in range(args.warmup):
         flush.zero_()
         g_step.replay()
@@ -202,21 +214,12 @@ def run_ours(args):
         g_step.replay()
         e.record(stream)
         starts.append(s), ends.append(e)
-    a0s, a1s = [], []
-    for _ in range(min(args.steps, 1000)):
-        flush.zero_()
-        a0, a1 = ev(), ev()
-        a0.record(stream)
-        g_apply.replay()
-        a1.record(stream)
-        a0s.append(a0), a1s.append(a1)
     torch.cuda.synchronize()
     t_wall1 = time.time()
     if dist is not None:
         dist.barrier()
     sampler.window = (t_wall0, t_wall1)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    apply_ms = [a.elapsed_time(b) for a, b in zip(a0s, a1s)]
     total_s = sum(step_ms) / 1e3
     if dist is not None:
         t = torch.tensor([total_s], dtype=torch.float64, device="cuda")
@@ -243,7 +246,7 @@ def run_ours(args):
         u_d.copy_(u_h, non_blocking=True)
         for dst, src in zip(p_d, p_h):
             dst.copy_(src, non_blocking=True)
-        dlr.dlr_layer(u_d, tuple(p_d), path="fft", workspace=ws, out=y)
+        dlr.dlr_layer(u_d, tuple(p_d), path="scan", workspace=ws, out=y)
         y_h.copy_(y, non_blocking=True)
         e.record(stream)
         if i >= 3:
@@ -259,34 +262,29 @@ def run_ours(args):
     sampler.stop()
     clocks = sampler.summary() if rank == 0 else None
 
-    # roofline of the dominant kernel (dlr_conv_apply: one launch of the FFT row kernel). It is
-    # bound by FP32 arithmetic, not by HBM: the algorithmic count of a real FFT of size M is
-    # 2.5 M log2 M flops, forward + inverse 5 M log2 M, plus 6 flops per spectral bin.
-    n = 1 << max(0, int(np.ceil(np.log2(L))))
-    M = 2 * n
-    apply_flops = B * H * (5 * M * np.log2(M) + 6 * (M // 2 + 1))
-    apply_bytes = 4 * B * H * L * 2 + 8 * H * (n + 1)  # u in + y out + spectra read once
-    apply_avg = sum(apply_ms) / len(apply_ms) / 1e3
+    # Roofline of the step (the tensor-core scan kernel dominates it; the table kernel is a few
+    # per cent). Algorithmic bytes: u read + y written once, plus the parameters. The tensor
+    # view: 320 multiply-adds per output element (2N chunk states + T Toeplitz + 2N carried-state
+    # outputs at N = 64, T = 64), each executed as three f16 MMAs (hi*hi + hi*lo + lo*hi).
+    step_avg = total_s / args.steps
+    layer_bytes = 4 * B * H * L * 2 + 4 * H * N * 4  # u + y + (log_re, log_im, W)
     peak_gbs, peak_kind = load_peaks()
-    sm_count = props.multi_processor_count
-    sm_mhz = load_sm_max_mhz()
-    peak_tflops = sm_count * 128 * 2 * sm_mhz * 1e6 / 1e12  # FP32 lanes x FMA x clock
-    achieved_tflops = apply_flops / apply_avg / 1e12
-    achieved = apply_bytes / apply_avg / 1e9
-    peak = peak_gbs
+    achieved = layer_bytes / step_avg / 1e9
+    macs = B * H * L * (2 * 2 * N + 64)
+    tc_flops = 3 * 2 * macs
+    tc_peak, tc_kind = load_tensor_peak()
     traffic = None
     if os.path.exists(PROFILE_TRAFFIC):
         with open(PROFILE_TRAFFIC) as fh:
             prof = json.load(fh)
-        entry = prof.get("conv_pairs")
-        if entry and entry.get("source_hash") == source_hash(CONV_SOURCES):
+        entry = prof.get("dlr_scan_tc_kernel")
+        if entry and entry.get("source_hash") == source_hash(SCAN_TC_SOURCES):
             traffic = entry.get("dram_bytes_per_launch")
-    layer_bytes = 4 * B * H * L * 2 + 4 * H * N * 4  # u + y + (log_re, log_im, W)
-    step_avg = total_s / args.steps
 
     extras = {}
     if rank == 0 and world == 1 and not args.no_extras:
-        extras = run_extras(torch, dlr, inputs, flush)
+        extras = run_extras(torch, dlr, inputs, flush, load_sm_max_mhz(),
+                            props.multi_processor_count)
 
     if rank != 0:
         if dist is not None:
@@ -298,26 +296,26 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; DLR init of the pages, u ~ N(0,1))",
-        "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "L": L, "path": "fft",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "L": L, "path": "scan",
                    "cast": "re", "causal": True, "parallelism": f"replicas x{world}",
                    "l2": "flushed before every step (2 x L2 write), flush outside the events",
-                   "step": "dlr_kernel + dlr_conv_spectrum + dlr_conv_apply, replayed as one "
-                           "CUDA graph"},
-        "layer_hbm": {"algorithmic_bytes": layer_bytes,
-                      "achieved_gbs": layer_bytes / step_avg / 1e9,
-                      "frac_of_measured_peak": layer_bytes / step_avg / 1e9 / peak},
-        "roofline": {"kernel": "conv_pairs (dlr_conv_apply)", "bound": "alu",
-                     "achieved": achieved_tflops, "peak": peak_tflops,
-                     "peak_kind": f"derived: {sm_count} SMs x 128 FP32 lanes x 2 x {sm_mhz:.0f} MHz",
-                     "unit": "TFLOP/s", "frac": achieved_tflops / peak_tflops,
-                     "traffic": traffic, "algorithmic_flops": apply_flops,
-                     "algorithmic_bytes": apply_bytes, "avg_launch_us": apply_avg * 1e6,
-                     "hbm": {"achieved": achieved, "peak": peak, "peak_kind": peak_kind,
-                             "unit": "GB/s", "frac": achieved / peak}},
+                   "step": "dlr_scan (tensor-core path): per-channel table kernel + chunked "
+                           "scan kernel, replayed as one CUDA graph"},
+        "layer_hbm": {"algorithmic_bytes": layer_bytes, "achieved_gbs": achieved,
+                      "frac_of_measured_peak": achieved / peak_gbs},
+        "roofline": {"kernel": "dlr_scan_tc_tables + dlr_scan_tc_kernel (whole step)",
+                     "bound": "hbm", "achieved": achieved, "peak": peak_gbs,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak_gbs,
+                     "traffic": traffic, "algorithmic_bytes": layer_bytes,
+                     "avg_step_us": step_avg * 1e6,
+                     "tensor": {"executed_flops": tc_flops,
+                                "achieved": tc_flops / step_avg / 1e12, "peak": tc_peak,
+                                "peak_kind": tc_kind, "unit": "TFLOP/s",
+                                "frac": tc_flops / step_avg / 1e12 / tc_peak}},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "paths": extras,
     }
@@ -344,15 +342,48 @@ def _time_steps(torch, fn, steps, warmup, flush):
     return statistics.median(s.elapsed_time(e) for s, e in ms)
 
 
-def run_extras(torch, dlr, inputs, flush):
-    """Secondary lines: the scan path on the same bank, and the other workloads."""
+def run_extras(torch, dlr, inputs, flush, sm_mhz, sm_count):
+    """Secondary lines: the FFT path and the float32 scan on the same bank, and the other
+    workloads."""
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     out = {}
     w = inputs.make_workload(WORKLOAD)
+    B, H, L = w.B, w.H, w.L
     u, fwd = dev(w.u), (dev(w.fwd.log_re), dev(w.fwd.log_im), dev(w.fwd.W))
     y = torch.empty_like(u)
-    ms = _time_steps(torch, lambda: dlr.dlr_scan(u, fwd, out=y), 20, 3, flush)
-    out["scan_" + WORKLOAD] = {"ms": ms, "elements_per_s": w.B * w.H * w.L / ms * 1e3}
+    # FFT layer: dlr_kernel + dlr_conv_spectrum + dlr_conv_apply, one CUDA graph; and the
+    # convolution kernel alone (it is bound by FP32 arithmetic: a real FFT of size M counts
+    # 2.5 M log2 M flops, forward + inverse 5 M log2 M, plus 6 flops per spectral bin)
+    K = torch.empty((H, L), dtype=torch.float32, device="cuda")
+    wsf = torch.empty(dlr.dlr_conv_workspace_size(H, L), dtype=torch.uint8, device="cuda")
+
+    def fft_step():
+        dlr.dlr_kernel(*fwd, L, "re", out=K)
+        dlr.dlr_conv_spectrum(K, workspace=wsf)
+        dlr.dlr_conv_apply(u, wsf, out=y)
+
+    for _ in range(3):
+        fft_step()
+    torch.cuda.synchronize()
+    g_fft, g_apply = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_fft):
+        fft_step()
+    with torch.cuda.graph(g_apply):
+        dlr.dlr_conv_apply(u, wsf, out=y)
+    ms = _time_steps(torch, g_fft.replay, 20, 3, flush)
+    ms_apply = _time_steps(torch, g_apply.replay, 20, 3, flush)
+    n = 1 << max(0, int(np.ceil(np.log2(L))))
+    M = 2 * n
+    apply_flops = B * H * (5 * M * np.log2(M) + 6 * (M // 2 + 1))
+    peak_tflops = sm_count * 128 * 2 * sm_mhz * 1e6 / 1e12
+    out["fft_" + WORKLOAD] = {
+        "ms": ms, "elements_per_s": B * H * L / ms * 1e3,
+        "conv_apply_us": ms_apply * 1e3,
+        "conv_apply_tflops": apply_flops / ms_apply / 1e9,
+        "conv_apply_frac_of_fp32_peak": apply_flops / ms_apply / 1e9 / peak_tflops}
+    del K, wsf
+    ms = _time_steps(torch, lambda: dlr.dlr_scan(u, fwd, out=y, algo="fp32"), 20, 3, flush)
+    out["scan_fp32_" + WORKLOAD] = {"ms": ms, "elements_per_s": B * H * L / ms * 1e3}
     del u, y
 
     w = inputs.make_workload("dlrprod_bidir_b4_h128_n1024_l16384")
@@ -371,7 +402,7 @@ def run_extras(torch, dlr, inputs, flush):
     u, fwd = dev(w.u), (dev(w.fwd.log_re), dev(w.fwd.log_im), dev(w.fwd.W))
     y = torch.empty_like(u)
     ms = _time_steps(torch, lambda: dlr.dlr_scan(u, fwd, out=y), 10, 2, flush)
-    out["scan_" + w.name] = {"ms": ms, "elements_per_s": w.B * w.H * w.L / ms * 1e3}
+    out["scan_tensor_" + w.name] = {"ms": ms, "elements_per_s": w.B * w.H * w.L / ms * 1e3}
     ws = torch.empty(dlr.dlr_conv_workspace_size(w.H, w.L), dtype=torch.uint8, device="cuda")
     ms = _time_steps(torch, lambda: dlr.dlr_layer(u, fwd, path="fft", workspace=ws, out=y), 10,
                      2, flush)
@@ -400,14 +431,23 @@ def run_extras(torch, dlr, inputs, flush):
 
 
 def cpu_baseline(w):
-    """The float64 oracle (as it stands) on the full bank, threaded over (b, h) rows."""
+    """The float64 oracle (as it stands) on the full bank, threaded over (b, h) rows; the bank
+    is repeated until at least one second of wall time (16+ core-seconds) has been spent."""
     import oracle
     threads = max(1, min(os.cpu_count() or 1, 64))
+    par = (w.fwd.log_re, w.fwd.log_im, w.fwd.W)
+    reps = 0
     t0 = time.perf_counter()
-    oracle.dlr_layer(w.u, (w.fwd.log_re, w.fwd.log_im, w.fwd.W), nthreads=threads)
-    dt = time.perf_counter() - t0
-    return {"value": w.B * w.H * w.L / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"full {WORKLOAD} bank (sequential float64 recurrence), {dt:.2f} s"}
+    while True:
+        oracle.dlr_layer(w.u, par, nthreads=threads)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= 1.0 or reps >= 200:
+            break
+    return {"value": reps * w.B * w.H * w.L / dt, "unit": UNIT, "cores": threads,
+            "kind": "oracle",
+            "sample": f"full {WORKLOAD} bank x {reps} (sequential float64 recurrence), "
+                      f"{dt:.2f} s wall"}
 
 
 # --------------------------------------------------------------------------------------------

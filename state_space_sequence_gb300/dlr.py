@@ -237,7 +237,7 @@ def dlr_layer(u, fwd, bwd=None, cast: str = "re", path: str = "fft", workspace=N
     if path == "scan":
         if cast != "re":
             raise ValueError("the scan path exists only for the Re cast")
-        return dlr_scan(u, fwd, bwd, out=out, stream=stream)
+        return dlr_scan(u, fwd, bwd, out=out, stream=stream, workspace=workspace)
     K1 = dlr_kernel(*fwd, L, cast, stream=stream)
     K2 = dlr_kernel(*bwd, L, cast, stream=stream) if bwd is not None else None
     return dlr_conv(u, K1, K2, out=out, workspace=workspace, stream=stream)
