@@ -74,7 +74,7 @@ namespace {
 
 constexpr int kT = 64;          // steps per chunk
 constexpr int kCols = 128;      // chunks per tile
-constexpr int kThreads = 416;   // warps 0-3 scan, 4-7 conv, 8-11 epi, 12 mma
+constexpr int kThreads = 448;   // warps 0-3 scan, 4-7 conv, 8-11 epi, 12 mma, 13 producer
 constexpr int kScanBar = 1, kConvBar = 2, kEpiBar = 3;  // named barriers (128 threads each)
 
 // TMEM columns (512 allocated): Q (hi 32 + lo 32 columns: A operand of GEMM1, two f16 per
@@ -92,30 +92,28 @@ constexpr uint32_t kUBuf = 32768, kULo = 16384;
 constexpr uint32_t kXHi = 65536, kXLo = 98304;      // Xin [128 chunks x 128 rows]
 constexpr uint32_t kTkHi = 131072, kTkLo = 139264;  // Toeplitz [64 t x 64 s], K-major
 constexpr uint32_t kGHi = 147456, kGLo = 163840;    // G [64 t x 128 rows], K-major
-constexpr uint32_t kStage = 180224;  // u staging: [2 halves][128 lines][32 floats], swizzled
-constexpr uint32_t kRowEs = kStage + 32768;  // int[2][128] u scale exponent of each row
+constexpr uint32_t kYStage = 180224;  // y staging, one 8 KB image per epilogue warp:
+                                      // [2 halves][32 lines][32 floats], swizzled
+constexpr uint32_t kRowEs = kYStage + 32768;  // int[2][128] u scale exponent of each row
 constexpr uint32_t kRowMaxU = kRowEs + 1024;  // uint[128] max |u| of each row (scratch)
 constexpr uint32_t kAy = kRowMaxU + 512;      // float[2][128] 1 / (u scale * K scale)
-constexpr uint32_t kColSx = kAy + 1024;     // float[2][128] Xin scale of chunk g
-constexpr uint32_t kBy = kColSx + 1024;     // float[2][128] 1 / (Xin scale * G scale)
-constexpr uint32_t kRowMax = kBy + 1024;    // float[128][4] per-row, per-warp max |Xin|
-constexpr uint32_t kChoice = kRowMax + 2048;     // int: the conv warps' next step
-constexpr uint32_t kBars = kChoice + 16;         // mbarriers
+constexpr uint32_t kBy = kAy + 1024;          // float[2][128] 1 / (Xin scale * G scale)
+constexpr uint32_t kScanRed = kBy + 1024;     // uint[4] per-warp max |carried state|
+constexpr uint32_t kBars = kScanRed + 16;     // mbarriers
 // A waiter may trail the phase it waits for by at most one completed phase (the parity test
 // cannot tell phase j from phase j + 2): every wait below is on a barrier that cannot
 // complete twice more before the waiter has passed it.
-constexpr int kBarStage = 0,   // u tile landed in the staging buffer (TMA bytes)
-    kBarUFull = 1,             // [2] u operand and its scales written (conv, 128)
-    kBarG1 = 3,                // [2] GEMM1 + Toeplitz done: S, Y1 ready, u buffer free (commit)
-    kBarSFree = 5,             // [2] Xin read out of S (conv, 128)
-    kBarXpReady = 7,           // [2] carries done, Xin in S, Xin scales written (scan, 128)
-    kBarXFull = 9,             // Xin operand written (conv, 128)
-    kBarG2 = 10,               // GEMM2 (state part) done: Y2 ready, Xin buffer free (commit)
-    kBarY1Free = 11,           // [2] Y1 read out of TMEM (epi, 128)
-    kBarY2Free = 13,           // Y2 read out of TMEM (epi, 128)
-    kBarTabTk = 14,            // Toeplitz operand copied (bytes)
-    kBarTabG = 15,             // G operand copied (bytes)
-    kNumBars = 16;
+constexpr int kBarStage = 0,   // [2] u tile (float32) landed in its operand buffer (TMA bytes)
+    kBarUFull = 2,             // [2] u operand and its scales written (conv, 128)
+    kBarG1 = 4,                // [2] GEMM1 + Toeplitz done: S, Y1 ready, u buffer free (commit)
+    kBarScanStart = 6,         // [2] u scales read, Xin scales written (scan, 128)
+    kBarXFull = 8,             // Xin operand written, S read (scan, 128)
+    kBarG2 = 9,                // GEMM2 (state part) done: Y2 ready, Xin buffer free (commit)
+    kBarY1Free = 10,           // [2] Y1 read out of TMEM (epi, 128)
+    kBarY2Free = 12,           // Y2 read out of TMEM (epi, 128)
+    kBarTabTk = 13,            // Toeplitz operand copied (bytes)
+    kBarTabG = 14,             // G operand copied (bytes)
+    kNumBars = 15;
 constexpr uint32_t kSlot = kBars + 8 * kNumBars;  // TMEM base address
 constexpr uint32_t kAbort = kSlot + 4;            // abort flag
 constexpr uint32_t kEnd = kAbort + 4;
@@ -470,10 +468,11 @@ __global__ void __launch_bounds__(256) dlr_scan_tc_tables(const TcScanArgs a, ui
 
 // ---- the roles ----------------------------------------------------------------------------
 
-// conv thread 0: the TMA tiles of u for tile k into the staging buffer (forward chunk order,
-// one 128-byte line per chunk and half), completing on kBarStage. Row mode: boxes of bc chunks
-// of each valid row; one-row mode: two boxes of 64 chunks. Chunks past the row (or before it,
-// reversed) read as zero.
+// producer thread: the TMA tiles of u for tile k, as float32, into the tile's operand buffer
+// (k & 1) -- forward chunk order, one 128-byte line per chunk and half, 128-byte swizzle --
+// completing on kBarStage + (k & 1). The conv warps convert them in place. Row mode: boxes of
+// bc chunks of each valid row; one-row mode: two boxes of 64 chunks. Chunks past the row (or
+// before it, reversed) read as zero.
 template <bool kRev>
 __device__ __forceinline__ void issue_u_tma(const TcScanArgs& a, const CUtensorMap* map,
                                             uint8_t* sm, int u0, int segs, int k) {
@@ -482,7 +481,9 @@ __device__ __forceinline__ void issue_u_tma(const TcScanArgs& a, const CUtensorM
   const int bc = a.bc;
   const int nrows = (a.R > 0) ? ti.nrows : 1;
   const int nblk = (a.R > 0) ? a.C / bc : kCols / bc;
-  tc::mbar_arrive_expect_tx(&bars[kBarStage], uint32_t(nrows * nblk * 2 * bc * 128));
+  uint64_t* bar = &bars[kBarStage + (k & 1)];
+  uint8_t* buf = sm + kU + (k & 1) * kUBuf;
+  tc::mbar_arrive_expect_tx(bar, uint32_t(nrows * nblk * 2 * bc * 128));
   for (int rl = 0; rl < nrows; ++rl)
     for (int cb = 0; cb < nblk; ++cb) {
       const int line0 = ((a.R > 0) ? rl * a.C : 0) + cb * bc;
@@ -491,8 +492,7 @@ __device__ __forceinline__ void issue_u_tma(const TcScanArgs& a, const CUtensorM
       const int z = (ti.b0 + rl) * a.H + ti.h;
 #pragma unroll
       for (int half = 0; half < 2; ++half)
-        tc::tma_load_3d(sm + kStage + half * 16384 + line0 * 128, map, half * 32, y, z,
-                        &bars[kBarStage]);
+        tc::tma_load_3d(buf + half * 16384 + line0 * 128, map, half * 32, y, z, bar);
     }
 }
 
@@ -505,9 +505,9 @@ __device__ __forceinline__ int mirrored_line(const TcScanArgs& a, int g) {
   return base + cb * bc + (bc - 1 - j);
 }
 
-// conv warps: u chunks of tile k -> scaled f16 pair, K-major (thread = chunk column g), from
-// the staging buffer (TMA path) or straight from memory. Returns false on abort.
-// Called once u_ready(k) holds (see conv_role).
+// conv warps: u chunks of tile k -> scaled f16 pair, K-major (thread = chunk column g), in
+// place over the float32 tile the TMA wrote into the same buffer (every thread has read its
+// chunk before the barrier inside, and writes only after it), or straight from memory.
 template <bool kRev>
 __device__ __forceinline__ void convert_u(const TcScanArgs& a, uint8_t* sm, int u0, int segs,
                                           int k, float sig_k) {
@@ -522,7 +522,7 @@ __device__ __forceinline__ void convert_u(const TcScanArgs& a, uint8_t* sm, int 
 #pragma unroll
     for (int q = 0; q < 16; ++q) {
       const float4 x = *reinterpret_cast<const float4*>(
-          sm + kStage + (q >> 3) * 16384 + line * 128 + ((uint32_t(q & 7) ^ sw) << 4));
+          sm + kU + par * kUBuf + (q >> 3) * 16384 + line * 128 + ((uint32_t(q & 7) ^ sw) << 4));
       if (!kRev) {
         v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
       } else {
@@ -580,51 +580,10 @@ __device__ __forceinline__ void load_q(const uint8_t* blob, uint32_t tmem) {
   }
 }
 
-// conv warps: Xin of tile k (in S, thread = state row r) -> scaled f16 pair, MN-major.
-// Called once xin_ready(k) holds (see conv_role).
-__device__ __forceinline__ void convert_xin(uint8_t* sm, uint32_t tmem, int k) {
-  const int r = threadIdx.x - 128, warp = threadIdx.x >> 5;
-  const int par = k & 1;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-  tc::fence_after_sync();
-  const float* sColSx = reinterpret_cast<const float*>(sm + kColSx) + par * 128;
-  const uint32_t tS = tmem + (uint32_t((warp & 3) * 32) << 16) + kTS + uint32_t(par) * 128;
-  const uint32_t kbase = uint32_t(r >> 3) * 2048u + uint32_t(r & 7) * 128u;
-  const uint32_t kr = uint32_t(r & 7);
-#pragma unroll 1
-  for (int blk = 0; blk < 4; ++blk) {
-    float v[32];
-    tc::tmem_ld32(tS + blk * 32, v);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int g0 = blk * 32 + q * 8;
-      const float4 c0 = *reinterpret_cast<const float4*>(sColSx + g0);
-      const float4 c1 = *reinterpret_cast<const float4*>(sColSx + g0 + 4);
-      const float sc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-      uint32_t h[4], l[4];
-#pragma unroll
-      for (int p = 0; p < 4; ++p)
-        split2(v[q * 8 + 2 * p] * sc[2 * p], v[q * 8 + 2 * p + 1] * sc[2 * p + 1], h[p], l[p]);
-      const uint32_t cg = uint32_t(g0 >> 3);
-      const uint32_t off = kbase + (cg >> 3) * 1024u + (((cg & 7u) ^ kr) << 4);
-      *reinterpret_cast<uint4*>(sm + kXHi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-      *reinterpret_cast<uint4*>(sm + kXLo + off) = make_uint4(l[0], l[1], l[2], l[3]);
-    }
-  }
-  tc::fence_proxy_async_smem();
-  tc::fence_before_sync();
-  mbar_arrive(&bars[kBarXFull]);
-  mbar_arrive(&bars[kBarSFree + par]);
-}
-
-// conv warps over all tiles of the CTA, in the order u of tile k+1, Xin of tile k (u of tile
-// k+1 only needs GEMM1 of tile k-1 to have released its buffers, which happens long before
-// the carries of tile k are done). u of tile k+1 is requested by TMA as soon as the u of tile
-// k has been read out of the staging buffer.
+// conv warps, tile k: the u operand of the tile, and Q of a new channel.
 template <bool kRev>
-__device__ __forceinline__ bool conv_u_step(const TcScanArgs& a, const CUtensorMap* map,
-                                            uint8_t* sm, uint32_t tmem, int u0, int segs,
-                                            int ntiles, int k, int& cur_h, float& sig_k,
+__device__ __forceinline__ bool conv_u_step(const TcScanArgs& a, uint8_t* sm, uint32_t tmem,
+                                            int u0, int segs, int k, int& cur_h, float& sig_k,
                                             volatile int* abort) {
   const int tid = threadIdx.x;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
@@ -632,14 +591,16 @@ __device__ __forceinline__ bool conv_u_step(const TcScanArgs& a, const CUtensorM
   const bool new_channel = ti.h != cur_h;
   const int par = k & 1;
   // the u buffer and scale slots of tile k-2 released (its GEMM1 done, its scales read by the
-  // epilogue); at a new channel also GEMM1 of tile k-1 done (Q is reloaded); the u tile landed
+  // scan and the epilogue); at a new channel also GEMM1 of tile k-1 done (Q is reloaded); the
+  // u tile landed
   bool ok = true;
   if (k >= 2)
     ok = warp_wait_phase(&bars[kBarG1 + par], ((k - 2) >> 1) & 1, abort) &&
+         warp_wait_phase(&bars[kBarScanStart + par], ((k - 2) >> 1) & 1, abort) &&
          warp_wait_phase(&bars[kBarY1Free + par], ((k - 2) >> 1) & 1, abort);
   if (ok && new_channel && k >= 1)
     ok = warp_wait_phase(&bars[kBarG1 + (par ^ 1)], ((k - 1) >> 1) & 1, abort);
-  if (ok && a.tma) ok = warp_wait_phase(&bars[kBarStage], k & 1, abort);
+  if (ok && a.tma) ok = warp_wait_phase(&bars[kBarStage + par], (k >> 1) & 1, abort);
   if (!named_bar_and(kConvBar, 128, ok)) return false;
   const uint8_t* blob = a.tables + (size_t)ti.h * kBlobBytes;
   if (new_channel) {
@@ -652,42 +613,80 @@ __device__ __forceinline__ bool conv_u_step(const TcScanArgs& a, const CUtensorM
     tc::tmem_wait_st();
   }
   tc::fence_before_sync();
-  named_bar(kConvBar, 128);  // the staging buffer is read: the next tile may land in it
-  reinterpret_cast<unsigned*>(sm + kRowMaxU)[tid - 128] = 0u;  // row maxima for the next tile
-  if (a.tma && tid == 128 && k + 1 < ntiles) issue_u_tma<kRev>(a, map, sm, u0, segs, k + 1);
   mbar_arrive(&bars[kBarUFull + par]);
+  named_bar(kConvBar, 128);  // every thread has read the row maxima of this tile
+  reinterpret_cast<unsigned*>(sm + kRowMaxU)[tid - 128] = 0u;
   return true;
 }
 
 template <bool kRev>
-__device__ __forceinline__ void conv_role(const TcScanArgs& a, const CUtensorMap* map,
-                                          uint8_t* sm, uint32_t tmem, int u0, int segs,
-                                          int ntiles, volatile int* abort) {
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-  if (ntiles == 0) return;
-  if (a.tma && threadIdx.x == 128) issue_u_tma<kRev>(a, map, sm, u0, segs, 0);
+__device__ __forceinline__ void conv_role(const TcScanArgs& a, uint8_t* sm, uint32_t tmem, int u0,
+                                          int segs, int ntiles, volatile int* abort) {
   int cur_h = -1;
   float sig_k = 1.f;
-  if (!conv_u_step<kRev>(a, map, sm, tmem, u0, segs, ntiles, 0, cur_h, sig_k, abort)) return;
-  for (int k = 0; k < ntiles; ++k) {
-    if (k + 1 < ntiles &&
-        !conv_u_step<kRev>(a, map, sm, tmem, u0, segs, ntiles, k + 1, cur_h, sig_k, abort))
-      return;
-    // Xin of tile k: its carries done and the Xin buffer free (GEMM2 of tile k-1 complete)
-    bool ok = warp_wait_phase(&bars[kBarXpReady + (k & 1)], (k >> 1) & 1, abort);
-    if (ok && k >= 1) ok = warp_wait_phase(&bars[kBarG2], (k - 1) & 1, abort);
-    if (!named_bar_and(kConvBar, 128, ok)) return;
-    convert_xin(sm, tmem, k);
+  for (int k = 0; k < ntiles; ++k)
+    if (!conv_u_step<kRev>(a, sm, tmem, u0, segs, k, cur_h, sig_k, abort)) return;
+}
+
+// producer (warp 13, lane 0): every bulk copy into shared memory, taken in the order the MMA
+// groups complete (GEMM1 of tile 0, then GEMM1 of tile k+1 and GEMM2 of tile k for k = 0, 1,
+// ...): u of tile k into operand buffer k & 1 once GEMM1 of tile k-2 has read that buffer;
+// the Toeplitz operand of a new channel once GEMM1 of the previous tile is done, its G operand
+// once GEMM2 of the previous tile is done. A thread blocked while the TMA unit takes a copy's
+// requests holds up nobody else.
+template <bool kRev>
+__device__ __forceinline__ void producer_role(const TcScanArgs& a, const CUtensorMap* map,
+                                              uint8_t* sm, int u0, int segs, int ntiles,
+                                              volatile int* abort) {
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  if (ntiles == 0) return;
+  auto channel = [&](int k) { return tile_info(a, u0, segs, k).h; };
+  auto copy_tk = [&](int h) {
+    tc::mbar_arrive_expect_tx(&bars[kBarTabTk], kGHi - kTkHi);
+    tc::bulk_load(sm + kTkHi, a.tables + (size_t)h * kBlobBytes, kGHi - kTkHi, &bars[kBarTabTk]);
+  };
+  auto copy_g = [&](int h) {
+    tc::mbar_arrive_expect_tx(&bars[kBarTabG], kGLo + 16384 - kGHi);
+    tc::bulk_load(sm + kGHi, a.tables + (size_t)h * kBlobBytes + (kGHi - kTkHi),
+                  kGLo + 16384 - kGHi, &bars[kBarTabG]);
+  };
+  if (a.tma) {
+    issue_u_tma<kRev>(a, map, sm, u0, segs, 0);
+    if (ntiles > 1) issue_u_tma<kRev>(a, map, sm, u0, segs, 1);
+  }
+  int h = channel(0);
+  copy_tk(h);
+  copy_g(h);
+  for (int k = -1; k < ntiles; ++k) {
+    // GEMM1 of tile j = k + 1 done: u of tile j + 2; the Toeplitz operand of tile j + 1
+    const int j = k + 1;
+    if (j < ntiles) {
+      const bool u_next = a.tma && j + 2 < ntiles;
+      const bool tk_next = j + 1 < ntiles && channel(j + 1) != channel(j);
+      if (u_next || tk_next) {
+        if (!wait_phase(&bars[kBarG1 + (j & 1)], (j >> 1) & 1, abort)) return;
+        if (u_next) issue_u_tma<kRev>(a, map, sm, u0, segs, j + 2);
+        if (tk_next) copy_tk(channel(j + 1));
+      }
+    }
+    // GEMM2 of tile k done: the G operand of tile k + 1
+    if (k >= 0 && k + 1 < ntiles && channel(k + 1) != channel(k)) {
+      if (!wait_phase(&bars[kBarG2], k & 1, abort)) return;
+      copy_g(channel(k + 1));
+    }
   }
 }
 
 // epi warps: y of tile k (thread = chunk column g = TMEM lane). Y1 (Toeplitz part, ready with
 // GEMM1) is read first into registers, releasing its TMEM buffer early; then Y2 (state part),
-// and y = Y1 / (u scale * K scale) + Y2 / (Xin scale * G scale) is stored (added at the
-// mirrored steps when kRev).
+// and y = Y1 / (u scale * K scale) + Y2 / (Xin scale * G scale). With whole-chunk rows (the
+// TMA shapes) each warp writes its 32 chunks into its staging image and one lane stores them
+// as two TMA tiles of 32 steps x 32 chunks (added, at the mirrored chunks and steps, when
+// kRev); otherwise each thread stores its chunk's 64 steps itself.
 template <bool kRev>
-__device__ __forceinline__ bool store_tile(const TcScanArgs& a, uint8_t* sm, uint32_t tmem,
-                                           int u0, int segs, int k, volatile int* abort) {
+__device__ __forceinline__ bool store_tile(const TcScanArgs& a, const CUtensorMap* ymap,
+                                           uint8_t* sm, uint32_t tmem, int u0, int segs, int k,
+                                           volatile int* abort) {
   const int g = threadIdx.x - 256, warp = threadIdx.x >> 5;
   const int par = k & 1;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
@@ -695,7 +694,7 @@ __device__ __forceinline__ bool store_tile(const TcScanArgs& a, uint8_t* sm, uin
   // Y1 of tile k with the u scales (conv) and Xin scales (scan) of tile k: once read, the Y1
   // buffer and both scale slots may take tile k + 2
   bool ok = warp_wait_phase(&bars[kBarG1 + par], (k >> 1) & 1, abort) &&
-            warp_wait_phase(&bars[kBarXpReady + par], (k >> 1) & 1, abort) &&
+            warp_wait_phase(&bars[kBarScanStart + par], (k >> 1) & 1, abort) &&
             warp_wait_phase(&bars[kBarUFull + par], (k >> 1) & 1, abort);
   if (!named_bar_and(kEpiBar, 128, ok)) return false;
   tc::fence_after_sync();
@@ -721,7 +720,35 @@ __device__ __forceinline__ bool store_tile(const TcScanArgs& a, uint8_t* sm, uin
   mbar_arrive(&bars[kBarY2Free]);
   const TileInfo ti = tile_info(a, u0, segs, k);
   const ColInfo ci = col_info(a, ti, g);
-  if (ci.valid) {
+  if (a.tma) {
+    const int lane = g & 31;
+    uint8_t* stg = sm + kYStage + (warp & 3) * 8192;
+    if (lane == 0) tc::bulk_wait_group_read0();  // this warp's previous tiles left the image
+    __syncwarp();
+    const int line = kRev ? 31 - lane : lane;
+    const uint32_t sw = uint32_t(line & 7);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {  // steps 4q .. 4q + 3 of the chunk (reversed when kRev)
+      const float4 v = kRev ? make_float4(y[63 - 4 * q], y[62 - 4 * q], y[61 - 4 * q],
+                                          y[60 - 4 * q])
+                            : make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
+      *reinterpret_cast<float4*>(stg + (q >> 3) * 4096 + line * 128 +
+                                 ((uint32_t(q & 7) ^ sw) << 4)) = v;
+    }
+    tc::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && ci.valid) {
+      // 32 columns of one row, chunks ci.c .. ci.c + 31 (reversed: forward chunks from C-32-c)
+      const int z = (ti.b0 + ci.rl) * a.H + ti.h;
+      const int yc = kRev ? a.C - 32 - ci.c : ci.c;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        if (kRev) tc::tma_reduce_add_3d(ymap, stg + half * 4096, half * 32, yc, z);
+        else tc::tma_store_3d(ymap, stg + half * 4096, half * 32, yc, z);
+      }
+      tc::bulk_commit_group();
+    }
+  } else if (ci.valid) {
     float* yrow = a.y + ci.rowoff;
     store_part<kRev>(yrow, a.L, ci.k0, *reinterpret_cast<float(*)[32]>(y));
     store_part<kRev>(yrow, a.L, ci.k0 + 32, *reinterpret_cast<float(*)[32]>(y + 32));
@@ -785,27 +812,24 @@ __device__ __forceinline__ void gemm2(uint8_t* sm, uint32_t tmem, int k) {
 }
 
 // MMA thread over all tiles of the CTA, in the order GEMM1 of tile k+1, GEMM2 of tile k. At a
-// change of channel the Toeplitz operand is copied in once GEMM1 of the previous tile has
-// completed, and the G operand once GEMM2 of the previous tile has completed, so only the work
-// that needs them waits. Returns false on abort.
+// change of channel GEMM1 waits for the producer's copy of the Toeplitz operand and GEMM2 for
+// its copy of G. Returns false on abort.
 __device__ __forceinline__ bool mma_g1(const TcScanArgs& a, uint8_t* sm, uint32_t tmem, int u0,
                                        int segs, int k, int& tk_h, uint32_t& tk_n,
                                        volatile int* abort) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
   const int par = k & 1;
   const int h = tile_info(a, u0, segs, k).h;
-  if (h != tk_h) {
-    if (k >= 1 && !wait_phase(&bars[kBarG1 + (par ^ 1)], ((k - 1) >> 1) & 1, abort)) return false;
-    tc::mbar_arrive_expect_tx(&bars[kBarTabTk], kGHi - kTkHi);
-    tc::bulk_load(sm + kTkHi, a.tables + (size_t)h * kBlobBytes, kGHi - kTkHi, &bars[kBarTabTk]);
+  if (h != tk_h) {  // the Toeplitz operand of a new channel (copied by the producer)
     if (!wait_phase(&bars[kBarTabTk], tk_n & 1, abort)) return false;
     ++tk_n;
     tk_h = h;
   }
+  // u of tile k written; the Y1 buffer read out (tile k-2). The S buffer of tile k-2 was read
+  // by the scan before it released Xin of that tile, which this thread waited for before
+  // issuing GEMM2 of tile k-2 (program order: GEMM1 k, GEMM2 k-1, GEMM1 k+1, ...).
   if (!wait_phase(&bars[kBarUFull + par], (k >> 1) & 1, abort)) return false;
-  if (k >= 2 && !(wait_phase(&bars[kBarSFree + par], ((k - 2) >> 1) & 1, abort) &&
-                  wait_phase(&bars[kBarY1Free + par], ((k - 2) >> 1) & 1, abort)))
-    return false;
+  if (k >= 2 && !wait_phase(&bars[kBarY1Free + par], ((k - 2) >> 1) & 1, abort)) return false;
   gemm1(sm, tmem, k);
   return true;
 }
@@ -815,11 +839,7 @@ __device__ __forceinline__ bool mma_g2(const TcScanArgs& a, uint8_t* sm, uint32_
                                        volatile int* abort) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
   const int h = tile_info(a, u0, segs, k).h;
-  if (h != g_h) {
-    if (k >= 1 && !wait_phase(&bars[kBarG2], (k - 1) & 1, abort)) return false;
-    tc::mbar_arrive_expect_tx(&bars[kBarTabG], kGLo + 16384 - kGHi);
-    tc::bulk_load(sm + kGHi, a.tables + (size_t)h * kBlobBytes + (kGHi - kTkHi),
-                  kGLo + 16384 - kGHi, &bars[kBarTabG]);
+  if (h != g_h) {  // the G operand of a new channel (copied by the producer)
     if (!wait_phase(&bars[kBarTabG], g_n & 1, abort)) return false;
     ++g_n;
     g_h = h;
@@ -841,196 +861,234 @@ __device__ __forceinline__ void mma_role(const TcScanArgs& a, uint8_t* sm, uint3
   }
 }
 
-// scan warps, one tile: carries along the chunks of S (in place: S becomes Xin), then the
-// Xin scale of every chunk column (the scale of its batch row).
+// ---- scan warps ---------------------------------------------------------------------------
+// Xin leaves the scan as X * 2^-xs, X in the S units of its tile (true state * 2^(es + 14)).
+// Within a tile |S| <= 64 * 2^14 * 2^14 per component, so a state that starts the tile at zero
+// stays below 127 * 2^34.5 < 2^41.5 and xs = 27 keeps Xin below 2^14.5, inside the f16 range
+// with room for the rounding of the split; a state carried in from the previous tile of a long
+// row raises xs by the excess of its bound over 2^41. Values far below the bound lose nothing
+// that matters: the f16 pair resolves 2^-24 absolute, i.e. 2^-24 of the row's largest |u|.
+constexpr int kXinShift = 27;
+
+// lambda^64 and the re-anchoring correction of the thread's state in (own, other) components:
+// the Im thread of a state pair runs the recurrence with the imaginary parts negated.
+struct ChainConst {
+  float mu_re, mu_im, dl_re, dl_im;
+};
+// state (xo, xt) <- mu * state + (s_own, s_oth)
+__device__ __forceinline__ void chain_step(const ChainConst& q, float s_own, float s_oth,
+                                           float& xo, float& xt) {
+  const float no = fmaf(q.mu_re, xo, fmaf(-q.mu_im, xt, s_own));
+  const float nt = fmaf(q.mu_re, xt, fmaf(q.mu_im, xo, s_oth));
+  xo = no;
+  xt = nt;
+}
+// re-anchoring at a 32-chunk boundary: state += (lambda^2048 - mu^32) * (state at the last
+// anchor); the corrected state becomes the new anchor
+__device__ __forceinline__ void chain_anchor(const ChainConst& q, float& xo, float& xt,
+                                             float& ao, float& at) {
+  xo = fmaf(q.dl_re, ao, fmaf(-q.dl_im, at, xo));
+  xt = fmaf(q.dl_re, at, fmaf(q.dl_im, ao, xt));
+  ao = xo;
+  at = xt;
+}
+
+// Byte offset of the 16-byte chunk of an Xin buffer holding K-row r, columns g0 .. g0 + 7
+// (g0 a multiple of 8): MN-major, 128-byte swizzle, atom (K-group r >> 3, MN-half g0 >> 6) at
+// (r >> 3) * 2048 + (g0 >> 6) * 1024, line r & 7, chunk ((g0 >> 3) & 7) XOR (r & 7).
+__device__ __forceinline__ uint32_t xin_chunk(int r, int g0) {
+  const uint32_t cg = uint32_t(g0 >> 3);
+  return uint32_t(r >> 3) * 2048u + (cg >> 3) * 1024u + uint32_t(r & 7) * 128u +
+         (((cg & 7u) ^ uint32_t(r & 7)) << 4);
+}
+// Eight Xin values of K-row r, columns g0 .. g0 + 7, times `s`, as the f16 pair.
+__device__ __forceinline__ void store_xin8(uint8_t* sm, int r, int g0, const float* v, float s) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) split2(v[2 * q] * s, v[2 * q + 1] * s, h[q], l[q]);
+  const uint32_t off = xin_chunk(r, g0);
+  *reinterpret_cast<uint4*>(sm + kXHi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(sm + kXLo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Row mode with rows of kC in {16, 32, 64} chunks (two or more rows per tile). The two threads
+// of state n split the rows: the even (Re) thread runs rows 0, 2, ..., the odd (Im) thread
+// rows 1, 3, ..., each the full complex recurrence; the other component of S comes from the
+// partner lane, which receives this lane's S of the partner's row in exchange. Each thread
+// writes both Xin K-rows of the state for its own columns. Software-pipelined by 8 chunks:
+// the stores of one piece and the recurrence of the next form one block, so the stores fill
+// the latency of the recurrence. The Xin buffer is written once GEMM2 of the previous tile
+// has released it (`wait_g2`, checked before the first store).
+template <int kC>
+__device__ __forceinline__ bool chain_pairs(uint8_t* sm, uint32_t tS, const ChainConst& q,
+                                            float xscale, bool wait_g2, uint32_t g2_parity,
+                                            volatile int* abort) {
+  const int tid = threadIdx.x;
+  const bool odd = (tid & 1) != 0;
+  const int col_off = odd ? kC : 0;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+#pragma unroll 1
+  for (int base = 0; base < kCols; base += 2 * kC) {
+    float xo = 0.f, xt = 0.f, ao = 0.f, at = 0.f;
+    float sa[8], sb[8];
+    tc::tmem_ld8x2(tS + base, tS + base + kC, sa, sb);
+    float oo[8], ot[8];  // outputs of the previous piece, stored with the next piece
+#pragma unroll 1
+    for (int c = base; c < base + kC; c += 8) {
+      if (c != base) {
+        if (((c - base) & 31) == 0) chain_anchor(q, xo, xt, ao, at);
+        if (wait_g2) {
+          if (!warp_wait_phase(&bars[kBarG2], g2_parity, abort)) return false;
+          wait_g2 = false;
+        }
+      }
+      float no[8], nt[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float own = odd ? sb[j] : sa[j];
+        const float oth = __shfl_xor_sync(0xffffffffu, odd ? sa[j] : sb[j], 1);
+        no[j] = xo;
+        nt[j] = xt;
+        chain_step(q, own, oth, xo, xt);
+      }
+      if (c != base) {
+        store_xin8(sm, tid, c - 8 + col_off, oo, xscale);
+        store_xin8(sm, tid ^ 1, c - 8 + col_off, ot, xscale);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        oo[j] = no[j];
+        ot[j] = nt[j];
+      }
+      if (c + 8 < base + kC) tc::tmem_ld8x2(tS + c + 8, tS + c + 8 + kC, sa, sb);
+    }
+    if (wait_g2) {
+      if (!warp_wait_phase(&bars[kBarG2], g2_parity, abort)) return false;
+      wait_g2 = false;
+    }
+    store_xin8(sm, tid, base + kC - 8 + col_off, oo, xscale);
+    store_xin8(sm, tid ^ 1, base + kC - 8 + col_off, ot, xscale);
+  }
+  return true;
+}
+
+// Any other row length, and rows longer than a tile (the state carried in xo, xt, ao, at):
+// both threads of a state pair run the recurrence over all 128 columns, the other component
+// of S from the partner lane, and each writes its own Xin K-row. Row mode resets the state at
+// every row start; anchors fall every 32 chunks from the row start (from the tile start for
+// long rows, where the anchor of a new row is zero).
+__device__ __forceinline__ bool chain_generic(const TcScanArgs& a, uint8_t* sm, uint32_t tS,
+                                              const ChainConst& q, float xscale, float& xo,
+                                              float& xt, float& ao, float& at, bool wait_g2,
+                                              uint32_t g2_parity, volatile int* abort) {
+  const int tid = threadIdx.x;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  const int C = a.C;
+  int next_reset = (a.R > 0) ? 0 : (1 << 30);
+  int next_anchor = 0;
+#pragma unroll 1
+  for (int c = 0; c < kCols; c += 16) {
+    float sv[16];
+    tc::tmem_ld16(tS + c, sv);
+    float oo[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int g = c + j;
+      const float oth = __shfl_xor_sync(0xffffffffu, sv[j], 1);
+      if (g == next_anchor) {
+        chain_anchor(q, xo, xt, ao, at);
+        next_anchor += 32;
+      }
+      if (g == next_reset) {
+        xo = xt = ao = at = 0.f;
+        next_reset += C;
+        next_anchor = g + 32;
+      }
+      oo[j] = xo;
+      chain_step(q, sv[j], oth, xo, xt);
+    }
+    if (wait_g2) {
+      if (!warp_wait_phase(&bars[kBarG2], g2_parity, abort)) return false;
+      wait_g2 = false;
+    }
+    store_xin8(sm, tid, c, oo, xscale);
+    store_xin8(sm, tid, c + 8, oo + 8, xscale);
+  }
+  return true;
+}
+
+// scan warps, one tile (thread r = TMEM lane r = state row r): the Xin scale of every chunk
+// column, then the carries along the chunks of S written as the Xin operand.
 __device__ __forceinline__ bool scan_tile(const TcScanArgs& a, uint8_t* sm, uint32_t tmem,
-                                          int k, bool new_row, float mu_re, float mu_im,
-                                          float dl_re, float dl_im, float sig_g, float& xo,
-                                          float& xt, float& ao, float& at, int& es_prev,
-                                          volatile int* abort) {
+                                          int k, bool new_row, const ChainConst& q, float sig_g,
+                                          float& xo, float& xt, float& ao, float& at,
+                                          int& es_prev, volatile int* abort) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int par = k & 1;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
   const int* sRowEs = reinterpret_cast<const int*>(sm + kRowEs) + par * 128;
-  float* sColSx = reinterpret_cast<float*>(sm + kColSx) + par * 128;
   float* sBy = reinterpret_cast<float*>(sm + kBy) + par * 128;
-  float* sRowMax = reinterpret_cast<float*>(sm + kRowMax);
+  unsigned* sRed = reinterpret_cast<unsigned*>(sm + kScanRed);
   const uint32_t tS = tmem + (uint32_t(warp * 32) << 16) + kTS + uint32_t(par) * 128;
 
-  // S of this tile, and (for the row scales) the conv threads' release of tile k
+  // S of this tile and the u scales of its rows
   bool ok = warp_wait_phase(&bars[kBarG1 + par], (k >> 1) & 1, abort) &&
             warp_wait_phase(&bars[kBarUFull + par], (k >> 1) & 1, abort);
   if (!named_bar_and(kScanBar, 128, ok)) return false;
   tc::fence_after_sync();
 
-  if (new_row) {
+  int xs = kXinShift;
+  if (a.R == 0) {
+    // one row walked tile by tile: the carried state and anchor move from the previous tile's
+    // S units to this tile's (times 2^(es - es_prev), in two exact steps); the Xin scale makes
+    // room for the carried state's magnitude
+    const int es = sRowEs[0];
+    if (new_row) {
+      xo = xt = ao = at = 0.f;
+    } else {
+      const int d = max(-252, min(252, es - es_prev));
+      const float f = exp2i(d / 2) * exp2i(d - d / 2);
+      xo *= f; xt *= f; ao *= f; at *= f;
+    }
+    es_prev = es;
+    const unsigned mw = __reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(fabsf(xo), fabsf(xt))));
+    if (lane == 0) sRed[warp] = mw;
+    named_bar(kScanBar, 128);
+    const unsigned m = max(max(sRed[0], sRed[1]), max(sRed[2], sRed[3]));
+    const int e = int((m >> 23) & 0xFFu) - 126;  // carried |state| < 2^e
+    xs += max(0, e - 41);
+  } else {
     xo = xt = ao = at = 0.f;
-  } else {
-    // the carried state and anchor, from the previous tile's units of S to this tile's
-    // (S scales with the row's u scale 2^es): times 2^(es - es_prev), in two exact steps
-    const int d = max(-252, min(252, sRowEs[0] - es_prev));
-    const float f = exp2i(d / 2) * exp2i(d - d / 2);
-    xo *= f; xt *= f; ao *= f; at *= f;
   }
-  es_prev = sRowEs[0];
-  const int C = a.C;
-  if (a.R > 0 && (C == 32 || C == 64)) {
-    // two independent chains: columns [0, 64) and [64, 128) (whole rows of 32 or 64 chunks);
-    // row starts and anchors fall on 32-column block starts
-    float xoB = 0.f, xtB = 0.f, aoB = 0.f, atB = 0.f, lA = 0.f, lB = 0.f;
-#pragma unroll 1
-    for (int bb = 0; bb < 2; ++bb) {
-      const int cA = bb * 32, cB = 64 + bb * 32;
-      if (cA % C == 0) {
-        xo = xt = ao = at = 0.f;
-        xoB = xtB = aoB = atB = 0.f;
-      } else {
-        xo = fmaf(dl_re, ao, fmaf(-dl_im, at, xo));
-        xt = fmaf(dl_re, at, fmaf(dl_im, ao, xt));
-        ao = xo;
-        at = xt;
-        xoB = fmaf(dl_re, aoB, fmaf(-dl_im, atB, xoB));
-        xtB = fmaf(dl_re, atB, fmaf(dl_im, aoB, xtB));
-        aoB = xoB;
-        atB = xtB;
-      }
-#pragma unroll 1
-      for (int hf = 0; hf < 2; ++hf) {
-      float sA[16], sB[16];
-      tc::tmem_ld16(tS + cA + 16 * hf, sA);
-      tc::tmem_ld16(tS + cB + 16 * hf, sB);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float pA = __shfl_xor_sync(0xffffffffu, sA[j], 1);
-        const float pB = __shfl_xor_sync(0xffffffffu, sB[j], 1);
-        const float oA = xo, oB = xoB;
-        lA = fmaxf(lA, fabsf(oA));
-        lB = fmaxf(lB, fabsf(oB));
-        const float noA = fmaf(mu_re, xo, fmaf(-mu_im, xt, sA[j]));
-        const float ntA = fmaf(mu_re, xt, fmaf(mu_im, xo, pA));
-        const float noB = fmaf(mu_re, xoB, fmaf(-mu_im, xtB, sB[j]));
-        const float ntB = fmaf(mu_re, xtB, fmaf(mu_im, xoB, pB));
-        sA[j] = oA;
-        sB[j] = oB;
-        xo = noA;
-        xt = ntA;
-        xoB = noB;
-        xtB = ntB;
-      }
-      tc::tmem_st16(tS + cA + 16 * hf, sA);
-      tc::tmem_st16(tS + cB + 16 * hf, sB);
-      }
-      if ((cA + 32) % C == 0) {  // rows end with this block
-        const unsigned mA = __reduce_max_sync(0xffffffffu, __float_as_uint(lA));
-        const unsigned mB = __reduce_max_sync(0xffffffffu, __float_as_uint(lB));
-        if (lane == 0) {
-          sRowMax[(cA / C) * 4 + warp] = __uint_as_float(mA);
-          sRowMax[(cB / C) * 4 + warp] = __uint_as_float(mB);
-        }
-        lA = lB = 0.f;
-      }
-    }
-    tc::tmem_wait_st();
-  } else if (a.R == 0 || C % 32 == 0) {
-    // one chain (one row per tile): a row start at column 0 when new_row, anchors at every
-    // other 32-column block start
-    float l = 0.f;
-#pragma unroll 1
-    for (int blk = 0; blk < 4; ++blk) {
-      const int c0 = blk * 32;
-      if (a.R > 0 && c0 % C == 0) {
-        xo = xt = ao = at = 0.f;
-      } else {
-        xo = fmaf(dl_re, ao, fmaf(-dl_im, at, xo));
-        xt = fmaf(dl_re, at, fmaf(dl_im, ao, xt));
-        ao = xo;
-        at = xt;
-      }
-#pragma unroll 1
-      for (int hf = 0; hf < 2; ++hf) {
-      float sv[16];
-      tc::tmem_ld16(tS + c0 + 16 * hf, sv);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float p = __shfl_xor_sync(0xffffffffu, sv[j], 1);
-        const float o = xo;
-        l = fmaxf(l, fabsf(o));
-        const float no = fmaf(mu_re, xo, fmaf(-mu_im, xt, sv[j]));
-        const float nt = fmaf(mu_re, xt, fmaf(mu_im, xo, p));
-        sv[j] = o;
-        xo = no;
-        xt = nt;
-      }
-      tc::tmem_st16(tS + c0 + 16 * hf, sv);
-      }
-    }
-    tc::tmem_wait_st();
-    const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(l));
-    if (lane == 0) sRowMax[warp] = __uint_as_float(m);
-  } else {
-    // any other row length: row starts and anchors checked column by column
-    int next_reset = 0;
-    int next_anchor = 0;
-    float lmax = 0.f;
-    int row_i = 0;
-#pragma unroll 1
-    for (int blk = 0; blk < 4; ++blk) {
-      float sv[32], o[32];
-      tc::tmem_ld32(tS + blk * 32, sv);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int g = blk * 32 + j;
-        const float sother = __shfl_xor_sync(0xffffffffu, sv[j], 1);
-        if (g == next_anchor) {
-          xo = fmaf(dl_re, ao, fmaf(-dl_im, at, xo));
-          xt = fmaf(dl_re, at, fmaf(dl_im, ao, xt));
-          ao = xo;
-          at = xt;
-          next_anchor += 32;
-        }
-        if (g == next_reset) {
-          if (g > 0) {
-            const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(lmax));
-            if (lane == 0) sRowMax[row_i * 4 + warp] = __uint_as_float(m);
-            ++row_i;
-            lmax = 0.f;
-          }
-          xo = xt = ao = at = 0.f;
-          next_reset += C;
-          next_anchor = g + 32;
-        }
-        o[j] = xo;
-        lmax = fmaxf(lmax, fabsf(xo));
-        const float no = fmaf(mu_re, xo, fmaf(-mu_im, xt, sv[j]));
-        const float nt = fmaf(mu_re, xt, fmaf(mu_im, xo, sother));
-        xo = no;
-        xt = nt;
-      }
-      tc::tmem_st32(tS + blk * 32, o);
-    }
-    tc::tmem_wait_st();
-    const unsigned m = __reduce_max_sync(0xffffffffu, __float_as_uint(lmax));
-    if (lane == 0) sRowMax[row_i * 4 + warp] = __uint_as_float(m);
-  }
-  named_bar(kScanBar, 128);
   {
+    // y = Y2 * 2^(xs - 14 - es) / sig_g for the column's row
     const int row = (a.R > 0) ? tid / a.C : 0;
-    const float xmax = fmaxf(fmaxf(sRowMax[row * 4], sRowMax[row * 4 + 1]),
-                             fmaxf(sRowMax[row * 4 + 2], sRowMax[row * 4 + 3]));
-    const int ex = scale_exp(xmax);
-    sColSx[tid] = exp2i(ex);
-    // true Xin = (S units) * 2^(-14 - es_row): Y2 / (2^ex sig_g) * 2^(-14 - es_row)
-    const int er = max(-126, -14 - sRowEs[row]);
-    sBy[tid] = exp2i(-ex) * exp2i(er) / sig_g;
+    sBy[tid] = exp2i(xs - kXinShift) * exp2i(kXinShift - 14 - sRowEs[row]) / sig_g;
   }
+  mbar_arrive(&bars[kBarScanStart + par]);
+
+  const float xscale = exp2i(-xs);
+  const bool wait_g2 = k > 0;
+  const uint32_t g2_parity = uint32_t(k - 1) & 1u;
+  if (a.R > 0 && a.C == 64)
+    ok = chain_pairs<64>(sm, tS, q, xscale, wait_g2, g2_parity, abort);
+  else if (a.R > 0 && a.C == 32)
+    ok = chain_pairs<32>(sm, tS, q, xscale, wait_g2, g2_parity, abort);
+  else if (a.R > 0 && a.C == 16)
+    ok = chain_pairs<16>(sm, tS, q, xscale, wait_g2, g2_parity, abort);
+  else
+    ok = chain_generic(a, sm, tS, q, xscale, xo, xt, ao, at, wait_g2, g2_parity, abort);
+  if (!ok) return false;
+  tc::fence_proxy_async_smem();
   tc::fence_before_sync();
-  mbar_arrive(&bars[kBarXpReady + par]);
+  mbar_arrive(&bars[kBarXFull]);
   return true;
 }
 
 template <bool kRev>
 __global__ void __maxnreg__(128)
-    dlr_scan_tc_kernel(const TcScanArgs a, const __grid_constant__ CUtensorMap umap) {
+    dlr_scan_tc_kernel(const TcScanArgs a, const __grid_constant__ CUtensorMap umap,
+                       const __grid_constant__ CUtensorMap ymap) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1040,17 +1098,16 @@ __global__ void __maxnreg__(128)
 
   const int tid = threadIdx.x, warp = tid >> 5;
   if (tid == 0) {
-    tc::mbar_init(&bars[kBarStage], 1);
     tc::mbar_init(&bars[kBarTabTk], 1);
     tc::mbar_init(&bars[kBarTabG], 1);
     tc::mbar_init(&bars[kBarG2], 1);
     tc::mbar_init(&bars[kBarXFull], 128);
     tc::mbar_init(&bars[kBarY2Free], 128);
     for (int p = 0; p < 2; ++p) {
+      tc::mbar_init(&bars[kBarStage + p], 1);
       tc::mbar_init(&bars[kBarUFull + p], 128);
       tc::mbar_init(&bars[kBarG1 + p], 1);
-      tc::mbar_init(&bars[kBarSFree + p], 128);
-      tc::mbar_init(&bars[kBarXpReady + p], 128);
+      tc::mbar_init(&bars[kBarScanStart + p], 128);
       tc::mbar_init(&bars[kBarY1Free + p], 128);
     }
     *abort = 0;
@@ -1072,7 +1129,8 @@ __global__ void __maxnreg__(128)
   const int ntiles = (u1 - u0) * segs;
 
   if (warp < 4) {
-    float mu_re = 0.f, mu_im = 0.f, dl_re = 0.f, dl_im = 0.f, sig_g = 1.f;
+    ChainConst q{0.f, 0.f, 0.f, 0.f};
+    float sig_g = 1.f;
     float xo = 0.f, xt = 0.f, ao = 0.f, at = 0.f;
     int es_prev = 0;
     int cur_h = -1;
@@ -1085,23 +1143,25 @@ __global__ void __maxnreg__(128)
         cur_h = ti.h;
         const uint8_t* blob = a.tables + (size_t)ti.h * kBlobBytes;
         const float4 m = __ldg(reinterpret_cast<const float4*>(blob + kBlobMu) + (tid >> 1));
-        mu_re = m.x;
-        dl_re = m.z;
-        mu_im = (tid & 1) ? -m.y : m.y;
-        dl_im = (tid & 1) ? -m.w : m.w;
+        q.mu_re = m.x;
+        q.dl_re = m.z;
+        q.mu_im = (tid & 1) ? -m.y : m.y;
+        q.dl_im = (tid & 1) ? -m.w : m.w;
         sig_g = __ldg(reinterpret_cast<const float*>(blob + kBlobSig) + 1);
       }
-      if (!scan_tile(a, sm, tmem, k, ti.seg == 0, mu_re, mu_im, dl_re, dl_im, sig_g, xo, xt, ao,
-                     at, es_prev, abort))
+      if (!scan_tile(a, sm, tmem, k, ti.seg == 0, q, sig_g, xo, xt, ao, at, es_prev, abort))
         break;
     }
   } else if (warp < 8) {
-    conv_role<kRev>(a, &umap, sm, tmem, u0, segs, ntiles, abort);
+    conv_role<kRev>(a, sm, tmem, u0, segs, ntiles, abort);
   } else if (warp < 12) {
     for (int k = 0; k < ntiles; ++k)
-      if (!store_tile<kRev>(a, sm, tmem, u0, segs, k, abort)) break;
+      if (!store_tile<kRev>(a, &ymap, sm, tmem, u0, segs, k, abort)) break;
+    if (a.tma && (tid & 31) == 0) tc::bulk_wait_group0();  // y stores done, staging unused
+  } else if (warp == 12) {
+    if ((tid & 31) == 0) mma_role(a, sm, tmem, u0, segs, ntiles, abort);
   } else if ((tid & 31) == 0) {
-    mma_role(a, sm, tmem, u0, segs, ntiles, abort);
+    producer_role<kRev>(a, &umap, sm, u0, segs, ntiles, abort);
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -1123,8 +1183,8 @@ int sm_count() {
   return n;
 }
 
-// 3D view of u for the TMA loads: [64 steps][C chunks][B*H rows], boxes of 32 steps x bc chunks
-// x 1 row, 128-byte swizzle (one 128-byte line per chunk and half).
+// 3D view of u (or y) for the TMA copies: [64 steps][C chunks][B*H rows], boxes of 32 steps x
+// bc chunks x 1 row, 128-byte swizzle (one 128-byte line per chunk and half).
 bool make_u_map(CUtensorMap* m, const float* u, int B, int H, int L, int bc) {
   auto fn = tc::tensor_map_encoder();
   if (!fn) return false;
@@ -1141,7 +1201,7 @@ bool make_u_map(CUtensorMap* m, const float* u, int B, int H, int L, int bc) {
 
 template <bool kRev>
 cudaError_t launch_one(const TcScanArgs& a, uint8_t* ws, const CUtensorMap& umap,
-                       cudaStream_t s) {
+                       const CUtensorMap& ymap, cudaStream_t s) {
   cudaError_t e = max_smem_once<dlr_scan_tc_kernel<kRev>>(kSmemBytes);
   if (e != cudaSuccess) return e;
   const int sms = sm_count();
@@ -1150,7 +1210,7 @@ cudaError_t launch_one(const TcScanArgs& a, uint8_t* ws, const CUtensorMap& umap
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int grid = std::min(a.units, sms);
-  dlr_scan_tc_kernel<kRev><<<grid, kThreads, kSmemBytes, s>>>(a, umap);
+  dlr_scan_tc_kernel<kRev><<<grid, kThreads, kSmemBytes, s>>>(a, umap, ymap);
   return cudaGetLastError();
 }
 
@@ -1187,18 +1247,21 @@ cudaError_t launch_dlr_scan_tc(const float* u, const float* lr, const float* li,
   const bool tma_shape = (L % kT == 0) && ((a.R > 0) ? (a.C == 32 || a.C == 64 || a.C == 128)
                                                       : (a.C % 64 == 0));
   a.bc = (a.C == 32) ? 32 : 64;
-  CUtensorMap umap;
+  CUtensorMap umap, ymap;
   std::memset(&umap, 0, sizeof(umap));
-  a.tma = tma_shape && make_u_map(&umap, u, B, H, L, a.bc) ? 1 : 0;
+  std::memset(&ymap, 0, sizeof(ymap));
+  a.tma = tma_shape && make_u_map(&umap, u, B, H, L, a.bc) && make_u_map(&ymap, y, B, H, L, 32)
+              ? 1
+              : 0;
   a.log_re = lr;
   a.log_im = li;
   a.W = reinterpret_cast<const float2*>(W);
-  cudaError_t e = launch_one<false>(a, static_cast<uint8_t*>(ws), umap, s);
+  cudaError_t e = launch_one<false>(a, static_cast<uint8_t*>(ws), umap, ymap, s);
   if (e != cudaSuccess || !bidir) return e;
   a.log_re = lr2;
   a.log_im = li2;
   a.W = reinterpret_cast<const float2*>(W2);
-  return launch_one<true>(a, static_cast<uint8_t*>(ws), umap, s);
+  return launch_one<true>(a, static_cast<uint8_t*>(ws), umap, ymap, s);
 }
 
 }  // namespace dlr
