@@ -70,6 +70,25 @@
 #include "tc_ptx.cuh"
 
 namespace dlr {
+
+// Timeline hooks of profiling builds (compiled with DLR_SCAN_TRACE: CTA 0 records the global
+// timer at fixed points into a device buffer the caller provides); no code otherwise.
+#ifdef DLR_SCAN_TRACE
+__device__ long long* g_scan_trace;
+#define SCAN_TRACE(slot)                                                        \
+  do {                                                                          \
+    if (blockIdx.x == 0 && (slot) >= 0 && (slot) < 4096) {                      \
+      unsigned long long t_;                                                    \
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                    \
+      g_scan_trace[(slot)] = (long long)t_;                                     \
+    }                                                                           \
+  } while (0)
+#else
+#define SCAN_TRACE(slot) \
+  do {                   \
+  } while (0)
+#endif
+
 namespace {
 
 constexpr int kT = 64;          // steps per chunk
@@ -129,10 +148,10 @@ constexpr uint32_t kBlobSig = kBlobMu + 1024; // float [4]: K scale, G scale
 constexpr uint32_t kBlobBytes = kBlobSig + 1024;  // 83968, a multiple of 1024
 static_assert(kBlobSmem == 49152 && kBlobBytes % 1024 == 0, "blob layout");
 
-// Shared memory of the tables kernel.
-constexpr uint32_t kTbKp = 0;                  // float [64 states][65] Re(W_n lambda_n^j)
+// Shared memory of the tables kernel: the blob image, then scratch.
+constexpr uint32_t kTbKp = kBlobBytes;         // float [64 states][65] Re(W_n lambda_n^j)
 constexpr uint32_t kTbK = kTbKp + 64 * 65 * 4; // float [64] K_0..K_63
-constexpr uint32_t kTbRed = kTbK + 256;        // float [32]
+constexpr uint32_t kTbRed = kTbK + 256;        // float [2][16]
 constexpr uint32_t kTbBytes = kTbRed + 128;
 
 struct TcScanArgs {
@@ -215,15 +234,18 @@ __device__ __forceinline__ bool warp_wait_phase(uint64_t* bar, uint32_t parity,
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
-// Max over the 256 threads of the tables kernel; `slot` picks 8 floats of `red`.
-__device__ __forceinline__ float block_max256(float v, float* red, int slot) {
+constexpr int kTbThreads = 512;  // threads of the tables kernel
+
+// Max over the kTbThreads threads of the tables kernel; `slot` picks 16 floats of `red`.
+__device__ __forceinline__ float block_max_tb(float v, float* red, int slot) {
+  constexpr int kWarps = kTbThreads / 32;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  if ((threadIdx.x & 31) == 0) red[slot * 8 + (threadIdx.x >> 5)] = v;
+  if ((threadIdx.x & 31) == 0) red[slot * kWarps + (threadIdx.x >> 5)] = v;
   __syncthreads();
-  float m = red[slot * 8];
+  float m = red[slot * kWarps];
 #pragma unroll
-  for (int i = 1; i < 8; ++i) m = fmaxf(m, red[slot * 8 + i]);
+  for (int i = 1; i < kWarps; ++i) m = fmaxf(m, red[slot * kWarps + i]);
   return m;
 }
 
@@ -355,80 +377,83 @@ __device__ __forceinline__ void store_part(float* __restrict__ row, int L, int k
   }
 }
 
-// Per-channel tables (one CTA of 256 threads per channel h) into the channel's blob: the
+// Per-channel tables (one CTA of 512 threads per channel h) into the channel's blob: the
 // Toeplitz block of K_0..K_63 and G (scaled f16 pairs, swizzled exactly as in the main
 // kernel's shared memory), Q (scaled f16 pairs as TMEM words), lambda^64 and the re-anchoring
-// correction lambda^2048 - (lambda^64)^32 of every state, the scales of K and G.
-// Thread (n, q) = (tid >> 2, tid & 3) owns state n and exponents j = 16q .. 16q + 16, held in
-// registers: lambda^{16q + 4c} (c <= 4) and lambda^d (d < 4) evaluated directly, the others
-// as one product of two of them.
-__global__ void __launch_bounds__(256) dlr_scan_tc_tables(const TcScanArgs a, uint8_t* ws) {
-  extern __shared__ __align__(16) uint8_t tsm[];
+// correction lambda^2048 - (lambda^64)^32 of every state, the scales of K and G. The blob is
+// assembled in shared memory and leaves in bulk copies.
+// Thread (n, q) = (tid & 63, tid >> 6) owns state n and exponents j = 8q .. 8q + 8, held in
+// registers: lambda^{8q + 4c} (c <= 2) and lambda^d (d < 4) evaluated directly, the others as
+// one product of two of them; warps 14 and 15 (q = 7) also form the re-anchoring correction.
+__global__ void __launch_bounds__(kTbThreads, 2)
+    dlr_scan_tc_tables(const TcScanArgs a, uint8_t* ws) {
+  extern __shared__ __align__(1024) uint8_t tsm[];
   const int tid = threadIdx.x;
   const int h = blockIdx.x;
-  uint8_t* blob = ws + (size_t)h * kBlobBytes;
+  uint8_t* img = tsm;  // the blob image
   float* sKp = reinterpret_cast<float*>(tsm + kTbKp);  // [64 states][65] Re(W_n lambda_n^j)
   float* sK = reinterpret_cast<float*>(tsm + kTbK);
   float* sRed = reinterpret_cast<float*>(tsm + kTbRed);
   const int N = a.N;
-  const int n = tid >> 2, q = tid & 3;
+  const int n = tid & 63, q = tid >> 6;
   const bool on = n < N;
+  if (tid == 0) SCAN_TRACE(3900);
   const lam_param p = on ? make_lam_param(a.log_re[(size_t)h * N + n], a.log_im[(size_t)h * N + n])
                          : lam_param{0.f, 0.f, 0.f};
   const float2 w = on ? __ldg(&a.W[(size_t)h * N + n]) : make_float2(0.f, 0.f);
-  const float sig_g = exp2i(scale_exp(block_max256(fmaxf(fabsf(w.x), fabsf(w.y)), sRed, 0)));
+  const float sig_g = exp2i(scale_exp(block_max_tb(fmaxf(fabsf(w.x), fabsf(w.y)), sRed, 0)));
+  if (tid == 0) SCAN_TRACE(3901);
 
-  // pw[i] = lambda^{16q + i}, i = 0..16
-  cf pw[17];
+  // pw[i] = lambda^{8q + i}, i = 0..8
+  cf pw[9];
   {
-    cf base[5], small[4];
+    cf base[3], small[4];
 #pragma unroll
-    for (int c = 0; c < 5; ++c) base[c] = on ? lam_pow(p, 16 * q + 4 * c) : cf{0.f, 0.f};
+    for (int c = 0; c < 3; ++c) base[c] = on ? lam_pow(p, 8 * q + 4 * c) : cf{0.f, 0.f};
+    small[0] = cf{1.f, 0.f};
 #pragma unroll
-    for (int d = 0; d < 4; ++d) small[d] = on ? lam_pow(p, d) : cf{0.f, 0.f};
+    for (int d = 1; d < 4; ++d) small[d] = on ? lam_pow(p, d) : cf{0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < 17; ++i) pw[i] = (i & 3) ? cmul(base[i >> 2], small[i & 3]) : base[i >> 2];
+    for (int i = 0; i < 9; ++i) pw[i] = (i & 3) ? cmul(base[i >> 2], small[i & 3]) : base[i >> 2];
   }
-  // Q rows 2n (Re) and 2n+1 (Im) at steps t = 63 - j, j in [16q, 16q + 16): TMEM words
-  // (lower step in the low half) 24 - 8q .. 31 - 8q of each row
+  // Q rows 2n (Re) and 2n+1 (Im) at steps t = 63 - j, j in [8q, 8q + 8): TMEM words (lower step
+  // in the low half) 28 - 4q .. 31 - 4q of each row
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
-    uint32_t hi[8], lo[8];
+    uint32_t hi[4], lo[4];
 #pragma unroll
-    for (int m = 0; m < 8; ++m) {
-      const cf p0 = pw[15 - 2 * m], p1 = pw[14 - 2 * m];  // steps t0 = 48 - 16q + 2m, t0 + 1
+    for (int m = 0; m < 4; ++m) {
+      const cf p0 = pw[7 - 2 * m], p1 = pw[6 - 2 * m];  // steps t0 = 56 - 8q + 2m, t0 + 1
       split2((c ? p0.im : p0.re) * 16384.f, (c ? p1.im : p1.re) * 16384.f, hi[m], lo[m]);
     }
-    uint4* row = reinterpret_cast<uint4*>(blob + kBlobQ + (2 * n + c) * 256);
-    row[6 - 2 * q] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    row[7 - 2 * q] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
-    row[14 - 2 * q] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-    row[15 - 2 * q] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+    uint4* row = reinterpret_cast<uint4*>(img + kBlobQ + (2 * n + c) * 256);
+    row[7 - q] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    row[15 - q] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
   }
-  // G rows t = 16q .. 16q + 15, columns 2n, 2n+1: Re, -Im of W_n lambda_n^{t+1}; and the
-  // products' real parts for the tap sums
+  // G rows t = 8q .. 8q + 7, columns 2n, 2n+1: Re, -Im of W_n lambda_n^{t+1}; and the products'
+  // real parts for the tap sums
   {
     const int kb = n >> 5;
     const uint32_t colb = uint32_t(((2 * n) & 7) * 2);  // byte offset of the pair in its chunk
     const uint32_t chunk = uint32_t((n & 31) >> 2);
-    uint8_t* gh = blob + (kGHi - kTkHi) + kb * 8192;
-    uint8_t* gl = blob + (kGLo - kTkHi) + kb * 8192;
+    uint8_t* gh = img + (kGHi - kTkHi) + kb * 8192;
+    uint8_t* gl = img + (kGLo - kTkHi) + kb * 8192;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int t = 16 * q + i;
+    for (int i = 0; i < 8; ++i) {
+      const int t = 8 * q + i;
       const cf g = cmul({w.x, w.y}, pw[i + 1]);
       uint32_t hb, lb;
       split2(g.re * sig_g, -g.im * sig_g, hb, lb);
       const uint32_t off = uint32_t(t) * 128u + ((chunk ^ uint32_t(t & 7)) << 4) + colb;
       *reinterpret_cast<uint32_t*>(gh + off) = hb;
       *reinterpret_cast<uint32_t*>(gl + off) = lb;
-      sKp[n * 65 + 16 * q + i] = cmul({w.x, w.y}, pw[i]).re;  // Re(W lambda^j), j = 16q + i
+      sKp[n * 65 + 8 * q + i] = cmul({w.x, w.y}, pw[i]).re;  // Re(W lambda^j), j = 8q + i
     }
   }
-  // lambda^64 and the re-anchoring correction (state n, thread q = 3 holds lambda^64)
-  if (q == 3) {
+  // lambda^64 and the re-anchoring correction (warps 14 and 15: q = 7 holds lambda^64)
+  if (q == 7) {
     float2 d = make_float2(0.f, 0.f);
-    const cf m = pw[16];
+    const cf m = pw[8];
     if (on) {
       cff pp = {{m.re, 0.f}, {m.im, 0.f}};
 #pragma unroll 1
@@ -438,32 +463,47 @@ __global__ void __launch_bounds__(256) dlr_scan_tc_tables(const TcScanArgs a, ui
       const ff di = ff_add(ff{a32.im, 0.f}, ff_neg(pp.im));
       d = make_float2(dr.hi + dr.lo, di.hi + di.lo);
     }
-    reinterpret_cast<float4*>(blob + kBlobMu)[n] = make_float4(m.re, m.im, d.x, d.y);
+    reinterpret_cast<float4*>(img + kBlobMu)[n] = make_float4(m.re, m.im, d.x, d.y);
   }
+  if (tid == 0) SCAN_TRACE(3902);
   __syncthreads();
-  // K_j = sum_n Re(W_n lambda_n^j): thread (j, part) = (tid >> 2, tid & 3) sums 16 states
-  const int j = tid >> 2, part = tid & 3;
+  if (tid == 0) SCAN_TRACE(3903);
+  // K_j = sum_n Re(W_n lambda_n^j): thread (j, part) = (tid >> 3, tid & 7) sums 8 states
+  const int j = tid >> 3, part = tid & 7;
   float ks = 0.f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) ks += sKp[(16 * part + i) * 65 + j];
+  for (int i = 0; i < 8; ++i) ks += sKp[(8 * part + i) * 65 + j];
   ks += __shfl_xor_sync(0xffffffffu, ks, 1);
   ks += __shfl_xor_sync(0xffffffffu, ks, 2);
+  ks += __shfl_xor_sync(0xffffffffu, ks, 4);
   if (part == 0) sK[j] = ks;
-  const float sig_k = exp2i(scale_exp(block_max256(part == 0 ? fabsf(ks) : 0.f, sRed, 1)));
+  const float sig_k = exp2i(scale_exp(block_max_tb(part == 0 ? fabsf(ks) : 0.f, sRed, 1)));
   if (tid == 0) {
-    reinterpret_cast<float*>(blob + kBlobSig)[0] = sig_k;
-    reinterpret_cast<float*>(blob + kBlobSig)[1] = sig_g;
+    reinterpret_cast<float*>(img + kBlobSig)[0] = sig_k;
+    reinterpret_cast<float*>(img + kBlobSig)[1] = sig_g;
   }
-  // Toeplitz row t = j, s in [16 part, 16 part + 16): K_{t-s} for s <= t (sK complete after the
-  // barrier inside block_max256)
-  float tv[16];
+  // Toeplitz row t = j, s in [8 part, 8 part + 8): K_{t-s} for s <= t (sK complete after the
+  // barrier inside block_max_tb)
+  float tv[8];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int ss = 16 * part + i;
+  for (int i = 0; i < 8; ++i) {
+    const int ss = 8 * part + i;
     tv[i] = (ss <= j) ? sK[j - ss] * sig_k : 0.f;
   }
-  store_chunk8(blob, blob + (kTkLo - kTkHi), j, 2 * part, tv);
-  store_chunk8(blob, blob + (kTkLo - kTkHi), j, 2 * part + 1, tv + 8);
+  store_chunk8(img, img + (kTkLo - kTkHi), j, part, tv);
+  // the image to the channel's blob
+  tc::fence_proxy_async_smem();
+  __syncthreads();
+  if (tid == 0) SCAN_TRACE(3904);
+  if (tid == 0) {
+    uint8_t* blob = ws + (size_t)h * kBlobBytes;
+    constexpr uint32_t kPart = kBlobBytes / 4;  // 20992, a multiple of 16
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tc::bulk_store(blob + i * kPart, img + i * kPart, kPart);
+    tc::bulk_commit_group();
+    tc::bulk_wait_group0();
+    SCAN_TRACE(3905);
+  }
 }
 
 // ---- the roles ----------------------------------------------------------------------------
@@ -602,6 +642,7 @@ __device__ __forceinline__ bool conv_u_step(const TcScanArgs& a, uint8_t* sm, ui
     ok = warp_wait_phase(&bars[kBarG1 + (par ^ 1)], ((k - 1) >> 1) & 1, abort);
   if (ok && a.tma) ok = warp_wait_phase(&bars[kBarStage + par], (k >> 1) & 1, abort);
   if (!named_bar_and(kConvBar, 128, ok)) return false;
+  if (tid == 128) SCAN_TRACE(1000 + k * 8 + 1);
   const uint8_t* blob = a.tables + (size_t)ti.h * kBlobBytes;
   if (new_channel) {
     cur_h = ti.h;
@@ -613,6 +654,7 @@ __device__ __forceinline__ bool conv_u_step(const TcScanArgs& a, uint8_t* sm, ui
     tc::tmem_wait_st();
   }
   tc::fence_before_sync();
+  if (tid == 128) SCAN_TRACE(1000 + k * 8 + 2);
   mbar_arrive(&bars[kBarUFull + par]);
   named_bar(kConvBar, 128);  // every thread has read the row maxima of this tile
   reinterpret_cast<unsigned*>(sm + kRowMaxU)[tid - 128] = 0u;
@@ -665,6 +707,7 @@ __device__ __forceinline__ void producer_role(const TcScanArgs& a, const CUtenso
       const bool tk_next = j + 1 < ntiles && channel(j + 1) != channel(j);
       if (u_next || tk_next) {
         if (!wait_phase(&bars[kBarG1 + (j & 1)], (j >> 1) & 1, abort)) return;
+        SCAN_TRACE(1000 + (j + 2) * 8 + 5);
         if (u_next) issue_u_tma<kRev>(a, map, sm, u0, segs, j + 2);
         if (tk_next) copy_tk(channel(j + 1));
       }
@@ -697,6 +740,7 @@ __device__ __forceinline__ bool store_tile(const TcScanArgs& a, const CUtensorMa
             warp_wait_phase(&bars[kBarScanStart + par], (k >> 1) & 1, abort) &&
             warp_wait_phase(&bars[kBarUFull + par], (k >> 1) & 1, abort);
   if (!named_bar_and(kEpiBar, 128, ok)) return false;
+  if (g == 0) SCAN_TRACE(2000 + k * 8 + 0);
   tc::fence_after_sync();
   const float ay = reinterpret_cast<const float*>(sm + kAy)[par * 128 + g];
   const float by = reinterpret_cast<const float*>(sm + kBy)[par * 128 + g];
@@ -708,6 +752,7 @@ __device__ __forceinline__ bool store_tile(const TcScanArgs& a, const CUtensorMa
   // Y2 of tile k
   ok = warp_wait_phase(&bars[kBarG2], k & 1, abort);
   if (!named_bar_and(kEpiBar, 128, ok)) return false;
+  if (g == 0) SCAN_TRACE(2000 + k * 8 + 1);
   tc::fence_after_sync();
 #pragma unroll
   for (int q4 = 0; q4 < 4; ++q4) {
@@ -748,6 +793,7 @@ __device__ __forceinline__ bool store_tile(const TcScanArgs& a, const CUtensorMa
       }
       tc::bulk_commit_group();
     }
+    if (g == 0) SCAN_TRACE(2000 + k * 8 + 2);
   } else if (ci.valid) {
     float* yrow = a.y + ci.rowoff;
     store_part<kRev>(yrow, a.L, ci.k0, *reinterpret_cast<float(*)[32]>(y));
@@ -761,6 +807,7 @@ __device__ __forceinline__ bool store_tile(const TcScanArgs& a, const CUtensorMa
 __device__ __forceinline__ void gemm1(uint8_t* sm, uint32_t tmem, int k) {
   const int par = k & 1;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  SCAN_TRACE(3000 + k * 4 + 0);
   tc::fence_after_sync();
   constexpr uint32_t id1 = tc::idesc_f16_f32(128, 128);
   constexpr uint32_t idk = tc::idesc_f16_f32(128, 64);
@@ -795,6 +842,7 @@ __device__ __forceinline__ void gemm1(uint8_t* sm, uint32_t tmem, int k) {
 // GEMM2 (state part) of tile k: Y2 = Xin G^T.
 __device__ __forceinline__ void gemm2(uint8_t* sm, uint32_t tmem, int k) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  SCAN_TRACE(3000 + k * 4 + 1);
   tc::fence_after_sync();
   constexpr uint32_t idm = tc::idesc_f16_f32(128, 64) | (1u << 15);  // A (Xin) MN-major
   const uint64_t gh = tc::smem_desc_k_sw128(sm + kGHi), gl = tc::smem_desc_k_sw128(sm + kGLo);
@@ -1036,6 +1084,7 @@ __device__ __forceinline__ bool scan_tile(const TcScanArgs& a, uint8_t* sm, uint
             warp_wait_phase(&bars[kBarUFull + par], (k >> 1) & 1, abort);
   if (!named_bar_and(kScanBar, 128, ok)) return false;
   tc::fence_after_sync();
+  if (tid == 0) SCAN_TRACE(k * 8 + 0);
 
   int xs = kXinShift;
   if (a.R == 0) {
@@ -1079,6 +1128,7 @@ __device__ __forceinline__ bool scan_tile(const TcScanArgs& a, uint8_t* sm, uint
   else
     ok = chain_generic(a, sm, tS, q, xscale, xo, xt, ao, at, wait_g2, g2_parity, abort);
   if (!ok) return false;
+  if (tid == 0) SCAN_TRACE(k * 8 + 3);
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   mbar_arrive(&bars[kBarXFull]);
@@ -1097,6 +1147,7 @@ __global__ void __maxnreg__(128)
   volatile int* abort = reinterpret_cast<volatile int*>(sm + kAbort);
 
   const int tid = threadIdx.x, warp = tid >> 5;
+  if (tid == 0) SCAN_TRACE(3999);
   if (tid == 0) {
     tc::mbar_init(&bars[kBarTabTk], 1);
     tc::mbar_init(&bars[kBarTabG], 1);
@@ -1165,6 +1216,7 @@ __global__ void __maxnreg__(128)
   }
   tc::fence_before_sync();
   __syncthreads();
+  if (tid == 0) SCAN_TRACE(3997);
   if (*abort) report_status(a.status, DLR_ERR_TIMEOUT);
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }
@@ -1206,7 +1258,9 @@ cudaError_t launch_one(const TcScanArgs& a, uint8_t* ws, const CUtensorMap& umap
   if (e != cudaSuccess) return e;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorUnknown;
-  dlr_scan_tc_tables<<<a.H, 256, kTbBytes, s>>>(a, ws);
+  e = max_smem_once<dlr_scan_tc_tables>(kTbBytes);
+  if (e != cudaSuccess) return e;
+  dlr_scan_tc_tables<<<a.H, kTbThreads, kTbBytes, s>>>(a, ws);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int grid = std::min(a.units, sms);
