@@ -25,34 +25,35 @@
 // Precision: every operand is split into two f16 halves a = a_hi + a_lo (a_lo = the f16
 // rounding of a - a_hi), and each product is hi*hi + hi*lo + lo*hi (three MMAs, f32
 // accumulation in tensor memory; the dropped lo*lo term is below 2^-22 relative). Before the
-// split every operand is scaled by a power of two so that its largest entry lies in
-// [2^13, 2^14): per batch row and tile for u and for Xin, per channel for K and G,
-// 2^14 for Q (|Q| <= 1), so that one row's scale never depends on another row's magnitude.
-// The scalings are exact and undone in fp32 when Xin and y are written (the carries run on
+// split every operand is scaled by a power of two: u per batch row and tile so that its
+// largest |u| lies in [2^13, 2^14) (one row's scale never depends on another row's
+// magnitude), K and G per channel the same way, Q by 2^14 (|Q| <= 1), and Xin by the fixed
+// 2^-27 of its tile's S units (raised for a state carried in from the previous tile; see
+// kXinShift). The scalings are exact and undone in fp32 when y is written (the carries run on
 // S in its scaled units; a row continued into the next tile is rescaled to that tile's units).
-// Powers lambda^j are evaluated from an exactly reduced phase (lam_pow) for j = 16q + 4c and
+// Powers lambda^j are evaluated from an exactly reduced phase (lam_pow) for j = 8q + 4c and
 // j < 4 and combined by one complex product, so no power carries a long multiplication chain.
 //
 // Two kernels. dlr_scan_tc_tables (one CTA per channel) evaluates the per-channel tables --
 // Q, the Toeplitz block of K_0..K_63 and G as scaled f16 pairs in the exact byte layout the
 // MMAs read, lambda^64, the re-anchoring correction and the two scales -- into a workspace
-// blob per channel. dlr_scan_tc_kernel then runs one persistent CTA per SM with four roles
+// blob per channel. dlr_scan_tc_kernel then runs one persistent CTA per SM with five roles
 // joined by mbarriers, two tiles in flight:
-//   warps 0-3   "scan": thread r owns TMEM lane r = state row r; runs step 2 on S in place
-//                       (S becomes Xin), and the per-row Xin scales,
-//   warps 4-7   "conv": loads u (3D TMA tiles into a staging buffer, or plain loads when the
-//                       rows are not whole chunks) and writes its scaled f16 pair, MN-major
-//                       (tile k); then reads Xin from TMEM (thread = state row) and writes its
-//                       scaled f16 pair, MN-major (tile k-1); loads Q into TMEM for a new
-//                       channel,
+//   warps 0-3   "scan": thread r owns TMEM lane r = state row r; runs step 2 on S and writes
+//                       the states straight into the Xin operand (MN-major f16 pair),
+//   warps 4-7   "conv": thread g = chunk g; converts the float32 u tile the producer landed
+//                       in the tile's operand buffer, in place, into its scaled f16 pair
+//                       (K-major), or loads u itself when the rows are not whole chunks; loads
+//                       Q into TMEM for a new channel,
 //   warps 8-11  "epi":  thread g owns TMEM lane g = chunk g; reads Y1, Y2, scales them and
-//                       writes y through a shared-memory staging image with row-coalesced
-//                       stores (the staging is the u operand buffer GEMM2 has finished with),
-//   warp 12, lane 0:    issues the MMAs, GEMM2 of the oldest tile whose Xin is ready, else
-//                       GEMM1 of the next tile whose u is ready, and copies the Toeplitz and G
-//                       operands of a new channel in between GEMM2s.
-// Buffers: u operand x2, S accumulator x2 (TMEM), Xin x1, Y1/Y2 x1, Q x2 (TMEM), Toeplitz and
-// G x1 (shared memory), u staging x1.
+//                       writes y through a per-warp staging image and TMA stores (or plain
+//                       stores when the rows are not whole chunks),
+//   warp 12, lane 0:    issues the MMAs: GEMM1 (with the Toeplitz part) of tile k+1, then
+//                       GEMM2 of tile k,
+//   warp 13, lane 0:    the producer: every bulk copy (u tiles, the Toeplitz and G operands of
+//                       a new channel), in the order the MMA groups complete.
+// Buffers: u operand x2, Xin x1, Toeplitz and G x1, y staging (shared memory); Q, S x2,
+// Y1 x2, Y2 (TMEM).
 // Units of work: a tile holds floor(128 / C) whole rows when a row has C <= 128 chunks
 // (several batch rows of one channel), otherwise one row walks its tiles in order and carries
 // its state from tile to tile. A CTA takes a contiguous range of units.
