@@ -167,6 +167,26 @@ dlr_status dlr_scan_ex(const float* u, const float* log_re, const float* log_im,
                        dlr_stream_t stream);
 
 /*
+ * dlr_scan_prepare / dlr_scan_apply -- the two halves of the tensor-core dlr_scan for one
+ * parameter set (same method and precision as DLR_SCAN_TENSOR), for callers that run many
+ * batches through the same parameters: the tables depend only on (log_re, log_im, W).
+ * dlr_scan_prepare writes the channel tables into `workspace` (dlr_scan_workspace_size bytes,
+ * 16-byte aligned; N <= 64, else DLR_ERR_UNSUPPORTED). dlr_scan_apply runs the layer on u with
+ * the tables that a preceding dlr_scan_prepare (same H and N, earlier in stream order) left in
+ * `workspace`, which it only reads: reverse = 0 writes y = DLR(u); reverse = 1 adds
+ * rev(DLR(rev(u))) to y (the second direction of the bidirectional layer, DLR paper section
+ * 2.1). u, y: [B, H, L], not overlapping each other or the workspace. dlr_scan_ex with
+ * DLR_SCAN_TENSOR is prepare + apply (twice for DLR_BIDIR). One kernel launch each; faults of
+ * apply's bounded waits are reported through dlr_get_device_status().
+ */
+dlr_status dlr_scan_prepare(const float* log_re, const float* log_im, const float* W, int64_t H,
+                            int64_t N, void* workspace, size_t workspace_bytes,
+                            dlr_stream_t stream);
+dlr_status dlr_scan_apply(const float* u, int64_t B, int64_t H, int64_t N, int64_t L,
+                          int reverse, float* y, const void* workspace, size_t workspace_bytes,
+                          dlr_stream_t stream);
+
+/*
  * s5_layer -- S5 SSM outputs (S5 paper section 3: diagonalised MIMO system; zero-order hold
  * with one timescale per state; diagonal feedthrough):
  *   Delta_p   = exp(log_delta[p])

@@ -17,6 +17,10 @@ cudaError_t launch_dlr_scan(const float* u, const float* lr, const float* li, co
                             const float* lr2, const float* li2, const float* W2, bool bidir,
                             int B, int H, int N, int L, float* y, cudaStream_t s);
 size_t scan_tc_workspace_bytes(int64_t H);
+cudaError_t launch_scan_tc_tables(const float* lr, const float* li, const float* W, int H, int N,
+                                  void* ws, cudaStream_t s);
+cudaError_t launch_scan_tc_apply(const float* u, int B, int H, int L, bool reverse, float* y,
+                                 const void* ws, int* status, cudaStream_t s);
 cudaError_t launch_dlr_scan_tc(const float* u, const float* lr, const float* li, const float* W,
                                const float* lr2, const float* li2, const float* W2, bool bidir,
                                int B, int H, int N, int L, float* y, void* ws, int* status,
@@ -69,7 +73,7 @@ dlr_status check_params(const float* log_re, const float* log_im, const float* W
 
 extern "C" {
 
-int dlr_abi_version(void) { return 2; }
+int dlr_abi_version(void) { return 3; }
 
 const char* dlr_last_cuda_error(void) { return t_last_cuda_error; }
 
@@ -202,6 +206,36 @@ dlr_status dlr_scan_ex(const float* u, const float* log_re, const float* log_im,
   return from_cuda(dlr::launch_dlr_scan(u, log_re, log_im, W, log_re2, log_im2, W2,
                                         dir == DLR_BIDIR, (int)B, (int)H, (int)N, (int)L, y,
                                         (cudaStream_t)stream));
+}
+
+dlr_status dlr_scan_prepare(const float* log_re, const float* log_im, const float* W, int64_t H,
+                            int64_t N, void* workspace, size_t workspace_bytes,
+                            dlr_stream_t stream) {
+  if (H < 1 || N < 1) return DLR_ERR_INVALID_ARG;
+  dlr_status st = check_params(log_re, log_im, W);
+  if (st != DLR_OK) return st;
+  if (N > 64 || H > kMaxGrid) return DLR_ERR_UNSUPPORTED;
+  const size_t need = dlr::scan_tc_workspace_bytes(H);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DLR_ERR_WORKSPACE;
+  return from_cuda(dlr::launch_scan_tc_tables(log_re, log_im, W, (int)H, (int)N, workspace,
+                                              (cudaStream_t)stream));
+}
+
+dlr_status dlr_scan_apply(const float* u, int64_t B, int64_t H, int64_t N, int64_t L,
+                          int reverse, float* y, const void* workspace, size_t workspace_bytes,
+                          dlr_stream_t stream) {
+  if (B < 1 || H < 1 || N < 1 || L < 1) return DLR_ERR_INVALID_ARG;
+  if (reverse != 0 && reverse != 1) return DLR_ERR_INVALID_ARG;
+  if (!u || !y || !aligned16(u) || !aligned16(y)) return DLR_ERR_INVALID_ARG;
+  const size_t bytes = sizeof(float) * (size_t)B * (size_t)H * (size_t)L;
+  if (ranges_overlap(u, bytes, y, bytes)) return DLR_ERR_INVALID_ARG;
+  if (N > 64 || L > kMaxL || B * H > kMaxGrid) return DLR_ERR_UNSUPPORTED;
+  const size_t need = dlr::scan_tc_workspace_bytes(H);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DLR_ERR_WORKSPACE;
+  if (ranges_overlap(workspace, need, u, bytes) || ranges_overlap(workspace, need, y, bytes))
+    return DLR_ERR_INVALID_ARG;
+  return from_cuda(dlr::launch_scan_tc_apply(u, (int)B, (int)H, (int)L, reverse != 0, y,
+                                             workspace, status_word(), (cudaStream_t)stream));
 }
 
 size_t s5_workspace_size(int64_t B, int64_t L, int64_t H, int64_t P, dlr_prec prec) {

@@ -1253,17 +1253,12 @@ bool make_u_map(CUtensorMap* m, const float* u, int B, int H, int L, int bc) {
 }
 
 template <bool kRev>
-cudaError_t launch_one(const TcScanArgs& a, uint8_t* ws, const CUtensorMap& umap,
-                       const CUtensorMap& ymap, cudaStream_t s) {
+cudaError_t launch_main(const TcScanArgs& a, const CUtensorMap& umap, const CUtensorMap& ymap,
+                        cudaStream_t s) {
   cudaError_t e = max_smem_once<dlr_scan_tc_kernel<kRev>>(kSmemBytes);
   if (e != cudaSuccess) return e;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorUnknown;
-  e = max_smem_once<dlr_scan_tc_tables>(kTbBytes);
-  if (e != cudaSuccess) return e;
-  dlr_scan_tc_tables<<<a.H, kTbThreads, kTbBytes, s>>>(a, ws);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
   const int grid = std::min(a.units, sms);
   dlr_scan_tc_kernel<kRev><<<grid, kThreads, kSmemBytes, s>>>(a, umap, ymap);
   return cudaGetLastError();
@@ -1273,18 +1268,30 @@ cudaError_t launch_one(const TcScanArgs& a, uint8_t* ws, const CUtensorMap& umap
 
 size_t scan_tc_workspace_bytes(int64_t H) { return (size_t)H * kBlobBytes; }
 
-// N <= 64 complex states; u, y [B, H, L]; bidirectional adds the reversed pass (run after the
-// forward one, reusing the workspace for its tables).
-cudaError_t launch_dlr_scan_tc(const float* u, const float* lr, const float* li, const float* W,
-                               const float* lr2, const float* li2, const float* W2, bool bidir,
-                               int B, int H, int N, int L, float* y, void* ws, int* status,
-                               cudaStream_t s) {
+// The channel tables of one parameter set (N <= 64 states) into the workspace.
+cudaError_t launch_scan_tc_tables(const float* lr, const float* li, const float* W, int H, int N,
+                                  void* ws, cudaStream_t s) {
+  TcScanArgs a{};
+  a.H = H;
+  a.N = N;
+  a.log_re = lr;
+  a.log_im = li;
+  a.W = reinterpret_cast<const float2*>(W);
+  cudaError_t e = max_smem_once<dlr_scan_tc_tables>(kTbBytes);
+  if (e != cudaSuccess) return e;
+  dlr_scan_tc_tables<<<H, kTbThreads, kTbBytes, s>>>(a, static_cast<uint8_t*>(ws));
+  return cudaGetLastError();
+}
+
+// The layer on u [B, H, L] with the tables in the workspace: y = DLR(u), or (reverse) y +=
+// rev(DLR(rev(u))).
+cudaError_t launch_scan_tc_apply(const float* u, int B, int H, int L, bool reverse, float* y,
+                                 const void* ws, int* status, cudaStream_t s) {
   TcScanArgs a{};
   a.u = u;
   a.y = y;
   a.B = B;
   a.H = H;
-  a.N = N;
   a.L = L;
   a.C = (L + kT - 1) / kT;
   if (a.C <= kCols) {
@@ -1308,15 +1315,21 @@ cudaError_t launch_dlr_scan_tc(const float* u, const float* lr, const float* li,
   a.tma = tma_shape && make_u_map(&umap, u, B, H, L, a.bc) && make_u_map(&ymap, y, B, H, L, 32)
               ? 1
               : 0;
-  a.log_re = lr;
-  a.log_im = li;
-  a.W = reinterpret_cast<const float2*>(W);
-  cudaError_t e = launch_one<false>(a, static_cast<uint8_t*>(ws), umap, ymap, s);
+  return reverse ? launch_main<true>(a, umap, ymap, s) : launch_main<false>(a, umap, ymap, s);
+}
+
+// N <= 64 complex states; u, y [B, H, L]; bidirectional adds the reversed pass (run after the
+// forward one, reusing the workspace for its tables).
+cudaError_t launch_dlr_scan_tc(const float* u, const float* lr, const float* li, const float* W,
+                               const float* lr2, const float* li2, const float* W2, bool bidir,
+                               int B, int H, int N, int L, float* y, void* ws, int* status,
+                               cudaStream_t s) {
+  cudaError_t e = launch_scan_tc_tables(lr, li, W, H, N, ws, s);
+  if (e == cudaSuccess) e = launch_scan_tc_apply(u, B, H, L, false, y, ws, status, s);
   if (e != cudaSuccess || !bidir) return e;
-  a.log_re = lr2;
-  a.log_im = li2;
-  a.W = reinterpret_cast<const float2*>(W2);
-  return launch_one<true>(a, static_cast<uint8_t*>(ws), umap, ymap, s);
+  e = launch_scan_tc_tables(lr2, li2, W2, H, N, ws, s);
+  if (e == cudaSuccess) e = launch_scan_tc_apply(u, B, H, L, true, y, ws, status, s);
+  return e;
 }
 
 }  // namespace dlr

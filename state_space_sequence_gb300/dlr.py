@@ -55,6 +55,10 @@ def _load():
         lib.dlr_scan_ex.argtypes = [P, P, P, P, P, P, P, i32, i64, i64, i64, i64, P, i32, P, sz,
                                     P]
         lib.dlr_scan_ex.restype = i32
+        lib.dlr_scan_prepare.argtypes = [P, P, P, i64, i64, P, sz, P]
+        lib.dlr_scan_prepare.restype = i32
+        lib.dlr_scan_apply.argtypes = [P, i64, i64, i64, i64, i32, P, P, sz, P]
+        lib.dlr_scan_apply.restype = i32
         lib.s5_workspace_size.argtypes = [i64, i64, i64, i64, i32]
         lib.s5_workspace_size.restype = sz
         lib.s5_layer.argtypes = [P, P, P, P, P, P, i64, i64, i64, i64, i32, P, P, sz, P]
@@ -193,6 +197,37 @@ def dlr_scan(u, fwd, bwd=None, out=None, stream=None, algo: str = "auto", worksp
                                         _ptr(li2), _ptr(W2), 1 if bwd is not None else 0, B, H,
                                         N, L, _ptr(out), SCAN_ALGO[algo], _ptr(workspace),
                                         ws_bytes, _stream(stream)))
+    return out
+
+
+def dlr_scan_prepare(params, workspace=None, stream=None, B: int = 1, L: int = 64):
+    """Channel tables of one parameter set (log_re, log_im, W) for dlr_scan_apply, into a uint8
+    device ``workspace`` of dlr_scan_workspace_size bytes (allocated here when not given).
+    Tensor-core path only (N <= 64)."""
+    lr, li, W = _params(params)
+    H, N = lr.shape
+    need = dlr_scan_workspace_size(B, H, N, L)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=lr.device)
+    _ok("dlr_scan_prepare", _load().dlr_scan_prepare(_ptr(lr), _ptr(li), _ptr(W), H, N,
+                                                     _ptr(workspace), workspace.numel(),
+                                                     _stream(stream)))
+    return workspace
+
+
+def dlr_scan_apply(u, workspace, N: int, out=None, reverse: bool = False, stream=None):
+    """The tensor-core scan of u [B, H, L] with the tables dlr_scan_prepare left in
+    ``workspace``: out = DLR(u), or (reverse) out += rev(DLR(rev(u)))."""
+    _check_f32(u)
+    B, H, L = u.shape
+    if out is None:
+        if reverse:
+            raise ValueError("reverse=True adds into out: pass it")
+        out = torch.empty_like(u)
+    _check_f32(out)
+    _ok("dlr_scan_apply", _load().dlr_scan_apply(_ptr(u), B, H, N, L, 1 if reverse else 0,
+                                                 _ptr(out), _ptr(workspace), workspace.numel(),
+                                                 _stream(stream)))
     return out
 
 

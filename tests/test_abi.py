@@ -44,7 +44,7 @@ def test_status_strings_and_version(lib):
     lib.dlr_status_string.restype = ctypes.c_char_p
     assert lib.dlr_status_string(0) == b"DLR_OK"
     assert lib.dlr_status_string(4) == b"DLR_ERR_TIMEOUT"
-    assert lib.dlr_abi_version() == 2
+    assert lib.dlr_abi_version() == 3
 
 
 def test_host_validation_rejects_bad_arguments(lib):
@@ -84,6 +84,15 @@ def test_host_validation_rejects_bad_arguments(lib):
     # reached here: N above 128 keeps the call on the host)
     assert lib.dlr_scan_ex(fake, fake, fake, fake, None, None, None, 0, 1, 1, 129, 64,
                            ctypes.c_void_p(0x9000), 1, None, 0, None) == 2
+    lib.dlr_scan_prepare.argtypes = [P, P, P, i64, i64, P, sz, P]
+    lib.dlr_scan_apply.argtypes = [P, i64, i64, i64, i64, ctypes.c_int, P, P, sz, P]
+    # tables for N above 64 -> unsupported; missing workspace; unknown direction flag
+    assert lib.dlr_scan_prepare(fake, fake, fake, 4, 65, fake, 1 << 30, None) == 2
+    assert lib.dlr_scan_prepare(fake, fake, fake, 4, 64, None, 0, None) == 5
+    assert lib.dlr_scan_apply(fake, 1, 1, 4, 64, 2, ctypes.c_void_p(0x9000), fake, 1 << 20,
+                              None) == 1
+    assert lib.dlr_scan_apply(fake, 1, 1, 4, 64, 0, ctypes.c_void_p(0x9000), None, 0,
+                              None) == 5
     lib.dlr_conv.argtypes = [P, P, P, ctypes.c_int, i64, i64, i64, P, P, ctypes.c_size_t, P]
     # missing workspace
     assert lib.dlr_conv(fake, fake, None, 0, 1, 1, 16, ctypes.c_void_p(0x9000), None, 0,
