@@ -20,7 +20,7 @@ size_t scan_tc_workspace_bytes(int64_t H);
 cudaError_t launch_scan_tc_tables(const float* lr, const float* li, const float* W, int H, int N,
                                   void* ws, cudaStream_t s);
 cudaError_t launch_scan_tc_apply(const float* u, int B, int H, int L, bool reverse, float* y,
-                                 const void* ws, int* status, cudaStream_t s);
+                                 const void* ws, int* status, cudaStream_t s, bool after_tables);
 cudaError_t launch_dlr_scan_tc(const float* u, const float* lr, const float* li, const float* W,
                                const float* lr2, const float* li2, const float* W2, bool bidir,
                                int B, int H, int N, int L, float* y, void* ws, int* status,
@@ -235,7 +235,8 @@ dlr_status dlr_scan_apply(const float* u, int64_t B, int64_t H, int64_t N, int64
   if (ranges_overlap(workspace, need, u, bytes) || ranges_overlap(workspace, need, y, bytes))
     return DLR_ERR_INVALID_ARG;
   return from_cuda(dlr::launch_scan_tc_apply(u, (int)B, (int)H, (int)L, reverse != 0, y,
-                                             workspace, status_word(), (cudaStream_t)stream));
+                                             workspace, status_word(), (cudaStream_t)stream,
+                                             false));
 }
 
 size_t s5_workspace_size(int64_t B, int64_t L, int64_t H, int64_t P, dlr_prec prec) {

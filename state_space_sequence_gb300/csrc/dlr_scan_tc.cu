@@ -190,6 +190,16 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+// Programmatic dependent launch: the table kernel lets the scan kernel launch early; the scan
+// kernel waits for the table kernel's completion (and memory) before it reads the tables. Both
+// are no-ops when the launch is not programmatic.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_wait_prerequisites() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
@@ -398,6 +408,7 @@ __global__ void __launch_bounds__(kTbThreads, 2)
   const int N = a.N;
   const int n = tid & 63, q = tid >> 6;
   const bool on = n < N;
+  grid_launch_dependents();
   if (tid == 0) SCAN_TRACE(3900);
   const lam_param p = on ? make_lam_param(a.log_re[(size_t)h * N + n], a.log_im[(size_t)h * N + n])
                          : lam_param{0.f, 0.f, 0.f};
@@ -697,6 +708,7 @@ __device__ __forceinline__ void producer_role(const TcScanArgs& a, const CUtenso
     issue_u_tma<kRev>(a, map, sm, u0, segs, 0);
     if (ntiles > 1) issue_u_tma<kRev>(a, map, sm, u0, segs, 1);
   }
+  grid_wait_prerequisites();  // the tables are written
   int h = channel(0);
   copy_tk(h);
   copy_g(h);
@@ -1180,6 +1192,8 @@ __global__ void __maxnreg__(128)
   const int segs = (a.R > 0) ? 1 : (a.C + kCols - 1) / kCols;
   const int ntiles = (u1 - u0) * segs;
 
+  // everything below the producer's first u copies reads the tables or data derived from them
+  if (warp != 13) grid_wait_prerequisites();
   if (warp < 4) {
     ChainConst q{0.f, 0.f, 0.f, 0.f};
     float sig_g = 1.f;
@@ -1254,14 +1268,26 @@ bool make_u_map(CUtensorMap* m, const float* u, int B, int H, int L, int bc) {
 
 template <bool kRev>
 cudaError_t launch_main(const TcScanArgs& a, const CUtensorMap& umap, const CUtensorMap& ymap,
-                        cudaStream_t s) {
+                        bool after_tables, cudaStream_t s) {
   cudaError_t e = max_smem_once<dlr_scan_tc_kernel<kRev>>(kSmemBytes);
   if (e != cudaSuccess) return e;
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorUnknown;
-  const int grid = std::min(a.units, sms);
-  dlr_scan_tc_kernel<kRev><<<grid, kThreads, kSmemBytes, s>>>(a, umap, ymap);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)std::min(a.units, sms));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  // Right after this library's table kernel (which writes only the tables and started after all
+  // earlier work, so u is final) the scan kernel is launched as its programmatic dependent: its
+  // prologue and first u copies overlap the table kernel's tail, and it waits for the tables
+  // in the kernel. After anything else it is launched normally.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_tables ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, dlr_scan_tc_kernel<kRev>, a, umap, ymap);
 }
 
 }  // namespace
@@ -1286,7 +1312,8 @@ cudaError_t launch_scan_tc_tables(const float* lr, const float* li, const float*
 // The layer on u [B, H, L] with the tables in the workspace: y = DLR(u), or (reverse) y +=
 // rev(DLR(rev(u))).
 cudaError_t launch_scan_tc_apply(const float* u, int B, int H, int L, bool reverse, float* y,
-                                 const void* ws, int* status, cudaStream_t s) {
+                                 const void* ws, int* status, cudaStream_t s,
+                                 bool after_tables) {
   TcScanArgs a{};
   a.u = u;
   a.y = y;
@@ -1315,7 +1342,8 @@ cudaError_t launch_scan_tc_apply(const float* u, int B, int H, int L, bool rever
   a.tma = tma_shape && make_u_map(&umap, u, B, H, L, a.bc) && make_u_map(&ymap, y, B, H, L, 32)
               ? 1
               : 0;
-  return reverse ? launch_main<true>(a, umap, ymap, s) : launch_main<false>(a, umap, ymap, s);
+  return reverse ? launch_main<true>(a, umap, ymap, after_tables, s)
+                 : launch_main<false>(a, umap, ymap, after_tables, s);
 }
 
 // N <= 64 complex states; u, y [B, H, L]; bidirectional adds the reversed pass (run after the
@@ -1325,10 +1353,10 @@ cudaError_t launch_dlr_scan_tc(const float* u, const float* lr, const float* li,
                                int B, int H, int N, int L, float* y, void* ws, int* status,
                                cudaStream_t s) {
   cudaError_t e = launch_scan_tc_tables(lr, li, W, H, N, ws, s);
-  if (e == cudaSuccess) e = launch_scan_tc_apply(u, B, H, L, false, y, ws, status, s);
+  if (e == cudaSuccess) e = launch_scan_tc_apply(u, B, H, L, false, y, ws, status, s, true);
   if (e != cudaSuccess || !bidir) return e;
   e = launch_scan_tc_tables(lr2, li2, W2, H, N, ws, s);
-  if (e == cudaSuccess) e = launch_scan_tc_apply(u, B, H, L, true, y, ws, status, s);
+  if (e == cudaSuccess) e = launch_scan_tc_apply(u, B, H, L, true, y, ws, status, s, true);
   return e;
 }
 

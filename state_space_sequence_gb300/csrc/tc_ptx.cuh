@@ -279,6 +279,31 @@ __device__ __forceinline__ void tmem_ld8x2(uint32_t taddr_a, uint32_t taddr_b, f
   }
 }
 
+// Two 8-column loads issued without waiting: the destination registers may be read only after
+// tmem_wait_ld8x2 on the same arrays, which names them as operands so that the compiler cannot
+// move their uses above the wait.
+__device__ __forceinline__ void tmem_ld8x2_issue(uint32_t taddr_a, uint32_t taddr_b,
+                                                 uint32_t (&r)[8], uint32_t (&s)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr_a)
+               : "memory");
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(s[0]), "=r"(s[1]), "=r"(s[2]), "=r"(s[3]), "=r"(s[4]), "=r"(s[5]),
+                 "=r"(s[6]), "=r"(s[7])
+               : "r"(taddr_b)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld8x2(uint32_t (&r)[8], uint32_t (&s)[8]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(s[0]), "+r"(s[1]), "+r"(s[2]), "+r"(s[3]),
+                 "+r"(s[4]), "+r"(s[5]), "+r"(s[6]), "+r"(s[7])
+               :
+               : "memory");
+}
+
 // Stores 32 consecutive 32-bit columns of the warp's 32 TMEM lanes (layout as tmem_ld32).
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
