@@ -84,9 +84,19 @@ __device__ long long* g_scan_trace;
       g_scan_trace[(slot)] = (long long)t_;                                     \
     }                                                                           \
   } while (0)
+// every CTA (its start and end times)
+#define SCAN_TRACE_ALL(slot)                                                    \
+  do {                                                                          \
+    unsigned long long t_;                                                      \
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                      \
+    g_scan_trace[(slot)] = (long long)t_;                                       \
+  } while (0)
 #else
 #define SCAN_TRACE(slot) \
   do {                   \
+  } while (0)
+#define SCAN_TRACE_ALL(slot) \
+  do {                       \
   } while (0)
 #endif
 
@@ -725,10 +735,14 @@ __device__ __forceinline__ void producer_role(const TcScanArgs& a, const CUtenso
         if (tk_next) copy_tk(channel(j + 1));
       }
     }
-    // GEMM2 of tile k done: the G operand of tile k + 1
-    if (k >= 0 && k + 1 < ntiles && channel(k + 1) != channel(k)) {
+    // GEMM2 of tile k done: the G operand of tile k + 1 at a new channel. G2 is one barrier
+    // whose parity test cannot tell phase k from phase k - 2, so every completion is waited
+    // for in order (free: GEMM2 of tile k completes before GEMM1 of tile k + 2, the next
+    // completion this thread waits for); this also keeps every skipped GEMM1 wait above at
+    // most one phase ahead.
+    if (k >= 0 && k + 1 < ntiles) {
       if (!wait_phase(&bars[kBarG2], k & 1, abort)) return;
-      copy_g(channel(k + 1));
+      if (channel(k + 1) != channel(k)) copy_g(channel(k + 1));
     }
   }
 }
@@ -1161,6 +1175,7 @@ __global__ void __maxnreg__(128)
 
   const int tid = threadIdx.x, warp = tid >> 5;
   if (tid == 0) SCAN_TRACE(3999);
+  if (tid == 0 && blockIdx.x < 192) SCAN_TRACE_ALL(3600 + blockIdx.x);
   if (tid == 0) {
     tc::mbar_init(&bars[kBarTabTk], 1);
     tc::mbar_init(&bars[kBarTabG], 1);
@@ -1232,6 +1247,7 @@ __global__ void __maxnreg__(128)
   tc::fence_before_sync();
   __syncthreads();
   if (tid == 0) SCAN_TRACE(3997);
+  if (tid == 0 && blockIdx.x < 192) SCAN_TRACE_ALL(3400 + blockIdx.x);
   if (*abort) report_status(a.status, DLR_ERR_TIMEOUT);
   if (warp == 0) tc::tmem_dealloc(tmem, kTmemCols);
 }

@@ -155,6 +155,21 @@ def test_tensor_scan_input_scaling_extremes():
     check_status()
 
 
+@pytest.mark.parametrize("B,H,N,L", [(8, 160, 16, 4096), (6, 300, 8, 2048)])
+def test_tensor_scan_channel_changes_inside_a_cta(B, H, N, L):
+    """More tiles than SMs: each persistent CTA walks several tiles and crosses channels, so
+    the per-channel operands (Q, the Toeplitz block, G) are replaced between tiles while
+    earlier tiles of the old channel may still be in flight."""
+    w = inputs.make_dlr(B, H, N, L, seed=B + H + N, unit_channels=1)
+    y = host(dlr.dlr_scan(dev(w.u), params_dev(w.fwd), algo="tensor"))
+    ref = oracle.dlr_layer(w.u, params_np(w.fwd))
+    assert oracle.rel_l2(y, ref) <= TOL
+    # row by row as well: a wrong tile is a few rows among many
+    err = np.linalg.norm(y - ref, axis=2) / np.maximum(np.linalg.norm(ref, axis=2), 1e-30)
+    assert err.max() <= 1e-4, np.argwhere(err > 1e-4)[:8]
+    check_status()
+
+
 @pytest.mark.parametrize("B,H,N,L", [(8, 16, 64, 4096), (3, 2, 40, 3000), (1, 2, 64, 20000)])
 def test_scan_prepare_apply_equals_scan(B, H, N, L):
     """dlr_scan_prepare + dlr_scan_apply (tables once, reused for several batches, both
