@@ -736,10 +736,13 @@ __device__ __forceinline__ void producer_role(const TcScanArgs& a, const CUtenso
       }
     }
     // GEMM2 of tile k done: the G operand of tile k + 1 at a new channel. G2 is one barrier
-    // whose parity test cannot tell phase k from phase k - 2, so every completion is waited
+    // whose parity test cannot tell phase k from phase k +- 2, so every completion is waited
     // for in order (free: GEMM2 of tile k completes before GEMM1 of tile k + 2, the next
-    // completion this thread waits for); this also keeps every skipped GEMM1 wait above at
-    // most one phase ahead.
+    // completion this thread waits for). This thread is then never a phase ahead of G2, and
+    // the skipped GEMM1 waits above stay exact. It can fall a phase behind only where GEMM2
+    // does not depend on it; such a wait just returns at a later completion (everything the
+    // later GEMM2s need from this thread -- u copies -- was issued before it), and at a channel
+    // change it is exact again: GEMM2 of the new channel's first tile needs the copy below.
     if (k >= 0 && k + 1 < ntiles) {
       if (!wait_phase(&bars[kBarG2], k & 1, abort)) return;
       if (channel(k + 1) != channel(k)) copy_g(channel(k + 1));
