@@ -155,14 +155,18 @@ def test_tensor_scan_input_scaling_extremes():
     check_status()
 
 
-@pytest.mark.parametrize("B,H,N,L", [(8, 160, 16, 4096), (6, 300, 8, 2048)])
-def test_tensor_scan_channel_changes_inside_a_cta(B, H, N, L):
+@pytest.mark.parametrize("B,H,N,L,bidir", [(8, 160, 16, 4096, False), (6, 300, 8, 2048, False),
+                                           (4, 200, 8, 4096, True), (2, 100, 8, 16384, False),
+                                           (2, 90, 4, 12288, True)])
+def test_tensor_scan_channel_changes_inside_a_cta(B, H, N, L, bidir):
     """More tiles than SMs: each persistent CTA walks several tiles and crosses channels, so
     the per-channel operands (Q, the Toeplitz block, G) are replaced between tiles while
-    earlier tiles of the old channel may still be in flight."""
-    w = inputs.make_dlr(B, H, N, L, seed=B + H + N, unit_channels=1)
-    y = host(dlr.dlr_scan(dev(w.u), params_dev(w.fwd), algo="tensor"))
-    ref = oracle.dlr_layer(w.u, params_np(w.fwd))
+    earlier tiles of the old channel may still be in flight; both directions (the reversed
+    pass adds through TMA reductions), rows packed in tiles and rows walked tile by tile."""
+    w = inputs.make_dlr(B, H, N, L, seed=B + H + N, bidir=bidir, unit_channels=1)
+    bwd_d = params_dev(w.bwd) if bidir else None
+    y = host(dlr.dlr_scan(dev(w.u), params_dev(w.fwd), bwd_d, algo="tensor"))
+    ref = oracle.dlr_layer(w.u, params_np(w.fwd), params_np(w.bwd) if bidir else None)
     assert oracle.rel_l2(y, ref) <= TOL
     # row by row as well: a wrong tile is a few rows among many
     err = np.linalg.norm(y - ref, axis=2) / np.maximum(np.linalg.norm(ref, axis=2), 1e-30)
