@@ -229,10 +229,6 @@ __device__ __forceinline__ bool named_bar_and(int id, int n, bool v) {
   return r != 0;
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(tc::smem_u32(bar)) : "memory");
-}
-
 // Bounded wait on an mbarrier phase (one thread) that also gives up when another role has
 // aborted. Each try may suspend the thread for a few microseconds.
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -677,7 +673,7 @@ __device__ __forceinline__ bool conv_u_step(const TcScanArgs& a, uint8_t* sm, ui
   }
   tc::fence_before_sync();
   if (tid == 128) SCAN_TRACE(1000 + k * 8 + 2);
-  mbar_arrive(&bars[kBarUFull + par]);
+  tc::mbar_arrive(&bars[kBarUFull + par]);
   named_bar(kConvBar, 128);  // every thread has read the row maxima of this tile
   reinterpret_cast<unsigned*>(sm + kRowMaxU)[tid - 128] = 0u;
   return true;
@@ -778,7 +774,7 @@ __device__ __forceinline__ bool store_tile(const TcScanArgs& a, const CUtensorMa
   tc::tmem_ld32(lane_base + kTY1 + par * 64, *reinterpret_cast<float(*)[32]>(y));
   tc::tmem_ld32(lane_base + kTY1 + par * 64 + 32, *reinterpret_cast<float(*)[32]>(y + 32));
   tc::fence_before_sync();
-  mbar_arrive(&bars[kBarY1Free + par]);
+  tc::mbar_arrive(&bars[kBarY1Free + par]);
   // Y2 of tile k
   ok = warp_wait_phase(&bars[kBarG2], k & 1, abort);
   if (!named_bar_and(kEpiBar, 128, ok)) return false;
@@ -792,7 +788,7 @@ __device__ __forceinline__ bool store_tile(const TcScanArgs& a, const CUtensorMa
     for (int j = 0; j < 16; ++j) y[q4 * 16 + j] = fmaf(y[q4 * 16 + j], ay, y2[j] * by);
   }
   tc::fence_before_sync();
-  mbar_arrive(&bars[kBarY2Free]);
+  tc::mbar_arrive(&bars[kBarY2Free]);
   const TileInfo ti = tile_info(a, u0, segs, k);
   const ColInfo ci = col_info(a, ti, g);
   if (a.tma) {
@@ -1144,7 +1140,7 @@ __device__ __forceinline__ bool scan_tile(const TcScanArgs& a, uint8_t* sm, uint
     const int row = (a.R > 0) ? tid / a.C : 0;
     sBy[tid] = exp2i(xs - kXinShift) * exp2i(kXinShift - 14 - sRowEs[row]) / sig_g;
   }
-  mbar_arrive(&bars[kBarScanStart + par]);
+  tc::mbar_arrive(&bars[kBarScanStart + par]);
 
   const float xscale = exp2i(-xs);
   const bool wait_g2 = k > 0;
@@ -1161,7 +1157,7 @@ __device__ __forceinline__ bool scan_tile(const TcScanArgs& a, uint8_t* sm, uint
   if (tid == 0) SCAN_TRACE(k * 8 + 3);
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
-  mbar_arrive(&bars[kBarXFull]);
+  tc::mbar_arrive(&bars[kBarXFull]);
   return true;
 }
 

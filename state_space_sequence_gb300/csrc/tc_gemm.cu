@@ -1,15 +1,21 @@
 // tc_gemm.cu -- C[M, N] (f32) = A[M, K] * B[N, K]^T (+ D[n] * E[m, n]) on 5th-generation tensor
-// cores: bf16 operands in shared memory (TMA tile loads, 128-byte swizzle), f32 accumulator in
-// tensor memory, tcgen05.mma issued by one thread, tcgen05.ld epilogue.
+// cores: bf16 operands in shared memory (TMA tile loads, 128-byte swizzle), f32 accumulators in
+// tensor memory, tcgen05.mma issued by one thread, tcgen05.ld epilogue with TMA tile stores.
 //
-// One CTA computes one 128 x 256 tile with 4 warps:
-//   warp 0 lane 0  TMA producer: K-blocks of 64 into a 2-stage ring (A 16 KB + B 32 KB),
-//   warp 1 lane 0  MMA issuer: four K=16 MMAs per K-block, then a commit that frees the stage;
-//                  a final commit marks the accumulator complete,
-//   warp 2         allocates / frees 256 TMEM columns,
-//   warps 0-3      epilogue: warp w reads TMEM lanes 32w..32w+31 (rows of the tile).
-// Two CTAs fit on an SM (96 KB shared memory, 256 TMEM columns each), so one CTA's epilogue
-// overlaps the other's main loop.
+// Persistent: one CTA per SM walks the 128 x 256 output tiles t = blockIdx.x, + gridDim.x, ...
+// with the N tile varying fastest (the CTAs working on the N tiles of one M tile at the same
+// time share its A rows through L2). Eight warps:
+//   warp 0 lane 0  TMA producer: K-blocks of 64 into a 3-stage ring (A 16 KB + B 32 KB), running
+//                  ahead across tiles,
+//   warp 1 lane 0  MMA issuer: four K=16 MMAs per K-block, a commit that frees the stage, and
+//                  per tile a commit that hands one of two TMEM accumulators to the epilogue,
+//   warp 2         allocates / frees the 512 TMEM columns (two 256-column accumulators),
+//   warps 4-7      epilogue: warp 4+q owns TMEM lanes 32q..32q+31 (rows of the tile). Per slice
+//                  of 32 columns: tcgen05.ld, + D (.) E with the E box brought in by TMA, into a
+//                  4 KB staging box (128-byte swizzle), out by one TMA store per warp. Three
+//                  boxes per warp rotate so the E load of the next slice and the stores of the
+//                  last two overlap the current one.
+// While the epilogue drains one accumulator the MMAs of the next tile fill the other.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -23,42 +29,59 @@
 namespace dlr {
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 2;
+constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 3;
+constexpr int kSlice = 32, kSlices = kBN / kSlice, kBoxes = 3;
 constexpr uint32_t kABytes = kBM * kBK * 2, kBBytes = kBN * kBK * 2;
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr size_t kSmemBytes = 1024 + kStages * kStageBytes + 256;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kBoxBytes = 32 * kSlice * 4;  // 32 rows x 32 f32 columns
+constexpr uint32_t kEpiOff = kStages * kStageBytes;
+constexpr uint32_t kBarOff = kEpiOff + 4 * kBoxes * kBoxBytes;
+constexpr size_t kSmemBytes = 1024 + kBarOff + 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kThreads = 256;
 
 struct GemmArgs {
   int M, N, K;
-  float* C;
-  const float* D;  // [N] or null
-  const float* E;  // [M, N] or null
+  const float* D;  // [N] or null (then E is not read)
   int* status;
 };
 
-__global__ void __launch_bounds__(128, 1)
+// Bounded wait by a whole warp with one verdict for all its lanes.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity)) != 0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_bf16(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+             const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmE,
              GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kStages * kStageBytes);
-  uint64_t* full = bars;                 // [kStages]
-  uint64_t* empty = bars + kStages;      // [kStages]
-  uint64_t* acc_full = bars + 2 * kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 1);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kBarOff);
+  uint64_t* full = bars;                       // [kStages]  operands landed
+  uint64_t* empty = bars + kStages;            // [kStages]  operands consumed by the MMAs
+  uint64_t* acc_full = bars + 2 * kStages;     // [2]        accumulator complete
+  uint64_t* acc_empty = acc_full + 2;          // [2]        accumulator read out (4 arrivals)
+  uint64_t* e_full = acc_empty + 2;            // [4][kBoxes] E box landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(e_full + 4 * kBoxes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kBN;
+  const int n_tiles = (g.N + kBN - 1) / kBN;
+  const int tiles = n_tiles * ((g.M + kBM - 1) / kBM);
   const int nk = (g.K + kBK - 1) / kBK;
+  const bool with_e = g.D != nullptr;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
     }
-    tc::mbar_init(acc_full, 1);
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(&acc_full[a], 1);
+      tc::mbar_init(&acc_empty[a], 4);
+    }
+    for (int i = 0; i < 4 * kBoxes; ++i) tc::mbar_init(&e_full[i], 1);
     tc::mbar_fence_init();
   }
   if (warp == 2) {
@@ -72,86 +95,119 @@ tc_gemm_bf16(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
   bool ok = true;
 
   if (warp == 0 && lane == 0) {
-    for (int kb = 0; kb < nk && ok; ++kb) {
-      const int s = kb % kStages;
-      const uint32_t round = kb / kStages;
-      if (kb >= kStages) ok = tc::mbar_wait(&empty[s], (round - 1) & 1);
-      if (!ok) break;
-      uint8_t* a = base + s * kStageBytes;
-      uint8_t* b = a + kABytes;
-      tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
-      tc::tma_load_2d(a, &tmA, kb * kBK, m0, &full[s]);
-      tc::tma_load_2d(b, &tmB, kb * kBK, n0, &full[s]);
+    uint32_t it = 0;
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      const int m0 = (t / n_tiles) * kBM, n0 = (t % n_tiles) * kBN;
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int s = it % kStages;
+        if (it >= kStages && !(ok = tc::mbar_wait(&empty[s], ((it / kStages) - 1) & 1))) break;
+        uint8_t* a = base + s * kStageBytes;
+        tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
+        tc::tma_load_2d(a, &tmA, kb * kBK, m0, &full[s]);
+        tc::tma_load_2d(a + kABytes, &tmB, kb * kBK, n0, &full[s]);
+      }
     }
+    // before the CTA may exit, every copy it issued has landed (normally long since consumed)
+    for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j)
+      ok &= tc::mbar_wait(&full[j % kStages], (j / kStages) & 1);
   } else if (warp == 1 && lane == 0) {
     constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
-    for (int kb = 0; kb < nk && ok; ++kb) {
-      const int s = kb % kStages;
-      ok = tc::mbar_wait(&full[s], (kb / kStages) & 1);
-      if (!ok) break;
+    uint32_t it = 0, local = 0;
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++local) {
+      const uint32_t acc = local & 1;
+      if (local >= 2 && !(ok = tc::mbar_wait(&acc_empty[acc], ((local >> 1) - 1) & 1))) break;
       tc::fence_after_sync();
-      const uint8_t* a = base + s * kStageBytes;
-      const uint64_t ad = tc::smem_desc_k_sw128(a);
-      const uint64_t bd = tc::smem_desc_k_sw128(a + kABytes);
+      const uint32_t d = tmem + acc * kBN;
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int s = it % kStages;
+        if (!(ok = tc::mbar_wait(&full[s], (it / kStages) & 1))) break;
+        tc::fence_after_sync();
+        const uint8_t* a = base + s * kStageBytes;
+        const uint64_t ad = tc::smem_desc_k_sw128(a);
+        const uint64_t bd = tc::smem_desc_k_sw128(a + kABytes);
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk)  // advance 16 bf16 = 32 bytes = 2 descriptor units
-        tc::mma_kind_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
-      tc::mma_commit(&empty[s]);
+        for (int kk = 0; kk < kBK / 16; ++kk)  // advance 16 bf16 = 32 bytes = 2 descriptor units
+          tc::mma_kind_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+        tc::mma_commit(&empty[s]);
+      }
+      tc::mma_commit(&acc_full[acc]);
     }
-    tc::mma_commit(acc_full);
-  }
-  __syncwarp();
-
-  // ---- epilogue: all four warps. Each 32-column slice of the accumulator goes TMEM ->
-  // registers (thread = row) -> shared memory (the drained stages) -> row-coalesced float4
-  // stores, with D (.) E added on the way out. ----
-  const bool acc_ok = tc::mbar_wait(acc_full, 0);
-  tc::fence_after_sync();
-  float* tile = reinterpret_cast<float*>(base);  // [128][33]
-  const bool vec = (g.N & 3) == 0;
-#pragma unroll 1
-  for (int c = 0; c < kBN / 32; ++c) {
-    const int nc = n0 + c * 32;
-    if (nc >= g.N) break;  // block-uniform
-    float v[32];
-    tc::tmem_ld32(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c * 32), v);
-    const int r_own = warp * 32 + lane;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) tile[r_own * 33 + j] = v[j];
-    __syncthreads();
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      const int idx = it * 128 + threadIdx.x;  // 128 rows x 8 float4 per slice
-      const int r = idx >> 3, c4 = (idx & 7) * 4;
-      const int row = m0 + r, col = nc + c4;
-      if (row < g.M && acc_ok) {
-        float o[4] = {tile[r * 33 + c4], tile[r * 33 + c4 + 1], tile[r * 33 + c4 + 2],
-                      tile[r * 33 + c4 + 3]};
-        if (vec && col + 3 < g.N) {
-          if (g.E) {
-            const float4 e = __ldg(reinterpret_cast<const float4*>(g.E + (size_t)row * g.N + col));
-            const float4 d = __ldg(reinterpret_cast<const float4*>(g.D + col));
-            o[0] = fmaf(d.x, e.x, o[0]);
-            o[1] = fmaf(d.y, e.y, o[1]);
-            o[2] = fmaf(d.z, e.z, o[2]);
-            o[3] = fmaf(d.w, e.w, o[3]);
+  } else if (warp >= 4) {
+    const int q = warp - 4;
+    uint8_t* boxes = base + kEpiOff + q * kBoxes * kBoxBytes;
+    uint64_t* ebar = e_full + q * kBoxes;
+    const uint32_t sw = uint32_t(lane & 7);
+    // the slices this warp walks: (tile, column block), tiles in the CTA's order
+    int t = blockIdx.x, c = 0;
+    auto n_slices = [&](int tt) { return min(kSlices, (g.N - (tt % n_tiles) * kBN + kSlice - 1) / kSlice); };
+    auto issue_e = [&](int tt, int cc, uint32_t sc) {
+      const int j = sc % kBoxes;
+      tc::mbar_arrive_expect_tx(&ebar[j], kBoxBytes);
+      tc::tma_load_2d(boxes + j * kBoxBytes, &tmE, (tt % n_tiles) * kBN + cc * kSlice,
+                      (tt / n_tiles) * kBM + q * 32, &ebar[j]);
+    };
+    uint32_t sc = 0, local = 0, e_issued = 0;
+    if (with_e && lane == 0 && t < tiles) { issue_e(t, 0, 0); e_issued = 1; }
+    for (; t < tiles && ok; t += gridDim.x, ++local) {
+      const uint32_t acc = local & 1;
+      if (!(ok = warp_wait(&acc_full[acc], (local >> 1) & 1))) break;
+      tc::fence_after_sync();
+      const int m0 = (t / n_tiles) * kBM, n0 = (t % n_tiles) * kBN;
+      const int ns = n_slices(t);
+      for (c = 0; c < ns; ++c, ++sc) {
+        const int j = sc % kBoxes;
+        uint8_t* box = boxes + j * kBoxBytes;
+        if (lane == 0) {
+          // the box of slice sc + 1 held slice sc - 2, whose store must have read it
+          tc::bulk_wait_group_read<1>();
+          if (with_e) {
+            int tn = t, cn = c + 1;
+            if (cn == ns) { tn = t + gridDim.x; cn = 0; }
+            if (tn < tiles) { issue_e(tn, cn, sc + 1); ++e_issued; }
           }
-          *reinterpret_cast<float4*>(g.C + (size_t)row * g.N + col) =
-              make_float4(o[0], o[1], o[2], o[3]);
+        }
+        __syncwarp();
+        float v[32];
+        tc::tmem_ld32(tmem + acc * kBN + (uint32_t(q * 32) << 16) + uint32_t(c * kSlice), v);
+        if (c == ns - 1) {  // accumulator read out: the MMAs of tile local + 2 may start
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&acc_empty[acc]);
+        }
+        if (with_e) {
+          if (!(ok = warp_wait(&ebar[j], (sc / kBoxes) & 1))) break;
+          const int nc = n0 + c * kSlice;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            float4* p = reinterpret_cast<float4*>(box + lane * 128 + ((uint32_t(k) ^ sw) << 4));
+            const float4 e = *p;
+            float4 dk = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (nc + 4 * k < g.N) dk = __ldg(reinterpret_cast<const float4*>(g.D + nc + 4 * k));
+            *p = make_float4(fmaf(dk.x, e.x, v[4 * k]), fmaf(dk.y, e.y, v[4 * k + 1]),
+                             fmaf(dk.z, e.z, v[4 * k + 2]), fmaf(dk.w, e.w, v[4 * k + 3]));
+          }
         } else {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (col + q < g.N) {
-              float val = o[q];
-              if (g.E) val = fmaf(g.D[col + q], g.E[(size_t)row * g.N + col + q], val);
-              g.C[(size_t)row * g.N + col + q] = val;
-            }
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<float4*>(box + lane * 128 + ((uint32_t(k) ^ sw) << 4)) =
+                make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tc::tma_store_2d(&tmC, box, n0 + c * kSlice, m0 + q * 32);
+          tc::bulk_commit_group();
         }
       }
     }
-    __syncthreads();
+    if (lane == 0) {
+      // E boxes issued but never consumed (only after a failed wait) land before the CTA exits
+      for (uint32_t s2 = sc; s2 < e_issued; ++s2)
+        ok &= tc::mbar_wait(&ebar[s2 % kBoxes], (s2 / kBoxes) & 1);
+      tc::bulk_wait_group0();
+    }
   }
-  if (!ok || !acc_ok) report_status(g.status, DLR_ERR_TIMEOUT);
+  if (!ok) report_status(g.status, DLR_ERR_TIMEOUT);
   tc::fence_before_sync();
   __syncthreads();
   if (warp == 2) tc::tmem_dealloc(tmem, kTmemCols);
@@ -193,19 +249,34 @@ __global__ void to_bf16_t(const float* __restrict__ x, __nv_bfloat16* __restrict
   }
 }
 
-// Row-major bf16 [rows, cols] with boxes of box_rows x 64 columns, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// Row-major [rows, cols] tensor of 2-byte (bf16) or 4-byte (f32) elements, boxes of
+// box_rows x box_cols elements with a 128-byte swizzle (box_cols * element size = 128).
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+              bool f32) {
   auto fn = tc::tensor_map_encoder();
   if (!fn) return false;
-  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (cols * 2) % 16) return false;
+  const uint64_t esz = f32 ? 4 : 2;
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (cols * esz) % 16) return false;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {kBK, box_rows};
+  cuuint64_t strides[1] = {cols * esz};
+  cuuint32_t box[2] = {uint32_t(128 / esz), box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
+  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  static int n = 0;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+      n = 1;
+  });
+  return n;
 }
 
 }  // namespace
@@ -229,17 +300,23 @@ cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t
   return cudaGetLastError();
 }
 
-// A: bf16 [M, K] row-major; B: bf16 [N, K] row-major; C: f32 [M, N].
+// A: bf16 [M, K] row-major; B: bf16 [N, K] row-major; C: f32 [M, N]; D: f32 [N] or null;
+// E: f32 [M, N] (read only when D is given).
 cudaError_t launch_tc_gemm(const void* A, const void* B, float* C, int M, int N, int K,
                            const float* D, const float* E, int* status, cudaStream_t s) {
-  CUtensorMap ma, mb;
-  if (!make_map(&ma, A, (uint64_t)M, (uint64_t)K, kBM)) return cudaErrorInvalidValue;
-  if (!make_map(&mb, B, (uint64_t)N, (uint64_t)K, kBN)) return cudaErrorInvalidValue;
+  if (M < 1 || N < 1 || K < 1) return cudaErrorInvalidValue;
+  CUtensorMap ma, mb, mc, me;
+  if (!make_map(&ma, A, (uint64_t)M, (uint64_t)K, kBM, false)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, B, (uint64_t)N, (uint64_t)K, kBN, false)) return cudaErrorInvalidValue;
+  if (!make_map(&mc, C, (uint64_t)M, (uint64_t)N, 32, true)) return cudaErrorInvalidValue;
+  if (D && !make_map(&me, E, (uint64_t)M, (uint64_t)N, 32, true)) return cudaErrorInvalidValue;
+  if (!D) me = mc;  // not read
   cudaError_t e = max_smem_once<tc_gemm_bf16>(kSmemBytes);
   if (e != cudaSuccess) return e;
-  GemmArgs g{M, N, K, C, D, E, status};
-  dim3 grid((M + kBM - 1) / kBM, (N + kBN - 1) / kBN);
-  tc_gemm_bf16<<<grid, 128, kSmemBytes, s>>>(ma, mb, g);
+  GemmArgs g{M, N, K, D, status};
+  const long long tiles = (long long)((N + kBN - 1) / kBN) * ((M + kBM - 1) / kBM);
+  const int grid = (int)std::min<long long>(tiles, sm_count());
+  tc_gemm_bf16<<<grid, kThreads, kSmemBytes, s>>>(ma, mb, mc, me, g);
   return cudaGetLastError();
 }
 

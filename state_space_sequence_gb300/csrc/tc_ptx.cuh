@@ -40,6 +40,9 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
@@ -115,6 +118,18 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// 2D tile store from shared memory to global (x innermost; x * element size a multiple of 16
+// bytes; both coordinates non-negative; the part of the box outside the tensor is not written),
+// tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x,
+                                             int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y)
+      : "memory");
+}
+
 // 3D tile store from shared memory to global (x innermost; x * element size a multiple of 16
 // bytes; every coordinate non-negative), tracked by the issuing thread's bulk group.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x,
@@ -148,6 +163,12 @@ __device__ __forceinline__ void bulk_commit_group() {
 // Waits until the issuing thread's committed bulk stores have read their shared-memory source.
 __device__ __forceinline__ void bulk_wait_group_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until at most N of the issuing thread's committed bulk groups are still reading their
+// shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 // Waits until the issuing thread's committed bulk stores are complete.
 __device__ __forceinline__ void bulk_wait_group0() {
