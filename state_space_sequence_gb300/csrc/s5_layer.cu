@@ -10,17 +10,20 @@
 //          operand [Re C~^T ; -Im C~^T].
 //   gemm   V[B*L, 2P] = u[B*L, H] * Bbar^T (float32 FFMA, register tiled)
 //   chunk  S_c = sum_t Lbar^{T-1-t} V_t (end state of chunk c from a zero start)
-//   carry  X_c = Lbar^T X_{c-1} + S_c, sequential over chunks in two-float arithmetic;
-//          stores the state entering each chunk
+//   carry  X_c = Lbar^T X_{c-1} + S_c in two-float arithmetic, one warp per (b, p) scanning
+//          groups of chunks; stores the state entering each chunk
 //   apply  x_t = Lbar^{t+1} X_in + l_t, l_t = Lbar l_{t-1} + V_t, written over V in place
 //   gemm   y = x * [Re C~^T ; -Im C~^T] + D (.) u
+// The bf16 tier runs the two projections on the tensor cores (tc_gemm.cu) with bf16 operands:
+// u and the two parameter operands are converted, and apply writes x as bf16.
+#include <cuda_bf16.h>
+
 #include "dlr_common.cuh"
 
 namespace dlr {
 namespace {
 
 constexpr int kT = 64;   // steps per chunk
-constexpr int kPB = 32;  // complex states per chunk-kernel CTA
 
 struct S5Work {
   void* bbar_t16;  // bf16 [2P][H]   (bf16 tier only)
@@ -29,7 +32,7 @@ struct S5Work {
   void* x16;       // bf16 [B*L][2P]
   float* bbar;     // [H][2P]
   float* cmat;     // [2P][H]
-  float2* lbar_pw; // [P][T+1]  Lbar^t
+  float2* lbar_pw; // [T+1][P]  Lbar^t (state fastest, so a warp's loads of one power coalesce)
   float4* lbar_T;  // [P] (re.hi, re.lo, im.hi, im.lo) of Lbar^T
   float2* S;       // [B][NC][P]
   float2* Xin;     // [B][NC][P]
@@ -60,7 +63,7 @@ __global__ void s5_prep(const float* __restrict__ lambda, const float* __restric
   }
   for (int t = threadIdx.x; t <= kT; t += blockDim.x) {
     const double m = exp(zr * t), ph = zi * t;
-    w.lbar_pw[(size_t)p * (kT + 1) + t] = make_float2((float)(m * cos(ph)), (float)(m * sin(ph)));
+    w.lbar_pw[(size_t)t * P + p] = make_float2((float)(m * cos(ph)), (float)(m * sin(ph)));
     if (t == kT) {
       double re = m * cos(ph), im = m * sin(ph);
       float rh = (float)re, ih = (float)im;
@@ -121,70 +124,99 @@ gemm_f32(const float* __restrict__ A, const float* __restrict__ Bm, float* __res
   }
 }
 
-// grid (P / kPB, NC, B): chunk end states from a zero start.
+// grid (NC, B), one thread per state p: the chunk end state from a zero start,
+// S_c = sum_t Lbar^{T-1-t} V_t with the directly computed powers. The V loads of a thread are
+// issued kBatch at a time ahead of their use, so each thread keeps several in flight.
+constexpr int kBatch = 16;
 __global__ void __launch_bounds__(256)
 s5_chunk_state(S5Work w, int L, int P, int NC) {
-  __shared__ float2 sV[kT][kPB + 1];
-  __shared__ float2 sPart[8][kPB];
-  const int pb = blockIdx.x * kPB, c = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x;
+  const int c = blockIdx.x, b = blockIdx.y;
   const int t0 = c * kT;
   const int valid = min(kT, L - t0);
-  for (int e = tid; e < kT * kPB; e += 256) {
-    int t = e / kPB, pl = e % kPB;
-    float2 v = make_float2(0.f, 0.f);
-    if (t < valid)
-      v = *reinterpret_cast<const float2*>(w.xv + ((size_t)b * L + t0 + t) * 2 * P + 2 * (pb + pl));
-    sV[t][pl] = v;
-  }
-  __syncthreads();
-  const int pl = tid & 31, g = tid >> 5;  // 8 groups of 8 steps
-  const float2* pw = w.lbar_pw + (size_t)(pb + pl) * (kT + 1);
-  cf acc = {0.f, 0.f};
-  for (int t = 8 * g; t < 8 * g + 8; ++t) {
-    float2 a = pw[kT - 1 - t], v = sV[t][pl];
-    acc = cfma({a.x, a.y}, {v.x, v.y}, acc);
-  }
-  sPart[g][pl] = make_float2(acc.re, acc.im);
-  __syncthreads();
-  if (tid < kPB) {
-    float sr = 0.f, si = 0.f;
-    for (int q = 0; q < 8; ++q) {
-      sr += sPart[q][tid].x;
-      si += sPart[q][tid].y;
+  for (int p = threadIdx.x; p < P; p += blockDim.x) {
+    const float2* col = reinterpret_cast<const float2*>(w.xv) + ((size_t)b * L + t0) * P + p;
+    cf acc = {0.f, 0.f};
+    for (int tb = 0; tb < valid; tb += kBatch) {
+      float2 v[kBatch], a[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const bool in = tb + j < valid;
+        v[j] = in ? col[(size_t)(tb + j) * P] : make_float2(0.f, 0.f);
+        a[j] = in ? w.lbar_pw[(size_t)(kT - 1 - tb - j) * P + p] : make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) acc = cfma({a[j].x, a[j].y}, {v[j].x, v[j].y}, acc);
     }
-    w.S[((size_t)b * NC + c) * P + pb + tid] = make_float2(sr, si);
+    w.S[((size_t)b * NC + c) * P + p] = make_float2(acc.re, acc.im);
   }
 }
 
-// one thread per (b, p): the state entering each chunk, chained in two-float arithmetic.
-// The chunk end states do not depend on the chain, so they are fetched eight at a time.
-__global__ void s5_carry(S5Work w, int B, int P, int NC) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= B * P) return;
-  const int b = i / P, p = i % P;
+__device__ __forceinline__ cff cff_mul(cff a, cff b) {
+  return cff_fma(a, b, {{0.f, 0.f}, {0.f, 0.f}});
+}
+__device__ __forceinline__ cff cff_shfl_up(cff a, int d) {
+  return {{__shfl_up_sync(0xffffffffu, a.re.hi, d), __shfl_up_sync(0xffffffffu, a.re.lo, d)},
+          {__shfl_up_sync(0xffffffffu, a.im.hi, d), __shfl_up_sync(0xffffffffu, a.im.lo, d)}};
+}
+
+// One warp per (b, p): the state entering each chunk, X_0 = 0, X_{c+1} = m X_c + S_c with
+// m = Lbar^T, in two-float arithmetic. Lane i takes G = ceil(NC / 32) consecutive chunks:
+//   1. its group's end state from a zero start,
+//   2. an inclusive Kogge-Stone scan over the lanes of the maps x -> m^G x + A_i (the step of
+//      offset d multiplies by m^{G d}), so lane i - 1 holds the state entering group i,
+//   3. the group's chain again from that state, storing the state entering each chunk.
+// Only the last non-empty group may be short; no lane before it reads its value.
+__global__ void __launch_bounds__(256)
+s5_carry(S5Work w, int B, int P, int NC) {
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (gw >= B * P) return;  // whole warps
+  const int b = gw / P, p = gw % P;
   const float4 lt = w.lbar_T[p];
   const cff m = {{lt.x, lt.y}, {lt.z, lt.w}};
-  cff x = {{0.f, 0.f}, {0.f, 0.f}};
+  const cff zero = {{0.f, 0.f}, {0.f, 0.f}};
+  const int G = (NC + 31) / 32;
+  const int c0 = min(NC, lane * G), c1 = min(NC, c0 + G);
   const size_t base = (size_t)b * NC * P + p;
-  for (int c0 = 0; c0 < NC; c0 += 8) {
-    float2 sv[8];
+  auto chain = [&](cff x, bool store) {
+    for (int cb = c0; cb < c1; cb += 8) {
+      float2 sv[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q)
-      sv[q] = (c0 + q < NC) ? w.S[base + (size_t)(c0 + q) * P] : make_float2(0.f, 0.f);
+      for (int q = 0; q < 8; ++q)
+        sv[q] = (cb + q < c1) ? w.S[base + (size_t)(cb + q) * P] : make_float2(0.f, 0.f);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      if (c0 + q >= NC) break;
-      w.Xin[base + (size_t)(c0 + q) * P] = make_float2(x.re.hi + x.re.lo, x.im.hi + x.im.lo);
-      x = cff_fma(m, x, {{sv[q].x, 0.f}, {sv[q].y, 0.f}});
+      for (int q = 0; q < 8; ++q) {
+        if (cb + q >= c1) break;
+        if (store)
+          w.Xin[base + (size_t)(cb + q) * P] =
+              make_float2(x.re.hi + x.re.lo, x.im.hi + x.im.lo);
+        x = cff_fma(m, x, {{sv[q].x, 0.f}, {sv[q].y, 0.f}});
+      }
     }
+    return x;
+  };
+  cff a = chain(zero, false);
+  // m^G by binary powering, then the scan
+  cff md = {{1.f, 0.f}, {0.f, 0.f}}, sq = m;
+  for (int e = G; e; e >>= 1) {
+    if (e & 1) md = cff_mul(md, sq);
+    if (e > 1) sq = cff_mul(sq, sq);
   }
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const cff prev = cff_shfl_up(a, d);
+    if (lane >= d) a = cff_fma(md, prev, a);
+    md = cff_mul(md, md);
+  }
+  const cff prev = cff_shfl_up(a, 1);
+  chain(lane ? prev : zero, true);
 }
 
 // grid (NC, B), one thread per state p: x_t = Lbar^{t+1} X_in + l_t with the in-chunk part
-// l_t = Lbar l_{t-1} + V_t (l_{-1} = 0) run as a 64-step recurrence, written over V in place.
+// l_t = Lbar l_{t-1} + V_t (l_{-1} = 0) run as a 64-step recurrence, written over V in place
+// (float32 tier) or as the bf16 operand of the output projection (bf16 tier).
 // The carried state enters through the directly computed power Lbar^{t+1}; only in-chunk lags
 // go through the float32 product chain (at most 64 roundings).
+template <bool kBf16Out>
 __global__ void __launch_bounds__(256)
 s5_chunk_apply(S5Work w, int L, int P, int NC) {
   const int c = blockIdx.x, b = blockIdx.y;
@@ -193,17 +225,30 @@ s5_chunk_apply(S5Work w, int L, int P, int NC) {
   for (int p = threadIdx.x; p < P; p += blockDim.x) {
     const float2 xi = w.Xin[((size_t)b * NC + c) * P + p];
     const cf xin = {xi.x, xi.y};
-    const float2* pw = w.lbar_pw + (size_t)p * (kT + 1);
-    const float2 lb = pw[1];
+    const float2 lb = w.lbar_pw[(size_t)P + p];
     const cf lam = {lb.x, lb.y};
     cf l = {0.f, 0.f};
-    float2* row = reinterpret_cast<float2*>(w.xv + ((size_t)b * L + t0) * 2 * P) + p;
-    for (int t = 0; t < valid; ++t) {
-      const float2 v = row[(size_t)t * P];
-      l = cfma(lam, l, {v.x, v.y});
-      const float2 a = pw[t + 1];
-      const cf x = cfma({a.x, a.y}, xin, l);
-      row[(size_t)t * P] = make_float2(x.re, x.im);
+    const size_t row0 = ((size_t)b * L + t0) * P + p;  // in complex elements
+    float2* row = reinterpret_cast<float2*>(w.xv) + row0;
+    __nv_bfloat162* row16 = reinterpret_cast<__nv_bfloat162*>(w.x16) + row0;
+    for (int tb = 0; tb < valid; tb += kBatch) {
+      float2 v[kBatch], a[kBatch];
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        const bool in = tb + j < valid;
+        v[j] = in ? row[(size_t)(tb + j) * P] : make_float2(0.f, 0.f);
+        a[j] = in ? w.lbar_pw[(size_t)(tb + j + 1) * P + p] : make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < kBatch; ++j) {
+        if (tb + j >= valid) break;
+        l = cfma(lam, l, {v[j].x, v[j].y});
+        const cf x = cfma({a[j].x, a[j].y}, xin, l);
+        if (kBf16Out)
+          row16[(size_t)(tb + j) * P] = __floats2bfloat162_rn(x.re, x.im);
+        else
+          row[(size_t)(tb + j) * P] = make_float2(x.re, x.im);
+      }
     }
   }
 }
@@ -260,13 +305,17 @@ cudaError_t launch_to_bf16_t(const float* x, void* y, int R, int C, cudaStream_t
 cudaError_t launch_tc_gemm(const void* A, const void* B, float* C, int M, int N, int K,
                            const float* D, const float* E, int* status, cudaStream_t s);
 
-// The chunked diagonal scan shared by both tiers: V (in w.xv) -> x (in w.xv), in place.
-static cudaError_t s5_scan_xv(const S5Work& w, int B, int L, int P, cudaStream_t s) {
+// The chunked diagonal scan shared by both tiers: V (in w.xv) -> x, in place in w.xv (float32)
+// or into w.x16 (bf16).
+static cudaError_t s5_scan_xv(const S5Work& w, int B, int L, int P, bool bf16, cudaStream_t s) {
   const int NC = (L + kT - 1) / kT;
-  dim3 gc(P / kPB, NC, B);
-  s5_chunk_state<<<gc, 256, 0, s>>>(w, L, P, NC);
-  s5_carry<<<(B * P + 127) / 128, 128, 0, s>>>(w, B, P, NC);
-  s5_chunk_apply<<<dim3(NC, B), 256, 0, s>>>(w, L, P, NC);
+  const int threads = P < 256 ? P : 256;  // P is a multiple of 32
+  s5_chunk_state<<<dim3(NC, B), threads, 0, s>>>(w, L, P, NC);
+  s5_carry<<<(B * P + 7) / 8, 256, 0, s>>>(w, B, P, NC);
+  if (bf16)
+    s5_chunk_apply<true><<<dim3(NC, B), threads, 0, s>>>(w, L, P, NC);
+  else
+    s5_chunk_apply<false><<<dim3(NC, B), threads, 0, s>>>(w, L, P, NC);
   return cudaGetLastError();
 }
 
@@ -281,7 +330,7 @@ cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delt
   if (!bf16) {
     dim3 g1((2 * P + kGN - 1) / kGN, (M + kGM - 1) / kGM);
     gemm_f32<<<g1, 256, 0, s>>>(u, w.bbar, w.xv, M, 2 * P, H, nullptr, nullptr);
-    e = s5_scan_xv(w, B, L, P, s);
+    e = s5_scan_xv(w, B, L, P, false, s);
     if (e != cudaSuccess) return e;
     dim3 g2((H + kGN - 1) / kGN, (M + kGM - 1) / kGM);
     gemm_f32<<<g2, 256, 0, s>>>(w.xv, w.cmat, y, M, H, 2 * P, D, u);
@@ -294,8 +343,7 @@ cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delt
   if ((e = launch_tc_gemm(w.u16, w.bbar_t16, w.xv, M, 2 * P, H, nullptr, nullptr, status, s)) !=
       cudaSuccess)
     return e;
-  if ((e = s5_scan_xv(w, B, L, P, s)) != cudaSuccess) return e;
-  if ((e = launch_to_bf16(w.xv, w.x16, (size_t)M * 2 * P, s)) != cudaSuccess) return e;
+  if ((e = s5_scan_xv(w, B, L, P, true, s)) != cudaSuccess) return e;
   return launch_tc_gemm(w.x16, w.cmat_t16, y, M, H, 2 * P, D, u, status, s);
 }
 
