@@ -14,8 +14,9 @@
 //          groups of chunks; stores the state entering each chunk
 //   apply  x_t = Lbar^{t+1} X_in + l_t, l_t = Lbar l_{t-1} + V_t, written over V in place
 //   gemm   y = x * [Re C~^T ; -Im C~^T] + D (.) u
-// The bf16 tier runs the two projections on the tensor cores (tc_gemm.cu) with bf16 operands:
-// u and the two parameter operands are converted, and apply writes x as bf16.
+// The tensor-core tier runs the two projections on tcgen05 (tc_gemm.cu): the input projection
+// reads the float32 u and Bbar as tf32 operands, the output projection takes x and C~ as bf16
+// operands (apply writes x as bf16).
 #include <cuda_bf16.h>
 
 #include "dlr_common.cuh"
@@ -26,9 +27,8 @@ namespace {
 constexpr int kT = 64;   // steps per chunk
 
 struct S5Work {
-  void* bbar_t16;  // bf16 [2P][H]   (bf16 tier only)
+  float* bbar_t;   // f32 [2P][H]    (tensor-core tier only)
   void* cmat_t16;  // bf16 [H][2P]
-  void* u16;       // bf16 [B*L][H]
   void* x16;       // bf16 [B*L][2P]
   float* bbar;     // [H][2P]
   float* cmat;     // [2P][H]
@@ -57,6 +57,10 @@ __global__ void s5_prep(const float* __restrict__ lambda, const float* __restric
     double br = qr * b.x - qi * b.y, bi = qr * b.y + qi * b.x;
     w.bbar[(size_t)h * 2 * P + 2 * p] = (float)br;
     w.bbar[(size_t)h * 2 * P + 2 * p + 1] = (float)bi;
+    if (w.bbar_t) {
+      w.bbar_t[(size_t)(2 * p) * H + h] = (float)br;
+      w.bbar_t[(size_t)(2 * p + 1) * H + h] = (float)bi;
+    }
     float2 c = Ct[(size_t)h * P + p];
     w.cmat[(size_t)(2 * p) * H + h] = c.x;
     w.cmat[(size_t)(2 * p + 1) * H + h] = -c.y;
@@ -268,11 +272,10 @@ S5Work carve(void* ws, int64_t B, int64_t L, int64_t H, int64_t P, bool bf16, si
   size_t o_S = take(sizeof(float2) * B * NC * P);
   size_t o_X = take(sizeof(float2) * B * NC * P);
   size_t o_xv = take(sizeof(float) * B * L * 2 * P);
-  size_t o_b16 = 0, o_c16 = 0, o_u16 = 0, o_x16 = 0;
+  size_t o_bt = 0, o_c16 = 0, o_x16 = 0;
   if (bf16) {
-    o_b16 = take(2 * 2 * P * H);
+    o_bt = take(sizeof(float) * 2 * P * H);
     o_c16 = take(2 * H * 2 * P);
-    o_u16 = take(2 * B * L * H);
     o_x16 = take(2 * B * L * 2 * P);
   }
   if (total) *total = off;
@@ -285,9 +288,8 @@ S5Work carve(void* ws, int64_t B, int64_t L, int64_t H, int64_t P, bool bf16, si
   w.S = reinterpret_cast<float2*>(base + o_S);
   w.Xin = reinterpret_cast<float2*>(base + o_X);
   w.xv = reinterpret_cast<float*>(base + o_xv);
-  w.bbar_t16 = bf16 ? base + o_b16 : nullptr;
+  w.bbar_t = bf16 ? reinterpret_cast<float*>(base + o_bt) : nullptr;
   w.cmat_t16 = bf16 ? base + o_c16 : nullptr;
-  w.u16 = bf16 ? base + o_u16 : nullptr;
   w.x16 = bf16 ? base + o_x16 : nullptr;
   return w;
 }
@@ -300,10 +302,9 @@ size_t s5_workspace_bytes(int64_t B, int64_t L, int64_t H, int64_t P, bool bf16)
   return total;
 }
 
-cudaError_t launch_to_bf16(const float* x, void* y, size_t n, cudaStream_t s);
 cudaError_t launch_to_bf16_t(const float* x, void* y, int R, int C, cudaStream_t s);
-cudaError_t launch_tc_gemm(const void* A, const void* B, float* C, int M, int N, int K,
-                           const float* D, const float* E, int* status, cudaStream_t s);
+cudaError_t launch_tc_gemm(const void* A, const void* B, bool tf32, float* C, int M, int N,
+                           int K, const float* D, const float* E, int* status, cudaStream_t s);
 
 // The chunked diagonal scan shared by both tiers: V (in w.xv) -> x, in place in w.xv (float32)
 // or into w.x16 (bf16).
@@ -336,15 +337,14 @@ cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delt
     gemm_f32<<<g2, 256, 0, s>>>(w.xv, w.cmat, y, M, H, 2 * P, D, u);
     return cudaGetLastError();
   }
-  // bf16 operands on the tensor cores, f32 accumulation; the scan stays f32
-  if ((e = launch_to_bf16_t(w.bbar, w.bbar_t16, H, 2 * P, s)) != cudaSuccess) return e;
+  // tensor cores with f32 accumulation: tf32 input projection straight from u, bf16 output
+  // projection; the scan stays f32
   if ((e = launch_to_bf16_t(w.cmat, w.cmat_t16, 2 * P, H, s)) != cudaSuccess) return e;
-  if ((e = launch_to_bf16(u, w.u16, (size_t)M * H, s)) != cudaSuccess) return e;
-  if ((e = launch_tc_gemm(w.u16, w.bbar_t16, w.xv, M, 2 * P, H, nullptr, nullptr, status, s)) !=
+  if ((e = launch_tc_gemm(u, w.bbar_t, true, w.xv, M, 2 * P, H, nullptr, nullptr, status, s)) !=
       cudaSuccess)
     return e;
   if ((e = s5_scan_xv(w, B, L, P, true, s)) != cudaSuccess) return e;
-  return launch_tc_gemm(w.x16, w.cmat_t16, y, M, H, 2 * P, D, u, status, s);
+  return launch_tc_gemm(w.x16, w.cmat_t16, false, y, M, H, 2 * P, D, u, status, s);
 }
 
 }  // namespace dlr

@@ -1,20 +1,22 @@
 // tc_gemm.cu -- C[M, N] (f32) = A[M, K] * B[N, K]^T (+ D[n] * E[m, n]) on 5th-generation tensor
-// cores: bf16 operands in shared memory (TMA tile loads, 128-byte swizzle), f32 accumulators in
-// tensor memory, tcgen05.mma issued by one thread, tcgen05.ld epilogue with TMA tile stores.
+// cores: bf16 operands (kind::f16) or float32 operands read as tf32 (kind::tf32) in shared
+// memory (TMA tile loads, 128-byte swizzle), f32 accumulators in tensor memory, tcgen05.mma
+// issued by one thread, tcgen05.ld epilogue with TMA tile stores.
 //
 // Persistent: one CTA per SM walks the 128 x 256 output tiles t = blockIdx.x, + gridDim.x, ...
 // with the N tile varying fastest (the CTAs working on the N tiles of one M tile at the same
 // time share its A rows through L2). Eight warps:
-//   warp 0 lane 0  TMA producer: K-blocks of 64 into a 3-stage ring (A 16 KB + B 32 KB), running
-//                  ahead across tiles,
-//   warp 1 lane 0  MMA issuer: four K=16 MMAs per K-block, a commit that frees the stage, and
+//   warp 0 lane 0  TMA producer: K-blocks of 128 bytes per row (64 bf16 or 32 float32) into a
+//                  ring of 3 or 4 stages (A 16 KB + B 32 KB), running ahead across tiles,
+//   warp 1 lane 0  MMA issuer: four MMAs of 32 bytes of K (K = 16 bf16 or 8 tf32) per K-block,
+//                  a commit that frees the stage, and
 //                  per tile a commit that hands one of two TMEM accumulators to the epilogue,
 //   warp 2         allocates / frees the 512 TMEM columns (two 256-column accumulators),
 //   warps 4-7      epilogue: warp 4+q owns TMEM lanes 32q..32q+31 (rows of the tile). Per slice
 //                  of 32 columns: tcgen05.ld, + D (.) E with the E box brought in by TMA, into a
-//                  4 KB staging box (128-byte swizzle), out by one TMA store per warp. Three
-//                  boxes per warp rotate so the E load of the next slice and the stores of the
-//                  last two overlap the current one.
+//                  4 KB staging box (128-byte swizzle), out by one TMA store per warp. The
+//                  boxes of a warp rotate: the E loads of the next two slices and the stores of
+//                  the last one or two are in flight while the current slice is worked on.
 // While the epilogue drains one accumulator the MMAs of the next tile fill the other.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -29,14 +31,24 @@
 namespace dlr {
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 64, kStages = 3;
-constexpr int kSlice = 32, kSlices = kBN / kSlice, kBoxes = 3;
-constexpr uint32_t kABytes = kBM * kBK * 2, kBBytes = kBN * kBK * 2;
+constexpr int kBM = 128, kBN = 256;
+constexpr int kRowBytes = 128;  // K bytes of one operand row per stage (the swizzle span)
+constexpr int kSlice = 32, kSlices = kBN / kSlice;
+constexpr uint32_t kABytes = kBM * kRowBytes, kBBytes = kBN * kRowBytes;
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kBoxBytes = 32 * kSlice * 4;  // 32 rows x 32 f32 columns
-constexpr uint32_t kEpiOff = kStages * kStageBytes;
-constexpr uint32_t kBarOff = kEpiOff + 4 * kBoxes * kBoxBytes;
-constexpr size_t kSmemBytes = 1024 + kBarOff + 256;
+
+// Shared-memory plan. With E the epilogue keeps four boxes per warp (two E loads ahead) and
+// the ring three stages; without E two boxes suffice and the ring gets a fourth stage.
+template <bool kWithE>
+struct Plan {
+  static constexpr int kStages = kWithE ? 3 : 4;
+  static constexpr int kBoxes = kWithE ? 4 : 2;
+  static constexpr uint32_t kEpiOff = kStages * kStageBytes;
+  static constexpr uint32_t kBarOff = kEpiOff + 4 * kBoxes * kBoxBytes;
+  static constexpr size_t kSmemBytes = 1024 + kBarOff + 256;
+  static_assert(kSmemBytes <= 232448, "shared memory");
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr int kThreads = 256;
 
@@ -51,14 +63,16 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity)) != 0;
 }
 
+template <bool kTf32, bool kWithE>
 __global__ void __launch_bounds__(kThreads, 1)
-tc_gemm_bf16(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmE,
              GemmArgs g) {
+  constexpr int kStages = Plan<kWithE>::kStages, kBoxes = Plan<kWithE>::kBoxes;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kBarOff);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + Plan<kWithE>::kBarOff);
   uint64_t* full = bars;                       // [kStages]  operands landed
   uint64_t* empty = bars + kStages;            // [kStages]  operands consumed by the MMAs
   uint64_t* acc_full = bars + 2 * kStages;     // [2]        accumulator complete
@@ -69,8 +83,9 @@ tc_gemm_bf16(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = (g.N + kBN - 1) / kBN;
   const int tiles = n_tiles * ((g.M + kBM - 1) / kBM);
+  constexpr int kBK = kTf32 ? kRowBytes / 4 : kRowBytes / 2;  // K elements per stage
   const int nk = (g.K + kBK - 1) / kBK;
-  const bool with_e = g.D != nullptr;
+  constexpr bool with_e = kWithE;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -111,7 +126,7 @@ tc_gemm_bf16(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
     for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j)
       ok &= tc::mbar_wait(&full[j % kStages], (j / kStages) & 1);
   } else if (warp == 1 && lane == 0) {
-    constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
+    constexpr uint32_t idesc = kTf32 ? tc::idesc_tf32_f32(kBM, kBN) : tc::idesc_bf16_f32(kBM, kBN);
     uint32_t it = 0, local = 0;
     for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++local) {
       const uint32_t acc = local & 1;
@@ -126,15 +141,19 @@ tc_gemm_bf16(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         const uint64_t ad = tc::smem_desc_k_sw128(a);
         const uint64_t bd = tc::smem_desc_k_sw128(a + kABytes);
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)  // advance 16 bf16 = 32 bytes = 2 descriptor units
-          tc::mma_kind_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+        for (int kk = 0; kk < 4; ++kk) {  // advance 32 bytes of K = 2 descriptor units
+          if (kTf32)
+            tc::mma_kind_tf32(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+          else
+            tc::mma_kind_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
+        }
         tc::mma_commit(&empty[s]);
       }
       tc::mma_commit(&acc_full[acc]);
     }
   } else if (warp >= 4) {
     const int q = warp - 4;
-    uint8_t* boxes = base + kEpiOff + q * kBoxes * kBoxBytes;
+    uint8_t* boxes = base + Plan<kWithE>::kEpiOff + q * kBoxes * kBoxBytes;
     uint64_t* ebar = e_full + q * kBoxes;
     const uint32_t sw = uint32_t(lane & 7);
     // the slices this warp walks: (tile, column block), tiles in the CTA's order
@@ -146,8 +165,14 @@ tc_gemm_bf16(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
       tc::tma_load_2d(boxes + j * kBoxBytes, &tmE, (tt % n_tiles) * kBN + cc * kSlice,
                       (tt / n_tiles) * kBM + q * 32, &ebar[j]);
     };
+    // advances (tt, cc) to the next slice of the walk over the CTA's tiles
+    auto ahead = [&](int& tt, int& cc) {
+      if (++cc == n_slices(tt)) { tt += gridDim.x; cc = 0; }
+    };
     uint32_t sc = 0, local = 0, e_issued = 0;
-    if (with_e && lane == 0 && t < tiles) { issue_e(t, 0, 0); e_issued = 1; }
+    int tp = t, cp = 0;  // the next slice whose E box is not yet requested
+    if (with_e && lane == 0)
+      for (int i = 0; i < 2 && tp < tiles; ++i, ahead(tp, cp)) issue_e(tp, cp, e_issued++);
     for (; t < tiles && ok; t += gridDim.x, ++local) {
       const uint32_t acc = local & 1;
       if (!(ok = warp_wait(&acc_full[acc], (local >> 1) & 1))) break;
@@ -158,12 +183,12 @@ tc_gemm_bf16(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CU
         const int j = sc % kBoxes;
         uint8_t* box = boxes + j * kBoxBytes;
         if (lane == 0) {
-          // the box of slice sc + 1 held slice sc - 2, whose store must have read it
+          // with E the box of slice sc + 2 held slice sc - 2, without E the box of slice sc
+          // did: that store must have read it
           tc::bulk_wait_group_read<1>();
-          if (with_e) {
-            int tn = t, cn = c + 1;
-            if (cn == ns) { tn = t + gridDim.x; cn = 0; }
-            if (tn < tiles) { issue_e(tn, cn, sc + 1); ++e_issued; }
+          if (with_e && tp < tiles) {
+            issue_e(tp, cp, e_issued++);
+            ahead(tp, cp);
           }
         }
         __syncwarp();
@@ -223,16 +248,6 @@ __global__ void selftest_wait_timeout(uint64_t limit_ns, int* status) {
   }
 }
 
-// fp32 -> bf16, same layout (n a multiple of 4, 16-byte aligned pointers)
-__global__ void to_bf16(const float4* __restrict__ x, __nv_bfloat162* __restrict__ y, size_t n4) {
-  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
-       i += (size_t)gridDim.x * blockDim.x) {
-    const float4 v = __ldg(&x[i]);
-    y[2 * i] = __floats2bfloat162_rn(v.x, v.y);
-    y[2 * i + 1] = __floats2bfloat162_rn(v.z, v.w);
-  }
-}
-
 // fp32 [R, C] -> bf16 [C, R] (transposed), small matrices
 __global__ void to_bf16_t(const float* __restrict__ x, __nv_bfloat16* __restrict__ y, int R,
                           int C) {
@@ -267,6 +282,16 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <bool kTf32, bool kWithE>
+cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
+                     const CUtensorMap& me, const GemmArgs& g, int grid, cudaStream_t s) {
+  constexpr size_t smem = Plan<kWithE>::kSmemBytes;
+  cudaError_t e = max_smem_once<tc_gemm<kTf32, kWithE>>(smem);
+  if (e != cudaSuccess) return e;
+  tc_gemm<kTf32, kWithE><<<grid, kThreads, smem, s>>>(ma, mb, mc, me, g);
+  return cudaGetLastError();
+}
+
 int sm_count() {
   static int n = 0;
   static std::once_flag once;
@@ -281,14 +306,6 @@ int sm_count() {
 
 }  // namespace
 
-cudaError_t launch_to_bf16(const float* x, void* y, size_t n, cudaStream_t s) {
-  const size_t n4 = n / 4;
-  const int blocks = (int)std::min<size_t>((n4 + 255) / 256, 152 * 16);
-  to_bf16<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(x),
-                                 reinterpret_cast<__nv_bfloat162*>(y), n4);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_to_bf16_t(const float* x, void* y, int R, int C, cudaStream_t s) {
   dim3 grid((C + 31) / 32, (R + 31) / 32);
   to_bf16_t<<<grid, dim3(32, 8), 0, s>>>(x, reinterpret_cast<__nv_bfloat16*>(y), R, C);
@@ -300,24 +317,25 @@ cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t
   return cudaGetLastError();
 }
 
-// A: bf16 [M, K] row-major; B: bf16 [N, K] row-major; C: f32 [M, N]; D: f32 [N] or null;
-// E: f32 [M, N] (read only when D is given).
-cudaError_t launch_tc_gemm(const void* A, const void* B, float* C, int M, int N, int K,
-                           const float* D, const float* E, int* status, cudaStream_t s) {
+// A: [M, K] row-major; B: [N, K] row-major, both bf16 (tf32 false) or both float32 (tf32
+// true); C: f32 [M, N]; D: f32 [N] or null; E: f32 [M, N] (read only when D is given).
+cudaError_t launch_tc_gemm(const void* A, const void* B, bool tf32, float* C, int M, int N,
+                           int K, const float* D, const float* E, int* status, cudaStream_t s) {
   if (M < 1 || N < 1 || K < 1) return cudaErrorInvalidValue;
   CUtensorMap ma, mb, mc, me;
-  if (!make_map(&ma, A, (uint64_t)M, (uint64_t)K, kBM, false)) return cudaErrorInvalidValue;
-  if (!make_map(&mb, B, (uint64_t)N, (uint64_t)K, kBN, false)) return cudaErrorInvalidValue;
+  if (!make_map(&ma, A, (uint64_t)M, (uint64_t)K, kBM, tf32)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, B, (uint64_t)N, (uint64_t)K, kBN, tf32)) return cudaErrorInvalidValue;
   if (!make_map(&mc, C, (uint64_t)M, (uint64_t)N, 32, true)) return cudaErrorInvalidValue;
   if (D && !make_map(&me, E, (uint64_t)M, (uint64_t)N, 32, true)) return cudaErrorInvalidValue;
   if (!D) me = mc;  // not read
-  cudaError_t e = max_smem_once<tc_gemm_bf16>(kSmemBytes);
-  if (e != cudaSuccess) return e;
   GemmArgs g{M, N, K, D, status};
   const long long tiles = (long long)((N + kBN - 1) / kBN) * ((M + kBM - 1) / kBM);
   const int grid = (int)std::min<long long>(tiles, sm_count());
-  tc_gemm_bf16<<<grid, kThreads, kSmemBytes, s>>>(ma, mb, mc, me, g);
-  return cudaGetLastError();
+  if (tf32)
+    return D ? run_gemm<true, true>(ma, mb, mc, me, g, grid, s)
+             : run_gemm<true, false>(ma, mb, mc, me, g, grid, s);
+  return D ? run_gemm<false, true>(ma, mb, mc, me, g, grid, s)
+           : run_gemm<false, false>(ma, mb, mc, me, g, grid, s);
 }
 
 }  // namespace dlr
