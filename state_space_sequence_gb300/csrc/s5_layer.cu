@@ -223,6 +223,7 @@ s5_carry(S5Work w, int B, int P, int NC) {
 template <bool kBf16Out>
 __global__ void __launch_bounds__(256)
 s5_chunk_apply(S5Work w, int L, int P, int NC) {
+  constexpr int kB = 8;  // steps per batch; the loads of batch i + 1 are in flight during batch i
   const int c = blockIdx.x, b = blockIdx.y;
   const int t0 = c * kT;
   const int valid = min(kT, L - t0);
@@ -235,23 +236,33 @@ s5_chunk_apply(S5Work w, int L, int P, int NC) {
     const size_t row0 = ((size_t)b * L + t0) * P + p;  // in complex elements
     float2* row = reinterpret_cast<float2*>(w.xv) + row0;
     __nv_bfloat162* row16 = reinterpret_cast<__nv_bfloat162*>(w.x16) + row0;
-    for (int tb = 0; tb < valid; tb += kBatch) {
-      float2 v[kBatch], a[kBatch];
+    float2 v[2][kB], a[2][kB];
+    auto fetch = [&](int buf, int tb) {
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
+      for (int j = 0; j < kB; ++j) {
         const bool in = tb + j < valid;
-        v[j] = in ? row[(size_t)(tb + j) * P] : make_float2(0.f, 0.f);
-        a[j] = in ? w.lbar_pw[(size_t)(tb + j + 1) * P + p] : make_float2(0.f, 0.f);
+        v[buf][j] = in ? row[(size_t)(tb + j) * P] : make_float2(0.f, 0.f);
+        a[buf][j] = in ? w.lbar_pw[(size_t)(tb + j + 1) * P + p] : make_float2(0.f, 0.f);
       }
+    };
+    fetch(0, 0);
+#pragma unroll 1
+    for (int tb = 0; tb < valid; tb += 2 * kB) {
 #pragma unroll
-      for (int j = 0; j < kBatch; ++j) {
-        if (tb + j >= valid) break;
-        l = cfma(lam, l, {v[j].x, v[j].y});
-        const cf x = cfma({a[j].x, a[j].y}, xin, l);
-        if (kBf16Out)
-          row16[(size_t)(tb + j) * P] = __floats2bfloat162_rn(x.re, x.im);
-        else
-          row[(size_t)(tb + j) * P] = make_float2(x.re, x.im);
+      for (int half = 0; half < 2; ++half) {
+        const int tc = tb + half * kB;
+        if (tc >= valid) break;
+        if (tc + kB < valid) fetch(half ^ 1, tc + kB);
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+          if (tc + j >= valid) break;
+          l = cfma(lam, l, {v[half][j].x, v[half][j].y});
+          const cf x = cfma({a[half][j].x, a[half][j].y}, xin, l);
+          if (kBf16Out)
+            row16[(size_t)(tc + j) * P] = __floats2bfloat162_rn(x.re, x.im);
+          else
+            row[(size_t)(tc + j) * P] = make_float2(x.re, x.im);
+        }
       }
     }
   }
