@@ -196,8 +196,8 @@ dlr_status dlr_scan_apply(const float* u, int64_t B, int64_t H, int64_t N, int64
  * u, y: [B, L, H] float32. lambda: [P, 2]. log_delta: [P]. Bt: [P, H, 2]. Ct: [H, P, 2].
  * D: [H]. prec = DLR_FP32: all products in float32 FMA. prec = DLR_BF16_TC: the two
  * projections on tensor cores with float32 accumulation, the input projection with tf32
- * operands (u read as float32), the output projection with bfloat16 operands (x and Ct
- * rounded to bfloat16); the scan in float32 either way.
+ * operands (u read as float32), the output projection with bfloat16 operands; the projected
+ * input and the states between them are kept in bfloat16, the scan arithmetic is float32.
  * workspace: >= s5_workspace_size(B, L, H, P, prec) bytes. u and y must not overlap.
  * Limits: H % 32 == 0, P % 32 == 0, 32 <= H, P <= 1024.
  */

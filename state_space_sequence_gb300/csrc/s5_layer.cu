@@ -15,8 +15,9 @@
 //   apply  x_t = Lbar^{t+1} X_in + l_t, l_t = Lbar l_{t-1} + V_t, written over V in place
 //   gemm   y = x * [Re C~^T ; -Im C~^T] + D (.) u
 // The tensor-core tier runs the two projections on tcgen05 (tc_gemm.cu): the input projection
-// reads the float32 u and Bbar as tf32 operands, the output projection takes x and C~ as bf16
-// operands (apply writes x as bf16).
+// reads the float32 u and Bbar as tf32 operands and writes V as bf16; the scan reads V in bf16
+// and computes in float32; apply writes x as bf16 over V, the operand of the output projection
+// with C~ in bf16.
 #include <cuda_bf16.h>
 
 #include "dlr_common.cuh"
@@ -29,14 +30,14 @@ constexpr int kT = 64;   // steps per chunk
 struct S5Work {
   float* bbar_t;   // f32 [2P][H]    (tensor-core tier only)
   void* cmat_t16;  // bf16 [H][2P]
-  void* x16;       // bf16 [B*L][2P]
+  void* vx16;      // bf16 [B*L][2P]: V, then x (tensor-core tier)
   float* bbar;     // [H][2P]
   float* cmat;     // [2P][H]
   float2* lbar_pw; // [T+1][P]  Lbar^t (state fastest, so a warp's loads of one power coalesce)
   float4* lbar_T;  // [P] (re.hi, re.lo, im.hi, im.lo) of Lbar^T
   float2* S;       // [B][NC][P]
   float2* Xin;     // [B][NC][P]
-  float* xv;       // [B*L][2P]: V, then x
+  float* xv;       // [B*L][2P]: V, then x (float32 tier)
 };
 
 __global__ void s5_prep(const float* __restrict__ lambda, const float* __restrict__ log_delta,
@@ -132,20 +133,22 @@ gemm_f32(const float* __restrict__ A, const float* __restrict__ Bm, float* __res
 // S_c = sum_t Lbar^{T-1-t} V_t with the directly computed powers. The V loads of a thread are
 // issued kBatch at a time ahead of their use, so each thread keeps several in flight.
 constexpr int kBatch = 16;
+
 __global__ void __launch_bounds__(256)
 s5_chunk_state(S5Work w, int L, int P, int NC) {
   const int c = blockIdx.x, b = blockIdx.y;
   const int t0 = c * kT;
   const int valid = min(kT, L - t0);
   for (int p = threadIdx.x; p < P; p += blockDim.x) {
-    const float2* col = reinterpret_cast<const float2*>(w.xv) + ((size_t)b * L + t0) * P + p;
+    const size_t col = ((size_t)b * L + t0) * P + p;  // in complex elements
     cf acc = {0.f, 0.f};
     for (int tb = 0; tb < valid; tb += kBatch) {
       float2 v[kBatch], a[kBatch];
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
         const bool in = tb + j < valid;
-        v[j] = in ? col[(size_t)(tb + j) * P] : make_float2(0.f, 0.f);
+        v[j] = in ? reinterpret_cast<const float2*>(w.xv)[col + (size_t)(tb + j) * P]
+                  : make_float2(0.f, 0.f);
         a[j] = in ? w.lbar_pw[(size_t)(kT - 1 - tb - j) * P + p] : make_float2(0.f, 0.f);
       }
 #pragma unroll
@@ -216,11 +219,9 @@ s5_carry(S5Work w, int B, int P, int NC) {
 }
 
 // grid (NC, B), one thread per state p: x_t = Lbar^{t+1} X_in + l_t with the in-chunk part
-// l_t = Lbar l_{t-1} + V_t (l_{-1} = 0) run as a 64-step recurrence, written over V in place
-// (float32 tier) or as the bf16 operand of the output projection (bf16 tier).
+// l_t = Lbar l_{t-1} + V_t (l_{-1} = 0) run as a 64-step recurrence, written over V in place.
 // The carried state enters through the directly computed power Lbar^{t+1}; only in-chunk lags
 // go through the float32 product chain (at most 64 roundings).
-template <bool kBf16Out>
 __global__ void __launch_bounds__(256)
 s5_chunk_apply(S5Work w, int L, int P, int NC) {
   constexpr int kB = 8;  // steps per batch; the loads of batch i + 1 are in flight during batch i
@@ -233,9 +234,7 @@ s5_chunk_apply(S5Work w, int L, int P, int NC) {
     const float2 lb = w.lbar_pw[(size_t)P + p];
     const cf lam = {lb.x, lb.y};
     cf l = {0.f, 0.f};
-    const size_t row0 = ((size_t)b * L + t0) * P + p;  // in complex elements
-    float2* row = reinterpret_cast<float2*>(w.xv) + row0;
-    __nv_bfloat162* row16 = reinterpret_cast<__nv_bfloat162*>(w.x16) + row0;
+    float2* row = reinterpret_cast<float2*>(w.xv) + ((size_t)b * L + t0) * P + p;
     float2 v[2][kB], a[2][kB];
     auto fetch = [&](int buf, int tb) {
 #pragma unroll
@@ -258,13 +257,101 @@ s5_chunk_apply(S5Work w, int L, int P, int NC) {
           if (tc + j >= valid) break;
           l = cfma(lam, l, {v[half][j].x, v[half][j].y});
           const cf x = cfma({a[half][j].x, a[half][j].y}, xin, l);
-          if (kBf16Out)
-            row16[(size_t)(tc + j) * P] = __floats2bfloat162_rn(x.re, x.im);
-          else
-            row[(size_t)(tc + j) * P] = make_float2(x.re, x.im);
+          row[(size_t)(tc + j) * P] = make_float2(x.re, x.im);
         }
       }
     }
+  }
+}
+
+// Tensor-core tier, V and x in bf16. One thread per (b, chunk c, four consecutive states),
+// 16-byte loads and stores; both kernels run the recurrence x <- Lbar x + V_t over the chunk in
+// float32 (64 roundings of the product, far below the bf16 rounding of V and x):
+//   state16  from x = 0, keeping the chunk end state S_c,
+//   apply16  from x = X_in (the state entering the chunk), writing x_t over V_t.
+struct Quad {
+  int b, c, p0;  // batch row, chunk, first of the four states
+};
+__device__ __forceinline__ bool quad_of(int B, int NC, int P, Quad& q) {
+  const int nq = P / 4;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)B * NC * nq) return false;
+  q.p0 = int(i % nq) * 4;
+  const long long r = i / nq;
+  q.c = int(r % NC);
+  q.b = int(r / NC);
+  return true;
+}
+__device__ __forceinline__ void unpack4(uint4 v, cf (&x)[4]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+    x[k] = {f.x, f.y};
+  }
+}
+__device__ __forceinline__ uint4 pack4(const cf (&x)[4]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x[k].re, x[k].im);
+    w[k] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <bool kApply>
+__global__ void __launch_bounds__(256)
+s5_chunk16(S5Work w, int B, int L, int P, int NC) {
+  constexpr int kB = 8;
+  Quad q;
+  if (!quad_of(B, NC, P, q)) return;
+  const int t0 = q.c * kT;
+  const int valid = min(kT, L - t0);
+  uint4* row = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat162*>(w.vx16) +
+                                        ((size_t)q.b * L + t0) * P + q.p0);
+  const size_t stride = (size_t)P / 4;  // uint4 per time step
+  cf lam[4], x[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 lb = w.lbar_pw[(size_t)P + q.p0 + k];
+    lam[k] = {lb.x, lb.y};
+    if (kApply) {
+      const float2 xi = w.Xin[((size_t)q.b * NC + q.c) * P + q.p0 + k];
+      x[k] = {xi.x, xi.y};
+    } else {
+      x[k] = {0.f, 0.f};
+    }
+  }
+  uint4 v[2][kB];
+  auto fetch = [&](int buf, int tb) {
+#pragma unroll
+    for (int j = 0; j < kB; ++j)
+      v[buf][j] = tb + j < valid ? row[(size_t)(tb + j) * stride] : make_uint4(0, 0, 0, 0);
+  };
+  fetch(0, 0);
+#pragma unroll 1
+  for (int tb = 0; tb < valid; tb += 2 * kB) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int tc = tb + half * kB;
+      if (tc >= valid) break;
+      if (tc + kB < valid) fetch(half ^ 1, tc + kB);
+#pragma unroll
+      for (int j = 0; j < kB; ++j) {
+        if (tc + j >= valid) break;
+        cf vin[4];
+        unpack4(v[half][j], vin);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[k] = cfma(lam[k], x[k], vin[k]);
+        if (kApply) row[(size_t)(tc + j) * stride] = pack4(x);
+      }
+    }
+  }
+  if (!kApply) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      w.S[((size_t)q.b * NC + q.c) * P + q.p0 + k] = make_float2(x[k].re, x[k].im);
   }
 }
 
@@ -282,12 +369,12 @@ S5Work carve(void* ws, int64_t B, int64_t L, int64_t H, int64_t P, bool bf16, si
   size_t o_lt = take(sizeof(float4) * P);
   size_t o_S = take(sizeof(float2) * B * NC * P);
   size_t o_X = take(sizeof(float2) * B * NC * P);
-  size_t o_xv = take(sizeof(float) * B * L * 2 * P);
-  size_t o_bt = 0, o_c16 = 0, o_x16 = 0;
+  size_t o_xv = bf16 ? 0 : take(sizeof(float) * B * L * 2 * P);
+  size_t o_bt = 0, o_c16 = 0, o_vx16 = 0;
   if (bf16) {
     o_bt = take(sizeof(float) * 2 * P * H);
     o_c16 = take(2 * H * 2 * P);
-    o_x16 = take(2 * B * L * 2 * P);
+    o_vx16 = take(2 * B * L * 2 * P);
   }
   if (total) *total = off;
   char* base = reinterpret_cast<char*>(ws);
@@ -298,10 +385,10 @@ S5Work carve(void* ws, int64_t B, int64_t L, int64_t H, int64_t P, bool bf16, si
   w.lbar_T = reinterpret_cast<float4*>(base + o_lt);
   w.S = reinterpret_cast<float2*>(base + o_S);
   w.Xin = reinterpret_cast<float2*>(base + o_X);
-  w.xv = reinterpret_cast<float*>(base + o_xv);
+  w.xv = bf16 ? nullptr : reinterpret_cast<float*>(base + o_xv);
   w.bbar_t = bf16 ? reinterpret_cast<float*>(base + o_bt) : nullptr;
   w.cmat_t16 = bf16 ? base + o_c16 : nullptr;
-  w.x16 = bf16 ? base + o_x16 : nullptr;
+  w.vx16 = bf16 ? base + o_vx16 : nullptr;
   return w;
 }
 
@@ -314,20 +401,26 @@ size_t s5_workspace_bytes(int64_t B, int64_t L, int64_t H, int64_t P, bool bf16)
 }
 
 cudaError_t launch_to_bf16_t(const float* x, void* y, int R, int C, cudaStream_t s);
-cudaError_t launch_tc_gemm(const void* A, const void* B, bool tf32, float* C, int M, int N,
-                           int K, const float* D, const float* E, int* status, cudaStream_t s);
+cudaError_t launch_tc_gemm(const void* A, const void* B, bool tf32, void* C, bool c_bf16, int M,
+                           int N, int K, const float* D, const float* E, int* status,
+                           cudaStream_t s);
 
-// The chunked diagonal scan shared by both tiers: V (in w.xv) -> x, in place in w.xv (float32)
-// or into w.x16 (bf16).
+// The chunked diagonal scan shared by both tiers: V -> x in place, in w.xv (float32 tier) or
+// w.vx16 (tensor-core tier).
 static cudaError_t s5_scan_xv(const S5Work& w, int B, int L, int P, bool bf16, cudaStream_t s) {
   const int NC = (L + kT - 1) / kT;
   const int threads = P < 256 ? P : 256;  // P is a multiple of 32
-  s5_chunk_state<<<dim3(NC, B), threads, 0, s>>>(w, L, P, NC);
+  const long long quads = (long long)B * NC * (P / 4);
+  const int grid16 = (int)((quads + 255) / 256);
+  if (bf16)
+    s5_chunk16<false><<<grid16, 256, 0, s>>>(w, B, L, P, NC);
+  else
+    s5_chunk_state<<<dim3(NC, B), threads, 0, s>>>(w, L, P, NC);
   s5_carry<<<(B * P + 7) / 8, 256, 0, s>>>(w, B, P, NC);
   if (bf16)
-    s5_chunk_apply<true><<<dim3(NC, B), threads, 0, s>>>(w, L, P, NC);
+    s5_chunk16<true><<<grid16, 256, 0, s>>>(w, B, L, P, NC);
   else
-    s5_chunk_apply<false><<<dim3(NC, B), threads, 0, s>>>(w, L, P, NC);
+    s5_chunk_apply<<<dim3(NC, B), threads, 0, s>>>(w, L, P, NC);
   return cudaGetLastError();
 }
 
@@ -348,14 +441,14 @@ cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delt
     gemm_f32<<<g2, 256, 0, s>>>(w.xv, w.cmat, y, M, H, 2 * P, D, u);
     return cudaGetLastError();
   }
-  // tensor cores with f32 accumulation: tf32 input projection straight from u, bf16 output
-  // projection; the scan stays f32
+  // tensor cores with f32 accumulation: tf32 input projection straight from u into bf16 V, the
+  // scan in f32 arithmetic writing bf16 x over V, bf16 output projection
   if ((e = launch_to_bf16_t(w.cmat, w.cmat_t16, 2 * P, H, s)) != cudaSuccess) return e;
-  if ((e = launch_tc_gemm(u, w.bbar_t, true, w.xv, M, 2 * P, H, nullptr, nullptr, status, s)) !=
-      cudaSuccess)
+  if ((e = launch_tc_gemm(u, w.bbar_t, true, w.vx16, true, M, 2 * P, H, nullptr, nullptr, status,
+                          s)) != cudaSuccess)
     return e;
   if ((e = s5_scan_xv(w, B, L, P, true, s)) != cudaSuccess) return e;
-  return launch_tc_gemm(w.x16, w.cmat_t16, false, y, M, H, 2 * P, D, u, status, s);
+  return launch_tc_gemm(w.vx16, w.cmat_t16, false, y, false, M, H, 2 * P, D, u, status, s);
 }
 
 }  // namespace dlr

@@ -1,4 +1,4 @@
-// tc_gemm.cu -- C[M, N] (f32) = A[M, K] * B[N, K]^T (+ D[n] * E[m, n]) on 5th-generation tensor
+// tc_gemm.cu -- C[M, N] (f32 or bf16) = A[M, K] * B[N, K]^T (+ D[n] * E[m, n]) on 5th-generation tensor
 // cores: bf16 operands (kind::f16) or float32 operands read as tf32 (kind::tf32) in shared
 // memory (TMA tile loads, 128-byte swizzle), f32 accumulators in tensor memory, tcgen05.mma
 // issued by one thread, tcgen05.ld epilogue with TMA tile stores.
@@ -13,8 +13,9 @@
 //                  per tile a commit that hands one of two TMEM accumulators to the epilogue,
 //   warp 2         allocates / frees the 512 TMEM columns (two 256-column accumulators),
 //   warps 4-7      epilogue: warp 4+q owns TMEM lanes 32q..32q+31 (rows of the tile). Per slice
-//                  of 32 columns: tcgen05.ld, + D (.) E with the E box brought in by TMA, into a
-//                  4 KB staging box (128-byte swizzle), out by one TMA store per warp. The
+//                  of 128 output bytes per row (32 f32 or 64 bf16 columns): tcgen05.ld, + D (.) E
+//                  with the E box brought in by TMA, into a 4 KB staging box (128-byte swizzle),
+//                  out by one TMA store per warp. The
 //                  boxes of a warp rotate: the E loads of the next two slices and the stores of
 //                  the last one or two are in flight while the current slice is worked on.
 // While the epilogue drains one accumulator the MMAs of the next tile fill the other.
@@ -33,10 +34,9 @@ namespace {
 
 constexpr int kBM = 128, kBN = 256;
 constexpr int kRowBytes = 128;  // K bytes of one operand row per stage (the swizzle span)
-constexpr int kSlice = 32, kSlices = kBN / kSlice;
 constexpr uint32_t kABytes = kBM * kRowBytes, kBBytes = kBN * kRowBytes;
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr uint32_t kBoxBytes = 32 * kSlice * 4;  // 32 rows x 32 f32 columns
+constexpr uint32_t kBoxBytes = 32 * 128;  // 32 rows x 128 bytes
 
 // Shared-memory plan. With E the epilogue keeps four boxes per warp (two E loads ahead) and
 // the ring three stages; without E two boxes suffice and the ring gets a fourth stage.
@@ -63,12 +63,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity)) != 0;
 }
 
-template <bool kTf32, bool kWithE>
+template <bool kTf32, bool kWithE, bool kBf16Out>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmE,
              GemmArgs g) {
+  static_assert(!(kWithE && kBf16Out), "D (.) E is added to f32 outputs only");
   constexpr int kStages = Plan<kWithE>::kStages, kBoxes = Plan<kWithE>::kBoxes;
+  constexpr int kSlice = kBf16Out ? 64 : 32;  // output columns per slice (128 bytes per row)
+  constexpr int kSlices = kBN / kSlice;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -158,7 +161,9 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
     const uint32_t sw = uint32_t(lane & 7);
     // the slices this warp walks: (tile, column block), tiles in the CTA's order
     int t = blockIdx.x, c = 0;
-    auto n_slices = [&](int tt) { return min(kSlices, (g.N - (tt % n_tiles) * kBN + kSlice - 1) / kSlice); };
+    auto n_slices = [&](int tt) {
+      return min(kSlices, (g.N - (tt % n_tiles) * kBN + kSlice - 1) / kSlice);
+    };
     auto issue_e = [&](int tt, int cc, uint32_t sc) {
       const int j = sc % kBoxes;
       tc::mbar_arrive_expect_tx(&ebar[j], kBoxBytes);
@@ -192,14 +197,29 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
           }
         }
         __syncwarp();
-        float v[32];
-        tc::tmem_ld32(tmem + acc * kBN + (uint32_t(q * 32) << 16) + uint32_t(c * kSlice), v);
+        const uint32_t tcol = tmem + acc * kBN + (uint32_t(q * 32) << 16) + uint32_t(c * kSlice);
+        float v[32], v2[32];
+        tc::tmem_ld32(tcol, v);
+        if constexpr (kBf16Out) tc::tmem_ld32(tcol + 32, v2);  // the other 32 of 64 columns
         if (c == ns - 1) {  // accumulator read out: the MMAs of tile local + 2 may start
           tc::fence_before_sync();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&acc_empty[acc]);
         }
-        if (with_e) {
+        if constexpr (kBf16Out) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float* src = k < 4 ? v + 8 * k : v2 + 8 * (k - 4);
+            uint32_t h[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(src[2 * i], src[2 * i + 1]);
+              h[i] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            *reinterpret_cast<uint4*>(box + lane * 128 + ((uint32_t(k) ^ sw) << 4)) =
+                make_uint4(h[0], h[1], h[2], h[3]);
+          }
+        } else if (with_e) {
           if (!(ok = warp_wait(&ebar[j], (sc / kBoxes) & 1))) break;
           const int nc = n0 + c * kSlice;
 #pragma unroll
@@ -282,13 +302,13 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kTf32, bool kWithE>
+template <bool kTf32, bool kWithE, bool kBf16Out>
 cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                      const CUtensorMap& me, const GemmArgs& g, int grid, cudaStream_t s) {
   constexpr size_t smem = Plan<kWithE>::kSmemBytes;
-  cudaError_t e = max_smem_once<tc_gemm<kTf32, kWithE>>(smem);
+  cudaError_t e = max_smem_once<tc_gemm<kTf32, kWithE, kBf16Out>>(smem);
   if (e != cudaSuccess) return e;
-  tc_gemm<kTf32, kWithE><<<grid, kThreads, smem, s>>>(ma, mb, mc, me, g);
+  tc_gemm<kTf32, kWithE, kBf16Out><<<grid, kThreads, smem, s>>>(ma, mb, mc, me, g);
   return cudaGetLastError();
 }
 
@@ -318,24 +338,29 @@ cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t
 }
 
 // A: [M, K] row-major; B: [N, K] row-major, both bf16 (tf32 false) or both float32 (tf32
-// true); C: f32 [M, N]; D: f32 [N] or null; E: f32 [M, N] (read only when D is given).
-cudaError_t launch_tc_gemm(const void* A, const void* B, bool tf32, float* C, int M, int N,
-                           int K, const float* D, const float* E, int* status, cudaStream_t s) {
-  if (M < 1 || N < 1 || K < 1) return cudaErrorInvalidValue;
+// true); C: [M, N], f32 or (c_bf16, no D) bf16; D: f32 [N] or null; E: f32 [M, N] (read only
+// when D is given).
+cudaError_t launch_tc_gemm(const void* A, const void* B, bool tf32, void* C, bool c_bf16, int M,
+                           int N, int K, const float* D, const float* E, int* status,
+                           cudaStream_t s) {
+  if (M < 1 || N < 1 || K < 1 || (c_bf16 && D)) return cudaErrorInvalidValue;
   CUtensorMap ma, mb, mc, me;
   if (!make_map(&ma, A, (uint64_t)M, (uint64_t)K, kBM, tf32)) return cudaErrorInvalidValue;
   if (!make_map(&mb, B, (uint64_t)N, (uint64_t)K, kBN, tf32)) return cudaErrorInvalidValue;
-  if (!make_map(&mc, C, (uint64_t)M, (uint64_t)N, 32, true)) return cudaErrorInvalidValue;
+  if (!make_map(&mc, C, (uint64_t)M, (uint64_t)N, 32, !c_bf16)) return cudaErrorInvalidValue;
   if (D && !make_map(&me, E, (uint64_t)M, (uint64_t)N, 32, true)) return cudaErrorInvalidValue;
   if (!D) me = mc;  // not read
   GemmArgs g{M, N, K, D, status};
   const long long tiles = (long long)((N + kBN - 1) / kBN) * ((M + kBM - 1) / kBM);
   const int grid = (int)std::min<long long>(tiles, sm_count());
-  if (tf32)
-    return D ? run_gemm<true, true>(ma, mb, mc, me, g, grid, s)
-             : run_gemm<true, false>(ma, mb, mc, me, g, grid, s);
-  return D ? run_gemm<false, true>(ma, mb, mc, me, g, grid, s)
-           : run_gemm<false, false>(ma, mb, mc, me, g, grid, s);
+  if (D)
+    return tf32 ? run_gemm<true, true, false>(ma, mb, mc, me, g, grid, s)
+                : run_gemm<false, true, false>(ma, mb, mc, me, g, grid, s);
+  if (c_bf16)
+    return tf32 ? run_gemm<true, false, true>(ma, mb, mc, me, g, grid, s)
+                : run_gemm<false, false, true>(ma, mb, mc, me, g, grid, s);
+  return tf32 ? run_gemm<true, false, false>(ma, mb, mc, me, g, grid, s)
+              : run_gemm<false, false, false>(ma, mb, mc, me, g, grid, s);
 }
 
 }  // namespace dlr
