@@ -43,34 +43,64 @@ struct S5Work {
 __global__ void s5_prep(const float* __restrict__ lambda, const float* __restrict__ log_delta,
                         const float2* __restrict__ Bt, const float2* __restrict__ Ct, int H, int P,
                         S5Work w) {
+  // One thread evaluates the state's transcendental functions in double (the FP64 units are
+  // few): Lbar, (Lbar - 1) / Lambda, and the powers Lbar^k, Lbar^(8k) for k = 0..8 by
+  // sequential products; every power t <= T is then one product Lbar^(8(t>>3)) Lbar^(t&7).
+  __shared__ double sp1[9][2], sp8[9][2];
+  __shared__ float2 sq;
   const int p = blockIdx.x;
-  const double lr = lambda[2 * p], li = lambda[2 * p + 1];
-  const double delta = exp((double)log_delta[p]);
-  const double zr = lr * delta, zi = li * delta;
-  const double er = exp(zr);
-  const double ar = er * cos(zi), ai = er * sin(zi);  // Lbar
-  // (Lbar - 1) / Lambda
-  const double nr = ar - 1.0, ni = ai;
-  const double den = lr * lr + li * li;
-  const double qr = (nr * lr + ni * li) / den, qi = (ni * lr - nr * li) / den;
-  for (int h = threadIdx.x; h < H; h += blockDim.x) {
-    float2 b = Bt[(size_t)p * H + h];
-    double br = qr * b.x - qi * b.y, bi = qr * b.y + qi * b.x;
-    w.bbar[(size_t)h * 2 * P + 2 * p] = (float)br;
-    w.bbar[(size_t)h * 2 * P + 2 * p + 1] = (float)bi;
-    if (w.bbar_t) {
-      w.bbar_t[(size_t)(2 * p) * H + h] = (float)br;
-      w.bbar_t[(size_t)(2 * p + 1) * H + h] = (float)bi;
+  if (threadIdx.x == 0) {
+    const double lr = lambda[2 * p], li = lambda[2 * p + 1];
+    const double delta = exp((double)log_delta[p]);
+    const double zr = lr * delta, zi = li * delta;
+    const double er = exp(zr);
+    const double ar = er * cos(zi), ai = er * sin(zi);  // Lbar
+    const double nr = ar - 1.0, ni = ai;                // (Lbar - 1) / Lambda
+    const double den = lr * lr + li * li;
+    sq = make_float2((float)((nr * lr + ni * li) / den), (float)((ni * lr - nr * li) / den));
+    double re = 1.0, im = 0.0;
+    for (int k = 0; k <= 8; ++k) {
+      sp1[k][0] = re;
+      sp1[k][1] = im;
+      const double r2 = re * ar - im * ai;
+      im = re * ai + im * ar;
+      re = r2;
     }
-    float2 c = Ct[(size_t)h * P + p];
-    w.cmat[(size_t)(2 * p) * H + h] = c.x;
-    w.cmat[(size_t)(2 * p + 1) * H + h] = -c.y;
+    const double br = sp1[8][0], bi = sp1[8][1];
+    re = 1.0, im = 0.0;
+    for (int k = 0; k <= 8; ++k) {
+      sp8[k][0] = re;
+      sp8[k][1] = im;
+      const double r2 = re * br - im * bi;
+      im = re * bi + im * br;
+      re = r2;
+    }
+  }
+  __syncthreads();
+  const float qr = sq.x, qi = sq.y;
+  const bool tc = w.bbar_t != nullptr;  // tensor-core tier: transposed B, bf16 C operands
+  for (int h = threadIdx.x; h < H; h += blockDim.x) {
+    const float2 b = Bt[(size_t)p * H + h];
+    const float br = fmaf(qr, b.x, -qi * b.y), bi = fmaf(qr, b.y, qi * b.x);
+    const float2 c = Ct[(size_t)h * P + p];
+    if (tc) {
+      w.bbar_t[(size_t)(2 * p) * H + h] = br;
+      w.bbar_t[(size_t)(2 * p + 1) * H + h] = bi;
+      reinterpret_cast<__nv_bfloat162*>(w.cmat_t16)[(size_t)h * P + p] =
+          __floats2bfloat162_rn(c.x, -c.y);
+    } else {
+      w.bbar[(size_t)h * 2 * P + 2 * p] = br;
+      w.bbar[(size_t)h * 2 * P + 2 * p + 1] = bi;
+      w.cmat[(size_t)(2 * p) * H + h] = c.x;
+      w.cmat[(size_t)(2 * p + 1) * H + h] = -c.y;
+    }
   }
   for (int t = threadIdx.x; t <= kT; t += blockDim.x) {
-    const double m = exp(zr * t), ph = zi * t;
-    w.lbar_pw[(size_t)t * P + p] = make_float2((float)(m * cos(ph)), (float)(m * sin(ph)));
+    const double* a8 = sp8[t >> 3];
+    const double* a1 = sp1[t & 7];
+    const double re = a8[0] * a1[0] - a8[1] * a1[1], im = a8[0] * a1[1] + a8[1] * a1[0];
+    w.lbar_pw[(size_t)t * P + p] = make_float2((float)re, (float)im);
     if (t == kT) {
-      double re = m * cos(ph), im = m * sin(ph);
       float rh = (float)re, ih = (float)im;
       w.lbar_T[p] = make_float4(rh, (float)(re - rh), ih, (float)(im - ih));
     }
@@ -363,8 +393,8 @@ S5Work carve(void* ws, int64_t B, int64_t L, int64_t H, int64_t P, bool bf16, si
     off += (bytes + 255) & ~size_t(255);
     return o;
   };
-  size_t o_bbar = take(sizeof(float) * H * 2 * P);
-  size_t o_cmat = take(sizeof(float) * 2 * P * H);
+  size_t o_bbar = bf16 ? 0 : take(sizeof(float) * H * 2 * P);
+  size_t o_cmat = bf16 ? 0 : take(sizeof(float) * 2 * P * H);
   size_t o_pw = take(sizeof(float2) * P * (kT + 1));
   size_t o_lt = take(sizeof(float4) * P);
   size_t o_S = take(sizeof(float2) * B * NC * P);
@@ -379,8 +409,8 @@ S5Work carve(void* ws, int64_t B, int64_t L, int64_t H, int64_t P, bool bf16, si
   if (total) *total = off;
   char* base = reinterpret_cast<char*>(ws);
   S5Work w;
-  w.bbar = reinterpret_cast<float*>(base + o_bbar);
-  w.cmat = reinterpret_cast<float*>(base + o_cmat);
+  w.bbar = bf16 ? nullptr : reinterpret_cast<float*>(base + o_bbar);
+  w.cmat = bf16 ? nullptr : reinterpret_cast<float*>(base + o_cmat);
   w.lbar_pw = reinterpret_cast<float2*>(base + o_pw);
   w.lbar_T = reinterpret_cast<float4*>(base + o_lt);
   w.S = reinterpret_cast<float2*>(base + o_S);
@@ -400,7 +430,6 @@ size_t s5_workspace_bytes(int64_t B, int64_t L, int64_t H, int64_t P, bool bf16)
   return total;
 }
 
-cudaError_t launch_to_bf16_t(const float* x, void* y, int R, int C, cudaStream_t s);
 cudaError_t launch_tc_gemm(const void* A, const void* B, bool tf32, void* C, bool c_bf16, int M,
                            int N, int K, const float* D, const float* E, int* status,
                            cudaStream_t s);
@@ -443,7 +472,6 @@ cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delt
   }
   // tensor cores with f32 accumulation: tf32 input projection straight from u into bf16 V, the
   // scan in f32 arithmetic writing bf16 x over V, bf16 output projection
-  if ((e = launch_to_bf16_t(w.cmat, w.cmat_t16, 2 * P, H, s)) != cudaSuccess) return e;
   if ((e = launch_tc_gemm(u, w.bbar_t, true, w.vx16, true, M, 2 * P, H, nullptr, nullptr, status,
                           s)) != cudaSuccess)
     return e;

@@ -268,22 +268,6 @@ __global__ void selftest_wait_timeout(uint64_t limit_ns, int* status) {
   }
 }
 
-// fp32 [R, C] -> bf16 [C, R] (transposed), small matrices
-__global__ void to_bf16_t(const float* __restrict__ x, __nv_bfloat16* __restrict__ y, int R,
-                          int C) {
-  __shared__ float tile[32][33];
-  const int r0 = blockIdx.y * 32, c0 = blockIdx.x * 32;
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-    const int r = r0 + i, c = c0 + threadIdx.x;
-    tile[i][threadIdx.x] = (r < R && c < C) ? x[(size_t)r * C + c] : 0.f;
-  }
-  __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-    const int c = c0 + i, r = r0 + threadIdx.x;
-    if (c < C && r < R) y[(size_t)c * R + r] = __float2bfloat16_rn(tile[threadIdx.x][i]);
-  }
-}
-
 // Row-major [rows, cols] tensor of 2-byte (bf16) or 4-byte (f32) elements, boxes of
 // box_rows x box_cols elements with a 128-byte swizzle (box_cols * element size = 128).
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
@@ -325,12 +309,6 @@ int sm_count() {
 }
 
 }  // namespace
-
-cudaError_t launch_to_bf16_t(const float* x, void* y, int R, int C, cudaStream_t s) {
-  dim3 grid((C + 31) / 32, (R + 31) / 32);
-  to_bf16_t<<<grid, dim3(32, 8), 0, s>>>(x, reinterpret_cast<__nv_bfloat16*>(y), R, C);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s) {
   selftest_wait_timeout<<<1, 32, 0, s>>>(limit_ns, status);
