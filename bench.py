@@ -435,10 +435,18 @@ def run_extras(torch, dlr, inputs, flush, sm_mhz, sm_count):
                      device="cuda")
     ms = _time_steps(torch, lambda: dlr.s5_layer(u, *args5, prec="bf16", workspace=ws, out=y),
                      10, 3, flush)
-    # two projections of 2 * (B L) * H * 2P flops each
+    # two projections of 2 * (B L) * H * 2P flops each; algorithmic bytes u in + y out + the
+    # parameters (lambda, log_delta, Bt, Ct, D)
     gemm_flops = 2 * 2 * w.B * w.L * w.H * 2 * w.P
-    out["s5_bf16_tc_" + w.name] = {"ms": ms, "elements_per_s": w.B * w.L * w.H / ms * 1e3,
-                                   "projection_tflops": gemm_flops / ms / 1e9}
+    s5_bytes = 4 * (2 * w.B * w.L * w.H + 2 * w.P + w.P + 2 * 2 * w.P * w.H + w.H)
+    peak_gbs, peak_kind = load_peaks()
+    out["s5_bf16_tc_" + w.name] = {
+        "ms": ms, "elements_per_s": w.B * w.L * w.H / ms * 1e3,
+        "projection_tflops": gemm_flops / ms / 1e9,
+        "hbm": {"algorithmic_bytes": s5_bytes, "achieved_gbs": s5_bytes / ms / 1e6,
+                "frac": s5_bytes / ms / 1e6 / peak_gbs, "peak_kind": peak_kind},
+        "precision": "input projection tf32, V and x bf16, output projection bf16, "
+                     "scan float32, f32 accumulation"}
     return out
 
 
