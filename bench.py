@@ -445,8 +445,8 @@ def run_extras(torch, dlr, inputs, flush, sm_mhz, sm_count):
         "projection_tflops": gemm_flops / ms / 1e9,
         "hbm": {"algorithmic_bytes": s5_bytes, "achieved_gbs": s5_bytes / ms / 1e6,
                 "frac": s5_bytes / ms / 1e6 / peak_gbs, "peak_kind": peak_kind},
-        "precision": "input projection tf32, V and x bf16, output projection bf16, "
-                     "scan float32, f32 accumulation"}
+        "precision": "bf16 projection operands (u rounded to bf16 in the kernel), V and x "
+                     "bf16, scan float32, f32 accumulation"}
     return out
 
 

@@ -195,9 +195,9 @@ dlr_status dlr_scan_apply(const float* u, int64_t B, int64_t H, int64_t N, int64
  *   y_k       = Re(Ct x_k) + D (.) u_k
  * u, y: [B, L, H] float32. lambda: [P, 2]. log_delta: [P]. Bt: [P, H, 2]. Ct: [H, P, 2].
  * D: [H]. prec = DLR_FP32: all products in float32 FMA. prec = DLR_BF16_TC: the two
- * projections on tensor cores with float32 accumulation, the input projection with tf32
- * operands (u read as float32), the output projection with bfloat16 operands; the projected
- * input and the states between them are kept in bfloat16, the scan arithmetic is float32.
+ * projections on tensor cores with bfloat16 operands and float32 accumulation (u is read as
+ * float32 and rounded to bfloat16 inside the kernel); the projected input and the states
+ * between the projections are kept in bfloat16, the scan arithmetic is float32.
  * workspace: >= s5_workspace_size(B, L, H, P, prec) bytes. u and y must not overlap.
  * Limits: H % 32 == 0, P % 32 == 0, 32 <= H, P <= 1024.
  */

@@ -14,10 +14,10 @@
 //          groups of chunks; stores the state entering each chunk
 //   apply  x_t = Lbar^{t+1} X_in + l_t, l_t = Lbar l_{t-1} + V_t, written over V in place
 //   gemm   y = x * [Re C~^T ; -Im C~^T] + D (.) u
-// The tensor-core tier runs the two projections on tcgen05 (tc_gemm.cu): the input projection
-// reads the float32 u and Bbar as tf32 operands and writes V as bf16; the scan reads V in bf16
-// and computes in float32; apply writes x as bf16 over V, the operand of the output projection
-// with C~ in bf16.
+// The tensor-core tier runs the two projections on tcgen05 (tc_gemm.cu) with bf16 operands and
+// float32 accumulation: the input projection converts the float32 u to bf16 in the kernel and
+// writes V as bf16; the scan reads V in bf16 and computes in float32; apply writes x as bf16
+// over V, the operand of the output projection.
 #include <cuda_bf16.h>
 
 #include "dlr_common.cuh"
@@ -28,7 +28,7 @@ namespace {
 constexpr int kT = 64;   // steps per chunk
 
 struct S5Work {
-  float* bbar_t;   // f32 [2P][H]    (tensor-core tier only)
+  void* bbar_t16;  // bf16 [2P][H]   (tensor-core tier only)
   void* cmat_t16;  // bf16 [H][2P]
   void* vx16;      // bf16 [B*L][2P]: V, then x (tensor-core tier)
   float* bbar;     // [H][2P]
@@ -78,14 +78,15 @@ __global__ void s5_prep(const float* __restrict__ lambda, const float* __restric
   }
   __syncthreads();
   const float qr = sq.x, qi = sq.y;
-  const bool tc = w.bbar_t != nullptr;  // tensor-core tier: transposed B, bf16 C operands
+  const bool tc = w.bbar_t16 != nullptr;  // tensor-core tier: bf16 operands
   for (int h = threadIdx.x; h < H; h += blockDim.x) {
     const float2 b = Bt[(size_t)p * H + h];
     const float br = fmaf(qr, b.x, -qi * b.y), bi = fmaf(qr, b.y, qi * b.x);
     const float2 c = Ct[(size_t)h * P + p];
     if (tc) {
-      w.bbar_t[(size_t)(2 * p) * H + h] = br;
-      w.bbar_t[(size_t)(2 * p + 1) * H + h] = bi;
+      __nv_bfloat16* bt = reinterpret_cast<__nv_bfloat16*>(w.bbar_t16);
+      bt[(size_t)(2 * p) * H + h] = __float2bfloat16_rn(br);
+      bt[(size_t)(2 * p + 1) * H + h] = __float2bfloat16_rn(bi);
       reinterpret_cast<__nv_bfloat162*>(w.cmat_t16)[(size_t)h * P + p] =
           __floats2bfloat162_rn(c.x, -c.y);
     } else {
@@ -402,7 +403,7 @@ S5Work carve(void* ws, int64_t B, int64_t L, int64_t H, int64_t P, bool bf16, si
   size_t o_xv = bf16 ? 0 : take(sizeof(float) * B * L * 2 * P);
   size_t o_bt = 0, o_c16 = 0, o_vx16 = 0;
   if (bf16) {
-    o_bt = take(sizeof(float) * 2 * P * H);
+    o_bt = take(2 * 2 * P * H);
     o_c16 = take(2 * H * 2 * P);
     o_vx16 = take(2 * B * L * 2 * P);
   }
@@ -416,7 +417,7 @@ S5Work carve(void* ws, int64_t B, int64_t L, int64_t H, int64_t P, bool bf16, si
   w.S = reinterpret_cast<float2*>(base + o_S);
   w.Xin = reinterpret_cast<float2*>(base + o_X);
   w.xv = bf16 ? nullptr : reinterpret_cast<float*>(base + o_xv);
-  w.bbar_t = bf16 ? reinterpret_cast<float*>(base + o_bt) : nullptr;
+  w.bbar_t16 = bf16 ? base + o_bt : nullptr;
   w.cmat_t16 = bf16 ? base + o_c16 : nullptr;
   w.vx16 = bf16 ? base + o_vx16 : nullptr;
   return w;
@@ -430,8 +431,8 @@ size_t s5_workspace_bytes(int64_t B, int64_t L, int64_t H, int64_t P, bool bf16)
   return total;
 }
 
-cudaError_t launch_tc_gemm(const void* A, const void* B, bool tf32, void* C, bool c_bf16, int M,
-                           int N, int K, const float* D, const float* E, int* status,
+cudaError_t launch_tc_gemm(const void* A, bool a_f32, const void* B, void* C, bool c_bf16,
+                           int M, int N, int K, const float* D, const float* E, int* status,
                            cudaStream_t s);
 
 // The chunked diagonal scan shared by both tiers: V -> x in place, in w.xv (float32 tier) or
@@ -470,13 +471,14 @@ cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delt
     gemm_f32<<<g2, 256, 0, s>>>(w.xv, w.cmat, y, M, H, 2 * P, D, u);
     return cudaGetLastError();
   }
-  // tensor cores with f32 accumulation: tf32 input projection straight from u into bf16 V, the
-  // scan in f32 arithmetic writing bf16 x over V, bf16 output projection
-  if ((e = launch_tc_gemm(u, w.bbar_t, true, w.vx16, true, M, 2 * P, H, nullptr, nullptr, status,
-                          s)) != cudaSuccess)
+  // tensor cores with f32 accumulation: the input projection reads the float32 u (converted to
+  // bf16 in the kernel) and writes bf16 V, the scan in f32 arithmetic writes bf16 x over V, the
+  // output projection adds D (.) u
+  if ((e = launch_tc_gemm(u, true, w.bbar_t16, w.vx16, true, M, 2 * P, H, nullptr, nullptr,
+                          status, s)) != cudaSuccess)
     return e;
   if ((e = s5_scan_xv(w, B, L, P, true, s)) != cudaSuccess) return e;
-  return launch_tc_gemm(w.vx16, w.cmat_t16, false, y, false, M, H, 2 * P, D, u, status, s);
+  return launch_tc_gemm(w.vx16, false, w.cmat_t16, y, false, M, H, 2 * P, D, u, status, s);
 }
 
 }  // namespace dlr

@@ -1,23 +1,26 @@
-// tc_gemm.cu -- C[M, N] (f32 or bf16) = A[M, K] * B[N, K]^T (+ D[n] * E[m, n]) on 5th-generation tensor
-// cores: bf16 operands (kind::f16) or float32 operands read as tf32 (kind::tf32) in shared
-// memory (TMA tile loads, 128-byte swizzle), f32 accumulators in tensor memory, tcgen05.mma
-// issued by one thread, tcgen05.ld epilogue with TMA tile stores.
+// tc_gemm.cu -- C[M, N] (f32 or bf16) = A[M, K] * B[N, K]^T (+ D[n] * E[m, n]) on 5th-generation
+// tensor cores: bf16 operands in shared memory (TMA tile loads, 128-byte swizzle; a float32 A
+// is converted to bf16 in the kernel), f32 accumulators in tensor memory, tcgen05.mma
+// (kind::f16) issued by one thread, tcgen05.ld epilogue with TMA tile stores.
 //
 // Persistent: one CTA per SM walks the 128 x 256 output tiles t = blockIdx.x, + gridDim.x, ...
 // with the N tile varying fastest (the CTAs working on the N tiles of one M tile at the same
-// time share its A rows through L2). Eight warps:
-//   warp 0 lane 0  TMA producer: K-blocks of 128 bytes per row (64 bf16 or 32 float32) into a
-//                  ring of 3 or 4 stages (A 16 KB + B 32 KB), running ahead across tiles,
-//   warp 1 lane 0  MMA issuer: four MMAs of 32 bytes of K (K = 16 bf16 or 8 tf32) per K-block,
-//                  a commit that frees the stage, and
+// time share its A rows through L2). Warps:
+//   warp 0 lane 0  TMA producer: K-blocks of 64 into a ring of 2-4 stages (A 16 KB + B 32 KB),
+//                  running ahead across tiles. With a float32 A it loads only A, as float32
+//                  (two 16 KB boxes per K-block), into a 3-slot staging ring, and
+//   warp 3 lane 0  loads B into the ring,
+//   warps 8-11     (float32 A only) convert: thread = row of the tile, 64 float32 of its row
+//                  from the staging slot to 64 bf16 in the operand layout of the ring,
+//   warp 1 lane 0  MMA issuer: four K=16 MMAs per K-block, a commit that frees the stage, and
 //                  per tile a commit that hands one of two TMEM accumulators to the epilogue,
 //   warp 2         allocates / frees the 512 TMEM columns (two 256-column accumulators),
 //   warps 4-7      epilogue: warp 4+q owns TMEM lanes 32q..32q+31 (rows of the tile). Per slice
 //                  of 128 output bytes per row (32 f32 or 64 bf16 columns): tcgen05.ld, + D (.) E
 //                  with the E box brought in by TMA, into a 4 KB staging box (128-byte swizzle),
-//                  out by one TMA store per warp. The
-//                  boxes of a warp rotate: the E loads of the next two slices and the stores of
-//                  the last one or two are in flight while the current slice is worked on.
+//                  out by one TMA store per warp. The boxes of a warp rotate: the E loads of the
+//                  next two slices and the stores of the last one or two are in flight while the
+//                  current slice is worked on.
 // While the epilogue drains one accumulator the MMAs of the next tile fill the other.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -38,19 +41,28 @@ constexpr uint32_t kABytes = kBM * kRowBytes, kBBytes = kBN * kRowBytes;
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kBoxBytes = 32 * 128;  // 32 rows x 128 bytes
 
+// Operand modes, both kind::f16 with bf16 operands: A and B bf16 in global memory; or A
+// float32 in global memory, converted to bf16 in shared memory by four converter warps.
+enum OpMode { kOpBf16 = 0, kOpCvtA = 1 };
+
 // Shared-memory plan. With E the epilogue keeps four boxes per warp (two E loads ahead) and
-// the ring three stages; without E two boxes suffice and the ring gets a fourth stage.
-template <bool kWithE>
+// the ring three stages; without E two boxes suffice and the ring gets a fourth stage. With a
+// converted A the ring has two stages and a three-slot float32 staging ring (32 KB a slot)
+// feeds the converters.
+template <bool kWithE, bool kCvt>
 struct Plan {
-  static constexpr int kStages = kWithE ? 3 : 4;
+  static constexpr int kStages = kCvt ? 2 : (kWithE ? 3 : 4);
+  static constexpr int kFStages = kCvt ? 3 : 0;
+  static constexpr uint32_t kFBytes = kBM * 2 * kRowBytes;  // 128 rows x 64 float32
   static constexpr int kBoxes = kWithE ? 4 : 2;
-  static constexpr uint32_t kEpiOff = kStages * kStageBytes;
+  static constexpr uint32_t kFOff = kStages * kStageBytes;
+  static constexpr uint32_t kEpiOff = kFOff + kFStages * kFBytes;
   static constexpr uint32_t kBarOff = kEpiOff + 4 * kBoxes * kBoxBytes;
   static constexpr size_t kSmemBytes = 1024 + kBarOff + 256;
+  static constexpr int kThreads = kCvt ? 384 : 256;
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
 constexpr uint32_t kTmemCols = 512;
-constexpr int kThreads = 256;
 
 struct GemmArgs {
   int M, N, K;
@@ -63,30 +75,36 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity)) != 0;
 }
 
-template <bool kTf32, bool kWithE, bool kBf16Out>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int kOp, bool kWithE, bool kBf16Out>
+__global__ void __launch_bounds__(Plan<kWithE, kOp == kOpCvtA>::kThreads, 1)
 tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmE,
              GemmArgs g) {
   static_assert(!(kWithE && kBf16Out), "D (.) E is added to f32 outputs only");
-  constexpr int kStages = Plan<kWithE>::kStages, kBoxes = Plan<kWithE>::kBoxes;
+  static_assert(!(kWithE && kOp == kOpCvtA), "no plan for E with a converted A");
+  constexpr bool kCvt = kOp == kOpCvtA;
+  using PL = Plan<kWithE, kCvt>;
+  constexpr int kStages = PL::kStages, kBoxes = PL::kBoxes, kF = PL::kFStages;
   constexpr int kSlice = kBf16Out ? 64 : 32;  // output columns per slice (128 bytes per row)
   constexpr int kSlices = kBN / kSlice;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(base + Plan<kWithE>::kBarOff);
-  uint64_t* full = bars;                       // [kStages]  operands landed
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + PL::kBarOff);
+  uint64_t* full = bars;                       // [kStages]  operands (B only with kCvt) landed
   uint64_t* empty = bars + kStages;            // [kStages]  operands consumed by the MMAs
   uint64_t* acc_full = bars + 2 * kStages;     // [2]        accumulator complete
   uint64_t* acc_empty = acc_full + 2;          // [2]        accumulator read out (4 arrivals)
   uint64_t* e_full = acc_empty + 2;            // [4][kBoxes] E box landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(e_full + 4 * kBoxes);
+  uint64_t* a_ready = e_full + 4 * kBoxes;     // [kStages]  converted A written (4 arrivals)
+  uint64_t* f_full = a_ready + kStages;        // [kF]       float32 A slot landed
+  uint64_t* f_empty = f_full + kF;             // [kF]       float32 A slot read (4 arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(f_empty + kF);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = (g.N + kBN - 1) / kBN;
   const int tiles = n_tiles * ((g.M + kBM - 1) / kBM);
-  constexpr int kBK = kTf32 ? kRowBytes / 4 : kRowBytes / 2;  // K elements per stage
+  constexpr int kBK = kRowBytes / 2;  // K elements (bf16) per stage
   const int nk = (g.K + kBK - 1) / kBK;
   constexpr bool with_e = kWithE;
 
@@ -100,6 +118,11 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
       tc::mbar_init(&acc_empty[a], 4);
     }
     for (int i = 0; i < 4 * kBoxes; ++i) tc::mbar_init(&e_full[i], 1);
+    for (int s = 0; s < kStages; ++s) tc::mbar_init(&a_ready[s], 4);
+    for (int s = 0; s < kF; ++s) {
+      tc::mbar_init(&f_full[s], 1);
+      tc::mbar_init(&f_empty[s], 4);
+    }
     tc::mbar_fence_init();
   }
   if (warp == 2) {
@@ -113,23 +136,101 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
   bool ok = true;
 
   if (warp == 0 && lane == 0) {
-    uint32_t it = 0;
-    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-      const int m0 = (t / n_tiles) * kBM, n0 = (t % n_tiles) * kBN;
-      for (int kb = 0; kb < nk; ++kb, ++it) {
-        const int s = it % kStages;
-        if (it >= kStages && !(ok = tc::mbar_wait(&empty[s], ((it / kStages) - 1) & 1))) break;
-        uint8_t* a = base + s * kStageBytes;
-        tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
-        tc::tma_load_2d(a, &tmA, kb * kBK, m0, &full[s]);
-        tc::tma_load_2d(a + kABytes, &tmB, kb * kBK, n0, &full[s]);
+    if constexpr (!kCvt) {
+      uint32_t it = 0;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int m0 = (t / n_tiles) * kBM, n0 = (t % n_tiles) * kBN;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % kStages;
+          if (it >= kStages && !(ok = tc::mbar_wait(&empty[s], ((it / kStages) - 1) & 1))) break;
+          uint8_t* a = base + s * kStageBytes;
+          tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
+          tc::tma_load_2d(a, &tmA, kb * kBK, m0, &full[s]);
+          tc::tma_load_2d(a + kABytes, &tmB, kb * kBK, n0, &full[s]);
+        }
+      }
+      // before the CTA may exit, every copy it issued has landed (normally long since consumed)
+      for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j)
+        ok &= tc::mbar_wait(&full[j % kStages], (j / kStages) & 1);
+    } else {
+      // converted A: float32 K-blocks of 64 (two 128-byte boxes) into the staging ring
+      uint8_t* fst = base + PL::kFOff;
+      uint32_t it = 0;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int m0 = (t / n_tiles) * kBM;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int fs = it % kF;
+          if (it >= kF && !(ok = tc::mbar_wait(&f_empty[fs], ((it / kF) - 1) & 1))) break;
+          uint8_t* f = fst + fs * PL::kFBytes;
+          tc::mbar_arrive_expect_tx(&f_full[fs], PL::kFBytes);
+          tc::tma_load_2d(f, &tmA, kb * kBK, m0, &f_full[fs]);
+          tc::tma_load_2d(f + PL::kFBytes / 2, &tmA, kb * kBK + kBK / 2, m0, &f_full[fs]);
+        }
+      }
+      for (uint32_t j = it > kF ? it - kF : 0; j < it; ++j)
+        ok &= tc::mbar_wait(&f_full[j % kF], (j / kF) & 1);
+    }
+  } else if (warp == 3 && lane == 0) {
+    if constexpr (kCvt) {
+      // converted A: the B operand into the ring
+      uint32_t it = 0;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const int n0 = (t % n_tiles) * kBN;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % kStages;
+          if (it >= kStages && !(ok = tc::mbar_wait(&empty[s], ((it / kStages) - 1) & 1))) break;
+          tc::mbar_arrive_expect_tx(&full[s], kBBytes);
+          tc::tma_load_2d(base + s * kStageBytes + kABytes, &tmB, kb * kBK, n0, &full[s]);
+        }
+      }
+      for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j)
+        ok &= tc::mbar_wait(&full[j % kStages], (j / kStages) & 1);
+    }
+  } else if (warp >= 8) {
+    if constexpr (kCvt) {
+      // converters: thread = row r of the tile; 64 float32 of row r -> 64 bf16 in the K-major
+      // 128-byte-swizzled layout the MMA reads (16-byte chunk c of row r at (c ^ (r & 7)) << 4)
+      const int r = (warp - 8) * 32 + lane;
+      const uint32_t sw = uint32_t(r & 7);
+      uint8_t* fst = base + PL::kFOff;
+      uint32_t it = 0;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        for (int kb = 0; kb < nk && ok; ++kb, ++it) {
+          const int fs = it % kF, s = it % kStages;
+          if (!(ok = warp_wait(&f_full[fs], (it / kF) & 1))) break;
+          const uint8_t* f = fst + fs * PL::kFBytes + r * kRowBytes;
+          float4 v[16];
+  #pragma unroll
+          for (int c = 0; c < 16; ++c)
+            v[c] = *reinterpret_cast<const float4*>(f + (c >> 3) * (PL::kFBytes / 2) +
+                                                    (((uint32_t(c) & 7u) ^ sw) << 4));
+          uint4 h[8];
+  #pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const __nv_bfloat162 b0 = __floats2bfloat162_rn(v[2 * c].x, v[2 * c].y);
+            const __nv_bfloat162 b1 = __floats2bfloat162_rn(v[2 * c].z, v[2 * c].w);
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * c + 1].x, v[2 * c + 1].y);
+            const __nv_bfloat162 b3 = __floats2bfloat162_rn(v[2 * c + 1].z, v[2 * c + 1].w);
+            h[c] = make_uint4(*reinterpret_cast<const uint32_t*>(&b0),
+                              *reinterpret_cast<const uint32_t*>(&b1),
+                              *reinterpret_cast<const uint32_t*>(&b2),
+                              *reinterpret_cast<const uint32_t*>(&b3));
+          }
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&f_empty[fs]);  // the slot's values are in registers
+          if (it >= kStages && !(ok = warp_wait(&empty[s], ((it / kStages) - 1) & 1))) break;
+          uint8_t* a = base + s * kStageBytes + r * kRowBytes;
+  #pragma unroll
+          for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(a + ((uint32_t(c) ^ sw) << 4)) = h[c];
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&a_ready[s]);
+        }
       }
     }
-    // before the CTA may exit, every copy it issued has landed (normally long since consumed)
-    for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j)
-      ok &= tc::mbar_wait(&full[j % kStages], (j / kStages) & 1);
   } else if (warp == 1 && lane == 0) {
-    constexpr uint32_t idesc = kTf32 ? tc::idesc_tf32_f32(kBM, kBN) : tc::idesc_bf16_f32(kBM, kBN);
+    constexpr uint32_t idesc = tc::idesc_bf16_f32(kBM, kBN);
     uint32_t it = 0, local = 0;
     for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++local) {
       const uint32_t acc = local & 1;
@@ -139,24 +240,21 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
       for (int kb = 0; kb < nk; ++kb, ++it) {
         const int s = it % kStages;
         if (!(ok = tc::mbar_wait(&full[s], (it / kStages) & 1))) break;
+        if (kCvt && !(ok = tc::mbar_wait(&a_ready[s], (it / kStages) & 1))) break;
         tc::fence_after_sync();
         const uint8_t* a = base + s * kStageBytes;
         const uint64_t ad = tc::smem_desc_k_sw128(a);
         const uint64_t bd = tc::smem_desc_k_sw128(a + kABytes);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {  // advance 32 bytes of K = 2 descriptor units
-          if (kTf32)
-            tc::mma_kind_tf32(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
-          else
-            tc::mma_kind_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
-        }
+        for (int kk = 0; kk < 4; ++kk)  // advance 16 bf16 = 32 bytes = 2 descriptor units
+          tc::mma_kind_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
         tc::mma_commit(&empty[s]);
       }
       tc::mma_commit(&acc_full[acc]);
     }
   } else if (warp >= 4) {
     const int q = warp - 4;
-    uint8_t* boxes = base + Plan<kWithE>::kEpiOff + q * kBoxes * kBoxBytes;
+    uint8_t* boxes = base + PL::kEpiOff + q * kBoxes * kBoxBytes;
     uint64_t* ebar = e_full + q * kBoxes;
     const uint32_t sw = uint32_t(lane & 7);
     // the slices this warp walks: (tile, column block), tiles in the CTA's order
@@ -286,13 +384,14 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kTf32, bool kWithE, bool kBf16Out>
+template <int kOp, bool kWithE, bool kBf16Out>
 cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                      const CUtensorMap& me, const GemmArgs& g, int grid, cudaStream_t s) {
-  constexpr size_t smem = Plan<kWithE>::kSmemBytes;
-  cudaError_t e = max_smem_once<tc_gemm<kTf32, kWithE, kBf16Out>>(smem);
+  using PL = Plan<kWithE, kOp == kOpCvtA>;
+  constexpr size_t smem = PL::kSmemBytes;
+  cudaError_t e = max_smem_once<tc_gemm<kOp, kWithE, kBf16Out>>(smem);
   if (e != cudaSuccess) return e;
-  tc_gemm<kTf32, kWithE, kBf16Out><<<grid, kThreads, smem, s>>>(ma, mb, mc, me, g);
+  tc_gemm<kOp, kWithE, kBf16Out><<<grid, PL::kThreads, smem, s>>>(ma, mb, mc, me, g);
   return cudaGetLastError();
 }
 
@@ -315,30 +414,28 @@ cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t
   return cudaGetLastError();
 }
 
-// A: [M, K] row-major; B: [N, K] row-major, both bf16 (tf32 false) or both float32 (tf32
-// true); C: [M, N], f32 or (c_bf16, no D) bf16; D: f32 [N] or null; E: f32 [M, N] (read only
-// when D is given).
-cudaError_t launch_tc_gemm(const void* A, const void* B, bool tf32, void* C, bool c_bf16, int M,
-                           int N, int K, const float* D, const float* E, int* status,
+// A: [M, K] row-major, bf16 (a_f32 false) or float32 (a_f32, converted to bf16 in the
+// kernel); B: bf16 [N, K] row-major. C: [M, N], f32 or (c_bf16, no D) bf16; D: f32 [N] or
+// null; E: f32 [M, N] (read only when D is given; not with a float32 A).
+cudaError_t launch_tc_gemm(const void* A, bool a_f32, const void* B, void* C, bool c_bf16,
+                           int M, int N, int K, const float* D, const float* E, int* status,
                            cudaStream_t s) {
-  if (M < 1 || N < 1 || K < 1 || (c_bf16 && D)) return cudaErrorInvalidValue;
+  if (M < 1 || N < 1 || K < 1 || (c_bf16 && D) || (a_f32 && D)) return cudaErrorInvalidValue;
   CUtensorMap ma, mb, mc, me;
-  if (!make_map(&ma, A, (uint64_t)M, (uint64_t)K, kBM, tf32)) return cudaErrorInvalidValue;
-  if (!make_map(&mb, B, (uint64_t)N, (uint64_t)K, kBN, tf32)) return cudaErrorInvalidValue;
+  if (!make_map(&ma, A, (uint64_t)M, (uint64_t)K, kBM, a_f32)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, B, (uint64_t)N, (uint64_t)K, kBN, false)) return cudaErrorInvalidValue;
   if (!make_map(&mc, C, (uint64_t)M, (uint64_t)N, 32, !c_bf16)) return cudaErrorInvalidValue;
   if (D && !make_map(&me, E, (uint64_t)M, (uint64_t)N, 32, true)) return cudaErrorInvalidValue;
   if (!D) me = mc;  // not read
   GemmArgs g{M, N, K, D, status};
   const long long tiles = (long long)((N + kBN - 1) / kBN) * ((M + kBM - 1) / kBM);
   const int grid = (int)std::min<long long>(tiles, sm_count());
-  if (D)
-    return tf32 ? run_gemm<true, true, false>(ma, mb, mc, me, g, grid, s)
-                : run_gemm<false, true, false>(ma, mb, mc, me, g, grid, s);
+  if (D) return run_gemm<kOpBf16, true, false>(ma, mb, mc, me, g, grid, s);
   if (c_bf16)
-    return tf32 ? run_gemm<true, false, true>(ma, mb, mc, me, g, grid, s)
-                : run_gemm<false, false, true>(ma, mb, mc, me, g, grid, s);
-  return tf32 ? run_gemm<true, false, false>(ma, mb, mc, me, g, grid, s)
-              : run_gemm<false, false, false>(ma, mb, mc, me, g, grid, s);
+    return a_f32 ? run_gemm<kOpCvtA, false, true>(ma, mb, mc, me, g, grid, s)
+                 : run_gemm<kOpBf16, false, true>(ma, mb, mc, me, g, grid, s);
+  return a_f32 ? run_gemm<kOpCvtA, false, false>(ma, mb, mc, me, g, grid, s)
+               : run_gemm<kOpBf16, false, false>(ma, mb, mc, me, g, grid, s);
 }
 
 }  // namespace dlr
