@@ -434,10 +434,16 @@ size_t s5_workspace_bytes(int64_t B, int64_t L, int64_t H, int64_t P, bool bf16)
 cudaError_t launch_tc_gemm(const void* A, bool a_f32, const void* B, void* C, bool c_bf16,
                            int M, int N, int K, const float* D, const float* E, int* status,
                            cudaStream_t s);
+cudaError_t launch_tc_gemm_apply(const void* V, const void* C, float* y, int M, int N, int K,
+                                 const float* D, const float* E, const float2* lam,
+                                 const float2* xin, int L, int P, int NC, int* status,
+                                 cudaStream_t s);
 
 // The chunked diagonal scan shared by both tiers: V -> x in place, in w.xv (float32 tier) or
-// w.vx16 (tensor-core tier).
-static cudaError_t s5_scan_xv(const S5Work& w, int B, int L, int P, bool bf16, cudaStream_t s) {
+// w.vx16 (tensor-core tier). Without `apply` it stops after the carries (the tensor-core
+// output projection runs the apply step on its operand tiles).
+static cudaError_t s5_scan_xv(const S5Work& w, int B, int L, int P, bool bf16, bool apply,
+                              cudaStream_t s) {
   const int NC = (L + kT - 1) / kT;
   const int threads = P < 256 ? P : 256;  // P is a multiple of 32
   const long long quads = (long long)B * NC * (P / 4);
@@ -447,6 +453,7 @@ static cudaError_t s5_scan_xv(const S5Work& w, int B, int L, int P, bool bf16, c
   else
     s5_chunk_state<<<dim3(NC, B), threads, 0, s>>>(w, L, P, NC);
   s5_carry<<<(B * P + 7) / 8, 256, 0, s>>>(w, B, P, NC);
+  if (!apply) return cudaGetLastError();
   if (bf16)
     s5_chunk16<true><<<grid16, 256, 0, s>>>(w, B, L, P, NC);
   else
@@ -465,19 +472,25 @@ cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delt
   if (!bf16) {
     dim3 g1((2 * P + kGN - 1) / kGN, (M + kGM - 1) / kGM);
     gemm_f32<<<g1, 256, 0, s>>>(u, w.bbar, w.xv, M, 2 * P, H, nullptr, nullptr);
-    e = s5_scan_xv(w, B, L, P, false, s);
+    e = s5_scan_xv(w, B, L, P, false, true, s);
     if (e != cudaSuccess) return e;
     dim3 g2((H + kGN - 1) / kGN, (M + kGM - 1) / kGM);
     gemm_f32<<<g2, 256, 0, s>>>(w.xv, w.cmat, y, M, H, 2 * P, D, u);
     return cudaGetLastError();
   }
   // tensor cores with f32 accumulation: the input projection reads the float32 u (converted to
-  // bf16 in the kernel) and writes bf16 V, the scan in f32 arithmetic writes bf16 x over V, the
-  // output projection adds D (.) u
+  // bf16 in the kernel) and writes bf16 V, the scan in f32 arithmetic, the output projection
+  // adds D (.) u. When L is a multiple of 64 (tiles of 128 steps start on chunk starts) the
+  // output projection turns V into x itself as its operand tiles arrive; otherwise the apply
+  // kernel writes bf16 x over V first.
   if ((e = launch_tc_gemm(u, true, w.bbar_t16, w.vx16, true, M, 2 * P, H, nullptr, nullptr,
                           status, s)) != cudaSuccess)
     return e;
-  if ((e = s5_scan_xv(w, B, L, P, true, s)) != cudaSuccess) return e;
+  const bool fused = L % kT == 0;
+  if ((e = s5_scan_xv(w, B, L, P, true, !fused, s)) != cudaSuccess) return e;
+  if (fused)
+    return launch_tc_gemm_apply(w.vx16, w.cmat_t16, y, M, H, 2 * P, D, u, w.lbar_pw + P, w.Xin,
+                                L, P, (L + kT - 1) / kT, status, s);
   return launch_tc_gemm(w.vx16, false, w.cmat_t16, y, false, M, H, 2 * P, D, u, status, s);
 }
 

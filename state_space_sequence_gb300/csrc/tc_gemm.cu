@@ -41,16 +41,22 @@ constexpr uint32_t kABytes = kBM * kRowBytes, kBBytes = kBN * kRowBytes;
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr uint32_t kBoxBytes = 32 * 128;  // 32 rows x 128 bytes
 
-// Operand modes, both kind::f16 with bf16 operands: A and B bf16 in global memory; or A
-// float32 in global memory, converted to bf16 in shared memory by four converter warps.
-enum OpMode { kOpBf16 = 0, kOpCvtA = 1 };
+// Operand modes, all kind::f16 with bf16 operands in shared memory:
+//   kOpBf16   A and B bf16 in global memory;
+//   kOpCvtA   A float32 in global memory, converted to bf16 by four converter warps;
+//   kOpApply  A = the chunked scan's per-step input V (bf16), turned in place into the states
+//             x_t = lambda x_{t-1} + V_t (restarting from the carried state at every chunk of
+//             64 steps) by two converter warps per ring stage (one per chunk) before the MMAs
+//             read it.
+enum OpMode { kOpBf16 = 0, kOpCvtA = 1, kOpApply = 2 };
 
 // Shared-memory plan. With E the epilogue keeps four boxes per warp (two E loads ahead) and
 // the ring three stages; without E two boxes suffice and the ring gets a fourth stage. With a
 // converted A the ring has two stages and a three-slot float32 staging ring (32 KB a slot)
 // feeds the converters.
-template <bool kWithE, bool kCvt>
+template <bool kWithE, int kOp>
 struct Plan {
+  static constexpr bool kCvt = kOp == kOpCvtA;
   static constexpr int kStages = kCvt ? 2 : (kWithE ? 3 : 4);
   static constexpr int kFStages = kCvt ? 3 : 0;
   static constexpr uint32_t kFBytes = kBM * 2 * kRowBytes;  // 128 rows x 64 float32
@@ -59,7 +65,7 @@ struct Plan {
   static constexpr uint32_t kEpiOff = kFOff + kFStages * kFBytes;
   static constexpr uint32_t kBarOff = kEpiOff + 4 * kBoxes * kBoxBytes;
   static constexpr size_t kSmemBytes = 1024 + kBarOff + 256;
-  static constexpr int kThreads = kCvt ? 384 : 256;
+  static constexpr int kThreads = kOp == kOpBf16 ? 256 : (kOp == kOpCvtA ? 384 : 448);
   static_assert(kSmemBytes <= 232448, "shared memory");
 };
 constexpr uint32_t kTmemCols = 512;
@@ -68,6 +74,11 @@ struct GemmArgs {
   int M, N, K;
   const float* D;  // [N] or null (then E is not read)
   int* status;
+  // kOpApply: lambda per state, the state entering each chunk [B][NC][P], sequence length
+  // (a multiple of 64), states P (A has K = 2P columns: Re, Im per state), chunks per row
+  const float2* lam;
+  const float2* xin;
+  int L, P, NC;
 };
 
 // Bounded wait by a whole warp with one verdict for all its lanes.
@@ -76,14 +87,14 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
 }
 
 template <int kOp, bool kWithE, bool kBf16Out>
-__global__ void __launch_bounds__(Plan<kWithE, kOp == kOpCvtA>::kThreads, 1)
+__global__ void __launch_bounds__(Plan<kWithE, kOp>::kThreads, 1)
 tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
              const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmE,
              GemmArgs g) {
   static_assert(!(kWithE && kBf16Out), "D (.) E is added to f32 outputs only");
   static_assert(!(kWithE && kOp == kOpCvtA), "no plan for E with a converted A");
-  constexpr bool kCvt = kOp == kOpCvtA;
-  using PL = Plan<kWithE, kCvt>;
+  constexpr bool kCvt = kOp == kOpCvtA, kApply = kOp == kOpApply;
+  using PL = Plan<kWithE, kOp>;
   constexpr int kStages = PL::kStages, kBoxes = PL::kBoxes, kF = PL::kFStages;
   constexpr int kSlice = kBf16Out ? 64 : 32;  // output columns per slice (128 bytes per row)
   constexpr int kSlices = kBN / kSlice;
@@ -118,7 +129,7 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
       tc::mbar_init(&acc_empty[a], 4);
     }
     for (int i = 0; i < 4 * kBoxes; ++i) tc::mbar_init(&e_full[i], 1);
-    for (int s = 0; s < kStages; ++s) tc::mbar_init(&a_ready[s], 4);
+    for (int s = 0; s < kStages; ++s) tc::mbar_init(&a_ready[s], kCvt ? 4 : 2);
     for (int s = 0; s < kF; ++s) {
       tc::mbar_init(&f_full[s], 1);
       tc::mbar_init(&f_empty[s], 4);
@@ -200,12 +211,12 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
           if (!(ok = warp_wait(&f_full[fs], (it / kF) & 1))) break;
           const uint8_t* f = fst + fs * PL::kFBytes + r * kRowBytes;
           float4 v[16];
-  #pragma unroll
+#pragma unroll
           for (int c = 0; c < 16; ++c)
             v[c] = *reinterpret_cast<const float4*>(f + (c >> 3) * (PL::kFBytes / 2) +
                                                     (((uint32_t(c) & 7u) ^ sw) << 4));
           uint4 h[8];
-  #pragma unroll
+#pragma unroll
           for (int c = 0; c < 8; ++c) {
             const __nv_bfloat162 b0 = __floats2bfloat162_rn(v[2 * c].x, v[2 * c].y);
             const __nv_bfloat162 b1 = __floats2bfloat162_rn(v[2 * c].z, v[2 * c].w);
@@ -220,12 +231,72 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
           if (lane == 0) tc::mbar_arrive(&f_empty[fs]);  // the slot's values are in registers
           if (it >= kStages && !(ok = warp_wait(&empty[s], ((it / kStages) - 1) & 1))) break;
           uint8_t* a = base + s * kStageBytes + r * kRowBytes;
-  #pragma unroll
+#pragma unroll
           for (int c = 0; c < 8; ++c)
             *reinterpret_cast<uint4*>(a + ((uint32_t(c) ^ sw) << 4)) = h[c];
           tc::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&a_ready[s]);
+        }
+      }
+    } else if constexpr (kApply) {
+      // warps 8 + 2s and 9 + 2s own ring stage s (so each waits every phase of its barriers in
+      // order), one chunk of 64 rows each: tiles start on chunk starts (L a multiple of 64), so
+      // rows 0 and 64 of a tile begin chunks and take the carried state. Lane j holds state
+      // p = 32 kb + j: the 4 bytes (Re, Im in bf16) at byte 4 (j & 3) of 16-byte chunk j >> 2
+      // of every row. The carried state and lambda of the warp's next stage are fetched while
+      // it works on the current one.
+      const int s = (warp - 8) >> 1, h = (warp - 8) & 1;
+      if (s < kStages) {
+        const uint32_t sub = uint32_t(lane & 3) * 4u, chunk = uint32_t(lane >> 2);
+        // carried state and lambda for ring iteration it (zero where the rows or states end)
+        auto fetch = [&](uint32_t it, cf& lam, cf& x) {
+          lam = {0.f, 0.f};
+          x = {0.f, 0.f};
+          const int tt = blockIdx.x + int(it / nk) * gridDim.x, kb = int(it % nk);
+          if (tt >= tiles) return;
+          const int m = (tt / n_tiles) * kBM + h * 64, p = kb * 32 + lane;
+          if (m >= g.M || p >= g.P) return;
+          const int b = m / g.L, t = m - b * g.L;
+          const float2 l = g.lam[p], v = g.xin[((size_t)b * g.NC + (t >> 6)) * g.P + p];
+          lam = {l.x, l.y};
+          x = {v.x, v.y};
+        };
+        const uint32_t total = uint32_t((tiles - int(blockIdx.x) + int(gridDim.x) - 1) /
+                                        int(gridDim.x)) * uint32_t(nk);
+        cf lam, x, lam_n, x_n;
+        fetch(uint32_t(s), lam, x);
+        for (uint32_t it = uint32_t(s); it < total && ok; it += kStages) {
+          fetch(it + kStages, lam_n, x_n);
+          if (!(ok = warp_wait(&full[s], (it / kStages) & 1))) break;
+          const int m0 = (blockIdx.x + int(it / nk) * gridDim.x) / n_tiles * kBM + h * 64;
+          const int rows = min(64, g.M - m0);
+          uint8_t* a = base + s * kStageBytes;
+#pragma unroll 1
+          for (int i0 = h * 64; i0 < h * 64 + rows; i0 += 16) {
+            uint32_t* ptr[16];
+            uint32_t v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int i = i0 + j;
+              ptr[j] = reinterpret_cast<uint32_t*>(a + i * kRowBytes +
+                                                   ((chunk ^ uint32_t(i & 7)) << 4) + sub);
+              v[j] = *ptr[j];
+            }
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float2 vf =
+                  __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v[j]));
+              x = cfma(lam, x, {vf.x, vf.y});
+              const __nv_bfloat162 hx = __floats2bfloat162_rn(x.re, x.im);
+              if (i0 + j < h * 64 + rows) *ptr[j] = *reinterpret_cast<const uint32_t*>(&hx);
+            }
+          }
+          tc::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&a_ready[s]);
+          lam = lam_n;
+          x = x_n;
         }
       }
     }
@@ -240,7 +311,7 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
       for (int kb = 0; kb < nk; ++kb, ++it) {
         const int s = it % kStages;
         if (!(ok = tc::mbar_wait(&full[s], (it / kStages) & 1))) break;
-        if (kCvt && !(ok = tc::mbar_wait(&a_ready[s], (it / kStages) & 1))) break;
+        if ((kCvt || kApply) && !(ok = tc::mbar_wait(&a_ready[s], (it / kStages) & 1))) break;
         tc::fence_after_sync();
         const uint8_t* a = base + s * kStageBytes;
         const uint64_t ad = tc::smem_desc_k_sw128(a);
@@ -387,7 +458,7 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uin
 template <int kOp, bool kWithE, bool kBf16Out>
 cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                      const CUtensorMap& me, const GemmArgs& g, int grid, cudaStream_t s) {
-  using PL = Plan<kWithE, kOp == kOpCvtA>;
+  using PL = Plan<kWithE, kOp>;
   constexpr size_t smem = PL::kSmemBytes;
   cudaError_t e = max_smem_once<tc_gemm<kOp, kWithE, kBf16Out>>(smem);
   if (e != cudaSuccess) return e;
@@ -427,7 +498,7 @@ cudaError_t launch_tc_gemm(const void* A, bool a_f32, const void* B, void* C, bo
   if (!make_map(&mc, C, (uint64_t)M, (uint64_t)N, 32, !c_bf16)) return cudaErrorInvalidValue;
   if (D && !make_map(&me, E, (uint64_t)M, (uint64_t)N, 32, true)) return cudaErrorInvalidValue;
   if (!D) me = mc;  // not read
-  GemmArgs g{M, N, K, D, status};
+  GemmArgs g{M, N, K, D, status, nullptr, nullptr, 0, 0, 0};
   const long long tiles = (long long)((N + kBN - 1) / kBN) * ((M + kBM - 1) / kBM);
   const int grid = (int)std::min<long long>(tiles, sm_count());
   if (D) return run_gemm<kOpBf16, true, false>(ma, mb, mc, me, g, grid, s);
@@ -436,6 +507,26 @@ cudaError_t launch_tc_gemm(const void* A, bool a_f32, const void* B, void* C, bo
                  : run_gemm<kOpBf16, false, true>(ma, mb, mc, me, g, grid, s);
   return a_f32 ? run_gemm<kOpCvtA, false, false>(ma, mb, mc, me, g, grid, s)
                : run_gemm<kOpBf16, false, false>(ma, mb, mc, me, g, grid, s);
+}
+
+// The S5 output projection with the chunked scan's last step fused in: V bf16 [M = B L, K = 2P]
+// (Re, Im per state), L a multiple of 64; x_t = lambda x_{t-1} + V_t inside each chunk of 64
+// steps, starting from xin[b][c][p] (the state entering the chunk); y = x C^T + D (.) E with C
+// bf16 [N, K] and E, y float32 [M, N].
+cudaError_t launch_tc_gemm_apply(const void* V, const void* C, float* y, int M, int N, int K,
+                                 const float* D, const float* E, const float2* lam,
+                                 const float2* xin, int L, int P, int NC, int* status,
+                                 cudaStream_t s) {
+  if (M < 1 || N < 1 || K != 2 * P || L % 64 || !D || !E) return cudaErrorInvalidValue;
+  CUtensorMap ma, mb, mc, me;
+  if (!make_map(&ma, V, (uint64_t)M, (uint64_t)K, kBM, false)) return cudaErrorInvalidValue;
+  if (!make_map(&mb, C, (uint64_t)N, (uint64_t)K, kBN, false)) return cudaErrorInvalidValue;
+  if (!make_map(&mc, y, (uint64_t)M, (uint64_t)N, 32, true)) return cudaErrorInvalidValue;
+  if (!make_map(&me, E, (uint64_t)M, (uint64_t)N, 32, true)) return cudaErrorInvalidValue;
+  GemmArgs g{M, N, K, D, status, lam, xin, L, P, NC};
+  const long long tiles = (long long)((N + kBN - 1) / kBN) * ((M + kBM - 1) / kBM);
+  const int grid = (int)std::min<long long>(tiles, sm_count());
+  return run_gemm<kOpApply, true, false>(ma, mb, mc, me, g, grid, s);
 }
 
 }  // namespace dlr
