@@ -36,6 +36,8 @@ struct S5Work {
   float2* lbar_pw; // [T+1][P]  Lbar^t (state fastest, so a warp's loads of one power coalesce)
   float4* lbar_T;  // [P] (re.hi, re.lo, im.hi, im.lo) of Lbar^T
   float2* S;       // [B][NC][P]
+  float2* S2;      // [B][NC][2][P]: the two 32-step halves of each chunk's end state (tensor-core
+                   // tier, L a multiple of 64: written by the input projection)
   float2* Xin;     // [B][NC][P]
   float* xv;       // [B*L][2P]: V, then x (float32 tier)
 };
@@ -204,6 +206,7 @@ __device__ __forceinline__ cff cff_shfl_up(cff a, int d) {
 //      offset d multiplies by m^{G d}), so lane i - 1 holds the state entering group i,
 //   3. the group's chain again from that state, storing the state entering each chunk.
 // Only the last non-empty group may be short; no lane before it reads its value.
+template <bool kHalves>
 __global__ void __launch_bounds__(256)
 s5_carry(S5Work w, int B, int P, int NC) {
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
@@ -215,12 +218,24 @@ s5_carry(S5Work w, int B, int P, int NC) {
   const int G = (NC + 31) / 32;
   const int c0 = min(NC, lane * G), c1 = min(NC, c0 + G);
   const size_t base = (size_t)b * NC * P + p;
+  // with kHalves the chunk end state is Lbar^32 h0 + h1 from its two 32-step halves
+  const float2 l32 = w.lbar_pw[(size_t)32 * P + p];
+  auto chunk_s = [&](int c) -> float2 {
+    if constexpr (kHalves) {
+      const size_t i = ((size_t)b * NC + c) * 2 * P + p;
+      const float2 h0 = w.S2[i], h1 = w.S2[i + P];
+      const cf sc = cfma({l32.x, l32.y}, {h0.x, h0.y}, {h1.x, h1.y});
+      return make_float2(sc.re, sc.im);
+    } else {
+      return w.S[base + (size_t)c * P];
+    }
+  };
   auto chain = [&](cff x, bool store) {
     for (int cb = c0; cb < c1; cb += 8) {
       float2 sv[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        sv[q] = (cb + q < c1) ? w.S[base + (size_t)(cb + q) * P] : make_float2(0.f, 0.f);
+        sv[q] = (cb + q < c1) ? chunk_s(cb + q) : make_float2(0.f, 0.f);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         if (cb + q >= c1) break;
@@ -401,11 +416,12 @@ S5Work carve(void* ws, int64_t B, int64_t L, int64_t H, int64_t P, bool bf16, si
   size_t o_S = take(sizeof(float2) * B * NC * P);
   size_t o_X = take(sizeof(float2) * B * NC * P);
   size_t o_xv = bf16 ? 0 : take(sizeof(float) * B * L * 2 * P);
-  size_t o_bt = 0, o_c16 = 0, o_vx16 = 0;
+  size_t o_bt = 0, o_c16 = 0, o_vx16 = 0, o_S2 = 0;
   if (bf16) {
     o_bt = take(2 * 2 * P * H);
     o_c16 = take(2 * H * 2 * P);
     o_vx16 = take(2 * B * L * 2 * P);
+    o_S2 = take(sizeof(float2) * B * NC * 2 * P);
   }
   if (total) *total = off;
   char* base = reinterpret_cast<char*>(ws);
@@ -420,6 +436,7 @@ S5Work carve(void* ws, int64_t B, int64_t L, int64_t H, int64_t P, bool bf16, si
   w.bbar_t16 = bf16 ? base + o_bt : nullptr;
   w.cmat_t16 = bf16 ? base + o_c16 : nullptr;
   w.vx16 = bf16 ? base + o_vx16 : nullptr;
+  w.S2 = bf16 ? reinterpret_cast<float2*>(base + o_S2) : nullptr;
   return w;
 }
 
@@ -433,27 +450,31 @@ size_t s5_workspace_bytes(int64_t B, int64_t L, int64_t H, int64_t P, bool bf16)
 
 cudaError_t launch_tc_gemm(const void* A, bool a_f32, const void* B, void* C, bool c_bf16,
                            int M, int N, int K, const float* D, const float* E, int* status,
-                           cudaStream_t s);
+                           cudaStream_t s, const float2* lam, float2* sums, int L, int NC);
 cudaError_t launch_tc_gemm_apply(const void* V, const void* C, float* y, int M, int N, int K,
                                  const float* D, const float* E, const float2* lam,
                                  const float2* xin, int L, int P, int NC, int* status,
                                  cudaStream_t s);
 
 // The chunked diagonal scan shared by both tiers: V -> x in place, in w.xv (float32 tier) or
-// w.vx16 (tensor-core tier). Without `apply` it stops after the carries (the tensor-core
-// output projection runs the apply step on its operand tiles).
-static cudaError_t s5_scan_xv(const S5Work& w, int B, int L, int P, bool bf16, bool apply,
+// w.vx16 (tensor-core tier). `fused` (tensor-core tier, L a multiple of 64): the input
+// projection has written the chunk end states in halves and the output projection runs the
+// apply step on its operand tiles, so only the carries run here.
+static cudaError_t s5_scan_xv(const S5Work& w, int B, int L, int P, bool bf16, bool fused,
                               cudaStream_t s) {
   const int NC = (L + kT - 1) / kT;
   const int threads = P < 256 ? P : 256;  // P is a multiple of 32
   const long long quads = (long long)B * NC * (P / 4);
   const int grid16 = (int)((quads + 255) / 256);
+  if (fused) {
+    s5_carry<true><<<(B * P + 7) / 8, 256, 0, s>>>(w, B, P, NC);
+    return cudaGetLastError();
+  }
   if (bf16)
     s5_chunk16<false><<<grid16, 256, 0, s>>>(w, B, L, P, NC);
   else
     s5_chunk_state<<<dim3(NC, B), threads, 0, s>>>(w, L, P, NC);
-  s5_carry<<<(B * P + 7) / 8, 256, 0, s>>>(w, B, P, NC);
-  if (!apply) return cudaGetLastError();
+  s5_carry<false><<<(B * P + 7) / 8, 256, 0, s>>>(w, B, P, NC);
   if (bf16)
     s5_chunk16<true><<<grid16, 256, 0, s>>>(w, B, L, P, NC);
   else
@@ -472,7 +493,7 @@ cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delt
   if (!bf16) {
     dim3 g1((2 * P + kGN - 1) / kGN, (M + kGM - 1) / kGM);
     gemm_f32<<<g1, 256, 0, s>>>(u, w.bbar, w.xv, M, 2 * P, H, nullptr, nullptr);
-    e = s5_scan_xv(w, B, L, P, false, true, s);
+    e = s5_scan_xv(w, B, L, P, false, false, s);
     if (e != cudaSuccess) return e;
     dim3 g2((H + kGN - 1) / kGN, (M + kGM - 1) / kGM);
     gemm_f32<<<g2, 256, 0, s>>>(w.xv, w.cmat, y, M, H, 2 * P, D, u);
@@ -483,15 +504,17 @@ cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delt
   // adds D (.) u. When L is a multiple of 64 (tiles of 128 steps start on chunk starts) the
   // output projection turns V into x itself as its operand tiles arrive; otherwise the apply
   // kernel writes bf16 x over V first.
-  if ((e = launch_tc_gemm(u, true, w.bbar_t16, w.vx16, true, M, 2 * P, H, nullptr, nullptr,
-                          status, s)) != cudaSuccess)
-    return e;
   const bool fused = L % kT == 0;
-  if ((e = s5_scan_xv(w, B, L, P, true, !fused, s)) != cudaSuccess) return e;
+  const int NC = (L + kT - 1) / kT;
+  if ((e = launch_tc_gemm(u, true, w.bbar_t16, w.vx16, true, M, 2 * P, H, nullptr, nullptr,
+                          status, s, w.lbar_pw + P, fused ? w.S2 : nullptr, L, NC)) != cudaSuccess)
+    return e;
+  if ((e = s5_scan_xv(w, B, L, P, true, fused, s)) != cudaSuccess) return e;
   if (fused)
     return launch_tc_gemm_apply(w.vx16, w.cmat_t16, y, M, H, 2 * P, D, u, w.lbar_pw + P, w.Xin,
-                                L, P, (L + kT - 1) / kT, status, s);
-  return launch_tc_gemm(w.vx16, false, w.cmat_t16, y, false, M, H, 2 * P, D, u, status, s);
+                                L, P, NC, status, s);
+  return launch_tc_gemm(w.vx16, false, w.cmat_t16, y, false, M, H, 2 * P, D, u, status, s,
+                        nullptr, nullptr, 0, 0);
 }
 
 }  // namespace dlr

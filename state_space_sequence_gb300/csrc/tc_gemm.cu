@@ -75,10 +75,14 @@ struct GemmArgs {
   const float* D;  // [N] or null (then E is not read)
   int* status;
   // kOpApply: lambda per state, the state entering each chunk [B][NC][P], sequence length
-  // (a multiple of 64), states P (A has K = 2P columns: Re, Im per state), chunks per row
+  // (a multiple of 64), states P (A has K = 2P columns: Re, Im per state), chunks per row.
+  // With `sums` (bf16 output, N = 2P, L a multiple of 64) the epilogue also writes, per 32-row
+  // block of each chunk, sum_i lambda^(31-i) C[row i] of the bf16-rounded outputs:
+  // sums[b][c][half][p].
   const float2* lam;
   const float2* xin;
   int L, P, NC;
+  float2* sums;
 };
 
 // Bounded wait by a whole warp with one verdict for all its lanes.
@@ -388,6 +392,29 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
             *reinterpret_cast<uint4*>(box + lane * 128 + ((uint32_t(k) ^ sw) << 4)) =
                 make_uint4(h[0], h[1], h[2], h[3]);
           }
+          if (g.sums) {
+            // lane j: state p = (n0 + 64 c) / 2 + j, the 4 bytes at byte 4 (j & 3) of 16-byte
+            // chunk j >> 2 of each of the warp's 32 rows; Horner over the rows
+            __syncwarp();
+            const int p = (n0 + c * kSlice) / 2 + lane, m = m0 + q * 32;
+            if (p < g.P && m < g.M) {
+              const float2 l = g.lam[p];
+              const cf lam = {l.x, l.y};
+              cf acc = {0.f, 0.f};
+              const uint32_t sub = uint32_t(lane & 3) * 4u, ck = uint32_t(lane >> 2);
+#pragma unroll 8
+              for (int i = 0; i < 32; ++i) {
+                const uint32_t wv = *reinterpret_cast<const uint32_t*>(
+                    box + i * 128 + ((ck ^ uint32_t(i & 7)) << 4) + sub);
+                const float2 vf =
+                    __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv));
+                acc = cfma(lam, acc, {vf.x, vf.y});
+              }
+              const int b = m / g.L, t = m - b * g.L;
+              g.sums[(((size_t)b * g.NC + (t >> 6)) * 2 + ((t >> 5) & 1)) * g.P + p] =
+                  make_float2(acc.re, acc.im);
+            }
+          }
         } else if (with_e) {
           if (!(ok = warp_wait(&ebar[j], (sc / kBoxes) & 1))) break;
           const int nc = n0 + c * kSlice;
@@ -487,18 +514,21 @@ cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t
 
 // A: [M, K] row-major, bf16 (a_f32 false) or float32 (a_f32, converted to bf16 in the
 // kernel); B: bf16 [N, K] row-major. C: [M, N], f32 or (c_bf16, no D) bf16; D: f32 [N] or
-// null; E: f32 [M, N] (read only when D is given; not with a float32 A).
+// null; E: f32 [M, N] (read only when D is given; not with a float32 A). With `sums` (bf16 C,
+// N = 2P, rows = B sequences of length L, L a multiple of 64): the per-32-row partial chunk
+// states of C, sums[b][c][half][p] = sum_i lam[p]^(31-i) C[b L + 64 c + 32 half + i][2p, 2p+1].
 cudaError_t launch_tc_gemm(const void* A, bool a_f32, const void* B, void* C, bool c_bf16,
                            int M, int N, int K, const float* D, const float* E, int* status,
-                           cudaStream_t s) {
+                           cudaStream_t s, const float2* lam, float2* sums, int L, int NC) {
   if (M < 1 || N < 1 || K < 1 || (c_bf16 && D) || (a_f32 && D)) return cudaErrorInvalidValue;
+  if (sums && (!c_bf16 || N % 2 || L % 64 || !lam)) return cudaErrorInvalidValue;
   CUtensorMap ma, mb, mc, me;
   if (!make_map(&ma, A, (uint64_t)M, (uint64_t)K, kBM, a_f32)) return cudaErrorInvalidValue;
   if (!make_map(&mb, B, (uint64_t)N, (uint64_t)K, kBN, false)) return cudaErrorInvalidValue;
   if (!make_map(&mc, C, (uint64_t)M, (uint64_t)N, 32, !c_bf16)) return cudaErrorInvalidValue;
   if (D && !make_map(&me, E, (uint64_t)M, (uint64_t)N, 32, true)) return cudaErrorInvalidValue;
   if (!D) me = mc;  // not read
-  GemmArgs g{M, N, K, D, status, nullptr, nullptr, 0, 0, 0};
+  GemmArgs g{M, N, K, D, status, lam, nullptr, L, N / 2, NC, sums};
   const long long tiles = (long long)((N + kBN - 1) / kBN) * ((M + kBM - 1) / kBM);
   const int grid = (int)std::min<long long>(tiles, sm_count());
   if (D) return run_gemm<kOpBf16, true, false>(ma, mb, mc, me, g, grid, s);
@@ -523,7 +553,7 @@ cudaError_t launch_tc_gemm_apply(const void* V, const void* C, float* y, int M, 
   if (!make_map(&mb, C, (uint64_t)N, (uint64_t)K, kBN, false)) return cudaErrorInvalidValue;
   if (!make_map(&mc, y, (uint64_t)M, (uint64_t)N, 32, true)) return cudaErrorInvalidValue;
   if (!make_map(&me, E, (uint64_t)M, (uint64_t)N, 32, true)) return cudaErrorInvalidValue;
-  GemmArgs g{M, N, K, D, status, lam, xin, L, P, NC};
+  GemmArgs g{M, N, K, D, status, lam, xin, L, P, NC, nullptr};
   const long long tiles = (long long)((N + kBN - 1) / kBN) * ((M + kBM - 1) / kBM);
   const int grid = (int)std::min<long long>(tiles, sm_count());
   return run_gemm<kOpApply, true, false>(ma, mb, mc, me, g, grid, s);
