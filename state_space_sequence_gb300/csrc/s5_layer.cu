@@ -11,7 +11,8 @@
 //   gemm   V[B*L, 2P] = u[B*L, H] * Bbar^T (float32 FFMA, register tiled)
 //   chunk  S_c = sum_t Lbar^{T-1-t} V_t (end state of chunk c from a zero start)
 //   carry  X_c = Lbar^T X_{c-1} + S_c in two-float arithmetic, one warp per (b, p) scanning
-//          groups of chunks; stores the state entering each chunk
+//          groups of chunks (the tensor-core tier: float32, one CTA per (b, 32 states) with a
+//          warp per group of chunks); stores the state entering each chunk
 //   apply  x_t = Lbar^{t+1} X_in + l_t, l_t = Lbar l_{t-1} + V_t, written over V in place
 //   gemm   y = x * [Re C~^T ; -Im C~^T] + D (.) u
 // The tensor-core tier runs the two projections on tcgen05 (tc_gemm.cu) with bf16 operands and
@@ -200,13 +201,13 @@ __device__ __forceinline__ cff cff_shfl_up(cff a, int d) {
 }
 
 // One warp per (b, p): the state entering each chunk, X_0 = 0, X_{c+1} = m X_c + S_c with
-// m = Lbar^T, in two-float arithmetic. Lane i takes G = ceil(NC / 32) consecutive chunks:
+// m = Lbar^T, in two-float arithmetic (float32 tier). Lane i takes G = ceil(NC / 32)
+// consecutive chunks:
 //   1. its group's end state from a zero start,
 //   2. an inclusive Kogge-Stone scan over the lanes of the maps x -> m^G x + A_i (the step of
 //      offset d multiplies by m^{G d}), so lane i - 1 holds the state entering group i,
 //   3. the group's chain again from that state, storing the state entering each chunk.
 // Only the last non-empty group may be short; no lane before it reads its value.
-template <bool kHalves>
 __global__ void __launch_bounds__(256)
 s5_carry(S5Work w, int B, int P, int NC) {
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
@@ -218,24 +219,12 @@ s5_carry(S5Work w, int B, int P, int NC) {
   const int G = (NC + 31) / 32;
   const int c0 = min(NC, lane * G), c1 = min(NC, c0 + G);
   const size_t base = (size_t)b * NC * P + p;
-  // with kHalves the chunk end state is Lbar^32 h0 + h1 from its two 32-step halves
-  const float2 l32 = w.lbar_pw[(size_t)32 * P + p];
-  auto chunk_s = [&](int c) -> float2 {
-    if constexpr (kHalves) {
-      const size_t i = ((size_t)b * NC + c) * 2 * P + p;
-      const float2 h0 = w.S2[i], h1 = w.S2[i + P];
-      const cf sc = cfma({l32.x, l32.y}, {h0.x, h0.y}, {h1.x, h1.y});
-      return make_float2(sc.re, sc.im);
-    } else {
-      return w.S[base + (size_t)c * P];
-    }
-  };
   auto chain = [&](cff x, bool store) {
     for (int cb = c0; cb < c1; cb += 8) {
       float2 sv[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q)
-        sv[q] = (cb + q < c1) ? chunk_s(cb + q) : make_float2(0.f, 0.f);
+        sv[q] = (cb + q < c1) ? w.S[base + (size_t)(cb + q) * P] : make_float2(0.f, 0.f);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         if (cb + q >= c1) break;
@@ -262,6 +251,62 @@ s5_carry(S5Work w, int B, int P, int NC) {
   }
   const cff prev = cff_shfl_up(a, 1);
   chain(lane ? prev : zero, true);
+}
+
+// Tensor-core tier carry, float32: grid (P / 32, B), 1024 threads. Lane j holds state
+// p = 32 blockIdx.x + j (coalesced loads and stores), warp g the chunk group
+// [g G, (g + 1) G), G = ceil(NC / 32):
+//   1. the group's end state from a zero start,
+//   2. through shared memory, each warp's carry-in: the earlier groups' end states chained with
+//      m^G (all groups before the last are full),
+//   3. the group's chain again from its carry-in, storing the state entering each chunk.
+// With kHalves the chunk end state is Lbar^32 h0 + h1 from its two 32-step halves.
+template <bool kHalves>
+__global__ void __launch_bounds__(1024)
+s5_carry_groups(S5Work w, int B, int P, int NC) {
+  __shared__ cf agg[32][32];
+  const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
+  const int b = blockIdx.y, p = blockIdx.x * 32 + lane;
+  const float4 lt = w.lbar_T[p];
+  const cf m = {lt.x, lt.z};
+  const float2 l32 = w.lbar_pw[(size_t)32 * P + p];
+  const int G = (NC + 31) / 32;
+  const int c0 = min(NC, grp * G), c1 = min(NC, c0 + G);
+  const size_t base = (size_t)b * NC * P + p;
+  auto chunk_s = [&](int c) -> cf {
+    if constexpr (kHalves) {
+      const size_t i = ((size_t)b * NC + c) * 2 * P + p;
+      const float2 h0 = w.S2[i], h1 = w.S2[i + P];
+      return cfma({l32.x, l32.y}, {h0.x, h0.y}, {h1.x, h1.y});
+    } else {
+      const float2 v = w.S[base + (size_t)c * P];
+      return {v.x, v.y};
+    }
+  };
+  auto chain = [&](cf x, bool store) {
+    for (int cb = c0; cb < c1; cb += 8) {
+      cf sv[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) sv[q] = (cb + q < c1) ? chunk_s(cb + q) : cf{0.f, 0.f};
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (cb + q >= c1) break;
+        if (store) w.Xin[base + (size_t)(cb + q) * P] = make_float2(x.re, x.im);
+        x = cfma(m, x, sv[q]);
+      }
+    }
+    return x;
+  };
+  agg[grp][lane] = chain({0.f, 0.f}, false);
+  cf mg = {1.f, 0.f}, sq = m;  // m^G
+  for (int e = G; e; e >>= 1) {
+    if (e & 1) mg = cmul(mg, sq);
+    if (e > 1) sq = cmul(sq, sq);
+  }
+  __syncthreads();
+  cf x = {0.f, 0.f};
+  for (int j = 0; j < grp; ++j) x = cfma(mg, x, agg[j][lane]);
+  chain(x, true);
 }
 
 // grid (NC, B), one thread per state p: x_t = Lbar^{t+1} X_in + l_t with the in-chunk part
@@ -467,14 +512,17 @@ static cudaError_t s5_scan_xv(const S5Work& w, int B, int L, int P, bool bf16, b
   const long long quads = (long long)B * NC * (P / 4);
   const int grid16 = (int)((quads + 255) / 256);
   if (fused) {
-    s5_carry<true><<<(B * P + 7) / 8, 256, 0, s>>>(w, B, P, NC);
+    s5_carry_groups<true><<<dim3(P / 32, B), 1024, 0, s>>>(w, B, P, NC);
     return cudaGetLastError();
   }
   if (bf16)
     s5_chunk16<false><<<grid16, 256, 0, s>>>(w, B, L, P, NC);
   else
     s5_chunk_state<<<dim3(NC, B), threads, 0, s>>>(w, L, P, NC);
-  s5_carry<false><<<(B * P + 7) / 8, 256, 0, s>>>(w, B, P, NC);
+  if (bf16)
+    s5_carry_groups<false><<<dim3(P / 32, B), 1024, 0, s>>>(w, B, P, NC);
+  else
+    s5_carry<<<(B * P + 7) / 8, 256, 0, s>>>(w, B, P, NC);
   if (bf16)
     s5_chunk16<true><<<grid16, 256, 0, s>>>(w, B, L, P, NC);
   else
