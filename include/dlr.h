@@ -187,6 +187,23 @@ dlr_status dlr_scan_apply(const float* u, int64_t B, int64_t H, int64_t N, int64
                           dlr_stream_t stream);
 
 /*
+ * dlr_scan_host -- the causal DLR layer (Re cast) of dlr_scan with DLR_SCAN_TENSOR on HOST
+ * buffers: u, y [B, H, L] and log_re, log_im [H, N], W [H, N, 2] are host pointers (page-locked
+ * for the copies to overlap anything), the device working copies live in `workspace` (device
+ * memory, dlr_scan_host_workspace_size bytes, 16-byte aligned; the library still allocates
+ * nothing). The batch is split into up to four pieces of whole batch rows (or, for B < 4, of
+ * channels; one piece when L % 4 != 0): the copies in, the layer and the copies out run on
+ * three internal streams joined by events, so the copy of one piece in, the compute of
+ * another and the copy of a third out overlap. Asynchronous with respect to the host; ordered
+ * after the work already on `stream` and before the work enqueued on it later, so y may be
+ * read after a synchronisation of `stream`. Same limits as dlr_scan_apply (N <= 64).
+ */
+size_t dlr_scan_host_workspace_size(int64_t B, int64_t H, int64_t N, int64_t L);
+dlr_status dlr_scan_host(const float* u, const float* log_re, const float* log_im,
+                         const float* W, int64_t B, int64_t H, int64_t N, int64_t L, float* y,
+                         void* workspace, size_t workspace_bytes, dlr_stream_t stream);
+
+/*
  * s5_layer -- S5 SSM outputs (S5 paper section 3: diagonalised MIMO system; zero-order hold
  * with one timescale per state; diagonal feedthrough):
  *   Delta_p   = exp(log_delta[p])
@@ -232,7 +249,7 @@ const char* dlr_status_string(dlr_status status);
  * reported as DLR_ERR_CUDA ("no error" if none). The string is static; do not free it. */
 const char* dlr_last_cuda_error(void);
 
-/* Library ABI version (incremented on any signature change). */
+/* Library ABI version (incremented on any signature change or added entry point). */
 int dlr_abi_version(void);
 
 #ifdef __cplusplus

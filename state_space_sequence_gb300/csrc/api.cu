@@ -2,6 +2,9 @@
 // workspace carving and kernel dispatch on the caller's stream.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <mutex>
+
 #include "dlr.h"
 
 namespace dlr {
@@ -58,6 +61,30 @@ dlr_status from_cuda(cudaError_t e) {
   return DLR_ERR_CUDA;
 }
 
+// Three non-blocking streams per device for the host-buffer entry point: copies in, compute,
+// copies out. Created on first use and kept for the life of the process.
+constexpr int kMaxDevices = 64;
+cudaStream_t g_pipe[kMaxDevices][3];
+std::once_flag g_pipe_once[kMaxDevices];
+cudaError_t g_pipe_err[kMaxDevices];
+
+cudaError_t pipe_streams(cudaStream_t (&st)[3]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::call_once(g_pipe_once[dev], [dev] {
+    g_pipe_err[dev] = cudaSuccess;
+    for (int i = 0; i < 3 && g_pipe_err[dev] == cudaSuccess; ++i)
+      g_pipe_err[dev] = cudaStreamCreateWithFlags(&g_pipe[dev][i], cudaStreamNonBlocking);
+  });
+  if (g_pipe_err[dev] != cudaSuccess) return g_pipe_err[dev];
+  for (int i = 0; i < 3; ++i) st[i] = g_pipe[dev][i];
+  return cudaSuccess;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
 bool ranges_overlap(const void* a, size_t an, const void* b, size_t bn) {
   uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
   return a0 < b0 + bn && b0 < a0 + an;
@@ -73,7 +100,7 @@ dlr_status check_params(const float* log_re, const float* log_im, const float* W
 
 extern "C" {
 
-int dlr_abi_version(void) { return 3; }
+int dlr_abi_version(void) { return 4; }
 
 const char* dlr_last_cuda_error(void) { return t_last_cuda_error; }
 
@@ -264,6 +291,111 @@ dlr_status s5_layer(const float* u, const float* lambda, const float* log_delta,
   if (bf16 && !status) return DLR_ERR_CUDA;
   return from_cuda(dlr::launch_s5(u, lambda, log_delta, Bt, Ct, D, (int)B, (int)L, (int)H,
                                   (int)P, bf16, y, workspace, status, (cudaStream_t)stream));
+}
+
+size_t dlr_scan_host_workspace_size(int64_t B, int64_t H, int64_t N, int64_t L) {
+  if (B < 1 || H < 1 || N < 1 || L < 1) return 0;
+  const size_t data = align256(sizeof(float) * (size_t)B * (size_t)H * (size_t)L);
+  const size_t par = align256(sizeof(float) * (size_t)H * (size_t)N);
+  return 2 * data + 4 * par + dlr::scan_tc_workspace_bytes(H);
+}
+
+dlr_status dlr_scan_host(const float* u, const float* log_re, const float* log_im,
+                         const float* W, int64_t B, int64_t H, int64_t N, int64_t L, float* y,
+                         void* workspace, size_t workspace_bytes, dlr_stream_t stream) {
+  if (B < 1 || H < 1 || N < 1 || L < 1) return DLR_ERR_INVALID_ARG;
+  if (!u || !y || !log_re || !log_im || !W) return DLR_ERR_INVALID_ARG;
+  const size_t rows = (size_t)B * (size_t)H;
+  const size_t bytes = sizeof(float) * rows * (size_t)L;
+  if (ranges_overlap(u, bytes, y, bytes)) return DLR_ERR_INVALID_ARG;
+  if (N > 64 || L > kMaxL || B * H > kMaxGrid) return DLR_ERR_UNSUPPORTED;
+  const size_t need = dlr_scan_host_workspace_size(B, H, N, L);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DLR_ERR_WORKSPACE;
+  char* base = static_cast<char*>(workspace);
+  const size_t data = align256(bytes), par = align256(sizeof(float) * (size_t)H * (size_t)N);
+  float* ud = reinterpret_cast<float*>(base);
+  float* yd = reinterpret_cast<float*>(base + data);
+  float* lrd = reinterpret_cast<float*>(base + 2 * data);
+  float* lid = reinterpret_cast<float*>(base + 2 * data + par);
+  float* Wd = reinterpret_cast<float*>(base + 2 * data + 2 * par);
+  char* tables = base + 2 * data + 4 * par;
+  int* status = status_word();
+  if (!status) return DLR_ERR_CUDA;
+
+  cudaStream_t st[3];
+  cudaError_t e = pipe_streams(st);
+  if (e != cudaSuccess) return from_cuda(e);
+  // pieces: groups of whole batch rows when B >= 4, else channel groups of each batch row, so
+  // that a piece is one contiguous [B', H', L] block whose tables start at channel h0
+  // (one piece when L % 4 != 0: piece starts must stay 16-byte aligned)
+  const int64_t kTarget = L % 4 ? 1 : 4;
+  const int64_t per_b = B >= kTarget ? (B + kTarget - 1) / kTarget : 1;
+  const int64_t groups = B >= kTarget ? 1 : std::min<int64_t>(H, (kTarget + B - 1) / B);
+  const int64_t per_h = (H + groups - 1) / groups;
+  const size_t table_bytes = dlr::scan_tc_workspace_bytes(1);
+
+  cudaEvent_t ev_start, ev_par, ev_end;
+  auto mk = [](cudaEvent_t* ev) { return cudaEventCreateWithFlags(ev, cudaEventDisableTiming); };
+  if ((e = mk(&ev_start)) != cudaSuccess) return from_cuda(e);
+  if ((e = mk(&ev_par)) != cudaSuccess || (e = mk(&ev_end)) != cudaSuccess) {
+    cudaEventDestroy(ev_start);
+    return from_cuda(e);
+  }
+  auto run = [&]() -> cudaError_t {
+    cudaError_t r;
+    // the caller's earlier work on `stream` comes first
+    if ((r = cudaEventRecord(ev_start, (cudaStream_t)stream)) != cudaSuccess) return r;
+    for (int i = 0; i < 3; ++i)
+      if ((r = cudaStreamWaitEvent(st[i], ev_start, 0)) != cudaSuccess) return r;
+    const size_t pb = sizeof(float) * (size_t)H * (size_t)N;
+    if ((r = cudaMemcpyAsync(lrd, log_re, pb, cudaMemcpyHostToDevice, st[0])) != cudaSuccess ||
+        (r = cudaMemcpyAsync(lid, log_im, pb, cudaMemcpyHostToDevice, st[0])) != cudaSuccess ||
+        (r = cudaMemcpyAsync(Wd, W, 2 * pb, cudaMemcpyHostToDevice, st[0])) != cudaSuccess)
+      return r;
+    if ((r = cudaEventRecord(ev_par, st[0])) != cudaSuccess) return r;
+    if ((r = cudaStreamWaitEvent(st[1], ev_par, 0)) != cudaSuccess) return r;
+    if ((r = dlr::launch_scan_tc_tables(lrd, lid, Wd, (int)H, (int)N, tables, st[1])) !=
+        cudaSuccess)
+      return r;
+    for (int64_t b0 = 0; b0 < B; b0 += per_b) {
+      const int64_t nb = std::min(per_b, B - b0);
+      for (int64_t h0 = 0; h0 < H; h0 += per_h) {
+        const int64_t nh = std::min(per_h, H - h0);
+        // a piece is contiguous: whole batch rows (nh == H) or channels of one batch row
+        const size_t off = ((size_t)b0 * (size_t)H + (size_t)h0) * (size_t)L;
+        const size_t pbytes = sizeof(float) * (size_t)nb * (size_t)nh * (size_t)L;
+        cudaEvent_t in, done;
+        if ((r = mk(&in)) != cudaSuccess) return r;
+        if ((r = mk(&done)) != cudaSuccess) {
+          cudaEventDestroy(in);
+          return r;
+        }
+        r = cudaMemcpyAsync(ud + off, u + off, pbytes, cudaMemcpyHostToDevice, st[0]);
+        if (r == cudaSuccess) r = cudaEventRecord(in, st[0]);
+        if (r == cudaSuccess) r = cudaStreamWaitEvent(st[1], in, 0);
+        if (r == cudaSuccess)
+          r = dlr::launch_scan_tc_apply(ud + off, (int)nb, (int)nh, (int)L, false, yd + off,
+                                        tables + (size_t)h0 * table_bytes, status, st[1],
+                                        false);
+        if (r == cudaSuccess) r = cudaEventRecord(done, st[1]);
+        if (r == cudaSuccess) r = cudaStreamWaitEvent(st[2], done, 0);
+        if (r == cudaSuccess)
+          r = cudaMemcpyAsync(y + off, yd + off, pbytes, cudaMemcpyDeviceToHost, st[2]);
+        cudaEventDestroy(in);  // released once recorded work completes
+        cudaEventDestroy(done);
+        if (r != cudaSuccess) return r;
+      }
+    }
+    // the caller's later work on `stream` waits for the last copy out (which follows every
+    // piece's compute, itself after the tables)
+    if ((r = cudaEventRecord(ev_end, st[2])) != cudaSuccess) return r;
+    return cudaStreamWaitEvent((cudaStream_t)stream, ev_end, 0);
+  };
+  e = run();
+  cudaEventDestroy(ev_start);
+  cudaEventDestroy(ev_par);
+  cudaEventDestroy(ev_end);
+  return from_cuda(e);
 }
 
 dlr_status dlr_selftest_timeout(int limit_ms, dlr_stream_t stream) {

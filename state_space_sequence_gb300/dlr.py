@@ -59,6 +59,10 @@ def _load():
         lib.dlr_scan_prepare.restype = i32
         lib.dlr_scan_apply.argtypes = [P, i64, i64, i64, i64, i32, P, P, sz, P]
         lib.dlr_scan_apply.restype = i32
+        lib.dlr_scan_host_workspace_size.argtypes = [i64, i64, i64, i64]
+        lib.dlr_scan_host_workspace_size.restype = sz
+        lib.dlr_scan_host.argtypes = [P, P, P, P, i64, i64, i64, i64, P, P, sz, P]
+        lib.dlr_scan_host.restype = i32
         lib.s5_workspace_size.argtypes = [i64, i64, i64, i64, i32]
         lib.s5_workspace_size.restype = sz
         lib.s5_layer.argtypes = [P, P, P, P, P, P, i64, i64, i64, i64, i32, P, P, sz, P]
@@ -228,6 +232,29 @@ def dlr_scan_apply(u, workspace, N: int, out=None, reverse: bool = False, stream
     _ok("dlr_scan_apply", _load().dlr_scan_apply(_ptr(u), B, H, N, L, 1 if reverse else 0,
                                                  _ptr(out), _ptr(workspace), workspace.numel(),
                                                  _stream(stream)))
+    return out
+
+
+def dlr_scan_host_workspace_size(B: int, H: int, N: int, L: int) -> int:
+    return int(_load().dlr_scan_host_workspace_size(B, H, N, L))
+
+
+def dlr_scan_host(u, params, out, workspace, stream=None):
+    """The causal DLR layer on host buffers: u, out [B, H, L] and the parameters are CPU float32
+    tensors (pinned for overlap); ``workspace`` is a uint8 device tensor of
+    dlr_scan_host_workspace_size bytes. Enqueued on ``stream``; synchronise it before reading
+    ``out``."""
+    lr, li, W = params
+    for t in (u, out, lr, li, W):
+        if t.device.type != "cpu" or t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("dlr_scan_host takes contiguous float32 host tensors")
+    B, H, L = u.shape
+    N = lr.shape[1]
+    if tuple(out.shape) != (B, H, L):
+        raise ValueError("out must have the shape of u")
+    _ok("dlr_scan_host", _load().dlr_scan_host(_ptr(u), _ptr(lr), _ptr(li), _ptr(W), B, H, N, L,
+                                               _ptr(out), _ptr(workspace), workspace.numel(),
+                                               _stream(stream)))
     return out
 
 

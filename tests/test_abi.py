@@ -44,7 +44,7 @@ def test_status_strings_and_version(lib):
     lib.dlr_status_string.restype = ctypes.c_char_p
     assert lib.dlr_status_string(0) == b"DLR_OK"
     assert lib.dlr_status_string(4) == b"DLR_ERR_TIMEOUT"
-    assert lib.dlr_abi_version() == 3
+    assert lib.dlr_abi_version() == 4
 
 
 def test_host_validation_rejects_bad_arguments(lib):
@@ -93,6 +93,19 @@ def test_host_validation_rejects_bad_arguments(lib):
                               None) == 1
     assert lib.dlr_scan_apply(fake, 1, 1, 4, 64, 0, ctypes.c_void_p(0x9000), None, 0,
                               None) == 5
+    # host-buffer entry point: the workspace holds u, y, the parameters and the tables
+    lib.dlr_scan_host_workspace_size.argtypes = [i64, i64, i64, i64]
+    lib.dlr_scan_host_workspace_size.restype = sz
+    lib.dlr_scan_host.argtypes = [P, P, P, P, i64, i64, i64, i64, P, P, sz, P]
+    need = lib.dlr_scan_host_workspace_size(8, 256, 64, 4096)
+    assert need >= 2 * 8 * 256 * 4096 * 4 + 256 * 83968
+    assert lib.dlr_scan_host_workspace_size(0, 1, 1, 1) == 0
+    y = ctypes.c_void_p(0x9000)
+    assert lib.dlr_scan_host(fake, fake, fake, fake, 0, 1, 4, 64, y, fake, 1 << 30, None) == 1
+    assert lib.dlr_scan_host(None, fake, fake, fake, 1, 1, 4, 64, y, fake, 1 << 30, None) == 1
+    assert lib.dlr_scan_host(fake, fake, fake, fake, 1, 1, 65, 64, y, fake, 1 << 30, None) == 2
+    assert lib.dlr_scan_host(fake, fake, fake, fake, 1, 1, 4, 64, y, None, 0, None) == 5
+    assert lib.dlr_scan_host(fake, fake, fake, fake, 1, 1, 4, 64, y, fake, 16, None) == 5
     lib.dlr_conv.argtypes = [P, P, P, ctypes.c_int, i64, i64, i64, P, P, ctypes.c_size_t, P]
     # missing workspace
     assert lib.dlr_conv(fake, fake, None, 0, 1, 1, 16, ctypes.c_void_p(0x9000), None, 0,
