@@ -9,7 +9,7 @@
 
 namespace dlr {
 cudaError_t launch_dlr_kernel(const float* log_re, const float* log_im, const float* W, int H,
-                              int N, int L, bool re_im, float* K, cudaStream_t s);
+                              int N, int L, bool re_im, float* K, int* status, cudaStream_t s);
 int conv_log2_size(int64_t L);
 size_t conv_workspace_bytes(int64_t H, int64_t L);
 cudaError_t launch_dlr_conv_spectrum(const float* K1, const float* K2, int H, int L, void* ws,
@@ -124,8 +124,11 @@ dlr_status dlr_kernel(const float* log_re, const float* log_im, const float* W, 
   if (st != DLR_OK) return st;
   if (!K || !aligned16(K)) return DLR_ERR_INVALID_ARG;
   if (L > kMaxL || H > 65535 || N > (int64_t(1) << 24)) return DLR_ERR_UNSUPPORTED;
+  int* status = status_word();
+  if (!status) return DLR_ERR_CUDA;
   return from_cuda(dlr::launch_dlr_kernel(log_re, log_im, W, (int)H, (int)N, (int)L,
-                                          cast == DLR_CAST_RE_IM, K, (cudaStream_t)stream));
+                                          cast == DLR_CAST_RE_IM, K, status,
+                                          (cudaStream_t)stream));
 }
 
 size_t dlr_conv_workspace_size(int64_t H, int64_t L, dlr_dir dir) {

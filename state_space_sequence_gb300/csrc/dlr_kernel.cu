@@ -207,8 +207,14 @@ cudaError_t launch_gen(const float* log_re, const float* log_im, const float* W,
 
 }  // namespace
 
+cudaError_t launch_dlr_kernel_tc(const float* log_re, const float* log_im, const float* W, int H,
+                                 int N, int L, bool re_im, float* K, int* status,
+                                 cudaStream_t s);
+
+// N >= 256 states: the tensor-core generator (dlr_kernel_tc.cu); fewer: this FFMA one.
 cudaError_t launch_dlr_kernel(const float* log_re, const float* log_im, const float* W, int H,
-                              int N, int L, bool re_im, float* K, cudaStream_t s) {
+                              int N, int L, bool re_im, float* K, int* status, cudaStream_t s) {
+  if (N >= 256) return launch_dlr_kernel_tc(log_re, log_im, W, H, N, L, re_im, K, status, s);
   const bool big = N >= 256;
   if (re_im)
     return big ? launch_gen<true, 32>(log_re, log_im, W, H, N, L, K, s)

@@ -40,8 +40,11 @@ def check_status():
 # ------------------------------------------------------------------------------------------
 # dlr_kernel
 
+# N >= 256 runs the tensor-core generator: a whole tile of 128 chunks, ragged blocks of
+# states and a ragged last chunk, the DLR-prod shape, and a tile that is mostly past L
 @pytest.mark.parametrize("H,N,L", [(1, 1, 1), (3, 5, 1000), (2, 16, 256), (4, 64, 4096),
-                                   (2, 33, 4097), (2, 64, 70000)])
+                                   (2, 33, 4097), (2, 64, 70000), (2, 256, 8192), (3, 300, 5000),
+                                   (1, 1024, 16384), (2, 257, 100)])
 @pytest.mark.parametrize("cast", ["re", "re_im"])
 def test_kernel_matches_oracle(H, N, L, cast):
     w = inputs.make_dlr(1, H, N, 1, seed=H * 1000 + N, unit_channels=min(1, H))
@@ -51,9 +54,10 @@ def test_kernel_matches_oracle(H, N, L, cast):
     check_status()
 
 
-def test_kernel_dft_identity_on_gpu():
-    """(log Lambda)_re = 0, theta_n = 2 pi n / N, L = N: K = N * IDFT(w) (real part)."""
-    N = 64
+@pytest.mark.parametrize("N", [64, 256, 512])
+def test_kernel_dft_identity_on_gpu(N):
+    """(log Lambda)_re = 0, theta_n = 2 pi n / N, L = N: K = N * IDFT(w) (real part); N >= 256
+    on the tensor-core generator, all states on the unit circle."""
     rng = np.random.default_rng(5)
     log_re = np.zeros((1, N), np.float32)
     log_im = (2 * np.pi * np.arange(N) / N).astype(np.float32)[None]
