@@ -20,10 +20,16 @@
 // (lambda, lambda^8, lambda^64, lambda^512, lambda^4096, W lambda^{j0}) combined by product
 // trees of depth <= 3, so no term is more than about a dozen roundings from exact.
 //
-// Roles (288 threads, one CTA per SM): warps 0-7 generate, per block of 32 states, the power
-// tables and then the A and Bm tiles straight into the f16 operand layout (K-major, 128-byte
-// swizzle) of a 2-stage ring; warp 8 allocates 4 x 128 TMEM columns and one of its threads
-// issues the MMAs; warps 0-3 then read the accumulators (thread = chunk row) and store K.
+// Roles (416 threads, one CTA per SM), joined by mbarriers:
+//   warps 0-3   tables, one block of 32 states ahead, into a double buffer: the directly
+//               evaluated powers, then per state (lambda, lambda^8, lambda^64)^{0..7} and
+//               W lambda^{j0 + 512 c1 + 4096 c2} for the 16 (c1, c2) of the tile's chunks;
+//   warps 4-11  tiles: A[c][n] = (W lambda^{j0 + 512 c1 + 4096 c2}) (lambda^64)^{c0} (c = c0 +
+//               8 c1 + 64 c2) and Bm[n][t] = lambda^{t mod 8} (lambda^8)^{t / 8}, scaled, split
+//               into f16 halves and written straight into the operand layout (K-major,
+//               128-byte swizzle) of a 2-stage ring; warps 4-7 then read the accumulators
+//               (thread = chunk row) and store K;
+//   warp 12     allocates 4 x 128 TMEM columns; one of its threads issues the MMAs.
 #include <cuda_fp16.h>
 
 #include "dlr_common.cuh"
@@ -35,25 +41,36 @@ namespace {
 constexpr int kT = 64;           // lags per chunk
 constexpr int kRows = 128;       // chunks per CTA (MMA M)
 constexpr int kSB = 32;          // complex states per K-block (64 f16 = 128 bytes per row)
-constexpr int kGen = 256;        // generator threads
-constexpr int kThreads = kGen + 32;
+constexpr int kTab = 128;        // table threads (warps 0-3)
+constexpr int kGen = 256;        // tile threads (warps 4-11)
+constexpr int kThreads = kTab + kGen + 32;
 constexpr int kStages = 2;
 constexpr uint32_t kTile = kRows * 128;          // 128 rows x 128 bytes
 constexpr uint32_t kStageBytes = 4 * kTile;      // A hi, A lo, B hi, B lo
+// table buffer: (lambda, lambda^8, lambda^64)^e [3][kSB][8], W lambda^{j0+512 c1+4096 c2}
+// [kSB][16]
+constexpr uint32_t kPOff = 0, kQOff = 3 * kSB * 8 * 8;
+constexpr uint32_t kTabBuf = kQOff + kSB * 16 * 8;
 constexpr uint32_t kTabOff = kStages * kStageBytes;
 constexpr int kDirect = 6;                       // lambda^{1,8,64,512,4096}, W lambda^{j0}
-constexpr uint32_t kTabBytes = (kSB * kDirect + 5 * kSB * 8) * 8;
+// table warps' scratch: direct powers [kSB][6], small powers [5][kSB][8]
+constexpr uint32_t kScrOff = kTabOff + 2 * kTabBuf;
+constexpr uint32_t kScrBytes = (kSB * kDirect + 5 * kSB * 8) * 8;
 constexpr int kPreChunk = 1024;                  // states per pre-pass pass
-constexpr uint32_t kPreOff = kTabOff + kTabBytes;
+constexpr uint32_t kPreOff = kScrOff + kScrBytes;
 constexpr uint32_t kScaleOff = kPreOff + kPreChunk * 8;
 constexpr uint32_t kBarOff = kScaleOff + 3 * kRows * 4;
-constexpr size_t kSmemBytes = 1024 + kBarOff + 64;
+constexpr size_t kSmemBytes = 1024 + kBarOff + 128;
+static_assert(kSmemBytes <= 232448, "shared memory");
 constexpr int kAcc = 4;                           // accumulators, K-blocks round-robin
 constexpr uint32_t kTmemCols = 128 * kAcc;
 constexpr float kLog2e = 1.44269504088896341f;
 
-__device__ __forceinline__ void gen_sync() {
+__device__ __forceinline__ void tile_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kGen) : "memory");
+}
+__device__ __forceinline__ void tab_sync() {
+  asm volatile("bar.sync 2, %0;" ::"n"(kTab) : "memory");
 }
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
   return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity)) != 0;
@@ -75,13 +92,18 @@ __device__ __forceinline__ void small_powers8(float2* p, cf x) {
   for (int i = 0; i < 8; ++i) p[i] = make_float2(q[i].re, q[i].im);
 }
 
-// (a, b) scaled by s as f16 pairs: hi = f16(a s, b s), lo = f16 of the remainders
+// (a, b) as f16 pairs: hi = f16(a, b), lo = f16 of the remainders
 __device__ __forceinline__ void split_h2(float a, float b, uint32_t& hi, uint32_t& lo) {
   const __half2 h = __floats2half2_rn(a, b);
   const float2 f = __half22float2(h);
   const __half2 l = __floats2half2_rn(a - f.x, b - f.y);
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+__device__ __forceinline__ float2 f2mul(float2 a, float2 b) {
+  const cf r = cmul({a.x, a.y}, {b.x, b.y});
+  return make_float2(r.re, r.im);
 }
 
 template <bool kReIm>
@@ -91,16 +113,18 @@ dlr_kernel_tc(const float* __restrict__ log_re, const float* __restrict__ log_im
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float2* sE = reinterpret_cast<float2*>(sm + kTabOff);            // [kSB][kDirect]
-  float2* sP = sE + kSB * kDirect;                                  // [5][kSB][8]
+  float2* sE = reinterpret_cast<float2*>(sm + kScrOff);            // [kSB][kDirect]
+  float2* sSp = sE + kSB * kDirect;                                 // [5][kSB][8]
   float2* sPre = reinterpret_cast<float2*>(sm + kPreOff);           // [kPreChunk]
   float* sMax = reinterpret_cast<float*>(sm + kScaleOff);           // [2][kRows]
   int* sExp = reinterpret_cast<int*>(sm + kScaleOff) + 2 * kRows;   // [kRows]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBarOff);
-  uint64_t* full = bars;               // [kStages] tiles written (8 warp arrivals)
-  uint64_t* empty = bars + kStages;    // [kStages] tiles consumed by the MMAs
-  uint64_t* done = bars + 2 * kStages; // accumulator complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* full = bars;                 // [kStages] tiles written (8 warp arrivals)
+  uint64_t* empty = bars + kStages;      // [kStages] tiles consumed by the MMAs
+  uint64_t* done = bars + 2 * kStages;   // accumulators complete
+  uint64_t* tab_full = done + 1;         // [2] table buffer written (2 warp arrivals)
+  uint64_t* tab_empty = tab_full + 2;    // [2] table buffer read (8 warp arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tab_empty + 2);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int h = blockIdx.y;
@@ -116,9 +140,13 @@ dlr_kernel_tc(const float* __restrict__ log_re, const float* __restrict__ log_im
       tc::mbar_init(&empty[s], 1);
     }
     tc::mbar_init(done, 1);
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&tab_full[b], kTab / 32);
+      tc::mbar_init(&tab_empty[b], kGen / 32);
+    }
     tc::mbar_fence_init();
   }
-  if (warp == 8) {
+  if (warp == 12) {
     tc::tmem_alloc(tmem_slot, kTmemCols);
     tc::tmem_relinquish();
   }
@@ -128,119 +156,153 @@ dlr_kernel_tc(const float* __restrict__ log_re, const float* __restrict__ log_im
   const uint32_t tmem = *tmem_slot;
   bool ok = true;
 
-  if (warp < 8) {
-    // ---- row scales: the largest log2|A[c][n]| = log2|W_n| - a_n^2 (j0 + 64 c) log2(e) ----
-    const int row = tid & (kRows - 1), half = tid >> 7;
-    const float jr = (float)(j0 + row * kT);
-    float mx = -INFINITY;
-    for (int n0 = 0; n0 < N; n0 += kPreChunk) {
-      const int cnt = min(kPreChunk, N - n0);
-      gen_sync();
-      for (int i = tid; i < cnt; i += kGen) {
-        const float lr = lr_h[n0 + i];
-        const float2 w = w_h[n0 + i];
-        sPre[i] = make_float2(0.5f * log2f(w.x * w.x + w.y * w.y), lr * lr * kLog2e);
+  if (warp < 4) {
+    // ---- tables, one block of states ahead of the tiles ----
+    // every table warp runs every iteration (the named barriers count both); after a failed
+    // wait a warp only stops writing the shared buffer
+    // the parameters of this thread's (at most two) direct-power items, fetched one block
+    // ahead so the loads from L2 overlap the current block's work
+    constexpr int kItems = (kSB * kDirect + kTab - 1) / kTab;
+    float par_r[kItems], par_i[kItems];
+    float2 par_w[kItems];
+    auto fetch = [&](int kb, float (&r)[kItems], float (&im)[kItems], float2 (&w)[kItems]) {
+#pragma unroll
+      for (int k = 0; k < kItems; ++k) {
+        const int item = tid + k * kTab, n = kb * kSB + item / kDirect;
+        const bool in = item < kSB * kDirect && kb < nkb && n < N;
+        r[k] = in ? lr_h[n] : 0.f;
+        im[k] = in ? li_h[n] : 0.f;
+        w[k] = in && item % kDirect == 5 ? w_h[n] : make_float2(0.f, 0.f);
       }
-      gen_sync();
-      for (int i = half; i < cnt; i += 2) mx = fmaxf(mx, fmaf(-sPre[i].y, jr, sPre[i].x));
-    }
-    sMax[half * kRows + row] = mx;
-    gen_sync();
-    if (half == 0) {
-      const float m = fmaxf(sMax[row], sMax[kRows + row]);
-      sExp[row] = (m > -1e30f) ? max(-100, min(100, 13 - (int)ceilf(m))) : 0;
-    }
-    gen_sync();
-
-    // ---- K-blocks of 32 states ----
-    const uint32_t sw = uint32_t(row & 7);
-    const float a_scale = exp2i(sExp[row]);
-    // every generator warp runs every iteration (the named barriers count all 256 threads);
-    // after a failed wait a warp only stops writing tiles
+    };
+    fetch(0, par_r, par_i, par_w);
     for (int kb = 0; kb < nkb; ++kb) {
-      const int n0 = kb * kSB, s = kb % kStages;
-      // direct powers of each state
-      if (tid < kSB * kDirect) {
-        const int nl = tid / kDirect, which = tid % kDirect, n = n0 + nl;
+      const int n0 = kb * kSB, b = kb & 1;
+      float2* buf = reinterpret_cast<float2*>(sm + kTabOff + b * kTabBuf);
+      float nx_r[kItems], nx_i[kItems];
+      float2 nx_w[kItems];
+      fetch(kb + 1, nx_r, nx_i, nx_w);
+      // direct powers: 32 states x 6
+#pragma unroll
+      for (int k = 0; k < kItems; ++k) {
+        const int item = tid + k * kTab;
+        if (item >= kSB * kDirect) break;
+        const int nl = item / kDirect, which = item % kDirect, n = n0 + nl;
         cf v = {0.f, 0.f};
         if (n < N) {
-          const lam_param p = make_lam_param(lr_h[n], li_h[n]);
+          const lam_param p = make_lam_param(par_r[k], par_i[k]);
           if (which < 5) {
             v = lam_pow(p, which == 0 ? 1 : which == 1 ? 8 : which == 2 ? 64 : which == 3 ? 512
                                                                                       : 4096);
           } else {
-            const float2 w = w_h[n];
-            v = cmul({w.x, w.y}, lam_pow(p, j0));
+            v = cmul({par_w[k].x, par_w[k].y}, lam_pow(p, j0));
           }
         }
-        sE[nl * kDirect + which] = make_float2(v.re, v.im);
+        sE[item] = make_float2(v.re, v.im);
       }
-      gen_sync();
-      // small-power tables: part 0..3 = (lambda, lambda^8, lambda^64, lambda^512)^{0..7},
+#pragma unroll
+      for (int k = 0; k < kItems; ++k) {
+        par_r[k] = nx_r[k];
+        par_i[k] = nx_i[k];
+        par_w[k] = nx_w[k];
+      }
+      tab_sync();
+      // small powers: parts 0..3 = (lambda, lambda^8, lambda^64, lambda^512)^{0..7};
       // part 4 = W lambda^{j0} (lambda^4096)^{0, 1}
-      if (tid < kSB * 5) {
-        const int nl = tid / 5, part = tid % 5;
-        float2* dst = sP + (part * kSB + nl) * 8;
+      for (int item = tid; item < kSB * 5; item += kTab) {
+        const int part = item / kSB, nl = item % kSB;
+        float2* dst = sSp + (part * kSB + nl) * 8;
         if (part < 4) {
           const float2 e = sE[nl * kDirect + part];
           small_powers8(dst, {e.x, e.y});
         } else {
           const float2 e = sE[nl * kDirect + 5], f = sE[nl * kDirect + 4];
-          const cf b = cmul({e.x, e.y}, {f.x, f.y});
           dst[0] = e;
-          dst[1] = make_float2(b.re, b.im);
+          dst[1] = f2mul(e, f);
         }
       }
-      gen_sync();
-      if (ok && kb >= kStages) ok = warp_wait(&empty[s], ((kb / kStages) - 1) & 1);
+      tab_sync();
+      if (ok && kb >= 2) ok = warp_wait(&tab_empty[b], ((kb >> 1) - 1) & 1);
+      if (ok) {
+        float2* pt = buf + kPOff / 8;
+        float2* q = buf + kQOff / 8;
+        for (int item = tid; item < 3 * kSB * 8; item += kTab) pt[item] = sSp[item];
+        for (int item = tid; item < kSB * 16; item += kTab) {  // W lambda^{j0+512 c1+4096 c2}
+          const int nl = item >> 4, k = item & 15;
+          q[item] = f2mul(sSp[(4 * kSB + nl) * 8 + (k >> 3)], sSp[(3 * kSB + nl) * 8 + (k & 7)]);
+        }
+      }
+      __syncwarp();
+      if (ok && lane == 0) tc::mbar_arrive(&tab_full[b]);
+      tab_sync();  // the scratch is rewritten by the next iteration
+    }
+  } else if (warp < 12) {
+    // ---- row scales: the largest log2|A[c][n]| = log2|W_n| - a_n^2 (j0 + 64 c) log2(e) ----
+    const int tt = tid - kTab;
+    const int row = tt & (kRows - 1), half = tt >> 7;
+    const float jr = (float)(j0 + row * kT);
+    float mx = -INFINITY;
+    for (int n0 = 0; n0 < N; n0 += kPreChunk) {
+      const int cnt = min(kPreChunk, N - n0);
+      tile_sync();
+      for (int i = tt; i < cnt; i += kGen) {
+        const float lr = lr_h[n0 + i];
+        const float2 w = w_h[n0 + i];
+        sPre[i] = make_float2(0.5f * log2f(w.x * w.x + w.y * w.y), lr * lr * kLog2e);
+      }
+      tile_sync();
+      for (int i = half; i < cnt; i += 2) mx = fmaxf(mx, fmaf(-sPre[i].y, jr, sPre[i].x));
+    }
+    sMax[half * kRows + row] = mx;
+    tile_sync();
+    if (half == 0) {
+      const float m = fmaxf(sMax[row], sMax[kRows + row]);
+      sExp[row] = (m > -1e30f) ? max(-100, min(100, 13 - (int)ceilf(m))) : 0;
+    }
+    tile_sync();
+
+    // ---- tiles ----
+    const uint32_t sw = uint32_t(row & 7);
+    const float a_scale = exp2i(sExp[row]);
+    const int c = row, cq = c >> 3, c0 = c & 7;  // A row: chunk c
+    const int t = row & 63;                       // Bm row: lag t, Re (row < 64) or Im part
+    const bool imrow = row >= 64;
+    for (int kb = 0; kb < nkb; ++kb) {
+      const int s = kb & 1;
+      if (ok) ok = warp_wait(&tab_full[s], (kb >> 1) & 1);
+      if (ok && kb >= kStages) ok = warp_wait(&empty[s], ((kb >> 1) - 1) & 1);
       if (!ok) continue;
+      const float2* buf = reinterpret_cast<const float2*>(sm + kTabOff + s * kTabBuf);
+      const float2* p1 = buf + kPOff / 8;   // [kSB][8] lambda^e
+      const float2* p8 = p1 + kSB * 8;      // (lambda^8)^e
+      const float2* p64 = p8 + kSB * 8;     // (lambda^64)^e
+      const float2* q = buf + kQOff / 8;
       uint8_t* st = sm + s * kStageBytes;
-      // A: row c = chunk, 16 states of this thread's half; each state's (Re, Im) = 4 bytes
-      {
-        const int c = row, c0 = c & 7, c1 = (c >> 3) & 7, c2 = c >> 6;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {  // 16-byte chunk 4 half + q: states 16 half + 4 q + i
-          uint32_t hi[4], lo[4];
+      for (int qq = 0; qq < 4; ++qq) {  // 16-byte chunk 4 half + qq: states 16 half + 4 qq + i
+        uint32_t ahi[4], alo[4], bhi[4], blo[4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int nl = half * 16 + q * 4 + i;
-            const float2 pw = sP[(4 * kSB + nl) * 8 + c2];
-            const float2 p64 = sP[(2 * kSB + nl) * 8 + c0];
-            const float2 p512 = sP[(3 * kSB + nl) * 8 + c1];
-            const cf a = cmul(cmul({pw.x, pw.y}, {p512.x, p512.y}), {p64.x, p64.y});
-            split_h2(a.re * a_scale, a.im * a_scale, hi[i], lo[i]);
-          }
-          const uint32_t off = uint32_t(row) * 128u + (((uint32_t(half * 4 + q)) ^ sw) << 4);
-          *reinterpret_cast<uint4*>(st + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(st + kTile + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        for (int i = 0; i < 4; ++i) {
+          const int nl = half * 16 + qq * 4 + i;
+          const float2 a = f2mul(q[nl * 16 + cq], p64[nl * 8 + c0]);
+          split_h2(a.x * a_scale, a.y * a_scale, ahi[i], alo[i]);
+          const float2 l = f2mul(p1[nl * 8 + (t & 7)], p8[nl * 8 + (t >> 3)]);
+          split_h2(16384.f * (imrow ? l.y : l.x), 16384.f * (imrow ? l.x : -l.y), bhi[i], blo[i]);
         }
-      }
-      // Bm: row r = lag t (r < 64: the Re-part row [Re, -Im]; r >= 64: the Im-part row
-      // [Im, Re] of lag r - 64), scaled by 2^14
-      {
-        const int t = row & 63;
-        const bool imrow = row >= 64;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int nl = half * 16 + q * 4 + i;
-            const float2 p1 = sP[(0 * kSB + nl) * 8 + (t & 7)];
-            const float2 p8 = sP[(1 * kSB + nl) * 8 + (t >> 3)];
-            const cf b = cmul({p1.x, p1.y}, {p8.x, p8.y});
-            const float x = 16384.f * (imrow ? b.im : b.re);
-            const float y = 16384.f * (imrow ? b.re : -b.im);
-            split_h2(x, y, hi[i], lo[i]);
-          }
-          const uint32_t off = uint32_t(row) * 128u + (((uint32_t(half * 4 + q)) ^ sw) << 4);
-          *reinterpret_cast<uint4*>(st + 2 * kTile + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(st + 3 * kTile + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
+        const uint32_t off = uint32_t(row) * 128u + (((uint32_t(half * 4 + qq)) ^ sw) << 4);
+        *reinterpret_cast<uint4*>(st + off) = make_uint4(ahi[0], ahi[1], ahi[2], ahi[3]);
+        *reinterpret_cast<uint4*>(st + kTile + off) = make_uint4(alo[0], alo[1], alo[2], alo[3]);
+        *reinterpret_cast<uint4*>(st + 2 * kTile + off) =
+            make_uint4(bhi[0], bhi[1], bhi[2], bhi[3]);
+        *reinterpret_cast<uint4*>(st + 3 * kTile + off) =
+            make_uint4(blo[0], blo[1], blo[2], blo[3]);
       }
       tc::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&full[s]);
+      if (lane == 0) {
+        tc::mbar_arrive(&full[s]);
+        tc::mbar_arrive(&tab_empty[s]);
+      }
     }
   } else if (lane == 0) {
     // ---- MMA issuer ----
@@ -266,25 +328,25 @@ dlr_kernel_tc(const float* __restrict__ log_re, const float* __restrict__ log_im
     tc::mma_commit(done);
   }
 
-  // ---- epilogue: warps 0-3, thread = chunk row c (TMEM lane c) ----
-  if (warp < 4) {
+  // ---- epilogue: warps 4-7, thread = chunk row c (TMEM lane c) ----
+  if (warp >= 4 && warp < 8) {
     const bool acc_ok = ok && warp_wait(done, 0);
     tc::fence_after_sync();
-    const int c = tid;
+    const int q4 = warp & 3, c = q4 * 32 + lane;
     const float unscale = exp2i(-(sExp[c] + 14));
     float* krow = K + (size_t)h * L;
     const int jc = j0 + c * kT;
     const bool vec = (L & 3) == 0;
     // accumulators that received a block (nkb may be below kAcc)
     const int nacc = min(kAcc, nkb);
-    const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
+    const uint32_t lane_base = tmem + (uint32_t(q4 * 32) << 16);
     auto sum_acc = [&](uint32_t col, float (&out)[32]) {
       tc::tmem_ld32(lane_base + col, out);
       for (int a = 1; a < nacc; ++a) {
-        float t[32];
-        tc::tmem_ld32(lane_base + uint32_t(a) * 128u + col, t);
+        float tv[32];
+        tc::tmem_ld32(lane_base + uint32_t(a) * 128u + col, tv);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) out[i] += t[i];
+        for (int i = 0; i < 32; ++i) out[i] += tv[i];
       }
     };
 #pragma unroll 1
@@ -317,7 +379,7 @@ dlr_kernel_tc(const float* __restrict__ log_re, const float* __restrict__ log_im
   if (!ok) report_status(status, DLR_ERR_TIMEOUT);
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == 8) tc::tmem_dealloc(tmem, kTmemCols);
+  if (warp == 12) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
