@@ -35,8 +35,8 @@ __device__ __forceinline__ void small_powers(cf (&p)[8], cf x) {
 }
 
 // per state group: A[c][n], Bm[n][t], five evaluations per state, small-power tables, for
-// blocks of kNB states (16 keeps up to six CTAs per SM for small N, so the whole grid of the
-// usual shapes runs in one wave; 32 amortises the per-block work better when N is large)
+// blocks of kNB = 16 states (up to six CTAs per SM, so the whole grid of the usual shapes runs
+// in one wave; N >= 256 goes to the tensor-core generator)
 template <int kNB>
 struct GroupSmem {
   float2 sA[kC][kNB + 1];
@@ -215,12 +215,8 @@ cudaError_t launch_dlr_kernel_tc(const float* log_re, const float* log_im, const
 cudaError_t launch_dlr_kernel(const float* log_re, const float* log_im, const float* W, int H,
                               int N, int L, bool re_im, float* K, int* status, cudaStream_t s) {
   if (N >= 256) return launch_dlr_kernel_tc(log_re, log_im, W, H, N, L, re_im, K, status, s);
-  const bool big = N >= 256;
-  if (re_im)
-    return big ? launch_gen<true, 32>(log_re, log_im, W, H, N, L, K, s)
-               : launch_gen<true, 16>(log_re, log_im, W, H, N, L, K, s);
-  return big ? launch_gen<false, 32>(log_re, log_im, W, H, N, L, K, s)
-             : launch_gen<false, 16>(log_re, log_im, W, H, N, L, K, s);
+  return re_im ? launch_gen<true, 16>(log_re, log_im, W, H, N, L, K, s)
+               : launch_gen<false, 16>(log_re, log_im, W, H, N, L, K, s);
 }
 
 }  // namespace dlr
