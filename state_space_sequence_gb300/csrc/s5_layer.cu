@@ -18,7 +18,10 @@
 // The tensor-core tier runs the two projections on tcgen05 (tc_gemm.cu) with bf16 operands and
 // float32 accumulation: the input projection converts the float32 u to bf16 in the kernel and
 // writes V as bf16; the scan reads V in bf16 and computes in float32; apply writes x as bf16
-// over V, the operand of the output projection.
+// over V, the operand of the output projection. When L is a multiple of 64 (the usual case)
+// the chunk and apply steps move into the projections: the input projection's epilogue writes
+// the chunk end states in two 32-step halves, and the output projection turns its V operand
+// tiles into x itself, so the tier is prep, input projection, carry, output projection.
 #include <cuda_bf16.h>
 
 #include "dlr_common.cuh"

@@ -12,6 +12,9 @@
 //   warp 3 lane 0  loads B into the ring,
 //   warps 8-11     (float32 A only) convert: thread = row of the tile, 64 float32 of its row
 //                  from the staging slot to 64 bf16 in the operand layout of the ring,
+//   warps 8-13     (A = the S5 scan's V only) turn the A tile of each ring stage in place into
+//                  the scan's states, two warps per stage (one per chunk of 64 rows), lane =
+//                  state,
 //   warp 1 lane 0  MMA issuer: four K=16 MMAs per K-block, a commit that frees the stage, and
 //                  per tile a commit that hands one of two TMEM accumulators to the epilogue,
 //   warp 2         allocates / frees the 512 TMEM columns (two 256-column accumulators),
