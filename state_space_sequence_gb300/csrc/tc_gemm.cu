@@ -6,12 +6,13 @@
 // Persistent: one CTA per SM walks the 128 x 256 output tiles t = blockIdx.x, + gridDim.x, ...
 // with the N tile varying fastest (the CTAs working on the N tiles of one M tile at the same
 // time share its A rows through L2). Warps:
-//   warp 0 lane 0  TMA producer: K-blocks of 64 into a ring of 2-4 stages (A 16 KB + B 32 KB),
-//                  running ahead across tiles. With a float32 A it loads only A, as float32
-//                  (two 16 KB boxes per K-block), into a 3-slot staging ring, and
-//   warp 3 lane 0  loads B into the ring,
-//   warps 8-11     (float32 A only) convert: thread = row of the tile, 64 float32 of its row
-//                  from the staging slot to 64 bf16 in the operand layout of the ring,
+//   warp 0 lane 0  TMA producer: K-blocks of 64 into a ring of 3-4 stages (A 16 KB + B 32 KB),
+//                  running ahead across tiles. With a float32 A a stage holds A as float32
+//                  (two 16 KB boxes per K-block) and B; warp 0 then loads only A, and
+//   warp 3 lane 0  loads B,
+//   warps 8-11     (float32 A only) convert in place: thread = row r of the tile reads the 64
+//                  float32 of its row and writes them as 64 bf16 over the first 16 KB of the
+//                  stage, in the operand layout (row r is read and written by thread r only),
 //   warps 8-13     (A = the S5 scan's V only) turn the A tile of each ring stage in place into
 //                  the scan's states, two warps per stage (one per chunk of 64 rows), lane =
 //                  state,
@@ -55,17 +56,17 @@ enum OpMode { kOpBf16 = 0, kOpCvtA = 1, kOpApply = 2 };
 
 // Shared-memory plan. With E the epilogue keeps four boxes per warp (two E loads ahead) and
 // the ring three stages; without E two boxes suffice and the ring gets a fourth stage. With a
-// converted A the ring has two stages and a three-slot float32 staging ring (32 KB a slot)
-// feeds the converters.
+// float32 A a stage is 64 KB (A as float32, later bf16 in its first half, then B) and the ring
+// has three.
 template <bool kWithE, int kOp>
 struct Plan {
   static constexpr bool kCvt = kOp == kOpCvtA;
-  static constexpr int kStages = kCvt ? 2 : (kWithE ? 3 : 4);
-  static constexpr int kFStages = kCvt ? 3 : 0;
+  static constexpr int kStages = kCvt ? 3 : (kWithE ? 3 : 4);
   static constexpr uint32_t kFBytes = kBM * 2 * kRowBytes;  // 128 rows x 64 float32
+  static constexpr uint32_t kBOff = kCvt ? kFBytes : kABytes;  // B within a stage
+  static constexpr uint32_t kStride = kBOff + kBBytes;        // stage size
   static constexpr int kBoxes = kWithE ? 4 : 2;
-  static constexpr uint32_t kFOff = kStages * kStageBytes;
-  static constexpr uint32_t kEpiOff = kFOff + kFStages * kFBytes;
+  static constexpr uint32_t kEpiOff = kStages * kStride;
   static constexpr uint32_t kBarOff = kEpiOff + 4 * kBoxes * kBoxBytes;
   static constexpr size_t kSmemBytes = 1024 + kBarOff + 256;
   static constexpr int kThreads = kOp == kOpBf16 ? 256 : (kOp == kOpCvtA ? 384 : 448);
@@ -102,7 +103,7 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
   static_assert(!(kWithE && kOp == kOpCvtA), "no plan for E with a converted A");
   constexpr bool kCvt = kOp == kOpCvtA, kApply = kOp == kOpApply;
   using PL = Plan<kWithE, kOp>;
-  constexpr int kStages = PL::kStages, kBoxes = PL::kBoxes, kF = PL::kFStages;
+  constexpr int kStages = PL::kStages, kBoxes = PL::kBoxes;
   constexpr int kSlice = kBf16Out ? 64 : 32;  // output columns per slice (128 bytes per row)
   constexpr int kSlices = kBN / kSlice;
   extern __shared__ uint8_t smem_raw[];
@@ -115,9 +116,8 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
   uint64_t* acc_empty = acc_full + 2;          // [2]        accumulator read out (4 arrivals)
   uint64_t* e_full = acc_empty + 2;            // [4][kBoxes] E box landed
   uint64_t* a_ready = e_full + 4 * kBoxes;     // [kStages]  converted A written (4 arrivals)
-  uint64_t* f_full = a_ready + kStages;        // [kF]       float32 A slot landed
-  uint64_t* f_empty = f_full + kF;             // [kF]       float32 A slot read (4 arrivals)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(f_empty + kF);
+  uint64_t* f_full = a_ready + kStages;        // [kStages]  float32 A landed (kCvt)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(f_full + kStages);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_tiles = (g.N + kBN - 1) / kBN;
@@ -137,10 +137,7 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
     }
     for (int i = 0; i < 4 * kBoxes; ++i) tc::mbar_init(&e_full[i], 1);
     for (int s = 0; s < kStages; ++s) tc::mbar_init(&a_ready[s], kCvt ? 4 : 2);
-    for (int s = 0; s < kF; ++s) {
-      tc::mbar_init(&f_full[s], 1);
-      tc::mbar_init(&f_empty[s], 4);
-    }
+    for (int s = 0; s < kStages; ++s) tc::mbar_init(&f_full[s], 1);
     tc::mbar_fence_init();
   }
   if (warp == 2) {
@@ -161,32 +158,31 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % kStages;
           if (it >= kStages && !(ok = tc::mbar_wait(&empty[s], ((it / kStages) - 1) & 1))) break;
-          uint8_t* a = base + s * kStageBytes;
+          uint8_t* a = base + s * PL::kStride;
           tc::mbar_arrive_expect_tx(&full[s], kStageBytes);
           tc::tma_load_2d(a, &tmA, kb * kBK, m0, &full[s]);
-          tc::tma_load_2d(a + kABytes, &tmB, kb * kBK, n0, &full[s]);
+          tc::tma_load_2d(a + PL::kBOff, &tmB, kb * kBK, n0, &full[s]);
         }
       }
       // before the CTA may exit, every copy it issued has landed (normally long since consumed)
       for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j)
         ok &= tc::mbar_wait(&full[j % kStages], (j / kStages) & 1);
     } else {
-      // converted A: float32 K-blocks of 64 (two 128-byte boxes) into the staging ring
-      uint8_t* fst = base + PL::kFOff;
+      // converted A: float32 K-blocks of 64 (two 128-byte boxes) into the stage
       uint32_t it = 0;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         const int m0 = (t / n_tiles) * kBM;
         for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int fs = it % kF;
-          if (it >= kF && !(ok = tc::mbar_wait(&f_empty[fs], ((it / kF) - 1) & 1))) break;
-          uint8_t* f = fst + fs * PL::kFBytes;
-          tc::mbar_arrive_expect_tx(&f_full[fs], PL::kFBytes);
-          tc::tma_load_2d(f, &tmA, kb * kBK, m0, &f_full[fs]);
-          tc::tma_load_2d(f + PL::kFBytes / 2, &tmA, kb * kBK + kBK / 2, m0, &f_full[fs]);
+          const int s = it % kStages;
+          if (it >= kStages && !(ok = tc::mbar_wait(&empty[s], ((it / kStages) - 1) & 1))) break;
+          uint8_t* f = base + s * PL::kStride;
+          tc::mbar_arrive_expect_tx(&f_full[s], PL::kFBytes);
+          tc::tma_load_2d(f, &tmA, kb * kBK, m0, &f_full[s]);
+          tc::tma_load_2d(f + PL::kFBytes / 2, &tmA, kb * kBK + kBK / 2, m0, &f_full[s]);
         }
       }
-      for (uint32_t j = it > kF ? it - kF : 0; j < it; ++j)
-        ok &= tc::mbar_wait(&f_full[j % kF], (j / kF) & 1);
+      for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j)
+        ok &= tc::mbar_wait(&f_full[j % kStages], (j / kStages) & 1);
     }
   } else if (warp == 3 && lane == 0) {
     if constexpr (kCvt) {
@@ -198,7 +194,7 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
           const int s = it % kStages;
           if (it >= kStages && !(ok = tc::mbar_wait(&empty[s], ((it / kStages) - 1) & 1))) break;
           tc::mbar_arrive_expect_tx(&full[s], kBBytes);
-          tc::tma_load_2d(base + s * kStageBytes + kABytes, &tmB, kb * kBK, n0, &full[s]);
+          tc::tma_load_2d(base + s * PL::kStride + PL::kBOff, &tmB, kb * kBK, n0, &full[s]);
         }
       }
       for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j)
@@ -207,16 +203,16 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
   } else if (warp >= 8) {
     if constexpr (kCvt) {
       // converters: thread = row r of the tile; 64 float32 of row r -> 64 bf16 in the K-major
-      // 128-byte-swizzled layout the MMA reads (16-byte chunk c of row r at (c ^ (r & 7)) << 4)
+      // 128-byte-swizzled layout the MMA reads (16-byte chunk c of row r at (c ^ (r & 7)) << 4),
+      // written over row r of the first float32 box (read by this thread alone)
       const int r = (warp - 8) * 32 + lane;
       const uint32_t sw = uint32_t(r & 7);
-      uint8_t* fst = base + PL::kFOff;
       uint32_t it = 0;
       for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
         for (int kb = 0; kb < nk && ok; ++kb, ++it) {
-          const int fs = it % kF, s = it % kStages;
-          if (!(ok = warp_wait(&f_full[fs], (it / kF) & 1))) break;
-          const uint8_t* f = fst + fs * PL::kFBytes + r * kRowBytes;
+          const int s = it % kStages;
+          if (!(ok = warp_wait(&f_full[s], (it / kStages) & 1))) break;
+          uint8_t* f = base + s * PL::kStride + r * kRowBytes;
           float4 v[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c)
@@ -234,13 +230,9 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
                               *reinterpret_cast<const uint32_t*>(&b2),
                               *reinterpret_cast<const uint32_t*>(&b3));
           }
-          __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&f_empty[fs]);  // the slot's values are in registers
-          if (it >= kStages && !(ok = warp_wait(&empty[s], ((it / kStages) - 1) & 1))) break;
-          uint8_t* a = base + s * kStageBytes + r * kRowBytes;
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(a + ((uint32_t(c) ^ sw) << 4)) = h[c];
+            *reinterpret_cast<uint4*>(f + ((uint32_t(c) ^ sw) << 4)) = h[c];
           tc::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&a_ready[s]);
@@ -278,7 +270,7 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
           if (!(ok = warp_wait(&full[s], (it / kStages) & 1))) break;
           const int m0 = (blockIdx.x + int(it / nk) * gridDim.x) / n_tiles * kBM + h * 64;
           const int rows = min(64, g.M - m0);
-          uint8_t* a = base + s * kStageBytes;
+          uint8_t* a = base + s * PL::kStride;
 #pragma unroll 1
           for (int i0 = h * 64; i0 < h * 64 + rows; i0 += 16) {
             uint32_t* ptr[16];
@@ -320,9 +312,9 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
         if (!(ok = tc::mbar_wait(&full[s], (it / kStages) & 1))) break;
         if ((kCvt || kApply) && !(ok = tc::mbar_wait(&a_ready[s], (it / kStages) & 1))) break;
         tc::fence_after_sync();
-        const uint8_t* a = base + s * kStageBytes;
+        const uint8_t* a = base + s * PL::kStride;
         const uint64_t ad = tc::smem_desc_k_sw128(a);
-        const uint64_t bd = tc::smem_desc_k_sw128(a + kABytes);
+        const uint64_t bd = tc::smem_desc_k_sw128(a + PL::kBOff);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)  // advance 16 bf16 = 32 bytes = 2 descriptor units
           tc::mma_kind_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, (kb | kk) != 0);
