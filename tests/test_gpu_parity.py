@@ -41,10 +41,11 @@ def check_status():
 # dlr_kernel
 
 # N >= 256 runs the tensor-core generator: a whole tile of 128 chunks, ragged blocks of
-# states and a ragged last chunk, the DLR-prod shape, and a tile that is mostly past L
+# states and a ragged last chunk, the DLR-prod shape, a tile that is mostly past L, and more
+# states than one pass of the row-scale pre-pass takes (1024)
 @pytest.mark.parametrize("H,N,L", [(1, 1, 1), (3, 5, 1000), (2, 16, 256), (4, 64, 4096),
                                    (2, 33, 4097), (2, 64, 70000), (2, 256, 8192), (3, 300, 5000),
-                                   (1, 1024, 16384), (2, 257, 100)])
+                                   (1, 1024, 16384), (2, 257, 100), (2, 1100, 9000)])
 @pytest.mark.parametrize("cast", ["re", "re_im"])
 def test_kernel_matches_oracle(H, N, L, cast):
     w = inputs.make_dlr(1, H, N, 1, seed=H * 1000 + N, unit_channels=min(1, H))
