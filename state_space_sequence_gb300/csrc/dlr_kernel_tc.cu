@@ -72,8 +72,10 @@ __device__ __forceinline__ void tile_sync() {
 __device__ __forceinline__ void tab_sync() {
   asm volatile("bar.sync 2, %0;" ::"n"(kTab) : "memory");
 }
+// Bounded wait by a whole warp with one verdict for its lanes; the tries may suspend the warp,
+// which keeps waiting warps off the issue slots the table and tile warps need.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
-  return __all_sync(0xffffffffu, tc::mbar_wait(bar, parity)) != 0;
+  return __all_sync(0xffffffffu, tc::mbar_wait_sleep(bar, parity)) != 0;
 }
 __device__ __forceinline__ float exp2i(int s) { return __int_as_float((s + 127) << 23); }
 
@@ -309,7 +311,7 @@ dlr_kernel_tc(const float* __restrict__ log_re, const float* __restrict__ log_im
     constexpr uint32_t idesc = tc::idesc_f16_f32(kRows, 128);
     for (int kb = 0; kb < nkb && ok; ++kb) {
       const int s = kb % kStages;
-      if (!(ok = tc::mbar_wait(&full[s], (kb / kStages) & 1))) break;
+      if (!(ok = tc::mbar_wait_sleep(&full[s], (kb / kStages) & 1))) break;
       tc::fence_after_sync();
       const uint8_t* st = sm + s * kStageBytes;
       const uint32_t d = tmem + uint32_t(kb % kAcc) * 128u;

@@ -84,6 +84,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// The same wait, but each try may suspend the thread (for up to about 0.5 us) while the phase is
+// incomplete, so waiting warps leave the issue slots to the working ones.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait_hint(bar, parity, 500)) return true;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // ---- TMA ---------------------------------------------------------------------------------
 // 2D tile load (x = innermost coordinate, in elements) into shared memory, completing
 // `bytes` of transaction count on `bar`.
