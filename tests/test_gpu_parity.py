@@ -346,10 +346,13 @@ def state_part(y, u, D):
 # (3, 7000, 64, 32): 165 row tiles, more than there are SMs, so CTAs of the persistent GEMM
 # take several tiles, the last one ragged. L a multiple of 64 takes the output projection with
 # the scan's apply step fused in: (3, 64, 64, 32) has tiles spanning two batch rows and a
-# ragged last tile, (2, 640, 96, 64) and (1, 192, 32, 32) several chunks per row.
+# ragged last tile, (2, 640, 96, 64) and (1, 192, 32, 32) several chunks per row; (1, 256, 64,
+# 512) and (2, 128, 96, 1024) run the in-place apply over 16 and 32 blocks of states (P up to the
+# limit of 1024).
 @pytest.mark.parametrize("B,L,H,P", [(1, 1, 32, 32), (1, 200, 64, 32), (2, 1000, 96, 64),
                                      (1, 300, 512, 256), (3, 7000, 64, 32), (3, 64, 64, 32),
-                                     (2, 640, 96, 64), (1, 192, 32, 32), (2, 4096, 512, 256)])
+                                     (2, 640, 96, 64), (1, 192, 32, 32), (2, 4096, 512, 256),
+                                     (1, 256, 64, 512), (2, 128, 96, 1024)])
 def test_s5_bf16_tensor_cores_match_oracle(B, L, H, P):
     w = inputs.make_s5(B, L, H, P, seed=7 * B + L + H + P)
     y = host(dlr.s5_layer(dev(w.u), *s5_dev(w.params), prec="bf16"))
