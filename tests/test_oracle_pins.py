@@ -362,8 +362,77 @@ def test_s5_feedthrough_and_linearity():
     np.testing.assert_allclose(ysum, a * y1 + b * y2, rtol=1e-5, atol=1e-6)
 
 
+def test_s5_zoh_small_step_limit():
+    """S5 section 3.2: for a small step the ZOH input matrix tends to Delta B~; the next two
+    terms of the series of (e^{lambda Delta} - 1)/lambda are Delta^2 lambda/2 and
+    Delta^3 lambda^2/6, so B_bar - Delta B~ (1 + lambda Delta/2) is bounded by the third."""
+    lam = np.array([[-0.5, 2.0], [-0.5, -7.0], [-0.5, 19.0]], np.float32)
+    Bt = np.array([[[0.3, -1.1]], [[-0.8, 0.2]], [[1.4, 0.9]]], np.float32)
+    for step in (1e-3, 1e-5):
+        ld = np.full(3, np.log(step), np.float32)
+        abar, bbar = oracle.s5_zoh(lam, ld, Bt)
+        delta = np.exp(ld.astype(np.float64))
+        lamc = lam[:, 0].astype(np.float64) + 1j * lam[:, 1]
+        Btc = Bt[:, 0, 0].astype(np.float64) + 1j * Bt[:, 0, 1]
+        first = delta * Btc
+        second = first * (1 + lamc * delta / 2)
+        # plus the double rounding of e^{lambda Delta} - 1, relative eps / |lambda Delta|
+        bound = np.abs(first) * (np.abs(lamc * delta) ** 2 / 6 * 1.01 +
+                                 4e-16 / np.abs(lamc * delta))
+        assert np.all(np.abs(bbar[:, 0] - second) <= bound)
+        assert np.all(np.abs(bbar[:, 0] - first) > 0.4 * np.abs(first * lamc * delta))
+        np.testing.assert_allclose(np.abs(abar), np.exp(-0.5 * delta), rtol=1e-14)
+
+
+def test_s5_one_state_one_feature_is_a_scalar_filter():
+    """P = 1, H = 1: the layer is the first-order complex filter x_k = a x_{k-1} + b u_k
+    (scipy lfilter) with a, b from the block exponential of [[lambda Delta, Delta B~], [0, 0]],
+    read out as Re(c x_k) + d u_k."""
+    lam = np.array([[-0.3, 1.7]], np.float32)
+    ld = np.array([np.log(0.2)], np.float32)
+    Bt = np.array([[[0.6, -0.9]]], np.float32)
+    Ct = np.array([[[-1.2, 0.4]]], np.float32)
+    D = np.array([0.35], np.float32)
+    rng = np.random.default_rng(35)
+    u = rng.standard_normal((2, 64, 1)).astype(np.float32)
+    y = oracle.s5_layer(u, lam, ld, Bt, Ct, D)
+    delta = float(np.exp(np.float64(ld[0])))
+    lamc = complex(float(lam[0, 0]), float(lam[0, 1]))
+    E = scipy.linalg.expm(np.array([[lamc * delta, delta * complex(float(Bt[0, 0, 0]),
+                                                                    float(Bt[0, 0, 1]))],
+                                    [0, 0]]))
+    a, b = E[0, 0], E[0, 1]
+    c = complex(float(Ct[0, 0, 0]), float(Ct[0, 0, 1]))
+    for r in range(2):
+        ur = u[r, :, 0].astype(np.float64)
+        x = scipy.signal.lfilter([b], [1.0, -a], ur.astype(complex))
+        np.testing.assert_allclose(y[r, :, 0], (c * x).real + float(D[0]) * ur, rtol=1e-11,
+                                   atol=1e-13)
+
+
 # ---------------------------------------------------------------------------------------
 # Input generator structure (HiPPO-N spectrum)
+
+@pytest.mark.parametrize("P", [4, 16, 64])
+def test_hippo_n_normal_plus_low_rank(P):
+    """Annotated S4 part 2: HiPPO-LegS is a normal matrix minus a rank-one term, A = S - p p^T
+    with S normal, so S = V Lambda V^* for a unitary V. Rebuild A from the generator's
+    eigenvalues and a unitary eigenbasis of S, and check S S^T = S^T S."""
+    n = np.arange(P, dtype=np.float64)
+    p = np.sqrt(n + 0.5)
+    A = inputs.hippo_legs(P)
+    S = A + np.outer(p, p)
+    np.testing.assert_allclose(S @ S.T, S.T @ S, atol=1e-9 * P * P)
+    mu, V = np.linalg.eigh(-1j * (S + 0.5 * np.eye(P)))  # Hermitian: V unitary
+    np.testing.assert_allclose(V.conj().T @ V, np.eye(P), atol=1e-12 * P)
+    lam = inputs.hippo_n_eigenvalues(P).astype(np.float64)
+    lam = lam[np.argsort(lam[:, 1])]
+    lamc = lam[:, 0] + 1j * lam[:, 1]
+    A_rec = (V * lamc) @ V.conj().T - np.outer(p, p)
+    scale = np.max(np.abs(lam[:, 1]))
+    np.testing.assert_allclose(A_rec.real, A, atol=1e-6 * scale)
+    np.testing.assert_allclose(A_rec.imag, 0.0, atol=1e-6 * scale)
+
 
 def test_hippo_legs_golden():
     rows = []
