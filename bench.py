@@ -396,7 +396,23 @@ def run_extras(torch, dlr, inputs, flush, sm_mhz, sm_count):
     del K, wsf
     ms = _time_steps(torch, lambda: dlr.dlr_scan(u, fwd, out=y, algo="fp32"), 20, 3, flush)
     out["scan_fp32_" + WORKLOAD] = {"ms": ms, "elements_per_s": B * H * L / ms * 1e3}
-    del u, y
+    # the recurrent mode (dlr_step) on the same bank: one sample per call (decode: the state
+    # is read and written once, with the per-channel tables), and the whole sequence in one
+    # call from a zero state (sequential in the samples)
+    N = w.N
+    wss = dlr.dlr_step_prepare(fwd)
+    xs = torch.zeros((B, H, N, 2), dtype=torch.float32, device="cuda")
+    u1, y1 = u[:, :, :1].contiguous(), torch.empty((B, H, 1), dtype=torch.float32, device="cuda")
+    us_dec = _time_steps(torch, lambda: dlr.dlr_step(u1, wss, xs, out=y1), 50, 5, flush) * 1e3
+    dec_bytes = 2 * B * H * N * 8 + 2 * B * H * 4 + H * N * 24
+    ms = _time_steps(torch, lambda: (xs.zero_(), dlr.dlr_step(u, wss, xs, out=y)), 10, 2, flush)
+    peak_gbs, peak_kind = load_peaks()
+    out["step_" + WORKLOAD] = {
+        "decode_us": us_dec, "decode_bytes": dec_bytes,
+        "decode_gbs": dec_bytes / us_dec / 1e3,
+        "decode_frac": dec_bytes / us_dec / 1e3 / peak_gbs, "peak_kind": peak_kind,
+        "sequence_ms": ms, "sequence_elements_per_s": B * H * L / ms * 1e3}
+    del u, y, xs, wss
 
     w = inputs.make_workload("dlrprod_bidir_b4_h128_n1024_l16384")
     u = dev(w.u)

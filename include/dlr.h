@@ -205,6 +205,31 @@ dlr_status dlr_scan_host(const float* u, const float* log_re, const float* log_i
                          void* workspace, size_t workspace_bytes, dlr_stream_t stream);
 
 /*
+ * dlr_step_prepare + dlr_step -- the causal DLR layer (Re cast) advanced from a carried state,
+ * the recurrent mode used to feed a sequence a few samples at a time ("The Annotated S4",
+ * part 1 "An SSM Neural Network": the layer's RNN mode with its state cache; part 3 "Sampling
+ * and Caching"):
+ *   x_{n,t} = lambda_n x_{n,t-1} + u_t,   y_t = sum_n Re(W_n x_{n,t}),   t = 0 .. T-1,
+ * with x_{n,-1} the state found in x on entry; on return x holds x_{n,T-1}. A zero x starts a
+ * fresh sequence, and feeding a sequence in consecutive pieces gives the outputs of one
+ * dlr_scan over the whole of it (DLR paper section 2, Eq. 1).
+ * dlr_step_prepare evaluates lambda_n = exp(-(log_re)^2 + i log_im) of one parameter set
+ * (log_re, log_im [H, N], W [H, N, 2]) in double precision and keeps it as a float pair, with
+ * W, in `workspace` (device, >= dlr_step_workspace_size(H, N) bytes, 16-byte aligned).
+ * dlr_step reads those tables (same H and N, earlier in stream order) and u [B, H, T],
+ * updates x [B, H, N, 2] (float pairs, read and written) and writes y [B, H, T]. u, y, x and
+ * the workspace must not overlap. T = 0 returns at once. Limits: N <= 256, T < 2^24. One
+ * kernel launch each.
+ */
+size_t dlr_step_workspace_size(int64_t H, int64_t N);
+dlr_status dlr_step_prepare(const float* log_re, const float* log_im, const float* W, int64_t H,
+                            int64_t N, void* workspace, size_t workspace_bytes,
+                            dlr_stream_t stream);
+dlr_status dlr_step(const float* u, int64_t B, int64_t H, int64_t N, int64_t T, float* x,
+                    float* y, const void* workspace, size_t workspace_bytes,
+                    dlr_stream_t stream);
+
+/*
  * s5_layer -- S5 SSM outputs (S5 paper section 3: diagonalised MIMO system; zero-order hold
  * with one timescale per state; diagonal feedthrough):
  *   Delta_p   = exp(log_delta[p])

@@ -33,6 +33,11 @@ cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delt
                       const float* Bt, const float* Ct, const float* D, int B, int L, int H, int P,
                       bool bf16, float* y, void* ws, int* status, cudaStream_t s);
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
+size_t step_workspace_bytes(int64_t H, int64_t N);
+cudaError_t launch_step_tables(const float* lr, const float* li, const float* W, int64_t H,
+                               int64_t N, void* ws, cudaStream_t s);
+cudaError_t launch_step(const float* u, int64_t B, int64_t H, int64_t N, int64_t T,
+                        const void* ws, float* x, float* y, cudaStream_t s);
 }  // namespace dlr
 
 // The library's device status word (one per device that loads the library).
@@ -100,7 +105,7 @@ dlr_status check_params(const float* log_re, const float* log_im, const float* W
 
 extern "C" {
 
-int dlr_abi_version(void) { return 4; }
+int dlr_abi_version(void) { return 5; }
 
 const char* dlr_last_cuda_error(void) { return t_last_cuda_error; }
 
@@ -267,6 +272,44 @@ dlr_status dlr_scan_apply(const float* u, int64_t B, int64_t H, int64_t N, int64
   return from_cuda(dlr::launch_scan_tc_apply(u, (int)B, (int)H, (int)L, reverse != 0, y,
                                              workspace, status_word(), (cudaStream_t)stream,
                                              false));
+}
+
+size_t dlr_step_workspace_size(int64_t H, int64_t N) {
+  if (H < 1 || N < 1 || N > 256 || H > (int64_t(1) << 31)) return 0;
+  return dlr::step_workspace_bytes(H, N);
+}
+
+dlr_status dlr_step_prepare(const float* log_re, const float* log_im, const float* W, int64_t H,
+                            int64_t N, void* workspace, size_t workspace_bytes,
+                            dlr_stream_t stream) {
+  if (H < 1 || N < 1) return DLR_ERR_INVALID_ARG;
+  dlr_status st = check_params(log_re, log_im, W);
+  if (st != DLR_OK) return st;
+  if (N > 256 || H > (int64_t(1) << 31)) return DLR_ERR_UNSUPPORTED;
+  const size_t need = dlr::step_workspace_bytes(H, N);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DLR_ERR_WORKSPACE;
+  return from_cuda(dlr::launch_step_tables(log_re, log_im, W, H, N, workspace,
+                                           (cudaStream_t)stream));
+}
+
+dlr_status dlr_step(const float* u, int64_t B, int64_t H, int64_t N, int64_t T, float* x,
+                    float* y, const void* workspace, size_t workspace_bytes,
+                    dlr_stream_t stream) {
+  if (B < 1 || H < 1 || N < 1 || T < 0) return DLR_ERR_INVALID_ARG;
+  if (N > 256 || T > kMaxL || B * H > kMaxGrid) return DLR_ERR_UNSUPPORTED;
+  if (!x || !aligned16(x)) return DLR_ERR_INVALID_ARG;
+  const size_t need = dlr::step_workspace_bytes(H, N);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DLR_ERR_WORKSPACE;
+  const size_t xbytes = 2 * sizeof(float) * (size_t)B * (size_t)H * (size_t)N;
+  if (ranges_overlap(workspace, need, x, xbytes)) return DLR_ERR_INVALID_ARG;
+  if (T == 0) return DLR_OK;
+  if (!u || !y || !aligned16(u) || !aligned16(y)) return DLR_ERR_INVALID_ARG;
+  const size_t bytes = sizeof(float) * (size_t)B * (size_t)H * (size_t)T;
+  if (ranges_overlap(u, bytes, y, bytes) || ranges_overlap(x, xbytes, u, bytes) ||
+      ranges_overlap(x, xbytes, y, bytes) || ranges_overlap(workspace, need, u, bytes) ||
+      ranges_overlap(workspace, need, y, bytes))
+    return DLR_ERR_INVALID_ARG;
+  return from_cuda(dlr::launch_step(u, B, H, N, T, workspace, x, y, (cudaStream_t)stream));
 }
 
 size_t s5_workspace_size(int64_t B, int64_t L, int64_t H, int64_t P, dlr_prec prec) {

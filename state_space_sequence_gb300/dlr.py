@@ -63,6 +63,12 @@ def _load():
         lib.dlr_scan_host_workspace_size.restype = sz
         lib.dlr_scan_host.argtypes = [P, P, P, P, i64, i64, i64, i64, P, P, sz, P]
         lib.dlr_scan_host.restype = i32
+        lib.dlr_step_workspace_size.argtypes = [i64, i64]
+        lib.dlr_step_workspace_size.restype = sz
+        lib.dlr_step_prepare.argtypes = [P, P, P, i64, i64, P, sz, P]
+        lib.dlr_step_prepare.restype = i32
+        lib.dlr_step.argtypes = [P, i64, i64, i64, i64, P, P, P, sz, P]
+        lib.dlr_step.restype = i32
         lib.s5_workspace_size.argtypes = [i64, i64, i64, i64, i32]
         lib.s5_workspace_size.restype = sz
         lib.s5_layer.argtypes = [P, P, P, P, P, P, i64, i64, i64, i64, i32, P, P, sz, P]
@@ -232,6 +238,44 @@ def dlr_scan_apply(u, workspace, N: int, out=None, reverse: bool = False, stream
     _ok("dlr_scan_apply", _load().dlr_scan_apply(_ptr(u), B, H, N, L, 1 if reverse else 0,
                                                  _ptr(out), _ptr(workspace), workspace.numel(),
                                                  _stream(stream)))
+    return out
+
+
+def dlr_step_workspace_size(H: int, N: int) -> int:
+    return int(_load().dlr_step_workspace_size(H, N))
+
+
+def dlr_step_prepare(params, workspace=None, stream=None):
+    """lambda (as a float pair) and W of one parameter set (log_re, log_im, W) for dlr_step,
+    into a uint8 device ``workspace`` of dlr_step_workspace_size bytes (allocated here when not
+    given)."""
+    lr, li, W = _params(params)
+    H, N = lr.shape
+    need = dlr_step_workspace_size(H, N)
+    if need == 0:
+        raise ValueError(f"dlr_step: unsupported H={H}, N={N}")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=lr.device)
+    _ok("dlr_step_prepare", _load().dlr_step_prepare(_ptr(lr), _ptr(li), _ptr(W), H, N,
+                                                     _ptr(workspace), workspace.numel(),
+                                                     _stream(stream)))
+    return workspace
+
+
+def dlr_step(u, workspace, state, out=None, stream=None):
+    """Advance the causal DLR layer over u [B, H, T] from ``state`` [B, H, N, 2] (float32,
+    updated in place: on return it holds the state after the last sample), with the tables of
+    dlr_step_prepare in ``workspace``. Returns y [B, H, T]."""
+    _check_f32(u, state)
+    B, H, T = u.shape
+    if state.dim() != 4 or tuple(state.shape[:2]) != (B, H) or state.shape[3] != 2:
+        raise ValueError("state must be [B, H, N, 2]")
+    N = state.shape[2]
+    if out is None:
+        out = torch.empty_like(u)
+    _check_f32(out)
+    _ok("dlr_step", _load().dlr_step(_ptr(u), B, H, N, T, _ptr(state), _ptr(out),
+                                     _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
 
 

@@ -31,7 +31,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ["dlr_kernel", "dlr_conv", "dlr_conv_workspace_size", "dlr_scan", "s5_layer",
                  "s5_workspace_size", "dlr_get_device_status", "dlr_status_string",
-                 "dlr_abi_version"]:
+                 "dlr_abi_version", "dlr_step_prepare", "dlr_step", "dlr_step_workspace_size"]:
         assert must in names, must
 
 
@@ -44,7 +44,7 @@ def test_status_strings_and_version(lib):
     lib.dlr_status_string.restype = ctypes.c_char_p
     assert lib.dlr_status_string(0) == b"DLR_OK"
     assert lib.dlr_status_string(4) == b"DLR_ERR_TIMEOUT"
-    assert lib.dlr_abi_version() == 4
+    assert lib.dlr_abi_version() == 5
 
 
 def test_host_validation_rejects_bad_arguments(lib):
@@ -133,3 +133,29 @@ def test_workspace_queries(lib):
     lib.s5_workspace_size.restype = ctypes.c_size_t
     lib.s5_workspace_size.argtypes = [ctypes.c_int64] * 4 + [ctypes.c_int]
     assert lib.s5_workspace_size(8, 16384, 512, 256, 0) >= 8 * 16384 * 512 * 4
+
+
+def test_step_validation(lib):
+    """dlr_step_prepare / dlr_step: sizes, limits, workspace and overlap are checked on the
+    host before anything is launched."""
+    P, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    lib.dlr_step_workspace_size.restype = sz
+    lib.dlr_step_workspace_size.argtypes = [i64, i64]
+    assert lib.dlr_step_workspace_size(256, 64) == 256 * 64 * 24
+    assert lib.dlr_step_workspace_size(4, 257) == 0
+    lib.dlr_step_prepare.argtypes = [P, P, P, i64, i64, P, sz, P]
+    fake = ctypes.c_void_p(0x1000)
+    ws = ctypes.c_void_p(0x100000)
+    assert lib.dlr_step_prepare(fake, fake, fake, 0, 4, ws, 1 << 20, None) == 1
+    assert lib.dlr_step_prepare(fake, fake, fake, 2, 300, ws, 1 << 20, None) == 2
+    assert lib.dlr_step_prepare(fake, fake, fake, 2, 4, ws, 10, None) == 5
+    lib.dlr_step.argtypes = [P, i64, i64, i64, i64, P, P, P, sz, P]
+    u, x, y = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30000)
+    # negative T, too many states, missing workspace
+    assert lib.dlr_step(u, 1, 2, 4, -1, x, y, ws, 1 << 20, None) == 1
+    assert lib.dlr_step(u, 1, 2, 300, 8, x, y, ws, 1 << 20, None) == 2
+    assert lib.dlr_step(u, 1, 2, 4, 8, x, y, None, 0, None) == 5
+    # T = 0 launches nothing and succeeds; u and y overlapping; x overlapping y
+    assert lib.dlr_step(None, 1, 2, 4, 0, x, None, ws, 1 << 20, None) == 0
+    assert lib.dlr_step(u, 1, 2, 4, 8, x, ctypes.c_void_p(0x10010), ws, 1 << 20, None) == 1
+    assert lib.dlr_step(u, 1, 2, 4, 8, x, ctypes.c_void_p(0x20010), ws, 1 << 20, None) == 1

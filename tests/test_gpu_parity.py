@@ -222,6 +222,72 @@ def test_scan_host_buffers_match_oracle_and_device_path(B, H, N, L):
     check_status()
 
 
+# ------------------------------------------------------------------------------------------
+# dlr_step (the recurrence advanced from a carried state)
+
+def _step_pieces(u_d, ws, x, pieces):
+    ys, t = [], 0
+    for n in pieces:
+        ys.append(dlr.dlr_step(u_d[:, :, t:t + n].contiguous(), ws, x))
+        t += n
+    assert t == u_d.shape[2]
+    return torch.cat(ys, dim=2)
+
+
+# states per lane 1, 2, 4, 8 with ragged last lanes; pieces of 1, across and on the 32-sample
+# blocks, empty, and longer than several blocks
+@pytest.mark.parametrize("B,H,N", [(2, 3, 5), (3, 2, 33), (8, 16, 64), (1, 4, 129), (2, 2, 256)])
+def test_step_pieces_match_oracle(B, H, N):
+    """Feeding a sequence in pieces through dlr_step, starting from zero, gives the oracle's
+    outputs of the whole sequence and its final state."""
+    pieces = [1, 1, 5, 31, 32, 33, 0, 100, 257]
+    L = sum(pieces)
+    w = inputs.make_dlr(B, H, N, L, seed=7 * B + H + N, unit_channels=1)
+    ws = dlr.dlr_step_prepare(params_dev(w.fwd))
+    x = torch.zeros((B, H, N, 2), dtype=torch.float32, device="cuda")
+    y = _step_pieces(dev(w.u), ws, x, pieces)
+    y_ref, x_ref = oracle.dlr_recurrence(w.u, *params_np(w.fwd), return_state=True)
+    assert oracle.rel_l2(host(y), y_ref) <= TOL
+    xs = host(x)
+    assert oracle.rel_l2(xs, np.stack([x_ref.real, x_ref.imag], -1)) <= TOL  # (re, im) pairs
+    check_status()
+
+
+def test_step_from_a_given_state():
+    """A nonzero carried state: y and the final state follow the oracle's recurrence from the
+    same initial state."""
+    B, H, N, L = 3, 5, 40, 300
+    w = inputs.make_dlr(B, H, N, L, seed=41, unit_channels=1)
+    rng = np.random.default_rng(42)
+    x0 = (rng.standard_normal((B, H, N, 2)) * 3).astype(np.float32)
+    ws = dlr.dlr_step_prepare(params_dev(w.fwd))
+    x = dev(x0)
+    y = dlr.dlr_step(dev(w.u), ws, x)
+    x0c = x0[..., 0].astype(np.float64) + 1j * x0[..., 1]
+    y_ref, x_ref = oracle.dlr_recurrence(w.u, *params_np(w.fwd), x0=x0c, return_state=True)
+    assert oracle.rel_l2(host(y), y_ref) <= TOL
+    xs = host(x)
+    assert oracle.rel_l2(xs, np.stack([x_ref.real, x_ref.imag], -1)) <= TOL  # (re, im) pairs
+    check_status()
+
+
+def test_step_bank_and_long_unit_circle_stream():
+    """The B=8 H=256 N=64 L=4096 bank fed in pieces of 512, and a stream of 16384 samples
+    through 16 channels of which 8 sit at |lambda| = 1, fed in pieces of 4096: both against
+    the oracle (the step path agrees with the chunked scan through it)."""
+    w = inputs.make_workload("dlr_b8_h256_n64_l4096")
+    ws = dlr.dlr_step_prepare(params_dev(w.fwd))
+    x = torch.zeros((w.B, w.H, w.N, 2), dtype=torch.float32, device="cuda")
+    y = _step_pieces(dev(w.u), ws, x, [512] * 8)
+    assert oracle.rel_l2(host(y), oracle.dlr_layer(w.u, params_np(w.fwd))) <= TOL
+    w = inputs.make_dlr(1, 16, 64, 16384, seed=43, unit_channels=8)
+    ws = dlr.dlr_step_prepare(params_dev(w.fwd))
+    x = torch.zeros((1, 16, 64, 2), dtype=torch.float32, device="cuda")
+    y = _step_pieces(dev(w.u), ws, x, [4096] * 4)
+    assert oracle.rel_l2(host(y), oracle.dlr_layer(w.u, params_np(w.fwd))) <= TOL
+    check_status()
+
+
 @pytest.mark.parametrize("bidir", [False, True])
 def test_fft_and_scan_layers_agree_small(bidir):
     w = inputs.make_dlr(2, 4, 32, 3000, seed=77, bidir=bidir, unit_channels=1)
