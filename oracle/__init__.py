@@ -160,6 +160,54 @@ def dlr_layer(u, fwd, bwd=None, cast: str = "re", nthreads: int = DEFAULT_THREAD
     return dlr_prod_layer(u, fwd, bwd, nthreads)
 
 
+def dlr_backward(u, g, log_re, log_im, W):
+    """Gradients of the causal DLR layer with the Re cast (section 2: y_k = sum_{j<=k} Re K_j
+    u_{k-j}, K_j = sum_n W_n lambda_n^j; section 2.2: lambda = exp(-a^2 + i theta) with
+    a = (log Lambda)_re, theta = (log Lambda)_im) for a loss whose gradient with respect to
+    y is g [B, H, L]. Written out from those definitions:
+      du_k        = sum_{j <= L-1-k} Re K_j g_{k+j}           (the same DLR run backwards)
+      c_j         = sum_b sum_k g_{b,k} u_{b,k-j}              (per channel, j < L)
+      S0, S1      = sum_j c_j lambda^j,  sum_j j c_j lambda^j
+      dW          = (Re S0, -Im S0)          since d Re K_j / d(W_re, W_im) = (Re, -Im) lambda^j
+      d log_re    = -2 a Re(W S1)            since d lambda^j / da = -2 a j lambda^j
+      d log_im    = -Im(W S1)                since d lambda^j / d theta = i j lambda^j
+    The convolution and correlation are numpy FFTs (zero-padded past 2L, so exact linear
+    sums); lambda^j is exp(j (-a^2 + i theta)) evaluated directly. Returns float64 du
+    [B, H, L], d_log_re [H, N], d_log_im [H, N], dW [H, N, 2]."""
+    u, g = _f32(u), _f64(g)
+    log_re, log_im, W = _f32(log_re), _f32(log_im), _f32(W)
+    B, H, L = u.shape
+    N = log_re.shape[1]
+    ud = u.astype(np.float64)
+    M = 1 << int(np.ceil(np.log2(2 * L)))
+    K = dlr_kernel(log_re, log_im, W, L, "complex")          # [H, L]
+    Kf = np.fft.rfft(K.real, M, axis=-1)                     # [H, M/2+1]
+    # du_k = sum_j ReK_j g_{k+j}: the causal convolution of the reversed g, reversed back
+    gr = g[..., ::-1]
+    du = np.fft.irfft(np.fft.rfft(gr, M, axis=-1) * Kf[None], M, axis=-1)[..., :L][..., ::-1]
+    # c_j = sum_b sum_k g_k u_{k-j}
+    c = np.fft.irfft((np.fft.rfft(g, M, axis=-1) * np.conj(np.fft.rfft(ud, M, axis=-1))).sum(0),
+                     M, axis=-1)[:, :L]                      # [H, L]
+    a = log_re.astype(np.float64)
+    th = log_im.astype(np.float64)
+    Wc = W[..., 0].astype(np.float64) + 1j * W[..., 1]
+    j = np.arange(L, dtype=np.float64)
+    d_re = np.empty((H, N))
+    d_im = np.empty((H, N))
+    dW = np.empty((H, N, 2))
+    for h in range(H):
+        z = -a[h] * a[h] + 1j * th[h]                        # log lambda, [N]
+        P = np.exp(np.outer(z, j))                           # lambda^j, [N, L]
+        S0 = P @ c[h]
+        S1 = P @ (j * c[h])
+        dW[h, :, 0] = S0.real
+        dW[h, :, 1] = -S0.imag
+        WS1 = Wc[h] * S1
+        d_re[h] = -2.0 * a[h] * WS1.real
+        d_im[h] = -WS1.imag
+    return np.ascontiguousarray(du), d_re, d_im, dW
+
+
 # ------------------------------------------------------------------------------------------
 # S5 ("Simplified State Space Layers for Sequence Modeling")
 

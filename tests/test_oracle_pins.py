@@ -411,6 +411,69 @@ def test_s5_one_state_one_feature_is_a_scalar_filter():
 
 
 # ---------------------------------------------------------------------------------------
+# Backward pass of the causal Re-cast layer
+
+@pytest.mark.parametrize("B,H,N,L,unit", [(2, 3, 4, 37, 1), (1, 2, 16, 200, 0), (3, 1, 1, 5, 1)])
+def test_backward_input_gradient_is_the_adjoint(B, H, N, L, unit):
+    """The layer is linear in u, so for any g the input gradient du satisfies
+    <g, DLR(u)> = <u, du> (DLR paper section 2: y is a causal convolution of u with Re K)."""
+    log_re, log_im, W = _params(H, N, seed=60 + L, unit=unit)
+    rng = np.random.default_rng(61 + L)
+    u = rng.standard_normal((B, H, L)).astype(np.float32)
+    g = rng.standard_normal((B, H, L))
+    du, _, _, _ = oracle.dlr_backward(u, g, log_re, log_im, W)
+    y = oracle.dlr_layer(u, (log_re, log_im, W))
+    lhs, rhs = float((g * y).sum()), float((u.astype(np.float64) * du).sum())
+    assert abs(lhs - rhs) <= 1e-11 * (np.abs(g * y).sum() + 1)
+    # and du is a function of g alone: the reversed-time layer applied to g
+    du_rev = oracle.dlr_layer(g[..., ::-1].astype(np.float32), (log_re, log_im, W))[..., ::-1]
+    g32 = g.astype(np.float32).astype(np.float64)
+    du32, _, _, _ = oracle.dlr_backward(u, g32, log_re, log_im, W)
+    np.testing.assert_allclose(du32, du_rev, rtol=1e-9, atol=1e-9 * np.abs(du_rev).max())
+
+
+def test_backward_parameter_gradients_match_finite_differences():
+    """d/d(log_re, log_im, W_re, W_im) of sum(g * y) against central differences of a float64
+    brute-force forward (K_j = sum_n W_n exp(j(-a^2 + i theta)), y = causal convolution of u
+    with Re K), one channel on the unit circle (a = 0, where d/da vanishes)."""
+    B, H, N, L = 2, 2, 3, 20
+    log_re, log_im, W = _params(H, N, seed=62, unit=1)
+    rng = np.random.default_rng(63)
+    u = rng.standard_normal((B, H, L)).astype(np.float32)
+    g = rng.standard_normal((B, H, L))
+    _, d_re, d_im, dW = oracle.dlr_backward(u, g, log_re, log_im, W)
+    ud = u.astype(np.float64)
+    j = np.arange(L)
+
+    def loss(a, th, wr, wi):
+        tot = 0.0
+        for h in range(H):
+            lam_j = np.exp(np.outer(-a[h] ** 2 + 1j * th[h], j))      # [N, L]
+            K = ((wr[h] + 1j * wi[h])[:, None] * lam_j).sum(0).real
+            for b in range(B):
+                tot += float(g[b, h] @ np.convolve(ud[b, h], K)[:L])
+        return tot
+
+    base = [log_re.astype(np.float64), log_im.astype(np.float64),
+            W[..., 0].astype(np.float64), W[..., 1].astype(np.float64)]
+    grads = [d_re, d_im, dW[..., 0], dW[..., 1]]
+    for which in range(4):
+        fd = np.empty((H, N))
+        for h in range(H):
+            for n in range(N):
+                step = 1e-6 * max(1.0, abs(base[which][h, n]))
+                plus = [x.copy() for x in base]
+                minus = [x.copy() for x in base]
+                plus[which][h, n] += step
+                minus[which][h, n] -= step
+                fd[h, n] = (loss(*plus) - loss(*minus)) / (2 * step)
+        scale = np.abs(fd).max()
+        np.testing.assert_allclose(grads[which], fd, rtol=0, atol=1e-6 * scale,
+                                   err_msg=["log_re", "log_im", "W_re", "W_im"][which])
+    assert np.all(d_re[log_re == 0] == 0)
+
+
+# ---------------------------------------------------------------------------------------
 # Input generator structure (HiPPO-N spectrum)
 
 @pytest.mark.parametrize("P", [4, 16, 64])
