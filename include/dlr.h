@@ -205,6 +205,23 @@ dlr_status dlr_scan_host(const float* u, const float* log_re, const float* log_i
                          void* workspace, size_t workspace_bytes, dlr_stream_t stream);
 
 /*
+ * dlr_scan_backward_input -- the input gradient of the causal DLR layer (Re cast): for a loss
+ * whose gradient with respect to y is g [B, H, L],
+ *   du_k = sum_{j <= L-1-k} Re K_j g_{k+j},   K_j = sum_n W_n lambda_n^j,
+ * i.e. the same layer run backwards in time on g (the layer is the causal convolution of u
+ * with Re K, DLR paper section 2; its adjoint is the correlation with the same kernel).
+ * Computed by the tensor-core scan's reversed pass with the layer's own parameters: du is
+ * zeroed, the channel tables go to `workspace` (dlr_scan_workspace_size bytes, as dlr_scan)
+ * and the reversed pass adds into du. g and du [B, H, L] must not overlap each other or the
+ * workspace. Limits as the tensor-core path of dlr_scan (N <= 64). A memset and two kernel
+ * launches; faults of the bounded waits are reported through dlr_get_device_status().
+ */
+dlr_status dlr_scan_backward_input(const float* g, const float* log_re, const float* log_im,
+                                   const float* W, int64_t B, int64_t H, int64_t N, int64_t L,
+                                   float* du, void* workspace, size_t workspace_bytes,
+                                   dlr_stream_t stream);
+
+/*
  * dlr_step_prepare + dlr_step -- the causal DLR layer (Re cast) advanced from a carried state,
  * the recurrent mode used to feed a sequence a few samples at a time ("The Annotated S4",
  * part 1 "An SSM Neural Network": the layer's RNN mode with its state cache; part 3 "Sampling

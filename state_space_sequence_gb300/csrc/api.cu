@@ -105,7 +105,7 @@ dlr_status check_params(const float* log_re, const float* log_im, const float* W
 
 extern "C" {
 
-int dlr_abi_version(void) { return 5; }
+int dlr_abi_version(void) { return 6; }
 
 const char* dlr_last_cuda_error(void) { return t_last_cuda_error; }
 
@@ -272,6 +272,32 @@ dlr_status dlr_scan_apply(const float* u, int64_t B, int64_t H, int64_t N, int64
   return from_cuda(dlr::launch_scan_tc_apply(u, (int)B, (int)H, (int)L, reverse != 0, y,
                                              workspace, status_word(), (cudaStream_t)stream,
                                              false));
+}
+
+dlr_status dlr_scan_backward_input(const float* g, const float* log_re, const float* log_im,
+                                   const float* W, int64_t B, int64_t H, int64_t N, int64_t L,
+                                   float* du, void* workspace, size_t workspace_bytes,
+                                   dlr_stream_t stream) {
+  if (B < 1 || H < 1 || N < 1 || L < 1) return DLR_ERR_INVALID_ARG;
+  if (!g || !du || !aligned16(g) || !aligned16(du)) return DLR_ERR_INVALID_ARG;
+  dlr_status st = check_params(log_re, log_im, W);
+  if (st != DLR_OK) return st;
+  const size_t bytes = sizeof(float) * (size_t)B * (size_t)H * (size_t)L;
+  if (ranges_overlap(g, bytes, du, bytes)) return DLR_ERR_INVALID_ARG;
+  if (N > 64 || L > kMaxL || B * H > kMaxGrid) return DLR_ERR_UNSUPPORTED;
+  const size_t need = dlr::scan_tc_workspace_bytes(H);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DLR_ERR_WORKSPACE;
+  if (ranges_overlap(workspace, need, g, bytes) || ranges_overlap(workspace, need, du, bytes))
+    return DLR_ERR_INVALID_ARG;
+  // du = rev(DLR(rev(g))) with the same parameters: the reversed pass adds into du
+  cudaError_t e = cudaMemsetAsync(du, 0, bytes, (cudaStream_t)stream);
+  if (e == cudaSuccess)
+    e = dlr::launch_scan_tc_tables(log_re, log_im, W, (int)H, (int)N, workspace,
+                                   (cudaStream_t)stream);
+  if (e == cudaSuccess)
+    e = dlr::launch_scan_tc_apply(g, (int)B, (int)H, (int)L, true, du, workspace, status_word(),
+                                  (cudaStream_t)stream, true);
+  return from_cuda(e);
 }
 
 size_t dlr_step_workspace_size(int64_t H, int64_t N) {

@@ -63,6 +63,8 @@ def _load():
         lib.dlr_scan_host_workspace_size.restype = sz
         lib.dlr_scan_host.argtypes = [P, P, P, P, i64, i64, i64, i64, P, P, sz, P]
         lib.dlr_scan_host.restype = i32
+        lib.dlr_scan_backward_input.argtypes = [P, P, P, P, i64, i64, i64, i64, P, P, sz, P]
+        lib.dlr_scan_backward_input.restype = i32
         lib.dlr_step_workspace_size.argtypes = [i64, i64]
         lib.dlr_step_workspace_size.restype = sz
         lib.dlr_step_prepare.argtypes = [P, P, P, i64, i64, P, sz, P]
@@ -238,6 +240,26 @@ def dlr_scan_apply(u, workspace, N: int, out=None, reverse: bool = False, stream
     _ok("dlr_scan_apply", _load().dlr_scan_apply(_ptr(u), B, H, N, L, 1 if reverse else 0,
                                                  _ptr(out), _ptr(workspace), workspace.numel(),
                                                  _stream(stream)))
+    return out
+
+
+def dlr_scan_backward_input(g, params, workspace=None, out=None, stream=None):
+    """Input gradient of the causal DLR layer for the output gradient g [B, H, L]: the layer
+    run backwards in time on g with the same parameters (N <= 64). Returns du [B, H, L]."""
+    _check_f32(g)
+    lr, li, W = _params(params)
+    B, H, L = g.shape
+    N = lr.shape[1]
+    if workspace is None:
+        workspace = torch.empty(max(dlr_scan_workspace_size(B, H, N, L), 1), dtype=torch.uint8,
+                                device=g.device)
+    if out is None:
+        out = torch.empty_like(g)
+    _check_f32(out)
+    _ok("dlr_scan_backward_input",
+        _load().dlr_scan_backward_input(_ptr(g), _ptr(lr), _ptr(li), _ptr(W), B, H, N, L,
+                                        _ptr(out), _ptr(workspace), workspace.numel(),
+                                        _stream(stream)))
     return out
 
 

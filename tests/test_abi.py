@@ -44,7 +44,7 @@ def test_status_strings_and_version(lib):
     lib.dlr_status_string.restype = ctypes.c_char_p
     assert lib.dlr_status_string(0) == b"DLR_OK"
     assert lib.dlr_status_string(4) == b"DLR_ERR_TIMEOUT"
-    assert lib.dlr_abi_version() == 5
+    assert lib.dlr_abi_version() == 6
 
 
 def test_host_validation_rejects_bad_arguments(lib):
@@ -159,3 +159,17 @@ def test_step_validation(lib):
     assert lib.dlr_step(None, 1, 2, 4, 0, x, None, ws, 1 << 20, None) == 0
     assert lib.dlr_step(u, 1, 2, 4, 8, x, ctypes.c_void_p(0x10010), ws, 1 << 20, None) == 1
     assert lib.dlr_step(u, 1, 2, 4, 8, x, ctypes.c_void_p(0x20010), ws, 1 << 20, None) == 1
+
+
+def test_backward_input_validation(lib):
+    P, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    lib.dlr_scan_backward_input.argtypes = [P, P, P, P, i64, i64, i64, i64, P, P, sz, P]
+    fake = ctypes.c_void_p(0x1000)
+    g, du, ws = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000), ctypes.c_void_p(0x100000)
+    assert lib.dlr_scan_backward_input(g, fake, fake, fake, 1, 2, 4, 0, du, ws, 1 << 20,
+                                       None) == 1
+    assert lib.dlr_scan_backward_input(g, fake, fake, fake, 1, 2, 65, 8, du, ws, 1 << 20,
+                                       None) == 2
+    assert lib.dlr_scan_backward_input(g, fake, fake, fake, 1, 2, 4, 8, du, None, 0, None) == 5
+    assert lib.dlr_scan_backward_input(g, fake, fake, fake, 1, 2, 4, 8, ctypes.c_void_p(0x10010),
+                                       ws, 1 << 20, None) == 1

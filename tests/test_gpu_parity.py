@@ -223,6 +223,23 @@ def test_scan_host_buffers_match_oracle_and_device_path(B, H, N, L):
 
 
 # ------------------------------------------------------------------------------------------
+# dlr_scan_backward_input (the layer's input gradient)
+
+# rows off the 64-step grid (plain loads), the bank shape (TMA), rows longer than a tile
+@pytest.mark.parametrize("B,H,N,L", [(2, 3, 5, 37), (8, 16, 64, 4096), (1, 2, 64, 20000),
+                                     (3, 2, 40, 3000)])
+def test_backward_input_matches_oracle(B, H, N, L):
+    """du for an output gradient g: the layer run backwards on g with the same parameters,
+    against the oracle's gradient of sum(g * y) with respect to u."""
+    w = inputs.make_dlr(B, H, N, L, seed=11 * B + H + N + L, unit_channels=1)
+    g = np.random.default_rng(B + L).standard_normal((B, H, L)).astype(np.float32)
+    du = dlr.dlr_scan_backward_input(dev(g), params_dev(w.fwd))
+    ref, _, _, _ = oracle.dlr_backward(w.u, g.astype(np.float64), *params_np(w.fwd))
+    assert oracle.rel_l2(host(du), ref) <= TOL
+    check_status()
+
+
+# ------------------------------------------------------------------------------------------
 # dlr_step (the recurrence advanced from a carried state)
 
 def _step_pieces(u_d, ws, x, pieces):
