@@ -4,8 +4,9 @@ TEST INFRASTRUCTURE ONLY: imported by the test-suite, by ``__graft_entry__.smoke
 the benchmark's CPU-baseline leg, never by the library. It shares no code with the CUDA path.
 
 The arithmetic lives in ``oracle.c`` (plain float64 loops) plus numpy library primitives
-(complex matmul, exp) where a step is a plain matrix product. Each function cites the passage
-it follows; the design doc lists the readings taken where the pages are silent.
+(complex matmul, exp, FFT) where a step is a plain matrix product or a convolution. Each
+function cites the passage it follows and states the reading it takes where the pages are
+silent.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py`` against closed
 forms, library routines (numpy FFT, scipy lfilter / toeplitz / expm) or brute force.
