@@ -173,3 +173,40 @@ def test_backward_input_validation(lib):
     assert lib.dlr_scan_backward_input(g, fake, fake, fake, 1, 2, 4, 8, du, None, 0, None) == 5
     assert lib.dlr_scan_backward_input(g, fake, fake, fake, 1, 2, 4, 8, ctypes.c_void_p(0x10010),
                                        ws, 1 << 20, None) == 1
+
+
+def test_conv_and_s5_validation(lib):
+    """dlr_conv_spectrum / dlr_conv_apply / dlr_conv_noalloc / s5_layer reject invalid sizes,
+    enums, pointers, overlaps, limits and short workspaces on the host, before any launch."""
+    P, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+    k, k2 = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000)
+    # far apart, so that only the intended check fails
+    u, y, ws = (ctypes.c_void_p(0x10000000), ctypes.c_void_p(0x20000000),
+                ctypes.c_void_p(0x30000000))
+    big = 1 << 40
+    lib.dlr_conv_spectrum.argtypes = [P, P, i32, i64, i64, P, sz, P]
+    assert lib.dlr_conv_spectrum(k, None, 0, 0, 64, ws, big, None) == 1       # H < 1
+    assert lib.dlr_conv_spectrum(k, None, 5, 2, 64, ws, big, None) == 1       # bad direction
+    assert lib.dlr_conv_spectrum(ctypes.c_void_p(0x1004), None, 0, 2, 64, ws, big, None) == 1
+    assert lib.dlr_conv_spectrum(k, k2, 0, 2, 64, ws, big, None) == 1         # causal + K_bwd
+    assert lib.dlr_conv_spectrum(k, None, 1, 2, 64, ws, big, None) == 1       # bidir, no K_bwd
+    assert lib.dlr_conv_spectrum(k, None, 0, 2, 70000, ws, big, None) == 2    # L > 65536
+    assert lib.dlr_conv_spectrum(k, None, 0, 2, 64, ws, 16, None) == 5        # short workspace
+    lib.dlr_conv_apply.argtypes = [P, i64, i64, i64, P, P, sz, P]
+    assert lib.dlr_conv_apply(u, 0, 2, 64, y, ws, big, None) == 1
+    assert lib.dlr_conv_apply(u, 1, 2, 64, ctypes.c_void_p(0x10000100), ws, big, None) == 1
+    assert lib.dlr_conv_apply(u, 1, 2, 70000, y, ws, big, None) == 2
+    assert lib.dlr_conv_apply(u, 1, 2, 64, y, None, 0, None) == 5
+    lib.dlr_conv_noalloc.argtypes = [P, P, P, i32, i64, i64, i64, P, P]
+    assert lib.dlr_conv_noalloc(u, k, None, 0, 1, 2, 20000, y, None) == 2     # L > 16384
+    far = ctypes.c_void_p(1 << 46)  # the 64 GB rows of this call overlap nothing
+    assert lib.dlr_conv_noalloc(u, k, None, 0, 1, 1 << 20, 16384, far, None) == 5  # > scratch
+    assert lib.dlr_conv_noalloc(u, k, k2, 0, 1, 2, 64, y, None) == 1
+    lib.s5_layer.argtypes = [P] * 6 + [i64] * 4 + [i32, P, P, sz, P]
+    p = [ctypes.c_void_p(0x1000 * (i + 1)) for i in range(5)]
+    assert lib.s5_layer(u, *p, 1, 64, 32, 32, 7, y, ws, big, None) == 1       # bad precision
+    assert lib.s5_layer(u, None, *p[1:], 1, 64, 32, 32, 0, y, ws, big, None) == 1
+    assert lib.s5_layer(u, *p, 1, 64, 32, 48, 0, y, ws, big, None) == 2       # P % 32
+    assert lib.s5_layer(u, *p, 1, 64, 32, 2048, 0, y, ws, big, None) == 2     # P > 1024
+    assert lib.s5_layer(u, *p, 1, 64, 32, 32, 0, ctypes.c_void_p(0x10000010), ws, big, None) == 1
+    assert lib.s5_layer(u, *p, 1, 64, 32, 32, 0, y, ws, 16, None) == 5        # short workspace
