@@ -161,7 +161,7 @@ def dlr_layer(u, fwd, bwd=None, cast: str = "re", nthreads: int = DEFAULT_THREAD
     return dlr_prod_layer(u, fwd, bwd, nthreads)
 
 
-def dlr_backward(u, g, log_re, log_im, W):
+def dlr_backward(u, g, log_re, log_im, W, cast: str = "re"):
     """Gradients of the causal DLR layer with the Re cast (section 2: y_k = sum_{j<=k} Re K_j
     u_{k-j}, K_j = sum_n W_n lambda_n^j; section 2.2: lambda = exp(-a^2 + i theta) with
     a = (log Lambda)_re, theta = (log Lambda)_im) for a loss whose gradient with respect to
@@ -172,9 +172,15 @@ def dlr_backward(u, g, log_re, log_im, W):
       dW          = (Re S0, -Im S0)          since d Re K_j / d(W_re, W_im) = (Re, -Im) lambda^j
       d log_re    = -2 a Re(W S1)            since d lambda^j / da = -2 a j lambda^j
       d log_im    = -Im(W S1)                since d lambda^j / d theta = i j lambda^j
+    With the DLR-prod cast (section 2.1: kappa_j = Re K_j Im K_j in place of Re K_j) the
+    gradient with respect to kappa_j is again c_j, and through K it becomes, with
+    T_j = c_j K_j: dW = (Im, Re) sum_j T_j lambda^j, d log_re = -2 a Im(W sum_j j T_j
+    lambda^j), d log_im = Re(W sum_j j T_j lambda^j); du uses kappa in place of Re K.
     The convolution and correlation are numpy FFTs (zero-padded past 2L, so exact linear
     sums); lambda^j is exp(j (-a^2 + i theta)) evaluated directly. Returns float64 du
     [B, H, L], d_log_re [H, N], d_log_im [H, N], dW [H, N, 2]."""
+    if cast not in ("re", "re_im"):
+        raise ValueError(cast)
     u, g = _f32(u), _f64(g)
     log_re, log_im, W = _f32(log_re), _f32(log_im), _f32(W)
     B, H, L = u.shape
@@ -182,7 +188,8 @@ def dlr_backward(u, g, log_re, log_im, W):
     ud = u.astype(np.float64)
     M = 1 << int(np.ceil(np.log2(2 * L)))
     K = dlr_kernel(log_re, log_im, W, L, "complex")          # [H, L]
-    Kf = np.fft.rfft(K.real, M, axis=-1)                     # [H, M/2+1]
+    kap = K.real if cast == "re" else K.real * K.imag        # the convolution kernel
+    Kf = np.fft.rfft(kap, M, axis=-1)                        # [H, M/2+1]
     # du_k = sum_j ReK_j g_{k+j}: the causal convolution of the reversed g, reversed back
     gr = g[..., ::-1]
     du = np.fft.irfft(np.fft.rfft(gr, M, axis=-1) * Kf[None], M, axis=-1)[..., :L][..., ::-1]
@@ -199,14 +206,38 @@ def dlr_backward(u, g, log_re, log_im, W):
     for h in range(H):
         z = -a[h] * a[h] + 1j * th[h]                        # log lambda, [N]
         P = np.exp(np.outer(z, j))                           # lambda^j, [N, L]
-        S0 = P @ c[h]
-        S1 = P @ (j * c[h])
-        dW[h, :, 0] = S0.real
-        dW[h, :, 1] = -S0.imag
+        wt = c[h] if cast == "re" else c[h] * K[h]           # c_j, or T_j = c_j K_j
+        S0 = P @ wt
+        S1 = P @ (j * wt)
         WS1 = Wc[h] * S1
-        d_re[h] = -2.0 * a[h] * WS1.real
-        d_im[h] = -WS1.imag
+        if cast == "re":
+            dW[h, :, 0] = S0.real
+            dW[h, :, 1] = -S0.imag
+            d_re[h] = -2.0 * a[h] * WS1.real
+            d_im[h] = -WS1.imag
+        else:
+            dW[h, :, 0] = S0.imag
+            dW[h, :, 1] = S0.real
+            d_re[h] = -2.0 * a[h] * WS1.imag
+            d_im[h] = WS1.real
     return np.ascontiguousarray(du), d_re, d_im, dW
+
+
+def dlr_layer_backward(u, g, fwd, bwd=None, cast: str = "re"):
+    """Gradients of dlr_layer (causal, or bidirectional with a second parameter set: section
+    2.1, y = DLR1(u) + rev(DLR2(rev(u)))) for the output gradient g. The second direction is
+    the causal layer on the reversed sequences, so its gradients are those of dlr_backward on
+    rev(u) and rev(g), and its input gradient enters du reversed. Returns du and a list of
+    (d_log_re, d_log_im, dW) per direction."""
+    du, dr, di, dw = dlr_backward(u, g, *fwd, cast=cast)
+    grads = [(dr, di, dw)]
+    if bwd is not None:
+        ur = np.ascontiguousarray(_f32(u)[..., ::-1])
+        gr = np.ascontiguousarray(_f64(g)[..., ::-1])
+        du2, dr2, di2, dw2 = dlr_backward(ur, gr, *bwd, cast=cast)
+        du = du + du2[..., ::-1]
+        grads.append((dr2, di2, dw2))
+    return np.ascontiguousarray(du), grads
 
 
 # ------------------------------------------------------------------------------------------

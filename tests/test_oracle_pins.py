@@ -473,6 +473,56 @@ def test_backward_parameter_gradients_match_finite_differences():
     assert np.all(d_re[log_re == 0] == 0)
 
 
+@pytest.mark.parametrize("cast", ["re", "re_im"])
+def test_backward_bidirectional_and_prod_cast_match_finite_differences(cast):
+    """Both parameter sets of the bidirectional layer (section 2.1: y = DLR1(u) +
+    rev(DLR2(rev(u)))), with the Re or the DLR-prod cast (kappa_j = Re K_j Im K_j), against
+    central differences of a float64 brute-force forward; and the input gradient against the
+    adjoint identity."""
+    B, H, N, L = 2, 2, 3, 16
+    w = inputs.make_dlr(B, H, N, L, seed=64, bidir=True, unit_channels=1)
+    rng = np.random.default_rng(65)
+    g = rng.standard_normal((B, H, L))
+    fwd = (w.fwd.log_re, w.fwd.log_im, w.fwd.W)
+    bwd = (w.bwd.log_re, w.bwd.log_im, w.bwd.W)
+    du, grads = oracle.dlr_layer_backward(w.u, g, fwd, bwd, cast)
+    ud = w.u.astype(np.float64)
+    j = np.arange(L)
+
+    def kernel(a, th, wr, wi, h):
+        K = ((wr[h] + 1j * wi[h])[:, None] * np.exp(np.outer(-a[h] ** 2 + 1j * th[h], j))).sum(0)
+        return K.real if cast == "re" else K.real * K.imag
+
+    def loss(p1, p2):
+        tot = 0.0
+        for h in range(H):
+            k1, k2 = kernel(*p1, h), kernel(*p2, h)
+            for b in range(B):
+                y = np.convolve(ud[b, h], k1)[:L] + np.convolve(ud[b, h][::-1], k2)[:L][::-1]
+                tot += float(g[b, h] @ y)
+        return tot
+
+    base = [[x.astype(np.float64) for x in (p[0], p[1], p[2][..., 0], p[2][..., 1])]
+            for p in (fwd, bwd)]
+    for d in range(2):
+        dr, di, dw = grads[d]
+        mine = [dr, di, dw[..., 0], dw[..., 1]]
+        for which in range(4):
+            fd = np.empty((H, N))
+            for h in range(H):
+                for n in range(N):
+                    step = 1e-6 * max(1.0, abs(base[d][which][h, n]))
+                    plus = [[x.copy() for x in q] for q in base]
+                    minus = [[x.copy() for x in q] for q in base]
+                    plus[d][which][h, n] += step
+                    minus[d][which][h, n] -= step
+                    fd[h, n] = (loss(*plus) - loss(*minus)) / (2 * step)
+            np.testing.assert_allclose(mine[which], fd, rtol=0, atol=1e-6 * np.abs(fd).max(),
+                                       err_msg=f"direction {d}, parameter {which}")
+    y = oracle.dlr_layer(w.u, fwd, bwd, cast=cast)
+    assert abs(float((g * y).sum()) - float((ud * du).sum())) <= 1e-11 * np.abs(g * y).sum()
+
+
 # ---------------------------------------------------------------------------------------
 # Input generator structure (HiPPO-N spectrum)
 
