@@ -134,6 +134,8 @@ def dlr_kernel(log_re, log_im, W, L: int, cast: str = "re", out=None, stream=Non
 
 
 def dlr_conv_workspace_size(H: int, L: int, bidir: bool = False) -> int:
+    """Bytes of device workspace dlr_conv / dlr_conv_spectrum need (twiddles and the H kernel
+    spectra); 0 for unsupported sizes."""
     return int(_load().dlr_conv_workspace_size(H, L, 1 if bidir else 0))
 
 
@@ -264,6 +266,7 @@ def dlr_scan_backward_input(g, params, workspace=None, out=None, stream=None):
 
 
 def dlr_step_workspace_size(H: int, N: int) -> int:
+    """Bytes of device workspace dlr_step_prepare fills (24 per state); 0 when N > 256."""
     return int(_load().dlr_step_workspace_size(H, N))
 
 
@@ -302,6 +305,8 @@ def dlr_step(u, workspace, state, out=None, stream=None):
 
 
 def dlr_scan_host_workspace_size(B: int, H: int, N: int, L: int) -> int:
+    """Bytes of device workspace dlr_scan_host needs (device copies of u, y and the
+    parameters, and the scan's channel tables)."""
     return int(_load().dlr_scan_host_workspace_size(B, H, N, L))
 
 
@@ -325,6 +330,7 @@ def dlr_scan_host(u, params, out, workspace, stream=None):
 
 
 def s5_workspace_size(B: int, L: int, H: int, P: int, prec: str = "fp32") -> int:
+    """Bytes of device workspace s5_layer needs at this size and precision tier."""
     return int(_load().s5_workspace_size(B, L, H, P, PREC[prec]))
 
 
