@@ -119,7 +119,9 @@ dlr_status dlr_conv_apply(const float* u, int64_t B, int64_t H, int64_t L, float
  *    the library until the process exits.
  *  - Limit: the call needs 24*n (two twiddle tables) + 8*H*(n+1) bytes of scratch, n = the next
  *    power of two >= L; larger requests return DLR_ERR_WORKSPACE and launch nothing (e.g.
- *    up to H = 508 at L = 4096, up to H = 124 at L = 16384). L <= 16384 as for dlr_conv.
+ *    up to H = 508 at L = 4096, up to H = 124 at L = 16384). This entry point takes
+ *    L <= 16384 only (one CTA per row); longer rows, which dlr_conv runs on its cluster path,
+ *    return DLR_ERR_UNSUPPORTED here.
  *  - The first call on a device looks up the scratch's device address (with that device
  *    current) and caches it; make that first call before any stream capture.
  *  - All calls in the process share the one scratch array, which keeps the last call's
@@ -198,6 +200,8 @@ dlr_status dlr_scan_apply(const float* u, int64_t B, int64_t H, int64_t N, int64
  * another and the copy of a third out overlap. Asynchronous with respect to the host; ordered
  * after the work already on `stream` and before the work enqueued on it later, so y may be
  * read after a synchronisation of `stream`. Same limits as dlr_scan_apply (N <= 64).
+ * If an enqueue fails part-way, the call waits for the pieces already queued before it returns
+ * the error, so the host buffers and the workspace are no longer in use when it returns.
  */
 size_t dlr_scan_host_workspace_size(int64_t B, int64_t H, int64_t N, int64_t L);
 dlr_status dlr_scan_host(const float* u, const float* log_re, const float* log_im,

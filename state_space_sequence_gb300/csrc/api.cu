@@ -44,6 +44,20 @@ cudaError_t launch_step(const float* u, int64_t B, int64_t H, int64_t N, int64_t
 __device__ int g_dlr_device_status = 0;
 
 namespace {
+// The last CUDA error a call of this thread turned into DLR_ERR_CUDA (for diagnostics).
+thread_local const char* t_last_cuda_error_msg = "no error";
+}  // namespace
+
+namespace dlr {
+// Every entry point maps a CUDA error through here, so dlr_last_cuda_error() names it.
+dlr_status status_from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return DLR_OK;
+  t_last_cuda_error_msg = cudaGetErrorString(e);
+  return DLR_ERR_CUDA;
+}
+}  // namespace dlr
+
+namespace {
 
 constexpr int64_t kMaxL = (int64_t(1) << 24) - 1;
 constexpr int64_t kMaxGrid = 2147483647;
@@ -57,14 +71,7 @@ int* status_word() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// The last CUDA error a call of this thread turned into DLR_ERR_CUDA (for diagnostics).
-thread_local const char* t_last_cuda_error = "no error";
-
-dlr_status from_cuda(cudaError_t e) {
-  if (e == cudaSuccess) return DLR_OK;
-  t_last_cuda_error = cudaGetErrorString(e);
-  return DLR_ERR_CUDA;
-}
+dlr_status from_cuda(cudaError_t e) { return dlr::status_from_cuda(e); }
 
 // Three non-blocking streams per device for the host-buffer entry point: copies in, compute,
 // copies out. Created on first use and kept for the life of the process.
@@ -107,7 +114,7 @@ extern "C" {
 
 int dlr_abi_version(void) { return 6; }
 
-const char* dlr_last_cuda_error(void) { return t_last_cuda_error; }
+const char* dlr_last_cuda_error(void) { return t_last_cuda_error_msg; }
 
 const char* dlr_status_string(dlr_status s) {
   switch (s) {
@@ -467,6 +474,12 @@ dlr_status dlr_scan_host(const float* u, const float* log_re, const float* log_i
     return cudaStreamWaitEvent((cudaStream_t)stream, ev_end, 0);
   };
   e = run();
+  if (e != cudaSuccess) {
+    // Some pieces may already be queued on the internal streams, reading the caller's host
+    // buffers and workspace: let them finish before the error returns, so that the caller may
+    // free or reuse those buffers at once.
+    for (int i = 0; i < 3; ++i) cudaStreamSynchronize(st[i]);
+  }
   cudaEventDestroy(ev_start);
   cudaEventDestroy(ev_par);
   cudaEventDestroy(ev_end);

@@ -26,6 +26,7 @@ cudaError_t launch_dlr_conv_spectrum(const float* K1, const float* K2, int H, in
                                      cudaStream_t s);
 cudaError_t launch_dlr_conv_apply(const float* u, int B, int H, int L, float* y, const void* ws,
                                   cudaStream_t s);
+dlr_status status_from_cuda(cudaError_t e);  // api.cu: records the error for dlr_last_cuda_error
 }  // namespace dlr
 
 namespace {
@@ -84,14 +85,13 @@ extern "C" dlr_status dlr_conv_noalloc(const float* u, const float* K_fwd, const
   // The fixed scratch must hold this call's twiddles and spectra.
   if (dlr::conv_workspace_bytes(H, L) > kNoAllocScratchBytes) return DLR_ERR_WORKSPACE;
   void* ws = nullptr;
-  if (scratch_address(&ws) != cudaSuccess) return DLR_ERR_CUDA;
+  cudaError_t e = scratch_address(&ws);
+  if (e != cudaSuccess) return dlr::status_from_cuda(e);
   // Nothing in the scratch has to start at zero: the spectrum launch rewrites the whole
   // twiddle table and every spectrum entry that the apply launch then reads.
   cudaStream_t s = (cudaStream_t)stream;
-  if (dlr::launch_dlr_conv_spectrum(K_fwd, dir == DLR_BIDIR ? K_bwd : nullptr, (int)H, (int)L,
-                                    ws, s) != cudaSuccess)
-    return DLR_ERR_CUDA;
-  if (dlr::launch_dlr_conv_apply(u, (int)B, (int)H, (int)L, y, ws, s) != cudaSuccess)
-    return DLR_ERR_CUDA;
-  return DLR_OK;
+  e = dlr::launch_dlr_conv_spectrum(K_fwd, dir == DLR_BIDIR ? K_bwd : nullptr, (int)H, (int)L,
+                                    ws, s);
+  if (e == cudaSuccess) e = dlr::launch_dlr_conv_apply(u, (int)B, (int)H, (int)L, y, ws, s);
+  return dlr::status_from_cuda(e);
 }

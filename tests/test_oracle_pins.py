@@ -580,3 +580,26 @@ def test_dlr_init_ranges():
     assert mag.min() >= np.exp(-0.25) * (1 - 1e-6)
     assert mag.max() <= np.exp(-0.00025) * (1 + 1e-6)
     np.testing.assert_allclose(p.log_im[0], 2 * np.pi * np.arange(64) / 64, rtol=1e-6)
+
+
+def test_oracle_lambda_magnitude_spans_the_init_range():
+    """The oracle's lambda against the range the DLR paper (section 2.2) fixes through its
+    initialisation: r ~ U(log 5e-4, log 0.5) and (log Lambda)_re = sqrt(e^r / 2) put
+    (log Lambda)_re^2 in [2.5e-4, 0.25], so |lambda| must lie in [e^-0.25, e^-0.00025] with
+    both ends reached by many draws, and the end points themselves map to those magnitudes.
+    A convention such as exp(-(log Lambda)_re) or exp(-2 (log Lambda)_re^2) leaves the range."""
+    p = inputs.dlr_params(np.random.default_rng(7), 128, 64)
+    lam = oracle.dlr_lambda(p.log_re, p.log_im)
+    mag = np.abs(lam)
+    lo, hi = np.exp(-0.25), np.exp(-0.00025)
+    assert mag.min() >= lo * (1 - 1e-6) and mag.max() <= hi * (1 + 1e-6)
+    # 8192 log-uniform draws: both ends of the range are approached
+    assert mag.min() < np.exp(-0.24) and mag.max() > np.exp(-0.0003)
+    # the phase is (log Lambda)_im
+    np.testing.assert_allclose(np.angle(lam[0, 1:32]), p.log_im[0, 1:32].astype(np.float64),
+                               rtol=0, atol=1e-12)
+    # end points of the init range: r = log 0.5 -> a = 0.5; r = log 5e-4 -> a = sqrt(2.5e-4)
+    a = np.array([[0.5, np.sqrt(2.5e-4)]], np.float32)
+    ends = np.abs(oracle.dlr_lambda(a, np.zeros_like(a)))[0]
+    np.testing.assert_allclose(ends, np.exp(-a[0].astype(np.float64) ** 2), rtol=1e-15)
+    np.testing.assert_allclose(ends, [lo, hi], rtol=1e-7)
