@@ -37,21 +37,25 @@
 // Two kernels. dlr_scan_tc_tables (one CTA per channel) evaluates the per-channel tables --
 // Q, the Toeplitz block of K_0..K_63 and G as scaled f16 pairs in the exact byte layout the
 // MMAs read, lambda^64, the re-anchoring correction and the two scales -- into a workspace
-// blob per channel. dlr_scan_tc_kernel then runs one persistent CTA per SM with five roles
+// blob per channel. dlr_scan_tc_kernel then runs one persistent CTA per SM with three roles
 // joined by mbarriers, two tiles in flight:
-//   warps 0-3   "scan": thread r owns TMEM lane r = state row r; runs step 2 on S and writes
-//                       the states straight into the Xin operand (MN-major f16 pair),
-//   warps 4-7   "conv": thread g = chunk g; converts the float32 u tile the producer landed
-//                       in the tile's operand buffer, in place, into its scaled f16 pair
-//                       (K-major), or loads u itself when the rows are not whole chunks; loads
-//                       Q into TMEM for a new channel,
-//   warps 8-11  "epi":  thread g owns TMEM lane g = chunk g; reads Y1, Y2, scales them and
-//                       writes y through a per-warp staging image and TMA stores (or plain
-//                       stores when the rows are not whole chunks),
-//   warp 12, lane 0:    issues the MMAs: GEMM1 (with the Toeplitz part) of tile k+1, then
-//                       GEMM2 of tile k,
-//   warp 13, lane 0:    the producer: every bulk copy (u tiles, the Toeplitz and G operands of
-//                       a new channel), in the order the MMA groups complete.
+//   warps 0-7 "main" (two warps per TMEM lane quarter, half h = warp >> 2). Iteration k:
+//     - the u operand of tile k+1: thread = chunk g, steps 32h .. 32h + 31; the float32 tile
+//       the producer landed in the tile's operand buffer is converted in place into its
+//       scaled f16 pair (K-major), or loaded directly when the rows are not whole chunks; Q
+//       into TMEM for a new channel;
+//     - the outputs of tile k-1: thread = chunk g = TMEM lane, steps 32h .. 32h + 31: Y1, Y2
+//       scaled, written through a per-warp staging image and a TMA store (plain stores when
+//       the rows are not whole chunks);
+//     - step 2 of tile k: thread r = TMEM lane r = state row r; the carries along the chunks
+//       of S written straight into the Xin operand (MN-major f16 pair), half h writing the
+//       columns 64h .. 64h + 63;
+//   warp 8, lane 0: issues the MMAs: GEMM1 (with the Toeplitz part) of tile k+1, then GEMM2
+//     of tile k,
+//   warp 9, lane 0: the producer: every bulk copy (u tiles, the Toeplitz and G operands of a
+//     new channel), in the order the MMA groups complete.
+// One role for the per-element work keeps the instruction stream small and lets the stages
+// of one tile follow each other without hand-offs between warps.
 // Buffers: u operand x2, Xin x1, Toeplitz and G x1, y staging (shared memory); Q, S x2,
 // Y1 x2, Y2 (TMEM).
 // Units of work: a tile holds floor(128 / C) whole rows when a row has C <= 128 chunks
@@ -104,8 +108,8 @@ namespace {
 
 constexpr int kT = 64;          // steps per chunk
 constexpr int kCols = 128;      // chunks per tile
-constexpr int kThreads = 448;   // warps 0-3 scan, 4-7 conv, 8-11 epi, 12 mma, 13 producer
-constexpr int kScanBar = 1, kConvBar = 2, kEpiBar = 3;  // named barriers (128 threads each)
+constexpr int kThreads = 320;   // warps 0-7 main, 8 mma, 9 producer
+constexpr int kMainBar = 1;     // named barrier of the 256 main threads
 
 // TMEM columns (512 allocated): Q (hi 32 + lo 32 columns: A operand of GEMM1, two f16 per
 // column), S x2, Y1 x2, Y2
@@ -122,28 +126,27 @@ constexpr uint32_t kUBuf = 32768, kULo = 16384;
 constexpr uint32_t kXHi = 65536, kXLo = 98304;      // Xin [128 chunks x 128 rows]
 constexpr uint32_t kTkHi = 131072, kTkLo = 139264;  // Toeplitz [64 t x 64 s], K-major
 constexpr uint32_t kGHi = 147456, kGLo = 163840;    // G [64 t x 128 rows], K-major
-constexpr uint32_t kYStage = 180224;  // y staging, one 8 KB image per epilogue warp:
-                                      // [2 halves][32 lines][32 floats], swizzled
-constexpr uint32_t kRowEs = kYStage + 32768;  // int[2][128] u scale exponent of each row
-constexpr uint32_t kRowMaxU = kRowEs + 1024;  // uint[128] max |u| of each row (scratch)
-constexpr uint32_t kAy = kRowMaxU + 512;      // float[2][128] 1 / (u scale * K scale)
-constexpr uint32_t kBy = kAy + 1024;          // float[2][128] 1 / (Xin scale * G scale)
-constexpr uint32_t kScanRed = kBy + 1024;     // uint[4] per-warp max |carried state|
+constexpr uint32_t kYStage = 180224;  // y staging, one 4 KB image per main warp:
+                                      // [32 lines][32 floats], swizzled
+constexpr uint32_t kRowEs = kYStage + 32768;  // int[4][128] u scale exponent of each row
+constexpr uint32_t kRowMaxU = kRowEs + 2048;  // uint[128] max |u| of each row (scratch)
+constexpr uint32_t kAy = kRowMaxU + 512;      // float[4][128] 1 / (u scale * K scale)
+constexpr uint32_t kBy = kAy + 2048;          // float[4][128] 1 / (Xin scale * G scale)
+constexpr uint32_t kScanRed = kBy + 2048;     // uint[4] per-warp max |carried state|
 constexpr uint32_t kBars = kScanRed + 16;     // mbarriers
 // A waiter may trail the phase it waits for by at most one completed phase (the parity test
 // cannot tell phase j from phase j + 2): every wait below is on a barrier that cannot
 // complete twice more before the waiter has passed it.
 constexpr int kBarStage = 0,   // [2] u tile (float32) landed in its operand buffer (TMA bytes)
-    kBarUFull = 2,             // [2] u operand and its scales written (conv, 128)
+    kBarUFull = 2,             // [2] u operand and its scales written (main, 256)
     kBarG1 = 4,                // [2] GEMM1 + Toeplitz done: S, Y1 ready, u buffer free (commit)
-    kBarScanStart = 6,         // [2] u scales read, Xin scales written (scan, 128)
-    kBarXFull = 8,             // Xin operand written, S read (scan, 128)
-    kBarG2 = 9,                // GEMM2 (state part) done: Y2 ready, Xin buffer free (commit)
-    kBarY1Free = 10,           // [2] Y1 read out of TMEM (epi, 128)
-    kBarY2Free = 12,           // Y2 read out of TMEM (epi, 128)
-    kBarTabTk = 13,            // Toeplitz operand copied (bytes)
-    kBarTabG = 14,             // G operand copied (bytes)
-    kNumBars = 15;
+    kBarXFull = 6,             // Xin operand written, S read (main, 256)
+    kBarG2 = 7,                // GEMM2 (state part) done: Y2 ready, Xin buffer free (commit)
+    kBarY1Free = 8,            // [2] Y1 read out of TMEM (main, 256)
+    kBarY2Free = 10,           // Y2 read out of TMEM (main, 256)
+    kBarTabTk = 11,            // Toeplitz operand copied (bytes)
+    kBarTabG = 12,             // G operand copied (bytes)
+    kNumBars = 13;
 constexpr uint32_t kSlot = kBars + 8 * kNumBars;  // TMEM base address
 constexpr uint32_t kAbort = kSlot + 4;            // abort flag
 constexpr uint32_t kEnd = kAbort + 4;
@@ -191,11 +194,19 @@ __device__ __forceinline__ int scale_exp(float m) {
 }
 __device__ __forceinline__ float exp2i(int s) { return __int_as_float((s + 127) << 23); }
 
-// a, b -> f16 pairs hi = rn(a, b), lo = rn(a - hi, b - hi)
+// a, b -> f16 pairs: hi = a and b rounded to 11 significant bits (to nearest, ties away from
+// zero, by an integer add at the 13th mantissa bit and a mask: exact in f16 for |a| >= 2^-14),
+// lo = the f16 rounding of the remainder (|lo| <= 2^-11 |a|). The pair carries a to 2^-22 of
+// |a| (and to 2^-24 absolute below the f16 normal range); every operand is scaled so that its
+// largest magnitude lies near 2^14, which keeps the absolute floor far below what the products
+// need. No conversion result feeds another conversion.
+__device__ __forceinline__ float round11(float a) {
+  return __uint_as_float((__float_as_uint(a) + 0x1000u) & 0xFFFFE000u);
+}
 __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __half2 h = __floats2half2_rn(a, b);
-  const float2 f = __half22float2(h);
-  const __half2 l = __floats2half2_rn(a - f.x, b - f.y);
+  const float ah = round11(a), bh = round11(b);
+  const __half2 h = __floats2half2_rn(ah, bh);
+  const __half2 l = __floats2half2_rn(a - ah, b - bh);
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
@@ -298,69 +309,66 @@ __device__ __forceinline__ TileInfo tile_info(const TcScanArgs& a, int u0, int s
   return t;
 }
 
+// The tiles of a CTA in order, without a division after the first: the channel, the group of
+// batch rows (row mode) or batch row (long rows) within it, and the segment of the row.
+struct TileIter {
+  TileInfo t;
+  int bt;  // group of rows (row mode) or batch row (long rows) within the channel
+};
+__device__ __forceinline__ TileIter tile_iter_begin(const TcScanArgs& a, int u0) {
+  TileIter it;
+  it.t.seg = 0;
+  if (a.R > 0) {
+    it.t.h = u0 / a.tiles_per_h;
+    it.bt = u0 - it.t.h * a.tiles_per_h;
+    it.t.b0 = it.bt * a.R;
+    it.t.nrows = min(a.R, a.B - it.t.b0);
+  } else {
+    it.t.h = u0 / a.B;
+    it.bt = u0 - it.t.h * a.B;
+    it.t.b0 = it.bt;
+    it.t.nrows = 1;
+  }
+  return it;
+}
+__device__ __forceinline__ void tile_iter_next(const TcScanArgs& a, int segs, TileIter& it) {
+  if (++it.t.seg < segs) return;
+  it.t.seg = 0;
+  if (++it.bt == ((a.R > 0) ? a.tiles_per_h : a.B)) {
+    it.bt = 0;
+    ++it.t.h;
+  }
+  if (a.R > 0) {
+    it.t.b0 = it.bt * a.R;
+    it.t.nrows = min(a.R, a.B - it.t.b0);
+  } else {
+    it.t.b0 = it.bt;
+  }
+}
+
 // Column g of a tile: its row within the tile, chunk index within its row, batch row offset
-// (elements) and first step, and whether it is used.
+// (elements) and first step, and whether it is used. In row mode the row and chunk of a column
+// are the same in every tile (`rc` = (g / C, g % C), computed once).
 struct ColInfo {
   size_t rowoff;
   int rl, c, k0;
   bool valid;
 };
-__device__ __forceinline__ ColInfo col_info(const TcScanArgs& a, const TileInfo& t, int g) {
-  ColInfo ci;
+__device__ __forceinline__ int2 col_rows(const TcScanArgs& a, int g) {
   if (a.R > 0) {
-    ci.rl = g / a.C;
-    ci.c = g - ci.rl * a.C;
-  } else {
-    ci.rl = 0;
-    ci.c = t.seg * kCols + g;
+    const int rl = g / a.C;
+    return make_int2(rl, g - rl * a.C);
   }
+  return make_int2(0, g);
+}
+__device__ __forceinline__ ColInfo col_info(const TcScanArgs& a, const TileInfo& t, int2 rc) {
+  ColInfo ci;
+  ci.rl = rc.x;
+  ci.c = (a.R > 0) ? rc.y : t.seg * kCols + rc.y;
   ci.valid = (a.R > 0) ? (ci.rl < t.nrows) : (ci.c < a.C);
   ci.rowoff = ((size_t)(t.b0 + (ci.valid ? ci.rl : 0)) * a.H + t.h) * (size_t)a.L;
   ci.k0 = ci.c * kT;
   return ci;
-}
-
-// One 64-element K-major row of an f16 operand tile pair (swizzled as described above).
-__device__ __forceinline__ void store_row64(uint8_t* hi_tile, uint8_t* lo_tile, int row,
-                                            const float (&v)[64]) {
-#pragma unroll
-  for (int p = 0; p < 8; ++p) {
-    uint32_t h[4], l[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) split2(v[8 * p + 2 * q], v[8 * p + 2 * q + 1], h[q], l[q]);
-    const uint32_t off = uint32_t(row) * 128u + ((uint32_t(p) ^ uint32_t(row & 7)) << 4);
-    *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
-  }
-}
-
-// u_{g,t} for t < 64 of the chunk starting at step k0 of a row (the reversed row when kRev);
-// zero past the end of the row or for an unused column.
-template <bool kRev>
-__device__ __forceinline__ void load_chunk(const float* __restrict__ row, int L, int k0,
-                                           bool valid, float (&v)[64]) {
-  const int len = valid ? min(kT, L - k0) : 0;
-  if (len == kT && (L & 3) == 0) {
-    if (!kRev) {
-      const float4* p = reinterpret_cast<const float4*>(row + k0);
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float4 x = __ldg(p + q);
-        v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
-      }
-    } else {
-      const float4* p = reinterpret_cast<const float4*>(row + (L - k0 - kT));
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        const float4 x = __ldg(p + q);
-        v[63 - 4 * q] = x.x; v[62 - 4 * q] = x.y; v[61 - 4 * q] = x.z; v[60 - 4 * q] = x.w;
-      }
-    }
-  } else {
-#pragma unroll
-    for (int t = 0; t < kT; ++t)
-      v[t] = (t < len) ? __ldg(row + (kRev ? (L - 1 - k0 - t) : (k0 + t))) : 0.f;
-  }
 }
 
 // y at steps kb .. kb+31 of a row: stored (forward) or added at the mirrored steps (kRev).
@@ -528,7 +536,7 @@ __global__ void __launch_bounds__(kTbThreads, 2)
 
 // producer thread: the TMA tiles of u for tile k, as float32, into the tile's operand buffer
 // (k & 1) -- forward chunk order, one 128-byte line per chunk and half, 128-byte swizzle --
-// completing on kBarStage + (k & 1). The conv warps convert them in place. Row mode: boxes of
+// completing on kBarStage + (k & 1). The main warps convert them in place. Row mode: boxes of
 // bc chunks of each valid row; one-row mode: two boxes of 64 chunks. Chunks past the row (or
 // before it, reversed) read as zero.
 template <bool kRev>
@@ -563,71 +571,42 @@ __device__ __forceinline__ int mirrored_line(const TcScanArgs& a, int g) {
   return base + cb * bc + (bc - 1 - j);
 }
 
-// conv warps: u chunks of tile k -> scaled f16 pair, K-major (thread = chunk column g), in
-// place over the float32 tile the TMA wrote into the same buffer (every thread has read its
-// chunk before the barrier inside, and writes only after it), or straight from memory.
+// u at steps kb .. kb + 31 of the chunk that starts at step k0 of a row (the reversed row when
+// kRev); zero past the end of the row or for an unused column.
 template <bool kRev>
-__device__ __forceinline__ void convert_u(const TcScanArgs& a, uint8_t* sm, int u0, int segs,
-                                          int k, float sig_k) {
-  const int g = threadIdx.x - 128;
-  const int par = k & 1;
-  const TileInfo ti = tile_info(a, u0, segs, k);
-  const ColInfo ci = col_info(a, ti, g);
-  float v[64];
-  if (a.tma) {
-    const int line = kRev ? mirrored_line(a, g) : g;
-    const uint32_t sw = uint32_t(line & 7);
+__device__ __forceinline__ void load_part32(const float* __restrict__ row, int L, int kb,
+                                            bool valid, float (&v)[32]) {
+  const int len = valid ? min(32, L - kb) : 0;
+  if (len == 32 && (L & 3) == 0) {
+    if (!kRev) {
+      const float4* p = reinterpret_cast<const float4*>(row + kb);
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const float4 x = *reinterpret_cast<const float4*>(
-          sm + kU + par * kUBuf + (q >> 3) * 16384 + line * 128 + ((uint32_t(q & 7) ^ sw) << 4));
-      if (!kRev) {
+      for (int q = 0; q < 8; ++q) {
+        const float4 x = __ldg(p + q);
         v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
-      } else {
-        v[63 - 4 * q] = x.x; v[62 - 4 * q] = x.y; v[61 - 4 * q] = x.z; v[60 - 4 * q] = x.w;
+      }
+    } else {
+      const float4* p = reinterpret_cast<const float4*>(row + (L - kb - 32));
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 x = __ldg(p + q);
+        v[31 - 4 * q] = x.x; v[30 - 4 * q] = x.y; v[29 - 4 * q] = x.z; v[28 - 4 * q] = x.w;
       }
     }
-    if (!ci.valid) {
-#pragma unroll
-      for (int t = 0; t < kT; ++t) v[t] = 0.f;
-    }
   } else {
-    load_chunk<kRev>(a.u + ci.rowoff, a.L, ci.k0, ci.valid, v);
-  }
-  // the row's largest |u| in this tile: a warp reduction when the warp's 32 chunks share a
-  // row, else one shared-memory atomic per chunk (non-negative floats order as their bits)
-  float m = 0.f;
 #pragma unroll
-  for (int t = 0; t < kT; ++t) m = fmaxf(m, fabsf(v[t]));
-  unsigned* rmax = reinterpret_cast<unsigned*>(sm + kRowMaxU);
-  const int rl = ci.rl;
-  const bool warp_row = __shfl_sync(0xffffffffu, rl, 0) == __shfl_sync(0xffffffffu, rl, 31);
-  if (warp_row) {
-    const unsigned mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
-    if ((g & 31) == 0) atomicMax(&rmax[rl], mw);
-  } else {
-    atomicMax(&rmax[rl], __float_as_uint(m));
+    for (int t = 0; t < 32; ++t)
+      v[t] = (t < len) ? __ldg(row + (kRev ? (L - 1 - kb - t) : (kb + t))) : 0.f;
   }
-  named_bar(kConvBar, 128);
-  const int es = scale_exp(__uint_as_float(rmax[rl]));
-  const float su = exp2i(es);
-#pragma unroll
-  for (int t = 0; t < kT; ++t) v[t] *= su;
-  uint8_t* ubuf = sm + kU + par * kUBuf;
-  store_row64(ubuf, ubuf + kULo, g, v);
-  if (ci.c == 0 || g == 0) reinterpret_cast<int*>(sm + kRowEs)[par * 128 + rl] = es;
-  reinterpret_cast<float*>(sm + kAy)[par * 128 + g] = exp2i(-es) / sig_k;
-  tc::fence_proxy_async_smem();
 }
 
-// conv warps, at the first tile of a channel: Q of the channel from its blob into TMEM
-// (thread r = lane r).
-__device__ __forceinline__ void load_q(const uint8_t* blob, uint32_t tmem) {
-  const int r = threadIdx.x - 128, warp = threadIdx.x >> 5;
-  const uint4* q = reinterpret_cast<const uint4*>(blob + kBlobQ + r * 256);
-  const uint32_t tl = tmem + (uint32_t((warp & 3) * 32) << 16) + kTQ;
+// main warps, at the first tile of a channel: half h of Q of the channel (the hi words for
+// h = 0, the lo words for h = 1) from its blob into TMEM (thread = lane r of its quarter).
+__device__ __forceinline__ void load_q_half(const uint8_t* blob, uint32_t tmem, int r, int h) {
+  const uint4* q = reinterpret_cast<const uint4*>(blob + kBlobQ + r * 256) + 8 * h;
+  const uint32_t tl = tmem + (uint32_t(r & ~31) << 16) + kTQ + 32 * h;
 #pragma unroll
-  for (int part = 0; part < 4; ++part) {  // words 16 part .. 16 part + 15 (hi: 0, 1; lo: 2, 3)
+  for (int part = 0; part < 2; ++part) {
     uint32_t w[16];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -638,57 +617,98 @@ __device__ __forceinline__ void load_q(const uint8_t* blob, uint32_t tmem) {
   }
 }
 
-// conv warps, tile k: the u operand of the tile, and Q of a new channel.
+// main warps, tile j: u -> the scaled f16 pair operand (K-major). Thread = chunk column g (lane
+// of its quarter), half h = steps 32h .. 32h + 31 of the chunk; the float32 tile the TMA wrote
+// into the same buffer is read by every thread before the barrier inside and overwritten only
+// after it. Also the row scales of the tile (ring slot j & 3) and, at a new channel, Q.
 template <bool kRev>
-__device__ __forceinline__ bool conv_u_step(const TcScanArgs& a, uint8_t* sm, uint32_t tmem,
-                                            int u0, int segs, int k, int& cur_h, float& sig_k,
-                                            volatile int* abort) {
-  const int tid = threadIdx.x;
+__device__ __forceinline__ bool conv_tile(const TcScanArgs& a, uint8_t* sm, uint32_t tmem,
+                                          const TileInfo& ti, int2 rc, int j, int& cur_h,
+                                          float& sig_k, volatile int* abort) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = warp >> 2, g = (warp & 3) * 32 + lane;
+  const int par = j & 1, slot = j & 3;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-  const TileInfo ti = tile_info(a, u0, segs, k);
   const bool new_channel = ti.h != cur_h;
-  const int par = k & 1;
-  // the u buffer and scale slots of tile k-2 released (its GEMM1 done, its scales read by the
-  // scan and the epilogue); at a new channel also GEMM1 of tile k-1 done (Q is reloaded); the
-  // u tile landed
+  // the u buffer released by GEMM1 of tile j-2; at a new channel also GEMM1 of tile j-1 done
+  // (Q is reloaded); the u tile landed
   bool ok = true;
-  if (k >= 2)
-    ok = warp_wait_phase(&bars[kBarG1 + par], ((k - 2) >> 1) & 1, abort) &&
-         warp_wait_phase(&bars[kBarScanStart + par], ((k - 2) >> 1) & 1, abort) &&
-         warp_wait_phase(&bars[kBarY1Free + par], ((k - 2) >> 1) & 1, abort);
-  if (ok && new_channel && k >= 1)
-    ok = warp_wait_phase(&bars[kBarG1 + (par ^ 1)], ((k - 1) >> 1) & 1, abort);
-  if (ok && a.tma) ok = warp_wait_phase(&bars[kBarStage + par], (k >> 1) & 1, abort);
-  if (!named_bar_and(kConvBar, 128, ok)) return false;
-  if (tid == 128) SCAN_TRACE(1000 + k * 8 + 1);
+  if (j >= 2) ok = warp_wait_phase(&bars[kBarG1 + par], ((j - 2) >> 1) & 1, abort);
+  if (ok && new_channel && j >= 1)
+    ok = warp_wait_phase(&bars[kBarG1 + (par ^ 1)], ((j - 1) >> 1) & 1, abort);
+  if (ok && a.tma) ok = warp_wait_phase(&bars[kBarStage + par], (j >> 1) & 1, abort);
+  if (!named_bar_and(kMainBar, 256, ok)) return false;
+  if (threadIdx.x == 0) SCAN_TRACE(1000 + j * 8 + 1);
   const uint8_t* blob = a.tables + (size_t)ti.h * kBlobBytes;
   if (new_channel) {
     cur_h = ti.h;
     sig_k = __ldg(reinterpret_cast<const float*>(blob + kBlobSig));
   }
-  convert_u<kRev>(a, sm, u0, segs, k, sig_k);
+  const ColInfo ci = col_info(a, ti, rc);
+  uint8_t* ubuf = sm + kU + par * kUBuf;
+  float v[32];
+  if (a.tma) {
+    const int line = kRev ? mirrored_line(a, g) : g;
+    const uint32_t sw = uint32_t(line & 7);
+    const uint8_t* src = ubuf + (kRev ? 1 - h : h) * 16384 + line * 128;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 x = *reinterpret_cast<const float4*>(src + ((uint32_t(q) ^ sw) << 4));
+      if (!kRev) {
+        v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
+      } else {
+        v[31 - 4 * q] = x.x; v[30 - 4 * q] = x.y; v[29 - 4 * q] = x.z; v[28 - 4 * q] = x.w;
+      }
+    }
+    if (!ci.valid) {
+#pragma unroll
+      for (int t = 0; t < 32; ++t) v[t] = 0.f;
+    }
+  } else {
+    load_part32<kRev>(a.u + ci.rowoff, a.L, ci.k0 + 32 * h, ci.valid, v);
+  }
+  // the row's largest |u| in this tile: a warp reduction when the warp's 32 chunks share a
+  // row, else one shared-memory atomic per thread (non-negative floats order as their bits)
+  float m = 0.f;
+#pragma unroll
+  for (int t = 0; t < 32; ++t) m = fmaxf(m, fabsf(v[t]));
+  unsigned* rmax = reinterpret_cast<unsigned*>(sm + kRowMaxU);
+  const int rl = ci.rl;
+  const bool warp_row = __shfl_sync(0xffffffffu, rl, 0) == __shfl_sync(0xffffffffu, rl, 31);
+  if (warp_row) {
+    const unsigned mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+    if (lane == 0) atomicMax(&rmax[rl], mw);
+  } else {
+    atomicMax(&rmax[rl], __float_as_uint(m));
+  }
+  named_bar(kMainBar, 256);
+  const int es = scale_exp(__uint_as_float(rmax[rl]));
+  const float su = exp2i(es);
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    float w8[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w8[i] = v[8 * p + i] * su;
+    store_chunk8(ubuf, ubuf + kULo, g, 4 * h + p, w8);
+  }
+  if (h == 0) {
+    if (ci.c == 0 || g == 0) reinterpret_cast<int*>(sm + kRowEs)[slot * 128 + rl] = es;
+    reinterpret_cast<float*>(sm + kAy)[slot * 128 + g] = exp2i(-es) / sig_k;
+  }
+  tc::fence_proxy_async_smem();
   if (new_channel) {
-    load_q(blob, tmem);
+    load_q_half(blob, tmem, g, h);
     tc::tmem_wait_st();
   }
   tc::fence_before_sync();
-  if (tid == 128) SCAN_TRACE(1000 + k * 8 + 2);
+  if (threadIdx.x == 0) SCAN_TRACE(1000 + j * 8 + 2);
   tc::mbar_arrive(&bars[kBarUFull + par]);
-  named_bar(kConvBar, 128);  // every thread has read the row maxima of this tile
-  reinterpret_cast<unsigned*>(sm + kRowMaxU)[tid - 128] = 0u;
+  named_bar(kMainBar, 256);  // every thread has read the row maxima of this tile
+  if (h == 0) rmax[g] = 0u;
   return true;
 }
 
-template <bool kRev>
-__device__ __forceinline__ void conv_role(const TcScanArgs& a, uint8_t* sm, uint32_t tmem, int u0,
-                                          int segs, int ntiles, volatile int* abort) {
-  int cur_h = -1;
-  float sig_k = 1.f;
-  for (int k = 0; k < ntiles; ++k)
-    if (!conv_u_step<kRev>(a, sm, tmem, u0, segs, k, cur_h, sig_k, abort)) return;
-}
-
-// producer (warp 13, lane 0): every bulk copy into shared memory, taken in the order the MMA
+// producer (warp 9, lane 0): every bulk copy into shared memory, taken in the order the MMA
 // groups complete (GEMM1 of tile 0, then GEMM1 of tile k+1 and GEMM2 of tile k for k = 0, 1,
 // ...): u of tile k into operand buffer k & 1 once GEMM1 of tile k-2 has read that buffer;
 // the Toeplitz operand of a new channel once GEMM1 of the previous tile is done, its G operand
@@ -746,85 +766,65 @@ __device__ __forceinline__ void producer_role(const TcScanArgs& a, const CUtenso
   }
 }
 
-// epi warps: y of tile k (thread = chunk column g = TMEM lane). Y1 (Toeplitz part, ready with
-// GEMM1) is read first into registers, releasing its TMEM buffer early; then Y2 (state part),
-// and y = Y1 / (u scale * K scale) + Y2 / (Xin scale * G scale). With whole-chunk rows (the
-// TMA shapes) each warp writes its 32 chunks into its staging image and one lane stores them
-// as two TMA tiles of 32 steps x 32 chunks (added, at the mirrored chunks and steps, when
-// kRev); otherwise each thread stores its chunk's 64 steps itself.
+// main warps: y of tile j once GEMM2 of the tile is done (thread = chunk column g = TMEM lane
+// of its quarter, half h = steps 32h .. 32h + 31): y = Y1 / (u scale * K scale) + Y2 / (Xin
+// scale * G scale). With whole-chunk rows (the TMA shapes) each warp writes its 32 chunks x 32
+// steps into its staging image and one lane stores them as one TMA tile (added, at the
+// mirrored chunks and steps, when kRev); otherwise each thread stores its 32 steps itself.
 template <bool kRev>
-__device__ __forceinline__ bool store_tile(const TcScanArgs& a, const CUtensorMap* ymap,
-                                           uint8_t* sm, uint32_t tmem, int u0, int segs, int k,
-                                           volatile int* abort) {
-  const int g = threadIdx.x - 256, warp = threadIdx.x >> 5;
-  const int par = k & 1;
+__device__ __forceinline__ bool epi_tile(const TcScanArgs& a, const CUtensorMap* ymap,
+                                         uint8_t* sm, uint32_t tmem, const TileInfo& ti,
+                                         int2 rc, int j, volatile int* abort) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = warp >> 2, quarter = warp & 3, g = quarter * 32 + lane;
+  const int par = j & 1, slot = j & 3;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-  const uint32_t lane_base = tmem + (uint32_t((warp & 3) * 32) << 16);
-  // Y1 of tile k with the u scales (conv) and Xin scales (scan) of tile k: once read, the Y1
-  // buffer and both scale slots may take tile k + 2
-  bool ok = warp_wait_phase(&bars[kBarG1 + par], (k >> 1) & 1, abort) &&
-            warp_wait_phase(&bars[kBarScanStart + par], (k >> 1) & 1, abort) &&
-            warp_wait_phase(&bars[kBarUFull + par], (k >> 1) & 1, abort);
-  if (!named_bar_and(kEpiBar, 128, ok)) return false;
-  if (g == 0) SCAN_TRACE(2000 + k * 8 + 0);
+  const bool ok = warp_wait_phase(&bars[kBarG2], j & 1, abort);
+  if (!named_bar_and(kMainBar, 256, ok)) return false;
+  if (threadIdx.x == 0) SCAN_TRACE(2000 + j * 8 + 1);
   tc::fence_after_sync();
-  const float ay = reinterpret_cast<const float*>(sm + kAy)[par * 128 + g];
-  const float by = reinterpret_cast<const float*>(sm + kBy)[par * 128 + g];
-  float y[64];
-  tc::tmem_ld32(lane_base + kTY1 + par * 64, *reinterpret_cast<float(*)[32]>(y));
-  tc::tmem_ld32(lane_base + kTY1 + par * 64 + 32, *reinterpret_cast<float(*)[32]>(y + 32));
+  const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
+  float y1[32], y2[32];
+  tc::tmem_ld32(lane_base + kTY1 + par * 64 + 32 * h, y1);
+  tc::tmem_ld32(lane_base + kTY2 + 32 * h, y2);
   tc::fence_before_sync();
   tc::mbar_arrive(&bars[kBarY1Free + par]);
-  // Y2 of tile k
-  ok = warp_wait_phase(&bars[kBarG2], k & 1, abort);
-  if (!named_bar_and(kEpiBar, 128, ok)) return false;
-  if (g == 0) SCAN_TRACE(2000 + k * 8 + 1);
-  tc::fence_after_sync();
-#pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4) {
-    float y2[16];
-    tc::tmem_ld16(lane_base + kTY2 + q4 * 16, y2);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) y[q4 * 16 + j] = fmaf(y[q4 * 16 + j], ay, y2[j] * by);
-  }
-  tc::fence_before_sync();
   tc::mbar_arrive(&bars[kBarY2Free]);
-  const TileInfo ti = tile_info(a, u0, segs, k);
-  const ColInfo ci = col_info(a, ti, g);
+  const float ay = reinterpret_cast<const float*>(sm + kAy)[slot * 128 + g];
+  const float by = reinterpret_cast<const float*>(sm + kBy)[slot * 128 + g];
+  float y[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) y[i] = fmaf(y1[i], ay, y2[i] * by);
+  const ColInfo ci = col_info(a, ti, rc);
   if (a.tma) {
-    const int lane = g & 31;
-    uint8_t* stg = sm + kYStage + (warp & 3) * 8192;
-    if (lane == 0) tc::bulk_wait_group_read0();  // this warp's previous tiles left the image
+    uint8_t* stg = sm + kYStage + warp * 4096;
+    if (lane == 0) tc::bulk_wait_group_read0();  // this warp's previous tile left the image
     __syncwarp();
     const int line = kRev ? 31 - lane : lane;
     const uint32_t sw = uint32_t(line & 7);
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {  // steps 4q .. 4q + 3 of the chunk (reversed when kRev)
-      const float4 v = kRev ? make_float4(y[63 - 4 * q], y[62 - 4 * q], y[61 - 4 * q],
-                                          y[60 - 4 * q])
+    for (int q = 0; q < 8; ++q) {  // steps 4q .. 4q + 3 of the half (reversed when kRev)
+      const float4 v = kRev ? make_float4(y[31 - 4 * q], y[30 - 4 * q], y[29 - 4 * q],
+                                          y[28 - 4 * q])
                             : make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
-      *reinterpret_cast<float4*>(stg + (q >> 3) * 4096 + line * 128 +
-                                 ((uint32_t(q & 7) ^ sw) << 4)) = v;
+      *reinterpret_cast<float4*>(stg + line * 128 + ((uint32_t(q) ^ sw) << 4)) = v;
     }
     tc::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0 && ci.valid) {
-      // 32 columns of one row, chunks ci.c .. ci.c + 31 (reversed: forward chunks from C-32-c)
+      // 32 chunks of one row, chunks ci.c .. ci.c + 31 (reversed: forward chunks from C-32-c),
+      // steps 32h .. 32h + 31 (reversed: forward steps 32(1-h) .. 32(1-h) + 31)
       const int z = (ti.b0 + ci.rl) * a.H + ti.h;
       const int yc = kRev ? a.C - 32 - ci.c : ci.c;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        if (kRev) tc::tma_reduce_add_3d(ymap, stg + half * 4096, half * 32, yc, z);
-        else tc::tma_store_3d(ymap, stg + half * 4096, half * 32, yc, z);
-      }
+      const int x = kRev ? 32 * (1 - h) : 32 * h;
+      if (kRev) tc::tma_reduce_add_3d(ymap, stg, x, yc, z);
+      else tc::tma_store_3d(ymap, stg, x, yc, z);
       tc::bulk_commit_group();
     }
-    if (g == 0) SCAN_TRACE(2000 + k * 8 + 2);
   } else if (ci.valid) {
-    float* yrow = a.y + ci.rowoff;
-    store_part<kRev>(yrow, a.L, ci.k0, *reinterpret_cast<float(*)[32]>(y));
-    store_part<kRev>(yrow, a.L, ci.k0 + 32, *reinterpret_cast<float(*)[32]>(y + 32));
+    store_part<kRev>(a.y + ci.rowoff, a.L, ci.k0 + 32 * h, y);
   }
+  if (threadIdx.x == 0) SCAN_TRACE(2000 + j * 8 + 2);
   return true;
 }
 
@@ -888,19 +888,17 @@ __device__ __forceinline__ void gemm2(uint8_t* sm, uint32_t tmem, int k) {
 // MMA thread over all tiles of the CTA, in the order GEMM1 of tile k+1, GEMM2 of tile k. At a
 // change of channel GEMM1 waits for the producer's copy of the Toeplitz operand and GEMM2 for
 // its copy of G. Returns false on abort.
-__device__ __forceinline__ bool mma_g1(const TcScanArgs& a, uint8_t* sm, uint32_t tmem, int u0,
-                                       int segs, int k, int& tk_h, uint32_t& tk_n,
-                                       volatile int* abort) {
+__device__ __forceinline__ bool mma_g1(uint8_t* sm, uint32_t tmem, int h, int k, int& tk_h,
+                                       uint32_t& tk_n, volatile int* abort) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
   const int par = k & 1;
-  const int h = tile_info(a, u0, segs, k).h;
   if (h != tk_h) {  // the Toeplitz operand of a new channel (copied by the producer)
     if (!wait_phase(&bars[kBarTabTk], tk_n & 1, abort)) return false;
     ++tk_n;
     tk_h = h;
   }
   // u of tile k written; the Y1 buffer read out (tile k-2). The S buffer of tile k-2 was read
-  // by the scan before it released Xin of that tile, which this thread waited for before
+  // by the chain before it released Xin of that tile, which this thread waited for before
   // issuing GEMM2 of tile k-2 (program order: GEMM1 k, GEMM2 k-1, GEMM1 k+1, ...).
   if (!wait_phase(&bars[kBarUFull + par], (k >> 1) & 1, abort)) return false;
   if (k >= 2 && !wait_phase(&bars[kBarY1Free + par], ((k - 2) >> 1) & 1, abort)) return false;
@@ -908,34 +906,42 @@ __device__ __forceinline__ bool mma_g1(const TcScanArgs& a, uint8_t* sm, uint32_
   return true;
 }
 
-__device__ __forceinline__ bool mma_g2(const TcScanArgs& a, uint8_t* sm, uint32_t tmem, int u0,
-                                       int segs, int k, int& g_h, uint32_t& g_n,
-                                       volatile int* abort) {
+__device__ __forceinline__ bool mma_g2(uint8_t* sm, uint32_t tmem, int h, int k, int& g_h,
+                                       uint32_t& g_n, volatile int* abort) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-  const int h = tile_info(a, u0, segs, k).h;
   if (h != g_h) {  // the G operand of a new channel (copied by the producer)
     if (!wait_phase(&bars[kBarTabG], g_n & 1, abort)) return false;
     ++g_n;
     g_h = h;
   }
+  SCAN_TRACE(3000 + k * 4 + 2);
   if (!wait_phase(&bars[kBarXFull], k & 1, abort)) return false;
   if (k >= 1 && !wait_phase(&bars[kBarY2Free], (k - 1) & 1, abort)) return false;
   gemm2(sm, tmem, k);
   return true;
 }
 
+// MMA thread over all tiles of the CTA, in the order GEMM1 of tile k+1, GEMM2 of tile k. At a
+// change of channel GEMM1 waits for the producer's copy of the Toeplitz operand and GEMM2 for
+// its copy of G.
 __device__ __forceinline__ void mma_role(const TcScanArgs& a, uint8_t* sm, uint32_t tmem,
                                          int u0, int segs, int ntiles, volatile int* abort) {
   int tk_h = -1, g_h = -1;
   uint32_t tk_n = 0, g_n = 0;
-  if (ntiles == 0 || !mma_g1(a, sm, tmem, u0, segs, 0, tk_h, tk_n, abort)) return;
+  if (ntiles == 0) return;
+  TileIter it1 = tile_iter_begin(a, u0), it2 = it1;
+  if (!mma_g1(sm, tmem, it1.t.h, 0, tk_h, tk_n, abort)) return;
   for (int k = 0; k < ntiles; ++k) {
-    if (k + 1 < ntiles && !mma_g1(a, sm, tmem, u0, segs, k + 1, tk_h, tk_n, abort)) return;
-    if (!mma_g2(a, sm, tmem, u0, segs, k, g_h, g_n, abort)) return;
+    if (k + 1 < ntiles) {
+      tile_iter_next(a, segs, it1);
+      if (!mma_g1(sm, tmem, it1.t.h, k + 1, tk_h, tk_n, abort)) return;
+    }
+    if (!mma_g2(sm, tmem, it2.t.h, k, g_h, g_n, abort)) return;
+    tile_iter_next(a, segs, it2);
   }
 }
 
-// ---- scan warps ---------------------------------------------------------------------------
+// ---- the chain ---------------------------------------------------------------------------
 // Xin leaves the scan as X * 2^-xs, X in the S units of its tile (true state * 2^(es + 14)).
 // Within a tile |S| <= 64 * 2^14 * 2^14 per component, so a state that starts the tile at zero
 // stays below 127 * 2^34.5 < 2^41.5 and xs = 27 keeps Xin below 2^14.5, inside the f16 range
@@ -985,138 +991,148 @@ __device__ __forceinline__ void store_xin8(uint8_t* sm, int r, int g0, const flo
   *reinterpret_cast<uint4*>(sm + kXLo + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// Row mode with rows of kC in {16, 32, 64} chunks (two or more rows per tile). The two threads
-// of state n split the rows: the even (Re) thread runs rows 0, 2, ..., the odd (Im) thread
-// rows 1, 3, ..., each the full complex recurrence; the other component of S comes from the
-// partner lane, which receives this lane's S of the partner's row in exchange. Each thread
-// writes both Xin K-rows of the state for its own columns. Software-pipelined by 8 chunks:
-// the stores of one piece and the recurrence of the next form one block, so the stores fill
-// the latency of the recurrence. The Xin buffer is written once GEMM2 of the previous tile
-// has released it (`wait_g2`, checked before the first store).
-template <int kC>
-__device__ __forceinline__ bool chain_pairs(uint8_t* sm, uint32_t tS, const ChainConst& q,
-                                            float xscale, bool wait_g2, uint32_t g2_parity,
-                                            volatile int* abort) {
-  const int tid = threadIdx.x;
-  const bool odd = (tid & 1) != 0;
-  const int col_off = odd ? kC : 0;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-#pragma unroll 1
-  for (int base = 0; base < kCols; base += 2 * kC) {
-    float xo = 0.f, xt = 0.f, ao = 0.f, at = 0.f;
-    float sa[8], sb[8];
-    tc::tmem_ld8x2(tS + base, tS + base + kC, sa, sb);
-    float oo[8], ot[8];  // outputs of the previous piece, stored with the next piece
-#pragma unroll 1
-    for (int c = base; c < base + kC; c += 8) {
-      if (c != base) {
-        if (((c - base) & 31) == 0) chain_anchor(q, xo, xt, ao, at);
-        if (wait_g2) {
-          if (!warp_wait_phase(&bars[kBarG2], g2_parity, abort)) return false;
-          wait_g2 = false;
-        }
-      }
-      float no[8], nt[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float own = odd ? sb[j] : sa[j];
-        const float oth = __shfl_xor_sync(0xffffffffu, odd ? sa[j] : sb[j], 1);
-        no[j] = xo;
-        nt[j] = xt;
-        chain_step(q, own, oth, xo, xt);
-      }
-      if (c != base) {
-        store_xin8(sm, tid, c - 8 + col_off, oo, xscale);
-        store_xin8(sm, tid ^ 1, c - 8 + col_off, ot, xscale);
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        oo[j] = no[j];
-        ot[j] = nt[j];
-      }
-      if (c + 8 < base + kC) tc::tmem_ld8x2(tS + c + 8, tS + c + 8 + kC, sa, sb);
-    }
-    if (wait_g2) {
-      if (!warp_wait_phase(&bars[kBarG2], g2_parity, abort)) return false;
-      wait_g2 = false;
-    }
-    store_xin8(sm, tid, base + kC - 8 + col_off, oo, xscale);
-    store_xin8(sm, tid ^ 1, base + kC - 8 + col_off, ot, xscale);
+// main warps, chain of tile k. Thread r owns TMEM lane r = state row r (lane quarter warp & 3)
+// and runs the complex recurrence of its state pair (the other component of S comes from the
+// partner lane r ^ 1; both threads of a pair run the same recurrence and each writes its own
+// Xin K-row). Half h writes the Xin columns 64h .. 64h + 63. When the rows start at both
+// halves (C divides 64) each half runs only its own columns; otherwise half 1 starts at the
+// last row start at or before column 64 (its earlier columns are recomputed, not stored) and
+// in long-row mode both halves run all 128 columns, so both carry the state into the next
+// tile. Row mode resets the state at every row start (multiples of C) and re-anchors every 32
+// chunks from it; long rows re-anchor every 32 chunks from the tile start. kStep: row starts
+// checked at every column (C not a multiple of 16); otherwise only where a piece of 16 columns
+// begins. S is read one piece ahead. The Xin buffer is free: the outputs of the previous tile,
+// taken earlier in the same iteration, waited for its GEMM2.
+template <bool kStep>
+__device__ __forceinline__ void chain_run(const TcScanArgs& a, uint8_t* sm, uint32_t tS, int r,
+                                          const ChainConst& q, float xscale, int c_begin,
+                                          int c_store, int c_end, float& xo, float& xt,
+                                          float& ao, float& at) {
+  const int c_store_end = c_store + 64;
+  int next_reset, next_anchor;
+  if (a.R > 0) {
+    next_reset = ((c_begin + a.C - 1) / a.C) * a.C;  // the first row start at or after c_begin
+    next_anchor = next_reset;
+  } else {
+    next_reset = 1 << 30;
+    next_anchor = 0;
   }
-  return true;
-}
-
-// Any other row length, and rows longer than a tile (the state carried in xo, xt, ao, at):
-// both threads of a state pair run the recurrence over all 128 columns, the other component
-// of S from the partner lane, and each writes its own Xin K-row. Row mode resets the state at
-// every row start; anchors fall every 32 chunks from the row start (from the tile start for
-// long rows, where the anchor of a new row is zero).
-__device__ __forceinline__ bool chain_generic(const TcScanArgs& a, uint8_t* sm, uint32_t tS,
-                                              const ChainConst& q, float xscale, float& xo,
-                                              float& xt, float& ao, float& at, bool wait_g2,
-                                              uint32_t g2_parity, volatile int* abort) {
-  const int tid = threadIdx.x;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-  const int C = a.C;
-  int next_reset = (a.R > 0) ? 0 : (1 << 30);
-  int next_anchor = 0;
+  uint32_t cur[16], nxt[16];
+  tc::tmem_ld16_issue(tS + c_begin, cur);
+  tc::tmem_wait_ld16(cur);
 #pragma unroll 1
-  for (int c = 0; c < kCols; c += 16) {
-    float sv[16];
-    tc::tmem_ld16(tS + c, sv);
-    float oo[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int g = c + j;
-      const float oth = __shfl_xor_sync(0xffffffffu, sv[j], 1);
-      if (g == next_anchor) {
+  for (int c = c_begin; c < c_end; c += 16) {
+    const bool more = c + 16 < c_end;
+    if (more) tc::tmem_ld16_issue(tS + c + 16, nxt);
+    if (!kStep) {
+      if (c == next_anchor) {
         chain_anchor(q, xo, xt, ao, at);
         next_anchor += 32;
       }
-      if (g == next_reset) {
+      if (c == next_reset) {
         xo = xt = ao = at = 0.f;
-        next_reset += C;
-        next_anchor = g + 32;
+        next_reset += a.C;
+        next_anchor = c + 32;
+      }
+    }
+    // the partner's components of the whole piece first: the exchanges do not depend on the
+    // recurrence, so their latency overlaps instead of adding to every step
+    float oth[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) oth[j] = __shfl_xor_sync(0xffffffffu, __uint_as_float(cur[j]), 1);
+    float oo[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float own = __uint_as_float(cur[j]);
+      if (kStep) {
+        const int g = c + j;
+        if (g == next_anchor) {
+          chain_anchor(q, xo, xt, ao, at);
+          next_anchor += 32;
+        }
+        if (g == next_reset) {
+          xo = xt = ao = at = 0.f;
+          next_reset += a.C;
+          next_anchor = g + 32;
+        }
       }
       oo[j] = xo;
-      chain_step(q, sv[j], oth, xo, xt);
+      chain_step(q, own, oth[j], xo, xt);
     }
-    if (wait_g2) {
-      if (!warp_wait_phase(&bars[kBarG2], g2_parity, abort)) return false;
-      wait_g2 = false;
+    if (c >= c_store && c < c_store_end) {
+      store_xin8(sm, r, c, oo, xscale);
+      store_xin8(sm, r, c + 8, oo + 8, xscale);
     }
-    store_xin8(sm, tid, c, oo, xscale);
-    store_xin8(sm, tid, c + 8, oo + 8, xscale);
+    if (more) {
+      tc::tmem_wait_ld16(nxt);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) cur[j] = nxt[j];
+    }
   }
-  return true;
 }
 
-// scan warps, one tile (thread r = TMEM lane r = state row r): the Xin scale of every chunk
-// column, then the carries along the chunks of S written as the Xin operand.
-__device__ __forceinline__ bool scan_tile(const TcScanArgs& a, uint8_t* sm, uint32_t tmem,
-                                          int k, bool new_row, const ChainConst& q, float sig_g,
-                                          float& xo, float& xt, float& ao, float& at,
-                                          int& es_prev, volatile int* abort) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int par = k & 1;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-  const int* sRowEs = reinterpret_cast<const int*>(sm + kRowEs) + par * 128;
-  float* sBy = reinterpret_cast<float*>(sm + kBy) + par * 128;
-  unsigned* sRed = reinterpret_cast<unsigned*>(sm + kScanRed);
-  const uint32_t tS = tmem + (uint32_t(warp * 32) << 16) + kTS + uint32_t(par) * 128;
+// The same for a half of the tile that is 64 columns from a row start with rows of C in
+// {16, 32, 64} chunks (row starts and anchors at multiples of 16 columns): the whole half in
+// registers, fully unrolled, so the conversion and stores of the first columns overlap the
+// recurrence of the later ones.
+__device__ __forceinline__ void chain64(uint8_t* sm, uint32_t tS, int r, int C,
+                                        const ChainConst& q, float xscale, int c0) {
+  uint32_t s0[16], s1[16], s2[16], s3[16];
+  tc::tmem_ld16_issue(tS + c0, s0);
+  tc::tmem_ld16_issue(tS + c0 + 16, s1);
+  tc::tmem_ld16_issue(tS + c0 + 32, s2);
+  tc::tmem_ld16_issue(tS + c0 + 48, s3);
+  tc::tmem_wait_ld16(s0);
+  tc::tmem_wait_ld16(s1);
+  tc::tmem_wait_ld16(s2);
+  tc::tmem_wait_ld16(s3);
+  float xo = 0.f, xt = 0.f, ao = 0.f, at = 0.f;
+  float out[64];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const uint32_t* sp = p == 0 ? s0 : p == 1 ? s1 : p == 2 ? s2 : s3;
+    float oth[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) oth[j] = __shfl_xor_sync(0xffffffffu, __uint_as_float(sp[j]), 1);
+    const int cr = (16 * p) & (C - 1);  // column within the row
+    if (p > 0 && cr == 0) xo = xt = ao = at = 0.f;
+    if (cr == 32) chain_anchor(q, xo, xt, ao, at);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      out[16 * p + j] = xo;
+      chain_step(q, __uint_as_float(sp[j]), oth[j], xo, xt);
+    }
+  }
+#pragma unroll
+  for (int g8 = 0; g8 < 8; ++g8) store_xin8(sm, r, c0 + 8 * g8, out + 8 * g8, xscale);
+}
 
-  // S of this tile and the u scales of its rows
-  bool ok = warp_wait_phase(&bars[kBarG1 + par], (k >> 1) & 1, abort) &&
-            warp_wait_phase(&bars[kBarUFull + par], (k >> 1) & 1, abort);
-  if (!named_bar_and(kScanBar, 128, ok)) return false;
+__device__ __forceinline__ bool chain_tile(const TcScanArgs& a, uint8_t* sm, uint32_t tmem,
+                                           int k, bool new_row, const ChainConst& q,
+                                           float sig_g, float& xo, float& xt, float& ao,
+                                           float& at, int& es_prev, volatile int* abort) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = warp >> 2, quarter = warp & 3, r = quarter * 32 + lane;
+  const int par = k & 1, slot = k & 3;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  const int* sRowEs = reinterpret_cast<const int*>(sm + kRowEs) + slot * 128;
+  unsigned* sRed = reinterpret_cast<unsigned*>(sm + kScanRed);
+  const uint32_t tS = tmem + (uint32_t(quarter * 32) << 16) + kTS + uint32_t(par) * 128;
+
+  // S of this tile
+  const bool ok = warp_wait_phase(&bars[kBarG1 + par], (k >> 1) & 1, abort);
+  if (!named_bar_and(kMainBar, 256, ok)) return false;
   tc::fence_after_sync();
-  if (tid == 0) SCAN_TRACE(k * 8 + 0);
+  if (threadIdx.x == 0) SCAN_TRACE(k * 8 + 0);
+#ifdef DLR_SCAN_TRACE
+  if (threadIdx.x == 0 && blockIdx.x == 0 && k < 8) g_scan_trace[3800 + 2 * k] = clock64();
+#endif
 
   int xs = kXinShift;
   if (a.R == 0) {
     // one row walked tile by tile: the carried state and anchor move from the previous tile's
     // S units to this tile's (times 2^(es - es_prev), in two exact steps); the Xin scale makes
-    // room for the carried state's magnitude
+    // room for the carried state's magnitude (both halves carry the same state)
     const int es = sRowEs[0];
     if (new_row) {
       xo = xt = ao = at = 0.f;
@@ -1127,42 +1143,108 @@ __device__ __forceinline__ bool scan_tile(const TcScanArgs& a, uint8_t* sm, uint
     }
     es_prev = es;
     const unsigned mw = __reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(fabsf(xo), fabsf(xt))));
-    if (lane == 0) sRed[warp] = mw;
-    named_bar(kScanBar, 128);
+    if (lane == 0 && h == 0) sRed[quarter] = mw;
+    named_bar(kMainBar, 256);
     const unsigned m = max(max(sRed[0], sRed[1]), max(sRed[2], sRed[3]));
     const int e = int((m >> 23) & 0xFFu) - 126;  // carried |state| < 2^e
     xs += max(0, e - 41);
   } else {
     xo = xt = ao = at = 0.f;
   }
-  {
+  if (h == 0) {
     // y = Y2 * 2^(xs - 14 - es) / sig_g for the column's row
-    const int row = (a.R > 0) ? tid / a.C : 0;
-    sBy[tid] = exp2i(xs - kXinShift) * exp2i(kXinShift - 14 - sRowEs[row]) / sig_g;
+    const int row = (a.R > 0) ? r / a.C : 0;
+    reinterpret_cast<float*>(sm + kBy)[slot * 128 + r] =
+        exp2i(xs - kXinShift) * exp2i(kXinShift - 14 - sRowEs[row]) / sig_g;
   }
-  tc::mbar_arrive(&bars[kBarScanStart + par]);
-
   const float xscale = exp2i(-xs);
-  const bool wait_g2 = k > 0;
-  const uint32_t g2_parity = uint32_t(k - 1) & 1u;
-  if (a.R > 0 && a.C == 64)
-    ok = chain_pairs<64>(sm, tS, q, xscale, wait_g2, g2_parity, abort);
-  else if (a.R > 0 && a.C == 32)
-    ok = chain_pairs<32>(sm, tS, q, xscale, wait_g2, g2_parity, abort);
-  else if (a.R > 0 && a.C == 16)
-    ok = chain_pairs<16>(sm, tS, q, xscale, wait_g2, g2_parity, abort);
+  int c_begin, c_end;
+  if (a.R > 0 && (64 % a.C) == 0) {
+    c_begin = 64 * h;
+    c_end = 64 * h + 64;
+  } else if (a.R > 0) {
+    c_begin = h ? ((64 / a.C) * a.C) & ~15 : 0;
+    c_end = 64 * h + 64;
+  } else {
+    c_begin = 0;
+    c_end = kCols;
+  }
+  if (a.R > 0 && (a.C == 16 || a.C == 32 || a.C == 64))
+    chain64(sm, tS, r, a.C, q, xscale, 64 * h);
+  else if (a.R > 0 && (a.C & 15) != 0)
+    chain_run<true>(a, sm, tS, r, q, xscale, c_begin, 64 * h, c_end, xo, xt, ao, at);
   else
-    ok = chain_generic(a, sm, tS, q, xscale, xo, xt, ao, at, wait_g2, g2_parity, abort);
-  if (!ok) return false;
-  if (tid == 0) SCAN_TRACE(k * 8 + 3);
+    chain_run<false>(a, sm, tS, r, q, xscale, c_begin, 64 * h, c_end, xo, xt, ao, at);
+  if (threadIdx.x == 0) SCAN_TRACE(k * 8 + 3);
+#ifdef DLR_SCAN_TRACE
+  if (threadIdx.x == 0 && blockIdx.x == 0 && k < 8) g_scan_trace[3801 + 2 * k] = clock64();
+#endif
   tc::fence_proxy_async_smem();
   tc::fence_before_sync();
   tc::mbar_arrive(&bars[kBarXFull]);
   return true;
 }
 
+// The main warps (0-7) over all tiles of the CTA. Iteration k: the u operand of tile k+1, the
+// outputs of tile k-1 (once its GEMM2 is done), the chain of tile k. The scale slots are rings
+// of four tiles, so tile k+1's u scales never overwrite those tile k-1's outputs still read.
+// Every wait is taken by all 256 threads together (named_bar_and), so a wait that gives up
+// makes all of them leave at the same point.
 template <bool kRev>
-__global__ void __maxnreg__(128)
+__device__ __forceinline__ void main_role(const TcScanArgs& a, const CUtensorMap* ymap,
+                                          uint8_t* sm, uint32_t tmem, int u0, int segs,
+                                          int ntiles, volatile int* abort) {
+  const int r = ((threadIdx.x >> 5) & 3) * 32 + (threadIdx.x & 31);  // lane = chunk or row
+  const int2 rc = col_rows(a, r);
+  int conv_h = -1;
+  float sig_k = 1.f;
+  ChainConst q{0.f, 0.f, 0.f, 0.f};
+  float sig_g = 1.f;
+  float xo = 0.f, xt = 0.f, ao = 0.f, at = 0.f;
+  int es_prev = 0;
+  int chain_h = -1;
+  if (ntiles == 0) return;
+  TileIter it_conv = tile_iter_begin(a, u0), it_epi = it_conv, it_chain = it_conv;
+  if (!conv_tile<kRev>(a, sm, tmem, it_conv.t, rc, 0, conv_h, sig_k, abort)) return;
+  tile_iter_next(a, segs, it_conv);
+  bool ok = true;
+  for (int k = 0; k < ntiles && ok; ++k) {
+    named_bar(kMainBar, 256);  // the previous stages' shared-memory writes are visible
+    if (k + 1 < ntiles) {
+      ok = conv_tile<kRev>(a, sm, tmem, it_conv.t, rc, k + 1, conv_h, sig_k, abort);
+      tile_iter_next(a, segs, it_conv);
+    }
+    if (ok && k >= 1) {
+      ok = epi_tile<kRev>(a, ymap, sm, tmem, it_epi.t, rc, k - 1, abort);
+      tile_iter_next(a, segs, it_epi);
+    }
+    if (!ok) break;
+    const TileInfo& ti = it_chain.t;
+    if (ti.h != chain_h) {
+      // this thread's lambda^64 and re-anchoring correction; the G scale of the channel. The
+      // state recurrence keeps (own, other) components; the Im row runs it with the sign of the
+      // imaginary parts flipped.
+      chain_h = ti.h;
+      const uint8_t* blob = a.tables + (size_t)ti.h * kBlobBytes;
+      const float4 m = __ldg(reinterpret_cast<const float4*>(blob + kBlobMu) + (r >> 1));
+      q.mu_re = m.x;
+      q.dl_re = m.z;
+      q.mu_im = (r & 1) ? -m.y : m.y;
+      q.dl_im = (r & 1) ? -m.w : m.w;
+      sig_g = __ldg(reinterpret_cast<const float*>(blob + kBlobSig) + 1);
+    }
+    ok = chain_tile(a, sm, tmem, k, ti.seg == 0, q, sig_g, xo, xt, ao, at, es_prev, abort);
+    tile_iter_next(a, segs, it_chain);
+  }
+  if (ok) {
+    named_bar(kMainBar, 256);
+    epi_tile<kRev>(a, ymap, sm, tmem, it_epi.t, rc, ntiles - 1, abort);
+  }
+  if (a.tma && (threadIdx.x & 31) == 0) tc::bulk_wait_group0();  // y stores done
+}
+
+template <bool kRev>
+__global__ void __launch_bounds__(kThreads, 1)
     dlr_scan_tc_kernel(const TcScanArgs a, const __grid_constant__ CUtensorMap umap,
                        const __grid_constant__ CUtensorMap ymap) {
   extern __shared__ uint8_t smem_raw[];
@@ -1179,14 +1261,13 @@ __global__ void __maxnreg__(128)
     tc::mbar_init(&bars[kBarTabTk], 1);
     tc::mbar_init(&bars[kBarTabG], 1);
     tc::mbar_init(&bars[kBarG2], 1);
-    tc::mbar_init(&bars[kBarXFull], 128);
-    tc::mbar_init(&bars[kBarY2Free], 128);
+    tc::mbar_init(&bars[kBarXFull], 256);
+    tc::mbar_init(&bars[kBarY2Free], 256);
     for (int p = 0; p < 2; ++p) {
       tc::mbar_init(&bars[kBarStage + p], 1);
-      tc::mbar_init(&bars[kBarUFull + p], 128);
+      tc::mbar_init(&bars[kBarUFull + p], 256);
       tc::mbar_init(&bars[kBarG1 + p], 1);
-      tc::mbar_init(&bars[kBarScanStart + p], 128);
-      tc::mbar_init(&bars[kBarY1Free + p], 128);
+      tc::mbar_init(&bars[kBarY1Free + p], 256);
     }
     *abort = 0;
     tc::mbar_fence_init();
@@ -1208,37 +1289,9 @@ __global__ void __maxnreg__(128)
 
   // everything below the producer's first u copies reads the tables or data derived from them
   if (warp != 13) grid_wait_prerequisites();
-  if (warp < 4) {
-    ChainConst q{0.f, 0.f, 0.f, 0.f};
-    float sig_g = 1.f;
-    float xo = 0.f, xt = 0.f, ao = 0.f, at = 0.f;
-    int es_prev = 0;
-    int cur_h = -1;
-    for (int k = 0; k < ntiles; ++k) {
-      const TileInfo ti = tile_info(a, u0, segs, k);
-      if (ti.h != cur_h) {
-        // this thread's lambda^64 and re-anchoring correction; the G scale of the channel.
-        // The state recurrence keeps (own, other) components; the Im row runs it with the
-        // sign of the imaginary parts flipped.
-        cur_h = ti.h;
-        const uint8_t* blob = a.tables + (size_t)ti.h * kBlobBytes;
-        const float4 m = __ldg(reinterpret_cast<const float4*>(blob + kBlobMu) + (tid >> 1));
-        q.mu_re = m.x;
-        q.dl_re = m.z;
-        q.mu_im = (tid & 1) ? -m.y : m.y;
-        q.dl_im = (tid & 1) ? -m.w : m.w;
-        sig_g = __ldg(reinterpret_cast<const float*>(blob + kBlobSig) + 1);
-      }
-      if (!scan_tile(a, sm, tmem, k, ti.seg == 0, q, sig_g, xo, xt, ao, at, es_prev, abort))
-        break;
-    }
-  } else if (warp < 8) {
-    conv_role<kRev>(a, sm, tmem, u0, segs, ntiles, abort);
-  } else if (warp < 12) {
-    for (int k = 0; k < ntiles; ++k)
-      if (!store_tile<kRev>(a, &ymap, sm, tmem, u0, segs, k, abort)) break;
-    if (a.tma && (tid & 31) == 0) tc::bulk_wait_group0();  // y stores done, staging unused
-  } else if (warp == 12) {
+  if (warp < 8) {
+    main_role<kRev>(a, &ymap, sm, tmem, u0, segs, ntiles, abort);
+  } else if (warp == 8) {
     if ((tid & 31) == 0) mma_role(a, sm, tmem, u0, segs, ntiles, abort);
   } else if ((tid & 31) == 0) {
     producer_role<kRev>(a, &umap, sm, u0, segs, ntiles, abort);
