@@ -408,8 +408,8 @@ __device__ __forceinline__ void store_part(float* __restrict__ row, int L, int k
 // correction lambda^2048 - (lambda^64)^32 of every state, the scales of K and G. The blob is
 // assembled in shared memory and leaves in bulk copies.
 // Thread (n, q) = (tid & 63, tid >> 6) owns state n and exponents j = 8q .. 8q + 8, held in
-// registers: lambda^{8q + 4c} (c <= 2) and lambda^d (d < 4) evaluated directly, the others as
-// one product of two of them; warps 14 and 15 (q = 7) also form the re-anchoring correction.
+// registers (lambda and lambda^{8q} evaluated directly, the rest by short products); warps 14
+// and 15 (q = 7) also form the re-anchoring correction.
 __global__ void __launch_bounds__(kTbThreads, 2)
     dlr_scan_tc_tables(const TcScanArgs a, uint8_t* ws) {
   extern __shared__ __align__(1024) uint8_t tsm[];
@@ -430,17 +430,29 @@ __global__ void __launch_bounds__(kTbThreads, 2)
   const float sig_g = exp2i(scale_exp(block_max_tb(fmaxf(fabsf(w.x), fabsf(w.y)), sRed, 0)));
   if (tid == 0) SCAN_TRACE(3901);
 
-  // pw[i] = lambda^{8q + i}, i = 0..8
+  // pw[i] = lambda^{8q + i}, i = 0..8: lambda and lambda^{8q} evaluated directly, lambda^i
+  // (i <= 8) by products of depth at most three, then one product with lambda^{8q}; each power
+  // carries at most a few roundings, never a chain that grows with the exponent. The table
+  // entries enter y once each, so a few roundings stay far below the tolerance.
   cf pw[9];
   {
-    cf base[3], small[4];
+    cf sm_[9];
+    sm_[0] = cf{1.f, 0.f};
+    sm_[1] = on ? lam_pow(p, 1) : cf{0.f, 0.f};
+    sm_[2] = cmul(sm_[1], sm_[1]);
+    sm_[3] = cmul(sm_[2], sm_[1]);
+    sm_[4] = cmul(sm_[2], sm_[2]);
+    sm_[5] = cmul(sm_[4], sm_[1]);
+    sm_[6] = cmul(sm_[4], sm_[2]);
+    sm_[7] = cmul(sm_[4], sm_[3]);
+    sm_[8] = cmul(sm_[4], sm_[4]);
+    const cf base = on ? lam_pow(p, 8 * q) : cf{0.f, 0.f};
+    pw[0] = base;
 #pragma unroll
-    for (int c = 0; c < 3; ++c) base[c] = on ? lam_pow(p, 8 * q + 4 * c) : cf{0.f, 0.f};
-    small[0] = cf{1.f, 0.f};
-#pragma unroll
-    for (int d = 1; d < 4; ++d) small[d] = on ? lam_pow(p, d) : cf{0.f, 0.f};
-#pragma unroll
-    for (int i = 0; i < 9; ++i) pw[i] = (i & 3) ? cmul(base[i >> 2], small[i & 3]) : base[i >> 2];
+    for (int i = 1; i < 9; ++i) pw[i] = (q == 0) ? sm_[i] : cmul(base, sm_[i]);
+    // lambda^64 = mu, whose rounding the chunk recurrence compounds between re-anchors:
+    // evaluated directly
+    if (q == 7 && on) pw[8] = lam_pow(p, 64);
   }
   // Q rows 2n (Re) and 2n+1 (Im) at steps t = 63 - j, j in [8q, 8q + 8): TMEM words (lower step
   // in the low half) 28 - 4q .. 31 - 4q of each row
@@ -731,8 +743,11 @@ __device__ __forceinline__ void producer_role(const TcScanArgs& a, const CUtenso
                   kGLo + 16384 - kGHi, &bars[kBarTabG]);
   };
   if (a.tma) {
+    SCAN_TRACE(1100);
     issue_u_tma<kRev>(a, map, sm, u0, segs, 0);
+    SCAN_TRACE(1101);
     if (ntiles > 1) issue_u_tma<kRev>(a, map, sm, u0, segs, 1);
+    SCAN_TRACE(1102);
   }
   grid_wait_prerequisites();  // the tables are written
   int h = channel(0);
@@ -1288,7 +1303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles = (u1 - u0) * segs;
 
   // everything below the producer's first u copies reads the tables or data derived from them
-  if (warp != 13) grid_wait_prerequisites();
+  if (warp != 9) grid_wait_prerequisites();
   if (warp < 8) {
     main_role<kRev>(a, &ymap, sm, tmem, u0, segs, ntiles, abort);
   } else if (warp == 8) {
