@@ -240,6 +240,36 @@ def dlr_layer_backward(u, g, fwd, bwd=None, cast: str = "re"):
     return np.ascontiguousarray(du), grads
 
 
+def dlr_spectrum(log_re, log_im, W, L: int, M: int, bwd=None) -> np.ndarray:
+    """Spectrum of the length-M circulant column of the Re-cast DLR kernel, bins k = 0..M/2,
+    evaluated directly from the parameters ("The Annotated S4", part 2: the kernel's truncated
+    generating function evaluated at the roots of unity instead of the kernel itself; for a
+    diagonal state matrix it is a sum of geometric series). With omega = exp(-2 pi i / M) and
+    A(k) = sum_n W_n G(lambda_n omega^k), G(z) = sum_{j<L} z^j = (1 - z^L) / (1 - z):
+      causal column [K_0 .. K_{L-1}, 0 ..]:       C_k = (A(k) + conj(A(-k))) / 2
+      with bwd, the anti-causal column K2_j at M - j (j >= 1) and K2_0 added at 0 (the
+      bidirectional DLR of section 2.1 as one circulant): + (A2(-k) + conj(A2(k))) / 2.
+    G is formed as expm1(L log z) / expm1(log z) with log z = -a^2 + i(theta - 2 pi k / M)
+    (complex128), and as L where log z = 0. Returns complex128 [H, M/2 + 1]."""
+    def A(lr, li, w, sign):
+        lr, li, w = _f32(lr), _f32(li), _f32(w)
+        a = lr.astype(np.float64)
+        th = li.astype(np.float64)
+        wc = w[..., 0].astype(np.float64) + 1j * w[..., 1].astype(np.float64)   # [H, N]
+        k = np.arange(M // 2 + 1, dtype=np.float64)
+        ell = (-a * a)[..., None] + 1j * (th[..., None] - sign * 2.0 * np.pi * k / M)
+        ell = ell.real + 1j * (np.mod(ell.imag + np.pi, 2.0 * np.pi) - np.pi)     # [H, N, K]
+        num = np.expm1(L * ell)
+        den = np.expm1(ell)
+        zero = np.abs(ell) == 0.0
+        G = np.where(zero, float(L), num / np.where(zero, 1.0, den))
+        return np.einsum("hn,hnk->hk", wc, G)
+    C = 0.5 * (A(log_re, log_im, W, +1) + np.conj(A(log_re, log_im, W, -1)))
+    if bwd is not None:
+        C = C + 0.5 * (A(*bwd, -1) + np.conj(A(*bwd, +1)))
+    return C
+
+
 # ------------------------------------------------------------------------------------------
 # S5 ("Simplified State Space Layers for Sequence Modeling")
 

@@ -603,3 +603,58 @@ def test_oracle_lambda_magnitude_spans_the_init_range():
     ends = np.abs(oracle.dlr_lambda(a, np.zeros_like(a)))[0]
     np.testing.assert_allclose(ends, np.exp(-a[0].astype(np.float64) ** 2), rtol=1e-15)
     np.testing.assert_allclose(ends, [lo, hi], rtol=1e-7)
+
+
+# ---------------------------------------------------------------------------------------
+# Direct spectrum (The Annotated S4, part 2: the truncated generating function at the roots
+# of unity)
+
+@pytest.mark.parametrize("bidir", [False, True])
+def test_direct_spectrum_equals_fft_of_the_circulant_column(bidir):
+    """The spectrum from the geometric series equals numpy's real FFT of the circulant column
+    built from the oracle's kernel (section 2.1 of the DLR paper: K zero-padded to 2L, the
+    anti-causal kernel wrapped to the end, lag 0 counted by both). Channels on the unit circle
+    (log_re = 0 with theta = 2 pi n / N) put some bins exactly on a pole of the series."""
+    H, N, L, M = 3, 16, 100, 256
+    rng = np.random.default_rng(31)
+    f = inputs.dlr_params(rng, H, N, unit_channels=1)
+    b = inputs.dlr_params(rng, H, N, unit_channels=1) if bidir else None
+    fwd = (f.log_re, f.log_im, f.W)
+    bwd = (b.log_re, b.log_im, b.W) if bidir else None
+    C = oracle.dlr_spectrum(*fwd, L, M, bwd=bwd)
+    col = np.zeros((H, M))
+    col[:, :L] = oracle.dlr_kernel(*fwd, L, cast="re")
+    if bidir:
+        k2 = oracle.dlr_kernel(*bwd, L, cast="re")
+        col[:, 0] += k2[:, 0]
+        col[:, M - L + 1:] += k2[:, 1:][:, ::-1]
+    ref = np.fft.rfft(col, axis=-1)
+    scale = np.max(np.abs(ref))
+    np.testing.assert_allclose(C, ref, rtol=0, atol=1e-10 * scale)
+
+
+def test_direct_spectrum_single_state_geometric_sum():
+    """One state with W = 1 and lambda = exp(-a^2 + i theta): C_k is the real part's DFT,
+    (G(lambda w^k) + conj(G(lambda w^-k))) / 2, and G is checked against the explicit sum of
+    L powers in float64; at a = 0, theta = 2 pi m / M the bin k = m holds the pole value L."""
+    L, M = 50, 128
+    for a, th in [(0.3, 0.7), (0.0, 2 * np.pi * 5 / M), (0.05, -1.1)]:
+        lr = np.array([[a]], np.float32)
+        li = np.array([[th]], np.float32)
+        W = np.array([[[1.0, 0.0]]], np.float32)
+        C = oracle.dlr_spectrum(lr, li, W, L, M)[0]
+        lam = np.exp(-np.float64(lr[0, 0]) ** 2 + 1j * np.float64(li[0, 0]))
+        j = np.arange(L)
+        k = np.arange(M // 2 + 1)
+        w = np.exp(-2j * np.pi * k / M)
+        Gp = np.array([np.sum((lam * wk) ** j) for wk in w])
+        Gm = np.array([np.sum((lam / wk) ** j) for wk in w])
+        np.testing.assert_allclose(C, 0.5 * (Gp + np.conj(Gm)), rtol=1e-9, atol=1e-9)
+    # the pole: with a = 0 and theta = 2 pi 5 / M (up to its float32 rounding) the causal
+    # series at bin 5 is L: 2 C_5 - conj(G(lambda w^-5)) = G(lambda w^5) ~ L
+    lr = np.zeros((1, 1), np.float32)
+    li = np.array([[2 * np.pi * 5 / M]], np.float32)
+    C = oracle.dlr_spectrum(lr, li, np.array([[[1.0, 0.0]]], np.float32), L, M)[0]
+    lam = np.exp(1j * np.float64(li[0, 0]))
+    Gm5 = np.sum((lam * np.exp(2j * np.pi * 5 / M)) ** np.arange(L))
+    assert abs(2 * C[5] - np.conj(Gm5) - L) < 1e-4 * L
