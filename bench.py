@@ -411,6 +411,17 @@ def run_extras(torch, dlr, inputs, flush, sm_mhz, sm_count):
         "conv_apply_us": ms_apply * 1e3,
         "conv_apply_tflops": apply_flops / ms_apply / 1e9,
         "conv_apply_frac_of_fp32_peak": apply_flops / ms_apply / 1e9 / peak_tflops}
+    # the same layer with the spectra evaluated straight from the parameters
+    # (dlr_conv_spectrum_direct + dlr_conv_apply: no kernel, no spectrum FFT)
+    def direct_step():
+        dlr.dlr_conv_spectrum_direct(fwd, None, L=L, workspace=wsf)
+        dlr.dlr_conv_apply(u, wsf, out=y)
+
+    ms_d = _time_steps(torch, direct_step, 10, 2, flush)
+    ms_s = _time_steps(torch, lambda: dlr.dlr_conv_spectrum_direct(fwd, None, L=L, workspace=wsf),
+                       10, 2, flush)
+    out["fft_direct_spectrum_" + WORKLOAD] = {
+        "ms": ms_d, "elements_per_s": B * H * L / ms_d * 1e3, "spectrum_ms": ms_s}
     del K, wsf
     ms = _time_steps(torch, lambda: dlr.dlr_scan(u, fwd, out=y, algo="fp32"), 20, 3, flush)
     out["scan_fp32_" + WORKLOAD] = {"ms": ms, "elements_per_s": B * H * L / ms * 1e3}
@@ -453,6 +464,10 @@ def run_extras(torch, dlr, inputs, flush, sm_mhz, sm_count):
     ms = _time_steps(torch, lambda: dlr.dlr_layer(u, fwd, path="fft", workspace=ws, out=y), 10,
                      2, flush)
     out["fft_cluster_" + w.name] = {"ms": ms, "elements_per_s": w.B * w.H * w.L / ms * 1e3}
+    ms = _time_steps(torch, lambda: (dlr.dlr_conv_spectrum_direct(fwd, None, L=w.L, workspace=ws),
+                                     dlr.dlr_conv_apply(u, ws, out=y)), 5, 2, flush)
+    out["fft_cluster_direct_spectrum_" + w.name] = {
+        "ms": ms, "elements_per_s": w.B * w.H * w.L / ms * 1e3}
     del u, y, ws
 
     w = inputs.make_workload("s5_b8_l16384_h512_p256")

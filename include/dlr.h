@@ -101,6 +101,31 @@ dlr_status dlr_conv_spectrum(const float* K_fwd, const float* K_bwd, dlr_dir dir
                              dlr_stream_t stream);
 
 /*
+ * dlr_conv_spectrum_direct -- the spectra that dlr_conv_spectrum would compute from the Re-cast
+ * kernel, evaluated straight from the parameters instead ("The Annotated S4", part 2: the
+ * truncated generating function of the kernel at the roots of unity; for the diagonal DLR of
+ * "Simplifying and Understanding State Space Models with Diagonal Linear RNNs", section 2, a
+ * sum of N geometric series per frequency: C_k = (A(k) + conj(A(-k))) / 2 with
+ * A(k) = sum_n W_n (1 - (lambda_n w^k)^L) / (1 - lambda_n w^k), w = exp(-2 pi i / M)), so the
+ * layer by FFT needs neither the kernel K nor its transform: dlr_conv_spectrum_direct followed
+ * by dlr_conv_apply gives the same y as dlr_kernel + dlr_conv. With dir = DLR_BIDIR the second
+ * parameter set forms the anti-causal column (section 2.1), lag 0 counted by both directions.
+ *  - log_re, log_im [H, N], W [H, N, 2] (8-byte aligned): device pointers as in dlr_kernel;
+ *    the second set NULL when dir = DLR_CAUSAL.
+ *  - workspace: dlr_conv_workspace_size(H, L, dir) bytes, written (twiddle tables and spectra)
+ *    in the layout dlr_conv_apply reads.
+ *  - Re cast only (DLR-prod has no N-term generating function); N <= 256, L <= 65536, else
+ *    DLR_ERR_UNSUPPORTED.
+ *  - Cost O(N L) complex divisions per channel: for the workloads measured here it is slower
+ *    than dlr_kernel + dlr_conv_spectrum; it needs no [H, L] kernel buffer.
+ */
+dlr_status dlr_conv_spectrum_direct(const float* log_re, const float* log_im, const float* W,
+                                    const float* log_re2, const float* log_im2,
+                                    const float* W2, dlr_dir dir, int64_t H, int64_t N,
+                                    int64_t L, void* workspace, size_t workspace_bytes,
+                                    dlr_stream_t stream);
+
+/*
  * dlr_conv_apply -- second half of dlr_conv: y = FFT convolution of u with the spectra that
  * a preceding dlr_conv_spectrum (same H and L, earlier in stream order) left in `workspace`.
  * Reads the workspace only; one kernel launch, one CTA per (b, h) row.

@@ -33,6 +33,9 @@ cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delt
                       const float* Bt, const float* Ct, const float* D, int B, int L, int H, int P,
                       bool bf16, float* y, void* ws, int* status, cudaStream_t s);
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
+cudaError_t launch_spectrum_direct(const float* lr1, const float* li1, const float* W1,
+                                   const float* lr2, const float* li2, const float* W2, int H,
+                                   int N, int L, void* ws, cudaStream_t s);
 size_t step_workspace_bytes(int64_t H, int64_t N);
 cudaError_t launch_step_tables(const float* lr, const float* li, const float* W, int64_t H,
                                int64_t N, void* ws, cudaStream_t s);
@@ -112,7 +115,7 @@ dlr_status check_params(const float* log_re, const float* log_im, const float* W
 
 extern "C" {
 
-int dlr_abi_version(void) { return 6; }
+int dlr_abi_version(void) { return 7; }
 
 const char* dlr_last_cuda_error(void) { return t_last_cuda_error_msg; }
 
@@ -168,6 +171,27 @@ dlr_status dlr_conv_spectrum(const float* K_fwd, const float* K_bwd, dlr_dir dir
   return from_cuda(dlr::launch_dlr_conv_spectrum(K_fwd, dir == DLR_BIDIR ? K_bwd : nullptr,
                                                  (int)H, (int)L, workspace,
                                                  (cudaStream_t)stream));
+}
+
+dlr_status dlr_conv_spectrum_direct(const float* log_re, const float* log_im, const float* W,
+                                    const float* log_re2, const float* log_im2,
+                                    const float* W2, dlr_dir dir, int64_t H, int64_t N,
+                                    int64_t L, void* workspace, size_t workspace_bytes,
+                                    dlr_stream_t stream) {
+  if (H < 1 || N < 1 || L < 1) return DLR_ERR_INVALID_ARG;
+  if (dir != DLR_CAUSAL && dir != DLR_BIDIR) return DLR_ERR_INVALID_ARG;
+  auto al8 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; };
+  if (!log_re || !log_im || !W || !al8(W)) return DLR_ERR_INVALID_ARG;
+  const bool two = dir == DLR_BIDIR;
+  if (two && (!log_re2 || !log_im2 || !W2 || !al8(W2))) return DLR_ERR_INVALID_ARG;
+  if (!two && (log_re2 || log_im2 || W2)) return DLR_ERR_INVALID_ARG;
+  if (N > 256 || L > 65536 || H > 65535) return DLR_ERR_UNSUPPORTED;
+  dlr_status st = check_conv_ws(H, L, workspace, workspace_bytes);
+  if (st != DLR_OK) return st;
+  return from_cuda(dlr::launch_spectrum_direct(log_re, log_im, W, two ? log_re2 : nullptr,
+                                               two ? log_im2 : nullptr, two ? W2 : nullptr,
+                                               (int)H, (int)N, (int)L, workspace,
+                                               (cudaStream_t)stream));
 }
 
 dlr_status dlr_conv_apply(const float* u, int64_t B, int64_t H, int64_t L, float* y,

@@ -577,6 +577,22 @@ cudaError_t launch_dlr_conv_spectrum(const float* K1, const float* K2, int H, in
 #undef SPEC_CALL
 }
 
+// The twiddle tables of the convolution workspace alone (for a spectrum written by another
+// route): the n-point table, and the 2n-point one where the two-rows-per-transform kernel may
+// run, or the local n/8-point table of the cluster transform.
+cudaError_t launch_twiddles(int lg, void* ws, cudaStream_t s) {
+  ConvWs w = carve_conv(ws, lg);
+  if (lg > 14) {
+    const int lloc = lg - 3;
+    twiddle_table<<<((1 << lloc) + 255) / 256, 256, 0, s>>>(w.tw, lloc, nullptr);
+    return cudaGetLastError();
+  }
+  const bool pairs = lg >= 11 && lg <= 13;
+  twiddle_table<<<((pairs ? 3 : 1) * (1 << lg) + 255) / 256, 256, 0, s>>>(w.tw, lg,
+                                                                            pairs ? w.tw2 : nullptr);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dlr_conv_apply(const float* u, int B, int H, int L, float* y, const void* ws,
                                   cudaStream_t s) {
   const int lg = conv_log2_size(L);

@@ -47,6 +47,7 @@ def _load():
         lib.dlr_conv_spectrum.argtypes = [P, P, i32, i64, i64, P, sz, P]
         lib.dlr_conv_spectrum.restype = i32
         lib.dlr_conv_apply.argtypes = [P, i64, i64, i64, P, P, sz, P]
+        lib.dlr_conv_spectrum_direct.argtypes = [P, P, P, P, P, P, i32, i64, i64, i64, P, sz, P]
         lib.dlr_conv_apply.restype = i32
         lib.dlr_scan_workspace_size.argtypes = [i64, i64, i64, i64]
         lib.dlr_scan_workspace_size.restype = sz
@@ -165,6 +166,27 @@ def dlr_conv_spectrum(K_fwd, K_bwd=None, workspace=None, stream=None):
     _ok("dlr_conv_spectrum", _load().dlr_conv_spectrum(
         _ptr(K_fwd), _ptr(K_bwd), 1 if K_bwd is not None else 0, H, L, _ptr(workspace),
         workspace.numel(), _stream(stream)))
+    return workspace
+
+
+def dlr_conv_spectrum_direct(fwd, bwd=None, L=None, workspace=None, stream=None):
+    """The spectra for dlr_conv_apply straight from the parameters (no kernel, no spectrum FFT):
+    ``fwd`` / ``bwd`` = (log_re [H, N], log_im [H, N], W [H, N, 2]); returns the workspace."""
+    lr, li, W = fwd
+    _check_f32(lr, li, W)
+    if bwd is not None:
+        _check_f32(*bwd)
+    H, N = lr.shape
+    if L is None:
+        raise ValueError("L (the sequence length) is required")
+    need = dlr_conv_workspace_size(H, L, bwd is not None)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=lr.device)
+    b = bwd if bwd is not None else (None, None, None)
+    _ok("dlr_conv_spectrum_direct", _load().dlr_conv_spectrum_direct(
+        _ptr(lr), _ptr(li), _ptr(W), _ptr(b[0]), _ptr(b[1]), _ptr(b[2]),
+        1 if bwd is not None else 0, H, N, L, _ptr(workspace), workspace.numel(),
+        _stream(stream)))
     return workspace
 
 

@@ -31,7 +31,8 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for must in ["dlr_kernel", "dlr_conv", "dlr_conv_workspace_size", "dlr_scan", "s5_layer",
                  "s5_workspace_size", "dlr_get_device_status", "dlr_status_string",
-                 "dlr_abi_version", "dlr_step_prepare", "dlr_step", "dlr_step_workspace_size"]:
+                 "dlr_abi_version", "dlr_step_prepare", "dlr_step", "dlr_step_workspace_size",
+                 "dlr_conv_spectrum_direct"]:
         assert must in names, must
 
 
@@ -44,7 +45,7 @@ def test_status_strings_and_version(lib):
     lib.dlr_status_string.restype = ctypes.c_char_p
     assert lib.dlr_status_string(0) == b"DLR_OK"
     assert lib.dlr_status_string(4) == b"DLR_ERR_TIMEOUT"
-    assert lib.dlr_abi_version() == 6
+    assert lib.dlr_abi_version() == 7
 
 
 def test_host_validation_rejects_bad_arguments(lib):
@@ -210,3 +211,28 @@ def test_conv_and_s5_validation(lib):
     assert lib.s5_layer(u, *p, 1, 64, 32, 2048, 0, y, ws, big, None) == 2     # P > 1024
     assert lib.s5_layer(u, *p, 1, 64, 32, 32, 0, ctypes.c_void_p(0x10000010), ws, big, None) == 1
     assert lib.s5_layer(u, *p, 1, 64, 32, 32, 0, y, ws, 16, None) == 5        # short workspace
+
+
+def test_direct_spectrum_validation(lib):
+    """dlr_conv_spectrum_direct: sizes, direction and second parameter set, the 8-byte W
+    alignment, limits and the workspace are checked on the host before any launch."""
+    P, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    lib.dlr_conv_spectrum_direct.argtypes = [P] * 6 + [ctypes.c_int, i64, i64, i64, P, sz, P]
+    lib.dlr_conv_workspace_size.argtypes = [i64, i64, ctypes.c_int]
+    lib.dlr_conv_workspace_size.restype = sz
+    f = ctypes.c_void_p(0x1000)
+    ws = ctypes.c_void_p(0x8000)
+    need = lib.dlr_conv_workspace_size(4, 100, 0)
+    call = lib.dlr_conv_spectrum_direct
+    assert call(f, f, f, None, None, None, 0, 0, 8, 100, ws, need, None) == 1   # H = 0
+    assert call(f, f, f, None, None, None, 0, 4, 0, 100, ws, need, None) == 1   # N = 0
+    assert call(None, f, f, None, None, None, 0, 4, 8, 100, ws, need, None) == 1
+    assert call(f, f, ctypes.c_void_p(0x1004), None, None, None, 0, 4, 8, 100, ws, need,
+                None) == 1                                                      # W misaligned
+    assert call(f, f, f, None, None, None, 3, 4, 8, 100, ws, need, None) == 1   # direction
+    assert call(f, f, f, None, None, None, 1, 4, 8, 100, ws, need, None) == 1   # no 2nd set
+    assert call(f, f, f, f, f, f, 0, 4, 8, 100, ws, need, None) == 1           # extra set
+    assert call(f, f, f, None, None, None, 0, 4, 257, 100, ws, need, None) == 2  # N > 256
+    assert call(f, f, f, None, None, None, 0, 4, 8, 65537, ws, need, None) == 2  # L
+    assert call(f, f, f, None, None, None, 0, 4, 8, 100, None, 0, None) == 5
+    assert call(f, f, f, None, None, None, 0, 4, 8, 100, ws, need - 1, None) == 5
