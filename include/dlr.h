@@ -234,6 +234,29 @@ dlr_status dlr_scan_host(const float* u, const float* log_re, const float* log_i
                          void* workspace, size_t workspace_bytes, dlr_stream_t stream);
 
 /*
+ * dlr_scan_backward_params -- the parameter gradients of the causal DLR layer (Re cast): for a
+ * loss whose gradient with respect to y is g [B, H, L] (u the layer's input), with
+ * c_j = sum_b sum_k g_{b,k} u_{b,k-j}, S0 = sum_j c_j lambda^j, S1 = sum_j j c_j lambda^j
+ * (DLR paper section 2, gradient analysis: d K_j / d W_n = lambda_n^j, d K_j / d lambda_n =
+ * W_n j lambda_n^{j-1}; section 2.2: lambda = exp(-a^2 + i theta)):
+ *   dW [H, N, 2] = (Re S0, -Im S0),  d_log_re [H, N] = -2 a Re(W S1),
+ *   d_log_im [H, N] = -Im(W S1).
+ * Computed as sums over the steps of g against the states of two recurrences driven by u,
+ * x_k = lambda x_{k-1} + u_k and D_k = lambda (D_{k-1} + x_{k-1}) (lambda times dx/d lambda):
+ * S0 = sum g x, S1 = sum g D, per (b, h, state) with lambda as a float pair, then summed over
+ * the batch. u, g [B, H, L] (4-byte aligned); parameters as in dlr_kernel; the three outputs
+ * (dW 8-byte aligned) must not overlap the parameters or each other. workspace: device
+ * memory, dlr_scan_backward_params_workspace_size(B, H, N) bytes (16 * B * H * N), 16-byte
+ * aligned. Two kernel launches; L < 2^24, N <= 65536.
+ */
+size_t dlr_scan_backward_params_workspace_size(int64_t B, int64_t H, int64_t N);
+dlr_status dlr_scan_backward_params(const float* u, const float* g, const float* log_re,
+                                    const float* log_im, const float* W, int64_t B, int64_t H,
+                                    int64_t N, int64_t L, float* d_log_re, float* d_log_im,
+                                    float* dW, void* workspace, size_t workspace_bytes,
+                                    dlr_stream_t stream);
+
+/*
  * dlr_scan_backward_input -- the input gradient of the causal DLR layer (Re cast): for a loss
  * whose gradient with respect to y is g [B, H, L],
  *   du_k = sum_{j <= L-1-k} Re K_j g_{k+j},   K_j = sum_n W_n lambda_n^j,

@@ -33,6 +33,11 @@ cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delt
                       const float* Bt, const float* Ct, const float* D, int B, int L, int H, int P,
                       bool bf16, float* y, void* ws, int* status, cudaStream_t s);
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
+size_t grad_workspace_bytes(int64_t B, int64_t H, int64_t N);
+cudaError_t launch_dlr_grad_params(const float* u, const float* g, const float* log_re,
+                                   const float* log_im, const float* W, int B, int H, int N,
+                                   int L, float* d_log_re, float* d_log_im, float* dW, void* ws,
+                                   cudaStream_t s);
 cudaError_t launch_spectrum_direct(const float* lr1, const float* li1, const float* W1,
                                    const float* lr2, const float* li2, const float* W2, int H,
                                    int N, int L, void* ws, cudaStream_t s);
@@ -115,7 +120,7 @@ dlr_status check_params(const float* log_re, const float* log_im, const float* W
 
 extern "C" {
 
-int dlr_abi_version(void) { return 7; }
+int dlr_abi_version(void) { return 8; }
 
 const char* dlr_last_cuda_error(void) { return t_last_cuda_error_msg; }
 
@@ -303,6 +308,43 @@ dlr_status dlr_scan_apply(const float* u, int64_t B, int64_t H, int64_t N, int64
   return from_cuda(dlr::launch_scan_tc_apply(u, (int)B, (int)H, (int)L, reverse != 0, y,
                                              workspace, status_word(), (cudaStream_t)stream,
                                              false));
+}
+
+size_t dlr_scan_backward_params_workspace_size(int64_t B, int64_t H, int64_t N) {
+  if (B < 1 || H < 1 || N < 1) return 0;
+  return dlr::grad_workspace_bytes(B, H, N);
+}
+
+dlr_status dlr_scan_backward_params(const float* u, const float* g, const float* log_re,
+                                    const float* log_im, const float* W, int64_t B, int64_t H,
+                                    int64_t N, int64_t L, float* d_log_re, float* d_log_im,
+                                    float* dW, void* workspace, size_t workspace_bytes,
+                                    dlr_stream_t stream) {
+  if (B < 1 || H < 1 || N < 1 || L < 1) return DLR_ERR_INVALID_ARG;
+  if (!u || !g || !d_log_re || !d_log_im || !dW) return DLR_ERR_INVALID_ARG;
+  auto al4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  auto al8 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; };
+  if (!al4(u) || !al4(g) || !al4(d_log_re) || !al4(d_log_im) || !al8(dW))
+    return DLR_ERR_INVALID_ARG;
+  dlr_status st = check_params(log_re, log_im, W);
+  if (st != DLR_OK) return st;
+  const size_t pn = sizeof(float) * (size_t)H * (size_t)N;
+  // the outputs must not overlap the parameters or each other
+  const void* outs[3] = {d_log_re, d_log_im, dW};
+  const size_t osz[3] = {pn, pn, 2 * pn};
+  const void* ins[3] = {log_re, log_im, W};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < 3; ++j)
+      if (ranges_overlap(outs[i], osz[i], ins[j], osz[j])) return DLR_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 3; ++j)
+      if (ranges_overlap(outs[i], osz[i], outs[j], osz[j])) return DLR_ERR_INVALID_ARG;
+  }
+  if (L > kMaxL || B * H > kMaxGrid / 64 || N > 65536) return DLR_ERR_UNSUPPORTED;
+  const size_t need = dlr::grad_workspace_bytes(B, H, N);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DLR_ERR_WORKSPACE;
+  return from_cuda(dlr::launch_dlr_grad_params(u, g, log_re, log_im, W, (int)B, (int)H, (int)N,
+                                               (int)L, d_log_re, d_log_im, dW, workspace,
+                                               (cudaStream_t)stream));
 }
 
 dlr_status dlr_scan_backward_input(const float* g, const float* log_re, const float* log_im,

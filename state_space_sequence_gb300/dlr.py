@@ -65,6 +65,11 @@ def _load():
         lib.dlr_scan_host.argtypes = [P, P, P, P, i64, i64, i64, i64, P, P, sz, P]
         lib.dlr_scan_host.restype = i32
         lib.dlr_scan_backward_input.argtypes = [P, P, P, P, i64, i64, i64, i64, P, P, sz, P]
+        lib.dlr_scan_backward_params_workspace_size.argtypes = [i64, i64, i64]
+        lib.dlr_scan_backward_params_workspace_size.restype = sz
+        lib.dlr_scan_backward_params.argtypes = [P, P, P, P, P, i64, i64, i64, i64, P, P, P, P,
+                                                 sz, P]
+        lib.dlr_scan_backward_params.restype = i32
         lib.dlr_scan_backward_input.restype = i32
         lib.dlr_step_workspace_size.argtypes = [i64, i64]
         lib.dlr_step_workspace_size.restype = sz
@@ -265,6 +270,26 @@ def dlr_scan_apply(u, workspace, N: int, out=None, reverse: bool = False, stream
                                                  _ptr(out), _ptr(workspace), workspace.numel(),
                                                  _stream(stream)))
     return out
+
+
+def dlr_scan_backward_params(u, g, params, workspace=None, stream=None):
+    """Parameter gradients of the causal DLR layer (Re cast) for input u and output gradient g
+    [B, H, L]: returns (d_log_re [H, N], d_log_im [H, N], dW [H, N, 2])."""
+    _check_f32(u, g)
+    lr, li, W = _params(params)
+    B, H, L = u.shape
+    N = lr.shape[1]
+    if workspace is None:
+        need = _load().dlr_scan_backward_params_workspace_size(B, H, N)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=u.device)
+    d_re = torch.empty_like(lr)
+    d_im = torch.empty_like(li)
+    dW = torch.empty_like(W)
+    _ok("dlr_scan_backward_params",
+        _load().dlr_scan_backward_params(_ptr(u), _ptr(g), _ptr(lr), _ptr(li), _ptr(W), B, H, N,
+                                         L, _ptr(d_re), _ptr(d_im), _ptr(dW), _ptr(workspace),
+                                         workspace.numel(), _stream(stream)))
+    return d_re, d_im, dW
 
 
 def dlr_scan_backward_input(g, params, workspace=None, out=None, stream=None):

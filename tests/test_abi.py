@@ -32,7 +32,7 @@ def test_header_declares_the_boundary():
     for must in ["dlr_kernel", "dlr_conv", "dlr_conv_workspace_size", "dlr_scan", "s5_layer",
                  "s5_workspace_size", "dlr_get_device_status", "dlr_status_string",
                  "dlr_abi_version", "dlr_step_prepare", "dlr_step", "dlr_step_workspace_size",
-                 "dlr_conv_spectrum_direct"]:
+                 "dlr_conv_spectrum_direct", "dlr_scan_backward_params"]:
         assert must in names, must
 
 
@@ -45,7 +45,7 @@ def test_status_strings_and_version(lib):
     lib.dlr_status_string.restype = ctypes.c_char_p
     assert lib.dlr_status_string(0) == b"DLR_OK"
     assert lib.dlr_status_string(4) == b"DLR_ERR_TIMEOUT"
-    assert lib.dlr_abi_version() == 7
+    assert lib.dlr_abi_version() == 8
 
 
 def test_host_validation_rejects_bad_arguments(lib):
@@ -236,3 +236,29 @@ def test_direct_spectrum_validation(lib):
     assert call(f, f, f, None, None, None, 0, 4, 8, 65537, ws, need, None) == 2  # L
     assert call(f, f, f, None, None, None, 0, 4, 8, 100, None, 0, None) == 5
     assert call(f, f, f, None, None, None, 0, 4, 8, 100, ws, need - 1, None) == 5
+
+
+def test_backward_params_validation(lib):
+    """dlr_scan_backward_params: sizes, pointers and alignment, outputs that overlap the
+    parameters or each other, limits and the workspace are checked on the host."""
+    P, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
+    lib.dlr_scan_backward_params.argtypes = [P] * 5 + [i64] * 4 + [P] * 4 + [sz, P]
+    lib.dlr_scan_backward_params_workspace_size.argtypes = [i64, i64, i64]
+    lib.dlr_scan_backward_params_workspace_size.restype = sz
+    assert lib.dlr_scan_backward_params_workspace_size(8, 256, 64) == 16 * 8 * 256 * 64
+    assert lib.dlr_scan_backward_params_workspace_size(0, 1, 1) == 0
+    u, g = ctypes.c_void_p(0x100000), ctypes.c_void_p(0x200000)
+    lr, li, W = ctypes.c_void_p(0x300000), ctypes.c_void_p(0x310000), ctypes.c_void_p(0x320000)
+    dr, di, dW = ctypes.c_void_p(0x400000), ctypes.c_void_p(0x410000), ctypes.c_void_p(0x420000)
+    ws = ctypes.c_void_p(0x500000)
+    need = lib.dlr_scan_backward_params_workspace_size(2, 3, 4)
+    call = lib.dlr_scan_backward_params
+    assert call(u, g, lr, li, W, 0, 3, 4, 10, dr, di, dW, ws, need, None) == 1
+    assert call(None, g, lr, li, W, 2, 3, 4, 10, dr, di, dW, ws, need, None) == 1
+    assert call(u, g, lr, li, W, 2, 3, 4, 10, dr, di, ctypes.c_void_p(0x420004), ws, need,
+                None) == 1                                                   # dW misaligned
+    assert call(u, g, lr, li, W, 2, 3, 4, 10, lr, di, dW, ws, need, None) == 1   # overlap
+    assert call(u, g, lr, li, W, 2, 3, 4, 10, dr, dr, dW, ws, need, None) == 1   # overlap
+    assert call(u, g, lr, li, W, 2, 3, 4, 1 << 24, dr, di, dW, ws, need, None) == 2
+    assert call(u, g, lr, li, W, 2, 3, 4, 10, dr, di, dW, None, 0, None) == 5
+    assert call(u, g, lr, li, W, 2, 3, 4, 10, dr, di, dW, ws, need - 16, None) == 5
