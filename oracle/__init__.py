@@ -56,6 +56,7 @@ def _load():
                                            ctypes.c_int]
         lib.orc_toeplitz_causal.argtypes = [i64, i64, i64, P, P, P, ctypes.c_int]
         lib.orc_diag_scan.argtypes = [i64, i64, P, P, P]
+        lib.orc_diag_scan_tv.argtypes = [i64, i64, P, P, P]
         _lib = lib
     return _lib
 
@@ -287,13 +288,36 @@ def s5_zoh(lam, log_delta, Bt):
     return abar, bbar
 
 
-def s5_layer(u, lam, log_delta, Bt, Ct, D) -> np.ndarray:
+def s5_bilinear(lam, log_delta, Bt):
+    """Bilinear discretisation of the diagonal system ("The Annotated S4", part 1, the discrete
+    SSM: A_bar = (I - Delta/2 A)^-1 (I + Delta/2 A), B_bar = (I - Delta/2 A)^-1 Delta B; S5
+    section 2.1 lists it beside ZOH). For a diagonal A, per state with z = Lambda Delta:
+    Lambda_bar = (1 + z/2) / (1 - z/2), B_bar = Delta / (1 - z/2) B~. Returns complex128
+    Lambda_bar [P], B_bar [P, H]."""
+    lam = _f64(lam)
+    lamc = lam[:, 0] + 1j * lam[:, 1]
+    delta = np.exp(_f64(log_delta))
+    z = lamc * delta
+    abar = (1.0 + 0.5 * z) / (1.0 - 0.5 * z)
+    Bt = _f64(Bt)
+    Btc = Bt[..., 0] + 1j * Bt[..., 1]
+    bbar = (delta / (1.0 - 0.5 * z))[:, None] * Btc
+    return abar, bbar
+
+
+def s5_layer(u, lam, log_delta, Bt, Ct, D, disc: str = "zoh") -> np.ndarray:
     """S5 SSM outputs (sections 2.2 and 3): per batch row,
     x_k = Lambda_bar x_{k-1} + B_bar u_k (x_{-1} = 0), y_k = Re(C~ x_k) + D (.) u_k.
-    u: [B, L, H] float32. B_bar u_k is a library complex matmul over all k at once."""
+    u: [B, L, H] float32; disc 'zoh' (s5_zoh) or 'bilinear' (s5_bilinear). B_bar u_k is a
+    library complex matmul over all k at once."""
     u = _f32(u)
     Bsz, L, H = u.shape
-    abar, bbar = s5_zoh(lam, log_delta, Bt)
+    if disc == "zoh":
+        abar, bbar = s5_zoh(lam, log_delta, Bt)
+    elif disc == "bilinear":
+        abar, bbar = s5_bilinear(lam, log_delta, Bt)
+    else:
+        raise ValueError(disc)
     P = abar.shape[0]
     Ct = _f64(Ct)
     Ctc = Ct[..., 0] + 1j * Ct[..., 1]  # [H, P]
@@ -310,6 +334,104 @@ def s5_layer(u, lam, log_delta, Bt, Ct, D) -> np.ndarray:
         xc = x[..., 0] + 1j * x[..., 1]
         y[b] = (xc @ Ctc.T).real + ub * D[None, :]
     return y
+
+
+def s5_layer_tv(u, dt, lam, log_delta, Bt, Ct, D) -> np.ndarray:
+    """S5 with a step that changes from step to step (S5 section 2.2: "supplying a different
+    A_bar_k at each step" for irregularly sampled sequences; section 6.3). Reading: the
+    observation gap dt_{b,k} > 0 (time since the previous sample, in units of the base step)
+    scales each state's learned step, Delta_{p,k} = Delta_p dt_{b,k}, and every step is a ZOH:
+      Lambda_bar_{p,k} = exp(Lambda_p Delta_{p,k}),  B_bar_{p,k} = (Lambda_bar_{p,k} - 1) / Lambda_p B~_p,
+      x_k = Lambda_bar_k x_{k-1} + B_bar_k u_k,      y_k = Re(C~ x_k) + D (.) u_k.
+    u: [B, L, H] float32, dt: [B, L] float32. Returns float64 [B, L, H]."""
+    u = _f32(u)
+    dt = _f32(dt)
+    Bsz, L, H = u.shape
+    lam = _f64(lam)
+    lamc = lam[:, 0] + 1j * lam[:, 1]
+    delta = np.exp(_f64(log_delta))
+    Bt = _f64(Bt)
+    Btc = Bt[..., 0] + 1j * Bt[..., 1]
+    Ct = _f64(Ct)
+    Ctc = Ct[..., 0] + 1j * Ct[..., 1]
+    Dd = _f64(D)
+    y = np.empty((Bsz, L, H), np.float64)
+    lib = _load()
+    for b in range(Bsz):
+        z = lamc[None, :] * delta[None, :] * dt[b].astype(np.float64)[:, None]   # [L, P]
+        abar = np.exp(z)
+        f = np.expm1(z) / lamc[None, :]
+        ub = u[b].astype(np.float64)
+        v = (ub @ Btc.T) * f                                                     # [L, P]
+        ab = _f64(np.stack([abar.real, abar.imag], -1))
+        va = _f64(np.stack([v.real, v.imag], -1))
+        x = np.empty_like(va)
+        lib.orc_diag_scan_tv(L, lamc.shape[0], _p(ab), _p(va), _p(x))
+        xc = x[..., 0] + 1j * x[..., 1]
+        y[b] = (xc @ Ctc.T).real + ub * Dd[None, :]
+    return y
+
+
+# ------------------------------------------------------------------------------------------
+# Other parameterisations of the DLR
+
+def dss_exp_params(Lam, log_delta, W):
+    """DSS_exp as a DLR ("Simplifying and Understanding State Space Models with Diagonal Linear
+    RNNs", section 2: DSS_exp discretises the continuous diagonal state space x' = Lambda x + u,
+    y = Re <W, x> with a zero-order hold over steps of size Delta, and the DLR of Eq. 1 drops
+    Delta and the extra input scaling). Reading of the missing equations: the discrete state is
+    x_k = exp(Delta Lambda) x_{k-1} + (exp(Delta Lambda) - 1) / Lambda u_k, which is the DLR with
+    lambda = exp(Delta Lambda), i.e. (log Lambda)_re = sqrt(-Delta Re Lambda),
+    (log Lambda)_im = Delta Im Lambda, and the scaling moved into the weights:
+    W' = W (exp(Delta Lambda) - 1) / Lambda. Lam [H, N, 2], log_delta [H] (one step per
+    channel), W [H, N, 2]. Returns float64 log_re, log_im [H, N] and W' [H, N, 2]."""
+    Lam = _f64(Lam)
+    Lc = Lam[..., 0] + 1j * Lam[..., 1]
+    delta = np.exp(_f64(log_delta))[:, None]
+    z = Lc * delta
+    W = _f64(W)
+    Wc = W[..., 0] + 1j * W[..., 1]
+    Wn = Wc * np.expm1(z) / Lc
+    return np.sqrt(-z.real), z.imag, np.stack([Wn.real, Wn.imag], -1)
+
+
+def dss_exp_layer(u, Lam, log_delta, W) -> np.ndarray:
+    """The DSS_exp layer by its definition: the zero-order-hold recurrence
+    x_k = exp(Delta Lambda) x_{k-1} + (exp(Delta Lambda) - 1) / Lambda u_k (x_{-1} = 0),
+    y_k = Re sum_n W_n x_{n,k}, for u [B, H, L] (complex128 arithmetic, a loop over k)."""
+    u = _f32(u).astype(np.float64)
+    Lam = _f64(Lam)
+    Lc = Lam[..., 0] + 1j * Lam[..., 1]
+    z = Lc * np.exp(_f64(log_delta))[:, None]
+    a = np.exp(z)
+    f = np.expm1(z) / Lc
+    W = _f64(W)
+    Wc = W[..., 0] + 1j * W[..., 1]
+    B, H, L = u.shape
+    x = np.zeros((B, H, Lc.shape[1]), complex)
+    y = np.empty((B, H, L))
+    for k in range(L):
+        x = a[None] * x + f[None] * u[:, :, k, None]
+        y[:, :, k] = (Wc[None] * x).sum(-1).real
+    return y
+
+
+def reparam_log_re(w, kind: str, a: float = 1.0, b: float = 1.0) -> np.ndarray:
+    """(log Lambda)_re for a decay rate given by a reparameterisation f(w) of the recurrent
+    weight (the StableSSM thread: lambda = f(w) with the exponential, softplus and 'best'
+    f(w) = 1 / (a w^2 + b) maps). Reading: f(w) > 0 is the decay rate, |lambda| = exp(-f(w)),
+    so with the DLR's |lambda| = exp(-(log Lambda)_re^2), (log Lambda)_re = sqrt(f(w)).
+    kind: 'exp' (f = e^w), 'softplus' (f = log(1 + e^w)), 'best'. Returns float64."""
+    w = _f64(w)
+    if kind == "exp":
+        f = np.exp(w)
+    elif kind == "softplus":
+        f = np.logaddexp(0.0, w)
+    elif kind == "best":
+        f = 1.0 / (a * w * w + b)
+    else:
+        raise ValueError(kind)
+    return np.sqrt(f)
 
 
 def rel_l2(y, y_ref) -> float:

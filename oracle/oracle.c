@@ -230,4 +230,19 @@ void orc_diag_scan(int64_t T, int64_t P, const double* abar, const double* v, do
   }
 }
 
+/* The same scan with a multiplier that changes from step to step: x_k = abar_k x_{k-1} + v_k,
+ * abar and v [T, P, 2]. */
+void orc_diag_scan_tv(int64_t T, int64_t P, const double* abar, const double* v, double* x) {
+  for (int64_t p = 0; p < P; ++p) {
+    cplx s = {0.0, 0.0};
+    for (int64_t k = 0; k < T; ++k) {
+      cplx a = {abar[2 * (k * P + p)], abar[2 * (k * P + p) + 1]};
+      cplx vk = {v[2 * (k * P + p)], v[2 * (k * P + p) + 1]};
+      s = c_add(c_mul(a, s), vk);
+      x[2 * (k * P + p)] = s.re;
+      x[2 * (k * P + p) + 1] = s.im;
+    }
+  }
+}
+
 int orc_version(void) { return 1; }

@@ -121,6 +121,25 @@ def hippo_n_eigenvalues(P: int) -> np.ndarray:
     return lam
 
 
+def hippo_n_block_eigenvalues(P: int, J: int) -> np.ndarray:
+    """Eigenvalues of the block-diagonal initialisation of S5 (section 4.3 and appendix D.4: J
+    blocks on the diagonal, each the HiPPO-N matrix of size P / J): the J blocks' spectra one
+    after the other, [P, 2]."""
+    if P % J:
+        raise ValueError("P must be a multiple of J")
+    return np.concatenate([hippo_n_eigenvalues(P // J)] * J, axis=0)
+
+
+def irregular_gaps(rng: np.random.Generator, B: int, L: int) -> np.ndarray:
+    """Observation gaps for irregularly sampled sequences (the setting of S5 section 6.3): per
+    batch row, L observation times drawn uniformly over [0, L) and sorted; dt_k is the time
+    since the previous observation (since 0 for the first), so the mean gap is about 1.
+    [B, L] float32."""
+    t = np.sort(rng.uniform(0.0, float(L), size=(B, L)), axis=1)
+    dt = np.diff(np.concatenate([np.zeros((B, 1)), t], axis=1), axis=1)
+    return dt.astype(np.float32)
+
+
 def s5_params(rng: np.random.Generator, H: int, P: int) -> S5Params:
     lam = hippo_n_eigenvalues(P)
     log_delta = rng.uniform(np.log(1e-3), np.log(1e-1), size=P)

@@ -658,3 +658,175 @@ def test_direct_spectrum_single_state_geometric_sum():
     lam = np.exp(1j * np.float64(li[0, 0]))
     Gm5 = np.sum((lam * np.exp(2j * np.pi * 5 / M)) ** np.arange(L))
     assert abs(2 * C[5] - np.conj(Gm5) - L) < 1e-4 * L
+
+
+# ---------------------------------------------------------------------------------------
+# Discretisation and parameterisation variants
+
+def test_bilinear_matches_scipy_cont2discrete():
+    """Per state, the complex scalar system x' = lambda x + b u in its real 2x2 form,
+    discretised by scipy.signal.cont2discrete(method='bilinear'), gives the oracle's
+    Lambda_bar (as a rotation-scaling block) and B_bar (The Annotated S4, part 1)."""
+    H, P = 3, 5
+    lam, ld, Bt, _, _ = _s5_small(H, P, seed=41)
+    abar, bbar = oracle.s5_bilinear(lam, ld, Bt)
+    for p in range(P):
+        lr, li = np.float64(lam[p, 0]), np.float64(lam[p, 1])
+        A = np.array([[lr, -li], [li, lr]])
+        Bm = np.stack([Bt[p, :, 0], Bt[p, :, 1]], 0).astype(np.float64)   # [2, H]
+        dt = float(np.exp(np.float64(ld[p])))
+        Ad, Bd, _, _, _ = scipy.signal.cont2discrete((A, Bm, np.eye(2), np.zeros((2, H))), dt,
+                                                     method="bilinear")
+        np.testing.assert_allclose(Ad, [[abar[p].real, -abar[p].imag],
+                                        [abar[p].imag, abar[p].real]], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(Bd[0] + 1j * Bd[1], bbar[p], rtol=1e-12, atol=1e-14)
+    # the Pade property: |Lambda_bar| < 1 in the left half-plane, exp(z) to O(z^3)
+    assert np.all(np.abs(abar) < 1.0)
+    z = 1e-3 * (np.float64(lam[:, 0]) + 1j * np.float64(lam[:, 1]))
+    small = (1 + z / 2) / (1 - z / 2)
+    # (1 + z/2) / (1 - z/2) - exp(z) = z^3 / 12 + O(z^4)
+    assert np.all(np.abs(small - np.exp(z)) <= np.abs(z) ** 3 / 12 * 1.01 + 1e-15)
+    assert np.all(np.abs(small - np.exp(z)) >= np.abs(z) ** 3 / 12 * 0.99)
+
+
+def test_s5_bilinear_equals_dense_system():
+    """The bilinear S5 layer equals the dense system in its original coordinates (A = V Lambda
+    V^-1, B = V B~, C = C~ V^-1) discretised by scipy's bilinear transform and run densely."""
+    H, P, L = 3, 4, 40
+    lam, ld, Bt, Ct, D = _s5_small(H, P, seed=43, equal_delta=True)
+    rng = np.random.default_rng(44)
+    V = rng.standard_normal((P, P)) + 1j * rng.standard_normal((P, P))
+    lamc = lam[:, 0].astype(np.float64) + 1j * lam[:, 1]
+    A = V @ np.diag(lamc) @ np.linalg.inv(V)
+    Btc = Bt[..., 0].astype(np.float64) + 1j * Bt[..., 1]
+    Ctc = Ct[..., 0].astype(np.float64) + 1j * Ct[..., 1]
+    Bd, Cd = V @ Btc, Ctc @ np.linalg.inv(V)
+    dt = float(np.exp(np.float64(ld[0])))
+    Ad, Bdd, _, _, _ = scipy.signal.cont2discrete((A, Bd, Cd, np.zeros((H, H))), dt,
+                                                  method="bilinear")
+    u = rng.standard_normal((2, L, H)).astype(np.float32)
+    y = oracle.s5_layer(u, lam, ld, Bt, Ct, D, disc="bilinear")
+    for b in range(2):
+        x = np.zeros(P, complex)
+        for k in range(L):
+            x = Ad @ x + Bdd @ u[b, k].astype(np.float64)
+            ref = np.real(Cd @ x) + D.astype(np.float64) * u[b, k]
+            np.testing.assert_allclose(y[b, k], ref, rtol=1e-9, atol=1e-11)
+
+
+def test_s5_time_varying_unit_gaps_equal_the_layer():
+    """dt = 1 at every step reduces the time-varying layer to the ZOH layer."""
+    H, P, L = 4, 6, 50
+    lam, ld, Bt, Ct, D = _s5_small(H, P, seed=45)
+    u = np.random.default_rng(46).standard_normal((2, L, H)).astype(np.float32)
+    y = oracle.s5_layer_tv(u, np.ones((2, L), np.float32), lam, ld, Bt, Ct, D)
+    np.testing.assert_allclose(y, oracle.s5_layer(u, lam, ld, Bt, Ct, D), rtol=1e-12,
+                               atol=1e-12)
+
+
+def test_s5_time_varying_exact_for_piecewise_constant_input():
+    """One state, one feature, u = c constant, irregular gaps: the ZOH at every step keeps the
+    sampled continuous solution x(T_k) = (exp(Lambda Delta T_k) - 1) / Lambda B~ c, T_k the
+    elapsed time (S5 section 6.3's irregular sampling)."""
+    lam = np.array([[-0.7, 3.1]], np.float32)
+    ld = np.array([np.log(0.2)], np.float32)
+    Bt = np.array([[[0.8, -0.3]]], np.float32)
+    Ct = np.array([[[1.0, 0.0]]], np.float32)
+    D = np.zeros(1, np.float32)
+    rng = np.random.default_rng(47)
+    dt = inputs.irregular_gaps(rng, 1, 30)
+    c = np.float32(1.5)
+    u = np.full((1, 30, 1), c, np.float32)
+    y = oracle.s5_layer_tv(u, dt, lam, ld, Bt, Ct, D)[0, :, 0]
+    lc = np.float64(lam[0, 0]) + 1j * np.float64(lam[0, 1])
+    T = np.cumsum(dt[0].astype(np.float64)) * np.exp(np.float64(ld[0]))
+    x = np.expm1(lc * T) / lc * (np.float64(Bt[0, 0, 0]) + 1j * np.float64(Bt[0, 0, 1])) * c
+    np.testing.assert_allclose(y, x.real, rtol=1e-10, atol=1e-12)
+
+
+def test_s5_time_varying_equals_dense_per_step_expm():
+    """Irregular gaps on a dense system: every step's ZOH by scipy's matrix exponential of the
+    augmented matrix [[A d, B d], [0, 0]] with d = Delta dt_k, run densely, equals the layer."""
+    H, P, L = 2, 3, 25
+    lam, ld, Bt, Ct, D = _s5_small(H, P, seed=48, equal_delta=True)
+    rng = np.random.default_rng(49)
+    V = rng.standard_normal((P, P)) + 1j * rng.standard_normal((P, P))
+    lamc = lam[:, 0].astype(np.float64) + 1j * lam[:, 1]
+    A = V @ np.diag(lamc) @ np.linalg.inv(V)
+    Btc = Bt[..., 0].astype(np.float64) + 1j * Bt[..., 1]
+    Ctc = Ct[..., 0].astype(np.float64) + 1j * Ct[..., 1]
+    Bd, Cd = V @ Btc, Ctc @ np.linalg.inv(V)
+    delta = float(np.exp(np.float64(ld[0])))
+    dt = inputs.irregular_gaps(rng, 1, L)
+    u = rng.standard_normal((1, L, H)).astype(np.float32)
+    y = oracle.s5_layer_tv(u, dt, lam, ld, Bt, Ct, D)
+    x = np.zeros(P, complex)
+    for k in range(L):
+        d = delta * np.float64(dt[0, k])
+        M = np.zeros((P + H, P + H), complex)
+        M[:P, :P] = A * d
+        M[:P, P:] = Bd * d
+        E = scipy.linalg.expm(M)
+        x = E[:P, :P] @ x + E[:P, P:] @ u[0, k].astype(np.float64)
+        ref = np.real(Cd @ x) + D.astype(np.float64) * u[0, k]
+        np.testing.assert_allclose(y[0, k], ref, rtol=1e-9, atol=1e-11)
+
+
+def test_dss_exp_as_dlr():
+    """DSS_exp (DLR paper section 2): the zero-order-hold recurrence of x' = Lambda x + u equals
+    the DLR with lambda = exp(Delta Lambda) and W' = W (exp(Delta Lambda) - 1) / Lambda (run by
+    the oracle's DLR recurrence on the mapped parameters rounded to float32), and for a
+    constant input the state is the sampled continuous solution (exp(Lambda t) - 1) / Lambda."""
+    rng = np.random.default_rng(50)
+    H, N, L, B = 2, 6, 80, 2
+    Lam = np.stack([-rng.uniform(0.01, 1.0, (H, N)), rng.uniform(-3, 3, (H, N))], -1)
+    ld = rng.uniform(np.log(0.01), np.log(0.5), H)
+    W = rng.standard_normal((H, N, 2)) / N
+    f = lambda a: np.asarray(a, np.float32)
+    Lam, ld, W = f(Lam), f(ld), f(W)
+    u = rng.standard_normal((B, H, L)).astype(np.float32)
+    y_def = oracle.dss_exp_layer(u, Lam, ld, W)
+    lr, li, Wn = oracle.dss_exp_params(Lam, ld, W)
+    y_dlr = oracle.dlr_recurrence(u, f(lr), f(li), f(Wn))
+    assert oracle.rel_l2(y_dlr, y_def) < 1e-6       # float32 rounding of the mapped parameters
+    # constant input: x_k = (exp(Lambda (k+1) Delta) - 1) / Lambda
+    uc = np.ones((1, H, L), np.float32)
+    yc = oracle.dss_exp_layer(uc, Lam, ld, W)[0]
+    Lc = Lam[..., 0].astype(np.float64) + 1j * Lam[..., 1]
+    t = (np.arange(L) + 1)[None, None, :] * np.exp(ld.astype(np.float64))[:, None, None]
+    x = np.expm1(Lc[..., None] * t) / Lc[..., None]
+    Wc = W[..., 0].astype(np.float64) + 1j * W[..., 1]
+    np.testing.assert_allclose(yc, (Wc[..., None] * x).sum(1).real, rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("kind", ["exp", "softplus", "best"])
+def test_reparam_maps_give_the_decay_rate(kind):
+    """The reparameterised decay rates (StableSSM thread: exponential, softplus, and
+    f(w) = 1 / (a w^2 + b)) as (log Lambda)_re: the oracle's lambda then has magnitude
+    exp(-f(w)) with f computed here from its own definition, and stays inside the unit disk."""
+    w = np.linspace(-4, 4, 33)[None, :]
+    a, b = 0.5, 2.0
+    lr = oracle.reparam_log_re(w, kind, a, b)
+    lam = oracle.dlr_lambda(lr.astype(np.float32), np.full_like(lr, 0.3, dtype=np.float32))
+    f = {"exp": np.exp(w), "softplus": np.log1p(np.exp(w)), "best": 1.0 / (a * w ** 2 + b)}[kind]
+    # log_re is rounded to float32 (relative 2^-24), which moves f by up to 2^-23 of itself
+    rel = np.abs(np.abs(lam) / np.exp(-f) - 1.0)
+    assert np.all(rel <= 1.1 * f * 2.0 ** -23 + 1e-12)
+    assert np.all(np.abs(lam) < 1.0)
+
+
+def test_block_diagonal_hippo_n():
+    """S5 section 4.3: J HiPPO-N blocks on the diagonal. The eigenvalues of the explicit block
+    diagonal matrix (each block the normal part of the (P/J)-point HiPPO-LegS) from a general
+    eigensolver equal the generator's spectrum; Re = -1/2 throughout."""
+    P, J = 24, 3
+    lam = inputs.hippo_n_block_eigenvalues(P, J)
+    m = P // J
+    n = np.arange(m, dtype=np.float64)
+    A = inputs.hippo_legs(m)
+    p = np.sqrt(n + 0.5)
+    S = A + np.outer(p, p)
+    ev = np.linalg.eigvals(scipy.linalg.block_diag(*([S] * J)))
+    np.testing.assert_allclose(np.sort(ev.imag), np.sort(lam[:, 1]), rtol=1e-9, atol=1e-9)
+    np.testing.assert_allclose(lam[:, 0], -0.5, atol=1e-12)
+    np.testing.assert_allclose(ev.real, -0.5, atol=1e-9)
