@@ -508,6 +508,20 @@ def run_extras(torch, dlr, inputs, flush, sm_mhz, sm_count):
                 "frac": s5_bytes / ms / 1e6 / peak_gbs, "peak_kind": peak_kind},
         "precision": "bf16 projection operands (u rounded to bf16 in the kernel), V and x "
                      "bf16, scan float32, f32 accumulation"}
+    # the discretisation variants on the same workload: the bilinear transform (tensor-core
+    # tier) and a step that changes from step to step (float32 tier, irregular gaps)
+    ms = _time_steps(torch, lambda: dlr.s5_layer_ex(u, *args5, prec="bf16", disc="bilinear",
+                                                    workspace=ws, out=y), 10, 3, flush)
+    out["s5_bf16_tc_bilinear_" + w.name] = {"ms": ms,
+                                            "elements_per_s": w.B * w.L * w.H / ms * 1e3}
+    del ws
+    dt = dev(inputs.irregular_gaps(np.random.default_rng(3), w.B, w.L))
+    ws = torch.empty(dlr.s5_workspace_size(w.B, w.L, w.H, w.P), dtype=torch.uint8,
+                     device="cuda")
+    ms = _time_steps(torch, lambda: dlr.s5_layer_tv(u, dt, *args5, workspace=ws, out=y), 5, 2,
+                     flush)
+    out["s5_fp32_time_varying_" + w.name] = {"ms": ms,
+                                             "elements_per_s": w.B * w.L * w.H / ms * 1e3}
     return out
 
 

@@ -53,6 +53,14 @@ typedef enum { DLR_CAUSAL = 0, DLR_BIDIR = 1 } dlr_dir;
 /* Precision tier of s5_layer's projections. */
 typedef enum { DLR_FP32 = 0, DLR_BF16_TC = 1 } dlr_prec;
 
+/* Discretisation of the continuous S5 system: the zero-order hold (S5 paper section 3) or the
+ * bilinear transform ("The Annotated S4", part 1). */
+typedef enum { DLR_DISC_ZOH = 0, DLR_DISC_BILINEAR = 1 } dlr_disc;
+
+/* Decay-rate reparameterisations f(w) (the StableSSM discussion): e^w, log(1 + e^w),
+ * 1 / (a w^2 + b). */
+typedef enum { DLR_REPARAM_EXP = 0, DLR_REPARAM_SOFTPLUS = 1, DLR_REPARAM_BEST = 2 } dlr_reparam;
+
 /* Kernels behind dlr_scan_ex. DLR_SCAN_FP32: every product in float32 FMA (N <= 128).
  * DLR_SCAN_TENSOR: the chunked scan's three dense contractions on tensor cores, each operand
  * split into two float16 halves with power-of-two scaling (three MMAs per product, float32
@@ -343,6 +351,60 @@ const char* dlr_status_string(dlr_status status);
 /* The CUDA runtime's message for the last error that a call made on this host thread
  * reported as DLR_ERR_CUDA ("no error" if none). The string is static; do not free it. */
 const char* dlr_last_cuda_error(void);
+
+/*
+ * s5_layer_ex -- s5_layer with a choice of discretisation. disc = DLR_DISC_ZOH is s5_layer;
+ * disc = DLR_DISC_BILINEAR discretises each state by the bilinear transform ("The Annotated
+ * S4", part 1: A_bar = (I - Delta/2 A)^-1 (I + Delta/2 A), B_bar = (I - Delta/2 A)^-1 Delta B;
+ * for the diagonal system Lambda_bar = (1 + z/2) / (1 - z/2), B_bar = Delta / (1 - z/2) B~,
+ * z = Lambda Delta, evaluated per state in double precision). Everything else, including both
+ * precision tiers, limits and the workspace, as s5_layer.
+ */
+dlr_status s5_layer_ex(const float* u, const float* lambda, const float* log_delta,
+                       const float* Bt, const float* Ct, const float* D, int64_t B, int64_t L,
+                       int64_t H, int64_t P, dlr_prec prec, dlr_disc disc, float* y,
+                       void* workspace, size_t workspace_bytes, dlr_stream_t stream);
+
+/*
+ * s5_layer_tv -- the S5 layer with a step that changes from step to step ("Simplified State
+ * Space Layers for Sequence Modeling", section 2.2: a different A_bar at each step, for
+ * irregularly sampled sequences; section 6.3). dt [B, L]: the gap before each observation
+ * (dt > 0, in units of the base step); state p steps by Delta_p dt_{b,k} with a zero-order
+ * hold: Lambda_bar = exp(Lambda_p Delta_p dt), B_bar = (Lambda_bar - 1) / Lambda_p B~_p,
+ * x_k = Lambda_bar_k x_{k-1} + B_bar_k u_k, y_k = Re(C~ x_k) + D u_k. Float32 tier only; other
+ * arguments, layouts and limits as s5_layer with DLR_FP32; workspace:
+ * s5_layer_tv_workspace_size bytes (the float32 tier's). dt must not overlap y.
+ */
+size_t s5_layer_tv_workspace_size(int64_t B, int64_t L, int64_t H, int64_t P);
+dlr_status s5_layer_tv(const float* u, const float* dt, const float* lambda,
+                       const float* log_delta, const float* Bt, const float* Ct, const float* D,
+                       int64_t B, int64_t L, int64_t H, int64_t P, float* y, void* workspace,
+                       size_t workspace_bytes, dlr_stream_t stream);
+
+/*
+ * dlr_params_from_dss_exp -- DSS_exp as a DLR (DLR paper section 2: the continuous diagonal
+ * state space x' = Lambda x + u, y = Re <W, x>, discretised by a zero-order hold over steps
+ * Delta, is the DLR with lambda = exp(Delta Lambda) and the input scaling folded into W):
+ *   log_re = sqrt(-Delta Re Lambda), log_im = Delta Im Lambda, W_out = W (exp(Delta Lambda) - 1) / Lambda.
+ * Lambda [H, N, 2], W [H, N, 2] (8-byte aligned), log_delta [H] (one step per channel);
+ * outputs log_re, log_im [H, N], W_out [H, N, 2] (8-byte aligned), not overlapping the inputs
+ * or each other; all device pointers. Evaluated in double precision per (h, n). A state with
+ * Re Lambda > 0 cannot be held by |lambda| <= 1: it is mapped to |lambda| = 1 and
+ * DLR_ERR_INVALID_ARG is recorded in the device status (dlr_get_device_status).
+ */
+dlr_status dlr_params_from_dss_exp(const float* Lambda, const float* log_delta, const float* W,
+                                   int64_t H, int64_t N, float* log_re, float* log_im,
+                                   float* W_out, dlr_stream_t stream);
+
+/*
+ * dlr_log_re_from_reparam -- (log Lambda)_re for decay rates given by a reparameterisation
+ * f(w) of the recurrent weights (the StableSSM discussion of lambda = f(w)): |lambda| =
+ * exp(-f(w)), so log_re = sqrt(f(w)), with f = e^w (DLR_REPARAM_EXP), log(1 + e^w)
+ * (DLR_REPARAM_SOFTPLUS) or 1 / (a w^2 + b) (DLR_REPARAM_BEST; a >= 0, b > 0, else
+ * DLR_ERR_INVALID_ARG). w and log_re: `count` floats on the device (4-byte aligned).
+ */
+dlr_status dlr_log_re_from_reparam(const float* w, int64_t count, dlr_reparam kind, float a,
+                                   float b, float* log_re, dlr_stream_t stream);
 
 /* Library ABI version (incremented on any signature change or added entry point). */
 int dlr_abi_version(void);

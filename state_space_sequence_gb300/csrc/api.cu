@@ -31,7 +31,17 @@ cudaError_t launch_dlr_scan_tc(const float* u, const float* lr, const float* li,
 size_t s5_workspace_bytes(int64_t B, int64_t L, int64_t H, int64_t P, bool bf16);
 cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delta,
                       const float* Bt, const float* Ct, const float* D, int B, int L, int H, int P,
-                      bool bf16, float* y, void* ws, int* status, cudaStream_t s);
+                      bool bf16, bool bilinear, float* y, void* ws, int* status,
+                      cudaStream_t s);
+cudaError_t launch_dss_exp_map(const float* Lam, const float* log_delta, const float* W,
+                               int64_t H, int64_t N, float* log_re, float* log_im, float* Wout,
+                               int* status, cudaStream_t s);
+cudaError_t launch_reparam_map(const float* w, int64_t count, int kind, float a, float b,
+                               float* log_re, cudaStream_t s);
+cudaError_t launch_s5_tv(const float* u, const float* dt, const float* lambda,
+                         const float* log_delta, const float* Bt, const float* Ct,
+                         const float* D, int B, int L, int H, int P, float* y, void* ws,
+                         cudaStream_t s);
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
 size_t grad_workspace_bytes(int64_t B, int64_t H, int64_t N);
 cudaError_t launch_dlr_grad_params(const float* u, const float* g, const float* log_re,
@@ -120,7 +130,7 @@ dlr_status check_params(const float* log_re, const float* log_im, const float* W
 
 extern "C" {
 
-int dlr_abi_version(void) { return 8; }
+int dlr_abi_version(void) { return 9; }
 
 const char* dlr_last_cuda_error(void) { return t_last_cuda_error_msg; }
 
@@ -416,12 +426,14 @@ size_t s5_workspace_size(int64_t B, int64_t L, int64_t H, int64_t P, dlr_prec pr
   return dlr::s5_workspace_bytes(B, L, H, P, prec == DLR_BF16_TC);
 }
 
-dlr_status s5_layer(const float* u, const float* lambda, const float* log_delta,
-                    const float* Bt, const float* Ct, const float* D, int64_t B, int64_t L,
-                    int64_t H, int64_t P, dlr_prec prec, float* y, void* workspace,
-                    size_t workspace_bytes, dlr_stream_t stream) {
+static dlr_status s5_common(const float* u, const float* lambda, const float* log_delta,
+                            const float* Bt, const float* Ct, const float* D, int64_t B,
+                            int64_t L, int64_t H, int64_t P, dlr_prec prec, dlr_disc disc,
+                            float* y, void* workspace, size_t workspace_bytes,
+                            dlr_stream_t stream) {
   if (B < 1 || L < 1 || H < 1 || P < 1) return DLR_ERR_INVALID_ARG;
   if (prec != DLR_FP32 && prec != DLR_BF16_TC) return DLR_ERR_INVALID_ARG;
+  if (disc != DLR_DISC_ZOH && disc != DLR_DISC_BILINEAR) return DLR_ERR_INVALID_ARG;
   const void* ptrs[] = {u, lambda, log_delta, Bt, Ct, D, y};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return DLR_ERR_INVALID_ARG;
@@ -435,7 +447,89 @@ dlr_status s5_layer(const float* u, const float* lambda, const float* log_delta,
   int* status = bf16 ? status_word() : nullptr;
   if (bf16 && !status) return DLR_ERR_CUDA;
   return from_cuda(dlr::launch_s5(u, lambda, log_delta, Bt, Ct, D, (int)B, (int)L, (int)H,
-                                  (int)P, bf16, y, workspace, status, (cudaStream_t)stream));
+                                  (int)P, bf16, disc == DLR_DISC_BILINEAR, y, workspace, status,
+                                  (cudaStream_t)stream));
+}
+
+dlr_status s5_layer(const float* u, const float* lambda, const float* log_delta,
+                    const float* Bt, const float* Ct, const float* D, int64_t B, int64_t L,
+                    int64_t H, int64_t P, dlr_prec prec, float* y, void* workspace,
+                    size_t workspace_bytes, dlr_stream_t stream) {
+  return s5_common(u, lambda, log_delta, Bt, Ct, D, B, L, H, P, prec, DLR_DISC_ZOH, y, workspace,
+                   workspace_bytes, stream);
+}
+
+dlr_status s5_layer_ex(const float* u, const float* lambda, const float* log_delta,
+                       const float* Bt, const float* Ct, const float* D, int64_t B, int64_t L,
+                       int64_t H, int64_t P, dlr_prec prec, dlr_disc disc, float* y,
+                       void* workspace, size_t workspace_bytes, dlr_stream_t stream) {
+  return s5_common(u, lambda, log_delta, Bt, Ct, D, B, L, H, P, prec, disc, y, workspace,
+                   workspace_bytes, stream);
+}
+
+size_t s5_layer_tv_workspace_size(int64_t B, int64_t L, int64_t H, int64_t P) {
+  if (B < 1 || L < 1 || H < 1 || P < 1) return 0;
+  return dlr::s5_workspace_bytes(B, L, H, P, false);
+}
+
+dlr_status s5_layer_tv(const float* u, const float* dt, const float* lambda,
+                       const float* log_delta, const float* Bt, const float* Ct, const float* D,
+                       int64_t B, int64_t L, int64_t H, int64_t P, float* y, void* workspace,
+                       size_t workspace_bytes, dlr_stream_t stream) {
+  if (B < 1 || L < 1 || H < 1 || P < 1) return DLR_ERR_INVALID_ARG;
+  const void* ptrs[] = {u, dt, lambda, log_delta, Bt, Ct, D, y};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return DLR_ERR_INVALID_ARG;
+  const size_t bytes = sizeof(float) * (size_t)B * (size_t)L * (size_t)H;
+  if (ranges_overlap(u, bytes, y, bytes) ||
+      ranges_overlap(dt, sizeof(float) * (size_t)B * (size_t)L, y, bytes))
+    return DLR_ERR_INVALID_ARG;
+  if (H % 32 || P % 32 || H > 1024 || P > 1024) return DLR_ERR_UNSUPPORTED;
+  if (B > 65535 || (L + 63) / 64 > 65535 || B * L > kMaxGrid / 4) return DLR_ERR_UNSUPPORTED;
+  const size_t need = dlr::s5_workspace_bytes(B, L, H, P, false);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DLR_ERR_WORKSPACE;
+  return from_cuda(dlr::launch_s5_tv(u, dt, lambda, log_delta, Bt, Ct, D, (int)B, (int)L, (int)H,
+                                     (int)P, y, workspace, (cudaStream_t)stream));
+}
+
+dlr_status dlr_params_from_dss_exp(const float* Lambda, const float* log_delta, const float* W,
+                                   int64_t H, int64_t N, float* log_re, float* log_im,
+                                   float* W_out, dlr_stream_t stream) {
+  if (H < 1 || N < 1) return DLR_ERR_INVALID_ARG;
+  auto al8 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; };
+  auto al4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  if (!Lambda || !log_delta || !W || !log_re || !log_im || !W_out) return DLR_ERR_INVALID_ARG;
+  if (!al8(Lambda) || !al8(W) || !al8(W_out) || !al4(log_delta) || !al4(log_re) || !al4(log_im))
+    return DLR_ERR_INVALID_ARG;
+  const size_t pn = sizeof(float) * (size_t)H * (size_t)N;
+  const void* outs[3] = {log_re, log_im, W_out};
+  const size_t osz[3] = {pn, pn, 2 * pn};
+  const void* ins[3] = {Lambda, log_delta, W};
+  const size_t isz[3] = {2 * pn, sizeof(float) * (size_t)H, 2 * pn};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < 3; ++j)
+      if (ranges_overlap(outs[i], osz[i], ins[j], isz[j])) return DLR_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 3; ++j)
+      if (ranges_overlap(outs[i], osz[i], outs[j], osz[j])) return DLR_ERR_INVALID_ARG;
+  }
+  if ((int64_t)H * N > kMaxGrid * 64) return DLR_ERR_UNSUPPORTED;
+  int* status = status_word();
+  if (!status) return DLR_ERR_CUDA;
+  return from_cuda(dlr::launch_dss_exp_map(Lambda, log_delta, W, H, N, log_re, log_im, W_out,
+                                           status, (cudaStream_t)stream));
+}
+
+dlr_status dlr_log_re_from_reparam(const float* w, int64_t count, dlr_reparam kind, float a,
+                                   float b, float* log_re, dlr_stream_t stream) {
+  if (count < 1 || !w || !log_re) return DLR_ERR_INVALID_ARG;
+  auto al4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  if (!al4(w) || !al4(log_re)) return DLR_ERR_INVALID_ARG;
+  if (kind != DLR_REPARAM_EXP && kind != DLR_REPARAM_SOFTPLUS && kind != DLR_REPARAM_BEST)
+    return DLR_ERR_INVALID_ARG;
+  if (kind == DLR_REPARAM_BEST && !(a >= 0.f && b > 0.f)) return DLR_ERR_INVALID_ARG;
+  if (count > kMaxGrid * 64) return DLR_ERR_UNSUPPORTED;
+  return from_cuda(dlr::launch_reparam_map(w, count, (int)kind, a, b, log_re,
+                                           (cudaStream_t)stream));
 }
 
 size_t dlr_scan_host_workspace_size(int64_t B, int64_t H, int64_t N, int64_t L) {

@@ -1,0 +1,88 @@
+// dlr_params.cu -- other parameterisations mapped onto the DLR's (log Lambda)_re, (log Lambda)_im
+// and W, so that every DLR kernel runs them unchanged.
+//
+// DSS_exp ("Simplifying and Understanding State Space Models with Diagonal Linear RNNs",
+// section 2): the continuous diagonal state space x' = Lambda x + u, y = Re <W, x>, discretised
+// by a zero-order hold over steps of size Delta (one per channel), is the DLR with
+// lambda = exp(Delta Lambda) and the input scaling moved into the weights:
+//   (log Lambda)_re = sqrt(-Delta Re Lambda),  (log Lambda)_im = Delta Im Lambda,
+//   W' = W (exp(Delta Lambda) - 1) / Lambda,
+// evaluated per (h, n) in double precision, exp(z) - 1 through expm1 so that a small Delta
+// Lambda loses nothing. A state with Re Lambda > 0 (a growing mode, which the DLR's
+// |lambda| = exp(-(log Lambda)_re^2) <= 1 cannot hold) is mapped to |lambda| = 1 and reported
+// as DLR_ERR_INVALID_ARG through the device status word.
+//
+// Decay-rate reparameterisations (the StableSSM discussion: lambda = f(w) with f(w) = e^w,
+// log(1 + e^w), or the "best" 1 / (a w^2 + b)): f(w) > 0 is the decay rate,
+// |lambda| = exp(-f(w)), so (log Lambda)_re = sqrt(f(w)).
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "dlr_common.cuh"
+
+namespace dlr {
+namespace {
+
+__global__ void dss_exp_map(const float2* __restrict__ Lam,
+                            const float* __restrict__ log_delta, const float2* __restrict__ W,
+                            int64_t H, int64_t N, float* __restrict__ lr, float* __restrict__ li,
+                            float2* __restrict__ Wout, int* status) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < H * N;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t h = i / N;
+    const double delta = exp((double)log_delta[h]);
+    const float2 L = Lam[i];
+    const double zr = (double)L.x * delta, zi = (double)L.y * delta;
+    if (zr > 0.0) report_status(status, DLR_ERR_INVALID_ARG);
+    lr[i] = (float)sqrt(zr < 0.0 ? -zr : 0.0);
+    li[i] = (float)zi;
+    // exp(z) - 1 = expm1(zr) cos(zi) - 2 sin^2(zi / 2) + i e^zr sin(zi)
+    const double s2 = sin(0.5 * zi);
+    const double er = exp(zr);
+    const double mr = expm1(zr) * cos(zi) - 2.0 * s2 * s2, mi = er * sin(zi);
+    const double den = (double)L.x * L.x + (double)L.y * L.y;
+    // (exp(z) - 1) / Lambda
+    const double fr = (mr * L.x + mi * L.y) / den, fi = (mi * L.x - mr * L.y) / den;
+    const float2 w = W[i];
+    Wout[i] = make_float2((float)(w.x * fr - w.y * fi), (float)(w.x * fi + w.y * fr));
+  }
+}
+
+__global__ void reparam_map(const float* __restrict__ w, int64_t count, int kind, float a,
+                            float b, float* __restrict__ lr) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < count;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const double x = w[i];
+    double f;
+    if (kind == 0) f = exp(x);
+    else if (kind == 1) f = x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x));
+    else f = 1.0 / ((double)a * x * x + (double)b);
+    lr[i] = (float)sqrt(f);
+  }
+}
+
+unsigned grid_for(int64_t n) {
+  const int64_t g = (n + 255) / 256;
+  return (unsigned)(g < 65535 ? (g > 0 ? g : 1) : 65535);
+}
+
+}  // namespace
+
+cudaError_t launch_dss_exp_map(const float* Lam, const float* log_delta, const float* W,
+                               int64_t H, int64_t N, float* log_re, float* log_im, float* Wout,
+                               int* status, cudaStream_t s) {
+  dss_exp_map<<<grid_for(H * N), 256, 0, s>>>(reinterpret_cast<const float2*>(Lam),
+                                               log_delta, reinterpret_cast<const float2*>(W), H,
+                                               N, log_re, log_im,
+                                               reinterpret_cast<float2*>(Wout), status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reparam_map(const float* w, int64_t count, int kind, float a, float b,
+                               float* log_re, cudaStream_t s) {
+  reparam_map<<<grid_for(count), 256, 0, s>>>(w, count, kind, a, b, log_re);
+  return cudaGetLastError();
+}
+
+}  // namespace dlr

@@ -48,7 +48,7 @@ struct S5Work {
 
 __global__ void s5_prep(const float* __restrict__ lambda, const float* __restrict__ log_delta,
                         const float2* __restrict__ Bt, const float2* __restrict__ Ct, int H, int P,
-                        S5Work w) {
+                        int bilinear, S5Work w) {
   // One thread evaluates the state's transcendental functions in double (the FP64 units are
   // few): Lbar, (Lbar - 1) / Lambda, and the powers Lbar^k, Lbar^(8k) for k = 0..8 by
   // sequential products; every power t <= T is then one product Lbar^(8(t>>3)) Lbar^(t&7).
@@ -59,11 +59,25 @@ __global__ void s5_prep(const float* __restrict__ lambda, const float* __restric
     const double lr = lambda[2 * p], li = lambda[2 * p + 1];
     const double delta = exp((double)log_delta[p]);
     const double zr = lr * delta, zi = li * delta;
-    const double er = exp(zr);
-    const double ar = er * cos(zi), ai = er * sin(zi);  // Lbar
-    const double nr = ar - 1.0, ni = ai;                // (Lbar - 1) / Lambda
-    const double den = lr * lr + li * li;
-    sq = make_float2((float)((nr * lr + ni * li) / den), (float)((ni * lr - nr * li) / den));
+    double ar, ai;
+    if (!bilinear) {
+      // zero-order hold: Lbar = exp(z), B_bar = (Lbar - 1) / Lambda B~
+      const double er = exp(zr);
+      ar = er * cos(zi);
+      ai = er * sin(zi);
+      const double nr = ar - 1.0, ni = ai;
+      const double den = lr * lr + li * li;
+      sq = make_float2((float)((nr * lr + ni * li) / den), (float)((ni * lr - nr * li) / den));
+    } else {
+      // bilinear transform ("The Annotated S4", part 1): Lbar = (1 + z/2) / (1 - z/2),
+      // B_bar = Delta / (1 - z/2) B~
+      const double dr = 1.0 - 0.5 * zr, di = -0.5 * zi;   // 1 - z/2
+      const double pr = 1.0 + 0.5 * zr, pi = 0.5 * zi;    // 1 + z/2
+      const double den = dr * dr + di * di;
+      ar = (pr * dr + pi * di) / den;
+      ai = (pi * dr - pr * di) / den;
+      sq = make_float2((float)(delta * dr / den), (float)(-delta * di / den));
+    }
     double re = 1.0, im = 0.0;
     for (int k = 0; k <= 8; ++k) {
       sp1[k][0] = re;
@@ -490,6 +504,111 @@ S5Work carve(void* ws, int64_t B, int64_t L, int64_t H, int64_t P, bool bf16, si
 
 }  // namespace
 
+// ---- S5 with a step that changes from step to step ----------------------------------------
+// "Simplified State Space Layers for Sequence Modeling", section 2.2 (a different A_bar at each
+// step, for irregularly sampled sequences) and section 6.3. Each batch row has observation gaps
+// dt_k > 0; state p steps by Delta_p dt_k with a zero-order hold:
+//   Lambda_bar_{p,k} = exp(Lambda_p Delta_p dt_k),  f_{p,k} = (Lambda_bar_{p,k} - 1) / Lambda_p,
+//   x_k = Lambda_bar_k x_{k-1} + f_k (B~ u_k),      y_k = Re(C~ x_k) + D u_k.
+// The float32 tier's kernels: V = u B~^T (the projection has no discretisation factor now),
+// then a chunked scan whose multipliers are formed per step (exp of the real part, an exactly
+// reduced phase, expm1 for Lambda_bar - 1 so that a short step loses nothing), the chunk carries
+// with exp(Lambda Delta tau), tau the chunk's elapsed time summed in two-float arithmetic, and
+// the output projection as before.
+
+// per state: (Re Lambda Delta, Im Lambda Delta / pi as hi + lo), (1 / Lambda)
+__global__ void s5tv_prep(const float* __restrict__ lambda, const float* __restrict__ log_delta,
+                          const float2* __restrict__ Bt, const float2* __restrict__ Ct, int H,
+                          int P, S5Work w, float4* __restrict__ st) {
+  const int p = blockIdx.x;
+  if (threadIdx.x == 0) {
+    const double lr = lambda[2 * p], li = lambda[2 * p + 1];
+    const double delta = exp((double)log_delta[p]);
+    const double th = li * delta / 3.14159265358979323846;
+    const float th_hi = (float)th;
+    const double den = lr * lr + li * li;
+    st[2 * p] = make_float4((float)(lr * delta), th_hi, (float)(th - (double)th_hi), 0.f);
+    st[2 * p + 1] = make_float4((float)(lr / den), (float)(-li / den), 0.f, 0.f);
+  }
+  for (int h = threadIdx.x; h < H; h += blockDim.x) {
+    const float2 b = Bt[(size_t)p * H + h];
+    w.bbar[(size_t)h * 2 * P + 2 * p] = b.x;
+    w.bbar[(size_t)h * 2 * P + 2 * p + 1] = b.y;
+    const float2 c = Ct[(size_t)h * P + p];
+    w.cmat[(size_t)(2 * p) * H + h] = c.x;
+    w.cmat[(size_t)(2 * p + 1) * H + h] = -c.y;
+  }
+}
+
+// Lambda_bar and (Lambda_bar - 1) / Lambda of one step of length dt
+__device__ __forceinline__ void s5tv_coef(const float4 s0, const float4 s1, float dt, cf& abar,
+                                          cf& f) {
+  const float x = s0.x * dt;
+  const float ph = reduce_halfturns(dt, s0.y, s0.z);  // (Im Lambda Delta dt) / pi mod 2
+  float sh, ch;
+  sincospif(0.5f * ph, &sh, &ch);
+  const float sn = 2.f * sh * ch, cs = 1.f - 2.f * sh * sh;
+  const float ex = expf(x), em = expm1f(x);
+  abar = {ex * cs, ex * sn};
+  const cf m = {fmaf(em, cs, -2.f * sh * sh), ex * sn};  // exp(z) - 1
+  f = cmul(m, cf{s1.x, s1.y});
+}
+
+// chunk end states from a zero start (thread per (b, chunk, state), states fastest)
+template <bool kApply>
+__global__ void s5tv_chunks(float* __restrict__ xv, const float* __restrict__ dt,
+                            const float4* __restrict__ st, const float2* __restrict__ Xin,
+                            float2* __restrict__ S, int B, int L, int P, int NC) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)B * NC * P) return;
+  const int p = (int)(i % P);
+  const int64_t bc = i / P;
+  const int c = (int)(bc % NC), b = (int)(bc / NC);
+  const float4 s0 = st[2 * p], s1 = st[2 * p + 1];
+  cf x = kApply ? cf{Xin[i].x, Xin[i].y} : cf{0.f, 0.f};
+  const int k0 = c * kT, k1 = min(L, k0 + kT);
+  const float* dtr = dt + (int64_t)b * L;
+  float2* v = reinterpret_cast<float2*>(xv) + ((int64_t)b * L) * P + p;
+#pragma unroll 4
+  for (int k = k0; k < k1; ++k) {
+    cf a, f;
+    s5tv_coef(s0, s1, __ldg(dtr + k), a, f);
+    const float2 vk = v[(int64_t)k * P];
+    x = cfma(a, x, cmul(f, cf{vk.x, vk.y}));
+    if (kApply) v[(int64_t)k * P] = make_float2(x.re, x.im);
+  }
+  if (!kApply) S[i] = make_float2(x.re, x.im);
+}
+
+// carries over the chunks of a row (thread per (b, state)): X_{c+1} = exp(Lambda Delta tau_c) X_c
+// + S_c, tau_c the chunk's elapsed time in two-float arithmetic
+__global__ void s5tv_carry(const float* __restrict__ dt, const float4* __restrict__ st,
+                           const float2* __restrict__ S, float2* __restrict__ Xin, int B, int L,
+                           int P, int NC) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)B * P) return;
+  const int p = (int)(i % P), b = (int)(i / P);
+  const float4 s0 = st[2 * p];
+  const float* dtr = dt + (int64_t)b * L;
+  cf X = {0.f, 0.f};
+  for (int c = 0; c < NC; ++c) {
+    const int64_t o = ((int64_t)b * NC + c) * P + p;
+    Xin[o] = make_float2(X.re, X.im);
+    ff tau = {0.f, 0.f};
+    const int k0 = c * kT, k1 = min(L, k0 + kT);
+    for (int k = k0; k < k1; ++k) tau = ff_add(tau, ff{__ldg(dtr + k), 0.f});
+    // exp(Lambda Delta tau): magnitude from the real part, phase reduced exactly for tau.hi and
+    // corrected by tau.lo
+    const float mag = expf(s0.x * (tau.hi + tau.lo));
+    float ph = reduce_halfturns(tau.hi, s0.y, s0.z) + s0.y * tau.lo;
+    ph -= 2.f * rintf(0.5f * ph);
+    float sn, cs;
+    sincospif(ph, &sn, &cs);
+    const float2 sc = S[o];
+    X = cfma(cf{mag * cs, mag * sn}, X, cf{sc.x, sc.y});
+  }
+}
+
 size_t s5_workspace_bytes(int64_t B, int64_t L, int64_t H, int64_t P, bool bf16) {
   size_t total = 0;
   carve(nullptr, B, L, H, P, bf16, &total);
@@ -535,10 +654,11 @@ static cudaError_t s5_scan_xv(const S5Work& w, int B, int L, int P, bool bf16, b
 
 cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delta,
                       const float* Bt, const float* Ct, const float* D, int B, int L, int H, int P,
-                      bool bf16, float* y, void* ws, int* status, cudaStream_t s) {
+                      bool bf16, bool bilinear, float* y, void* ws, int* status,
+                      cudaStream_t s) {
   S5Work w = carve(ws, B, L, H, P, bf16, nullptr);
   s5_prep<<<P, 128, 0, s>>>(lambda, log_delta, reinterpret_cast<const float2*>(Bt),
-                            reinterpret_cast<const float2*>(Ct), H, P, w);
+                            reinterpret_cast<const float2*>(Ct), H, P, bilinear ? 1 : 0, w);
   const int M = B * L;
   cudaError_t e;
   if (!bf16) {
@@ -566,6 +686,30 @@ cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delt
                                 L, P, NC, status, s);
   return launch_tc_gemm(w.vx16, false, w.cmat_t16, y, false, M, H, 2 * P, D, u, status, s,
                         nullptr, nullptr, 0, 0);
+}
+
+cudaError_t launch_s5_tv(const float* u, const float* dt, const float* lambda,
+                         const float* log_delta, const float* Bt, const float* Ct,
+                         const float* D, int B, int L, int H, int P, float* y, void* ws,
+                         cudaStream_t s) {
+  S5Work w = carve(ws, B, L, H, P, false, nullptr);
+  // the per-state constants in the (otherwise unused) power table: 2 float4 per state
+  float4* st = reinterpret_cast<float4*>(w.lbar_pw);
+  s5tv_prep<<<P, 128, 0, s>>>(lambda, log_delta, reinterpret_cast<const float2*>(Bt),
+                              reinterpret_cast<const float2*>(Ct), H, P, w, st);
+  const int M = B * L;
+  const int NC = (L + kT - 1) / kT;
+  dim3 g1((2 * P + kGN - 1) / kGN, (M + kGM - 1) / kGM);
+  gemm_f32<<<g1, 256, 0, s>>>(u, w.bbar, w.xv, M, 2 * P, H, nullptr, nullptr);
+  const int64_t nchunk = (int64_t)B * NC * P;
+  const unsigned gc = (unsigned)((nchunk + 255) / 256);
+  s5tv_chunks<false><<<gc, 256, 0, s>>>(w.xv, dt, st, nullptr, w.S, B, L, P, NC);
+  s5tv_carry<<<(unsigned)(((int64_t)B * P + 127) / 128), 128, 0, s>>>(dt, st, w.S, w.Xin, B, L,
+                                                                        P, NC);
+  s5tv_chunks<true><<<gc, 256, 0, s>>>(w.xv, dt, st, w.Xin, nullptr, B, L, P, NC);
+  dim3 g2((H + kGN - 1) / kGN, (M + kGM - 1) / kGM);
+  gemm_f32<<<g2, 256, 0, s>>>(w.xv, w.cmat, y, M, H, 2 * P, D, u);
+  return cudaGetLastError();
 }
 
 }  // namespace dlr

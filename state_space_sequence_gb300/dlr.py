@@ -80,6 +80,16 @@ def _load():
         lib.s5_workspace_size.argtypes = [i64, i64, i64, i64, i32]
         lib.s5_workspace_size.restype = sz
         lib.s5_layer.argtypes = [P, P, P, P, P, P, i64, i64, i64, i64, i32, P, P, sz, P]
+        lib.s5_layer_ex.argtypes = [P, P, P, P, P, P, i64, i64, i64, i64, i32, i32, P, P, sz, P]
+        lib.s5_layer_ex.restype = i32
+        lib.s5_layer_tv_workspace_size.argtypes = [i64, i64, i64, i64]
+        lib.s5_layer_tv_workspace_size.restype = sz
+        lib.s5_layer_tv.argtypes = [P, P, P, P, P, P, P, i64, i64, i64, i64, P, P, sz, P]
+        lib.s5_layer_tv.restype = i32
+        lib.dlr_params_from_dss_exp.argtypes = [P, P, P, i64, i64, P, P, P, P]
+        lib.dlr_params_from_dss_exp.restype = i32
+        lib.dlr_log_re_from_reparam.argtypes = [P, i64, i32, ctypes.c_float, ctypes.c_float, P, P]
+        lib.dlr_log_re_from_reparam.restype = i32
         lib.s5_layer.restype = i32
         lib.dlr_selftest_timeout.argtypes = [i32, P]
         lib.dlr_selftest_timeout.restype = i32
@@ -396,6 +406,70 @@ def s5_layer(u, lam, log_delta, Bt, Ct, D, prec: str = "fp32", out=None, workspa
     _ok("s5_layer", _load().s5_layer(_ptr(u), _ptr(lam), _ptr(log_delta), _ptr(Bt), _ptr(Ct),
                                      _ptr(D), B, L, H, P, PREC[prec], _ptr(out),
                                      _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+DISC = {"zoh": 0, "bilinear": 1}
+REPARAM = {"exp": 0, "softplus": 1, "best": 2}
+
+
+def s5_layer_ex(u, lam, log_delta, Bt, Ct, D, prec: str = "fp32", disc: str = "zoh",
+                out=None, workspace=None, stream=None):
+    """s5_layer with the discretisation chosen: 'zoh' or 'bilinear'."""
+    _check_f32(u, lam, log_delta, Bt, Ct, D)
+    B, L, H = u.shape
+    P = lam.shape[0]
+    if out is None:
+        out = torch.empty_like(u)
+    _check_f32(out)
+    need = s5_workspace_size(B, L, H, P, prec)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=u.device)
+    _ok("s5_layer_ex", _load().s5_layer_ex(_ptr(u), _ptr(lam), _ptr(log_delta), _ptr(Bt),
+                                           _ptr(Ct), _ptr(D), B, L, H, P, PREC[prec],
+                                           DISC[disc], _ptr(out), _ptr(workspace),
+                                           workspace.numel(), _stream(stream)))
+    return out
+
+
+def s5_layer_tv(u, dt, lam, log_delta, Bt, Ct, D, out=None, workspace=None, stream=None):
+    """S5 with per-step gaps dt [B, L] (irregular sampling); float32 tier."""
+    _check_f32(u, dt, lam, log_delta, Bt, Ct, D)
+    B, L, H = u.shape
+    P = lam.shape[0]
+    if out is None:
+        out = torch.empty_like(u)
+    _check_f32(out)
+    need = _load().s5_layer_tv_workspace_size(B, L, H, P)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=u.device)
+    _ok("s5_layer_tv", _load().s5_layer_tv(_ptr(u), _ptr(dt), _ptr(lam), _ptr(log_delta),
+                                           _ptr(Bt), _ptr(Ct), _ptr(D), B, L, H, P, _ptr(out),
+                                           _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def dlr_params_from_dss_exp(Lam, log_delta, W, stream=None):
+    """DSS_exp parameters (Lam [H, N, 2], log_delta [H], W [H, N, 2]) as the DLR's
+    (log_re, log_im, W')."""
+    _check_f32(Lam, log_delta, W)
+    H, N = Lam.shape[0], Lam.shape[1]
+    lr = torch.empty((H, N), dtype=torch.float32, device=Lam.device)
+    li = torch.empty_like(lr)
+    Wo = torch.empty_like(W)
+    _ok("dlr_params_from_dss_exp",
+        _load().dlr_params_from_dss_exp(_ptr(Lam), _ptr(log_delta), _ptr(W), H, N, _ptr(lr),
+                                        _ptr(li), _ptr(Wo), _stream(stream)))
+    return lr, li, Wo
+
+
+def dlr_log_re_from_reparam(w, kind: str, a: float = 1.0, b: float = 1.0, stream=None):
+    """(log Lambda)_re = sqrt(f(w)) for the decay-rate maps 'exp', 'softplus', 'best'."""
+    _check_f32(w)
+    out = torch.empty_like(w)
+    _ok("dlr_log_re_from_reparam",
+        _load().dlr_log_re_from_reparam(_ptr(w), w.numel(), REPARAM[kind], float(a), float(b),
+                                        _ptr(out), _stream(stream)))
     return out
 
 

@@ -32,7 +32,8 @@ def test_header_declares_the_boundary():
     for must in ["dlr_kernel", "dlr_conv", "dlr_conv_workspace_size", "dlr_scan", "s5_layer",
                  "s5_workspace_size", "dlr_get_device_status", "dlr_status_string",
                  "dlr_abi_version", "dlr_step_prepare", "dlr_step", "dlr_step_workspace_size",
-                 "dlr_conv_spectrum_direct", "dlr_scan_backward_params"]:
+                 "dlr_conv_spectrum_direct", "dlr_scan_backward_params", "s5_layer_ex",
+                 "s5_layer_tv", "dlr_params_from_dss_exp", "dlr_log_re_from_reparam"]:
         assert must in names, must
 
 
@@ -45,7 +46,7 @@ def test_status_strings_and_version(lib):
     lib.dlr_status_string.restype = ctypes.c_char_p
     assert lib.dlr_status_string(0) == b"DLR_OK"
     assert lib.dlr_status_string(4) == b"DLR_ERR_TIMEOUT"
-    assert lib.dlr_abi_version() == 8
+    assert lib.dlr_abi_version() == 9
 
 
 def test_host_validation_rejects_bad_arguments(lib):
@@ -262,3 +263,37 @@ def test_backward_params_validation(lib):
     assert call(u, g, lr, li, W, 2, 3, 4, 1 << 24, dr, di, dW, ws, need, None) == 2
     assert call(u, g, lr, li, W, 2, 3, 4, 10, dr, di, dW, None, 0, None) == 5
     assert call(u, g, lr, li, W, 2, 3, 4, 10, dr, di, dW, ws, need - 16, None) == 5
+
+
+def test_variant_entry_points_validation(lib):
+    """s5_layer_ex, s5_layer_tv, dlr_params_from_dss_exp and dlr_log_re_from_reparam check their
+    arguments on the host before any launch."""
+    P, i64, sz, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int, \
+        ctypes.c_float
+    f = ctypes.c_void_p(0x100000)
+    y = ctypes.c_void_p(0x900000)
+    ws = ctypes.c_void_p(0xa00000)
+    lib.s5_layer_ex.argtypes = [P] * 6 + [i64] * 4 + [i32, i32, P, P, sz, P]
+    assert lib.s5_layer_ex(f, f, f, f, f, f, 1, 8, 32, 32, 0, 2, y, ws, 1 << 30, None) == 1
+    assert lib.s5_layer_ex(f, f, f, f, f, f, 1, 8, 33, 32, 0, 1, y, ws, 1 << 30, None) == 2
+    assert lib.s5_layer_ex(f, f, f, f, f, f, 1, 8, 32, 32, 0, 1, y, None, 0, None) == 5
+    lib.s5_layer_tv.argtypes = [P] * 7 + [i64] * 4 + [P, P, sz, P]
+    lib.s5_layer_tv_workspace_size.argtypes = [i64] * 4
+    lib.s5_layer_tv_workspace_size.restype = sz
+    assert lib.s5_layer_tv_workspace_size(0, 1, 32, 32) == 0
+    assert lib.s5_layer_tv(f, None, f, f, f, f, f, 1, 8, 32, 32, y, ws, 1 << 30, None) == 1
+    assert lib.s5_layer_tv(f, y, f, f, f, f, f, 1, 8, 32, 32, y, ws, 1 << 30, None) == 1
+    assert lib.s5_layer_tv(f, f, f, f, f, f, f, 1, 8, 32, 48, y, ws, 1 << 30, None) == 2
+    assert lib.s5_layer_tv(f, f, f, f, f, f, f, 1, 8, 32, 32, y, ws, 16, None) == 5
+    lib.dlr_params_from_dss_exp.argtypes = [P, P, P, i64, i64, P, P, P, P]
+    a, b, c = ctypes.c_void_p(0x200000), ctypes.c_void_p(0x210000), ctypes.c_void_p(0x220000)
+    o1, o2, o3 = ctypes.c_void_p(0x300000), ctypes.c_void_p(0x310000), ctypes.c_void_p(0x320000)
+    assert lib.dlr_params_from_dss_exp(a, b, c, 0, 4, o1, o2, o3, None) == 1
+    assert lib.dlr_params_from_dss_exp(ctypes.c_void_p(0x200004), b, c, 2, 4, o1, o2, o3,
+                                       None) == 1
+    assert lib.dlr_params_from_dss_exp(a, b, c, 2, 4, a, o2, o3, None) == 1    # overlap
+    lib.dlr_log_re_from_reparam.argtypes = [P, i64, i32, f32, f32, P, P]
+    assert lib.dlr_log_re_from_reparam(a, 10, 3, 1.0, 1.0, o1, None) == 1      # kind
+    assert lib.dlr_log_re_from_reparam(a, 10, 2, 1.0, 0.0, o1, None) == 1      # b <= 0
+    assert lib.dlr_log_re_from_reparam(a, 10, 2, -1.0, 1.0, o1, None) == 1     # a < 0
+    assert lib.dlr_log_re_from_reparam(a, 0, 0, 1.0, 1.0, o1, None) == 1
