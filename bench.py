@@ -465,7 +465,20 @@ def run_extras(torch, dlr, inputs, flush, sm_mhz, sm_count):
     ms = _time_steps(torch, lambda: dlr.dlr_layer(u, f, b, cast="re_im", workspace=ws, out=y),
                      10, 2, flush)
     out["fft_" + w.name] = {"ms": ms, "elements_per_s": w.B * w.H * w.L / ms * 1e3}
-    del u, y, ws
+    # the kernel generator alone (N >= 256: the tensor-core generator), both directions. Per
+    # channel it is a real [L/64 x 2N] x [2N x 128] product (64 lags of Re K and Im K per
+    # chunk row), 8 N L flops, executed as three f16 products (hi*hi + hi*lo + lo*hi)
+    Kf = torch.empty((w.H, w.L), dtype=torch.float32, device="cuda")
+    Kb = torch.empty_like(Kf)
+    ms_k = _time_steps(torch, lambda: (dlr.dlr_kernel(*f, w.L, "re_im", out=Kf),
+                                       dlr.dlr_kernel(*b, w.L, "re_im", out=Kb)), 10, 3, flush)
+    kgen_flops = 2 * 3 * 8 * w.N * w.L * w.H
+    tc_peak, tc_kind = load_tensor_peak()
+    out["kernel_gen_tc_" + w.name] = {
+        "ms": ms_k, "directions": 2, "executed_flops": kgen_flops,
+        "tensor": {"achieved": kgen_flops / ms_k / 1e9, "peak": tc_peak, "peak_kind": tc_kind,
+                   "unit": "TFLOP/s", "frac": kgen_flops / ms_k / 1e9 / tc_peak}}
+    del u, y, ws, Kf, Kb
 
     w = inputs.make_workload("dlr_b1_h256_n64_l65536_unit8")
     u, fwd = dev(w.u), (dev(w.fwd.log_re), dev(w.fwd.log_im), dev(w.fwd.W))
