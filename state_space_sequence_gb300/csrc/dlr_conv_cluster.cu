@@ -126,33 +126,44 @@ conv_cluster(const float* __restrict__ src, const float* __restrict__ src2, int 
   const int half = (L + 1) >> 1;
 
   // ---- 0) this CTA's slice of the packed row: z[rank * nl + i] ----
+  // All of a thread's loads are issued before the first shared-memory store, so their latency
+  // is paid once rather than once per point.
+  constexpr int PER = nl / T;
+  static_assert(nl % T == 0, "points per thread");
   if constexpr (kSpectrum) {
     const float* k1 = src + (size_t)row * L;
     const float* k2 = src2 ? src2 + (size_t)row * L : nullptr;
     auto col = [&](int i) -> float {  // circulant column of length 2n
-      float v = (i < L) ? k1[i] : 0.f;
+      float v = (i < L) ? __ldg(k1 + i) : 0.f;
       if (k2) {
-        if (i == 0) v += k2[0];
-        else if (i > 2 * n - L) v += k2[2 * n - i];
+        if (i == 0) v += __ldg(k2);
+        else if (i > 2 * n - L) v += __ldg(k2 + (2 * n - i));
       }
       return v;
     };
-    for (int i = tid; i < nl; i += T) {
-      const int m = (int)rank * nl + i;
-      buf0[padded(i)] = make_float2(col(2 * m), col(2 * m + 1));
+    float2 z[PER];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int m = (int)rank * nl + tid + q * T;
+      z[q] = make_float2(col(2 * m), col(2 * m + 1));
     }
+#pragma unroll
+    for (int q = 0; q < PER; ++q) buf0[padded(tid + q * T)] = z[q];
   } else {
     const float* ur = src + (size_t)row * L;
     const bool even = (L & 1) == 0;
-    for (int i = tid; i < nl; i += T) {
-      const int m = (int)rank * nl + i;
-      float2 z = make_float2(0.f, 0.f);
+    float2 z[PER];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int m = (int)rank * nl + tid + q * T;
+      z[q] = make_float2(0.f, 0.f);
       if (m < half) {
-        if (even) z = __ldg(reinterpret_cast<const float2*>(ur) + m);
-        else z = make_float2(ur[2 * m], (2 * m + 1 < L) ? ur[2 * m + 1] : 0.f);
+        if (even) z[q] = __ldg(reinterpret_cast<const float2*>(ur) + m);
+        else z[q] = make_float2(__ldg(ur + 2 * m), (2 * m + 1 < L) ? __ldg(ur + 2 * m + 1) : 0.f);
       }
-      buf0[padded(i)] = z;
     }
+#pragma unroll
+    for (int q = 0; q < PER; ++q) buf0[padded(tid + q * T)] = z[q];
   }
   cluster_sync();
 
@@ -202,47 +213,74 @@ conv_cluster(const float* __restrict__ src, const float* __restrict__ src2, int 
     // ---- real spectrum X_k, k = k1 + 8 k2, scaled by 1/(4n), stored in cluster order ----
     const float scale = 1.0f / (float)(4 * n);
     float2* out = spec + (size_t)row * (n + 1);
-    for (int k2 = tid; k2 < nl; k2 += T) {
-      const int k = k1 + kC * k2;
-      const float2 fa = cur[padded(k2)];
-      const float2 fb = ld_cluster(mirrorBase + 8u * padded(mirror_local(k2)));
-      const cf E = {0.5f * (fa.x + fb.x), 0.5f * (fa.y - fb.y)};
-      const cf O = {0.5f * (fa.y + fb.y), -0.5f * (fa.x - fb.x)};
-      float s, co;
-      sincospif(ldexpf((float)k, -(kLog + 3)), &s, &co);
-      const cf wO = cmul({co, -s}, O);
-      const cf Xk = cadd(E, wO);
-      out[k1 * nl + k2] = make_float2(Xk.re * scale, Xk.im * scale);
-      if (k == 0) {  // X_n = E - O at k = 0
-        const cf Xn = {E.re - wO.re, -(E.im - wO.im)};
-        out[n] = make_float2(Xn.re * scale, Xn.im * scale);
+    constexpr int kBatch = 4;
+    static_assert(PER % kBatch == 0, "batches");
+#pragma unroll 1
+    for (int q0 = 0; q0 < PER; q0 += kBatch) {
+      float2 fa[kBatch], fb[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int k2 = tid + (q0 + b) * T;
+        fb[b] = ld_cluster(mirrorBase + 8u * padded(mirror_local(k2)));
+        fa[b] = cur[padded(k2)];
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int k2 = tid + (q0 + b) * T;
+        const int k = k1 + kC * k2;
+        const cf E = {0.5f * (fa[b].x + fb[b].x), 0.5f * (fa[b].y - fb[b].y)};
+        const cf O = {0.5f * (fa[b].y + fb[b].y), -0.5f * (fa[b].x - fb[b].x)};
+        float s, co;
+        sincospif(ldexpf((float)k, -(kLog + 3)), &s, &co);
+        const cf wO = cmul({co, -s}, O);
+        const cf Xk = cadd(E, wO);
+        out[k1 * nl + k2] = make_float2(Xk.re * scale, Xk.im * scale);
+        if (k == 0) {  // X_n = E - O at k = 0
+          const cf Xn = {E.re - wO.re, -(E.im - wO.im)};
+          out[n] = make_float2(Xn.re * scale, Xn.im * scale);
+        }
       }
     }
     cluster_sync();  // mirrors read before any CTA exits
     return;
   } else {
     // ---- spectral step: Z'_k from Z_k, Z_{n-k} and the spectra, into nxt ----
+    // In batches of kBatch points per thread: the mirror (distributed shared memory) and
+    // spectrum (global) loads of a batch are all issued before any of them is used.
     const float2* S = spec + (size_t)(row % H) * (n + 1);
-    for (int k2 = tid; k2 < nl; k2 += T) {
-      const int k = k1 + kC * k2;
-      const int mk2 = mirror_local(k2);
-      const float2 fa = cur[padded(k2)];
-      const float2 fb = ld_cluster(mirrorBase + 8u * padded(mk2));
-      float s, co;
-      sincospif(ldexpf((float)k, -(kLog + 3)), &s, &co);
-      const cf w = {co, -s};  // e^{-i pi k / n}
-      const cf E = {fa.x + fb.x, fa.y - fb.y};
-      const cf O = {fa.y + fb.y, fb.x - fa.x};
-      const cf wO = cmul(w, O);
-      const cf X = cadd(E, wO);
-      const cf Xn = {E.re - wO.re, wO.im - E.im};
-      const float2 sk = __ldg(&S[k1 * nl + k2]);
-      const float2 sn = __ldg(&S[k == 0 ? n : (int)mirrorRank * nl + mk2]);
-      const cf Yk = cmul(X, {sk.x, sk.y});
-      const cf Yn = cmul(Xn, {sn.x, sn.y});
-      const cf Ep = {Yk.re + Yn.re, Yk.im - Yn.im};
-      const cf Op = cmul({Yk.re - Yn.re, Yk.im + Yn.im}, cconj(w));
-      nxt[padded(k2)] = make_float2(Ep.re - Op.im, Ep.im + Op.re);
+    constexpr int kBatch = 4;
+    static_assert(PER % kBatch == 0, "batches");
+#pragma unroll 1
+    for (int q0 = 0; q0 < PER; q0 += kBatch) {
+      float2 fa[kBatch], fb[kBatch], sk[kBatch], sn[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int k2 = tid + (q0 + b) * T;
+        const int k = k1 + kC * k2;
+        const int mk2 = mirror_local(k2);
+        fb[b] = ld_cluster(mirrorBase + 8u * padded(mk2));
+        sk[b] = __ldg(&S[k1 * nl + k2]);
+        sn[b] = __ldg(&S[k == 0 ? n : (int)mirrorRank * nl + mk2]);
+        fa[b] = cur[padded(k2)];
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int k2 = tid + (q0 + b) * T;
+        const int k = k1 + kC * k2;
+        float s, co;
+        sincospif(ldexpf((float)k, -(kLog + 3)), &s, &co);
+        const cf w = {co, -s};  // e^{-i pi k / n}
+        const cf E = {fa[b].x + fb[b].x, fa[b].y - fb[b].y};
+        const cf O = {fa[b].y + fb[b].y, fb[b].x - fa[b].x};
+        const cf wO = cmul(w, O);
+        const cf X = cadd(E, wO);
+        const cf Xn = {E.re - wO.re, wO.im - E.im};
+        const cf Yk = cmul(X, {sk[b].x, sk[b].y});
+        const cf Yn = cmul(Xn, {sn[b].x, sn[b].y});
+        const cf Ep = {Yk.re + Yn.re, Yk.im - Yn.im};
+        const cf Op = cmul({Yk.re - Yn.re, Yk.im + Yn.im}, cconj(w));
+        nxt[padded(k2)] = make_float2(Ep.re - Op.im, Ep.im + Op.re);
+      }
     }
     cluster_sync();  // mirror reads of `cur` done everywhere before it is reused
     {
