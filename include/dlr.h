@@ -314,12 +314,16 @@ dlr_status dlr_step(const float* u, int64_t B, int64_t H, int64_t N, int64_t T, 
  *   x_k       = Lbar (.) x_{k-1} + Bbar u_k   (x_{-1} = 0)
  *   y_k       = Re(Ct x_k) + D (.) u_k
  * u, y: [B, L, H] float32. lambda: [P, 2]. log_delta: [P]. Bt: [P, H, 2]. Ct: [H, P, 2].
- * D: [H]. prec = DLR_FP32: all products in float32 FMA. prec = DLR_BF16_TC: the two
+ * D: [H]. prec = DLR_FP32: float32 results throughout -- the two projections on tensor cores
+ * as three tf32 products per float32 product (each operand split into its tf32 part and the
+ * float32 remainder: hi*hi + hi*lo + lo*hi, float32 accumulation; error near float32
+ * rounding), the scan in float32 arithmetic. prec = DLR_BF16_TC: the two
  * projections on tensor cores with bfloat16 operands and float32 accumulation (u is read as
  * float32 and rounded to bfloat16 inside the kernel); the projected input and the states
  * between the projections are kept in bfloat16, the scan arithmetic is float32.
  * workspace: >= s5_workspace_size(B, L, H, P, prec) bytes. u and y must not overlap.
- * Limits: H % 32 == 0, P % 32 == 0, 32 <= H, P <= 1024.
+ * Limits: H % 32 == 0, P % 32 == 0, 32 <= H, P <= 1024. Faults of the tensor-core pipelines'
+ * bounded waits are reported through dlr_get_device_status().
  */
 size_t s5_workspace_size(int64_t B, int64_t L, int64_t H, int64_t P, dlr_prec prec);
 dlr_status s5_layer(const float* u, const float* lambda, const float* log_delta,

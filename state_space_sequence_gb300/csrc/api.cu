@@ -41,7 +41,7 @@ cudaError_t launch_reparam_map(const float* w, int64_t count, int kind, float a,
 cudaError_t launch_s5_tv(const float* u, const float* dt, const float* lambda,
                          const float* log_delta, const float* Bt, const float* Ct,
                          const float* D, int B, int L, int H, int P, float* y, void* ws,
-                         cudaStream_t s);
+                         int* status, cudaStream_t s);
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
 size_t grad_workspace_bytes(int64_t B, int64_t H, int64_t N);
 cudaError_t launch_dlr_grad_params(const float* u, const float* g, const float* log_re,
@@ -444,8 +444,8 @@ static dlr_status s5_common(const float* u, const float* lambda, const float* lo
   const bool bf16 = prec == DLR_BF16_TC;
   const size_t need = dlr::s5_workspace_bytes(B, L, H, P, bf16);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DLR_ERR_WORKSPACE;
-  int* status = bf16 ? status_word() : nullptr;
-  if (bf16 && !status) return DLR_ERR_CUDA;
+  int* status = status_word();
+  if (!status) return DLR_ERR_CUDA;
   return from_cuda(dlr::launch_s5(u, lambda, log_delta, Bt, Ct, D, (int)B, (int)L, (int)H,
                                   (int)P, bf16, disc == DLR_DISC_BILINEAR, y, workspace, status,
                                   (cudaStream_t)stream));
@@ -488,8 +488,10 @@ dlr_status s5_layer_tv(const float* u, const float* dt, const float* lambda,
   if (B > 65535 || (L + 63) / 64 > 65535 || B * L > kMaxGrid / 4) return DLR_ERR_UNSUPPORTED;
   const size_t need = dlr::s5_workspace_bytes(B, L, H, P, false);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DLR_ERR_WORKSPACE;
+  int* status = status_word();
+  if (!status) return DLR_ERR_CUDA;
   return from_cuda(dlr::launch_s5_tv(u, dt, lambda, log_delta, Bt, Ct, D, (int)B, (int)L, (int)H,
-                                     (int)P, y, workspace, (cudaStream_t)stream));
+                                     (int)P, y, workspace, status, (cudaStream_t)stream));
 }
 
 dlr_status dlr_params_from_dss_exp(const float* Lambda, const float* log_delta, const float* W,

@@ -35,8 +35,8 @@ struct S5Work {
   void* bbar_t16;  // bf16 [2P][H]   (tensor-core tier only)
   void* cmat_t16;  // bf16 [H][2P]
   void* vx16;      // bf16 [B*L][2P]: V, then x (tensor-core tier)
-  float* bbar;     // [H][2P]
-  float* cmat;     // [2P][H]
+  float* b1;       // [2][2P][H]: B_bar as the input projection's [N, K] operand, tf32 hi, lo
+  float* b2;       // [2][H][2P]: [Re C~, -Im C~] as the output projection's operand, hi, lo
   float2* lbar_pw; // [T+1][P]  Lbar^t (state fastest, so a warp's loads of one power coalesce)
   float4* lbar_T;  // [P] (re.hi, re.lo, im.hi, im.lo) of Lbar^T
   float2* S;       // [B][NC][P]
@@ -45,6 +45,33 @@ struct S5Work {
   float2* Xin;     // [B][NC][P]
   float* xv;       // [B*L][2P]: V, then x (float32 tier)
 };
+
+// x as its tf32 part (the 13 low mantissa bits cleared) and the float32 remainder
+__device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
+  hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+  lo = x - hi;
+}
+
+// The float32 tier's projection operands for state p and feature h, split into tf32 hi and lo
+// halves: B_bar (br + i bi) at rows 2p, 2p + 1 of the input projection's [2P, H] operand, and
+// Re C~, -Im C~ at columns 2p, 2p + 1 of row h of the output projection's [H, 2P] operand.
+__device__ __forceinline__ void store_operands(const S5Work& w, int H, int P, int p, int h,
+                                               float br, float bi, float2 c) {
+  const size_t n1 = (size_t)2 * P * H;
+  float hi, lo;
+  split_tf32(br, hi, lo);
+  w.b1[(size_t)(2 * p) * H + h] = hi;
+  w.b1[n1 + (size_t)(2 * p) * H + h] = lo;
+  split_tf32(bi, hi, lo);
+  w.b1[(size_t)(2 * p + 1) * H + h] = hi;
+  w.b1[n1 + (size_t)(2 * p + 1) * H + h] = lo;
+  split_tf32(c.x, hi, lo);
+  w.b2[(size_t)h * 2 * P + 2 * p] = hi;
+  w.b2[n1 + (size_t)h * 2 * P + 2 * p] = lo;
+  split_tf32(-c.y, hi, lo);
+  w.b2[(size_t)h * 2 * P + 2 * p + 1] = hi;
+  w.b2[n1 + (size_t)h * 2 * P + 2 * p + 1] = lo;
+}
 
 __global__ void s5_prep(const float* __restrict__ lambda, const float* __restrict__ log_delta,
                         const float2* __restrict__ Bt, const float2* __restrict__ Ct, int H, int P,
@@ -110,10 +137,7 @@ __global__ void s5_prep(const float* __restrict__ lambda, const float* __restric
       reinterpret_cast<__nv_bfloat162*>(w.cmat_t16)[(size_t)h * P + p] =
           __floats2bfloat162_rn(c.x, -c.y);
     } else {
-      w.bbar[(size_t)h * 2 * P + 2 * p] = br;
-      w.bbar[(size_t)h * 2 * P + 2 * p + 1] = bi;
-      w.cmat[(size_t)(2 * p) * H + h] = c.x;
-      w.cmat[(size_t)(2 * p + 1) * H + h] = -c.y;
+      store_operands(w, H, P, p, h, br, bi, c);
     }
   }
   for (int t = threadIdx.x; t <= kT; t += blockDim.x) {
@@ -124,58 +148,6 @@ __global__ void s5_prep(const float* __restrict__ lambda, const float* __restric
     if (t == kT) {
       float rh = (float)re, ih = (float)im;
       w.lbar_T[p] = make_float4(rh, (float)(re - rh), ih, (float)(im - ih));
-    }
-  }
-}
-
-// C[M, N] = A[M, K] * Bm[K, N] (+ D[n] * E[m, n] when E != nullptr); row-major, K % 16 == 0.
-constexpr int kGM = 64, kGN = 64, kGK = 16;
-__global__ void __launch_bounds__(256)
-gemm_f32(const float* __restrict__ A, const float* __restrict__ Bm, float* __restrict__ C, int M,
-         int N, int K, const float* __restrict__ D, const float* __restrict__ E) {
-  __shared__ float sA[kGK][kGM + 4];
-  __shared__ __align__(16) float sB[kGK][kGN];
-  const int tid = threadIdx.x;
-  const int tx = tid & 15, ty = tid >> 4;
-  const int m0 = blockIdx.y * kGM, n0 = blockIdx.x * kGN;
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < K; k0 += kGK) {
-    for (int e = tid; e < kGM * kGK; e += 256) {
-      int r = e / kGK, k = e % kGK;
-      int m = m0 + r;
-      sA[k][r] = (m < M) ? A[(size_t)m * K + k0 + k] : 0.f;
-    }
-    for (int e = tid; e < kGK * kGN; e += 256) {
-      int k = e / kGN, c = e % kGN;
-      int n = n0 + c;
-      sB[k][c] = (n < N) ? Bm[(size_t)(k0 + k) * N + n] : 0.f;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < kGK; ++k) {
-      float a[4], b[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = sA[k][ty + 16 * i];
-      float4 bv = *reinterpret_cast<const float4*>(&sB[k][4 * tx]);
-      b[0] = bv.x; b[1] = bv.y; b[2] = bv.z; b[3] = bv.w;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    int m = m0 + ty + 16 * i;
-    if (m >= M) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      int n = n0 + 4 * tx + j;
-      if (n >= N) continue;
-      float v = acc[i][j];
-      if (E) v = fmaf(D[n], E[(size_t)m * N + n], v);
-      C[(size_t)m * N + n] = v;
     }
   }
 }
@@ -471,8 +443,8 @@ S5Work carve(void* ws, int64_t B, int64_t L, int64_t H, int64_t P, bool bf16, si
     off += (bytes + 255) & ~size_t(255);
     return o;
   };
-  size_t o_bbar = bf16 ? 0 : take(sizeof(float) * H * 2 * P);
-  size_t o_cmat = bf16 ? 0 : take(sizeof(float) * 2 * P * H);
+  size_t o_b1 = bf16 ? 0 : take(sizeof(float) * 2 * 2 * P * H);
+  size_t o_b2 = bf16 ? 0 : take(sizeof(float) * 2 * H * 2 * P);
   size_t o_pw = take(sizeof(float2) * P * (kT + 1));
   size_t o_lt = take(sizeof(float4) * P);
   size_t o_S = take(sizeof(float2) * B * NC * P);
@@ -488,8 +460,8 @@ S5Work carve(void* ws, int64_t B, int64_t L, int64_t H, int64_t P, bool bf16, si
   if (total) *total = off;
   char* base = reinterpret_cast<char*>(ws);
   S5Work w;
-  w.bbar = bf16 ? nullptr : reinterpret_cast<float*>(base + o_bbar);
-  w.cmat = bf16 ? nullptr : reinterpret_cast<float*>(base + o_cmat);
+  w.b1 = bf16 ? nullptr : reinterpret_cast<float*>(base + o_b1);
+  w.b2 = bf16 ? nullptr : reinterpret_cast<float*>(base + o_b2);
   w.lbar_pw = reinterpret_cast<float2*>(base + o_pw);
   w.lbar_T = reinterpret_cast<float4*>(base + o_lt);
   w.S = reinterpret_cast<float2*>(base + o_S);
@@ -532,11 +504,7 @@ __global__ void s5tv_prep(const float* __restrict__ lambda, const float* __restr
   }
   for (int h = threadIdx.x; h < H; h += blockDim.x) {
     const float2 b = Bt[(size_t)p * H + h];
-    w.bbar[(size_t)h * 2 * P + 2 * p] = b.x;
-    w.bbar[(size_t)h * 2 * P + 2 * p + 1] = b.y;
-    const float2 c = Ct[(size_t)h * P + p];
-    w.cmat[(size_t)(2 * p) * H + h] = c.x;
-    w.cmat[(size_t)(2 * p + 1) * H + h] = -c.y;
+    store_operands(w, H, P, p, h, b.x, b.y, Ct[(size_t)h * P + p]);
   }
 }
 
@@ -622,6 +590,9 @@ cudaError_t launch_tc_gemm_apply(const void* V, const void* C, float* y, int M, 
                                  const float* D, const float* E, const float2* lam,
                                  const float2* xin, int L, int P, int NC, int* status,
                                  cudaStream_t s);
+cudaError_t launch_tc_gemm_x3(const float* A, const float* Bh, const float* Bl, float* C, int M,
+                              int N, int K, const float* D, const float* E, int* status,
+                              cudaStream_t s);
 
 // The chunked diagonal scan shared by both tiers: V -> x in place, in w.xv (float32 tier) or
 // w.vx16 (tensor-core tier). `fused` (tensor-core tier, L a multiple of 64): the input
@@ -662,13 +633,15 @@ cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delt
   const int M = B * L;
   cudaError_t e;
   if (!bf16) {
-    dim3 g1((2 * P + kGN - 1) / kGN, (M + kGM - 1) / kGM);
-    gemm_f32<<<g1, 256, 0, s>>>(u, w.bbar, w.xv, M, 2 * P, H, nullptr, nullptr);
-    e = s5_scan_xv(w, B, L, P, false, false, s);
-    if (e != cudaSuccess) return e;
-    dim3 g2((H + kGN - 1) / kGN, (M + kGM - 1) / kGM);
-    gemm_f32<<<g2, 256, 0, s>>>(w.xv, w.cmat, y, M, H, 2 * P, D, u);
-    return cudaGetLastError();
+    // float32 tier: both projections as three tf32 products on the tensor cores, the scan in
+    // float32 between them
+    const size_t n1 = (size_t)2 * P * H;
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_tc_gemm_x3(u, w.b1, w.b1 + n1, w.xv, M, 2 * P, H, nullptr, nullptr, status,
+                               s)) != cudaSuccess)
+      return e;
+    if ((e = s5_scan_xv(w, B, L, P, false, false, s)) != cudaSuccess) return e;
+    return launch_tc_gemm_x3(w.xv, w.b2, w.b2 + n1, y, M, H, 2 * P, D, u, status, s);
   }
   // tensor cores with f32 accumulation: the input projection reads the float32 u (converted to
   // bf16 in the kernel) and writes bf16 V, the scan in f32 arithmetic, the output projection
@@ -691,7 +664,7 @@ cudaError_t launch_s5(const float* u, const float* lambda, const float* log_delt
 cudaError_t launch_s5_tv(const float* u, const float* dt, const float* lambda,
                          const float* log_delta, const float* Bt, const float* Ct,
                          const float* D, int B, int L, int H, int P, float* y, void* ws,
-                         cudaStream_t s) {
+                         int* status, cudaStream_t s) {
   S5Work w = carve(ws, B, L, H, P, false, nullptr);
   // the per-state constants in the (otherwise unused) power table: 2 float4 per state
   float4* st = reinterpret_cast<float4*>(w.lbar_pw);
@@ -699,17 +672,20 @@ cudaError_t launch_s5_tv(const float* u, const float* dt, const float* lambda,
                               reinterpret_cast<const float2*>(Ct), H, P, w, st);
   const int M = B * L;
   const int NC = (L + kT - 1) / kT;
-  dim3 g1((2 * P + kGN - 1) / kGN, (M + kGM - 1) / kGM);
-  gemm_f32<<<g1, 256, 0, s>>>(u, w.bbar, w.xv, M, 2 * P, H, nullptr, nullptr);
+  const size_t n1 = (size_t)2 * P * H;
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if ((e = launch_tc_gemm_x3(u, w.b1, w.b1 + n1, w.xv, M, 2 * P, H, nullptr, nullptr, status,
+                             s)) != cudaSuccess)
+    return e;
   const int64_t nchunk = (int64_t)B * NC * P;
   const unsigned gc = (unsigned)((nchunk + 255) / 256);
   s5tv_chunks<false><<<gc, 256, 0, s>>>(w.xv, dt, st, nullptr, w.S, B, L, P, NC);
   s5tv_carry<<<(unsigned)(((int64_t)B * P + 127) / 128), 128, 0, s>>>(dt, st, w.S, w.Xin, B, L,
                                                                         P, NC);
   s5tv_chunks<true><<<gc, 256, 0, s>>>(w.xv, dt, st, w.Xin, nullptr, B, L, P, NC);
-  dim3 g2((H + kGN - 1) / kGN, (M + kGM - 1) / kGM);
-  gemm_f32<<<g2, 256, 0, s>>>(w.xv, w.cmat, y, M, H, 2 * P, D, u);
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return launch_tc_gemm_x3(w.xv, w.b2, w.b2 + n1, y, M, H, 2 * P, D, u, status, s);
 }
 
 }  // namespace dlr

@@ -449,6 +449,237 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
   if (warp == 2) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
+// ---- float32 GEMM from three tf32 products ----------------------------------------------
+// C[M, N] = A[M, K] * B[N, K]^T (+ D[n] * E[m, n]) with float32 A, B, C. Each operand x is
+// split into x_hi = x with the 13 low mantissa bits cleared (exactly a tf32 value) and
+// x_lo = x - x_hi (exact in float32; the MMA uses its 11 leading significant bits), and the
+// product is A_hi B_hi + A_hi B_lo + A_lo B_hi (three kind::tf32 MMAs into one f32 TMEM
+// accumulator). The dropped A_lo B_lo term and the truncation of the lo parts are below
+// 2^-21 of |A||B| per term; tf32 keeps float32's exponent range, so no operand scaling is
+// needed. B comes split (B_hi, B_lo: two float32 arrays); A is split in the kernel.
+//
+// Persistent, one CTA per SM over 128 x 256 output tiles (N tile fastest). K-blocks of 32
+// (128 bytes of float32 per row, the swizzle span) in a 2-stage ring of 96 KB stages:
+//   warp 0 lane 0  TMA: A (float32, into the stage's A_hi slot), B_hi, B_lo;
+//   warps 8-11     split A in place: thread = row r reads its 32 floats, writes x_hi over them
+//                  and x_lo into the A_lo slot (same swizzled layout);
+//   warp 1 lane 0  per K-block 4 K-steps x 3 MMAs of 128 x 256 x 8, a commit that frees the
+//                  stage, per tile a commit that hands one of two 256-column accumulators over;
+//   warp 2         TMEM allocation (512 columns);
+//   warps 4-7      epilogue: slices of 32 columns, tcgen05.ld, + D (.) E (E read with plain
+//                  loads one slice ahead), a 4 KB staging box per slice, TMA store.
+namespace x3 {
+constexpr int kBM = 128, kBN = 256, kBK = 32;
+constexpr int kStages = 2;
+constexpr uint32_t kAB = kBM * 128, kBB = kBN * 128;  // one operand half of a stage
+constexpr uint32_t kOffALo = kAB, kOffBHi = 2 * kAB, kOffBLo = 2 * kAB + kBB;
+constexpr uint32_t kStride = 2 * kAB + 2 * kBB;  // 96 KB
+constexpr int kBoxes = 2;
+constexpr uint32_t kEpiOff = kStages * kStride;
+constexpr uint32_t kBarOff = kEpiOff + 4 * kBoxes * kBoxBytes;
+constexpr size_t kSmemBytes = 1024 + kBarOff + 256;
+constexpr int kThreads = 384;
+static_assert(kSmemBytes <= 232448, "shared memory");
+}  // namespace x3
+
+struct X3Args {
+  int M, N, K;
+  const float* D;  // [N] or null
+  const float* E;  // [M, N] (read when D is given)
+  int* status;
+};
+
+template <bool kWithE>
+__global__ void __launch_bounds__(x3::kThreads, 1)
+tc_gemm_x3(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmBh,
+           const __grid_constant__ CUtensorMap tmBl, const __grid_constant__ CUtensorMap tmC,
+           X3Args g) {
+  constexpr int kBM = x3::kBM, kBN = x3::kBN, kBK = x3::kBK, kStages = x3::kStages;
+  constexpr int kBoxes = x3::kBoxes;
+  constexpr uint32_t kAB = x3::kAB, kBB = x3::kBB, kStride = x3::kStride;
+  constexpr uint32_t kOffALo = x3::kOffALo, kOffBHi = x3::kOffBHi, kOffBLo = x3::kOffBLo;
+  constexpr uint32_t kEpiOff = x3::kEpiOff, kBarOff = x3::kBarOff;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + kBarOff);
+  uint64_t* full = bars;                    // [kStages] A (float32), B_hi, B_lo landed
+  uint64_t* empty = bars + kStages;         // [kStages] the MMAs have read the stage
+  uint64_t* a_ready = bars + 2 * kStages;   // [kStages] A split (4 arrivals)
+  uint64_t* acc_full = bars + 3 * kStages;  // [2]
+  uint64_t* acc_empty = acc_full + 2;       // [2] (4 arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tiles = (g.N + kBN - 1) / kBN;
+  const int tiles = n_tiles * ((g.M + kBM - 1) / kBM);
+  const int nk = g.K / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+      tc::mbar_init(&a_ready[s], 4);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(&acc_full[a], 1);
+      tc::mbar_init(&acc_empty[a], 4);
+    }
+    tc::mbar_fence_init();
+  }
+  if (warp == 2) {
+    tc::tmem_alloc(tmem_slot, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+
+  if (warp == 0 && lane == 0) {
+    uint32_t it = 0;
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      const int m0 = (t / n_tiles) * kBM, n0 = (t % n_tiles) * kBN;
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int s = it % kStages;
+        if (it >= kStages && !(ok = tc::mbar_wait(&empty[s], ((it / kStages) - 1) & 1))) break;
+        uint8_t* st = base + s * kStride;
+        tc::mbar_arrive_expect_tx(&full[s], kAB + 2 * kBB);
+        tc::tma_load_2d(st, &tmA, kb * kBK, m0, &full[s]);
+        tc::tma_load_2d(st + kOffBHi, &tmBh, kb * kBK, n0, &full[s]);
+        tc::tma_load_2d(st + kOffBLo, &tmBl, kb * kBK, n0, &full[s]);
+      }
+    }
+    // every copy issued has landed before the CTA may exit
+    for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j)
+      ok &= tc::mbar_wait(&full[j % kStages], (j / kStages) & 1);
+  } else if (warp >= 8) {
+    // thread = row r of the tile: its 32 floats (8 chunks of 16 bytes at (c ^ (r & 7)) << 4)
+    const int r = (warp - 8) * 32 + lane;
+    const uint32_t sw = uint32_t(r & 7);
+    uint32_t it = 0;
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      for (int kb = 0; kb < nk && ok; ++kb, ++it) {
+        const int s = it % kStages;
+        if (!(ok = warp_wait(&full[s], (it / kStages) & 1))) break;
+        uint8_t* row = base + s * kStride + r * 128;
+        uint4 v[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          v[c] = *reinterpret_cast<const uint4*>(row + ((uint32_t(c) ^ sw) << 4));
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 hi = make_uint4(v[c].x & 0xFFFFE000u, v[c].y & 0xFFFFE000u,
+                                      v[c].z & 0xFFFFE000u, v[c].w & 0xFFFFE000u);
+          const uint4 lo = make_uint4(
+              __float_as_uint(__uint_as_float(v[c].x) - __uint_as_float(hi.x)),
+              __float_as_uint(__uint_as_float(v[c].y) - __uint_as_float(hi.y)),
+              __float_as_uint(__uint_as_float(v[c].z) - __uint_as_float(hi.z)),
+              __float_as_uint(__uint_as_float(v[c].w) - __uint_as_float(hi.w)));
+          const uint32_t o = (uint32_t(c) ^ sw) << 4;
+          *reinterpret_cast<uint4*>(row + o) = hi;
+          *reinterpret_cast<uint4*>(row + kOffALo + o) = lo;
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&a_ready[s]);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t idesc = tc::idesc_tf32_f32(kBM, kBN);
+    uint32_t it = 0, local = 0;
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++local) {
+      const uint32_t acc = local & 1;
+      if (local >= 2 && !(ok = tc::mbar_wait(&acc_empty[acc], ((local >> 1) - 1) & 1))) break;
+      tc::fence_after_sync();
+      const uint32_t d = tmem + acc * kBN;
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int s = it % kStages;
+        if (!(ok = tc::mbar_wait(&full[s], (it / kStages) & 1))) break;
+        if (!(ok = tc::mbar_wait(&a_ready[s], (it / kStages) & 1))) break;
+        tc::fence_after_sync();
+        const uint8_t* st = base + s * kStride;
+        const uint64_t ah = tc::smem_desc_k_sw128(st), al = tc::smem_desc_k_sw128(st + kOffALo);
+        const uint64_t bh = tc::smem_desc_k_sw128(st + kOffBHi);
+        const uint64_t bl = tc::smem_desc_k_sw128(st + kOffBLo);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {  // 8 tf32 = 32 bytes = 2 descriptor units per K-step
+          tc::mma_kind_tf32(d, ah + 2 * kk, bh + 2 * kk, idesc, (kb | kk) != 0);
+          tc::mma_kind_tf32(d, ah + 2 * kk, bl + 2 * kk, idesc, 1);
+          tc::mma_kind_tf32(d, al + 2 * kk, bh + 2 * kk, idesc, 1);
+        }
+        tc::mma_commit(&empty[s]);
+      }
+      tc::mma_commit(&acc_full[acc]);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    const int q = warp - 4;
+    uint8_t* boxes = base + kEpiOff + q * kBoxes * kBoxBytes;
+    const uint32_t sw = uint32_t(lane & 7);
+    uint32_t sc = 0, local = 0;
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++local) {
+      const uint32_t acc = local & 1;
+      const int m0 = (t / n_tiles) * kBM, n0 = (t % n_tiles) * kBN;
+      const int ns = min(kBN, g.N - n0) / 32;  // N is a multiple of 32
+      const int m = m0 + q * 32 + lane;         // this thread's row
+      // E of the first slice, loaded before the accumulator is ready
+      float4 e[8], en[8];
+      auto load_e = [&](int c, float4 (&dst)[8]) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) dst[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (kWithE && m < g.M && c < ns) {
+          const float4* src =
+              reinterpret_cast<const float4*>(g.E + (size_t)m * g.N + n0 + 32 * c);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) dst[k] = __ldg(src + k);
+        }
+      };
+      load_e(0, e);
+      if (!(ok = warp_wait(&acc_full[acc], (local >> 1) & 1))) break;
+      tc::fence_after_sync();
+      for (int c = 0; c < ns; ++c, ++sc) {
+        uint8_t* box = boxes + (sc % kBoxes) * kBoxBytes;
+        if (lane == 0) tc::bulk_wait_group_read<kBoxes - 1>();  // the box's last store read it
+        __syncwarp();
+        float v[32];
+        tc::tmem_ld32(tmem + acc * kBN + (uint32_t(q * 32) << 16) + uint32_t(c * 32), v);
+        if (c == ns - 1) {  // accumulator read out: the MMAs of tile local + 2 may start
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&acc_empty[acc]);
+        }
+        load_e(c + 1, en);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          float4 o = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+          if (kWithE) {
+            const float4 dk = __ldg(reinterpret_cast<const float4*>(g.D + n0 + 32 * c + 4 * k));
+            o.x = fmaf(dk.x, e[k].x, o.x);
+            o.y = fmaf(dk.y, e[k].y, o.y);
+            o.z = fmaf(dk.z, e[k].z, o.z);
+            o.w = fmaf(dk.w, e[k].w, o.w);
+          }
+          *reinterpret_cast<float4*>(box + lane * 128 + ((uint32_t(k) ^ sw) << 4)) = o;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) e[k] = en[k];
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tc::tma_store_2d(&tmC, box, n0 + c * 32, m0 + q * 32);
+          tc::bulk_commit_group();
+        }
+      }
+    }
+    if (lane == 0) tc::bulk_wait_group0();
+  }
+  if (!ok) report_status(g.status, DLR_ERR_TIMEOUT);
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 2) tc::tmem_dealloc(tmem, kTmemCols);
+}
+
 // Failure-reporting self-test: one thread waits on a barrier that nothing completes.
 __global__ void selftest_wait_timeout(uint64_t limit_ns, int* status) {
   __shared__ uint64_t bar;
@@ -552,6 +783,36 @@ cudaError_t launch_tc_gemm_apply(const void* V, const void* C, float* y, int M, 
   const long long tiles = (long long)((N + kBN - 1) / kBN) * ((M + kBM - 1) / kBM);
   const int grid = (int)std::min<long long>(tiles, sm_count());
   return run_gemm<kOpApply, true, false>(ma, mb, mc, me, g, grid, s);
+}
+
+
+// C[M, N] = A[M, K] B[N, K]^T (+ D (.) E) in float32 from three tf32 products (tc_gemm_x3). A,
+// Bh, Bl, C, E: row-major float32, 16-byte aligned; Bh = B with the 13 low mantissa bits
+// cleared, Bl = B - Bh; K and N multiples of 32; D [N] or null.
+cudaError_t launch_tc_gemm_x3(const float* A, const float* Bh, const float* Bl, float* C, int M,
+                              int N, int K, const float* D, const float* E, int* status,
+                              cudaStream_t s) {
+  if (M < 1 || N < 1 || K < 1 || K % 32 || N % 32 || (D && !E)) return cudaErrorInvalidValue;
+  if (D && ((reinterpret_cast<uintptr_t>(D) | reinterpret_cast<uintptr_t>(E)) & 15))
+    return cudaErrorInvalidValue;
+  CUtensorMap ma, mbh, mbl, mc;
+  if (!make_map(&ma, A, (uint64_t)M, (uint64_t)K, x3::kBM, true) ||
+      !make_map(&mbh, Bh, (uint64_t)N, (uint64_t)K, x3::kBN, true) ||
+      !make_map(&mbl, Bl, (uint64_t)N, (uint64_t)K, x3::kBN, true) ||
+      !make_map(&mc, C, (uint64_t)M, (uint64_t)N, 32, true))
+    return cudaErrorInvalidValue;
+  X3Args g{M, N, K, D, E, status};
+  const long long tiles = (long long)((N + x3::kBN - 1) / x3::kBN) * ((M + x3::kBM - 1) / x3::kBM);
+  const int grid = (int)std::min<long long>(tiles, sm_count());
+  cudaError_t e;
+  if (D) {
+    if ((e = max_smem_once<tc_gemm_x3<true>>(x3::kSmemBytes)) != cudaSuccess) return e;
+    tc_gemm_x3<true><<<grid, x3::kThreads, x3::kSmemBytes, s>>>(ma, mbh, mbl, mc, g);
+  } else {
+    if ((e = max_smem_once<tc_gemm_x3<false>>(x3::kSmemBytes)) != cudaSuccess) return e;
+    tc_gemm_x3<false><<<grid, x3::kThreads, x3::kSmemBytes, s>>>(ma, mbh, mbl, mc, g);
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace dlr

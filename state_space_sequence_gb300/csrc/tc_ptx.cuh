@@ -397,6 +397,27 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
   return (1u << 4) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
+// kind::tf32 with tf32 A and B (format fields 2), f32 accumulator, both K-major. A tf32
+// operand is a 32-bit word of which the MMA uses the sign, the exponent and the 10 leading
+// mantissa bits.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(N >> 3) << 17) |
+         (uint32_t(M >> 4) << 24);
+}
+
+// D (TMEM) [+]= A (smem) * B (smem)^T, kind::tf32, issued by one thread.
+__device__ __forceinline__ void mma_kind_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n"
+      "  .reg .pred p;\n"
+      "  setp.ne.b32 p, %4, 0;\n"
+      "  tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D (TMEM) [+]= A (smem) * B (smem)^T, issued by one thread (kind::f16: the operand type,
 // f16 or bf16, comes from the instruction descriptor).
 __device__ __forceinline__ void mma_kind_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
