@@ -502,8 +502,18 @@ def run_extras(torch, dlr, inputs, flush, sm_mhz, sm_count):
     ws = torch.empty(dlr.s5_workspace_size(w.B, w.L, w.H, w.P), dtype=torch.uint8,
                      device="cuda")
     y = torch.empty_like(u)
-    ms = _time_steps(torch, lambda: dlr.s5_layer(u, *args5, workspace=ws, out=y), 5, 2, flush)
-    out["s5_fp32_" + w.name] = {"ms": ms, "elements_per_s": w.B * w.L * w.H / ms * 1e3}
+    ms = _time_steps(torch, lambda: dlr.s5_layer(u, *args5, workspace=ws, out=y), 10, 3, flush)
+    # both projections as three tf32 products (kind::tf32 runs at half the f16 rate, so the
+    # peak is the measured bf16 peak / 2)
+    x3_flops = 3 * 2 * 2 * w.B * w.L * w.H * 2 * w.P
+    tc_peak, tc_kind = load_tensor_peak()
+    out["s5_fp32_tc_" + w.name] = {
+        "ms": ms, "elements_per_s": w.B * w.L * w.H / ms * 1e3,
+        "tensor": {"executed_tf32_flops": x3_flops, "achieved": x3_flops / ms / 1e9,
+                   "peak": tc_peak / 2, "peak_kind": tc_kind + ", halved for tf32",
+                   "unit": "TFLOP/s", "frac": x3_flops / ms / 1e9 / (tc_peak / 2)},
+        "precision": "float32: projections as tf32 hi*hi + hi*lo + lo*hi with f32 "
+                     "accumulation, scan in float32"}
     del ws
     ws = torch.empty(dlr.s5_workspace_size(w.B, w.L, w.H, w.P, "bf16"), dtype=torch.uint8,
                      device="cuda")
