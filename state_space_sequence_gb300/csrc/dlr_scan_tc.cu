@@ -224,22 +224,6 @@ __device__ __forceinline__ void grid_wait_prerequisites() {
 __device__ __forceinline__ void named_bar(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
-// Barrier over `n` threads of named barrier `id` that also ANDs a predicate across them.
-__device__ __forceinline__ bool named_bar_and(int id, int n, bool v) {
-  int r;
-  asm volatile(
-      "{\n"
-      "  .reg .pred p, q;\n"
-      "  setp.ne.s32 p, %1, 0;\n"
-      "  bar.red.and.pred q, %2, %3, p;\n"
-      "  selp.s32 %0, 1, 0, q;\n"
-      "}\n"
-      : "=r"(r)
-      : "r"((int)v), "r"(id), "r"(n)
-      : "memory");
-  return r != 0;
-}
-
 // Bounded wait on an mbarrier phase (one thread) that also gives up when another role has
 // aborted. Each try may suspend the thread for a few microseconds.
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort) {
@@ -254,12 +238,13 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
     }
   }
 }
-// The same for a whole warp: lane 0 waits, the other lanes are held at the shuffle.
-__device__ __forceinline__ bool warp_wait_phase(uint64_t* bar, uint32_t parity,
-                                                volatile int* abort) {
-  bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = wait_phase(bar, parity, abort);
-  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+// The main warps' wait for a phase: every lane waits (and so acquires what the phase
+// published). A wait that gives up leaves the abort flag set and returns; the warp then carries
+// on through its schedule (every later wait returns at once), so all main warps still reach
+// every named barrier and the kernel ends; the caller reports DLR_ERR_TIMEOUT.
+__device__ __forceinline__ bool lanes_wait_phase(uint64_t* bar, uint32_t parity,
+                                                 volatile int* abort) {
+  return wait_phase(bar, parity, abort);
 }
 
 constexpr int kTbThreads = 512;  // threads of the tables kernel
@@ -645,17 +630,12 @@ __device__ __forceinline__ bool conv_tile(const TcScanArgs& a, uint8_t* sm, uint
   // the u buffer released by GEMM1 of tile j-2; at a new channel also GEMM1 of tile j-1 done
   // (Q is reloaded); the u tile landed
   bool ok = true;
-  if (j >= 2) ok = warp_wait_phase(&bars[kBarG1 + par], ((j - 2) >> 1) & 1, abort);
-  if (ok && new_channel && j >= 1)
-    ok = warp_wait_phase(&bars[kBarG1 + (par ^ 1)], ((j - 1) >> 1) & 1, abort);
-  if (ok && a.tma) ok = warp_wait_phase(&bars[kBarStage + par], (j >> 1) & 1, abort);
-  if (!named_bar_and(kMainBar, 256, ok)) return false;
+  if (j >= 2) ok = lanes_wait_phase(&bars[kBarG1 + par], ((j - 2) >> 1) & 1, abort);
+  if (new_channel && j >= 1)
+    ok &= lanes_wait_phase(&bars[kBarG1 + (par ^ 1)], ((j - 1) >> 1) & 1, abort);
+  if (a.tma) ok &= lanes_wait_phase(&bars[kBarStage + par], (j >> 1) & 1, abort);
   if (threadIdx.x == 0) SCAN_TRACE(1000 + j * 8 + 1);
   const uint8_t* blob = a.tables + (size_t)ti.h * kBlobBytes;
-  if (new_channel) {
-    cur_h = ti.h;
-    sig_k = __ldg(reinterpret_cast<const float*>(blob + kBlobSig));
-  }
   const ColInfo ci = col_info(a, ti, rc);
   uint8_t* ubuf = sm + kU + par * kUBuf;
   float v[32];
@@ -702,6 +682,13 @@ __device__ __forceinline__ bool conv_tile(const TcScanArgs& a, uint8_t* sm, uint
 #pragma unroll
     for (int i = 0; i < 8; ++i) w8[i] = v[8 * p + i] * su;
     store_chunk8(ubuf, ubuf + kULo, g, 4 * h + p, w8);
+  }
+  if (new_channel) {
+    // the first read of the tables: at the CTA's first tile, wait here for the table kernel
+    // (programmatic dependent launch), so the conversion above overlaps its end
+    if (cur_h < 0) grid_wait_prerequisites();
+    cur_h = ti.h;
+    sig_k = __ldg(reinterpret_cast<const float*>(blob + kBlobSig));
   }
   if (h == 0) {
     if (ci.c == 0 || g == 0) reinterpret_cast<int*>(sm + kRowEs)[slot * 128 + rl] = es;
@@ -794,8 +781,7 @@ __device__ __forceinline__ bool epi_tile(const TcScanArgs& a, const CUtensorMap*
   const int h = warp >> 2, quarter = warp & 3, g = quarter * 32 + lane;
   const int par = j & 1, slot = j & 3;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
-  const bool ok = warp_wait_phase(&bars[kBarG2], j & 1, abort);
-  if (!named_bar_and(kMainBar, 256, ok)) return false;
+  const bool ok = lanes_wait_phase(&bars[kBarG2], j & 1, abort);
   if (threadIdx.x == 0) SCAN_TRACE(2000 + j * 8 + 1);
   tc::fence_after_sync();
   const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
@@ -1135,8 +1121,7 @@ __device__ __forceinline__ bool chain_tile(const TcScanArgs& a, uint8_t* sm, uin
   const uint32_t tS = tmem + (uint32_t(quarter * 32) << 16) + kTS + uint32_t(par) * 128;
 
   // S of this tile
-  const bool ok = warp_wait_phase(&bars[kBarG1 + par], (k >> 1) & 1, abort);
-  if (!named_bar_and(kMainBar, 256, ok)) return false;
+  const bool ok = lanes_wait_phase(&bars[kBarG1 + par], (k >> 1) & 1, abort);
   tc::fence_after_sync();
   if (threadIdx.x == 0) SCAN_TRACE(k * 8 + 0);
 #ifdef DLR_SCAN_TRACE
@@ -1203,8 +1188,8 @@ __device__ __forceinline__ bool chain_tile(const TcScanArgs& a, uint8_t* sm, uin
 // The main warps (0-7) over all tiles of the CTA. Iteration k: the u operand of tile k+1, the
 // outputs of tile k-1 (once its GEMM2 is done), the chain of tile k. The scale slots are rings
 // of four tiles, so tile k+1's u scales never overwrite those tile k-1's outputs still read.
-// Every wait is taken by all 256 threads together (named_bar_and), so a wait that gives up
-// makes all of them leave at the same point.
+// Each warp takes its waits on its own (lanes_wait_phase); the warps meet only at the named
+// barriers of the u conversion and at the top of each iteration.
 template <bool kRev>
 __device__ __forceinline__ void main_role(const TcScanArgs& a, const CUtensorMap* ymap,
                                           uint8_t* sm, uint32_t tmem, int u0, int segs,
@@ -1220,20 +1205,20 @@ __device__ __forceinline__ void main_role(const TcScanArgs& a, const CUtensorMap
   int chain_h = -1;
   if (ntiles == 0) return;
   TileIter it_conv = tile_iter_begin(a, u0), it_epi = it_conv, it_chain = it_conv;
-  if (!conv_tile<kRev>(a, sm, tmem, it_conv.t, rc, 0, conv_h, sig_k, abort)) return;
+  conv_tile<kRev>(a, sm, tmem, it_conv.t, rc, 0, conv_h, sig_k, abort);
   tile_iter_next(a, segs, it_conv);
-  bool ok = true;
-  for (int k = 0; k < ntiles && ok; ++k) {
+  // Every warp runs the whole schedule even after an abort (its waits then return at once), so
+  // the named barriers below are always reached by all 256 threads.
+  for (int k = 0; k < ntiles; ++k) {
     named_bar(kMainBar, 256);  // the previous stages' shared-memory writes are visible
     if (k + 1 < ntiles) {
-      ok = conv_tile<kRev>(a, sm, tmem, it_conv.t, rc, k + 1, conv_h, sig_k, abort);
+      conv_tile<kRev>(a, sm, tmem, it_conv.t, rc, k + 1, conv_h, sig_k, abort);
       tile_iter_next(a, segs, it_conv);
     }
-    if (ok && k >= 1) {
-      ok = epi_tile<kRev>(a, ymap, sm, tmem, it_epi.t, rc, k - 1, abort);
+    if (k >= 1) {
+      epi_tile<kRev>(a, ymap, sm, tmem, it_epi.t, rc, k - 1, abort);
       tile_iter_next(a, segs, it_epi);
     }
-    if (!ok) break;
     const TileInfo& ti = it_chain.t;
     if (ti.h != chain_h) {
       // this thread's lambda^64 and re-anchoring correction; the G scale of the channel. The
@@ -1248,13 +1233,11 @@ __device__ __forceinline__ void main_role(const TcScanArgs& a, const CUtensorMap
       q.dl_im = (r & 1) ? -m.w : m.w;
       sig_g = __ldg(reinterpret_cast<const float*>(blob + kBlobSig) + 1);
     }
-    ok = chain_tile(a, sm, tmem, k, ti.seg == 0, q, sig_g, xo, xt, ao, at, es_prev, abort);
+    chain_tile(a, sm, tmem, k, ti.seg == 0, q, sig_g, xo, xt, ao, at, es_prev, abort);
     tile_iter_next(a, segs, it_chain);
   }
-  if (ok) {
-    named_bar(kMainBar, 256);
-    epi_tile<kRev>(a, ymap, sm, tmem, it_epi.t, rc, ntiles - 1, abort);
-  }
+  named_bar(kMainBar, 256);
+  epi_tile<kRev>(a, ymap, sm, tmem, it_epi.t, rc, ntiles - 1, abort);
   if (a.tma && (threadIdx.x & 31) == 0) tc::bulk_wait_group0();  // y stores done
 }
 
@@ -1302,8 +1285,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int segs = (a.R > 0) ? 1 : (a.C + kCols - 1) / kCols;
   const int ntiles = (u1 - u0) * segs;
 
-  // everything below the producer's first u copies reads the tables or data derived from them
-  if (warp != 9) grid_wait_prerequisites();
+  // The tables written by the table kernel are read by the producer's copies (it waits for the
+  // table kernel after issuing its first u copies) and by the main warps (they wait at their
+  // first read, in conv_tile); the MMA thread reads only what those two produce.
   if (warp < 8) {
     main_role<kRev>(a, &ymap, sm, tmem, u0, segs, ntiles, abort);
   } else if (warp == 8) {
