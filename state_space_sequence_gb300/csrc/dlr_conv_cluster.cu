@@ -14,6 +14,16 @@
 // kernel otherwise ("Simplifying and Understanding State Space Models with Diagonal Linear
 // RNNs", section 2.1 and appendix A.1: Toeplitz product as a circulant product of size >= 2L).
 // Spectra are stored in cluster order S'[k1 n_loc + k2] = S[k1 + 8 k2], with S[n] last.
+//
+// Every step works in place in one shared buffer of n_loc points (70 KB at n_loc = 8192), so
+// two CTAs (of different clusters) share an SM and hide each other's barrier and load
+// latency:
+//   F1 / I1  the thread of column i reads position i of the 8 CTAs and writes position i of
+//            the 8 CTAs (F1) or global memory (I1); no other thread touches position i;
+//   F2 / I2  each Stockham pass loads all of a thread's points, synchronises, stores them;
+//   spectral step: one thread per pair (k, n - k) reads both points and writes both outputs
+//            (the partner may sit in the mirror CTA), so each point is read and written by
+//            one thread.
 #include "fft_rows.cuh"
 
 namespace dlr {
@@ -66,50 +76,69 @@ __device__ __forceinline__ void powers8(cf (&p)[8], cf x) {
   p[7] = cmul(p[4], p[3]);
 }
 
-// Local Stockham FFT of n_loc = 2^kLog points held in `cur` (natural order); the result ends
-// in natural order in `cur` (the pointers are swapped as the passes alternate buffers).
+// Local Stockham FFT of n_loc = 2^kLog points in `buf` (natural order in and out), in place:
+// every pass loads all of a thread's points, synchronises, then stores.
 template <int kLog, bool kInv>
-__device__ __forceinline__ void local_fft(float2*& cur, float2*& nxt,
-                                          const float2* __restrict__ tw) {
+__device__ __forceinline__ void local_fft(float2* buf, const float2* __restrict__ tw) {
   using P = fftr::Plan<kLog>;
-  cf a[P::PER0][P::R0];
-#pragma unroll
-  for (int q = 0; q < P::PER0; ++q) {
-    const int j = threadIdx.x + q * P::T;
-    if (P::NB0 % P::T == 0 || j < P::NB0) {
-#pragma unroll
-      for (int r = 0; r < P::R0; ++r) {
-        const float2 f = cur[padded(j + r * P::NB0)];
-        a[q][r] = {f.x, f.y};
-      }
-      fft::dft<P::R0, kInv>(a[q]);
-    }
-  }
-  fftr::pass0_store<kLog>(nxt, a);
-  __syncthreads();
   {
-    float2* t = cur;
-    cur = nxt;
-    nxt = t;
+    cf a[P::PER0][P::R0];
+#pragma unroll
+    for (int q = 0; q < P::PER0; ++q) {
+      const int j = threadIdx.x + q * P::T;
+      if (P::NB0 % P::T == 0 || j < P::NB0) {
+#pragma unroll
+        for (int r = 0; r < P::R0; ++r) {
+          const float2 f = buf[padded(j + r * P::NB0)];
+          a[q][r] = {f.x, f.y};
+        }
+        fft::dft<P::R0, kInv>(a[q]);
+      }
+    }
+    __syncthreads();
+    fftr::pass0_store<kLog>(buf, a);
+    __syncthreads();
   }
   int ns = P::R0;
 #pragma unroll 1
   for (int p = 0; p < P::n16; ++p) {
     cf v[P::PER16][16];
-    fftr::pass16_load_compute<kLog, kInv>(cur, ns, tw, v);
-    fftr::pass16_store<kLog>(nxt, ns, v);
+    fftr::pass16_load_compute<kLog, kInv>(buf, ns, tw, v);
     __syncthreads();
-    float2* t = cur;
-    cur = nxt;
-    nxt = t;
+    fftr::pass16_store<kLog>(buf, ns, v);
+    __syncthreads();
     ns *= 16;
   }
+}
+
+// The spectral step's output at bin k from the packed transform's Z_k (fa) and Z_{n-k} (fb),
+// the kernel spectra S_k (sk) and S_{n-k} (sn; S_n at k = 0), w = e^{-i pi k / n}: the real
+// spectra X_k, X_{n-k} unpacked, multiplied, and repacked as the inverse transform's input.
+__device__ __forceinline__ float2 spectral_point(float2 fa, float2 fb, float2 sk, float2 sn,
+                                                 cf w) {
+  const cf E = {fa.x + fb.x, fa.y - fb.y};
+  const cf O = {fa.y + fb.y, fb.x - fa.x};
+  const cf wO = cmul(w, O);
+  const cf X = cadd(E, wO);
+  const cf Xn = {E.re - wO.re, wO.im - E.im};
+  const cf Yk = cmul(X, {sk.x, sk.y});
+  const cf Yn = cmul(Xn, {sn.x, sn.y});
+  const cf Ep = {Yk.re + Yn.re, Yk.im - Yn.im};
+  const cf Op = cmul({Yk.re - Yn.re, Yk.im + Yn.im}, cconj(w));
+  return make_float2(Ep.re - Op.im, Ep.im + Op.re);
+}
+
+template <int kLog>
+__device__ __forceinline__ cf half_turn_twiddle(int k) {  // e^{-i pi k / n}, n = 8 n_loc
+  float s, co;
+  sincospif(ldexpf((float)k, -(kLog + 3)), &s, &co);
+  return {co, -s};
 }
 
 // kSpectrum: transform the circulant column of channel `row` and write its spectrum.
 // Otherwise: convolve row `row` of u with the spectra and write y.
 template <int kLog, bool kSpectrum>
-__global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(fftr::Plan<kLog>::T)
+__global__ void __cluster_dims__(kC, 1, 1) __launch_bounds__(fftr::Plan<kLog>::T, 2)
 conv_cluster(const float* __restrict__ src, const float* __restrict__ src2, int H, int L,
              const float2* __restrict__ tw, float2* __restrict__ spec, float* __restrict__ y) {
   using P = fftr::Plan<kLog>;
@@ -118,95 +147,89 @@ conv_cluster(const float* __restrict__ src, const float* __restrict__ src2, int 
   constexpr int T = P::T;
   constexpr int colsPer = nl / kC;  // F1 / I1 columns per CTA
   extern __shared__ float2 smem[];
-  float2* buf0 = smem;
-  float2* buf1 = smem + P::buf_elems;
+  float2* buf = smem;
   const uint32_t rank = cluster_rank();
   const int row = blockIdx.x / kC;
   const int tid = threadIdx.x;
   const int half = (L + 1) >> 1;
+  const uint32_t bufAddr = smem_addr(buf);
 
   // ---- 0) this CTA's slice of the packed row: z[rank * nl + i] ----
   // All of a thread's loads are issued before the first shared-memory store, so their latency
   // is paid once rather than once per point.
   constexpr int PER = nl / T;
   static_assert(nl % T == 0, "points per thread");
-  if constexpr (kSpectrum) {
-    const float* k1 = src + (size_t)row * L;
-    const float* k2 = src2 ? src2 + (size_t)row * L : nullptr;
-    auto col = [&](int i) -> float {  // circulant column of length 2n
-      float v = (i < L) ? __ldg(k1 + i) : 0.f;
-      if (k2) {
-        if (i == 0) v += __ldg(k2);
-        else if (i > 2 * n - L) v += __ldg(k2 + (2 * n - i));
-      }
-      return v;
-    };
+  {
     float2 z[PER];
+    if constexpr (kSpectrum) {
+      const float* k1 = src + (size_t)row * L;
+      const float* k2 = src2 ? src2 + (size_t)row * L : nullptr;
+      auto col = [&](int i) -> float {  // circulant column of length 2n
+        float v = (i < L) ? __ldg(k1 + i) : 0.f;
+        if (k2) {
+          if (i == 0) v += __ldg(k2);
+          else if (i > 2 * n - L) v += __ldg(k2 + (2 * n - i));
+        }
+        return v;
+      };
 #pragma unroll
-    for (int q = 0; q < PER; ++q) {
-      const int m = (int)rank * nl + tid + q * T;
-      z[q] = make_float2(col(2 * m), col(2 * m + 1));
+      for (int q = 0; q < PER; ++q) {
+        const int m = (int)rank * nl + tid + q * T;
+        z[q] = make_float2(col(2 * m), col(2 * m + 1));
+      }
+    } else {
+      const float* ur = src + (size_t)row * L;
+      const bool even = (L & 1) == 0;
+#pragma unroll
+      for (int q = 0; q < PER; ++q) {
+        const int m = (int)rank * nl + tid + q * T;
+        z[q] = make_float2(0.f, 0.f);
+        if (m < half) {
+          if (even) z[q] = __ldg(reinterpret_cast<const float2*>(ur) + m);
+          else z[q] = make_float2(__ldg(ur + 2 * m), (2 * m + 1 < L) ? __ldg(ur + 2 * m + 1) : 0.f);
+        }
+      }
     }
 #pragma unroll
-    for (int q = 0; q < PER; ++q) buf0[padded(tid + q * T)] = z[q];
-  } else {
-    const float* ur = src + (size_t)row * L;
-    const bool even = (L & 1) == 0;
-    float2 z[PER];
-#pragma unroll
-    for (int q = 0; q < PER; ++q) {
-      const int m = (int)rank * nl + tid + q * T;
-      z[q] = make_float2(0.f, 0.f);
-      if (m < half) {
-        if (even) z[q] = __ldg(reinterpret_cast<const float2*>(ur) + m);
-        else z[q] = make_float2(__ldg(ur + 2 * m), (2 * m + 1 < L) ? __ldg(ur + 2 * m + 1) : 0.f);
-      }
-    }
-#pragma unroll
-    for (int q = 0; q < PER; ++q) buf0[padded(tid + q * T)] = z[q];
+    for (int q = 0; q < PER; ++q) buf[padded(tid + q * T)] = z[q];
   }
   cluster_sync();
 
   // ---- F1: radix-8 DFT across the cluster, twiddle W_n^{i k1}, output k1 -> CTA k1 ----
-  {
-    const uint32_t b0 = smem_addr(buf0), b1 = smem_addr(buf1);
-    for (int ii = tid; ii < colsPer; ii += T) {
-      const int i = (int)rank * colsPer + ii;
-      cf v[8];
+  for (int ii = tid; ii < colsPer; ii += T) {
+    const int i = (int)rank * colsPer + ii;
+    const uint32_t off = 8u * padded(i);
+    cf v[8];
 #pragma unroll
-      for (int c = 0; c < kC; ++c) {
-        // the conv input is zero for m >= n/2, i.e. c >= 4
-        if (!kSpectrum && c >= kC / 2) {
-          v[c] = {0.f, 0.f};
-        } else {
-          const float2 f = ld_cluster(map_rank(b0, c) + 8u * padded(i));
-          v[c] = {f.x, f.y};
-        }
+    for (int c = 0; c < kC; ++c) {
+      // the conv input is zero for m >= n/2, i.e. c >= 4
+      if (!kSpectrum && c >= kC / 2) {
+        v[c] = {0.f, 0.f};
+      } else {
+        const float2 f = ld_cluster(map_rank(bufAddr, c) + off);
+        v[c] = {f.x, f.y};
       }
-      fft::dft<8, false>(v);
-      float s, co;
-      sincospif(-ldexpf((float)i, 1 - (kLog + 3)), &s, &co);  // W_n^i = e^{-2 pi i i / n}
-      cf w[8];
-      powers8(w, {co, s});
+    }
+    fft::dft<8, false>(v);
+    float s, co;
+    sincospif(-ldexpf((float)i, 1 - (kLog + 3)), &s, &co);  // W_n^i = e^{-2 pi i i / n}
+    cf w[8];
+    powers8(w, {co, s});
 #pragma unroll
-      for (int k1 = 0; k1 < kC; ++k1) {
-        const cf t = k1 ? cmul(v[k1], w[k1]) : v[k1];
-        st_cluster(map_rank(b1, k1) + 8u * padded(i), make_float2(t.re, t.im));
-      }
+    for (int k1 = 0; k1 < kC; ++k1) {
+      const cf t = k1 ? cmul(v[k1], w[k1]) : v[k1];
+      st_cluster(map_rank(bufAddr, k1) + off, make_float2(t.re, t.im));
     }
   }
   cluster_sync();
 
   // ---- F2: local FFT over i; CTA k1 = rank then holds Z[k1 + 8 k2] at k2 ----
-  float2* cur = buf1;
-  float2* nxt = buf0;
-  local_fft<kLog, false>(cur, nxt, tw);
+  local_fft<kLog, false>(buf, tw);
   cluster_sync();  // every CTA's Z is complete before mirrors are read
 
   const int k1 = (int)rank;
-  const uint32_t curAddr = smem_addr(cur);
   const uint32_t mirrorRank = (kC - k1) & (kC - 1);
-  const uint32_t mirrorBase = map_rank(curAddr, mirrorRank);
+  const uint32_t mirrorBase = map_rank(bufAddr, mirrorRank);
   auto mirror_local = [&](int k2) { return k1 == 0 ? (nl - k2) & (nl - 1) : nl - 1 - k2; };
 
   if constexpr (kSpectrum) {
@@ -222,7 +245,7 @@ conv_cluster(const float* __restrict__ src, const float* __restrict__ src2, int 
       for (int b = 0; b < kBatch; ++b) {
         const int k2 = tid + (q0 + b) * T;
         fb[b] = ld_cluster(mirrorBase + 8u * padded(mirror_local(k2)));
-        fa[b] = cur[padded(k2)];
+        fa[b] = buf[padded(k2)];
       }
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
@@ -230,9 +253,7 @@ conv_cluster(const float* __restrict__ src, const float* __restrict__ src2, int 
         const int k = k1 + kC * k2;
         const cf E = {0.5f * (fa[b].x + fb[b].x), 0.5f * (fa[b].y - fb[b].y)};
         const cf O = {0.5f * (fa[b].y + fb[b].y), -0.5f * (fa[b].x - fb[b].x)};
-        float s, co;
-        sincospif(ldexpf((float)k, -(kLog + 3)), &s, &co);
-        const cf wO = cmul({co, -s}, O);
+        const cf wO = cmul(half_turn_twiddle<kLog>(k), O);
         const cf Xk = cadd(E, wO);
         out[k1 * nl + k2] = make_float2(Xk.re * scale, Xk.im * scale);
         if (k == 0) {  // X_n = E - O at k = 0
@@ -244,56 +265,56 @@ conv_cluster(const float* __restrict__ src, const float* __restrict__ src2, int 
     cluster_sync();  // mirrors read before any CTA exits
     return;
   } else {
-    // ---- spectral step: Z'_k from Z_k, Z_{n-k} and the spectra, into nxt ----
-    // In batches of kBatch points per thread: the mirror (distributed shared memory) and
-    // spectrum (global) loads of a batch are all issued before any of them is used.
+    // ---- spectral step, one thread per pair of bins (k, n - k), in place ----
+    // Item p in [0, nl/2) of CTA k1 is the pair (k1, p) <-> (mirror CTA, mirror_local(p)):
+    // CTA k1 and its mirror each take the first half of their own positions, which covers
+    // the second half of the other's. CTA 0 pairs p with nl - p (p = 0 with itself) and its
+    // item 0 also takes position nl/2 (bin n/2, paired with itself); CTA 4 pairs p with
+    // nl - 1 - p inside itself.
     const float2* S = spec + (size_t)(row % H) * (n + 1);
+    constexpr int kItems = nl / 2 / T;
     constexpr int kBatch = 4;
-    static_assert(PER % kBatch == 0, "batches");
+    static_assert(kItems % kBatch == 0 || kItems < kBatch, "batches");
+    constexpr int kB = kItems < kBatch ? kItems : kBatch;
+    const bool local_pair = mirrorRank == (uint32_t)k1;
 #pragma unroll 1
-    for (int q0 = 0; q0 < PER; q0 += kBatch) {
-      float2 fa[kBatch], fb[kBatch], sk[kBatch], sn[kBatch];
+    for (int q0 = 0; q0 < kItems; q0 += kB) {
+      float2 fa[kB], fb[kB], s1[kB], s2[kB];
 #pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        const int k2 = tid + (q0 + b) * T;
-        const int k = k1 + kC * k2;
-        const int mk2 = mirror_local(k2);
-        fb[b] = ld_cluster(mirrorBase + 8u * padded(mk2));
-        sk[b] = __ldg(&S[k1 * nl + k2]);
-        sn[b] = __ldg(&S[k == 0 ? n : (int)mirrorRank * nl + mk2]);
-        fa[b] = cur[padded(k2)];
+      for (int b = 0; b < kB; ++b) {
+        const int p1 = tid + (q0 + b) * T;
+        const int p2 = mirror_local(p1);
+        fa[b] = buf[padded(p1)];
+        fb[b] = local_pair ? buf[padded(p2)] : ld_cluster(mirrorBase + 8u * padded(p2));
+        s1[b] = __ldg(&S[k1 * nl + p1]);
+        s2[b] = __ldg(&S[(k1 == 0 && p1 == 0) ? n : (int)mirrorRank * nl + p2]);
       }
 #pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        const int k2 = tid + (q0 + b) * T;
-        const int k = k1 + kC * k2;
-        float s, co;
-        sincospif(ldexpf((float)k, -(kLog + 3)), &s, &co);
-        const cf w = {co, -s};  // e^{-i pi k / n}
-        const cf E = {fa[b].x + fb[b].x, fa[b].y - fb[b].y};
-        const cf O = {fa[b].y + fb[b].y, fb[b].x - fa[b].x};
-        const cf wO = cmul(w, O);
-        const cf X = cadd(E, wO);
-        const cf Xn = {E.re - wO.re, wO.im - E.im};
-        const cf Yk = cmul(X, {sk[b].x, sk[b].y});
-        const cf Yn = cmul(Xn, {sn[b].x, sn[b].y});
-        const cf Ep = {Yk.re + Yn.re, Yk.im - Yn.im};
-        const cf Op = cmul({Yk.re - Yn.re, Yk.im + Yn.im}, cconj(w));
-        nxt[padded(k2)] = make_float2(Ep.re - Op.im, Ep.im + Op.re);
+      for (int b = 0; b < kB; ++b) {
+        const int p1 = tid + (q0 + b) * T;
+        const int p2 = mirror_local(p1);
+        const int ka = k1 + kC * p1;                     // bin of p1
+        const int kb = (int)mirrorRank + kC * p2;        // bin of p2 = n - ka (mod n)
+        buf[padded(p1)] = spectral_point(fa[b], fb[b], s1[b], s2[b], half_turn_twiddle<kLog>(ka));
+        if (!(k1 == 0 && p1 == 0)) {
+          const float2 o2 = spectral_point(fb[b], fa[b], s2[b], s1[b], half_turn_twiddle<kLog>(kb));
+          if (local_pair) buf[padded(p2)] = o2;
+          else st_cluster(mirrorBase + 8u * padded(p2), o2);
+        }
       }
     }
-    cluster_sync();  // mirror reads of `cur` done everywhere before it is reused
-    {
-      float2* t = cur;
-      cur = nxt;
-      nxt = t;
+    if (k1 == 0 && tid == 0) {  // bin n/2 at position nl/2 of CTA 0, paired with itself
+      const float2 f = buf[padded(nl / 2)];
+      const float2 sh = __ldg(&S[nl / 2]);
+      buf[padded(nl / 2)] = spectral_point(f, f, sh, sh, half_turn_twiddle<kLog>(n / 2));
     }
+    cluster_sync();  // every CTA's inputs of the inverse transform are written
+
     // ---- I2: local inverse FFT over k2 -> index i ----
-    local_fft<kLog, true>(cur, nxt, tw);
+    local_fft<kLog, true>(buf, tw);
     cluster_sync();
 
     // ---- I1: twiddle conj(W_n^{i k1}) and radix-8 inverse DFT across the cluster ----
-    const uint32_t cAddr = smem_addr(cur);
     float* yr = y + (size_t)row * L;
     const bool even = (L & 1) == 0;
     for (int ii = tid; ii < colsPer; ii += T) {
@@ -305,7 +326,7 @@ conv_cluster(const float* __restrict__ src, const float* __restrict__ src2, int 
       cf v[8];
 #pragma unroll
       for (int c = 0; c < kC; ++c) {
-        const float2 f = ld_cluster(map_rank(cAddr, c) + 8u * padded(i));
+        const float2 f = ld_cluster(map_rank(bufAddr, c) + 8u * padded(i));
         v[c] = c ? cmul({f.x, f.y}, w[c]) : cf{f.x, f.y};
       }
       fft::dft<8, true>(v);
@@ -330,7 +351,7 @@ template <int kLog, bool kSpectrum>
 cudaError_t launch_cluster(const float* src, const float* src2, int rows, int H, int L,
                            const float2* tw, float2* spec, float* y, cudaStream_t s) {
   using P = fftr::Plan<kLog>;
-  const size_t smem = 2 * P::buf_elems * sizeof(float2);
+  const size_t smem = P::buf_elems * sizeof(float2);
   cudaError_t e = max_smem_once<conv_cluster<kLog, kSpectrum>>(smem);
   if (e != cudaSuccess) return e;
   conv_cluster<kLog, kSpectrum><<<(unsigned)(rows * kC), P::T, smem, s>>>(src, src2, H, L, tw,
