@@ -39,7 +39,9 @@ typedef enum {
   DLR_ERR_UNSUPPORTED = 2, /* valid request outside what the kernels implement           */
   DLR_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed                 */
   DLR_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up (see dlr_get_device_status) */
-  DLR_ERR_WORKSPACE = 5    /* workspace missing or smaller than *_workspace_size()        */
+  DLR_ERR_WORKSPACE = 5,   /* workspace missing or smaller than *_workspace_size()        */
+  DLR_ERR_BOUNDS = 6       /* bounds-checked build only: an index outside its buffer was
+                              found and the access skipped (see dlr_bounds_site)           */
 } dlr_status;
 
 /* Kernel cast. DLR paper section 2: y_k = sum_{j<=k} Re(K_j) u_{k-j} (the Re cast);
@@ -348,6 +350,24 @@ dlr_status dlr_get_device_status(dlr_stream_t stream);
  * dlr_get_device_status() reports DLR_ERR_TIMEOUT and clears it. Returns DLR_OK once launched.
  */
 dlr_status dlr_selftest_timeout(int limit_ms, dlr_stream_t stream);
+
+/*
+ * The bounds-checked build. A library compiled with DLR_BOUNDS_CHECK checks the shared- and
+ * global-memory indices of its kernels' accesses: an index outside its buffer skips the access,
+ * records DLR_ERR_BOUNDS in the device status word (read by dlr_get_device_status) and the
+ * first failing site. It computes the same results as the normal build, more slowly; it
+ * stands in for a memory checker.
+ *   dlr_bounds_checked()     1 in the checked build, 0 otherwise.
+ *   dlr_bounds_site()        synchronise the device, return and clear the first failing site
+ *                            (file number * 100000 + source line; 0: none, -1: CUDA error).
+ *   dlr_selftest_bounds()    checked build: one kernel reads an element one past the end of a
+ *                            32-element buffer through the check, which skips it; the next
+ *                            dlr_get_device_status reports DLR_ERR_BOUNDS and dlr_bounds_site a
+ *                            nonzero site. Normal build: DLR_ERR_UNSUPPORTED, nothing launched.
+ */
+int dlr_bounds_checked(void);
+int dlr_bounds_site(void);
+dlr_status dlr_selftest_bounds(dlr_stream_t stream);
 
 /* Human-readable name of a status code (static storage, never NULL). */
 const char* dlr_status_string(dlr_status status);

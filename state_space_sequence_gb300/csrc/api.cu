@@ -8,6 +8,8 @@
 #include "dlr.h"
 
 namespace dlr {
+// source file number of the bounds-checked build's failing sites
+[[maybe_unused]] constexpr int kSiteFile = 1;
 cudaError_t launch_dlr_kernel(const float* log_re, const float* log_im, const float* W, int H,
                               int N, int L, bool re_im, float* K, int* status, cudaStream_t s);
 int conv_log2_size(int64_t L);
@@ -43,6 +45,7 @@ cudaError_t launch_s5_tv(const float* u, const float* dt, const float* lambda,
                          const float* D, int B, int L, int H, int P, float* y, void* ws,
                          int* status, cudaStream_t s);
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
+cudaError_t launch_selftest_bounds(cudaStream_t s);
 size_t grad_workspace_bytes(int64_t B, int64_t H, int64_t N);
 cudaError_t launch_dlr_grad_params(const float* u, const float* g, const float* log_re,
                                    const float* log_im, const float* W, int B, int H, int N,
@@ -58,8 +61,10 @@ cudaError_t launch_step(const float* u, int64_t B, int64_t H, int64_t N, int64_t
                         const void* ws, float* x, float* y, cudaStream_t s);
 }  // namespace dlr
 
-// The library's device status word (one per device that loads the library).
+// The library's device status word (one per device that loads the library), and the first
+// failing site of the bounds-checked build.
 __device__ int g_dlr_device_status = 0;
+__device__ int g_dlr_bounds_site = 0;
 
 namespace {
 // The last CUDA error a call of this thread turned into DLR_ERR_CUDA (for diagnostics).
@@ -130,7 +135,7 @@ dlr_status check_params(const float* log_re, const float* log_im, const float* W
 
 extern "C" {
 
-int dlr_abi_version(void) { return 9; }
+int dlr_abi_version(void) { return 10; }
 
 const char* dlr_last_cuda_error(void) { return t_last_cuda_error_msg; }
 
@@ -142,6 +147,7 @@ const char* dlr_status_string(dlr_status s) {
     case DLR_ERR_CUDA: return "DLR_ERR_CUDA";
     case DLR_ERR_TIMEOUT: return "DLR_ERR_TIMEOUT";
     case DLR_ERR_WORKSPACE: return "DLR_ERR_WORKSPACE";
+    case DLR_ERR_BOUNDS: return "DLR_ERR_BOUNDS";
   }
   return "DLR_ERR_UNKNOWN";
 }
@@ -654,6 +660,34 @@ dlr_status dlr_selftest_timeout(int limit_ms, dlr_stream_t stream) {
   if (!status) return DLR_ERR_CUDA;
   return from_cuda(dlr::launch_selftest_timeout((uint64_t)limit_ms * 1000000ull, status,
                                                 (cudaStream_t)stream));
+}
+
+int dlr_bounds_checked(void) {
+#ifdef DLR_BOUNDS_CHECK
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+int dlr_bounds_site(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_dlr_bounds_site, sizeof(int)) != cudaSuccess) return -1;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_dlr_bounds_site, &zero, sizeof(int)) != cudaSuccess) return -1;
+  }
+  return v;
+}
+
+dlr_status dlr_selftest_bounds(dlr_stream_t stream) {
+#ifdef DLR_BOUNDS_CHECK
+  return from_cuda(dlr::launch_selftest_bounds((cudaStream_t)stream));
+#else
+  (void)stream;
+  return DLR_ERR_UNSUPPORTED;
+#endif
 }
 
 dlr_status dlr_get_device_status(dlr_stream_t stream) {

@@ -24,7 +24,11 @@
 
 #include <cstdint>
 
+#include "dlr_common.cuh"
+
 namespace dlr {
+// source file number of the bounds-checked build's failing sites
+[[maybe_unused]] constexpr int kSiteFile = 2;
 
 namespace {
 
@@ -88,7 +92,8 @@ __global__ void __launch_bounds__(kGradWarps * 32)
     s1r += p1r;
     s1i += p1i;
   }
-  if (on) part[row * (int64_t)N + n] = make_float4(s0r, s0i, s1r, s1i);
+  if (on && DLR_IN(row * (int64_t)N + n, (int64_t)B * H * N))
+    part[row * (int64_t)N + n] = make_float4(s0r, s0i, s1r, s1i);
 }
 
 // Sum over the batch rows and the gradients: dW = (Re S0, -Im S0), d log_re = -2 a Re(W S1),
@@ -102,7 +107,9 @@ __global__ void dlr_grad_finish(const float4* __restrict__ part, const float* __
   const int64_t hn = i;
   double s0r = 0.0, s0i = 0.0, s1r = 0.0, s1i = 0.0;
   for (int b = 0; b < B; ++b) {
-    const float4 p = part[(int64_t)b * H * N + hn];
+    const float4 p = DLR_IN((int64_t)b * H * N + hn, (int64_t)B * H * N)
+                         ? part[(int64_t)b * H * N + hn]
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
     s0r += p.x;
     s0i += p.y;
     s1r += p.z;

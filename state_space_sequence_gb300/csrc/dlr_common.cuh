@@ -8,6 +8,12 @@
 
 #include "dlr.h"
 
+#ifdef DLR_BOUNDS_CHECK
+// the library's device status word and first failing site (defined once, in api.cu)
+extern __device__ int g_dlr_device_status;
+extern __device__ int g_dlr_bounds_site;
+#endif
+
 namespace dlr {
 
 struct cf {
@@ -115,6 +121,26 @@ __device__ __forceinline__ cff cff_fma(cff a, cff b, cff c) {
   ff im = ff_add(ff_add(ff_mul(a.re, b.im), ff_mul(a.im, b.re)), c.im);
   return {re, im};
 }
+
+// Index checks of the bounds-checked build. Compiled with DLR_BOUNDS_CHECK (relocatable device
+// code, so that every kernel reaches the same two device words), DLR_IN(i, n) is true when
+// 0 <= i < n; otherwise it records DLR_ERR_BOUNDS in the device status word and the first
+// failing site (kSiteFile * 100000 + source line, kSiteFile set per source file; headers use
+// DLR_IN_FILE with their own number) and returns false, and the guarded access is skipped. In
+// the normal build both are the constant true.
+#ifdef DLR_BOUNDS_CHECK
+__device__ __forceinline__ bool dlr_in(long long i, long long n, int site) {
+  if (i >= 0 && i < n) return true;
+  atomicMax(&::g_dlr_device_status, 6);  // DLR_ERR_BOUNDS
+  atomicCAS(&::g_dlr_bounds_site, 0, site);
+  return false;
+}
+#define DLR_IN(i, n) dlr_in((long long)(i), (long long)(n), kSiteFile * 100000 + __LINE__)
+#define DLR_IN_FILE(i, n, file) dlr_in((long long)(i), (long long)(n), (file) * 100000 + __LINE__)
+#else
+#define DLR_IN(i, n) true
+#define DLR_IN_FILE(i, n, file) true
+#endif
 
 // Kernels whose bounded waits run out record the reason in the library's device status
 // word (its address is passed to them as a kernel argument); dlr_get_device_status() reads

@@ -27,6 +27,8 @@
 #include "fft_rows.cuh"
 
 namespace dlr {
+// source file number of the bounds-checked build's failing sites
+[[maybe_unused]] constexpr int kSiteFile = 4;
 namespace {
 
 using fft::padded;
@@ -89,7 +91,8 @@ __device__ __forceinline__ void local_fft(float2* buf, const float2* __restrict_
       if (P::NB0 % P::T == 0 || j < P::NB0) {
 #pragma unroll
         for (int r = 0; r < P::R0; ++r) {
-          const float2 f = buf[padded(j + r * P::NB0)];
+          const float2 f = DLR_IN(padded(j + r * P::NB0), P::buf_elems) ? buf[padded(j + r * P::NB0)]
+                                                                        : make_float2(0.f, 0.f);
           a[q][r] = {f.x, f.y};
         }
         fft::dft<P::R0, kInv>(a[q]);
@@ -191,7 +194,8 @@ conv_cluster(const float* __restrict__ src, const float* __restrict__ src2, int 
       }
     }
 #pragma unroll
-    for (int q = 0; q < PER; ++q) buf[padded(tid + q * T)] = z[q];
+    for (int q = 0; q < PER; ++q)
+      if (DLR_IN(padded(tid + q * T), P::buf_elems)) buf[padded(tid + q * T)] = z[q];
   }
   cluster_sync();
 
@@ -244,8 +248,9 @@ conv_cluster(const float* __restrict__ src, const float* __restrict__ src2, int 
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
         const int k2 = tid + (q0 + b) * T;
-        fb[b] = ld_cluster(mirrorBase + 8u * padded(mirror_local(k2)));
-        fa[b] = buf[padded(k2)];
+        const bool in = DLR_IN(padded(mirror_local(k2)), P::buf_elems) && DLR_IN(padded(k2), P::buf_elems);
+        fb[b] = in ? ld_cluster(mirrorBase + 8u * padded(mirror_local(k2))) : make_float2(0.f, 0.f);
+        fa[b] = in ? buf[padded(k2)] : make_float2(0.f, 0.f);
       }
 #pragma unroll
       for (int b = 0; b < kBatch; ++b) {
@@ -255,7 +260,7 @@ conv_cluster(const float* __restrict__ src, const float* __restrict__ src2, int 
         const cf O = {0.5f * (fa[b].y + fb[b].y), -0.5f * (fa[b].x - fb[b].x)};
         const cf wO = cmul(half_turn_twiddle<kLog>(k), O);
         const cf Xk = cadd(E, wO);
-        out[k1 * nl + k2] = make_float2(Xk.re * scale, Xk.im * scale);
+        if (DLR_IN(k1 * nl + k2, n + 1)) out[k1 * nl + k2] = make_float2(Xk.re * scale, Xk.im * scale);
         if (k == 0) {  // X_n = E - O at k = 0
           const cf Xn = {E.re - wO.re, -(E.im - wO.im)};
           out[n] = make_float2(Xn.re * scale, Xn.im * scale);
@@ -284,10 +289,14 @@ conv_cluster(const float* __restrict__ src, const float* __restrict__ src2, int 
       for (int b = 0; b < kB; ++b) {
         const int p1 = tid + (q0 + b) * T;
         const int p2 = mirror_local(p1);
-        fa[b] = buf[padded(p1)];
-        fb[b] = local_pair ? buf[padded(p2)] : ld_cluster(mirrorBase + 8u * padded(p2));
-        s1[b] = __ldg(&S[k1 * nl + p1]);
-        s2[b] = __ldg(&S[(k1 == 0 && p1 == 0) ? n : (int)mirrorRank * nl + p2]);
+        const int i2 = (k1 == 0 && p1 == 0) ? n : (int)mirrorRank * nl + p2;
+        const bool in = DLR_IN(padded(p1), P::buf_elems) && DLR_IN(padded(p2), P::buf_elems) &&
+                        DLR_IN(k1 * nl + p1, n + 1) && DLR_IN(i2, n + 1);
+        fa[b] = in ? buf[padded(p1)] : make_float2(0.f, 0.f);
+        fb[b] = !in ? make_float2(0.f, 0.f)
+                    : local_pair ? buf[padded(p2)] : ld_cluster(mirrorBase + 8u * padded(p2));
+        s1[b] = in ? __ldg(&S[k1 * nl + p1]) : make_float2(0.f, 0.f);
+        s2[b] = in ? __ldg(&S[i2]) : make_float2(0.f, 0.f);
       }
 #pragma unroll
       for (int b = 0; b < kB; ++b) {
@@ -295,8 +304,9 @@ conv_cluster(const float* __restrict__ src, const float* __restrict__ src2, int 
         const int p2 = mirror_local(p1);
         const int ka = k1 + kC * p1;                     // bin of p1
         const int kb = (int)mirrorRank + kC * p2;        // bin of p2 = n - ka (mod n)
-        buf[padded(p1)] = spectral_point(fa[b], fb[b], s1[b], s2[b], half_turn_twiddle<kLog>(ka));
-        if (!(k1 == 0 && p1 == 0)) {
+        if (DLR_IN(padded(p1), P::buf_elems))
+          buf[padded(p1)] = spectral_point(fa[b], fb[b], s1[b], s2[b], half_turn_twiddle<kLog>(ka));
+        if (!(k1 == 0 && p1 == 0) && DLR_IN(padded(p2), P::buf_elems)) {
           const float2 o2 = spectral_point(fb[b], fa[b], s2[b], s1[b], half_turn_twiddle<kLog>(kb));
           if (local_pair) buf[padded(p2)] = o2;
           else st_cluster(mirrorBase + 8u * padded(p2), o2);

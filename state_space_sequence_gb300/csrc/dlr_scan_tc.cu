@@ -75,6 +75,8 @@
 #include "tc_ptx.cuh"
 
 namespace dlr {
+// source file number of the bounds-checked build's failing sites
+[[maybe_unused]] constexpr int kSiteFile = 10;
 
 // Timeline hooks of profiling builds (compiled with DLR_SCAN_TRACE: CTA 0 records the global
 // timer at fixed points into a device buffer the caller provides); no code otherwise.
@@ -265,13 +267,15 @@ __device__ __forceinline__ float block_max_tb(float v, float* red, int slot) {
 // Eight values of one K-major row of an f16 operand tile pair (16-byte chunk `chunk`), at a
 // shared or global address.
 __device__ __forceinline__ void store_chunk8(uint8_t* hi_tile, uint8_t* lo_tile, int row,
-                                             int chunk, const float* v) {
+                                             int chunk, const float* v, int rows) {
   uint32_t h[4], l[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) split2(v[2 * q], v[2 * q + 1], h[q], l[q]);
   const uint32_t off = uint32_t(row) * 128u + ((uint32_t(chunk) ^ uint32_t(row & 7)) << 4);
-  *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
-  *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  if (DLR_IN(row, rows) && DLR_IN(chunk, 8)) {
+    *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
 }
 
 // Where tile k of this CTA lies: channel, first batch row and row count, segment of the row.
@@ -450,8 +454,10 @@ __global__ void __launch_bounds__(kTbThreads, 2)
       split2((c ? p0.im : p0.re) * 16384.f, (c ? p1.im : p1.re) * 16384.f, hi[m], lo[m]);
     }
     uint4* row = reinterpret_cast<uint4*>(img + kBlobQ + (2 * n + c) * 256);
-    row[7 - q] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-    row[15 - q] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    if (DLR_IN(2 * n + c, 128) && DLR_IN(15 - q, 16) && DLR_IN(7 - q, 8)) {
+      row[7 - q] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      row[15 - q] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
   }
   // G rows t = 8q .. 8q + 7, columns 2n, 2n+1: Re, -Im of W_n lambda_n^{t+1}; and the products'
   // real parts for the tap sums
@@ -468,9 +474,12 @@ __global__ void __launch_bounds__(kTbThreads, 2)
       uint32_t hb, lb;
       split2(g.re * sig_g, -g.im * sig_g, hb, lb);
       const uint32_t off = uint32_t(t) * 128u + ((chunk ^ uint32_t(t & 7)) << 4) + colb;
-      *reinterpret_cast<uint32_t*>(gh + off) = hb;
-      *reinterpret_cast<uint32_t*>(gl + off) = lb;
-      sKp[n * 65 + 8 * q + i] = cmul({w.x, w.y}, pw[i]).re;  // Re(W lambda^j), j = 8q + i
+      if (DLR_IN(kb * 8192 + off + 3, 16384)) {
+        *reinterpret_cast<uint32_t*>(gh + off) = hb;
+        *reinterpret_cast<uint32_t*>(gl + off) = lb;
+      }
+      if (DLR_IN(n * 65 + 8 * q + i, 64 * 65))
+        sKp[n * 65 + 8 * q + i] = cmul({w.x, w.y}, pw[i]).re;  // Re(W lambda^j), j = 8q + i
     }
   }
   // lambda^64 and the re-anchoring correction (warps 14 and 15: q = 7 holds lambda^64)
@@ -486,7 +495,8 @@ __global__ void __launch_bounds__(kTbThreads, 2)
       const ff di = ff_add(ff{a32.im, 0.f}, ff_neg(pp.im));
       d = make_float2(dr.hi + dr.lo, di.hi + di.lo);
     }
-    reinterpret_cast<float4*>(img + kBlobMu)[n] = make_float4(m.re, m.im, d.x, d.y);
+    if (DLR_IN(n, 64))
+      reinterpret_cast<float4*>(img + kBlobMu)[n] = make_float4(m.re, m.im, d.x, d.y);
   }
   if (tid == 0) SCAN_TRACE(3902);
   __syncthreads();
@@ -495,11 +505,12 @@ __global__ void __launch_bounds__(kTbThreads, 2)
   const int j = tid >> 3, part = tid & 7;
   float ks = 0.f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) ks += sKp[(8 * part + i) * 65 + j];
+  for (int i = 0; i < 8; ++i)
+    if (DLR_IN((8 * part + i) * 65 + j, 64 * 65)) ks += sKp[(8 * part + i) * 65 + j];
   ks += __shfl_xor_sync(0xffffffffu, ks, 1);
   ks += __shfl_xor_sync(0xffffffffu, ks, 2);
   ks += __shfl_xor_sync(0xffffffffu, ks, 4);
-  if (part == 0) sK[j] = ks;
+  if (part == 0 && DLR_IN(j, 64)) sK[j] = ks;
   const float sig_k = exp2i(scale_exp(block_max_tb(part == 0 ? fabsf(ks) : 0.f, sRed, 1)));
   if (tid == 0) {
     reinterpret_cast<float*>(img + kBlobSig)[0] = sig_k;
@@ -511,9 +522,9 @@ __global__ void __launch_bounds__(kTbThreads, 2)
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int ss = 8 * part + i;
-    tv[i] = (ss <= j) ? sK[j - ss] * sig_k : 0.f;
+    tv[i] = (ss <= j && DLR_IN(j - ss, 64)) ? sK[j - ss] * sig_k : 0.f;
   }
-  store_chunk8(img, img + (kTkLo - kTkHi), j, part, tv);
+  store_chunk8(img, img + (kTkLo - kTkHi), j, part, tv, 64);
   // the image to the channel's blob
   tc::fence_proxy_async_smem();
   __syncthreads();
@@ -600,7 +611,7 @@ __device__ __forceinline__ void load_part32(const float* __restrict__ row, int L
 // main warps, at the first tile of a channel: half h of Q of the channel (the hi words for
 // h = 0, the lo words for h = 1) from its blob into TMEM (thread = lane r of its quarter).
 __device__ __forceinline__ void load_q_half(const uint8_t* blob, uint32_t tmem, int r, int h) {
-  const uint4* q = reinterpret_cast<const uint4*>(blob + kBlobQ + r * 256) + 8 * h;
+  const uint4* q = reinterpret_cast<const uint4*>(blob + kBlobQ + (DLR_IN(r, 128) ? r : 0) * 256) + 8 * h;
   const uint32_t tl = tmem + (uint32_t(r & ~31) << 16) + kTQ + 32 * h;
 #pragma unroll
   for (int part = 0; part < 2; ++part) {
@@ -645,7 +656,9 @@ __device__ __forceinline__ bool conv_tile(const TcScanArgs& a, uint8_t* sm, uint
     const uint8_t* src = ubuf + (kRev ? 1 - h : h) * 16384 + line * 128;
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
-      const float4 x = *reinterpret_cast<const float4*>(src + ((uint32_t(q) ^ sw) << 4));
+      const float4 x = DLR_IN(line, 128)
+                           ? *reinterpret_cast<const float4*>(src + ((uint32_t(q) ^ sw) << 4))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
       if (!kRev) {
         v[4 * q] = x.x; v[4 * q + 1] = x.y; v[4 * q + 2] = x.z; v[4 * q + 3] = x.w;
       } else {
@@ -669,19 +682,19 @@ __device__ __forceinline__ bool conv_tile(const TcScanArgs& a, uint8_t* sm, uint
   const bool warp_row = __shfl_sync(0xffffffffu, rl, 0) == __shfl_sync(0xffffffffu, rl, 31);
   if (warp_row) {
     const unsigned mw = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
-    if (lane == 0) atomicMax(&rmax[rl], mw);
+    if (lane == 0 && DLR_IN(rl, 128)) atomicMax(&rmax[rl], mw);
   } else {
-    atomicMax(&rmax[rl], __float_as_uint(m));
+    if (DLR_IN(rl, 128)) atomicMax(&rmax[rl], __float_as_uint(m));
   }
   named_bar(kMainBar, 256);
-  const int es = scale_exp(__uint_as_float(rmax[rl]));
+  const int es = scale_exp(__uint_as_float(DLR_IN(rl, 128) ? rmax[rl] : 0u));
   const float su = exp2i(es);
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
     float w8[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) w8[i] = v[8 * p + i] * su;
-    store_chunk8(ubuf, ubuf + kULo, g, 4 * h + p, w8);
+    store_chunk8(ubuf, ubuf + kULo, g, 4 * h + p, w8, 128);
   }
   if (new_channel) {
     // the first read of the tables: at the CTA's first tile, wait here for the table kernel
@@ -691,8 +704,10 @@ __device__ __forceinline__ bool conv_tile(const TcScanArgs& a, uint8_t* sm, uint
     sig_k = __ldg(reinterpret_cast<const float*>(blob + kBlobSig));
   }
   if (h == 0) {
-    if (ci.c == 0 || g == 0) reinterpret_cast<int*>(sm + kRowEs)[slot * 128 + rl] = es;
-    reinterpret_cast<float*>(sm + kAy)[slot * 128 + g] = exp2i(-es) / sig_k;
+    if ((ci.c == 0 || g == 0) && DLR_IN(slot * 128 + rl, 512))
+      reinterpret_cast<int*>(sm + kRowEs)[slot * 128 + rl] = es;
+    if (DLR_IN(slot * 128 + g, 512))
+      reinterpret_cast<float*>(sm + kAy)[slot * 128 + g] = exp2i(-es) / sig_k;
   }
   tc::fence_proxy_async_smem();
   if (new_channel) {
@@ -786,13 +801,20 @@ __device__ __forceinline__ bool epi_tile(const TcScanArgs& a, const CUtensorMap*
   tc::fence_after_sync();
   const uint32_t lane_base = tmem + (uint32_t(quarter * 32) << 16);
   float y1[32], y2[32];
-  tc::tmem_ld32(lane_base + kTY1 + par * 64 + 32 * h, y1);
-  tc::tmem_ld32(lane_base + kTY2 + 32 * h, y2);
+  // (the TMEM column ranges are uniform over the warp: a failed check skips the warp's loads)
+  if (DLR_IN(kTY1 + par * 64 + 32 * h + 31, kTmemCols) && DLR_IN(kTY2 + 32 * h + 31, kTmemCols)) {
+    tc::tmem_ld32(lane_base + kTY1 + par * 64 + 32 * h, y1);
+    tc::tmem_ld32(lane_base + kTY2 + 32 * h, y2);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) y1[i] = y2[i] = 0.f;
+  }
   tc::fence_before_sync();
   tc::mbar_arrive(&bars[kBarY1Free + par]);
   tc::mbar_arrive(&bars[kBarY2Free]);
-  const float ay = reinterpret_cast<const float*>(sm + kAy)[slot * 128 + g];
-  const float by = reinterpret_cast<const float*>(sm + kBy)[slot * 128 + g];
+  const bool sc_in = DLR_IN(slot * 128 + g, 512);
+  const float ay = sc_in ? reinterpret_cast<const float*>(sm + kAy)[slot * 128 + g] : 0.f;
+  const float by = sc_in ? reinterpret_cast<const float*>(sm + kBy)[slot * 128 + g] : 0.f;
   float y[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) y[i] = fmaf(y1[i], ay, y2[i] * by);
@@ -808,7 +830,8 @@ __device__ __forceinline__ bool epi_tile(const TcScanArgs& a, const CUtensorMap*
       const float4 v = kRev ? make_float4(y[31 - 4 * q], y[30 - 4 * q], y[29 - 4 * q],
                                           y[28 - 4 * q])
                             : make_float4(y[4 * q], y[4 * q + 1], y[4 * q + 2], y[4 * q + 3]);
-      *reinterpret_cast<float4*>(stg + line * 128 + ((uint32_t(q) ^ sw) << 4)) = v;
+      if (DLR_IN(warp * 4096 + line * 128 + 127, 8 * 4096))
+        *reinterpret_cast<float4*>(stg + line * 128 + ((uint32_t(q) ^ sw) << 4)) = v;
     }
     tc::fence_proxy_async_smem();
     __syncwarp();
@@ -988,8 +1011,10 @@ __device__ __forceinline__ void store_xin8(uint8_t* sm, int r, int g0, const flo
 #pragma unroll
   for (int q = 0; q < 4; ++q) split2(v[2 * q] * s, v[2 * q + 1] * s, h[q], l[q]);
   const uint32_t off = xin_chunk(r, g0);
-  *reinterpret_cast<uint4*>(sm + kXHi + off) = make_uint4(h[0], h[1], h[2], h[3]);
-  *reinterpret_cast<uint4*>(sm + kXLo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  if (DLR_IN(off + 15, kXLo - kXHi)) {
+    *reinterpret_cast<uint4*>(sm + kXHi + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(sm + kXLo + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
 }
 
 // main warps, chain of tile k. Thread r owns TMEM lane r = state row r (lane quarter warp & 3)
@@ -1009,6 +1034,8 @@ __device__ __forceinline__ void chain_run(const TcScanArgs& a, uint8_t* sm, uint
                                           const ChainConst& q, float xscale, int c_begin,
                                           int c_store, int c_end, float& xo, float& xt,
                                           float& ao, float& at) {
+  // the S columns read lie in TMEM (uniform over the warp; a failed check skips the chain)
+  if (!DLR_IN(int(tS & 0xFFFFu) + c_end - 1, int(kTmemCols))) return;
   const int c_store_end = c_store + 64;
   int next_reset, next_anchor;
   if (a.R > 0) {
@@ -1078,6 +1105,7 @@ __device__ __forceinline__ void chain_run(const TcScanArgs& a, uint8_t* sm, uint
 // recurrence of the later ones.
 __device__ __forceinline__ void chain64(uint8_t* sm, uint32_t tS, int r, int C,
                                         const ChainConst& q, float xscale, int c0) {
+  if (!DLR_IN(int(tS & 0xFFFFu) + c0 + 63, int(kTmemCols))) return;
   uint32_t s0[16], s1[16], s2[16], s3[16];
   tc::tmem_ld16_issue(tS + c0, s0);
   tc::tmem_ld16_issue(tS + c0 + 16, s1);
@@ -1143,7 +1171,7 @@ __device__ __forceinline__ bool chain_tile(const TcScanArgs& a, uint8_t* sm, uin
     }
     es_prev = es;
     const unsigned mw = __reduce_max_sync(0xffffffffu, __float_as_uint(fmaxf(fabsf(xo), fabsf(xt))));
-    if (lane == 0 && h == 0) sRed[quarter] = mw;
+    if (lane == 0 && h == 0 && DLR_IN(quarter, 4)) sRed[quarter] = mw;
     named_bar(kMainBar, 256);
     const unsigned m = max(max(sRed[0], sRed[1]), max(sRed[2], sRed[3]));
     const int e = int((m >> 23) & 0xFFu) - 126;  // carried |state| < 2^e
@@ -1154,7 +1182,7 @@ __device__ __forceinline__ bool chain_tile(const TcScanArgs& a, uint8_t* sm, uin
   if (h == 0) {
     // y = Y2 * 2^(xs - 14 - es) / sig_g for the column's row
     const int row = (a.R > 0) ? r / a.C : 0;
-    reinterpret_cast<float*>(sm + kBy)[slot * 128 + r] =
+    if (DLR_IN(slot * 128 + r, 512)) reinterpret_cast<float*>(sm + kBy)[slot * 128 + r] =
         exp2i(xs - kXinShift) * exp2i(kXinShift - 14 - sRowEs[row]) / sig_g;
   }
   const float xscale = exp2i(-xs);
@@ -1226,7 +1254,8 @@ __device__ __forceinline__ void main_role(const TcScanArgs& a, const CUtensorMap
       // imaginary parts flipped.
       chain_h = ti.h;
       const uint8_t* blob = a.tables + (size_t)ti.h * kBlobBytes;
-      const float4 m = __ldg(reinterpret_cast<const float4*>(blob + kBlobMu) + (r >> 1));
+      const float4 m =
+          __ldg(reinterpret_cast<const float4*>(blob + kBlobMu) + (DLR_IN(r >> 1, 64) ? r >> 1 : 0));
       q.mu_re = m.x;
       q.dl_re = m.z;
       q.mu_im = (r & 1) ? -m.y : m.y;

@@ -32,6 +32,8 @@
 #include "dlr_common.cuh"
 
 namespace dlr {
+// source file number of the bounds-checked build's failing sites
+[[maybe_unused]] constexpr int kSiteFile = 11;
 int conv_log2_size(int64_t L);
 cudaError_t launch_twiddles(int lg, void* ws, cudaStream_t s);  // dlr_conv.cu
 
@@ -158,7 +160,7 @@ __global__ void __launch_bounds__(kSpecThreads)
     const int nl = n >> 3;
     idx = (size_t)(k & 7) * nl + (k >> 3);
   }
-  spec[(size_t)h * (n + 1) + idx] = make_float2(cre * scale, cim * scale);
+  if (DLR_IN(idx, n + 1)) spec[(size_t)h * (n + 1) + idx] = make_float2(cre * scale, cim * scale);
 }
 
 }  // namespace

@@ -22,9 +22,13 @@
 // time) takes a plain warp sum instead. The state goes back to x at the end.
 #include <cuda_runtime.h>
 
+#include "dlr_common.cuh"
+
 #include <cstdint>
 
 namespace dlr {
+// source file number of the bounds-checked build's failing sites
+[[maybe_unused]] constexpr int kSiteFile = 12;
 
 namespace {
 
@@ -96,7 +100,7 @@ dlr_step_kernel(const float* __restrict__ u, const float4* __restrict__ lam,
       float acc = advance(__shfl_sync(0xffffffffu, uv, 0));  // u_t is in lane 0
 #pragma unroll
       for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      if (lane == 0) yr[t0] = acc;
+      if (lane == 0 && DLR_IN(t0, T)) yr[t0] = acc;
       continue;
     }
     float p[32];
@@ -123,7 +127,7 @@ dlr_step_kernel(const float* __restrict__ u, const float4* __restrict__ lam,
         p[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
       }
     }
-    if (lane < nt) yr[t0 + lane] = p[0];
+    if (lane < nt && DLR_IN(t0 + lane, T)) yr[t0 + lane] = p[0];
   }
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {

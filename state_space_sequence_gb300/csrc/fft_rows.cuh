@@ -16,6 +16,8 @@
 namespace dlr {
 namespace fftr {
 
+constexpr int kSiteFileRows = 21;  // bounds-checked build: this header's site number
+
 using fft::padded;
 using fft::padded_size;
 
@@ -90,13 +92,16 @@ __device__ __forceinline__ void pass16_load_compute(const float2* src, int ns,
         const float2* s0 = src + padded(j);  // padded(j + r NB) = padded(j) + r * 17 NB / 16
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-          float2 f = s0[r * (P::NB16 + P::NB16 / 16)];
+          const int e = padded(j) + r * (P::NB16 + P::NB16 / 16);
+          float2 f = DLR_IN_FILE(e, P::buf_elems, kSiteFileRows) ? s0[r * (P::NB16 + P::NB16 / 16)]
+                                                                 : make_float2(0.f, 0.f);
           v[q][r] = {f.x, f.y};
         }
       } else {
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
-          float2 f = src[padded(j + r * P::NB16)];
+          const int e = padded(j + r * P::NB16);
+          float2 f = DLR_IN_FILE(e, P::buf_elems, kSiteFileRows) ? src[e] : make_float2(0.f, 0.f);
           v[q][r] = {f.x, f.y};
         }
       }
@@ -121,11 +126,14 @@ __device__ __forceinline__ void pass16_store(float2* dst, int ns,
         float2* d0 = dst + padded(d);
         const int st = ns + (ns >> 4);
 #pragma unroll
-        for (int r = 0; r < 16; ++r) d0[r * st] = make_float2(v[q][r].re, v[q][r].im);
+        for (int r = 0; r < 16; ++r)
+          if (DLR_IN_FILE(padded(d) + r * st, P::buf_elems, kSiteFileRows))
+            d0[r * st] = make_float2(v[q][r].re, v[q][r].im);
       } else {
 #pragma unroll
         for (int r = 0; r < 16; ++r)
-          dst[padded(d + r * ns)] = make_float2(v[q][r].re, v[q][r].im);
+          if (DLR_IN_FILE(padded(d + r * ns), P::buf_elems, kSiteFileRows))
+            dst[padded(d + r * ns)] = make_float2(v[q][r].re, v[q][r].im);
       }
     }
   }
@@ -141,7 +149,9 @@ __device__ __forceinline__ void pass0_store(float2* dst, const cf (&a)[Plan<kLog
       // R0 divides 16, so padded(j R0 + r) = padded(j R0) + r for r < R0
       float2* d0 = dst + padded(j * P::R0);
 #pragma unroll
-      for (int r = 0; r < P::R0; ++r) d0[r] = make_float2(a[q][r].re, a[q][r].im);
+      for (int r = 0; r < P::R0; ++r)
+        if (DLR_IN_FILE(padded(j * P::R0) + r, P::buf_elems, kSiteFileRows))
+          d0[r] = make_float2(a[q][r].re, a[q][r].im);
     }
   }
 }

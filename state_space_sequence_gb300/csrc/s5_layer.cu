@@ -27,6 +27,8 @@
 #include "dlr_common.cuh"
 
 namespace dlr {
+// source file number of the bounds-checked build's failing sites
+[[maybe_unused]] constexpr int kSiteFile = 13;
 namespace {
 
 constexpr int kT = 64;   // steps per chunk
@@ -169,7 +171,9 @@ s5_chunk_state(S5Work w, int L, int P, int NC) {
       float2 v[kBatch], a[kBatch];
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) {
-        const bool in = tb + j < valid;
+        const bool in = tb + j < valid &&
+                        DLR_IN(col + (size_t)(tb + j) * P, (size_t)gridDim.y * L * P) &&
+                        DLR_IN((size_t)(kT - 1 - tb - j) * P + p, (size_t)(kT + 1) * P);
         v[j] = in ? reinterpret_cast<const float2*>(w.xv)[col + (size_t)(tb + j) * P]
                   : make_float2(0.f, 0.f);
         a[j] = in ? w.lbar_pw[(size_t)(kT - 1 - tb - j) * P + p] : make_float2(0.f, 0.f);
@@ -177,7 +181,8 @@ s5_chunk_state(S5Work w, int L, int P, int NC) {
 #pragma unroll
       for (int j = 0; j < kBatch; ++j) acc = cfma({a[j].x, a[j].y}, {v[j].x, v[j].y}, acc);
     }
-    w.S[((size_t)b * NC + c) * P + p] = make_float2(acc.re, acc.im);
+    if (DLR_IN(((size_t)b * NC + c) * P + p, (size_t)gridDim.y * NC * P))
+      w.S[((size_t)b * NC + c) * P + p] = make_float2(acc.re, acc.im);
   }
 }
 
@@ -280,7 +285,8 @@ s5_carry_groups(S5Work w, int B, int P, int NC) {
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         if (cb + q >= c1) break;
-        if (store) w.Xin[base + (size_t)(cb + q) * P] = make_float2(x.re, x.im);
+        if (store && DLR_IN(base + (size_t)(cb + q) * P, (size_t)B * NC * P))
+          w.Xin[base + (size_t)(cb + q) * P] = make_float2(x.re, x.im);
         x = cfma(m, x, sv[q]);
       }
     }
@@ -319,7 +325,8 @@ s5_chunk_apply(S5Work w, int L, int P, int NC) {
     auto fetch = [&](int buf, int tb) {
 #pragma unroll
       for (int j = 0; j < kB; ++j) {
-        const bool in = tb + j < valid;
+        const bool in = tb + j < valid && DLR_IN(tb + j + 1, kT + 1) &&
+                        DLR_IN(((size_t)b * L + t0 + tb + j) * P + p, (size_t)gridDim.y * L * P);
         v[buf][j] = in ? row[(size_t)(tb + j) * P] : make_float2(0.f, 0.f);
         a[buf][j] = in ? w.lbar_pw[(size_t)(tb + j + 1) * P + p] : make_float2(0.f, 0.f);
       }
@@ -337,7 +344,8 @@ s5_chunk_apply(S5Work w, int L, int P, int NC) {
           if (tc + j >= valid) break;
           l = cfma(lam, l, {v[half][j].x, v[half][j].y});
           const cf x = cfma({a[half][j].x, a[half][j].y}, xin, l);
-          row[(size_t)(tc + j) * P] = make_float2(x.re, x.im);
+          if (DLR_IN(((size_t)b * L + t0 + tc + j) * P + p, (size_t)gridDim.y * L * P))
+            row[(size_t)(tc + j) * P] = make_float2(x.re, x.im);
         }
       }
     }
@@ -407,7 +415,10 @@ s5_chunk16(S5Work w, int B, int L, int P, int NC) {
   auto fetch = [&](int buf, int tb) {
 #pragma unroll
     for (int j = 0; j < kB; ++j)
-      v[buf][j] = tb + j < valid ? row[(size_t)(tb + j) * stride] : make_uint4(0, 0, 0, 0);
+      v[buf][j] = (tb + j < valid &&
+                   DLR_IN(((size_t)q.b * L + t0 + tb + j) * P + q.p0 + 3, (size_t)B * L * P))
+                      ? row[(size_t)(tb + j) * stride]
+                      : make_uint4(0, 0, 0, 0);
   };
   fetch(0, 0);
 #pragma unroll 1
@@ -424,14 +435,16 @@ s5_chunk16(S5Work w, int B, int L, int P, int NC) {
         unpack4(v[half][j], vin);
 #pragma unroll
         for (int k = 0; k < 4; ++k) x[k] = cfma(lam[k], x[k], vin[k]);
-        if (kApply) row[(size_t)(tc + j) * stride] = pack4(x);
+        if (kApply && DLR_IN(((size_t)q.b * L + t0 + tc + j) * P + q.p0 + 3, (size_t)B * L * P))
+          row[(size_t)(tc + j) * stride] = pack4(x);
       }
     }
   }
   if (!kApply) {
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      w.S[((size_t)q.b * NC + q.c) * P + q.p0 + k] = make_float2(x[k].re, x[k].im);
+      if (DLR_IN(((size_t)q.b * NC + q.c) * P + q.p0 + k, (size_t)B * NC * P))
+        w.S[((size_t)q.b * NC + q.c) * P + q.p0 + k] = make_float2(x[k].re, x[k].im);
   }
 }
 
@@ -541,9 +554,10 @@ __global__ void s5tv_chunks(float* __restrict__ xv, const float* __restrict__ dt
   for (int k = k0; k < k1; ++k) {
     cf a, f;
     s5tv_coef(s0, s1, __ldg(dtr + k), a, f);
-    const float2 vk = v[(int64_t)k * P];
+    const bool in = DLR_IN(((int64_t)b * L + k) * P + p, (int64_t)B * L * P);
+    const float2 vk = in ? v[(int64_t)k * P] : make_float2(0.f, 0.f);
     x = cfma(a, x, cmul(f, cf{vk.x, vk.y}));
-    if (kApply) v[(int64_t)k * P] = make_float2(x.re, x.im);
+    if (kApply && in) v[(int64_t)k * P] = make_float2(x.re, x.im);
   }
   if (!kApply) S[i] = make_float2(x.re, x.im);
 }
@@ -561,6 +575,7 @@ __global__ void s5tv_carry(const float* __restrict__ dt, const float4* __restric
   cf X = {0.f, 0.f};
   for (int c = 0; c < NC; ++c) {
     const int64_t o = ((int64_t)b * NC + c) * P + p;
+    if (!DLR_IN(o, (int64_t)B * NC * P)) break;
     Xin[o] = make_float2(X.re, X.im);
     ff tau = {0.f, 0.f};
     const int k0 = c * kT, k1 = min(L, k0 + kT);

@@ -37,6 +37,8 @@
 #include "tc_ptx.cuh"
 
 namespace dlr {
+// source file number of the bounds-checked build's failing sites
+[[maybe_unused]] constexpr int kSiteFile = 14;
 namespace {
 
 constexpr int kBM = 128, kBN = 256;
@@ -230,9 +232,11 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
                               *reinterpret_cast<const uint32_t*>(&b2),
                               *reinterpret_cast<const uint32_t*>(&b3));
           }
+          if (DLR_IN(r, kBM)) {
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(f + ((uint32_t(c) ^ sw) << 4)) = h[c];
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4*>(f + ((uint32_t(c) ^ sw) << 4)) = h[c];
+          }
           tc::fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(&a_ready[s]);
@@ -277,7 +281,7 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
             uint32_t v[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const int i = i0 + j;
+              const int i = DLR_IN(i0 + j, kBM) ? i0 + j : 0;
               ptr[j] = reinterpret_cast<uint32_t*>(a + i * kRowBytes +
                                                    ((chunk ^ uint32_t(i & 7)) << 4) + sub);
               v[j] = *ptr[j];
@@ -406,8 +410,9 @@ tc_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtenso
                 acc = cfma(lam, acc, {vf.x, vf.y});
               }
               const int b = m / g.L, t = m - b * g.L;
-              g.sums[(((size_t)b * g.NC + (t >> 6)) * 2 + ((t >> 5) & 1)) * g.P + p] =
-                  make_float2(acc.re, acc.im);
+              const size_t si = (((size_t)b * g.NC + (t >> 6)) * 2 + ((t >> 5) & 1)) * g.P + p;
+              if (DLR_IN(si, (size_t)(g.M / g.L) * g.NC * 2 * g.P))
+                g.sums[si] = make_float2(acc.re, acc.im);
             }
           }
         } else if (with_e) {
@@ -563,7 +568,7 @@ tc_gemm_x3(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
       for (int kb = 0; kb < nk && ok; ++kb, ++it) {
         const int s = it % kStages;
         if (!(ok = warp_wait(&full[s], (it / kStages) & 1))) break;
-        uint8_t* row = base + s * kStride + r * 128;
+        uint8_t* row = base + s * kStride + (DLR_IN(r, kBM) ? r : 0) * 128;
         uint4 v[8];
 #pragma unroll
         for (int c = 0; c < 8; ++c)
@@ -628,7 +633,8 @@ tc_gemm_x3(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
       auto load_e = [&](int c, float4 (&dst)[8]) {
 #pragma unroll
         for (int k = 0; k < 8; ++k) dst[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (kWithE && m < g.M && c < ns) {
+        if (kWithE && m < g.M && c < ns &&
+            DLR_IN((size_t)m * g.N + n0 + 32 * c + 31, (size_t)g.M * g.N)) {
           const float4* src =
               reinterpret_cast<const float4*>(g.E + (size_t)m * g.N + n0 + 32 * c);
 #pragma unroll
@@ -654,7 +660,10 @@ tc_gemm_x3(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
         for (int k = 0; k < 8; ++k) {
           float4 o = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
           if (kWithE) {
-            const float4 dk = __ldg(reinterpret_cast<const float4*>(g.D + n0 + 32 * c + 4 * k));
+            const float4 dk =
+                DLR_IN(n0 + 32 * c + 4 * k + 3, g.N)
+                    ? __ldg(reinterpret_cast<const float4*>(g.D + n0 + 32 * c + 4 * k))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
             o.x = fmaf(dk.x, e[k].x, o.x);
             o.y = fmaf(dk.y, e[k].y, o.y);
             o.z = fmaf(dk.z, e[k].z, o.z);
@@ -679,6 +688,20 @@ tc_gemm_x3(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUte
   __syncthreads();
   if (warp == 2) tc::tmem_dealloc(tmem, kTmemCols);
 }
+
+#ifdef DLR_BOUNDS_CHECK
+// Bounds-check self-test: thread t of one warp reads element t + 1 of a 32-element shared
+// buffer through the check, so thread 31's read (one past the end) is skipped and reported.
+__global__ void selftest_bounds_kernel(float* sink) {
+  __shared__ float buf[32];
+  const int t = threadIdx.x;
+  buf[t] = (float)t;
+  __syncwarp();
+  float v = 0.f;
+  if (DLR_IN(t + 1, 32)) v = buf[t + 1];
+  if (v < 0.f) *sink = v;  // never true; keeps the read
+}
+#endif
 
 // Failure-reporting self-test: one thread waits on a barrier that nothing completes.
 __global__ void selftest_wait_timeout(uint64_t limit_ns, int* status) {
@@ -737,6 +760,13 @@ cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t
   selftest_wait_timeout<<<1, 32, 0, s>>>(limit_ns, status);
   return cudaGetLastError();
 }
+
+#ifdef DLR_BOUNDS_CHECK
+cudaError_t launch_selftest_bounds(cudaStream_t s) {
+  selftest_bounds_kernel<<<1, 32, 0, s>>>(nullptr);
+  return cudaGetLastError();
+}
+#endif
 
 // A: [M, K] row-major, bf16 (a_f32 false) or float32 (a_f32, converted to bf16 in the
 // kernel); B: bf16 [N, K] row-major. C: [M, N], f32 or (c_bf16, no D) bf16; D: f32 [N] or

@@ -32,10 +32,16 @@ class DLRError(RuntimeError):
         self.status = status
 
 
+def _checked() -> bool:
+    """The bounds-checked library is loaded instead of the normal one when the environment
+    variable DLR_BOUNDS_CHECK is 1 at the first call."""
+    return os.environ.get("DLR_BOUNDS_CHECK", "0") == "1"
+
+
 def _load():
     global _lib
     if _lib is None:
-        path = _build.build()
+        path = _build.build(checked=_checked())
         lib = ctypes.CDLL(path)
         P, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
         lib.dlr_kernel.argtypes = [P, P, P, i64, i64, i64, i32, P, P]
@@ -98,15 +104,35 @@ def _load():
         lib.dlr_status_string.argtypes = [i32]
         lib.dlr_status_string.restype = ctypes.c_char_p
         lib.dlr_abi_version.restype = i32
+        lib.dlr_bounds_checked.restype = i32
+        lib.dlr_bounds_site.restype = i32
+        lib.dlr_selftest_bounds.argtypes = [P]
+        lib.dlr_selftest_bounds.restype = i32
         lib.dlr_last_cuda_error.restype = ctypes.c_char_p
         _lib = lib
     return _lib
 
 
 def library_path() -> str:
-    """Absolute path of the loaded libdlr.so (loads it if needed)."""
+    """Absolute path of the loaded library (loads it if needed)."""
     _load()
-    return os.path.abspath(_build.LIB)
+    return os.path.abspath(_build.LIB_CHECKED if _checked() else _build.LIB)
+
+
+def bounds_checked() -> bool:
+    """True when the loaded library is the bounds-checked build."""
+    return bool(_load().dlr_bounds_checked())
+
+
+def bounds_site() -> int:
+    """Synchronise; return and clear the first failing site of the bounds-checked build
+    (file number * 100000 + source line; 0 if none)."""
+    return int(_load().dlr_bounds_site())
+
+
+def selftest_bounds(stream=None) -> None:
+    """Checked build: run the self-test whose one out-of-range read the check skips."""
+    _ok("dlr_selftest_bounds", _load().dlr_selftest_bounds(_stream(stream)))
 
 
 def _ptr(t: Optional[torch.Tensor]):

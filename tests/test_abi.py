@@ -33,7 +33,8 @@ def test_header_declares_the_boundary():
                  "s5_workspace_size", "dlr_get_device_status", "dlr_status_string",
                  "dlr_abi_version", "dlr_step_prepare", "dlr_step", "dlr_step_workspace_size",
                  "dlr_conv_spectrum_direct", "dlr_scan_backward_params", "s5_layer_ex",
-                 "s5_layer_tv", "dlr_params_from_dss_exp", "dlr_log_re_from_reparam"]:
+                 "s5_layer_tv", "dlr_params_from_dss_exp", "dlr_log_re_from_reparam",
+                 "dlr_bounds_checked", "dlr_bounds_site", "dlr_selftest_bounds"]:
         assert must in names, must
 
 
@@ -46,7 +47,16 @@ def test_status_strings_and_version(lib):
     lib.dlr_status_string.restype = ctypes.c_char_p
     assert lib.dlr_status_string(0) == b"DLR_OK"
     assert lib.dlr_status_string(4) == b"DLR_ERR_TIMEOUT"
-    assert lib.dlr_abi_version() == 9
+    assert lib.dlr_status_string(6) == b"DLR_ERR_BOUNDS"
+    assert lib.dlr_abi_version() == 10
+
+
+def test_normal_build_has_no_bounds_checks(lib):
+    """The normal library reports itself unchecked and refuses the bounds self-test without
+    launching anything (its guards compile to nothing, so the planted read must not run)."""
+    assert lib.dlr_bounds_checked() == 0
+    lib.dlr_selftest_bounds.argtypes = [ctypes.c_void_p]
+    assert lib.dlr_selftest_bounds(None) == 2  # DLR_ERR_UNSUPPORTED
 
 
 def test_host_validation_rejects_bad_arguments(lib):
