@@ -6,15 +6,16 @@
 //
 // Float32 tier, as a sequence of kernels over a workspace:
 //   prep   (one CTA per state p, double precision): Lbar_p, the powers Lbar_p^t (t <= T) and
-//          Lbar_p^T as two floats, Bbar as the real [H, 2P] operand, C~ as the real [2P, H]
-//          operand [Re C~^T ; -Im C~^T].
-//   gemm   V[B*L, 2P] = u[B*L, H] * Bbar^T (float32 FFMA, register tiled)
+//          Lbar_p^T as two floats, Bbar as the real [2P, H] operand and C~ as the real [H, 2P]
+//          operand [Re C~, -Im C~], each split into its tf32 part and the float32 remainder.
+//   gemm   V[B*L, 2P] = u[B*L, H] * Bbar^T in float32 from three tf32 tensor-core products
+//          (tc_gemm_x3 in tc_gemm.cu)
 //   chunk  S_c = sum_t Lbar^{T-1-t} V_t (end state of chunk c from a zero start)
 //   carry  X_c = Lbar^T X_{c-1} + S_c in two-float arithmetic, one warp per (b, p) scanning
 //          groups of chunks (the tensor-core tier: float32, one CTA per (b, 32 states) with a
 //          warp per group of chunks); stores the state entering each chunk
 //   apply  x_t = Lbar^{t+1} X_in + l_t, l_t = Lbar l_{t-1} + V_t, written over V in place
-//   gemm   y = x * [Re C~^T ; -Im C~^T] + D (.) u
+//   gemm   y = x * [Re C~, -Im C~]^T + D (.) u (tc_gemm_x3)
 // The tensor-core tier runs the two projections on tcgen05 (tc_gemm.cu) with bf16 operands and
 // float32 accumulation: the input projection converts the float32 u to bf16 in the kernel and
 // writes V as bf16; the scan reads V in bf16 and computes in float32; apply writes x as bf16
