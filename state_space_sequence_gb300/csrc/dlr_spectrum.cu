@@ -23,7 +23,11 @@
 //     in two-float arithmetic, the second an exact integer ratio; where |L phi| < 1 it is the
 //     product L phi itself, which keeps its relative precision as the angle shrinks;
 //   - where |L l| < 2^-10 (a pole of the series, reached by channels on the unit circle) G is
-//     L (1 + (L - 1) l / 2), whose omitted terms are below (L |l|)^2 / 6 relative.
+//     L (1 + (L - 1) l / 2), whose omitted terms are below (L |l|)^2 / 6 relative;
+//   - away from the pole (|phi| >= 1/16 half-turn, so |1 - z| > 0.19 when |lambda| ~ 1) the
+//     same G = (z^L - 1) / (z - 1) comes from products instead: z = e^{-a^2} cis(theta) times
+//     the bin's cis(-pi k / n), z^L = lambda^L times the bin's cis(-pi v_k); their absolute
+//     errors of a few 2^-24 stay below 1e-6 relative to |z - 1| there.
 // Cost: N complex divisions and two sincospif per state and bin, O(N L) per channel -- more than
 // the O(N L) multiply-adds of dlr_kernel followed by an O(L log L) FFT, so the kernel route
 // stays the default; this one needs no kernel buffer and no spectrum FFT.
@@ -47,6 +51,8 @@ struct SpecState {
   float th_hi, th_lo;            // theta / pi in about [-1, 1], two-float
   float rL;                      // L theta / pi mod 2, in about [-1, 1]
   float w_re, w_im;
+  float z_re, z_im;              // lambda = e^-a^2 cis(theta)
+  float zl_re, zl_im;            // lambda^L = e^-L a^2 cis(pi rL)
 };
 
 // expm1(x + i pi f) from expm1(x), e^x and f (|f| <= 2)
@@ -96,6 +102,26 @@ __device__ __forceinline__ cf geom(const SpecState& p, int L, float kn, float vk
   return {(num.re * den.re + num.im * den.im) * inv, (num.im * den.re - num.re * den.im) * inv};
 }
 
+// G away from the pole: (z^L - 1) / (z - 1) with z = lambda cis(-sign pi k / n) and
+// z^L = lambda^L cis(-sign pi v_k), (ck, sk) = cis(-pi k / n), (cv, sv) = cis(-pi v_k).
+__device__ __forceinline__ cf geom_far(const SpecState& p, float ck, float sk, float cv, float sv,
+                                       int sign) {
+  const float sks = sign > 0 ? sk : -sk, svs = sign > 0 ? sv : -sv;
+  const float zr = p.z_re * ck - p.z_im * sks, zi = fmaf(p.z_re, sks, p.z_im * ck);
+  const float nr = fmaf(p.zl_re, cv, fmaf(-p.zl_im, svs, -1.f));
+  const float ni = fmaf(p.zl_re, svs, p.zl_im * cv);
+  const float dr = zr - 1.f, di = zi;
+  const float inv = 1.f / fmaf(dr, dr, di * di);
+  return {(nr * dr + ni * di) * inv, (ni * dr - nr * di) * inv};
+}
+
+// phi = theta / pi - sign k / n folded to about (-1, 1] (for the choice of path only)
+__device__ __forceinline__ float phase_near(const SpecState& p, float kn, int sign) {
+  float d = sign > 0 ? p.th_hi - kn : p.th_hi + kn;
+  d -= 2.f * rintf(0.5f * d);
+  return d;
+}
+
 // One CTA per (block of bins, channel); the channel's state parameters in shared memory.
 __global__ void __launch_bounds__(kSpecThreads)
     spectrum_direct(const float* __restrict__ lr1, const float* __restrict__ li1,
@@ -122,6 +148,13 @@ __global__ void __launch_bounds__(kSpecThreads)
     p.th_hi = lp.th_hi;
     p.th_lo = lp.th_lo;
     p.rL = reduce_halfturns((float)L, lp.th_hi, lp.th_lo);
+    float sn, cs;
+    sincospif(lp.th_hi + lp.th_lo, &sn, &cs);
+    p.z_re = p.e1 * cs;
+    p.z_im = p.e1 * sn;
+    sincospif(p.rL, &sn, &cs);
+    p.zl_re = p.e1L * cs;
+    p.zl_im = p.e1L * sn;
     const float2 w = W[o];
     p.w_re = w.x;
     p.w_im = w.y;
@@ -133,6 +166,12 @@ __global__ void __launch_bounds__(kSpecThreads)
   const float kn = ldexpf((float)k, -lg);
   const long long lk = ((long long)L * (long long)k) % (2LL * n);
   const float vk = ldexpf((float)lk, -lg);
+  // the bin's twiddles for the far-from-pole path: cis(-pi k / n), cis(-pi v_k)
+  float sk, ck, sv, cv;
+  sincospif(kn, &sk, &ck);
+  sk = -sk;
+  sincospif(vk, &sv, &cv);
+  sv = -sv;
   float cre = 0.f, cim = 0.f;
 #pragma unroll 1
   for (int set = 0; set < sets; ++set) {
@@ -142,8 +181,10 @@ __global__ void __launch_bounds__(kSpecThreads)
 #pragma unroll 2
     for (int m = 0; m < N; ++m) {
       const SpecState& p = st[set][m];
-      const cf gp = geom(p, L, kn, vk, sp);
-      const cf gm = geom(p, L, kn, vk, -sp);
+      const cf gp = fabsf(phase_near(p, kn, sp)) < 0.0625f ? geom(p, L, kn, vk, sp)
+                                                          : geom_far(p, ck, sk, cv, sv, sp);
+      const cf gm = fabsf(phase_near(p, kn, -sp)) < 0.0625f ? geom(p, L, kn, vk, -sp)
+                                                           : geom_far(p, ck, sk, cv, sv, -sp);
       are = fmaf(p.w_re, gp.re, fmaf(-p.w_im, gp.im, are));
       aim = fmaf(p.w_re, gp.im, fmaf(p.w_im, gp.re, aim));
       bre = fmaf(p.w_re, gm.re, fmaf(-p.w_im, gm.im, bre));
