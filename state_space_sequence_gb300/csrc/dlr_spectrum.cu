@@ -28,9 +28,10 @@
 //     same G = (z^L - 1) / (z - 1) comes from products instead: z = e^{-a^2} cis(theta) times
 //     the bin's cis(-pi k / n), z^L = lambda^L times the bin's cis(-pi v_k); their absolute
 //     errors of a few 2^-24 stay below 1e-6 relative to |z - 1| there.
-// Cost: N complex divisions and two sincospif per state and bin, O(N L) per channel -- more than
-// the O(N L) multiply-adds of dlr_kernel followed by an O(L log L) FFT, so the kernel route
-// stays the default; this one needs no kernel buffer and no spectrum FFT.
+// Cost: per state and bin two complex divisions (the bins at +-k), and near a pole two
+// sincospif -- O(N L) per channel with more work per term than the O(N L) multiply-adds of
+// dlr_kernel followed by an O(L log L) FFT, so the kernel route stays the default; this one
+// needs no kernel buffer and no spectrum FFT.
 #include <cuda_runtime.h>
 
 #include "dlr_common.cuh"
