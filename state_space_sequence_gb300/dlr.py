@@ -419,7 +419,9 @@ def s5_workspace_size(B: int, L: int, H: int, P: int, prec: str = "fp32") -> int
 
 def s5_layer(u, lam, log_delta, Bt, Ct, D, prec: str = "fp32", out=None, workspace=None,
              stream=None):
-    """S5 SSM outputs for u [B, L, H]; parameters as in include/dlr.h."""
+    """S5 SSM outputs for u [B, L, H]; parameters as in include/dlr.h. ``prec``: "fp32" (float32
+    results: projections as three tf32 tensor-core products, float32 scan) or "bf16" (bf16
+    projection operands and intermediates, float32 accumulation and scan)."""
     _check_f32(u, lam, log_delta, Bt, Ct, D)
     B, L, H = u.shape
     P = lam.shape[0]
