@@ -442,18 +442,21 @@ def run_extras(torch, dlr, inputs, flush, sm_mhz, sm_count):
         "decode_frac": dec_bytes / us_dec / 1e3 / peak_gbs, "peak_kind": peak_kind,
         "sequence_ms": ms, "sequence_elements_per_s": B * H * L / ms * 1e3}
     # the backward pass of the same layer for an output gradient g: the input gradient (the
-    # tensor-core scan's reversed pass) and the parameter gradients (sums of g against the
-    # states of x and of lambda dx/d lambda)
+    # tensor-core scan's reversed pass) and the parameter gradients (the lag correlation of g
+    # with u by transforms, then its power sums per state)
     g = torch.randn_like(u)
     du = torch.empty_like(u)
     wsb = torch.empty(dlr.dlr_scan_workspace_size(B, H, N, L), dtype=torch.uint8, device="cuda")
+    wsp = torch.empty(dlr.dlr_scan_backward_params_workspace_size(B, H, N, L), dtype=torch.uint8,
+                      device="cuda")
     ms_in = _time_steps(torch, lambda: dlr.dlr_scan_backward_input(g, fwd, workspace=wsb,
                                                                    out=du), 10, 2, flush)
-    ms_par = _time_steps(torch, lambda: dlr.dlr_scan_backward_params(u, g, fwd), 10, 2, flush)
+    ms_par = _time_steps(torch, lambda: dlr.dlr_scan_backward_params(u, g, fwd, workspace=wsp),
+                         10, 2, flush)
     out["backward_" + WORKLOAD] = {
         "input_ms": ms_in, "params_ms": ms_par, "ms": ms_in + ms_par,
         "elements_per_s": B * H * L / (ms_in + ms_par) * 1e3}
-    del u, y, xs, wss, g, du, wsb
+    del u, y, xs, wss, g, du, wsb, wsp
 
     w = inputs.make_workload("dlrprod_bidir_b4_h128_n1024_l16384")
     u = dev(w.u)

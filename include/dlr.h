@@ -251,15 +251,23 @@ dlr_status dlr_scan_host(const float* u, const float* log_re, const float* log_i
  * W_n j lambda_n^{j-1}; section 2.2: lambda = exp(-a^2 + i theta)):
  *   dW [H, N, 2] = (Re S0, -Im S0),  d_log_re [H, N] = -2 a Re(W S1),
  *   d_log_im [H, N] = -Im(W S1).
- * Computed as sums over the steps of g against the states of two recurrences driven by u,
- * x_k = lambda x_{k-1} + u_k and D_k = lambda (D_{k-1} + x_{k-1}) (lambda times dx/d lambda):
- * S0 = sum g x, S1 = sum g D, per (b, h, state) with lambda as a float pair, then summed over
- * the batch. u, g [B, H, L] (4-byte aligned); parameters as in dlr_kernel; the three outputs
- * (dW 8-byte aligned) must not overlap the parameters or each other. workspace: device
- * memory, dlr_scan_backward_params_workspace_size(B, H, N) bytes (16 * B * H * N), 16-byte
- * aligned. Two kernel launches; L < 2^24, N <= 65536.
+ * Two routes, chosen from N and L alone:
+ *  - N >= 16 and L <= 8192: c itself by transforms, c = IFFT(sum_b FFT(g_b) conj FFT(u_b))
+ *    with both rows of a batch entry in one complex transform of M = 2^ceil(log2(2L - 1))
+ *    points, one CTA per channel; then S0 and S1 per state as sums over the lags with
+ *    lambda^j = lambda^{32m} lambda^t, both factors evaluated directly from the parameters;
+ *  - otherwise: sums over the steps of g against the states of two recurrences driven by u,
+ *    x_k = lambda x_{k-1} + u_k and D_k = lambda (D_{k-1} + x_{k-1}) (lambda times
+ *    dx/d lambda): S0 = sum g x, S1 = sum g D, per (b, h, state) with lambda as a float pair,
+ *    then summed over the batch.
+ * u, g [B, H, L] (4-byte aligned); parameters as in dlr_kernel; the three outputs (dW 8-byte
+ * aligned) must not overlap the parameters or each other. workspace: device memory,
+ * dlr_scan_backward_params_workspace_size(B, H, N, L) bytes, 16-byte aligned (the first
+ * route: the M-point twiddle table and c [H, L] floats; the second: 16 * B * H * N). Two
+ * kernel launches (three on the first route); L < 2^24, N <= 65536. The workspace size is 0
+ * for arguments out of range.
  */
-size_t dlr_scan_backward_params_workspace_size(int64_t B, int64_t H, int64_t N);
+size_t dlr_scan_backward_params_workspace_size(int64_t B, int64_t H, int64_t N, int64_t L);
 dlr_status dlr_scan_backward_params(const float* u, const float* g, const float* log_re,
                                     const float* log_im, const float* W, int64_t B, int64_t H,
                                     int64_t N, int64_t L, float* d_log_re, float* d_log_im,

@@ -46,7 +46,7 @@ cudaError_t launch_s5_tv(const float* u, const float* dt, const float* lambda,
                          int* status, cudaStream_t s);
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
 cudaError_t launch_selftest_bounds(cudaStream_t s);
-size_t grad_workspace_bytes(int64_t B, int64_t H, int64_t N);
+size_t grad_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t L);
 cudaError_t launch_dlr_grad_params(const float* u, const float* g, const float* log_re,
                                    const float* log_im, const float* W, int B, int H, int N,
                                    int L, float* d_log_re, float* d_log_im, float* dW, void* ws,
@@ -135,7 +135,7 @@ dlr_status check_params(const float* log_re, const float* log_im, const float* W
 
 extern "C" {
 
-int dlr_abi_version(void) { return 10; }
+int dlr_abi_version(void) { return 11; }
 
 const char* dlr_last_cuda_error(void) { return t_last_cuda_error_msg; }
 
@@ -326,9 +326,9 @@ dlr_status dlr_scan_apply(const float* u, int64_t B, int64_t H, int64_t N, int64
                                              false));
 }
 
-size_t dlr_scan_backward_params_workspace_size(int64_t B, int64_t H, int64_t N) {
-  if (B < 1 || H < 1 || N < 1) return 0;
-  return dlr::grad_workspace_bytes(B, H, N);
+size_t dlr_scan_backward_params_workspace_size(int64_t B, int64_t H, int64_t N, int64_t L) {
+  if (B < 1 || H < 1 || N < 1 || L < 1 || L > kMaxL) return 0;
+  return dlr::grad_workspace_bytes(B, H, N, L);
 }
 
 dlr_status dlr_scan_backward_params(const float* u, const float* g, const float* log_re,
@@ -356,7 +356,7 @@ dlr_status dlr_scan_backward_params(const float* u, const float* g, const float*
       if (ranges_overlap(outs[i], osz[i], outs[j], osz[j])) return DLR_ERR_INVALID_ARG;
   }
   if (L > kMaxL || B * H > kMaxGrid / 64 || N > 65536) return DLR_ERR_UNSUPPORTED;
-  const size_t need = dlr::grad_workspace_bytes(B, H, N);
+  const size_t need = dlr::grad_workspace_bytes(B, H, N, L);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DLR_ERR_WORKSPACE;
   return from_cuda(dlr::launch_dlr_grad_params(u, g, log_re, log_im, W, (int)B, (int)H, (int)N,
                                                (int)L, d_log_re, d_log_im, dW, workspace,

@@ -13,26 +13,63 @@
 // (the second recurrence is lambda times the derivative of x with respect to lambda), so the
 // gradients need neither the kernel nor the correlation c.
 //
-// dlr_grad_rows: one thread per (b, h, n) runs both recurrences over the row. lambda is the
-// float pair hi + lo of its double-precision value (as in the recurrent mode), so its rounding
-// does not compound over the row. A warp holds 32 states of one (b, h) row: lane j loads
-// u_{k0+j} and g_{k0+j}, the steps take them by shuffles. The products are summed in float
-// over each block of 32 steps, the blocks into the running sums. Each thread leaves its
-// row's (S0, S1) in the workspace; dlr_grad_finish adds the B rows of each (h, n) and forms
-// the three gradients.
+// Two routes compute S0 and S1.
+//
+// Lag correlation (N >= 16, L <= 8192): c is formed first, then the two power sums per state.
+//  - grad_corr: one CTA per channel h. For each batch row, z = u + i g (zero-padded to
+//    M = 2^lg >= 2L - 1 points, so the circular correlation equals the linear one for lags
+//    0 .. L-1) is transformed once; the two real spectra come out as U_f = (Z_f + conj
+//    Z_{M-f}) / 2 and G_f = (Z_f - conj Z_{M-f}) / 2i, and A_f += G_f conj(U_f) is summed
+//    over the batch for f = 0 .. M/2 (A is Hermitian: c is real). One inverse transform then
+//    gives c_j = (1/M) sum_f A_f e^{2 pi i f j / M}.
+//  - grad_moments: one warp per four states of a channel, lanes along the lag: lane t sums
+//    c_{32m+t} lambda^{32m} and (32m+t) c_{32m+t} lambda^{32m} over the blocks m, each
+//    lambda^{32m} evaluated directly from the parameters (a batch of 32 by the 32 lanes,
+//    passed round by shuffles), then multiplies by its own lambda^t, the warp adds the lanes
+//    and lane 0 forms the three gradients.
+// Per input element this is one complex FFT point per row and a few flops per (state, lag)
+// instead of the recurrences' two complex updates per (state, step, row).
+//
+// Recurrences (fewer states, or longer rows):
+// dlr_grad_rows: one thread per (b, h, n) runs both recurrences over the row, in blocks of 32
+// steps. A warp holds 32 states of one (b, h) row: lane j loads u_{k0+j} and g_{k0+j}, the steps
+// take them by shuffles. Within a block both recurrences start from zero in float (lambda a
+// float, at most 32 products deep) and, with t the step within the block, the state carried in
+// (X at the block's start, DX = lambda dX/d lambda) adds lambda^{t+1} X to x and
+// (t+1) lambda^{t+1} X + lambda^{t+1} DX to D; so the block adds
+//     to S0:  sum g x_loc + Gam X,              Gam  = sum_t g_t lambda^{t+1},
+//     to S1:  sum g D_loc + Gam DX + Gam1 X,    Gam1 = sum_t (t+1) g_t lambda^{t+1},
+// and the carries move on as X <- mu X + x_loc, DX <- 32 mu X + mu DX + D_loc (mu = lambda^32,
+// from double). X, DX, S0 and S1 are two-float complex numbers, so no rounding accumulates
+// along the row: a plain float recurrence drifts as sqrt(L) rounding errors on unit-circle
+// states (2e-5 relative at L = 9000). Each thread leaves its row's (S0, S1) in the workspace;
+// dlr_grad_finish adds the B rows of each (h, n) and forms the three gradients.
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
-#include "dlr_common.cuh"
+#include "fft_rows.cuh"
 
 namespace dlr {
 // source file number of the bounds-checked build's failing sites
 [[maybe_unused]] constexpr int kSiteFile = 2;
 
+cudaError_t launch_twiddle_table(float2* tw, int logn, cudaStream_t s);
+
 namespace {
 
+using fft::padded;
+
 constexpr int kGradWarps = 4;  // warps per block
+
+__device__ __forceinline__ ff split_double(double v) {
+  const float hi = (float)v;
+  return {hi, (float)(v - (double)hi)};
+}
+__device__ __forceinline__ cff cff_of(cf a) { return {{a.re, 0.f}, {a.im, 0.f}}; }
+__device__ __forceinline__ cff cff_add(cff a, cff b) {
+  return {ff_add(a.re, b.re), ff_add(a.im, b.im)};
+}
 
 __global__ void __launch_bounds__(kGradWarps * 32)
     dlr_grad_rows(const float* __restrict__ u, const float* __restrict__ g,
@@ -45,55 +82,72 @@ __global__ void __launch_bounds__(kGradWarps * 32)
   const int n = (int)(wid - row * warps_per_row) * 32 + lane;
   const int h = (int)(row % H);
   const bool on = n < N;
-  // lambda as a float pair
-  float lhr = 0.f, lhi = 0.f, llr = 0.f, lli = 0.f;
+  // lambda (float) and mu = lambda^32 (two-float), from double
+  cf lam = {0.f, 0.f};
+  cff mu = {{0.f, 0.f}, {0.f, 0.f}};
   if (on) {
     const double a = log_re[(size_t)h * N + n], th = log_im[(size_t)h * N + n];
-    const double mag = exp(-a * a);
     double s, c;
     sincos(th, &s, &c);
-    const double re = mag * c, im = mag * s;
-    lhr = (float)re;
-    lhi = (float)im;
-    llr = (float)(re - (double)lhr);
-    lli = (float)(im - (double)lhi);
+    const double mag = exp(-a * a);
+    lam = {(float)(mag * c), (float)(mag * s)};
+    sincos(32.0 * th, &s, &c);
+    const double mag32 = exp(-32.0 * a * a);
+    mu = {split_double(mag32 * c), split_double(mag32 * s)};
   }
   const float* ur = u + row * (int64_t)L;
   const float* gr = g + row * (int64_t)L;
-  float xr = 0.f, xi = 0.f, dr = 0.f, di = 0.f;
-  float s0r = 0.f, s0i = 0.f, s1r = 0.f, s1i = 0.f;
+  const cff zero = {{0.f, 0.f}, {0.f, 0.f}};
+  cff X = zero, DX = zero, S0 = zero, S1 = zero;
 #pragma unroll 1
   for (int k0 = 0; k0 < L; k0 += 32) {
     const int k = k0 + lane;
     const float uk = k < L ? __ldg(ur + k) : 0.f;
     const float gk = k < L ? __ldg(gr + k) : 0.f;
     const int steps = min(32, L - k0);
-    float p0r = 0.f, p0i = 0.f, p1r = 0.f, p1i = 0.f;
+    float xr = 0.f, xi = 0.f, dr = 0.f, di = 0.f;     // block-local x, D
+    float rr = lam.re, ri = lam.im;                   // lambda^{t+1}
+    float p0r = 0.f, p0i = 0.f, p1r = 0.f, p1i = 0.f;  // sum g x_loc, sum g D_loc
+    float g0r = 0.f, g0i = 0.f, g1r = 0.f, g1i = 0.f;  // Gam, Gam1
 #pragma unroll 8
     for (int t = 0; t < steps; ++t) {
       const float ut = __shfl_sync(0xffffffffu, uk, t);
       const float gt = __shfl_sync(0xffffffffu, gk, t);
-      // D_k = lambda (D_{k-1} + x_{k-1}), then x_k = lambda x_{k-1} + u_k (lambda = hi + lo,
-      // the lo products first)
+      // D_loc <- lambda (D_loc + x_loc), then x_loc <- lambda x_loc + u_t
       const float er = dr + xr, ei = di + xi;
-      dr = fmaf(lhr, er, fmaf(-lhi, ei, fmaf(llr, er, -lli * ei)));
-      di = fmaf(lhr, ei, fmaf(lhi, er, fmaf(llr, ei, lli * er)));
-      const float nr = fmaf(lhr, xr, fmaf(-lhi, xi, fmaf(llr, xr, fmaf(-lli, xi, ut))));
-      const float ni = fmaf(lhr, xi, fmaf(lhi, xr, fmaf(llr, xi, lli * xr)));
+      dr = fmaf(lam.re, er, -lam.im * ei);
+      di = fmaf(lam.re, ei, lam.im * er);
+      const float nr = fmaf(lam.re, xr, fmaf(-lam.im, xi, ut));
+      const float ni = fmaf(lam.re, xi, lam.im * xr);
       xr = nr;
       xi = ni;
       p0r = fmaf(gt, xr, p0r);
       p0i = fmaf(gt, xi, p0i);
       p1r = fmaf(gt, dr, p1r);
       p1i = fmaf(gt, di, p1i);
+      const float gw = (float)(t + 1) * gt;
+      g0r = fmaf(gt, rr, g0r);
+      g0i = fmaf(gt, ri, g0i);
+      g1r = fmaf(gw, rr, g1r);
+      g1i = fmaf(gw, ri, g1i);
+      const float qr = fmaf(lam.re, rr, -lam.im * ri);
+      ri = fmaf(lam.re, ri, lam.im * rr);
+      rr = qr;
     }
-    s0r += p0r;
-    s0i += p0i;
-    s1r += p1r;
-    s1i += p1i;
+    const cff gam = cff_of({g0r, g0i}), gam1 = cff_of({g1r, g1i});
+    S0 = cff_fma(gam, X, cff_add(S0, cff_of({p0r, p0i})));
+    S1 = cff_fma(gam1, X, cff_fma(gam, DX, cff_add(S1, cff_of({p1r, p1i}))));
+    if (steps == 32) {
+      // DX <- 32 mu X + mu DX + D_loc (32 mu X exact: a power of two), X <- mu X + x_loc
+      const cff muX = cff_fma(mu, X, zero);
+      const cff mu32X = {{32.f * muX.re.hi, 32.f * muX.re.lo}, {32.f * muX.im.hi, 32.f * muX.im.lo}};
+      DX = cff_fma(mu, DX, cff_add(mu32X, cff_of({dr, di})));
+      X = cff_add(muX, cff_of({xr, xi}));
+    }
   }
   if (on && DLR_IN(row * (int64_t)N + n, (int64_t)B * H * N))
-    part[row * (int64_t)N + n] = make_float4(s0r, s0i, s1r, s1i);
+    part[row * (int64_t)N + n] = make_float4(S0.re.hi + S0.re.lo, S0.im.hi + S0.im.lo,
+                                             S1.re.hi + S1.re.lo, S1.im.hi + S1.im.lo);
 }
 
 // Sum over the batch rows and the gradients: dW = (Re S0, -Im S0), d log_re = -2 a Re(W S1),
@@ -123,9 +177,172 @@ __global__ void dlr_grad_finish(const float4* __restrict__ part, const float* __
   d_log_im[hn] = (float)(-ws1i);
 }
 
+// ---- lag correlation route ----
+
+// One CTA per channel h: c[h, j] = sum_b sum_k g_{b,h,k} u_{b,h,k-j}, j < L, by transforms of
+// M = 2^kLog >= 2L - 1 points. Shared memory: the transform buffer (padded) and A_f, f <= M/2.
+template <int kLog>
+__global__ void __launch_bounds__(fftr::Plan<kLog>::T, kLog <= 13 ? 2 : 1)
+    grad_corr(const float* __restrict__ u, const float* __restrict__ g, int B, int H, int L,
+              const float2* __restrict__ tw, float* __restrict__ c) {
+  using P = fftr::Plan<kLog>;
+  constexpr int M = P::n, T = P::T, kHalf = M / 2;
+  constexpr int PER = (M + T - 1) / T;
+  extern __shared__ float2 smem[];
+  float2* buf = smem;
+  float2* acc = smem + P::buf_elems;
+  const int tid = threadIdx.x;
+  const int h = blockIdx.x;
+  for (int f = tid; f <= kHalf; f += T)
+    if (DLR_IN(f, kHalf + 1)) acc[f] = make_float2(0.f, 0.f);
+#pragma unroll 1
+  for (int b = 0; b < B; ++b) {
+    const float* ur = u + ((size_t)b * H + h) * (size_t)L;
+    const float* gr = g + ((size_t)b * H + h) * (size_t)L;
+    // every load of the row before the first store
+    float2 z[PER];
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int m = tid + q * T;
+      z[q] = m < L ? make_float2(__ldg(ur + m), __ldg(gr + m)) : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      const int m = tid + q * T;
+      if (m < M && DLR_IN(padded(m), P::buf_elems)) buf[padded(m)] = z[q];
+    }
+    __syncthreads();
+    fftr::local_fft<kLog, false>(buf, tw);  // ends with a barrier
+    for (int f = tid; f <= kHalf; f += T) {
+      const int fm = (M - f) & (M - 1);
+      if (!DLR_IN(padded(f), P::buf_elems) || !DLR_IN(padded(fm), P::buf_elems) ||
+          !DLR_IN(f, kHalf + 1))
+        continue;
+      const float2 za = buf[padded(f)], zb = buf[padded(fm)];
+      // U_f = (Z_f + conj Z_{M-f}) / 2, G_f = (Z_f - conj Z_{M-f}) / 2i
+      const float ur_ = 0.5f * (za.x + zb.x), ui = 0.5f * (za.y - zb.y);
+      const float gr_ = 0.5f * (za.y + zb.y), gi = 0.5f * (zb.x - za.x);
+      float2 a = acc[f];
+      a.x = fmaf(gr_, ur_, fmaf(gi, ui, a.x));  // Re G conj(U)
+      a.y = fmaf(gi, ur_, fmaf(-gr_, ui, a.y));  // Im G conj(U)
+      acc[f] = a;
+    }
+    __syncthreads();  // the next row overwrites the buffer
+  }
+  // the Hermitian spectrum of the real correlation, then its inverse transform
+  for (int f = tid; f <= kHalf; f += T) {
+    if (!DLR_IN(f, kHalf + 1) || !DLR_IN(padded(f), P::buf_elems)) continue;
+    const float2 a = acc[f];
+    buf[padded(f)] = a;
+    if (f > 0 && f < kHalf && DLR_IN(padded(M - f), P::buf_elems))
+      buf[padded(M - f)] = make_float2(a.x, -a.y);
+  }
+  __syncthreads();
+  fftr::local_fft<kLog, true>(buf, tw);
+  const float inv = 1.0f / (float)M;
+  float* ch = c + (size_t)h * (size_t)L;
+  for (int j = tid; j < L; j += T)
+    if (DLR_IN(padded(j), P::buf_elems)) ch[j] = buf[padded(j)].x * inv;
+}
+
+constexpr int kMomWarps = 8;   // warps per block
+constexpr int kMomStates = 4;  // states per warp
+
+// S0 = sum_j c_j lambda^j and S1 = sum_j j c_j lambda^j for kMomStates states of channel h per
+// warp, then the gradients of those states.
+__global__ void __launch_bounds__(kMomWarps * 32)
+    grad_moments(const float* __restrict__ c, const float* __restrict__ log_re,
+                 const float* __restrict__ log_im, const float2* __restrict__ W, int H, int N,
+                 int L, int blocks_per_h, float* __restrict__ d_log_re,
+                 float* __restrict__ d_log_im, float2* __restrict__ dW) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int h = blockIdx.x / blocks_per_h;
+  const int n0 = ((blockIdx.x - h * blocks_per_h) * kMomWarps + warp) * kMomStates;
+  if (h >= H || n0 >= N) return;  // whole warps
+  const float* ch = c + (size_t)h * (size_t)L;
+  lam_param p[kMomStates];
+#pragma unroll
+  for (int s = 0; s < kMomStates; ++s) {
+    const int n = min(n0 + s, N - 1);
+    p[s] = make_lam_param(log_re[(size_t)h * N + n], log_im[(size_t)h * N + n]);
+  }
+  cf a0[kMomStates], a1[kMomStates];
+#pragma unroll
+  for (int s = 0; s < kMomStates; ++s) a0[s] = a1[s] = {0.f, 0.f};
+  const int nb = (L + 31) / 32;
+#pragma unroll 1
+  for (int mb = 0; mb < nb; mb += 32) {
+    cf pw[kMomStates];  // lambda^{32 (mb + lane)}
+#pragma unroll
+    for (int s = 0; s < kMomStates; ++s) pw[s] = lam_pow(p[s], 32 * (mb + lane));
+    const int cnt = min(32, nb - mb);
+#pragma unroll 4
+    for (int i = 0; i < cnt; ++i) {
+      const int j = 32 * (mb + i) + lane;
+      const float cj = j < L ? __ldg(ch + j) : 0.f;
+      const float jc = (float)j * cj;
+#pragma unroll
+      for (int s = 0; s < kMomStates; ++s) {
+        const float wr = __shfl_sync(0xffffffffu, pw[s].re, i);
+        const float wi = __shfl_sync(0xffffffffu, pw[s].im, i);
+        a0[s].re = fmaf(cj, wr, a0[s].re);
+        a0[s].im = fmaf(cj, wi, a0[s].im);
+        a1[s].re = fmaf(jc, wr, a1[s].re);
+        a1[s].im = fmaf(jc, wi, a1[s].im);
+      }
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < kMomStates; ++s) {
+    const cf lt = lam_pow(p[s], lane);
+    cf s0 = cmul(a0[s], lt), s1 = cmul(a1[s], lt);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      s0.re += __shfl_xor_sync(0xffffffffu, s0.re, o);
+      s0.im += __shfl_xor_sync(0xffffffffu, s0.im, o);
+      s1.re += __shfl_xor_sync(0xffffffffu, s1.re, o);
+      s1.im += __shfl_xor_sync(0xffffffffu, s1.im, o);
+    }
+    const int n = n0 + s;
+    if (lane == 0 && n < N) {
+      const size_t hn = (size_t)h * N + n;
+      const float2 w = W[hn];
+      const double ws1r = (double)w.x * s1.re - (double)w.y * s1.im;
+      const double ws1i = (double)w.x * s1.im + (double)w.y * s1.re;
+      dW[hn] = make_float2(s0.re, -s0.im);
+      d_log_re[hn] = (float)(-2.0 * (double)log_re[hn] * ws1r);
+      d_log_im[hn] = (float)(-ws1i);
+    }
+  }
+}
+
+template <int kLog>
+cudaError_t launch_corr(const float* u, const float* g, int B, int H, int L, const float2* tw,
+                        float* c, cudaStream_t s) {
+  using P = fftr::Plan<kLog>;
+  const size_t smem = (P::buf_elems + (size_t)(P::n / 2 + 1)) * sizeof(float2);
+  cudaError_t e = max_smem_once<grad_corr<kLog>>(smem);
+  if (e != cudaSuccess) return e;
+  grad_corr<kLog><<<(unsigned)H, P::T, smem, s>>>(u, g, B, H, L, tw, c);
+  return cudaGetLastError();
+}
+
+// M = 2^lg >= 2L - 1 points
+int corr_log2_size(int64_t L) {
+  int lg = 0;
+  while ((int64_t(1) << lg) < 2 * L - 1) ++lg;
+  return lg;
+}
+
+bool corr_route(int64_t N, int64_t L) { return N >= 16 && L <= 8192; }
+
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
 }  // namespace
 
-size_t grad_workspace_bytes(int64_t B, int64_t H, int64_t N) {
+size_t grad_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t L) {
+  if (corr_route(N, L))
+    return align256(sizeof(float2) << corr_log2_size(L)) + sizeof(float) * (size_t)H * (size_t)L;
   return sizeof(float4) * (size_t)B * (size_t)H * (size_t)N;
 }
 
@@ -133,6 +350,29 @@ cudaError_t launch_dlr_grad_params(const float* u, const float* g, const float* 
                                    const float* log_im, const float* W, int B, int H, int N,
                                    int L, float* d_log_re, float* d_log_im, float* dW, void* ws,
                                    cudaStream_t s) {
+  if (corr_route(N, L)) {
+    const int lg = corr_log2_size(L);
+    float2* tw = static_cast<float2*>(ws);
+    float* c = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
+                                        align256(sizeof(float2) << lg));
+    cudaError_t e = launch_twiddle_table(tw, lg, s);
+    if (e != cudaSuccess) return e;
+    switch (lg) {
+#define CORR_CASE(G) \
+  case G: e = launch_corr<G>(u, g, B, H, L, tw, c, s); break;
+      CORR_CASE(0) CORR_CASE(1) CORR_CASE(2) CORR_CASE(3) CORR_CASE(4) CORR_CASE(5)
+      CORR_CASE(6) CORR_CASE(7) CORR_CASE(8) CORR_CASE(9) CORR_CASE(10) CORR_CASE(11)
+      CORR_CASE(12) CORR_CASE(13) CORR_CASE(14)
+#undef CORR_CASE
+      default: return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
+    const int bph = (N + kMomWarps * kMomStates - 1) / (kMomWarps * kMomStates);
+    grad_moments<<<(unsigned)((int64_t)H * bph), kMomWarps * 32, 0, s>>>(
+        c, log_re, log_im, reinterpret_cast<const float2*>(W), H, N, L, bph, d_log_re, d_log_im,
+        reinterpret_cast<float2*>(dW));
+    return cudaGetLastError();
+  }
   float4* part = static_cast<float4*>(ws);
   const int wpr = (N + 31) / 32;
   const int64_t warps = (int64_t)B * H * wpr;

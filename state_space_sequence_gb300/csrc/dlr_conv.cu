@@ -605,6 +605,12 @@ cudaError_t launch_twiddles(int lg, void* ws, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// tw[m] = exp(-2 pi i m / n), m < n = 2^logn, for another module's transforms.
+cudaError_t launch_twiddle_table(float2* tw, int logn, cudaStream_t s) {
+  twiddle_table<<<((1 << logn) + 255) / 256, 256, 0, s>>>(tw, logn, nullptr);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dlr_conv_apply(const float* u, int B, int H, int L, float* y, const void* ws,
                                   cudaStream_t s) {
   const int lg = conv_log2_size(L);

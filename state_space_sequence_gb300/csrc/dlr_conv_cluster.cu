@@ -33,6 +33,7 @@ namespace {
 
 using fft::padded;
 using fft::padded_size;
+using fftr::local_fft;
 constexpr int kC = 8;  // CTAs per cluster
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -76,42 +77,6 @@ __device__ __forceinline__ void powers8(cf (&p)[8], cf x) {
   p[5] = cmul(p[4], x);
   p[6] = cmul(p[4], p[2]);
   p[7] = cmul(p[4], p[3]);
-}
-
-// Local Stockham FFT of n_loc = 2^kLog points in `buf` (natural order in and out), in place:
-// every pass loads all of a thread's points, synchronises, then stores.
-template <int kLog, bool kInv>
-__device__ __forceinline__ void local_fft(float2* buf, const float2* __restrict__ tw) {
-  using P = fftr::Plan<kLog>;
-  {
-    cf a[P::PER0][P::R0];
-#pragma unroll
-    for (int q = 0; q < P::PER0; ++q) {
-      const int j = threadIdx.x + q * P::T;
-      if (P::NB0 % P::T == 0 || j < P::NB0) {
-#pragma unroll
-        for (int r = 0; r < P::R0; ++r) {
-          const float2 f = DLR_IN(padded(j + r * P::NB0), P::buf_elems) ? buf[padded(j + r * P::NB0)]
-                                                                        : make_float2(0.f, 0.f);
-          a[q][r] = {f.x, f.y};
-        }
-        fft::dft<P::R0, kInv>(a[q]);
-      }
-    }
-    __syncthreads();
-    fftr::pass0_store<kLog>(buf, a);
-    __syncthreads();
-  }
-  int ns = P::R0;
-#pragma unroll 1
-  for (int p = 0; p < P::n16; ++p) {
-    cf v[P::PER16][16];
-    fftr::pass16_load_compute<kLog, kInv>(buf, ns, tw, v);
-    __syncthreads();
-    fftr::pass16_store<kLog>(buf, ns, v);
-    __syncthreads();
-    ns *= 16;
-  }
 }
 
 // The spectral step's output at bin k from the packed transform's Z_k (fa) and Z_{n-k} (fb),

@@ -156,5 +156,44 @@ __device__ __forceinline__ void pass0_store(float2* dst, const cf (&a)[Plan<kLog
   }
 }
 
+// Stockham FFT of n = 2^kLog points held in `buf` (padded layout; natural order in and out),
+// in place: every pass loads all of a thread's points, synchronises, then stores. Forward
+// (e^{-2 pi i jk/n}) or, with kInv, the unnormalised inverse; tw is the n-point table above.
+// Every thread of the CTA (Plan<kLog>::T of them) must call it.
+template <int kLog, bool kInv>
+__device__ __forceinline__ void local_fft(float2* buf, const float2* __restrict__ tw) {
+  using P = Plan<kLog>;
+  {
+    cf a[P::PER0][P::R0];
+#pragma unroll
+    for (int q = 0; q < P::PER0; ++q) {
+      const int j = threadIdx.x + q * P::T;
+      if (P::NB0 % P::T == 0 || j < P::NB0) {
+#pragma unroll
+        for (int r = 0; r < P::R0; ++r) {
+          const float2 f = DLR_IN_FILE(padded(j + r * P::NB0), P::buf_elems, kSiteFileRows)
+                               ? buf[padded(j + r * P::NB0)]
+                               : make_float2(0.f, 0.f);
+          a[q][r] = {f.x, f.y};
+        }
+        fft::dft<P::R0, kInv>(a[q]);
+      }
+    }
+    __syncthreads();
+    pass0_store<kLog>(buf, a);
+    __syncthreads();
+  }
+  int ns = P::R0;
+#pragma unroll 1
+  for (int p = 0; p < P::n16; ++p) {
+    cf v[P::PER16][16];
+    pass16_load_compute<kLog, kInv>(buf, ns, tw, v);
+    __syncthreads();
+    pass16_store<kLog>(buf, ns, v);
+    __syncthreads();
+    ns *= 16;
+  }
+}
+
 }  // namespace fftr
 }  // namespace dlr

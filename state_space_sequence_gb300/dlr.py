@@ -71,7 +71,7 @@ def _load():
         lib.dlr_scan_host.argtypes = [P, P, P, P, i64, i64, i64, i64, P, P, sz, P]
         lib.dlr_scan_host.restype = i32
         lib.dlr_scan_backward_input.argtypes = [P, P, P, P, i64, i64, i64, i64, P, P, sz, P]
-        lib.dlr_scan_backward_params_workspace_size.argtypes = [i64, i64, i64]
+        lib.dlr_scan_backward_params_workspace_size.argtypes = [i64, i64, i64, i64]
         lib.dlr_scan_backward_params_workspace_size.restype = sz
         lib.dlr_scan_backward_params.argtypes = [P, P, P, P, P, i64, i64, i64, i64, P, P, P, P,
                                                  sz, P]
@@ -308,6 +308,11 @@ def dlr_scan_apply(u, workspace, N: int, out=None, reverse: bool = False, stream
     return out
 
 
+def dlr_scan_backward_params_workspace_size(B: int, H: int, N: int, L: int) -> int:
+    """Bytes of device workspace dlr_scan_backward_params needs (0 for arguments out of range)."""
+    return int(_load().dlr_scan_backward_params_workspace_size(B, H, N, L))
+
+
 def dlr_scan_backward_params(u, g, params, workspace=None, stream=None):
     """Parameter gradients of the causal DLR layer (Re cast) for input u and output gradient g
     [B, H, L]: returns (d_log_re [H, N], d_log_im [H, N], dW [H, N, 2])."""
@@ -316,7 +321,7 @@ def dlr_scan_backward_params(u, g, params, workspace=None, stream=None):
     B, H, L = u.shape
     N = lr.shape[1]
     if workspace is None:
-        need = _load().dlr_scan_backward_params_workspace_size(B, H, N)
+        need = dlr_scan_backward_params_workspace_size(B, H, N, L)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=u.device)
     d_re = torch.empty_like(lr)
     d_im = torch.empty_like(li)

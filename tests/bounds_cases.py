@@ -105,6 +105,15 @@ def run():
     d_lr, d_li, dW = dlr.dlr_scan_backward_params(dev(w.u), dev(g), pdev(w.fwd))
     got = np.concatenate([host(d_lr).ravel(), host(d_li).ravel(), host(dW).ravel()])
     record("backward parameters", got, np.concatenate([r_re.ravel(), r_im.ravel(), r_W.ravel()]))
+    # the recurrence route (few states) and the correlation route's largest transform
+    for B, H, N, L in [(2, 2, 8, 300), (1, 1, 18, 8000)]:
+        w = inputs.make_dlr(B, H, N, L, seed=N + L, unit_channels=1)
+        g = np.random.default_rng(N).standard_normal(w.u.shape).astype(np.float32)
+        _, r_re, r_im, r_W = oracle.dlr_backward(w.u, g, *pnp(w.fwd))
+        d_lr, d_li, dW = dlr.dlr_scan_backward_params(dev(w.u), dev(g), pdev(w.fwd))
+        got = np.concatenate([host(d_lr).ravel(), host(d_li).ravel(), host(dW).ravel()])
+        record(f"backward parameters N{N} L{L}", got,
+               np.concatenate([r_re.ravel(), r_im.ravel(), r_W.ravel()]))
 
     # S5: float32 and bf16 tiers (L a multiple of 64 takes the fused output projection),
     # bilinear, a step that changes from step to step

@@ -48,7 +48,7 @@ def test_status_strings_and_version(lib):
     assert lib.dlr_status_string(0) == b"DLR_OK"
     assert lib.dlr_status_string(4) == b"DLR_ERR_TIMEOUT"
     assert lib.dlr_status_string(6) == b"DLR_ERR_BOUNDS"
-    assert lib.dlr_abi_version() == 10
+    assert lib.dlr_abi_version() == 11
 
 
 def test_normal_build_has_no_bounds_checks(lib):
@@ -254,15 +254,23 @@ def test_backward_params_validation(lib):
     parameters or each other, limits and the workspace are checked on the host."""
     P, i64, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t
     lib.dlr_scan_backward_params.argtypes = [P] * 5 + [i64] * 4 + [P] * 4 + [sz, P]
-    lib.dlr_scan_backward_params_workspace_size.argtypes = [i64, i64, i64]
+    lib.dlr_scan_backward_params_workspace_size.argtypes = [i64] * 4
     lib.dlr_scan_backward_params_workspace_size.restype = sz
-    assert lib.dlr_scan_backward_params_workspace_size(8, 256, 64) == 16 * 8 * 256 * 64
-    assert lib.dlr_scan_backward_params_workspace_size(0, 1, 1) == 0
+    wsz = lib.dlr_scan_backward_params_workspace_size
+    # correlation route (N >= 16, L <= 8192): the M-point twiddle table (M = 2^ceil(log2(2L-1)))
+    # and c [H, L]; otherwise 16 bytes per (b, h, n)
+    assert wsz(8, 256, 64, 4096) == 8 * 8192 + 4 * 256 * 4096
+    assert wsz(2, 3, 16, 5) == 256 + 4 * 3 * 5                  # M = 16, table padded to 256 B
+    assert wsz(8, 256, 8, 4096) == 16 * 8 * 256 * 8              # few states
+    assert wsz(8, 256, 64, 8193) == 16 * 8 * 256 * 64            # long rows
+    assert wsz(0, 1, 1, 1) == 0
+    assert wsz(1, 1, 1, 0) == 0
+    assert wsz(1, 1, 1, 1 << 24) == 0
     u, g = ctypes.c_void_p(0x100000), ctypes.c_void_p(0x200000)
     lr, li, W = ctypes.c_void_p(0x300000), ctypes.c_void_p(0x310000), ctypes.c_void_p(0x320000)
     dr, di, dW = ctypes.c_void_p(0x400000), ctypes.c_void_p(0x410000), ctypes.c_void_p(0x420000)
     ws = ctypes.c_void_p(0x500000)
-    need = lib.dlr_scan_backward_params_workspace_size(2, 3, 4)
+    need = wsz(2, 3, 4, 10)
     call = lib.dlr_scan_backward_params
     assert call(u, g, lr, li, W, 0, 3, 4, 10, dr, di, dW, ws, need, None) == 1
     assert call(None, g, lr, li, W, 2, 3, 4, 10, dr, di, dW, ws, need, None) == 1

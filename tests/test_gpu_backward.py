@@ -25,10 +25,16 @@ def host(t):
     return t.detach().cpu().numpy().astype(np.float64)
 
 
-@pytest.mark.parametrize("B,H,N,L", [(1, 1, 1, 1), (2, 3, 16, 256), (3, 2, 40, 1000),
-                                     (1, 2, 64, 4096), (4, 3, 33, 777), (2, 1, 100, 3000)])
+@pytest.mark.parametrize("B,H,N,L", [
+    # lag-correlation route (N >= 16, L <= 8192): transforms of M = 2^ceil(log2(2L-1)) points,
+    # from M = 1 and 4 up to 16384
+    (3, 1, 16, 1), (2, 1, 17, 2), (1, 1, 32, 33), (2, 3, 16, 256), (3, 2, 40, 1000),
+    (1, 2, 64, 4096), (4, 3, 33, 777), (2, 1, 100, 3000), (2, 2, 16, 8192), (1, 1, 70, 5000),
+    # recurrence route: few states, rows longer than 8192
+    (1, 1, 1, 1), (2, 2, 8, 1000), (1, 2, 20, 9000)])
 def test_backward_params_match_oracle(B, H, N, L):
-    """Ragged L, N not a multiple of 32, one unit-circle channel (d log_re = 0 there)."""
+    """Both routes; ragged L, N not a multiple of 32 or of the four states a warp takes, one
+    unit-circle channel (d log_re = 0 there)."""
     w = inputs.make_dlr(B, H, N, L, seed=B * 101 + H * 7 + N + L, unit_channels=1)
     g = np.random.default_rng(L + N).standard_normal((B, H, L)).astype(np.float32)
     p = (w.fwd.log_re, w.fwd.log_im, w.fwd.W)
