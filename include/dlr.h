@@ -263,9 +263,10 @@ dlr_status dlr_scan_host(const float* u, const float* log_re, const float* log_i
  * u, g [B, H, L] (4-byte aligned); parameters as in dlr_kernel; the three outputs (dW 8-byte
  * aligned) must not overlap the parameters or each other. workspace: device memory,
  * dlr_scan_backward_params_workspace_size(B, H, N, L) bytes, 16-byte aligned (the first
- * route: the M-point twiddle table and c [H, L] floats; the second: 16 * B * H * N). Two
- * kernel launches (three on the first route); L < 2^24, N <= 65536. The workspace size is 0
- * for arguments out of range.
+ * route: the M-point twiddle table and c [H, L] floats; the second: 16 * B * H * N; each part
+ * rounded up to 256 bytes). Two kernel launches (three on the first route); L < 2^24,
+ * N <= 65536. The workspace size is 0 for arguments out of range. dlr_layer_backward gives
+ * the same for the bidirectional layer and the DLR-prod cast, with the input gradient.
  */
 size_t dlr_scan_backward_params_workspace_size(int64_t B, int64_t H, int64_t N, int64_t L);
 dlr_status dlr_scan_backward_params(const float* u, const float* g, const float* log_re,
@@ -273,6 +274,44 @@ dlr_status dlr_scan_backward_params(const float* u, const float* g, const float*
                                     int64_t N, int64_t L, float* d_log_re, float* d_log_im,
                                     float* dW, void* workspace, size_t workspace_bytes,
                                     dlr_stream_t stream);
+
+/*
+ * dlr_layer_backward -- the gradients of the DLR layer as dlr_kernel + dlr_conv apply it:
+ * causal or bidirectional (DLR paper section 2.1: y = DLR1(u) + rev(DLR2(rev(u))), the
+ * second direction with the second parameter set), Re cast or DLR-prod cast (section 2.1:
+ * kappa_j = Re K_j Im K_j), for a loss whose gradient with respect to y is g [B, H, L]:
+ *  - du [B, H, L] (optional: NULL skips it): du_k = sum_j kappa1_j g_{k+j} + sum_j kappa2_j
+ *    g_{k-j}, the layer's adjoint (the two directions swapped), by the FFT convolution of g
+ *    with kappa2 as its causal and kappa1 as its anti-causal kernel (kappa2 = 0 for a causal
+ *    layer);
+ *  - the parameter gradients of each direction, from the lag correlation
+ *    c_j = sum_b sum_k g_{b,k} u_{b,k-j} (the second direction uses c_{-j}, i.e. the causal
+ *    layer on the reversed rows), with S0 = sum_j w_j lambda^j and S1 = sum_j j w_j lambda^j:
+ *      Re cast (w = c):              dW = (Re S0, -Im S0), d_log_re = -2a Re(W S1),
+ *                                    d_log_im = -Im(W S1);
+ *      DLR-prod cast (w = c K, K the complex kernel, since d kappa_j = Im(K_j dK_j)):
+ *                                    dW = (Im S0, Re S0),  d_log_re = -2a Im(W S1),
+ *                                    d_log_im = Re(W S1).
+ *    As dlr_scan_backward_params: c by transforms when N >= 16 and L <= 8192 (and always for
+ *    the DLR-prod cast, which needs c itself), else the blocked recurrences (on the reversed
+ *    rows for the second direction).
+ * u, g, du 16-byte aligned; parameters as in dlr_kernel, the second set (and its three
+ * outputs) given exactly when dir == DLR_BIDIR; outputs as dlr_scan_backward_params (none may
+ * overlap a parameter, another output, u, g or the workspace). workspace: device memory,
+ * dlr_layer_backward_workspace_size(B, H, N, L, dir, cast) bytes (0 for arguments out of
+ * range), 16-byte aligned. Limits: L <= 65536 (L <= 8192 for the DLR-prod cast, else
+ * DLR_ERR_UNSUPPORTED), N <= 65536. Faults of the tensor-core kernel generator's bounded
+ * waits (N >= 256, or N >= 64 at L >= 16384) are reported through dlr_get_device_status().
+ */
+size_t dlr_layer_backward_workspace_size(int64_t B, int64_t H, int64_t N, int64_t L,
+                                         dlr_dir dir, dlr_cast cast);
+dlr_status dlr_layer_backward(const float* u, const float* g, const float* log_re,
+                              const float* log_im, const float* W, const float* log_re2,
+                              const float* log_im2, const float* W2, dlr_dir dir, dlr_cast cast,
+                              int64_t B, int64_t H, int64_t N, int64_t L, float* du,
+                              float* d_log_re, float* d_log_im, float* dW, float* d_log_re2,
+                              float* d_log_im2, float* dW2, void* workspace,
+                              size_t workspace_bytes, dlr_stream_t stream);
 
 /*
  * dlr_scan_backward_input -- the input gradient of the causal DLR layer (Re cast): for a loss

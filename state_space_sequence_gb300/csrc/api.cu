@@ -47,6 +47,12 @@ cudaError_t launch_s5_tv(const float* u, const float* dt, const float* lambda,
 cudaError_t launch_selftest_timeout(uint64_t limit_ns, int* status, cudaStream_t s);
 cudaError_t launch_selftest_bounds(cudaStream_t s);
 size_t grad_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t L);
+size_t grads_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t L, bool bidir, bool prod);
+cudaError_t launch_dlr_grads(const float* u, const float* g, const float* lr1, const float* li1,
+                             const float* W1, const float* lr2, const float* li2,
+                             const float* W2, int B, int H, int N, int L, bool prod,
+                             float* dr1, float* di1, float* dW1, float* dr2, float* di2,
+                             float* dW2, void* ws, cudaStream_t s);
 cudaError_t launch_dlr_grad_params(const float* u, const float* g, const float* log_re,
                                    const float* log_im, const float* W, int B, int H, int N,
                                    int L, float* d_log_re, float* d_log_im, float* dW, void* ws,
@@ -135,7 +141,7 @@ dlr_status check_params(const float* log_re, const float* log_im, const float* W
 
 extern "C" {
 
-int dlr_abi_version(void) { return 11; }
+int dlr_abi_version(void) { return 12; }
 
 const char* dlr_last_cuda_error(void) { return t_last_cuda_error_msg; }
 
@@ -361,6 +367,106 @@ dlr_status dlr_scan_backward_params(const float* u, const float* g, const float*
   return from_cuda(dlr::launch_dlr_grad_params(u, g, log_re, log_im, W, (int)B, (int)H, (int)N,
                                                (int)L, d_log_re, d_log_im, dW, workspace,
                                                (cudaStream_t)stream));
+}
+
+// Workspace of dlr_layer_backward: the gradients' part, then the two kernels of the input
+// gradient's convolution and the convolution workspace, each rounded up to 256 bytes.
+namespace {
+size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
+size_t layer_bwd_grads_bytes(int64_t B, int64_t H, int64_t N, int64_t L, bool bidir, bool prod) {
+  return round256(dlr::grads_workspace_bytes(B, H, N, L, bidir, prod));
+}
+}  // namespace
+
+size_t dlr_layer_backward_workspace_size(int64_t B, int64_t H, int64_t N, int64_t L,
+                                         dlr_dir dir, dlr_cast cast) {
+  if (B < 1 || H < 1 || N < 1 || L < 1 || L > 65536) return 0;
+  if (dir != DLR_CAUSAL && dir != DLR_BIDIR) return 0;
+  if (cast != DLR_CAST_RE && cast != DLR_CAST_RE_IM) return 0;
+  if (cast == DLR_CAST_RE_IM && L > 8192) return 0;
+  const size_t hl = sizeof(float) * (size_t)H * (size_t)L;
+  return layer_bwd_grads_bytes(B, H, N, L, dir == DLR_BIDIR, cast == DLR_CAST_RE_IM) +
+         2 * round256(hl) + dlr::conv_workspace_bytes(H, L);
+}
+
+dlr_status dlr_layer_backward(const float* u, const float* g, const float* log_re,
+                              const float* log_im, const float* W, const float* log_re2,
+                              const float* log_im2, const float* W2, dlr_dir dir, dlr_cast cast,
+                              int64_t B, int64_t H, int64_t N, int64_t L, float* du,
+                              float* d_log_re, float* d_log_im, float* dW, float* d_log_re2,
+                              float* d_log_im2, float* dW2, void* workspace,
+                              size_t workspace_bytes, dlr_stream_t stream) {
+  if (B < 1 || H < 1 || N < 1 || L < 1) return DLR_ERR_INVALID_ARG;
+  if (dir != DLR_CAUSAL && dir != DLR_BIDIR) return DLR_ERR_INVALID_ARG;
+  if (cast != DLR_CAST_RE && cast != DLR_CAST_RE_IM) return DLR_ERR_INVALID_ARG;
+  const bool bidir = dir == DLR_BIDIR, prod = cast == DLR_CAST_RE_IM;
+  if (!u || !g || !aligned16(u) || !aligned16(g)) return DLR_ERR_INVALID_ARG;
+  if (du && !aligned16(du)) return DLR_ERR_INVALID_ARG;
+  dlr_status st = check_params(log_re, log_im, W);
+  if (st != DLR_OK) return st;
+  if (bidir) {
+    st = check_params(log_re2, log_im2, W2);
+    if (st != DLR_OK) return st;
+  } else if (log_re2 || log_im2 || W2 || d_log_re2 || d_log_im2 || dW2) {
+    return DLR_ERR_INVALID_ARG;
+  }
+  auto al4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; };
+  auto al8 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; };
+  const int sets = bidir ? 2 : 1;
+  float* outs[6] = {d_log_re, d_log_im, dW, d_log_re2, d_log_im2, dW2};
+  const float* ins[6] = {log_re, log_im, W, log_re2, log_im2, W2};
+  const size_t pn = sizeof(float) * (size_t)H * (size_t)N;
+  const size_t sz[6] = {pn, pn, 2 * pn, pn, pn, 2 * pn};
+  for (int i = 0; i < 3 * sets; ++i) {
+    if (!outs[i] || !al4(outs[i]) || (i % 3 == 2 && !al8(outs[i]))) return DLR_ERR_INVALID_ARG;
+    for (int j = 0; j < 3 * sets; ++j)
+      if (ranges_overlap(outs[i], sz[i], ins[j], sz[j])) return DLR_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 3 * sets; ++j)
+      if (ranges_overlap(outs[i], sz[i], outs[j], sz[j])) return DLR_ERR_INVALID_ARG;
+  }
+  const size_t bytes = sizeof(float) * (size_t)B * (size_t)H * (size_t)L;
+  if (du) {
+    if (ranges_overlap(du, bytes, u, bytes) || ranges_overlap(du, bytes, g, bytes))
+      return DLR_ERR_INVALID_ARG;
+    for (int i = 0; i < 3 * sets; ++i)
+      if (ranges_overlap(du, bytes, outs[i], sz[i])) return DLR_ERR_INVALID_ARG;
+  }
+  if (L > 65536 || N > 65536 || B * H > kMaxGrid / 64) return DLR_ERR_UNSUPPORTED;
+  if (prod && L > 8192) return DLR_ERR_UNSUPPORTED;
+  const size_t need = dlr_layer_backward_workspace_size(B, H, N, L, dir, cast);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DLR_ERR_WORKSPACE;
+  if (ranges_overlap(workspace, need, u, bytes) || ranges_overlap(workspace, need, g, bytes) ||
+      (du && ranges_overlap(workspace, need, du, bytes)))
+    return DLR_ERR_INVALID_ARG;
+  for (int i = 0; i < 3 * sets; ++i)
+    if (ranges_overlap(workspace, need, outs[i], sz[i])) return DLR_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = dlr::launch_dlr_grads(u, g, log_re, log_im, W, log_re2, log_im2, W2, (int)B,
+                                        (int)H, (int)N, (int)L, prod, d_log_re, d_log_im, dW,
+                                        d_log_re2, d_log_im2, dW2, ws, s);
+  if (e != cudaSuccess || !du) return from_cuda(e);
+  // du: the convolution of g whose causal kernel is the second direction's and whose
+  // anti-causal kernel is the first's (the adjoint swaps the directions); zero causal kernel
+  // for a causal layer
+  const size_t hl = sizeof(float) * (size_t)H * (size_t)L;
+  uint8_t* p = ws + layer_bwd_grads_bytes(B, H, N, L, bidir, prod);
+  float* kap1 = reinterpret_cast<float*>(p);
+  float* kap2 = reinterpret_cast<float*>(p + round256(hl));
+  void* cws = p + 2 * round256(hl);
+  int* status = status_word();
+  if ((e = dlr::launch_dlr_kernel(log_re, log_im, W, (int)H, (int)N, (int)L, prod, kap1, status,
+                                  s)) != cudaSuccess)
+    return from_cuda(e);
+  if (bidir)
+    e = dlr::launch_dlr_kernel(log_re2, log_im2, W2, (int)H, (int)N, (int)L, prod, kap2, status,
+                               s);
+  else
+    e = cudaMemsetAsync(kap2, 0, hl, s);
+  if (e != cudaSuccess) return from_cuda(e);
+  if ((e = dlr::launch_dlr_conv_spectrum(kap2, kap1, (int)H, (int)L, cws, s)) != cudaSuccess)
+    return from_cuda(e);
+  return from_cuda(dlr::launch_dlr_conv_apply(g, (int)B, (int)H, (int)L, du, cws, s));
 }
 
 dlr_status dlr_scan_backward_input(const float* g, const float* log_re, const float* log_im,

@@ -74,7 +74,7 @@ __device__ __forceinline__ cff cff_add(cff a, cff b) {
 __global__ void __launch_bounds__(kGradWarps * 32)
     dlr_grad_rows(const float* __restrict__ u, const float* __restrict__ g,
                   const float* __restrict__ log_re, const float* __restrict__ log_im, int B,
-                  int H, int N, int L, int warps_per_row, float4* __restrict__ part) {
+                  int H, int N, int L, int warps_per_row, int rev, float4* __restrict__ part) {
   const int lane = threadIdx.x & 31;
   const int64_t wid = (int64_t)blockIdx.x * kGradWarps + (threadIdx.x >> 5);
   const int64_t row = wid / warps_per_row;  // (b, h)
@@ -102,8 +102,9 @@ __global__ void __launch_bounds__(kGradWarps * 32)
 #pragma unroll 1
   for (int k0 = 0; k0 < L; k0 += 32) {
     const int k = k0 + lane;
-    const float uk = k < L ? __ldg(ur + k) : 0.f;
-    const float gk = k < L ? __ldg(gr + k) : 0.f;
+    const int kk = rev ? L - 1 - k : k;  // rev: the reversed row (the second direction)
+    const float uk = k < L ? __ldg(ur + kk) : 0.f;
+    const float gk = k < L ? __ldg(gr + kk) : 0.f;
     const int steps = min(32, L - k0);
     float xr = 0.f, xi = 0.f, dr = 0.f, di = 0.f;     // block-local x, D
     float rr = lam.re, ri = lam.im;                   // lambda^{t+1}
@@ -184,7 +185,7 @@ __global__ void dlr_grad_finish(const float4* __restrict__ part, const float* __
 template <int kLog>
 __global__ void __launch_bounds__(fftr::Plan<kLog>::T, kLog <= 13 ? 2 : 1)
     grad_corr(const float* __restrict__ u, const float* __restrict__ g, int B, int H, int L,
-              const float2* __restrict__ tw, float* __restrict__ c) {
+              const float2* __restrict__ tw, float* __restrict__ c, float* __restrict__ c2) {
   using P = fftr::Plan<kLog>;
   constexpr int M = P::n, T = P::T, kHalf = M / 2;
   constexpr int PER = (M + T - 1) / T;
@@ -243,18 +244,30 @@ __global__ void __launch_bounds__(fftr::Plan<kLog>::T, kLog <= 13 ? 2 : 1)
   float* ch = c + (size_t)h * (size_t)L;
   for (int j = tid; j < L; j += T)
     if (DLR_IN(padded(j), P::buf_elems)) ch[j] = buf[padded(j)].x * inv;
+  if (c2) {  // the negative lags: c2_j = sum_b sum_k g_{b,k} u_{b,k+j}, at M - j (j > 0)
+    float* c2h = c2 + (size_t)h * (size_t)L;
+    for (int j = tid; j < L; j += T) {
+      const int m = (M - j) & (M - 1);
+      if (DLR_IN(padded(m), P::buf_elems)) c2h[j] = buf[padded(m)].x * inv;
+    }
+  }
 }
 
 constexpr int kMomWarps = 8;   // warps per block
 constexpr int kMomStates = 4;  // states per warp
 
-// S0 = sum_j c_j lambda^j and S1 = sum_j j c_j lambda^j for kMomStates states of channel h per
-// warp, then the gradients of those states.
+// S0 = sum_j w_j lambda^j and S1 = sum_j j w_j lambda^j for kMomStates states of channel h per
+// warp, then the gradients of those states. Re cast: w_j = c_j, dW = (Re S0, -Im S0),
+// d log_re = -2a Re(W S1), d log_im = -Im(W S1). DLR-prod cast (kappa_j = Re K_j Im K_j, so
+// d kappa_j = Im(K_j dK_j)): w_j = c_j K_j with the complex kernel Kc, dW = (Im S0, Re S0),
+// d log_re = -2a Im(W S1), d log_im = Re(W S1).
+template <bool kProd>
 __global__ void __launch_bounds__(kMomWarps * 32)
-    grad_moments(const float* __restrict__ c, const float* __restrict__ log_re,
-                 const float* __restrict__ log_im, const float2* __restrict__ W, int H, int N,
-                 int L, int blocks_per_h, float* __restrict__ d_log_re,
-                 float* __restrict__ d_log_im, float2* __restrict__ dW) {
+    grad_moments(const float* __restrict__ c, const float2* __restrict__ Kc,
+                 const float* __restrict__ log_re, const float* __restrict__ log_im,
+                 const float2* __restrict__ W, int H, int N, int L, int blocks_per_h,
+                 float* __restrict__ d_log_re, float* __restrict__ d_log_im,
+                 float2* __restrict__ dW) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int h = blockIdx.x / blocks_per_h;
   const int n0 = ((blockIdx.x - h * blocks_per_h) * kMomWarps + warp) * kMomStates;
@@ -280,15 +293,27 @@ __global__ void __launch_bounds__(kMomWarps * 32)
     for (int i = 0; i < cnt; ++i) {
       const int j = 32 * (mb + i) + lane;
       const float cj = j < L ? __ldg(ch + j) : 0.f;
-      const float jc = (float)j * cj;
+      if constexpr (!kProd) {
+        const float jc = (float)j * cj;
 #pragma unroll
-      for (int s = 0; s < kMomStates; ++s) {
-        const float wr = __shfl_sync(0xffffffffu, pw[s].re, i);
-        const float wi = __shfl_sync(0xffffffffu, pw[s].im, i);
-        a0[s].re = fmaf(cj, wr, a0[s].re);
-        a0[s].im = fmaf(cj, wi, a0[s].im);
-        a1[s].re = fmaf(jc, wr, a1[s].re);
-        a1[s].im = fmaf(jc, wi, a1[s].im);
+        for (int s = 0; s < kMomStates; ++s) {
+          const float wr = __shfl_sync(0xffffffffu, pw[s].re, i);
+          const float wi = __shfl_sync(0xffffffffu, pw[s].im, i);
+          a0[s].re = fmaf(cj, wr, a0[s].re);
+          a0[s].im = fmaf(cj, wi, a0[s].im);
+          a1[s].re = fmaf(jc, wr, a1[s].re);
+          a1[s].im = fmaf(jc, wi, a1[s].im);
+        }
+      } else {
+        const float2 kj = j < L ? __ldg(Kc + (size_t)h * L + j) : make_float2(0.f, 0.f);
+        const cf t = {cj * kj.x, cj * kj.y};
+        const cf jt = {(float)j * t.re, (float)j * t.im};
+#pragma unroll
+        for (int s = 0; s < kMomStates; ++s) {
+          const cf w = {__shfl_sync(0xffffffffu, pw[s].re, i), __shfl_sync(0xffffffffu, pw[s].im, i)};
+          a0[s] = cfma(t, w, a0[s]);
+          a1[s] = cfma(jt, w, a1[s]);
+        }
       }
     }
   }
@@ -309,21 +334,27 @@ __global__ void __launch_bounds__(kMomWarps * 32)
       const float2 w = W[hn];
       const double ws1r = (double)w.x * s1.re - (double)w.y * s1.im;
       const double ws1i = (double)w.x * s1.im + (double)w.y * s1.re;
-      dW[hn] = make_float2(s0.re, -s0.im);
-      d_log_re[hn] = (float)(-2.0 * (double)log_re[hn] * ws1r);
-      d_log_im[hn] = (float)(-ws1i);
+      if constexpr (!kProd) {
+        dW[hn] = make_float2(s0.re, -s0.im);
+        d_log_re[hn] = (float)(-2.0 * (double)log_re[hn] * ws1r);
+        d_log_im[hn] = (float)(-ws1i);
+      } else {
+        dW[hn] = make_float2(s0.im, s0.re);
+        d_log_re[hn] = (float)(-2.0 * (double)log_re[hn] * ws1i);
+        d_log_im[hn] = (float)ws1r;
+      }
     }
   }
 }
 
 template <int kLog>
 cudaError_t launch_corr(const float* u, const float* g, int B, int H, int L, const float2* tw,
-                        float* c, cudaStream_t s) {
+                        float* c, float* c2, cudaStream_t s) {
   using P = fftr::Plan<kLog>;
   const size_t smem = (P::buf_elems + (size_t)(P::n / 2 + 1)) * sizeof(float2);
   cudaError_t e = max_smem_once<grad_corr<kLog>>(smem);
   if (e != cudaSuccess) return e;
-  grad_corr<kLog><<<(unsigned)H, P::T, smem, s>>>(u, g, B, H, L, tw, c);
+  grad_corr<kLog><<<(unsigned)H, P::T, smem, s>>>(u, g, B, H, L, tw, c, c2);
   return cudaGetLastError();
 }
 
@@ -334,51 +365,70 @@ int corr_log2_size(int64_t L) {
   return lg;
 }
 
-bool corr_route(int64_t N, int64_t L) { return N >= 16 && L <= 8192; }
+bool corr_route(int64_t N, int64_t L, bool prod) { return prod || (N >= 16 && L <= 8192); }
 
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
-}  // namespace
-
-size_t grad_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t L) {
-  if (corr_route(N, L))
-    return align256(sizeof(float2) << corr_log2_size(L)) + sizeof(float) * (size_t)H * (size_t)L;
-  return sizeof(float4) * (size_t)B * (size_t)H * (size_t)N;
+// Workspace of the gradients. Correlation route: the M-point twiddle table, c [H, L], with a
+// second direction the negative lags c2 [H, L], with the DLR-prod cast the complex kernel of
+// each direction [H, L] float2. Recurrence route: the per-row sums [B, H, N] float4, reused
+// by the second direction.
+struct GradWs {
+  float2* tw;
+  float *c, *c2;
+  float2 *k1, *k2;
+  float4* part;
+};
+GradWs carve_grads(void* ws, int64_t B, int64_t H, int64_t N, int64_t L, bool bidir, bool prod,
+                   size_t* total) {
+  uint8_t* p = static_cast<uint8_t*>(ws);
+  GradWs w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* q = p ? p + off : nullptr;
+    off += align256(bytes);
+    return q;
+  };
+  if (corr_route(N, L, prod)) {
+    const size_t hl = (size_t)H * (size_t)L;
+    w.tw = reinterpret_cast<float2*>(take(sizeof(float2) << corr_log2_size(L)));
+    w.c = reinterpret_cast<float*>(take(sizeof(float) * hl));
+    if (bidir) w.c2 = reinterpret_cast<float*>(take(sizeof(float) * hl));
+    if (prod) w.k1 = reinterpret_cast<float2*>(take(sizeof(float2) * hl));
+    if (prod && bidir) w.k2 = reinterpret_cast<float2*>(take(sizeof(float2) * hl));
+  } else {
+    w.part = reinterpret_cast<float4*>(take(sizeof(float4) * (size_t)B * H * N));
+  }
+  if (total) *total = off;
+  return w;
 }
 
-cudaError_t launch_dlr_grad_params(const float* u, const float* g, const float* log_re,
-                                   const float* log_im, const float* W, int B, int H, int N,
-                                   int L, float* d_log_re, float* d_log_im, float* dW, void* ws,
-                                   cudaStream_t s) {
-  if (corr_route(N, L)) {
-    const int lg = corr_log2_size(L);
-    float2* tw = static_cast<float2*>(ws);
-    float* c = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
-                                        align256(sizeof(float2) << lg));
-    cudaError_t e = launch_twiddle_table(tw, lg, s);
-    if (e != cudaSuccess) return e;
-    switch (lg) {
-#define CORR_CASE(G) \
-  case G: e = launch_corr<G>(u, g, B, H, L, tw, c, s); break;
-      CORR_CASE(0) CORR_CASE(1) CORR_CASE(2) CORR_CASE(3) CORR_CASE(4) CORR_CASE(5)
-      CORR_CASE(6) CORR_CASE(7) CORR_CASE(8) CORR_CASE(9) CORR_CASE(10) CORR_CASE(11)
-      CORR_CASE(12) CORR_CASE(13) CORR_CASE(14)
-#undef CORR_CASE
-      default: return cudaErrorInvalidValue;
-    }
-    if (e != cudaSuccess) return e;
-    const int bph = (N + kMomWarps * kMomStates - 1) / (kMomWarps * kMomStates);
-    grad_moments<<<(unsigned)((int64_t)H * bph), kMomWarps * 32, 0, s>>>(
-        c, log_re, log_im, reinterpret_cast<const float2*>(W), H, N, L, bph, d_log_re, d_log_im,
-        reinterpret_cast<float2*>(dW));
-    return cudaGetLastError();
-  }
-  float4* part = static_cast<float4*>(ws);
+// The moments of one parameter set from its weights (c, and the complex kernel for DLR-prod).
+cudaError_t launch_moments(const float* c, const float2* Kc, bool prod, const float* log_re,
+                           const float* log_im, const float* W, int H, int N, int L,
+                           float* d_log_re, float* d_log_im, float* dW, cudaStream_t s) {
+  const int bph = (N + kMomWarps * kMomStates - 1) / (kMomWarps * kMomStates);
+  const unsigned grid = (unsigned)((int64_t)H * bph);
+  const float2* Wc = reinterpret_cast<const float2*>(W);
+  float2* dWc = reinterpret_cast<float2*>(dW);
+  if (prod)
+    grad_moments<true><<<grid, kMomWarps * 32, 0, s>>>(c, Kc, log_re, log_im, Wc, H, N, L, bph,
+                                                        d_log_re, d_log_im, dWc);
+  else
+    grad_moments<false><<<grid, kMomWarps * 32, 0, s>>>(c, Kc, log_re, log_im, Wc, H, N, L, bph,
+                                                         d_log_re, d_log_im, dWc);
+  return cudaGetLastError();
+}
+
+// The recurrence route for one parameter set (rev: on the reversed rows).
+cudaError_t launch_rows(const float* u, const float* g, const float* log_re, const float* log_im,
+                        const float* W, int B, int H, int N, int L, bool rev, float4* part,
+                        float* d_log_re, float* d_log_im, float* dW, cudaStream_t s) {
   const int wpr = (N + 31) / 32;
   const int64_t warps = (int64_t)B * H * wpr;
   const int64_t blocks = (warps + kGradWarps - 1) / kGradWarps;
   dlr_grad_rows<<<(unsigned)blocks, kGradWarps * 32, 0, s>>>(u, g, log_re, log_im, B, H, N, L,
-                                                              wpr, part);
+                                                              wpr, rev ? 1 : 0, part);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t hn = (int64_t)H * N;
@@ -386,6 +436,74 @@ cudaError_t launch_dlr_grad_params(const float* u, const float* g, const float* 
       part, log_re, reinterpret_cast<const float2*>(W), B, H, N, d_log_re, d_log_im,
       reinterpret_cast<float2*>(dW));
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dlr_kernel_complex(const float* log_re, const float* log_im, const float* W,
+                                      int H, int N, int L, float2* K, cudaStream_t s);
+
+size_t grads_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t L, bool bidir, bool prod) {
+  size_t total = 0;
+  carve_grads(nullptr, B, H, N, L, bidir, prod, &total);
+  return total;
+}
+
+size_t grad_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t L) {
+  return grads_workspace_bytes(B, H, N, L, false, false);
+}
+
+// The parameter gradients of the causal (lr2 == nullptr) or bidirectional layer in either
+// cast. The second direction is the causal layer on the reversed rows with the second
+// parameter set: its correlation is c at negative lags, its recurrences run on reversed rows.
+// The DLR-prod cast takes the correlation route (L <= 8192).
+cudaError_t launch_dlr_grads(const float* u, const float* g, const float* lr1, const float* li1,
+                             const float* W1, const float* lr2, const float* li2,
+                             const float* W2, int B, int H, int N, int L, bool prod,
+                             float* dr1, float* di1, float* dW1, float* dr2, float* di2,
+                             float* dW2, void* ws, cudaStream_t s) {
+  const bool bidir = lr2 != nullptr;
+  const GradWs w = carve_grads(ws, B, H, N, L, bidir, prod, nullptr);
+  cudaError_t e;
+  if (!corr_route(N, L, prod)) {
+    if ((e = launch_rows(u, g, lr1, li1, W1, B, H, N, L, false, w.part, dr1, di1, dW1, s)) !=
+        cudaSuccess)
+      return e;
+    if (bidir)
+      return launch_rows(u, g, lr2, li2, W2, B, H, N, L, true, w.part, dr2, di2, dW2, s);
+    return cudaSuccess;
+  }
+  if (L > 8192) return cudaErrorInvalidValue;
+  const int lg = corr_log2_size(L);
+  if ((e = launch_twiddle_table(w.tw, lg, s)) != cudaSuccess) return e;
+  switch (lg) {
+#define CORR_CASE(G) \
+  case G: e = launch_corr<G>(u, g, B, H, L, w.tw, w.c, w.c2, s); break;
+    CORR_CASE(0) CORR_CASE(1) CORR_CASE(2) CORR_CASE(3) CORR_CASE(4) CORR_CASE(5)
+    CORR_CASE(6) CORR_CASE(7) CORR_CASE(8) CORR_CASE(9) CORR_CASE(10) CORR_CASE(11)
+    CORR_CASE(12) CORR_CASE(13) CORR_CASE(14)
+#undef CORR_CASE
+    default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return e;
+  if (prod) {
+    if ((e = launch_dlr_kernel_complex(lr1, li1, W1, H, N, L, w.k1, s)) != cudaSuccess) return e;
+    if (bidir && (e = launch_dlr_kernel_complex(lr2, li2, W2, H, N, L, w.k2, s)) != cudaSuccess)
+      return e;
+  }
+  if ((e = launch_moments(w.c, w.k1, prod, lr1, li1, W1, H, N, L, dr1, di1, dW1, s)) !=
+      cudaSuccess)
+    return e;
+  if (bidir) return launch_moments(w.c2, w.k2, prod, lr2, li2, W2, H, N, L, dr2, di2, dW2, s);
+  return cudaSuccess;
+}
+
+cudaError_t launch_dlr_grad_params(const float* u, const float* g, const float* log_re,
+                                   const float* log_im, const float* W, int B, int H, int N,
+                                   int L, float* d_log_re, float* d_log_im, float* dW, void* ws,
+                                   cudaStream_t s) {
+  return launch_dlr_grads(u, g, log_re, log_im, W, nullptr, nullptr, nullptr, B, H, N, L, false,
+                          d_log_re, d_log_im, dW, nullptr, nullptr, nullptr, ws, s);
 }
 
 }  // namespace dlr

@@ -55,7 +55,8 @@ __device__ __forceinline__ void group_sync(int g) {
   else asm volatile("bar.sync 2, 128;" ::: "memory");
 }
 
-template <bool kReIm, int kNB>
+// kMode: 0 writes Re K, 1 Re K * Im K (DLR-prod), 2 the complex K as float2 pairs.
+template <int kMode, int kNB>
 __global__ void __launch_bounds__(kThreads)
 dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_im,
                const float2* __restrict__ W, int N, int L, float* __restrict__ K) {
@@ -145,7 +146,7 @@ dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_i
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           acc_re[i][k] = fmaf(a[i].x, b[k].x, fmaf(-a[i].y, b[k].y, acc_re[i][k]));
-          if (kReIm) acc_im[i][k] = fmaf(a[i].x, b[k].y, fmaf(a[i].y, b[k].x, acc_im[i][k]));
+          if (kMode != 0) acc_im[i][k] = fmaf(a[i].x, b[k].y, fmaf(a[i].y, b[k].x, acc_im[i][k]));
         }
     }
     group_sync(g);
@@ -161,7 +162,7 @@ dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_i
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         red[(i * 4 + k) * kGroup + tid] = acc_re[i][k];
-        if (kReIm) red[(16 + i * 4 + k) * kGroup + tid] = acc_im[i][k];
+        if (kMode != 0) red[(16 + i * 4 + k) * kGroup + tid] = acc_im[i][k];
       }
   }
   __syncthreads();
@@ -171,10 +172,23 @@ dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_i
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       acc_re[i][k] += red[(i * 4 + k) * kGroup + tid];
-      if (kReIm) acc_im[i][k] += red[(16 + i * 4 + k) * kGroup + tid];
+      if (kMode != 0) acc_im[i][k] += red[(16 + i * 4 + k) * kGroup + tid];
     }
 
   // 6) store: row h, j = j0 + c T + t for t in {2 tx, 2 tx + 1} and {32 + 2 tx, 33 + 2 tx}
+  if constexpr (kMode == 2) {
+    float2* kc = reinterpret_cast<float2*>(K) + (size_t)h * L;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int jc = j0 + (ty + 8 * i) * kT;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int j = jc + 32 * (k >> 1) + 2 * tx + (k & 1);
+        if (j < L && DLR_IN(j, L)) kc[j] = make_float2(acc_re[i][k], acc_im[i][k]);
+      }
+    }
+    return;
+  }
   float* krow = K + (size_t)h * L;
   const bool vec = ((L & 1) == 0);
 #pragma unroll
@@ -182,7 +196,7 @@ dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_i
     const int jc = j0 + (ty + 8 * i) * kT;
     float v[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) v[k] = kReIm ? acc_re[i][k] * acc_im[i][k] : acc_re[i][k];
+    for (int k = 0; k < 4; ++k) v[k] = kMode == 1 ? acc_re[i][k] * acc_im[i][k] : acc_re[i][k];
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int j = jc + 32 * half + 2 * tx;
@@ -196,13 +210,13 @@ dlr_kernel_gen(const float* __restrict__ log_re, const float* __restrict__ log_i
   }
 }
 
-template <bool kReIm, int kNB>
+template <int kMode, int kNB>
 cudaError_t launch_gen(const float* log_re, const float* log_im, const float* W, int H, int N,
                        int L, float* K, cudaStream_t s) {
   dim3 grid((L + kT * kC - 1) / (kT * kC), H);
-  cudaError_t e = max_smem_once<dlr_kernel_gen<kReIm, kNB>>(gen_smem<kNB>());
+  cudaError_t e = max_smem_once<dlr_kernel_gen<kMode, kNB>>(gen_smem<kNB>());
   if (e != cudaSuccess) return e;
-  dlr_kernel_gen<kReIm, kNB><<<grid, kThreads, gen_smem<kNB>(), s>>>(
+  dlr_kernel_gen<kMode, kNB><<<grid, kThreads, gen_smem<kNB>(), s>>>(
       log_re, log_im, reinterpret_cast<const float2*>(W), N, L, K);
   return cudaGetLastError();
 }
@@ -220,8 +234,14 @@ cudaError_t launch_dlr_kernel(const float* log_re, const float* log_im, const fl
                               int N, int L, bool re_im, float* K, int* status, cudaStream_t s) {
   if (N >= 256 || (N >= 64 && L >= 16384))
     return launch_dlr_kernel_tc(log_re, log_im, W, H, N, L, re_im, K, status, s);
-  return re_im ? launch_gen<true, 16>(log_re, log_im, W, H, N, L, K, s)
-               : launch_gen<false, 16>(log_re, log_im, W, H, N, L, K, s);
+  return re_im ? launch_gen<1, 16>(log_re, log_im, W, H, N, L, K, s)
+               : launch_gen<0, 16>(log_re, log_im, W, H, N, L, K, s);
+}
+
+// The complex kernel K [H, L] as float2 pairs (any N, on FFMA; for the DLR-prod gradients).
+cudaError_t launch_dlr_kernel_complex(const float* log_re, const float* log_im, const float* W,
+                                      int H, int N, int L, float2* K, cudaStream_t s) {
+  return launch_gen<2, 16>(log_re, log_im, W, H, N, L, reinterpret_cast<float*>(K), s);
 }
 
 }  // namespace dlr

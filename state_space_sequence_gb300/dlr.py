@@ -76,6 +76,10 @@ def _load():
         lib.dlr_scan_backward_params.argtypes = [P, P, P, P, P, i64, i64, i64, i64, P, P, P, P,
                                                  sz, P]
         lib.dlr_scan_backward_params.restype = i32
+        lib.dlr_layer_backward_workspace_size.argtypes = [i64, i64, i64, i64, i32, i32]
+        lib.dlr_layer_backward_workspace_size.restype = sz
+        lib.dlr_layer_backward.argtypes = [P] * 8 + [i32, i32] + [i64] * 4 + [P] * 8 + [sz, P]
+        lib.dlr_layer_backward.restype = i32
         lib.dlr_scan_backward_input.restype = i32
         lib.dlr_step_workspace_size.argtypes = [i64, i64]
         lib.dlr_step_workspace_size.restype = sz
@@ -331,6 +335,43 @@ def dlr_scan_backward_params(u, g, params, workspace=None, stream=None):
                                          L, _ptr(d_re), _ptr(d_im), _ptr(dW), _ptr(workspace),
                                          workspace.numel(), _stream(stream)))
     return d_re, d_im, dW
+
+
+def dlr_layer_backward_workspace_size(B: int, H: int, N: int, L: int, bidir: bool = False,
+                                      cast: str = "re") -> int:
+    """Bytes of device workspace dlr_layer_backward needs (0 for arguments out of range)."""
+    return int(_load().dlr_layer_backward_workspace_size(B, H, N, L, 1 if bidir else 0,
+                                                         CAST[cast]))
+
+
+def dlr_layer_backward(u, g, fwd, bwd=None, cast: str = "re", input_grad: bool = True,
+                       workspace=None, stream=None):
+    """Gradients of the DLR layer (causal, or bidirectional with the second parameter set
+    `bwd`; Re or DLR-prod cast) for input u and output gradient g [B, H, L]. Returns
+    (du or None, [(d_log_re, d_log_im, dW) per direction])."""
+    _check_f32(u, g)
+    lr, li, W = _params(fwd)
+    B, H, L = u.shape
+    N = lr.shape[1]
+    if bwd is not None:
+        lr2, li2, W2 = _params(bwd)
+    else:
+        lr2 = li2 = W2 = None
+    if workspace is None:
+        need = dlr_layer_backward_workspace_size(B, H, N, L, bwd is not None, cast)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=u.device)
+    du = torch.empty_like(u) if input_grad else None
+    outs = [(torch.empty_like(lr), torch.empty_like(li), torch.empty_like(W))]
+    if bwd is not None:
+        outs.append((torch.empty_like(lr2), torch.empty_like(li2), torch.empty_like(W2)))
+    o2 = outs[1] if bwd is not None else (None, None, None)
+    _ok("dlr_layer_backward",
+        _load().dlr_layer_backward(_ptr(u), _ptr(g), _ptr(lr), _ptr(li), _ptr(W), _ptr(lr2),
+                                   _ptr(li2), _ptr(W2), 1 if bwd is not None else 0, CAST[cast],
+                                   B, H, N, L, _ptr(du), *[_ptr(t) for t in outs[0]],
+                                   *[_ptr(t) for t in o2], _ptr(workspace), workspace.numel(),
+                                   _stream(stream)))
+    return du, outs
 
 
 def dlr_scan_backward_input(g, params, workspace=None, out=None, stream=None):

@@ -115,6 +115,21 @@ def run():
         record(f"backward parameters N{N} L{L}", got,
                np.concatenate([r_re.ravel(), r_im.ravel(), r_W.ravel()]))
 
+    # the layer's gradients: both directions, both casts, both routes
+    for bidir, cast, B, H, N, L in [(True, "re", 2, 2, 16, 300), (True, "re", 2, 1, 8, 300),
+                                    (True, "re_im", 2, 2, 20, 500), (False, "re_im", 1, 1, 8, 33)]:
+        w = inputs.make_dlr(B, H, N, L, seed=N + L, bidir=bidir, unit_channels=1)
+        g = np.random.default_rng(L).standard_normal(w.u.shape).astype(np.float32)
+        bwd = pnp(w.bwd) if bidir else None
+        du, grads = dlr.dlr_layer_backward(dev(w.u), dev(g), pdev(w.fwd),
+                                           pdev(w.bwd) if bidir else None, cast=cast)
+        r_du, r_grads = oracle.dlr_layer_backward(w.u, g, pnp(w.fwd), bwd, cast=cast)
+        record(f"layer backward du {cast} bidir={bidir} N{N} L{L}", host(du), r_du)
+        for d, (gr, rg) in enumerate(zip(grads, r_grads)):
+            got = np.concatenate([host(t).ravel() for t in gr])
+            record(f"layer backward grads {d} {cast} bidir={bidir} N{N} L{L}", got,
+                   np.concatenate([t.ravel() for t in rg]))
+
     # S5: float32 and bf16 tiers (L a multiple of 64 takes the fused output projection),
     # bilinear, a step that changes from step to step
     for B, L, H, P in [(2, 63, 32, 32), (1, 128, 64, 32)]:

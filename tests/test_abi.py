@@ -48,7 +48,7 @@ def test_status_strings_and_version(lib):
     assert lib.dlr_status_string(0) == b"DLR_OK"
     assert lib.dlr_status_string(4) == b"DLR_ERR_TIMEOUT"
     assert lib.dlr_status_string(6) == b"DLR_ERR_BOUNDS"
-    assert lib.dlr_abi_version() == 11
+    assert lib.dlr_abi_version() == 12
 
 
 def test_normal_build_has_no_bounds_checks(lib):
@@ -258,9 +258,9 @@ def test_backward_params_validation(lib):
     lib.dlr_scan_backward_params_workspace_size.restype = sz
     wsz = lib.dlr_scan_backward_params_workspace_size
     # correlation route (N >= 16, L <= 8192): the M-point twiddle table (M = 2^ceil(log2(2L-1)))
-    # and c [H, L]; otherwise 16 bytes per (b, h, n)
+    # and c [H, L]; otherwise 16 bytes per (b, h, n); each part rounded up to 256 bytes
     assert wsz(8, 256, 64, 4096) == 8 * 8192 + 4 * 256 * 4096
-    assert wsz(2, 3, 16, 5) == 256 + 4 * 3 * 5                  # M = 16, table padded to 256 B
+    assert wsz(2, 3, 16, 5) == 256 + 256                         # M = 16; c of 60 bytes
     assert wsz(8, 256, 8, 4096) == 16 * 8 * 256 * 8              # few states
     assert wsz(8, 256, 64, 8193) == 16 * 8 * 256 * 64            # long rows
     assert wsz(0, 1, 1, 1) == 0
@@ -281,6 +281,50 @@ def test_backward_params_validation(lib):
     assert call(u, g, lr, li, W, 2, 3, 4, 1 << 24, dr, di, dW, ws, need, None) == 2
     assert call(u, g, lr, li, W, 2, 3, 4, 10, dr, di, dW, None, 0, None) == 5
     assert call(u, g, lr, li, W, 2, 3, 4, 10, dr, di, dW, ws, need - 16, None) == 5
+
+
+def test_layer_backward_validation(lib):
+    """dlr_layer_backward: directions and casts, the second parameter set given exactly when
+    bidirectional, output alignment and overlaps, the DLR-prod cast's row limit and the
+    workspace are checked on the host; the workspace size is the gradients' part, two kernel
+    buffers and the convolution workspace."""
+    P, i64, sz, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_size_t, ctypes.c_int
+    lib.dlr_layer_backward_workspace_size.argtypes = [i64] * 4 + [i32, i32]
+    lib.dlr_layer_backward_workspace_size.restype = sz
+    lib.dlr_conv_workspace_size.argtypes = [i64, i64, i32]
+    lib.dlr_conv_workspace_size.restype = sz
+    lib.dlr_layer_backward.argtypes = [P] * 8 + [i32, i32] + [i64] * 4 + [P] * 8 + [sz, P]
+    wsz = lib.dlr_layer_backward_workspace_size
+    conv = lib.dlr_conv_workspace_size(256, 4096, 0)
+    # causal Re, correlation route: table 64 KB + c 4 MB; kernels 2 x 4 MB; convolution
+    assert wsz(8, 256, 64, 4096, 0, 0) == 8 * 8192 + 4 * 256 * 4096 + 2 * 4 * 256 * 4096 + conv
+    # bidirectional DLR-prod: + c2 4 MB + two complex kernels of 8 MB
+    assert wsz(8, 256, 64, 4096, 1, 1) == (8 * 8192 + 2 * 4 * 256 * 4096 + 2 * 8 * 256 * 4096 +
+                                          2 * 4 * 256 * 4096 + conv)
+    assert wsz(8, 256, 64, 8193, 0, 1) == 0      # DLR-prod needs L <= 8192
+    assert wsz(1, 1, 1, 65537, 0, 0) == 0
+    assert wsz(1, 1, 1, 8, 2, 0) == 0
+    assert wsz(1, 1, 1, 8, 0, 2) == 0
+    u, g = ctypes.c_void_p(0x100000), ctypes.c_void_p(0x200000)
+    a = [ctypes.c_void_p(0x300000 + 0x10000 * i) for i in range(6)]   # two parameter sets
+    o = [ctypes.c_void_p(0x400000 + 0x10000 * i) for i in range(6)]   # their gradients
+    du, ws = ctypes.c_void_p(0x500000), ctypes.c_void_p(0x1000000)
+    call = lib.dlr_layer_backward
+    need = wsz(2, 3, 20, 100, 1, 0)
+    assert need > 0
+    ok = (u, g, *a, 1, 0, 2, 3, 20, 100, du, *o, ws, need, None)
+    assert call(*ok[:8], 2, *ok[9:]) == 1                                      # direction
+    assert call(*ok[:9], 2, *ok[10:]) == 1                                     # cast
+    assert call(u, g, *a[:3], None, None, None, *ok[8:]) == 1                  # bidir: set 2
+    assert call(u, g, *a[:3], None, None, None, 0, 0, 2, 3, 20, 100, du, *o[:3], *o[:3], ws,
+                need, None) == 1                                               # causal: no set 2
+    assert call(*ok[:14], ctypes.c_void_p(0x500004), *ok[15:]) == 1           # du alignment
+    assert call(*ok[:15], a[0], *ok[16:]) == 1                                 # output on input
+    assert call(*ok[:15], o[0], o[0], *ok[17:]) == 1                          # outputs overlap
+    assert call(*ok[:14], u, *ok[15:]) == 1                                    # du on u
+    assert call(*ok[:9], 1, 2, 3, 20, 9000, *ok[14:]) == 2                     # DLR-prod, long
+    assert call(*ok[:-3], None, 0, None) == 5
+    assert call(*ok[:-2], need - 16, None) == 5
 
 
 def test_variant_entry_points_validation(lib):

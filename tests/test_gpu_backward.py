@@ -73,3 +73,47 @@ def test_backward_params_linear_in_g():
     for x, y, z in zip(a, b, c):
         ref = host(x) + 2 * host(y)
         assert oracle.rel_l2(host(z), ref) <= 1e-5
+
+
+@pytest.mark.parametrize("bidir,cast,B,H,N,L", [
+    (False, "re", 2, 3, 16, 300),        # correlation route; du by the FFT convolution
+    (True, "re", 2, 3, 16, 300),         # both directions: c at positive and negative lags
+    (True, "re", 3, 2, 8, 1000),         # recurrence route, the second direction on reversed rows
+    (True, "re", 1, 2, 20, 9000),        # recurrence route, rows longer than 8192
+    (False, "re_im", 2, 2, 24, 777),     # DLR-prod: weights c_j K_j
+    (True, "re_im", 3, 2, 40, 1000),
+    (True, "re_im", 1, 1, 8, 8192),      # DLR-prod with few states, the largest transform
+    (True, "re", 2, 2, 16, 20000),       # du on the 8-CTA cluster transform
+])
+def test_layer_backward_matches_oracle(bidir, cast, B, H, N, L):
+    """dlr_layer_backward against the oracle's dlr_layer_backward: du and the three gradients
+    of each direction, causal and bidirectional, Re and DLR-prod casts, both routes."""
+    w = inputs.make_dlr(B, H, N, L, seed=B * 13 + N + L + (7 if bidir else 0), bidir=bidir,
+                        unit_channels=1)
+    g = np.random.default_rng(N + L).standard_normal((B, H, L)).astype(np.float32)
+    fwd = (w.fwd.log_re, w.fwd.log_im, w.fwd.W)
+    bwd = (w.bwd.log_re, w.bwd.log_im, w.bwd.W) if bidir else None
+    du, grads = dlr.dlr_layer_backward(dev(w.u), dev(g), tuple(dev(a) for a in fwd),
+                                       tuple(dev(a) for a in bwd) if bidir else None, cast=cast)
+    r_du, r_grads = oracle.dlr_layer_backward(w.u, g, fwd, bwd, cast=cast)
+    assert oracle.rel_l2(host(du), r_du) <= TOL
+    assert len(grads) == len(r_grads) == (2 if bidir else 1)
+    for got, ref in zip(grads, r_grads):
+        for a, b in zip(got, ref):
+            assert oracle.rel_l2(host(a), b) <= TOL
+    assert dlr.device_status() == 0
+
+
+def test_layer_backward_causal_re_equals_the_scan_gradients():
+    """The causal Re-cast case of dlr_layer_backward gives the parameter gradients of
+    dlr_scan_backward_params (the same kernels) and, by another route (FFT convolution against
+    the tensor-core scan's reversed pass), the input gradient of dlr_scan_backward_input."""
+    w = inputs.make_dlr(4, 3, 32, 1500, seed=21, unit_channels=1)
+    g = np.random.default_rng(5).standard_normal(w.u.shape).astype(np.float32)
+    p = tuple(dev(a) for a in (w.fwd.log_re, w.fwd.log_im, w.fwd.W))
+    u, gd = dev(w.u), dev(g)
+    du, grads = dlr.dlr_layer_backward(u, gd, p)
+    a = dlr.dlr_scan_backward_params(u, gd, p)
+    for x, y in zip(grads[0], a):
+        assert torch.equal(x, y)
+    assert oracle.rel_l2(host(du), host(dlr.dlr_scan_backward_input(gd, p))) <= TOL
