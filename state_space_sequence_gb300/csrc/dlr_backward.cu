@@ -1,4 +1,4 @@
-// dlr_backward.cu -- gradients of the causal DLR layer (Re cast) with respect to its parameters
+// dlr_backward.cu -- gradients of the DLR layer with respect to its parameters
 // ("Simplifying and Understanding State Space Models with Diagonal Linear RNNs", section 2:
 // y_k = sum_{j<=k} Re K_j u_{k-j}, K_j = sum_n W_n lambda_n^j, and the gradient analysis there,
 // d K_j / d lambda_n = W_n j lambda_n^{j-1}, d K_j / d W_n = lambda_n^j; section 2.2:
@@ -13,9 +13,17 @@
 // (the second recurrence is lambda times the derivative of x with respect to lambda), so the
 // gradients need neither the kernel nor the correlation c.
 //
+// The bidirectional layer (section 2.1: y = DLR1(u) + rev(DLR2(rev(u)))) adds the gradients of
+// the causal layer on the reversed rows with the second parameter set: its correlation is c at
+// negative lags, c_{-j} = sum_b sum_k g_{b,k} u_{b,k+j}. The DLR-prod cast (section 2.1:
+// kappa_j = Re K_j Im K_j) changes only the weights: d kappa_j = Im(K_j dK_j), so with
+// w_j = c_j K_j (K complex), S0 = sum_j w_j lambda^j, S1 = sum_j j w_j lambda^j:
+//     dW = (Im S0, Re S0),   d a = -2 a Im(W S1),   d theta = Re(W S1).
+//
 // Two routes compute S0 and S1.
 //
-// Lag correlation (N >= 16, L <= 8192): c is formed first, then the two power sums per state.
+// Lag correlation (N >= 16, L <= 8192, and the DLR-prod cast, which needs c itself): c is
+// formed first, then the two power sums per state.
 //  - grad_corr: one CTA per channel h. For each batch row, z = u + i g (zero-padded to
 //    M = 2^lg >= 2L - 1 points, so the circular correlation equals the linear one for lags
 //    0 .. L-1) is transformed once; the two real spectra come out as U_f = (Z_f + conj
