@@ -252,10 +252,13 @@ dlr_status dlr_scan_host(const float* u, const float* log_re, const float* log_i
  *   dW [H, N, 2] = (Re S0, -Im S0),  d_log_re [H, N] = -2 a Re(W S1),
  *   d_log_im [H, N] = -Im(W S1).
  * Two routes, chosen from N and L alone:
- *  - N >= 16 and L <= 8192: c itself by transforms, c = IFFT(sum_b FFT(g_b) conj FFT(u_b))
- *    with both rows of a batch entry in one complex transform of M = 2^ceil(log2(2L - 1))
- *    points, one CTA per channel; then S0 and S1 per state as sums over the lags with
- *    lambda^j = lambda^{32m} lambda^t, both factors evaluated directly from the parameters;
+ *  - N >= 16 and L <= 65536: c itself by transforms, c = IFFT(sum_b FFT(g_b) conj FFT(u_b)):
+ *    for L <= 8192 with both rows of a batch entry in one complex transform of
+ *    M = 2^ceil(log2(2L - 1)) points, one CTA per channel; for longer rows through the
+ *    spectrum and apply kernels of dlr_conv (the rows' spectra, their products summed over
+ *    the batch, the inverse by applying that spectrum to an impulse); then S0 and S1 per state
+ *    as sums over the lags with lambda^j = lambda^{32m} lambda^t, both factors evaluated
+ *    directly from the parameters;
  *  - otherwise: sums over the steps of g against the states of two recurrences driven by u,
  *    x_k = lambda x_{k-1} + u_k and D_k = lambda (D_{k-1} + x_{k-1}) (lambda times
  *    dx/d lambda): S0 = sum g x, S1 = sum g D, per (b, h, state) with lambda as a float pair,
@@ -263,8 +266,9 @@ dlr_status dlr_scan_host(const float* u, const float* log_re, const float* log_i
  * u, g [B, H, L] (4-byte aligned); parameters as in dlr_kernel; the three outputs (dW 8-byte
  * aligned) must not overlap the parameters or each other. workspace: device memory,
  * dlr_scan_backward_params_workspace_size(B, H, N, L) bytes, 16-byte aligned (the first
- * route: the M-point twiddle table and c [H, L] floats; the second: 16 * B * H * N; each part
- * rounded up to 256 bytes). Two kernel launches (three on the first route); L < 2^24,
+ * route: the M-point twiddle table and c [H, L] floats, for L > 8192 instead two dlr_conv
+ * workspaces for B * H rows, one for H rows and an impulse buffer [H, L]; the second: 16 * B *
+ * H * N; each part rounded up to 256 bytes). Two kernel launches (three on the first route); L < 2^24,
  * N <= 65536. The workspace size is 0 for arguments out of range. dlr_layer_backward gives
  * the same for the bidirectional layer and the DLR-prod cast, with the input gradient.
  */
@@ -292,15 +296,15 @@ dlr_status dlr_scan_backward_params(const float* u, const float* g, const float*
  *      DLR-prod cast (w = c K, K the complex kernel, since d kappa_j = Im(K_j dK_j)):
  *                                    dW = (Im S0, Re S0),  d_log_re = -2a Im(W S1),
  *                                    d_log_im = Re(W S1).
- *    As dlr_scan_backward_params: c by transforms when N >= 16 and L <= 8192 (and always for
- *    the DLR-prod cast, which needs c itself), else the blocked recurrences (on the reversed
- *    rows for the second direction).
+ *    As dlr_scan_backward_params: c by transforms when N >= 16 (and always for the DLR-prod
+ *    cast, which needs c itself), else the blocked recurrences (on the reversed rows for the
+ *    second direction).
  * u, g, du 16-byte aligned; parameters as in dlr_kernel, the second set (and its three
  * outputs) given exactly when dir == DLR_BIDIR; outputs as dlr_scan_backward_params (none may
  * overlap a parameter, another output, u, g or the workspace). workspace: device memory,
  * dlr_layer_backward_workspace_size(B, H, N, L, dir, cast) bytes (0 for arguments out of
- * range), 16-byte aligned. Limits: L <= 65536 (L <= 8192 for the DLR-prod cast, else
- * DLR_ERR_UNSUPPORTED), N <= 65536. Faults of the tensor-core kernel generator's bounded
+ * range), 16-byte aligned. Limits: L <= 65536, N <= 65536. Faults of the tensor-core kernel
+ * generator's bounded
  * waits (N >= 256, or N >= 64 at L >= 16384) are reported through dlr_get_device_status().
  */
 size_t dlr_layer_backward_workspace_size(int64_t B, int64_t H, int64_t N, int64_t L,

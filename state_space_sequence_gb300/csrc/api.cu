@@ -383,7 +383,6 @@ size_t dlr_layer_backward_workspace_size(int64_t B, int64_t H, int64_t N, int64_
   if (B < 1 || H < 1 || N < 1 || L < 1 || L > 65536) return 0;
   if (dir != DLR_CAUSAL && dir != DLR_BIDIR) return 0;
   if (cast != DLR_CAST_RE && cast != DLR_CAST_RE_IM) return 0;
-  if (cast == DLR_CAST_RE_IM && L > 8192) return 0;
   const size_t hl = sizeof(float) * (size_t)H * (size_t)L;
   return layer_bwd_grads_bytes(B, H, N, L, dir == DLR_BIDIR, cast == DLR_CAST_RE_IM) +
          2 * round256(hl) + dlr::conv_workspace_bytes(H, L);
@@ -432,7 +431,6 @@ dlr_status dlr_layer_backward(const float* u, const float* g, const float* log_r
       if (ranges_overlap(du, bytes, outs[i], sz[i])) return DLR_ERR_INVALID_ARG;
   }
   if (L > 65536 || N > 65536 || B * H > kMaxGrid / 64) return DLR_ERR_UNSUPPORTED;
-  if (prod && L > 8192) return DLR_ERR_UNSUPPORTED;
   const size_t need = dlr_layer_backward_workspace_size(B, H, N, L, dir, cast);
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DLR_ERR_WORKSPACE;
   if (ranges_overlap(workspace, need, u, bytes) || ranges_overlap(workspace, need, g, bytes) ||

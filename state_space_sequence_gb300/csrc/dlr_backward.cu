@@ -22,8 +22,9 @@
 //
 // Two routes compute S0 and S1.
 //
-// Lag correlation (N >= 16, L <= 8192, and the DLR-prod cast, which needs c itself): c is
-// formed first, then the two power sums per state.
+// Lag correlation (N >= 16 or the DLR-prod cast, which needs c itself; L <= 65536): c is
+// formed first, then the two power sums per state. Rows of up to 8192 take grad_corr below;
+// longer rows take the FFT convolution's own spectrum and apply kernels (grad_cross).
 //  - grad_corr: one CTA per channel h. For each batch row, z = u + i g (zero-padded to
 //    M = 2^lg >= 2L - 1 points, so the circular correlation equals the linear one for lags
 //    0 .. L-1) is transformed once; the two real spectra come out as U_f = (Z_f + conj
@@ -63,6 +64,15 @@ namespace dlr {
 [[maybe_unused]] constexpr int kSiteFile = 2;
 
 cudaError_t launch_twiddle_table(float2* tw, int logn, cudaStream_t s);
+// the FFT convolution (dlr_conv.cu), for the correlation of rows longer than 8192
+int conv_log2_size(int64_t L);
+size_t conv_workspace_bytes(int64_t H, int64_t L);
+float2* conv_spectra(void* ws, int64_t L);
+cudaError_t launch_dlr_conv_spectrum(const float* K1, const float* K2, int H, int L, void* ws,
+                                     cudaStream_t s);
+cudaError_t launch_twiddles(int lg, void* ws, cudaStream_t s);
+cudaError_t launch_dlr_conv_apply(const float* u, int B, int H, int L, float* y, const void* ws,
+                                  cudaStream_t s);
 
 namespace {
 
@@ -261,6 +271,35 @@ __global__ void __launch_bounds__(fftr::Plan<kLog>::T, kLog <= 13 ? 2 : 1)
   }
 }
 
+// ---- lag correlation of rows longer than 8192, through the FFT convolution's kernels ----
+// The convolution's spectrum kernel, run on the rows of u and of g as if they were kernel
+// columns, stores their zero-padded spectra as X/(4n) (n + 1 bins of the 2n-point real
+// transform); A = (4n) sum_b G conj(U) is then stored as the spectrum of the real column c
+// (c_j at j, c_{-j} at 2n - j), and the convolution's apply kernel on an impulse returns that
+// column's first L entries: c. With conj(A) it returns the negative lags.
+__global__ void grad_cross(const float2* __restrict__ su, const float2* __restrict__ sg, int B,
+                           int H, int nb, float scale, float2* __restrict__ a) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // h * nb + f
+  if (i >= (int64_t)H * nb) return;
+  const int64_t h = i / nb, f = i - h * nb;
+  float ar = 0.f, ai = 0.f;
+  for (int b = 0; b < B; ++b) {
+    const int64_t o = ((int64_t)b * H + h) * nb + f;
+    const float2 x = su[o], y = sg[o];
+    ar = fmaf(y.x, x.x, fmaf(y.y, x.y, ar));   // Re G conj(U)
+    ai = fmaf(y.y, x.x, fmaf(-y.x, x.y, ai));  // Im G conj(U)
+  }
+  if (DLR_IN(i, (int64_t)H * nb)) a[i] = make_float2(ar * scale, ai * scale);
+}
+__global__ void conj_spectra(float2* __restrict__ a, int64_t count) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < count) a[i].y = -a[i].y;
+}
+__global__ void impulse_rows(float* __restrict__ d, int H, int L) {  // d zeroed before
+  const int h = blockIdx.x * blockDim.x + threadIdx.x;
+  if (h < H && DLR_IN((int64_t)h * L, (int64_t)H * L)) d[(size_t)h * L] = 1.f;
+}
+
 constexpr int kMomWarps = 8;   // warps per block
 constexpr int kMomStates = 4;  // states per warp
 
@@ -373,7 +412,10 @@ int corr_log2_size(int64_t L) {
   return lg;
 }
 
-bool corr_route(int64_t N, int64_t L, bool prod) { return prod || (N >= 16 && L <= 8192); }
+// Correlation routes: one CTA per channel (L <= 8192) or through the convolution's kernels
+// (L <= 65536); otherwise the blocked recurrences (Re cast only).
+bool corr_route(int64_t N, int64_t L, bool prod) { return (prod || N >= 16) && L <= 65536; }
+bool corr_long(int64_t L) { return L > 8192; }
 
 size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
 
@@ -386,6 +428,8 @@ struct GradWs {
   float *c, *c2;
   float2 *k1, *k2;
   float4* part;
+  void *su, *sg, *sa;  // long rows: convolution workspaces of the u rows, g rows, channels
+  float* imp;          // long rows: the impulse rows [H, L]
 };
 GradWs carve_grads(void* ws, int64_t B, int64_t H, int64_t N, int64_t L, bool bidir, bool prod,
                    size_t* total) {
@@ -399,7 +443,14 @@ GradWs carve_grads(void* ws, int64_t B, int64_t H, int64_t N, int64_t L, bool bi
   };
   if (corr_route(N, L, prod)) {
     const size_t hl = (size_t)H * (size_t)L;
-    w.tw = reinterpret_cast<float2*>(take(sizeof(float2) << corr_log2_size(L)));
+    if (corr_long(L)) {
+      w.su = take(conv_workspace_bytes(B * H, L));
+      w.sg = take(conv_workspace_bytes(B * H, L));
+      w.sa = take(conv_workspace_bytes(H, L));
+      w.imp = reinterpret_cast<float*>(take(sizeof(float) * hl));
+    } else {
+      w.tw = reinterpret_cast<float2*>(take(sizeof(float2) << corr_log2_size(L)));
+    }
     w.c = reinterpret_cast<float*>(take(sizeof(float) * hl));
     if (bidir) w.c2 = reinterpret_cast<float*>(take(sizeof(float) * hl));
     if (prod) w.k1 = reinterpret_cast<float2*>(take(sizeof(float2) * hl));
@@ -481,19 +532,40 @@ cudaError_t launch_dlr_grads(const float* u, const float* g, const float* lr1, c
       return launch_rows(u, g, lr2, li2, W2, B, H, N, L, true, w.part, dr2, di2, dW2, s);
     return cudaSuccess;
   }
-  if (L > 8192) return cudaErrorInvalidValue;
-  const int lg = corr_log2_size(L);
-  if ((e = launch_twiddle_table(w.tw, lg, s)) != cudaSuccess) return e;
-  switch (lg) {
+  if (L > 65536) return cudaErrorInvalidValue;
+  if (corr_long(L)) {
+    const int n = 1 << conv_log2_size(L);
+    const int nb = n + 1;
+    if ((e = launch_dlr_conv_spectrum(u, nullptr, B * H, L, w.su, s)) != cudaSuccess) return e;
+    if ((e = launch_dlr_conv_spectrum(g, nullptr, B * H, L, w.sg, s)) != cudaSuccess) return e;
+    float2* a = conv_spectra(w.sa, L);
+    const int64_t bins = (int64_t)H * nb;
+    grad_cross<<<(unsigned)((bins + 255) / 256), 256, 0, s>>>(
+        conv_spectra(w.su, L), conv_spectra(w.sg, L), B, H, nb, 4.0f * (float)n, a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_twiddles(conv_log2_size(L), w.sa, s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(w.imp, 0, sizeof(float) * (size_t)H * L, s)) != cudaSuccess)
+      return e;
+    impulse_rows<<<(H + 255) / 256, 256, 0, s>>>(w.imp, H, L);
+    if ((e = launch_dlr_conv_apply(w.imp, 1, H, L, w.c, w.sa, s)) != cudaSuccess) return e;
+    if (bidir) {
+      conj_spectra<<<(unsigned)((bins + 255) / 256), 256, 0, s>>>(a, bins);
+      if ((e = launch_dlr_conv_apply(w.imp, 1, H, L, w.c2, w.sa, s)) != cudaSuccess) return e;
+    }
+  } else {
+    const int lg = corr_log2_size(L);
+    if ((e = launch_twiddle_table(w.tw, lg, s)) != cudaSuccess) return e;
+    switch (lg) {
 #define CORR_CASE(G) \
   case G: e = launch_corr<G>(u, g, B, H, L, w.tw, w.c, w.c2, s); break;
-    CORR_CASE(0) CORR_CASE(1) CORR_CASE(2) CORR_CASE(3) CORR_CASE(4) CORR_CASE(5)
-    CORR_CASE(6) CORR_CASE(7) CORR_CASE(8) CORR_CASE(9) CORR_CASE(10) CORR_CASE(11)
-    CORR_CASE(12) CORR_CASE(13) CORR_CASE(14)
+      CORR_CASE(0) CORR_CASE(1) CORR_CASE(2) CORR_CASE(3) CORR_CASE(4) CORR_CASE(5)
+      CORR_CASE(6) CORR_CASE(7) CORR_CASE(8) CORR_CASE(9) CORR_CASE(10) CORR_CASE(11)
+      CORR_CASE(12) CORR_CASE(13) CORR_CASE(14)
 #undef CORR_CASE
-    default: return cudaErrorInvalidValue;
+      default: return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
   }
-  if (e != cudaSuccess) return e;
   if (prod) {
     if ((e = launch_dlr_kernel_complex(lr1, li1, W1, H, N, L, w.k1, s)) != cudaSuccess) return e;
     if (bidir && (e = launch_dlr_kernel_complex(lr2, li2, W2, H, N, L, w.k2, s)) != cudaSuccess)

@@ -605,6 +605,11 @@ cudaError_t launch_twiddles(int lg, void* ws, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// The spectra region of a convolution workspace for rows of L (n = 2^conv_log2_size(L) + 1
+// bins per row, in the transform's own bin order), for another module that forms spectra
+// pointwise from spectra this file wrote.
+float2* conv_spectra(void* ws, int64_t L) { return carve_conv(ws, conv_log2_size(L)).spec; }
+
 // tw[m] = exp(-2 pi i m / n), m < n = 2^logn, for another module's transforms.
 cudaError_t launch_twiddle_table(float2* tw, int logn, cudaStream_t s) {
   twiddle_table<<<((1 << logn) + 255) / 256, 256, 0, s>>>(tw, logn, nullptr);

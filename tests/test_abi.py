@@ -262,7 +262,15 @@ def test_backward_params_validation(lib):
     assert wsz(8, 256, 64, 4096) == 8 * 8192 + 4 * 256 * 4096
     assert wsz(2, 3, 16, 5) == 256 + 256                         # M = 16; c of 60 bytes
     assert wsz(8, 256, 8, 4096) == 16 * 8 * 256 * 8              # few states
-    assert wsz(8, 256, 64, 8193) == 16 * 8 * 256 * 64            # long rows
+    # rows longer than 8192: two dlr_conv workspaces for the B * H rows, one for the H
+    # channels, the impulse rows and c; rows longer than 65536: the recurrences
+    lib.dlr_conv_workspace_size.argtypes = [i64, i64, ctypes.c_int]
+    lib.dlr_conv_workspace_size.restype = sz
+    r256 = lambda b: (b + 255) // 256 * 256
+    cw = lib.dlr_conv_workspace_size
+    assert wsz(8, 256, 64, 8193) == (2 * r256(cw(8 * 256, 8193, 0)) + r256(cw(256, 8193, 0)) +
+                                     2 * r256(4 * 256 * 8193))
+    assert wsz(8, 256, 64, 65537) == 16 * 8 * 256 * 64
     assert wsz(0, 1, 1, 1) == 0
     assert wsz(1, 1, 1, 0) == 0
     assert wsz(1, 1, 1, 1 << 24) == 0
@@ -301,7 +309,7 @@ def test_layer_backward_validation(lib):
     # bidirectional DLR-prod: + c2 4 MB + two complex kernels of 8 MB
     assert wsz(8, 256, 64, 4096, 1, 1) == (8 * 8192 + 2 * 4 * 256 * 4096 + 2 * 8 * 256 * 4096 +
                                           2 * 4 * 256 * 4096 + conv)
-    assert wsz(8, 256, 64, 8193, 0, 1) == 0      # DLR-prod needs L <= 8192
+    assert wsz(8, 256, 64, 65537, 0, 1) == 0
     assert wsz(1, 1, 1, 65537, 0, 0) == 0
     assert wsz(1, 1, 1, 8, 2, 0) == 0
     assert wsz(1, 1, 1, 8, 0, 2) == 0
@@ -322,7 +330,7 @@ def test_layer_backward_validation(lib):
     assert call(*ok[:15], a[0], *ok[16:]) == 1                                 # output on input
     assert call(*ok[:15], o[0], o[0], *ok[17:]) == 1                          # outputs overlap
     assert call(*ok[:14], u, *ok[15:]) == 1                                    # du on u
-    assert call(*ok[:9], 1, 2, 3, 20, 9000, *ok[14:]) == 2                     # DLR-prod, long
+    assert call(*ok[:9], 1, 2, 3, 20, 65537, *ok[14:]) == 2                    # rows too long
     assert call(*ok[:-3], None, 0, None) == 5
     assert call(*ok[:-2], need - 16, None) == 5
 

@@ -30,8 +30,11 @@ def host(t):
     # from M = 1 and 4 up to 16384
     (3, 1, 16, 1), (2, 1, 17, 2), (1, 1, 32, 33), (2, 3, 16, 256), (3, 2, 40, 1000),
     (1, 2, 64, 4096), (4, 3, 33, 777), (2, 1, 100, 3000), (2, 2, 16, 8192), (1, 1, 70, 5000),
-    # recurrence route: few states, rows longer than 8192
-    (1, 1, 1, 1), (2, 2, 8, 1000), (1, 2, 20, 9000)])
+    # rows longer than 8192: the correlation through the FFT convolution's kernels (one CTA per
+    # row up to 16384, the 8-CTA cluster above)
+    (1, 2, 20, 9000), (2, 2, 16, 20000), (1, 1, 24, 65536),
+    # recurrence route: few states, rows longer than 65536
+    (1, 1, 1, 1), (2, 2, 8, 1000), (1, 1, 2, 9000), (1, 1, 16, 66000)])
 def test_backward_params_match_oracle(B, H, N, L):
     """Both routes; ragged L, N not a multiple of 32 or of the four states a warp takes, one
     unit-circle channel (d log_re = 0 there)."""
@@ -83,7 +86,10 @@ def test_backward_params_linear_in_g():
     (False, "re_im", 2, 2, 24, 777),     # DLR-prod: weights c_j K_j
     (True, "re_im", 3, 2, 40, 1000),
     (True, "re_im", 1, 1, 8, 8192),      # DLR-prod with few states, the largest transform
-    (True, "re", 2, 2, 16, 20000),       # du on the 8-CTA cluster transform
+    (True, "re", 2, 2, 16, 20000),       # long rows: c through the convolution's kernels
+    (True, "re_im", 2, 2, 24, 16384),
+    (True, "re_im", 1, 2, 16, 40000),    # ... on the 8-CTA cluster transform
+    (True, "re", 2, 1, 4, 20000),        # recurrence route on reversed rows, du on the cluster
 ])
 def test_layer_backward_matches_oracle(bidir, cast, B, H, N, L):
     """dlr_layer_backward against the oracle's dlr_layer_backward: du and the three gradients
@@ -117,3 +123,26 @@ def test_layer_backward_causal_re_equals_the_scan_gradients():
     for x, y in zip(grads[0], a):
         assert torch.equal(x, y)
     assert oracle.rel_l2(host(du), host(dlr.dlr_scan_backward_input(gd, p))) <= TOL
+
+
+def test_layer_backward_dlrprod_workload_sampled_channels():
+    """The bidirectional DLR-prod workload at full size (B4 H128 N1024 L16384): all gradients
+    on the GPU, compared with the oracle on a seeded sample of channels (the channels are
+    independent, so the oracle runs on those channels' slices) and on du of the same
+    channels."""
+    w = inputs.make_workload("dlrprod_bidir_b4_h128_n1024_l16384")
+    g = np.random.default_rng(23).standard_normal(w.u.shape).astype(np.float32)
+    fwd = (w.fwd.log_re, w.fwd.log_im, w.fwd.W)
+    bwd = (w.bwd.log_re, w.bwd.log_im, w.bwd.W)
+    du, grads = dlr.dlr_layer_backward(dev(w.u), dev(g), tuple(dev(a) for a in fwd),
+                                       tuple(dev(a) for a in bwd), cast="re_im")
+    assert dlr.device_status() == 0
+    hs = np.sort(np.random.default_rng(3).choice(w.H, 4, replace=False))
+    sl = lambda p: tuple(np.ascontiguousarray(a[hs]) for a in p)
+    r_du, r_grads = oracle.dlr_layer_backward(np.ascontiguousarray(w.u[:, hs]),
+                                              np.ascontiguousarray(g[:, hs]), sl(fwd), sl(bwd),
+                                              cast="re_im")
+    assert oracle.rel_l2(host(du)[:, hs], r_du) <= TOL
+    for got, ref in zip(grads, r_grads):
+        for a, b in zip(got, ref):
+            assert oracle.rel_l2(host(a)[hs], b) <= TOL
