@@ -31,7 +31,9 @@
 //    Z_{M-f}) / 2 and G_f = (Z_f - conj Z_{M-f}) / 2i, and A_f += G_f conj(U_f) is summed
 //    over the batch for f = 0 .. M/2 (A is Hermitian: c is real). One inverse transform then
 //    gives c_j = (1/M) sum_f A_f e^{2 pi i f j / M}.
-//  - grad_moments: one warp per four states of a channel, lanes along the lag: lane t sums
+//  - grad_moments: one warp per four states of a channel, lanes along the lag (the block's
+//    eight warps share one channel and stage its weights in shared memory, 1024 lags at a
+//    time, the next tile's loads in flight during the current one): lane t sums
 //    c_{32m+t} lambda^{32m} and (32m+t) c_{32m+t} lambda^{32m} over the blocks m, each
 //    lambda^{32m} evaluated directly from the parameters (a batch of 32 by the 32 lanes,
 //    passed round by shuffles), then multiplies by its own lambda^t, the warp adds the lanes
@@ -56,6 +58,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "fft_rows.cuh"
 
@@ -308,6 +311,8 @@ constexpr int kMomStates = 4;  // states per warp
 // d log_re = -2a Re(W S1), d log_im = -Im(W S1). DLR-prod cast (kappa_j = Re K_j Im K_j, so
 // d kappa_j = Im(K_j dK_j)): w_j = c_j K_j with the complex kernel Kc, dW = (Im S0, Re S0),
 // d log_re = -2a Im(W S1), d log_im = Re(W S1).
+constexpr int kLagTile = 1024;  // lags staged in shared memory at a time (32 blocks of 32)
+
 template <bool kProd>
 __global__ void __launch_bounds__(kMomWarps * 32)
     grad_moments(const float* __restrict__ c, const float2* __restrict__ Kc,
@@ -315,11 +320,16 @@ __global__ void __launch_bounds__(kMomWarps * 32)
                  const float2* __restrict__ W, int H, int N, int L, int blocks_per_h,
                  float* __restrict__ d_log_re, float* __restrict__ d_log_im,
                  float2* __restrict__ dW) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int h = blockIdx.x / blocks_per_h;
+  // the weights of a lag: (w_j, j w_j), real (Re cast: float2) or complex (DLR-prod: float4)
+  using WT = typename std::conditional<kProd, float4, float2>::type;
+  constexpr int kPer = kLagTile / (kMomWarps * 32);  // lags a thread stages per tile
+  __shared__ WT sw[2][kLagTile];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.x / blocks_per_h;  // every warp of the block takes channel h
   const int n0 = ((blockIdx.x - h * blocks_per_h) * kMomWarps + warp) * kMomStates;
-  if (h >= H || n0 >= N) return;  // whole warps
+  const bool active = n0 < N;  // idle warps still stage weights and meet at the barriers
   const float* ch = c + (size_t)h * (size_t)L;
+  const float2* kh = kProd ? Kc + (size_t)h * (size_t)L : nullptr;
   lam_param p[kMomStates];
 #pragma unroll
   for (int s = 0; s < kMomStates; ++s) {
@@ -329,41 +339,60 @@ __global__ void __launch_bounds__(kMomWarps * 32)
   cf a0[kMomStates], a1[kMomStates];
 #pragma unroll
   for (int s = 0; s < kMomStates; ++s) a0[s] = a1[s] = {0.f, 0.f};
-  const int nb = (L + 31) / 32;
-#pragma unroll 1
-  for (int mb = 0; mb < nb; mb += 32) {
-    cf pw[kMomStates];  // lambda^{32 (mb + lane)}
+  WT reg[kPer];
+  auto load_tile = [&](int t) {  // the next tile's weights into registers (loads in flight)
 #pragma unroll
-    for (int s = 0; s < kMomStates; ++s) pw[s] = lam_pow(p[s], 32 * (mb + lane));
-    const int cnt = min(32, nb - mb);
-#pragma unroll 4
-    for (int i = 0; i < cnt; ++i) {
-      const int j = 32 * (mb + i) + lane;
+    for (int q = 0; q < kPer; ++q) {
+      const int j = t * kLagTile + q * (kMomWarps * 32) + tid;
       const float cj = j < L ? __ldg(ch + j) : 0.f;
       if constexpr (!kProd) {
-        const float jc = (float)j * cj;
-#pragma unroll
-        for (int s = 0; s < kMomStates; ++s) {
-          const float wr = __shfl_sync(0xffffffffu, pw[s].re, i);
-          const float wi = __shfl_sync(0xffffffffu, pw[s].im, i);
-          a0[s].re = fmaf(cj, wr, a0[s].re);
-          a0[s].im = fmaf(cj, wi, a0[s].im);
-          a1[s].re = fmaf(jc, wr, a1[s].re);
-          a1[s].im = fmaf(jc, wi, a1[s].im);
-        }
+        reg[q] = make_float2(cj, (float)j * cj);
       } else {
-        const float2 kj = j < L ? __ldg(Kc + (size_t)h * L + j) : make_float2(0.f, 0.f);
-        const cf t = {cj * kj.x, cj * kj.y};
-        const cf jt = {(float)j * t.re, (float)j * t.im};
+        const float2 kj = j < L ? __ldg(kh + j) : make_float2(0.f, 0.f);
+        const float tr = cj * kj.x, ti = cj * kj.y;
+        reg[q] = make_float4(tr, ti, (float)j * tr, (float)j * ti);
+      }
+    }
+  };
+  auto store_tile = [&](int buf) {
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) sw[buf][q * (kMomWarps * 32) + tid] = reg[q];
+  };
+  const int ntiles = (L + kLagTile - 1) / kLagTile;
+  load_tile(0);
+  store_tile(0);
+  __syncthreads();
+#pragma unroll 1
+  for (int t = 0; t < ntiles; ++t) {
+    const int buf = t & 1;
+    if (t + 1 < ntiles) load_tile(t + 1);
+    if (active) {
+      cf pw[kMomStates];  // lambda^{32 m} for the tile's block m = 32 t + lane
+#pragma unroll
+      for (int s = 0; s < kMomStates; ++s) pw[s] = lam_pow(p[s], 32 * (32 * t + lane));
+#pragma unroll 8
+      for (int i = 0; i < 32; ++i) {
+        const WT wv = sw[buf][32 * i + lane];  // lag j = 1024 t + 32 i + lane
 #pragma unroll
         for (int s = 0; s < kMomStates; ++s) {
-          const cf w = {__shfl_sync(0xffffffffu, pw[s].re, i), __shfl_sync(0xffffffffu, pw[s].im, i)};
-          a0[s] = cfma(t, w, a0[s]);
-          a1[s] = cfma(jt, w, a1[s]);
+          const cf w = {__shfl_sync(0xffffffffu, pw[s].re, i),
+                        __shfl_sync(0xffffffffu, pw[s].im, i)};
+          if constexpr (!kProd) {
+            a0[s].re = fmaf(wv.x, w.re, a0[s].re);
+            a0[s].im = fmaf(wv.x, w.im, a0[s].im);
+            a1[s].re = fmaf(wv.y, w.re, a1[s].re);
+            a1[s].im = fmaf(wv.y, w.im, a1[s].im);
+          } else {
+            a0[s] = cfma({wv.x, wv.y}, w, a0[s]);
+            a1[s] = cfma({wv.z, wv.w}, w, a1[s]);
+          }
         }
       }
     }
+    if (t + 1 < ntiles) store_tile(buf ^ 1);  // that buffer was last read before the barrier
+    __syncthreads();
   }
+  if (!active) return;
 #pragma unroll
   for (int s = 0; s < kMomStates; ++s) {
     const cf lt = lam_pow(p[s], lane);
