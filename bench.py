@@ -481,7 +481,15 @@ def run_extras(torch, dlr, inputs, flush, sm_mhz, sm_count):
         "ms": ms_k, "directions": 2, "executed_flops": kgen_flops,
         "tensor": {"achieved": kgen_flops / ms_k / 1e9, "peak": tc_peak, "peak_kind": tc_kind,
                    "unit": "TFLOP/s", "frac": kgen_flops / ms_k / 1e9 / tc_peak}}
-    del u, y, ws, Kf, Kb
+    # the same layer's gradients (du and both directions' parameter gradients, DLR-prod cast)
+    g = torch.randn_like(u)
+    wsg = torch.empty(dlr.dlr_layer_backward_workspace_size(w.B, w.H, w.N, w.L, True, "re_im"),
+                      dtype=torch.uint8, device="cuda")
+    ms_g = _time_steps(torch, lambda: dlr.dlr_layer_backward(u, g, f, b, cast="re_im",
+                                                             workspace=wsg), 5, 2, flush)
+    out["backward_" + w.name] = {"ms": ms_g, "elements_per_s": w.B * w.H * w.L / ms_g * 1e3,
+                                 "outputs": "du and both directions' parameter gradients"}
+    del u, y, ws, Kf, Kb, g, wsg
 
     w = inputs.make_workload("dlr_b1_h256_n64_l65536_unit8")
     u, fwd = dev(w.u), (dev(w.fwd.log_re), dev(w.fwd.log_im), dev(w.fwd.W))
