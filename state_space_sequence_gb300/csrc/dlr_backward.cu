@@ -210,6 +210,7 @@ __global__ void __launch_bounds__(fftr::Plan<kLog>::T, kLog <= 13 ? 2 : 1)
   using P = fftr::Plan<kLog>;
   constexpr int M = P::n, T = P::T, kHalf = M / 2;
   constexpr int PER = (M + T - 1) / T;
+  constexpr bool kDup = P::R0 == 2 && P::n16 > 0;  // the first pass is radix 2 (see below)
   extern __shared__ float2 smem[];
   float2* buf = smem;
   float2* acc = smem + P::buf_elems;
@@ -221,20 +222,42 @@ __global__ void __launch_bounds__(fftr::Plan<kLog>::T, kLog <= 13 ? 2 : 1)
   for (int b = 0; b < B; ++b) {
     const float* ur = u + ((size_t)b * H + h) * (size_t)L;
     const float* gr = g + ((size_t)b * H + h) * (size_t)L;
-    // every load of the row before the first store
-    float2 z[PER];
+    if constexpr (kDup) {
+      // a radix-2 first pass over z (zero above M/2 > L - 1) leaves z_m at 2m and 2m + 1:
+      // written here directly, and the transform starts at its second pass
+      constexpr int PH = (kHalf + T - 1) / T;
+      float2 z[PH];
 #pragma unroll
-    for (int q = 0; q < PER; ++q) {
-      const int m = tid + q * T;
-      z[q] = m < L ? make_float2(__ldg(ur + m), __ldg(gr + m)) : make_float2(0.f, 0.f);
-    }
+      for (int q = 0; q < PH; ++q) {
+        const int m = tid + q * T;
+        z[q] = m < L ? make_float2(__ldg(ur + m), __ldg(gr + m)) : make_float2(0.f, 0.f);
+      }
 #pragma unroll
-    for (int q = 0; q < PER; ++q) {
-      const int m = tid + q * T;
-      if (m < M && DLR_IN(padded(m), P::buf_elems)) buf[padded(m)] = z[q];
+      for (int q = 0; q < PH; ++q) {
+        const int m = tid + q * T;
+        if (m < kHalf && DLR_IN(padded(2 * m) + 1, P::buf_elems)) {
+          buf[padded(2 * m)] = z[q];  // 2m and 2m + 1 share a padding group (2m even)
+          buf[padded(2 * m) + 1] = z[q];
+        }
+      }
+      __syncthreads();
+      fftr::local_fft<kLog, false, true>(buf, tw);  // ends with a barrier
+    } else {
+      // every load of the row before the first store
+      float2 z[PER];
+#pragma unroll
+      for (int q = 0; q < PER; ++q) {
+        const int m = tid + q * T;
+        z[q] = m < L ? make_float2(__ldg(ur + m), __ldg(gr + m)) : make_float2(0.f, 0.f);
+      }
+#pragma unroll
+      for (int q = 0; q < PER; ++q) {
+        const int m = tid + q * T;
+        if (m < M && DLR_IN(padded(m), P::buf_elems)) buf[padded(m)] = z[q];
+      }
+      __syncthreads();
+      fftr::local_fft<kLog, false>(buf, tw);  // ends with a barrier
     }
-    __syncthreads();
-    fftr::local_fft<kLog, false>(buf, tw);  // ends with a barrier
     for (int f = tid; f <= kHalf; f += T) {
       const int fm = (M - f) & (M - 1);
       if (!DLR_IN(padded(f), P::buf_elems) || !DLR_IN(padded(fm), P::buf_elems) ||

@@ -159,11 +159,13 @@ __device__ __forceinline__ void pass0_store(float2* dst, const cf (&a)[Plan<kLog
 // Stockham FFT of n = 2^kLog points held in `buf` (padded layout; natural order in and out),
 // in place: every pass loads all of a thread's points, synchronises, then stores. Forward
 // (e^{-2 pi i jk/n}) or, with kInv, the unnormalised inverse; tw is the n-point table above.
-// Every thread of the CTA (Plan<kLog>::T of them) must call it.
-template <int kLog, bool kInv>
+// Every thread of the CTA (Plan<kLog>::T of them) must call it. kAfterPass0: the caller has
+// already written the first pass's output (for a radix-2 first pass over an input whose upper
+// half is zero that is each point x_j at positions 2j and 2j + 1).
+template <int kLog, bool kInv, bool kAfterPass0 = false>
 __device__ __forceinline__ void local_fft(float2* buf, const float2* __restrict__ tw) {
   using P = Plan<kLog>;
-  {
+  if constexpr (!kAfterPass0) {
     cf a[P::PER0][P::R0];
 #pragma unroll
     for (int q = 0; q < P::PER0; ++q) {
