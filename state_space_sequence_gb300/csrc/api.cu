@@ -52,7 +52,7 @@ cudaError_t launch_dlr_grads(const float* u, const float* g, const float* lr1, c
                              const float* W1, const float* lr2, const float* li2,
                              const float* W2, int B, int H, int N, int L, bool prod,
                              float* dr1, float* di1, float* dW1, float* dr2, float* di2,
-                             float* dW2, void* ws, cudaStream_t s);
+                             float* dW2, void* ws, int* status, cudaStream_t s);
 cudaError_t launch_dlr_grad_params(const float* u, const float* g, const float* log_re,
                                    const float* log_im, const float* W, int B, int H, int N,
                                    int L, float* d_log_re, float* d_log_im, float* dW, void* ws,
@@ -442,7 +442,7 @@ dlr_status dlr_layer_backward(const float* u, const float* g, const float* log_r
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   cudaError_t e = dlr::launch_dlr_grads(u, g, log_re, log_im, W, log_re2, log_im2, W2, (int)B,
                                         (int)H, (int)N, (int)L, prod, d_log_re, d_log_im, dW,
-                                        d_log_re2, d_log_im2, dW2, ws, s);
+                                        d_log_re2, d_log_im2, dW2, ws, status_word(), s);
   if (e != cudaSuccess || !du) return from_cuda(e);
   // du: the convolution of g whose causal kernel is the second direction's and whose
   // anti-causal kernel is the first's (the adjoint swaps the directions); zero causal kernel

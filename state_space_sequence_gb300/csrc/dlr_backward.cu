@@ -552,7 +552,8 @@ cudaError_t launch_rows(const float* u, const float* g, const float* log_re, con
 }  // namespace
 
 cudaError_t launch_dlr_kernel_complex(const float* log_re, const float* log_im, const float* W,
-                                      int H, int N, int L, float2* K, cudaStream_t s);
+                                      int H, int N, int L, float2* K, int* status,
+                                      cudaStream_t s);
 
 size_t grads_workspace_bytes(int64_t B, int64_t H, int64_t N, int64_t L, bool bidir, bool prod) {
   size_t total = 0;
@@ -572,7 +573,7 @@ cudaError_t launch_dlr_grads(const float* u, const float* g, const float* lr1, c
                              const float* W1, const float* lr2, const float* li2,
                              const float* W2, int B, int H, int N, int L, bool prod,
                              float* dr1, float* di1, float* dW1, float* dr2, float* di2,
-                             float* dW2, void* ws, cudaStream_t s) {
+                             float* dW2, void* ws, int* status, cudaStream_t s) {
   const bool bidir = lr2 != nullptr;
   const GradWs w = carve_grads(ws, B, H, N, L, bidir, prod, nullptr);
   cudaError_t e;
@@ -619,8 +620,10 @@ cudaError_t launch_dlr_grads(const float* u, const float* g, const float* lr1, c
     if (e != cudaSuccess) return e;
   }
   if (prod) {
-    if ((e = launch_dlr_kernel_complex(lr1, li1, W1, H, N, L, w.k1, s)) != cudaSuccess) return e;
-    if (bidir && (e = launch_dlr_kernel_complex(lr2, li2, W2, H, N, L, w.k2, s)) != cudaSuccess)
+    if ((e = launch_dlr_kernel_complex(lr1, li1, W1, H, N, L, w.k1, status, s)) != cudaSuccess)
+      return e;
+    if (bidir &&
+        (e = launch_dlr_kernel_complex(lr2, li2, W2, H, N, L, w.k2, status, s)) != cudaSuccess)
       return e;
   }
   if ((e = launch_moments(w.c, w.k1, prod, lr1, li1, W1, H, N, L, dr1, di1, dW1, s)) !=
@@ -635,7 +638,7 @@ cudaError_t launch_dlr_grad_params(const float* u, const float* g, const float* 
                                    int L, float* d_log_re, float* d_log_im, float* dW, void* ws,
                                    cudaStream_t s) {
   return launch_dlr_grads(u, g, log_re, log_im, W, nullptr, nullptr, nullptr, B, H, N, L, false,
-                          d_log_re, d_log_im, dW, nullptr, nullptr, nullptr, ws, s);
+                          d_log_re, d_log_im, dW, nullptr, nullptr, nullptr, ws, nullptr, s);
 }
 
 }  // namespace dlr

@@ -238,9 +238,17 @@ cudaError_t launch_dlr_kernel(const float* log_re, const float* log_im, const fl
                : launch_gen<0, 16>(log_re, log_im, W, H, N, L, K, s);
 }
 
-// The complex kernel K [H, L] as float2 pairs (any N, on FFMA; for the DLR-prod gradients).
+cudaError_t launch_dlr_kernel_tc_complex(const float* log_re, const float* log_im,
+                                         const float* W, int H, int N, int L, float2* K,
+                                         int* status, cudaStream_t s);
+
+// The complex kernel K [H, L] as float2 pairs (for the DLR-prod gradients), on the same two
+// generators as the casts.
 cudaError_t launch_dlr_kernel_complex(const float* log_re, const float* log_im, const float* W,
-                                      int H, int N, int L, float2* K, cudaStream_t s) {
+                                      int H, int N, int L, float2* K, int* status,
+                                      cudaStream_t s) {
+  if (N >= 256 || (N >= 64 && L >= 16384))
+    return launch_dlr_kernel_tc_complex(log_re, log_im, W, H, N, L, K, status, s);
   return launch_gen<2, 16>(log_re, log_im, W, H, N, L, reinterpret_cast<float*>(K), s);
 }
 

@@ -110,7 +110,8 @@ __device__ __forceinline__ float2 f2mul(float2 a, float2 b) {
   return make_float2(r.re, r.im);
 }
 
-template <bool kReIm>
+// kMode: 0 writes Re K, 1 Re K * Im K (DLR-prod), 2 the complex K as float2 pairs.
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 dlr_kernel_tc(const float* __restrict__ log_re, const float* __restrict__ log_im,
               const float2* __restrict__ W, int N, int L, float* __restrict__ K, int* status) {
@@ -358,8 +359,26 @@ dlr_kernel_tc(const float* __restrict__ log_re, const float* __restrict__ log_im
     for (int part = 0; part < 2; ++part) {  // lags 32 part .. 32 part + 31
       float re[32];
       sum_acc(uint32_t(part * 32), re);
+      if constexpr (kMode == 2) {
+        float im[32];
+        sum_acc(uint32_t(64 + part * 32), im);
+        if (!acc_ok) continue;
+        const int jb = jc + part * 32;
+        float2* kc = reinterpret_cast<float2*>(K) + (size_t)h * L;
+        if ((L & 1) == 0 && jb + 32 <= L) {  // 16-byte aligned pairs of lags
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            *reinterpret_cast<float4*>(kc + jb + 2 * i) =
+                make_float4(re[2 * i] * unscale, im[2 * i] * unscale, re[2 * i + 1] * unscale,
+                            im[2 * i + 1] * unscale);
+        } else {
+          for (int i = 0; i < 32; ++i)
+            if (jb + i < L) kc[jb + i] = make_float2(re[i] * unscale, im[i] * unscale);
+        }
+        continue;
+      }
       float v[32];
-      if (kReIm) {
+      if (kMode == 1) {
         float im[32];
         sum_acc(uint32_t(64 + part * 32), im);
 #pragma unroll
@@ -396,12 +415,25 @@ cudaError_t launch_dlr_kernel_tc(const float* log_re, const float* log_im, const
   const float2* w2 = reinterpret_cast<const float2*>(W);
   cudaError_t e;
   if (re_im) {
-    if ((e = max_smem_once<dlr_kernel_tc<true>>(kSmemBytes)) != cudaSuccess) return e;
-    dlr_kernel_tc<true><<<grid, kThreads, kSmemBytes, s>>>(log_re, log_im, w2, N, L, K, status);
+    if ((e = max_smem_once<dlr_kernel_tc<1>>(kSmemBytes)) != cudaSuccess) return e;
+    dlr_kernel_tc<1><<<grid, kThreads, kSmemBytes, s>>>(log_re, log_im, w2, N, L, K, status);
   } else {
-    if ((e = max_smem_once<dlr_kernel_tc<false>>(kSmemBytes)) != cudaSuccess) return e;
-    dlr_kernel_tc<false><<<grid, kThreads, kSmemBytes, s>>>(log_re, log_im, w2, N, L, K, status);
+    if ((e = max_smem_once<dlr_kernel_tc<0>>(kSmemBytes)) != cudaSuccess) return e;
+    dlr_kernel_tc<0><<<grid, kThreads, kSmemBytes, s>>>(log_re, log_im, w2, N, L, K, status);
   }
+  return cudaGetLastError();
+}
+
+// The complex kernel K [H, L] as float2 pairs.
+cudaError_t launch_dlr_kernel_tc_complex(const float* log_re, const float* log_im,
+                                         const float* W, int H, int N, int L, float2* K,
+                                         int* status, cudaStream_t s) {
+  dim3 grid((L + kRows * kT - 1) / (kRows * kT), H);
+  cudaError_t e = max_smem_once<dlr_kernel_tc<2>>(kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dlr_kernel_tc<2><<<grid, kThreads, kSmemBytes, s>>>(
+      log_re, log_im, reinterpret_cast<const float2*>(W), N, L, reinterpret_cast<float*>(K),
+      status);
   return cudaGetLastError();
 }
 
