@@ -35,9 +35,9 @@
 //    eight warps share one channel and stage its weights in shared memory, 1024 lags at a
 //    time, the next tile's loads in flight during the current one): lane t sums
 //    c_{32m+t} lambda^{32m} and (32m+t) c_{32m+t} lambda^{32m} over the blocks m, each
-//    lambda^{32m} evaluated directly from the parameters (a batch of 32 by the 32 lanes,
-//    passed round by shuffles), then multiplies by its own lambda^t, the warp adds the lanes
-//    and lane 0 forms the three gradients.
+//    lambda^{32m} evaluated directly from the parameters (a batch of 32 by the 32 lanes, read
+//    back from a per-warp shared table), then multiplies by its own lambda^t; the warp adds
+//    the lanes and lane 0 forms the three gradients.
 // Per input element this is one complex FFT point per row and a few flops per (state, lag)
 // instead of the recurrences' two complex updates per (state, step, row).
 //
@@ -347,6 +347,7 @@ __global__ void __launch_bounds__(kMomWarps * 32)
   using WT = typename std::conditional<kProd, float4, float2>::type;
   constexpr int kPer = kLagTile / (kMomWarps * 32);  // lags a thread stages per tile
   __shared__ WT sw[2][kLagTile];
+  __shared__ float2 spw[kMomWarps][kMomStates][32];  // each warp's lambda^{32 m} of a tile
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int h = blockIdx.x / blocks_per_h;  // every warp of the block takes channel h
   const int n0 = ((blockIdx.x - h * blocks_per_h) * kMomWarps + warp) * kMomStates;
@@ -390,16 +391,21 @@ __global__ void __launch_bounds__(kMomWarps * 32)
     const int buf = t & 1;
     if (t + 1 < ntiles) load_tile(t + 1);
     if (active) {
-      cf pw[kMomStates];  // lambda^{32 m} for the tile's block m = 32 t + lane
+      // lambda^{32 m} for the tile's block m = 32 t + lane, into the warp's table (read back
+      // as one broadcast per state and block)
 #pragma unroll
-      for (int s = 0; s < kMomStates; ++s) pw[s] = lam_pow(p[s], 32 * (32 * t + lane));
+      for (int s = 0; s < kMomStates; ++s) {
+        const cf pw = lam_pow(p[s], 32 * (32 * t + lane));
+        spw[warp][s][lane] = make_float2(pw.re, pw.im);
+      }
+      __syncwarp();
 #pragma unroll 8
       for (int i = 0; i < 32; ++i) {
         const WT wv = sw[buf][32 * i + lane];  // lag j = 1024 t + 32 i + lane
 #pragma unroll
         for (int s = 0; s < kMomStates; ++s) {
-          const cf w = {__shfl_sync(0xffffffffu, pw[s].re, i),
-                        __shfl_sync(0xffffffffu, pw[s].im, i)};
+          const float2 pf = spw[warp][s][i];
+          const cf w = {pf.x, pf.y};
           if constexpr (!kProd) {
             a0[s].re = fmaf(wv.x, w.re, a0[s].re);
             a0[s].im = fmaf(wv.x, w.im, a0[s].im);
@@ -411,6 +417,7 @@ __global__ void __launch_bounds__(kMomWarps * 32)
           }
         }
       }
+      __syncwarp();  // the table is rewritten at the next tile
     }
     if (t + 1 < ntiles) store_tile(buf ^ 1);  // that buffer was last read before the barrier
     __syncthreads();
