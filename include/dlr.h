@@ -228,11 +228,10 @@ dlr_status dlr_scan_apply(const float* u, int64_t B, int64_t H, int64_t N, int64
  * buffers: u, y [B, H, L] and log_re, log_im [H, N], W [H, N, 2] are host pointers (page-locked
  * for the copies to overlap anything), the device working copies live in `workspace` (device
  * memory, dlr_scan_host_workspace_size bytes, 16-byte aligned; the library still allocates
- * nothing). The batch is split into pieces of about a quarter of the batch rows, the last
- * group halved (for B < 4, into channel groups; one piece when L % 4 != 0): the copies in,
- * the layer and the copies out run on
- * three internal streams joined by events, so the copy of one piece in, the compute of
- * another and the copy of a third out overlap. Asynchronous with respect to the host; ordered
+ * nothing). The batch is split into pieces of about a quarter of the batch rows, the first
+ * and last groups halved (for B < 4, into channel groups; one piece when L % 4 != 0): the
+ * copies in, the layer and the copies out run on three internal streams joined by events, so
+ * the copy of one piece in, the compute of another and the copy of a third out overlap. Asynchronous with respect to the host; ordered
  * after the work already on `stream` and before the work enqueued on it later, so y may be
  * read after a synchronisation of `stream`. Same limits as dlr_scan_apply (N <= 64).
  * If an enqueue fails part-way, the call waits for the pieces already queued before it returns

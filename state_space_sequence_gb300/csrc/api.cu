@@ -708,10 +708,11 @@ dlr_status dlr_scan_host(const float* u, const float* log_re, const float* log_i
     if ((r = dlr::launch_scan_tc_tables(lrd, lid, Wd, (int)H, (int)N, tables, st[1])) !=
         cudaSuccess)
       return r;
-    // the last group of rows is halved: what remains after the last copy in is the compute and
-    // copy out of the last piece, so a smaller last piece shortens that tail
+    // the first and last groups of rows are halved: nothing overlaps the first piece's copy in
+    // or the last piece's compute and copy out, so smaller end pieces shorten both
     for (int64_t b0 = 0, nb = 0; b0 < B; b0 += nb) {
       nb = std::min(per_b, B - b0);
+      if (b0 == 0 && nb > 1 && B > per_b) nb /= 2;
       if (b0 + nb == B && nb > 1) nb /= 2;
       for (int64_t h0 = 0; h0 < H; h0 += per_h) {
         const int64_t nh = std::min(per_h, H - h0);
