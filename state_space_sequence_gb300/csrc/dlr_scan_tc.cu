@@ -212,6 +212,17 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
+// The same for a * s and b * s, the scaling and the remainders in two-wide float instructions
+// (each lane of a pair rounds as the scalar operation would: the results are identical).
+__device__ __forceinline__ void split2s(float a, float b, float s, uint32_t& hi, uint32_t& lo) {
+  const float2 v = __fmul2_rn(make_float2(a, b), make_float2(s, s));
+  const float ah = round11(v.x), bh = round11(v.y);
+  const float2 r = __ffma2_rn(make_float2(ah, bh), make_float2(-1.f, -1.f), v);  // v - (ah, bh)
+  const __half2 h = __floats2half2_rn(ah, bh);
+  const __half2 l = __floats2half2_rn(r.x, r.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
 
 // Programmatic dependent launch: the table kernel lets the scan kernel launch early; the scan
 // kernel waits for the table kernel's completion (and memory) before it reads the tables. Both
@@ -271,6 +282,19 @@ __device__ __forceinline__ void store_chunk8(uint8_t* hi_tile, uint8_t* lo_tile,
   uint32_t h[4], l[4];
 #pragma unroll
   for (int q = 0; q < 4; ++q) split2(v[2 * q], v[2 * q + 1], h[q], l[q]);
+  const uint32_t off = uint32_t(row) * 128u + ((uint32_t(chunk) ^ uint32_t(row & 7)) << 4);
+  if (DLR_IN(row, rows) && DLR_IN(chunk, 8)) {
+    *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(lo_tile + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  }
+}
+
+// store_chunk8 of v * s (the scaling in two-wide float instructions).
+__device__ __forceinline__ void store_chunk8s(uint8_t* hi_tile, uint8_t* lo_tile, int row,
+                                              int chunk, const float* v, float s, int rows) {
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) split2s(v[2 * q], v[2 * q + 1], s, h[q], l[q]);
   const uint32_t off = uint32_t(row) * 128u + ((uint32_t(chunk) ^ uint32_t(row & 7)) << 4);
   if (DLR_IN(row, rows) && DLR_IN(chunk, 8)) {
     *reinterpret_cast<uint4*>(hi_tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
@@ -690,12 +714,7 @@ __device__ __forceinline__ bool conv_tile(const TcScanArgs& a, uint8_t* sm, uint
   const int es = scale_exp(__uint_as_float(DLR_IN(rl, 128) ? rmax[rl] : 0u));
   const float su = exp2i(es);
 #pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    float w8[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w8[i] = v[8 * p + i] * su;
-    store_chunk8(ubuf, ubuf + kULo, g, 4 * h + p, w8, 128);
-  }
+  for (int p = 0; p < 4; ++p) store_chunk8s(ubuf, ubuf + kULo, g, 4 * h + p, v + 8 * p, su, 128);
   if (new_channel) {
     // the first read of the tables: at the CTA's first tile, wait here for the table kernel
     // (programmatic dependent launch), so the conversion above overlaps its end
@@ -815,9 +834,14 @@ __device__ __forceinline__ bool epi_tile(const TcScanArgs& a, const CUtensorMap*
   const bool sc_in = DLR_IN(slot * 128 + g, 512);
   const float ay = sc_in ? reinterpret_cast<const float*>(sm + kAy)[slot * 128 + g] : 0.f;
   const float by = sc_in ? reinterpret_cast<const float*>(sm + kBy)[slot * 128 + g] : 0.f;
-  float y[32];
+  float y[32];  // y1 * ay + y2 * by, two outputs per instruction
 #pragma unroll
-  for (int i = 0; i < 32; ++i) y[i] = fmaf(y1[i], ay, y2[i] * by);
+  for (int i = 0; i < 32; i += 2) {
+    const float2 t = __fmul2_rn(make_float2(y2[i], y2[i + 1]), make_float2(by, by));
+    const float2 r = __ffma2_rn(make_float2(y1[i], y1[i + 1]), make_float2(ay, ay), t);
+    y[i] = r.x;
+    y[i + 1] = r.y;
+  }
   const ColInfo ci = col_info(a, ti, rc);
   if (a.tma) {
     uint8_t* stg = sm + kYStage + warp * 4096;
@@ -1009,7 +1033,7 @@ __device__ __forceinline__ uint32_t xin_chunk(int r, int g0) {
 __device__ __forceinline__ void store_xin8(uint8_t* sm, int r, int g0, const float* v, float s) {
   uint32_t h[4], l[4];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) split2(v[2 * q] * s, v[2 * q + 1] * s, h[q], l[q]);
+  for (int q = 0; q < 4; ++q) split2s(v[2 * q], v[2 * q + 1], s, h[q], l[q]);
   const uint32_t off = xin_chunk(r, g0);
   if (DLR_IN(off + 15, kXLo - kXHi)) {
     *reinterpret_cast<uint4*>(sm + kXHi + off) = make_uint4(h[0], h[1], h[2], h[3]);
