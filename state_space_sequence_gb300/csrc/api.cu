@@ -52,11 +52,12 @@ cudaError_t launch_dlr_grads(const float* u, const float* g, const float* lr1, c
                              const float* W1, const float* lr2, const float* li2,
                              const float* W2, int B, int H, int N, int L, bool prod,
                              float* dr1, float* di1, float* dW1, float* dr2, float* di2,
-                             float* dW2, void* ws, int* status, cudaStream_t s);
+                             float* dW2, void* ws, int* status, cudaStream_t s, float* kap1,
+                             float* kap2);
 cudaError_t launch_dlr_grad_params(const float* u, const float* g, const float* log_re,
                                    const float* log_im, const float* W, int B, int H, int N,
                                    int L, float* d_log_re, float* d_log_im, float* dW, void* ws,
-                                   cudaStream_t s);
+                                   int* status, cudaStream_t s);
 cudaError_t launch_spectrum_direct(const float* lr1, const float* li1, const float* W1,
                                    const float* lr2, const float* li2, const float* W2, int H,
                                    int N, int L, void* ws, cudaStream_t s);
@@ -366,7 +367,7 @@ dlr_status dlr_scan_backward_params(const float* u, const float* g, const float*
   if (!workspace || workspace_bytes < need || !aligned16(workspace)) return DLR_ERR_WORKSPACE;
   return from_cuda(dlr::launch_dlr_grad_params(u, g, log_re, log_im, W, (int)B, (int)H, (int)N,
                                                (int)L, d_log_re, d_log_im, dW, workspace,
-                                               (cudaStream_t)stream));
+                                               status_word(), (cudaStream_t)stream));
 }
 
 // Workspace of dlr_layer_backward: the gradients' part, then the two kernels of the input
@@ -440,28 +441,32 @@ dlr_status dlr_layer_backward(const float* u, const float* g, const float* log_r
     if (ranges_overlap(workspace, need, outs[i], sz[i])) return DLR_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  cudaError_t e = dlr::launch_dlr_grads(u, g, log_re, log_im, W, log_re2, log_im2, W2, (int)B,
-                                        (int)H, (int)N, (int)L, prod, d_log_re, d_log_im, dW,
-                                        d_log_re2, d_log_im2, dW2, ws, status_word(), s);
-  if (e != cudaSuccess || !du) return from_cuda(e);
-  // du: the convolution of g whose causal kernel is the second direction's and whose
-  // anti-causal kernel is the first's (the adjoint swaps the directions); zero causal kernel
-  // for a causal layer
+  int* status = status_word();
+  // du's kernels: kappa1 of the first direction, kappa2 of the second (zero for a causal
+  // layer); with the DLR-prod cast the gradients' complex kernels give them
   const size_t hl = sizeof(float) * (size_t)H * (size_t)L;
   uint8_t* p = ws + layer_bwd_grads_bytes(B, H, N, L, bidir, prod);
   float* kap1 = reinterpret_cast<float*>(p);
   float* kap2 = reinterpret_cast<float*>(p + round256(hl));
   void* cws = p + 2 * round256(hl);
-  int* status = status_word();
-  if ((e = dlr::launch_dlr_kernel(log_re, log_im, W, (int)H, (int)N, (int)L, prod, kap1, status,
-                                  s)) != cudaSuccess)
-    return from_cuda(e);
-  if (bidir)
-    e = dlr::launch_dlr_kernel(log_re2, log_im2, W2, (int)H, (int)N, (int)L, prod, kap2, status,
-                               s);
-  else
-    e = cudaMemsetAsync(kap2, 0, hl, s);
-  if (e != cudaSuccess) return from_cuda(e);
+  cudaError_t e = dlr::launch_dlr_grads(u, g, log_re, log_im, W, log_re2, log_im2, W2, (int)B,
+                                        (int)H, (int)N, (int)L, prod, d_log_re, d_log_im, dW,
+                                        d_log_re2, d_log_im2, dW2, ws, status, s,
+                                        du && prod ? kap1 : nullptr,
+                                        du && prod ? kap2 : nullptr);
+  if (e != cudaSuccess || !du) return from_cuda(e);
+  // du: the convolution of g whose causal kernel is the second direction's and whose
+  // anti-causal kernel is the first's (the adjoint swaps the directions)
+  if (!prod) {
+    if ((e = dlr::launch_dlr_kernel(log_re, log_im, W, (int)H, (int)N, (int)L, false, kap1,
+                                    status, s)) != cudaSuccess)
+      return from_cuda(e);
+    if (bidir &&
+        (e = dlr::launch_dlr_kernel(log_re2, log_im2, W2, (int)H, (int)N, (int)L, false, kap2,
+                                    status, s)) != cudaSuccess)
+      return from_cuda(e);
+  }
+  if (!bidir && (e = cudaMemsetAsync(kap2, 0, hl, s)) != cudaSuccess) return from_cuda(e);
   if ((e = dlr::launch_dlr_conv_spectrum(kap2, kap1, (int)H, (int)L, cws, s)) != cudaSuccess)
     return from_cuda(e);
   return from_cuda(dlr::launch_dlr_conv_apply(g, (int)B, (int)H, (int)L, du, cws, s));

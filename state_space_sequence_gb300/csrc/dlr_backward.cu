@@ -317,6 +317,14 @@ __global__ void grad_cross(const float2* __restrict__ su, const float2* __restri
   }
   if (DLR_IN(i, (int64_t)H * nb)) a[i] = make_float2(ar * scale, ai * scale);
 }
+// kappa_j = Re K_j Im K_j from the complex kernel (the DLR-prod cast, as the generators form it)
+__global__ void prod_cast(const float2* __restrict__ K, float* __restrict__ kap, int64_t count) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < count) {
+    const float2 k = K[i];
+    kap[i] = k.x * k.y;
+  }
+}
 __global__ void conj_spectra(float2* __restrict__ a, int64_t count) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i < count) a[i].y = -a[i].y;
@@ -521,10 +529,22 @@ GradWs carve_grads(void* ws, int64_t B, int64_t H, int64_t N, int64_t L, bool bi
   return w;
 }
 
-// The moments of one parameter set from its weights (c, and the complex kernel for DLR-prod).
+}  // namespace
+cudaError_t launch_moments_tc(const float* c, const float2* Kc, bool prod, const float* log_re,
+                              const float* log_im, const float* W, int H, int N, int L,
+                              float* d_log_re, float* d_log_im, float* dW, int* status,
+                              cudaStream_t s);
+namespace {
+
+// The moments of one parameter set from its weights (c, and the complex kernel for DLR-prod):
+// on the tensor cores (dlr_moments_tc.cu) for 64 states or more, else on FFMA.
 cudaError_t launch_moments(const float* c, const float2* Kc, bool prod, const float* log_re,
                            const float* log_im, const float* W, int H, int N, int L,
-                           float* d_log_re, float* d_log_im, float* dW, cudaStream_t s) {
+                           float* d_log_re, float* d_log_im, float* dW, int* status,
+                           cudaStream_t s) {
+  if (N >= 64)
+    return launch_moments_tc(c, Kc, prod, log_re, log_im, W, H, N, L, d_log_re, d_log_im, dW,
+                             status, s);
   const int bph = (N + kMomWarps * kMomStates - 1) / (kMomWarps * kMomStates);
   const unsigned grid = (unsigned)((int64_t)H * bph);
   const float2* Wc = reinterpret_cast<const float2*>(W);
@@ -580,7 +600,8 @@ cudaError_t launch_dlr_grads(const float* u, const float* g, const float* lr1, c
                              const float* W1, const float* lr2, const float* li2,
                              const float* W2, int B, int H, int N, int L, bool prod,
                              float* dr1, float* di1, float* dW1, float* dr2, float* di2,
-                             float* dW2, void* ws, int* status, cudaStream_t s) {
+                             float* dW2, void* ws, int* status, cudaStream_t s, float* kap1,
+                             float* kap2) {
   const bool bidir = lr2 != nullptr;
   const GradWs w = carve_grads(ws, B, H, N, L, bidir, prod, nullptr);
   cudaError_t e;
@@ -632,20 +653,28 @@ cudaError_t launch_dlr_grads(const float* u, const float* g, const float* lr1, c
     if (bidir &&
         (e = launch_dlr_kernel_complex(lr2, li2, W2, H, N, L, w.k2, status, s)) != cudaSuccess)
       return e;
+    // the cast kernels of the input gradient's convolution, when asked for
+    const int64_t hl = (int64_t)H * L;
+    const unsigned gb = (unsigned)((hl + 255) / 256);
+    if (kap1) prod_cast<<<gb, 256, 0, s>>>(w.k1, kap1, hl);
+    if (kap2 && bidir) prod_cast<<<gb, 256, 0, s>>>(w.k2, kap2, hl);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  if ((e = launch_moments(w.c, w.k1, prod, lr1, li1, W1, H, N, L, dr1, di1, dW1, s)) !=
+  if ((e = launch_moments(w.c, w.k1, prod, lr1, li1, W1, H, N, L, dr1, di1, dW1, status, s)) !=
       cudaSuccess)
     return e;
-  if (bidir) return launch_moments(w.c2, w.k2, prod, lr2, li2, W2, H, N, L, dr2, di2, dW2, s);
+  if (bidir)
+    return launch_moments(w.c2, w.k2, prod, lr2, li2, W2, H, N, L, dr2, di2, dW2, status, s);
   return cudaSuccess;
 }
 
 cudaError_t launch_dlr_grad_params(const float* u, const float* g, const float* log_re,
                                    const float* log_im, const float* W, int B, int H, int N,
                                    int L, float* d_log_re, float* d_log_im, float* dW, void* ws,
-                                   cudaStream_t s) {
+                                   int* status, cudaStream_t s) {
   return launch_dlr_grads(u, g, log_re, log_im, W, nullptr, nullptr, nullptr, B, H, N, L, false,
-                          d_log_re, d_log_im, dW, nullptr, nullptr, nullptr, ws, nullptr, s);
+                          d_log_re, d_log_im, dW, nullptr, nullptr, nullptr, ws, status, s,
+                          nullptr, nullptr);
 }
 
 }  // namespace dlr

@@ -106,7 +106,7 @@ def run():
     got = np.concatenate([host(d_lr).ravel(), host(d_li).ravel(), host(dW).ravel()])
     record("backward parameters", got, np.concatenate([r_re.ravel(), r_im.ravel(), r_W.ravel()]))
     # the recurrence route (few states) and the correlation route's largest transform
-    for B, H, N, L in [(2, 2, 8, 300), (1, 1, 18, 8000)]:
+    for B, H, N, L in [(2, 2, 8, 300), (1, 1, 18, 8000), (2, 1, 70, 700)]:
         w = inputs.make_dlr(B, H, N, L, seed=N + L, unit_channels=1)
         g = np.random.default_rng(N).standard_normal(w.u.shape).astype(np.float32)
         _, r_re, r_im, r_W = oracle.dlr_backward(w.u, g, *pnp(w.fwd))
