@@ -31,7 +31,8 @@
 //    Z_{M-f}) / 2 and G_f = (Z_f - conj Z_{M-f}) / 2i, and A_f += G_f conj(U_f) is summed
 //    over the batch for f = 0 .. M/2 (A is Hermitian: c is real). One inverse transform then
 //    gives c_j = (1/M) sum_f A_f e^{2 pi i f j / M}.
-//  - grad_moments: one warp per four states of a channel, lanes along the lag (the block's
+//  - the power sums: for 64 states or more on the tensor cores (dlr_moments_tc.cu); else
+//    grad_moments: one warp per four states of a channel, lanes along the lag (the block's
 //    eight warps share one channel and stage its weights in shared memory, 1024 lags at a
 //    time, the next tile's loads in flight during the current one): lane t sums
 //    c_{32m+t} lambda^{32m} and (32m+t) c_{32m+t} lambda^{32m} over the blocks m, each
@@ -39,7 +40,9 @@
 //    back from a per-warp shared table), then multiplies by its own lambda^t; the warp adds
 //    the lanes and lane 0 forms the three gradients.
 // Per input element this is one complex FFT point per row and a few flops per (state, lag)
-// instead of the recurrences' two complex updates per (state, step, row).
+// instead of the recurrences' two complex updates per (state, step, row). For the DLR-prod
+// cast the complex kernel comes from the generators' complex mode, and the input gradient's
+// Re K Im K kernels are formed from it (prod_cast).
 //
 // Recurrences (fewer states, or longer rows):
 // dlr_grad_rows: one thread per (b, h, n) runs both recurrences over the row, in blocks of 32
