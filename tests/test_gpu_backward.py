@@ -146,3 +146,28 @@ def test_layer_backward_dlrprod_workload_sampled_channels():
     for got, ref in zip(grads, r_grads):
         for a, b in zip(got, ref):
             assert oracle.rel_l2(host(a)[hs], b) <= TOL
+
+
+@pytest.mark.parametrize("bidir,cast,B,H,N,L", [
+    (True, "re", 1, 1, 1, 1), (True, "re_im", 1, 1, 1, 1), (False, "re_im", 2, 1, 1, 2),
+    (True, "re", 2, 1, 16, 8192), (True, "re", 2, 1, 16, 8193),        # correlation routes
+    (False, "re_im", 1, 1, 20, 16384), (False, "re_im", 1, 1, 20, 16385),  # one CTA / cluster
+    (True, "re", 2, 1, 63, 500), (True, "re", 2, 1, 64, 500),          # FFMA / tensor-core sums
+    (False, "re_im", 1, 2, 127, 300), (False, "re_im", 1, 2, 128, 300), (True, "re", 1, 1, 129, 300),
+])
+def test_layer_backward_route_boundaries(bidir, cast, B, H, N, L):
+    """dlr_layer_backward at the sizes where its routes change (the correlation by one CTA per
+    channel or through the convolution, the convolution on one CTA or eight, the power sums on
+    FFMA or on the tensor cores with 128 states per CTA) and at the smallest sizes."""
+    w = inputs.make_dlr(B, H, N, L, seed=N * 3 + L, bidir=bidir, unit_channels=1)
+    g = np.random.default_rng(N + 2 * L).standard_normal((B, H, L)).astype(np.float32)
+    fwd = (w.fwd.log_re, w.fwd.log_im, w.fwd.W)
+    bwd = (w.bwd.log_re, w.bwd.log_im, w.bwd.W) if bidir else None
+    du, grads = dlr.dlr_layer_backward(dev(w.u), dev(g), tuple(dev(a) for a in fwd),
+                                       tuple(dev(a) for a in bwd) if bidir else None, cast=cast)
+    r_du, r_grads = oracle.dlr_layer_backward(w.u, g, fwd, bwd, cast=cast)
+    assert oracle.rel_l2(host(du), r_du) <= TOL
+    for got, ref in zip(grads, r_grads):
+        for a, b in zip(got, ref):
+            assert oracle.rel_l2(host(a), b) <= TOL
+    assert dlr.device_status() == 0
