@@ -6,9 +6,9 @@
 //
 // Chunked powers, as in the kernel generators but transposed: with j = 64 C + t,
 //   S0_n = sum_C lambda_n^{64 C} P[n][C],   P[n][C] = sum_t lambda_n^t w_{64 C + t},
-// and S1 the same with the weights j w_j. For 128 states and a block of 64 chunks, P (for both
-// weight sets) is one real product
-//   [128 states x 128] . [128 x 256]:  A[n][k] = Re lambda_n^k (k < 64), Im lambda_n^(k-64);
+// and S1 the same with the weights j w_j. For 128 states and a block of 32 chunks, P (for both
+// weight sets) is one real product [128 states x 128] . [128 x 128] (4 columns per chunk):
+//   A[n][k] = Re lambda_n^k (k < 64), Im lambda_n^(k-64);
 //   B row (C, Re) = [Re w_t, -Im w_t],  B row (C, Im) = [Im w_t, Re w_t]  (and the same for
 //   j w_j), so that A . B^T gives Re P and Im P in adjacent columns,
 // run as three kind::f16 MMAs per K step (hi*hi + hi*lo + lo*hi of operands scaled by powers
@@ -18,8 +18,10 @@
 // directly evaluated powers combined by one product (lambda^{8a} lambda^b, lambda^{512a}
 // lambda^{64b}).
 //
-// One CTA of 256 threads per (channel, 128 states): all threads write the operands, thread 0
-// issues the MMAs, warps 0-3 (thread = TMEM lane = state) read the accumulator. The MMA
+// One CTA of 256 threads per (channel, 128 states), blocks of 32 chunks in a two-deep pipeline:
+// all threads write block k + 1's B operand (two buffers) while thread 0's MMAs of block k run
+// into one of two TMEM accumulators, then all eight warps read block k's accumulator (thread =
+// TMEM lane = state, the two warps of a lane quarter taking half the columns each). Each MMA
 // completion is an mbarrier wait bounded by the global timer (DLR_ERR_TIMEOUT on expiry).
 #include <cuda_fp16.h>
 
@@ -33,18 +35,21 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kStates = 128;  // MMA M
-constexpr int kChunks = 64;   // chunks per block; MMA N = 4 * kChunks
+constexpr int kChunks = 32;   // chunks per block; MMA N = 4 * kChunks
 constexpr int kN = 4 * kChunks;
 constexpr uint32_t kATile = kStates * 128;  // one K-block (64 f16 per row) of A, bytes
 constexpr uint32_t kBTile = kN * 128;       // one K-block of B
-// shared memory: A [2 K-blocks][hi, lo], B [2 K-blocks][hi, lo], row exponents, barrier, slot
+constexpr uint32_t kBBuf = 4 * kBTile;      // one B buffer: [2 K-blocks][hi, lo]
+// shared memory: A [2 K-blocks][hi, lo], B [2 buffers], their row exponents [2][kN], the
+// partial sums of the second column half [kStates][4], barriers [2], TMEM slot
 constexpr uint32_t kAOff = 0;
 constexpr uint32_t kBOff = kAOff + 4 * kATile;
-constexpr uint32_t kEOff = kBOff + 4 * kBTile;  // int [kN]
-constexpr uint32_t kBarOff = kEOff + 4 * kN;
-constexpr uint32_t kSlotOff = kBarOff + 8;
-constexpr uint32_t kSmemBytes = kSlotOff + 8 + 1024;  // + alignment slack
-constexpr uint32_t kTmemCols = kN;
+constexpr uint32_t kEOff = kBOff + 2 * kBBuf;
+constexpr uint32_t kPOff = kEOff + 2 * 4 * kN;
+constexpr uint32_t kBarOff = kPOff + kStates * 16;
+constexpr uint32_t kSlotOff = kBarOff + 16;
+constexpr uint32_t kSmemBytes = kSlotOff + 16 + 1024;  // + alignment slack
+constexpr uint32_t kTmemCols = 2 * kN;                 // two accumulators
 
 __device__ __forceinline__ float round11(float a) {
   return __uint_as_float((__float_as_uint(a) + 0x1000u) & 0xFFFFE000u);
@@ -98,7 +103,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float2* kh = kProd ? Kc + (size_t)h * (size_t)L : nullptr;
 
   if (tid == 0) {
-    tc::mbar_init(bar, 1);
+    tc::mbar_init(&bar[0], 1);
+    tc::mbar_init(&bar[1], 1);
     tc::mbar_fence_init();
   }
   if (warp == 0) {
@@ -140,129 +146,154 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = *slot;
 
-  // epilogue state (warps 0-3: state n0 + tid)
-  const int ns = n0 + tid;
-  const bool epi = warp < 4;
+  // ---- the epilogue thread: state n0 + r, accumulator columns of chunk half hc ----
+  const int r = 32 * (warp & 3) + (tid & 31), hc = warp >> 2;
+  const int ns = n0 + r;
   lam_param pe{};
   cf l64[8];  // lambda^{64 b}
   cf s0 = {0.f, 0.f}, s1 = {0.f, 0.f};
-  if (epi) {
+  {
     const bool on = ns < N;
     pe = make_lam_param(on ? log_re[(size_t)h * N + ns] : 0.f,
                         on ? log_im[(size_t)h * N + ns] : 0.f);
 #pragma unroll
     for (int b = 0; b < 8; ++b) l64[b] = lam_pow(pe, 64 * b);
   }
-
   const int nchunks = (L + 63) / 64;
   const int nblocks = (nchunks + kChunks - 1) / kChunks;
+
+  // B of block blk into buffer buf: rows 4 cc + kind (kind 0/1: Re/Im rows of w, 2/3: of j w)
+  // for chunk 32 blk + cc; two adjacent threads share a row, 32 lags each
+  auto build_b = [&](int blk, int buf) {
+    const int row = tid >> 1, part = tid & 1, cc = row >> 2, kind = row & 3;
+    const int jb = 64 * (blk * kChunks + cc) + 32 * part;
+    const bool jw = kind >= 2, im_row = kind & 1;
+    float wr[32], wi[32];
+    float m = 0.f;
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      const int j = jb + t;
+      float xr = 0.f, xi = 0.f;
+      if (j < L) {
+        const float cj = __ldg(ch + j);
+        if constexpr (kProd) {
+          const float2 kj = __ldg(kh + j);
+          xr = cj * kj.x;
+          xi = cj * kj.y;
+        } else {
+          xr = cj;
+        }
+        if (jw) {
+          xr *= (float)j;
+          xi *= (float)j;
+        }
+      }
+      wr[t] = xr;
+      wi[t] = xi;
+      m = fmaxf(m, fmaxf(fabsf(xr), fabsf(xi)));
+    }
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));  // the row's 64 lags
+    const int e = exp_of(m);  // |entries| < 2^e: scaled by 2^(13 - e)
+    const float sc = exp2i(13 - e);
+    if (part == 0 && DLR_IN(buf * kN + row, 2 * kN)) sE[buf * kN + row] = e;
+    uint8_t* b_re_hi = sm + kBOff + buf * kBBuf;  // K-block 0 (multiplies Re lambda^t)
+    uint8_t* b_re_lo = b_re_hi + kBTile;
+    uint8_t* b_im_hi = b_re_lo + kBTile;  // K-block 1 (multiplies Im lambda^t)
+    uint8_t* b_im_lo = b_im_hi + kBTile;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      float v0[8], v1[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        const int t = 8 * q + b;
+        // Re row: [Re w, -Im w]; Im row: [Im w, Re w]
+        v0[b] = (im_row ? wi[t] : wr[t]) * sc;
+        v1[b] = (im_row ? wr[t] : -wi[t]) * sc;
+      }
+      put8(b_re_hi, b_re_lo, row, 4 * part + q, v0, kBTile);
+      put8(b_im_hi, b_im_lo, row, 4 * part + q, v1, kBTile);
+    }
+  };
+  // the three-product MMAs of the block in buffer buf into accumulator buf (thread 0)
+  auto issue = [&](int buf) {
+    constexpr uint32_t idesc = tc::idesc_f16_f32(kStates, kN);
+    const uint32_t d = tmem + uint32_t(buf * kN);
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb) {
+      const uint64_t ah = tc::smem_desc_k_sw128(sm + kAOff + (2 * kb) * kATile);
+      const uint64_t al = tc::smem_desc_k_sw128(sm + kAOff + (2 * kb + 1) * kATile);
+      const uint64_t bh = tc::smem_desc_k_sw128(sm + kBOff + buf * kBBuf + (2 * kb) * kBTile);
+      const uint64_t bl =
+          tc::smem_desc_k_sw128(sm + kBOff + buf * kBBuf + (2 * kb + 1) * kBTile);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {  // 16 f16 = 32 bytes = 2 descriptor units
+        tc::mma_kind_f16(d, ah + 2 * kk, bh + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
+        tc::mma_kind_f16(d, ah + 2 * kk, bl + 2 * kk, idesc, 1u);
+        tc::mma_kind_f16(d, al + 2 * kk, bh + 2 * kk, idesc, 1u);
+      }
+    }
+    tc::mma_commit(&bar[buf]);
+  };
+
+  // The pipeline: B of block k + 1 is written while the MMAs of block k run; then every warp
+  // reads block k's accumulator. Buffer and accumulator k & 1 are free again once block k - 1's
+  // readers passed the barrier that ends its iteration (they waited for its MMAs first).
   bool ok = true;
+  build_b(0, 0);
+  tc::fence_proxy_async_smem();
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  if (tid == 0 && nblocks > 0) issue(0);
 #pragma unroll 1
   for (int blk = 0; blk < nblocks; ++blk) {
-    const int C0 = blk * kChunks;
-    // ---- B: row 4 cc + kind (kind 0/1: Re/Im rows of w, 2/3: of j w) for chunk C0 + cc ----
-    {
-      const int row = tid, cc = row >> 2, kind = row & 3;
-      const int jb = 64 * (C0 + cc);
-      const bool jw = kind >= 2, im_row = kind & 1;
-      // the 64 weights of the chunk: (Re, Im) of w_j or j w_j
-      float wr[64], wi[64];
-      float m = 0.f;
-#pragma unroll
-      for (int t = 0; t < 64; ++t) {
-        const int j = jb + t;
-        float xr = 0.f, xi = 0.f;
-        if (j < L) {
-          const float cj = __ldg(ch + j);
-          if constexpr (kProd) {
-            const float2 kj = __ldg(kh + j);
-            xr = cj * kj.x;
-            xi = cj * kj.y;
-          } else {
-            xr = cj;
-          }
-          if (jw) {
-            xr *= (float)j;
-            xi *= (float)j;
-          }
-        }
-        wr[t] = xr;
-        wi[t] = xi;
-        m = fmaxf(m, fmaxf(fabsf(xr), fabsf(xi)));
-      }
-      const int e = exp_of(m);  // |entries| < 2^e: scaled by 2^(13 - e)
-      const float sc = exp2i(13 - e);
-      if (DLR_IN(row, kN)) sE[row] = e;
-      uint8_t* b_re_hi = sm + kBOff;  // K-block 0 (multiplies Re lambda^t)
-      uint8_t* b_re_lo = b_re_hi + kBTile;
-      uint8_t* b_im_hi = b_re_lo + kBTile;  // K-block 1 (multiplies Im lambda^t)
-      uint8_t* b_im_lo = b_im_hi + kBTile;
+    const int buf = blk & 1;
+    if (blk + 1 < nblocks) {
+      build_b(blk + 1, buf ^ 1);
+      tc::fence_proxy_async_smem();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    if (blk + 1 < nblocks && tid == 0) issue(buf ^ 1);
+    ok = ok && tc::mbar_wait(&bar[buf], (blk >> 1) & 1);
+    tc::fence_after_sync();
+    const int C0 = blk * kChunks + 16 * hc;  // this thread's first chunk of the block
+    const uint32_t lane_base = tmem + (uint32_t(32 * (warp & 3)) << 16) + uint32_t(buf * kN);
+#pragma unroll 1
+    for (int part = 0; part < 2; ++part) {  // chunks C0 + 8 part .. C0 + 8 part + 7
+      float v[32];
+      tc::tmem_ld32(lane_base + uint32_t(64 * hc + 32 * part), v);
+      if (!ok || C0 + 8 * part >= nchunks) continue;
+      // lambda^{64 C} = lambda^{512 (C / 8)} lambda^{64 (C % 8)}
+      const cf l512 = lam_pow(pe, 512 * ((C0 >> 3) + part));
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        float v0[8], v1[8];
-#pragma unroll
-        for (int b = 0; b < 8; ++b) {
-          const int t = 8 * q + b;
-          // Re row: [Re w, -Im w]; Im row: [Im w, Re w]
-          v0[b] = (im_row ? wi[t] : wr[t]) * sc;
-          v1[b] = (im_row ? wr[t] : -wi[t]) * sc;
-        }
-        put8(b_re_hi, b_re_lo, row, q, v0, kBTile);
-        put8(b_im_hi, b_im_lo, row, q, v1, kBTile);
+        const int cc = 16 * hc + 8 * part + q;  // chunk within the block
+        if (C0 + 8 * part + q >= nchunks) break;
+        // undo the operand scales: 2^14 (A) and 2^(13 - e) (the B row)
+        const float u0 = exp2i(sE[buf * kN + 4 * cc] - 27);
+        const float u1 = exp2i(sE[buf * kN + 4 * cc + 2] - 27);
+        const cf P = {v[4 * q] * u0, v[4 * q + 1] * u0};
+        const cf P1 = {v[4 * q + 2] * u1, v[4 * q + 3] * u1};
+        const cf wgt = cmul(l512, l64[q]);
+        s0 = cfma(wgt, P, s0);
+        s1 = cfma(wgt, P1, s1);
       }
     }
-    tc::fence_proxy_async_smem();
     tc::fence_before_sync();
-    __syncthreads();  // operands written; the previous block's accumulator has been read
-    tc::fence_after_sync();
-    if (tid == 0) {
-      constexpr uint32_t idesc = tc::idesc_f16_f32(kStates, kN);
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb) {
-        const uint64_t ah = tc::smem_desc_k_sw128(sm + kAOff + (2 * kb) * kATile);
-        const uint64_t al = tc::smem_desc_k_sw128(sm + kAOff + (2 * kb + 1) * kATile);
-        const uint64_t bh = tc::smem_desc_k_sw128(sm + kBOff + (2 * kb) * kBTile);
-        const uint64_t bl = tc::smem_desc_k_sw128(sm + kBOff + (2 * kb + 1) * kBTile);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {  // 16 f16 = 32 bytes = 2 descriptor units
-          tc::mma_kind_f16(tmem, ah + 2 * kk, bh + 2 * kk, idesc, (kb | kk) ? 1u : 0u);
-          tc::mma_kind_f16(tmem, ah + 2 * kk, bl + 2 * kk, idesc, 1u);
-          tc::mma_kind_f16(tmem, al + 2 * kk, bh + 2 * kk, idesc, 1u);
-        }
-      }
-      tc::mma_commit(bar);
-    }
-    if (epi) {
-      ok = ok && tc::mbar_wait(bar, blk & 1);
-      tc::fence_after_sync();
-      const uint32_t lane_base = tmem + (uint32_t(warp * 32) << 16);
-#pragma unroll 1
-      for (int part = 0; part < kN / 32; ++part) {  // chunks C0 + 8 part .. C0 + 8 part + 7
-        float v[32];
-        tc::tmem_ld32(lane_base + uint32_t(part * 32), v);
-        if (!ok || C0 + 8 * part >= nchunks) continue;
-        // lambda^{64 C} = lambda^{512 (C / 8)} lambda^{64 (C % 8)}, C / 8 = C0 / 8 + part
-        const cf l512 = lam_pow(pe, 512 * ((C0 >> 3) + part));
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const int cc = part * 8 + q;
-          if (C0 + cc >= nchunks) break;
-          // undo the operand scales: 2^14 (A) and 2^(13 - e) (the B row)
-          const float u0 = exp2i(sE[4 * cc] - 27), u1 = exp2i(sE[4 * cc + 2] - 27);
-          const cf P = {v[4 * q] * u0, v[4 * q + 1] * u0};
-          const cf P1 = {v[4 * q + 2] * u1, v[4 * q + 3] * u1};
-          const cf wgt = cmul(l512, l64[q]);
-          s0 = cfma(wgt, P, s0);
-          s1 = cfma(wgt, P1, s1);
-        }
-      }
-      tc::fence_before_sync();
-    }
-    __syncthreads();  // the MMAs are done and the row exponents read: the next block may write
+    __syncthreads();  // accumulator and exponents of buffer buf read: free for block k + 2
   }
-  if (!ok && tid == 0) report_status(status, DLR_ERR_TIMEOUT);
-  if (epi && ns < N && ok) {
-    // S0, S1 -> the three gradients (the S terms hold lambda^t only through the A operand)
+  if (!ok) report_status(status, DLR_ERR_TIMEOUT);
+  // the two column halves of each state: the second half's sums through shared memory
+  float4* sP = reinterpret_cast<float4*>(sm + kPOff);
+  if (hc == 1) sP[r] = make_float4(s0.re, s0.im, s1.re, s1.im);
+  __syncthreads();
+  if (hc == 0 && ns < N && ok) {
+    const float4 o = sP[r];
+    s0 = {s0.re + o.x, s0.im + o.y};
+    s1 = {s1.re + o.z, s1.im + o.w};
+    // S0, S1 -> the three gradients
     const size_t hn = (size_t)h * N + ns;
     const float2 w = W[hn];
     const double ws1r = (double)w.x * s1.re - (double)w.y * s1.im;
