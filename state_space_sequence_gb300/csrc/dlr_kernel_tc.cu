@@ -96,11 +96,15 @@ __device__ __forceinline__ void small_powers8(float2* p, cf x) {
   for (int i = 0; i < 8; ++i) p[i] = make_float2(q[i].re, q[i].im);
 }
 
-// (a, b) as f16 pairs: hi = f16(a, b), lo = f16 of the remainders
-__device__ __forceinline__ void split_h2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __half2 h = __floats2half2_rn(a, b);
+// v * (s, s) as an f16 pair: hi = f16 of the scaled values, lo = f16 of the remainders; the
+// scaling and the remainders in two-wide float instructions (each lane rounds as the scalar
+// operation would).
+__device__ __forceinline__ void split_h2s(float2 v, float s, uint32_t& hi, uint32_t& lo) {
+  const float2 x = __fmul2_rn(v, make_float2(s, s));
+  const __half2 h = __floats2half2_rn(x.x, x.y);
   const float2 f = __half22float2(h);
-  const __half2 l = __floats2half2_rn(a - f.x, b - f.y);
+  const float2 r = __ffma2_rn(f, make_float2(-1.f, -1.f), x);  // x - f
+  const __half2 l = __floats2half2_rn(r.x, r.y);
   hi = *reinterpret_cast<const uint32_t*>(&h);
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
@@ -290,9 +294,10 @@ dlr_kernel_tc(const float* __restrict__ log_re, const float* __restrict__ log_im
         for (int i = 0; i < 4; ++i) {
           const int nl = DLR_IN(half * 16 + qq * 4 + i, kSB) ? half * 16 + qq * 4 + i : 0;
           const float2 a = f2mul(q[nl * 16 + cq], p64[nl * 8 + c0]);
-          split_h2(a.x * a_scale, a.y * a_scale, ahi[i], alo[i]);
+          split_h2s(a, a_scale, ahi[i], alo[i]);
           const float2 l = f2mul(p1[nl * 8 + (t & 7)], p8[nl * 8 + (t >> 3)]);
-          split_h2(16384.f * (imrow ? l.y : l.x), 16384.f * (imrow ? l.x : -l.y), bhi[i], blo[i]);
+          split_h2s(imrow ? make_float2(l.y, l.x) : make_float2(l.x, -l.y), 16384.f, bhi[i],
+                    blo[i]);
         }
         const uint32_t off = uint32_t(row) * 128u + (((uint32_t(half * 4 + qq)) ^ sw) << 4);
         if (!DLR_IN(off + 15, kTile)) continue;
