@@ -163,16 +163,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nblocks = (nchunks + kChunks - 1) / kChunks;
 
   // B of block blk into buffer buf: rows 4 cc + kind (kind 0/1: Re/Im rows of w, 2/3: of j w)
-  // for chunk 32 blk + cc; two adjacent threads share a row, 32 lags each
+  // for chunk 32 blk + cc. Thread (cc, p) loads lags 8p .. 8p + 7 of its chunk once and writes
+  // their 16-byte piece of all four rows; the rows' scales come from the chunk's largest |w|
+  // and |j w|, reduced over its eight threads (adjacent lanes).
   auto build_b = [&](int blk, int buf) {
-    const int row = tid >> 1, part = tid & 1, cc = row >> 2, kind = row & 3;
-    const int jb = 64 * (blk * kChunks + cc) + 32 * part;
-    const bool jw = kind >= 2, im_row = kind & 1;
-    float wr[32], wi[32];
-    float m = 0.f;
+    const int cc = tid >> 3, p = tid & 7;
+    const int j0 = 64 * (blk * kChunks + cc) + 8 * p;
+    float wr[8], wi[8], vr[8], vi[8];  // w_j and j w_j
+    float mw = 0.f, mv = 0.f;
 #pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      const int j = jb + t;
+    for (int b = 0; b < 8; ++b) {
+      const int j = j0 + b;
       float xr = 0.f, xi = 0.f;
       if (j < L) {
         const float cj = __ldg(ch + j);
@@ -183,35 +184,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           xr = cj;
         }
-        if (jw) {
-          xr *= (float)j;
-          xi *= (float)j;
-        }
       }
-      wr[t] = xr;
-      wi[t] = xi;
-      m = fmaxf(m, fmaxf(fabsf(xr), fabsf(xi)));
+      wr[b] = xr;
+      wi[b] = xi;
+      vr[b] = (float)j * xr;
+      vi[b] = (float)j * xi;
+      mw = fmaxf(mw, fmaxf(fabsf(xr), fabsf(xi)));
+      mv = fmaxf(mv, fmaxf(fabsf(vr[b]), fabsf(vi[b])));
     }
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));  // the row's 64 lags
-    const int e = exp_of(m);  // |entries| < 2^e: scaled by 2^(13 - e)
-    const float sc = exp2i(13 - e);
-    if (part == 0 && DLR_IN(buf * kN + row, 2 * kN)) sE[buf * kN + row] = e;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
+      mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
+    }
+    const int ew = exp_of(mw), ev = exp_of(mv);  // |entries| < 2^e: scaled by 2^(13 - e)
+    const float sw = exp2i(13 - ew), sv = exp2i(13 - ev);
+    if (p == 0 && DLR_IN(buf * kN + 4 * cc + 3, 2 * kN)) {
+      sE[buf * kN + 4 * cc] = ew;
+      sE[buf * kN + 4 * cc + 1] = ew;
+      sE[buf * kN + 4 * cc + 2] = ev;
+      sE[buf * kN + 4 * cc + 3] = ev;
+    }
     uint8_t* b_re_hi = sm + kBOff + buf * kBBuf;  // K-block 0 (multiplies Re lambda^t)
     uint8_t* b_re_lo = b_re_hi + kBTile;
     uint8_t* b_im_hi = b_re_lo + kBTile;  // K-block 1 (multiplies Im lambda^t)
     uint8_t* b_im_lo = b_im_hi + kBTile;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int kind = 0; kind < 4; ++kind) {
+      const bool jw = kind >= 2, im_row = kind & 1;
+      const float* xr = jw ? vr : wr;
+      const float* xi = jw ? vi : wi;
+      const float sc = jw ? sv : sw;
       float v0[8], v1[8];
 #pragma unroll
       for (int b = 0; b < 8; ++b) {
-        const int t = 8 * q + b;
         // Re row: [Re w, -Im w]; Im row: [Im w, Re w]
-        v0[b] = (im_row ? wi[t] : wr[t]) * sc;
-        v1[b] = (im_row ? wr[t] : -wi[t]) * sc;
+        v0[b] = (im_row ? xi[b] : xr[b]) * sc;
+        v1[b] = (im_row ? xr[b] : -xi[b]) * sc;
       }
-      put8(b_re_hi, b_re_lo, row, 4 * part + q, v0, kBTile);
-      put8(b_im_hi, b_im_lo, row, 4 * part + q, v1, kBTile);
+      put8(b_re_hi, b_re_lo, 4 * cc + kind, p, v0, kBTile);
+      put8(b_im_hi, b_im_lo, 4 * cc + kind, p, v1, kBTile);
     }
   };
   // the three-product MMAs of the block in buffer buf into accumulator buf (thread 0)
