@@ -171,3 +171,20 @@ def test_layer_backward_route_boundaries(bidir, cast, B, H, N, L):
         for a, b in zip(got, ref):
             assert oracle.rel_l2(host(a), b) <= TOL
     assert dlr.device_status() == 0
+
+
+@pytest.mark.parametrize("bidir,cast", [(True, "re"), (True, "re_im"), (False, "re_im")])
+def test_layer_backward_without_input_gradient(bidir, cast):
+    """du is optional: with it skipped the parameter gradients are the same bits as with it."""
+    w = inputs.make_dlr(2, 2, 24, 600, seed=31, bidir=bidir, unit_channels=1)
+    g = dev(np.random.default_rng(2).standard_normal(w.u.shape).astype(np.float32))
+    u = dev(w.u)
+    fwd = tuple(dev(a) for a in (w.fwd.log_re, w.fwd.log_im, w.fwd.W))
+    bwd = tuple(dev(a) for a in (w.bwd.log_re, w.bwd.log_im, w.bwd.W)) if bidir else None
+    du, full = dlr.dlr_layer_backward(u, g, fwd, bwd, cast=cast)
+    none, part = dlr.dlr_layer_backward(u, g, fwd, bwd, cast=cast, input_grad=False)
+    assert none is None and du is not None
+    for a, b in zip(full, part):
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+    assert dlr.device_status() == 0
