@@ -100,3 +100,37 @@ def test_step_on_the_callers_stream():
     x1 = torch.zeros_like(x0)
     check(y_ref, dlr.dlr_step(ul, tab, x1, stream=s), s)
     assert torch.equal(x0, x1)
+
+
+def test_concurrent_calls_on_two_streams():
+    """Calls on two streams with their own workspaces run at the same time without sharing
+    state: the tensor-core scan on one, the DLR-prod gradients (tensor-core generator and power
+    sums, FFT convolutions) on the other, each equal to the same call run alone."""
+    w = inputs.make_dlr(4, 16, 64, 4096, seed=12, unit_channels=1)
+    f = [dev(a) for a in (w.fwd.log_re, w.fwd.log_im, w.fwd.W)]
+    u = dev(w.u)
+    wp = inputs.make_dlr(2, 8, 256, 2048, seed=13, bidir=True, unit_channels=1)
+    fp = [dev(a) for a in (wp.fwd.log_re, wp.fwd.log_im, wp.fwd.W)]
+    bp = [dev(a) for a in (wp.bwd.log_re, wp.bwd.log_im, wp.bwd.W)]
+    up = dev(wp.u)
+    gp = dev(np.random.default_rng(3).standard_normal(wp.u.shape).astype(np.float32))
+    y_ref = dlr.dlr_scan(u, f)
+    du_ref, gr_ref = dlr.dlr_layer_backward(up, gp, fp, bp, cast="re_im")
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    ws1 = torch.empty(dlr.dlr_scan_workspace_size(4, 16, 64, 4096), dtype=torch.uint8,
+                      device="cuda")
+    ws2 = torch.empty(dlr.dlr_layer_backward_workspace_size(2, 8, 256, 2048, True, "re_im"),
+                      dtype=torch.uint8, device="cuda")
+    ys, outs = [], []
+    for _ in range(3):
+        ys.append(dlr.dlr_scan(u, f, workspace=ws1, stream=s1))
+        outs.append(dlr.dlr_layer_backward(up, gp, fp, bp, cast="re_im", workspace=ws2,
+                                           stream=s2))
+        s1.synchronize()
+        s2.synchronize()
+    for y, (du, gr) in zip(ys, outs):
+        assert torch.equal(y, y_ref) and torch.equal(du, du_ref)
+        for a, b in zip([t for x in gr for t in x], [t for x in gr_ref for t in x]):
+            assert torch.equal(a, b)
+    assert dlr.device_status() == 0
